@@ -1,0 +1,160 @@
+"""Float64 CPU oracle for paged-KV attention, paged K/V append and greedy accept.
+
+TEST INFRASTRUCTURE ONLY.  This package states, plainly and slowly, what the GPU
+path computes.  Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline
+and reference arms of ``bench.py`` may import it.  The CUDA library and its
+Python binding never import, link or call it, and it never imports them.
+
+The arithmetic lives in ``pkv_oracle.c`` (plain C99, float64, OpenMP over
+(sequence, KV head)); this module compiles it with gcc on first use and wraps it
+with numpy.  The passages each function follows are cited in the C source:
+TensorSharp "advanced features" (sections on continuous batching and the paged
+KV cache, native paged attention with the sinks variant, and ForwardBatch's
+paged K/V scatter) and the TensorFold article (section on the GPU accept
+kernel).
+
+Parity pins: every function here is checked by ``tests/test_oracle_*.py``
+against closed forms, invariants, library routines (torch's float64 scaled
+dot-product attention, numpy's argmax) and hand-worked fixtures in
+``tests/golden/``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pkv_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libpkv_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build_oracle(force: bool = False) -> str:
+    """Compile pkv_oracle.c into a shared library with gcc; returns its path."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-std=c99", "-O2", "-ffp-contract=off", "-fopenmp", "-fPIC",
+               "-shared", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build_oracle())
+            P = ctypes.c_void_p
+            i32 = ctypes.c_int32
+            lib.oracle_paged_kv_append.argtypes = [P, P, i32, i32, i32, i32, P, i32, P, P, P, P, i32]
+            lib.oracle_paged_kv_append.restype = ctypes.c_int
+            lib.oracle_paged_attention.argtypes = [P, P, i32, i32, i32, i32, P, P, P, i32, P, i32,
+                                                   i32, P, P, i32, ctypes.c_double, P, i32]
+            lib.oracle_paged_attention.restype = ctypes.c_int
+            lib.oracle_argmax_rows.argtypes = [P, ctypes.c_int64, i32, P]
+            lib.oracle_argmax_rows.restype = None
+            lib.oracle_spec_accept_greedy.argtypes = [P, i32, P, P, i32, P, P, P]
+            lib.oracle_spec_accept_greedy.restype = None
+            _lib = lib
+        return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def default_num_threads() -> int:
+    return len(os.sched_getaffinity(0))
+
+
+def paged_kv_append(k_pool, v_pool, block_tables, context_lens_old, new_starts, k_new, v_new):
+    """Scatter the new tokens' K/V rows into the pools, in place.
+
+    k_pool/v_pool: uint16 (bf16 bits) [num_blocks, H_kv, block_size, head_dim], C-contiguous.
+    block_tables: int32 [S, max_blocks]; context_lens_old: int32 [S];
+    new_starts: int32 [S+1]; k_new/v_new: uint16 [R_new, H_kv, head_dim].
+    """
+    lib = _load()
+    assert k_pool.dtype == np.uint16 and k_pool.flags.c_contiguous
+    assert v_pool.dtype == np.uint16 and v_pool.flags.c_contiguous
+    nb, hkv, bs, d = k_pool.shape
+    bt = _c(block_tables, np.int32)
+    rc = lib.oracle_paged_kv_append(
+        _ptr(k_pool), _ptr(v_pool), nb, bs, hkv, d, _ptr(bt), bt.shape[1],
+        _ptr(_c(context_lens_old, np.int32)), _ptr(_c(new_starts, np.int32)),
+        _ptr(_c(k_new, np.uint16)), _ptr(_c(v_new, np.uint16)), bt.shape[0])
+    if rc != 0:
+        raise ValueError(f"oracle_paged_kv_append failed with status {rc}")
+
+
+def paged_attention(k_pool, v_pool, q, q_starts, block_tables, context_lens,
+                    kv_head_of_q_head=None, sinks=None, causal=False, scale=None,
+                    num_threads=None):
+    """Float64 attention over the paged pool; returns float64 [R, H_q, head_dim].
+
+    q: uint16 (bf16 bits) [R, H_q, head_dim]; q_starts: int32 [S+1];
+    context_lens: int32 [S] (keys in the cache, including any just appended);
+    kv_head_of_q_head: int32 [H_q] or None (contiguous groups);
+    sinks: float32 [H_q] or None; scale: None means 1/sqrt(head_dim).
+    """
+    lib = _load()
+    nb, hkv, bs, d = k_pool.shape
+    q = _c(q, np.uint16)
+    r, hq, dq = q.shape
+    assert dq == d
+    bt = _c(block_tables, np.int32)
+    qs = _c(q_starts, np.int32)
+    cl = _c(context_lens, np.int32)
+    hm = None if kv_head_of_q_head is None else _c(kv_head_of_q_head, np.int32)
+    sk = None if sinks is None else _c(sinks, np.float32)
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    out = np.zeros((r, hq, d), dtype=np.float64)
+    rc = lib.oracle_paged_attention(
+        _ptr(_c(k_pool, np.uint16)), _ptr(_c(v_pool, np.uint16)), nb, bs, hkv, d,
+        _ptr(q), _ptr(qs), _ptr(bt), bt.shape[1], _ptr(cl), cl.shape[0], hq, _ptr(hm),
+        _ptr(sk), int(bool(causal)), float(scale), _ptr(out),
+        int(num_threads or default_num_threads()))
+    if rc != 0:
+        raise ValueError(f"oracle_paged_attention failed with status {rc}")
+    return out
+
+
+def argmax_rows(logits):
+    """Per-row argmax with ties to the lowest index; int32 [rows]."""
+    lib = _load()
+    lg = _c(logits, np.float32)
+    rows, vocab = lg.shape
+    out = np.empty(rows, dtype=np.int32)
+    lib.oracle_argmax_rows(_ptr(lg), rows, vocab, _ptr(out))
+    return out
+
+
+def spec_accept_greedy(logits, q_starts, draft_tokens):
+    """Greedy accept: returns (argmax [R], accept_len [S], out_tokens [R]), all int32."""
+    lib = _load()
+    lg = _c(logits, np.float32)
+    rows, vocab = lg.shape
+    qs = _c(q_starts, np.int32)
+    dr = _c(draft_tokens, np.int32)
+    s = qs.shape[0] - 1
+    assert qs[-1] == rows and dr.shape[0] == rows
+    am = np.empty(rows, dtype=np.int32)
+    al = np.empty(s, dtype=np.int32)
+    ot = np.empty(rows, dtype=np.int32)
+    lib.oracle_spec_accept_greedy(_ptr(lg), vocab, _ptr(qs), _ptr(dr), s, _ptr(am), _ptr(al), _ptr(ot))
+    return am, al, ot

@@ -1,0 +1,273 @@
+/*
+ * pkv_oracle.c -- float64 CPU oracle for batched paged-KV attention, the paged
+ * K/V scatter-append and the greedy speculative accept step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, plain statement of what the
+ * GPU path computes.  Only the test suite, the smoke check and the benchmark's
+ * CPU-baseline / reference arm may build, load or call it.  It shares no code,
+ * header, table or helper with the CUDA library, and the CUDA library never
+ * calls it: there is no CPU fallback.
+ *
+ * Sources (page title, section):
+ *  - TensorSharp "高级功能" (advanced features), section "连续批处理与分页 KV 缓存"
+ *    (continuous batching and paged KV cache): the KV cache is cut into
+ *    fixed-size blocks drawn from a shared pool; every full block is
+ *    content-hashed so identical prefixes share physical blocks.
+ *  - same page, section "原生分页注意力" (native paged attention): K/V are
+ *    gathered from the paged buffers per sequence and fed to an ordinary
+ *    attention; a variant carries per-head attention-sink logits (GPT OSS).
+ *  - same page, section "批量前向" (batched forward, the paragraph on
+ *    ForwardBatch): new tokens' K/V are scattered into their paged slots.
+ *  - TensorFold article, section "接受规则：GPU 上的 accept 内核" (the accept
+ *    rule: the accept kernel on the GPU): each draft token is compared with the
+ *    target's choice and the accepted path follows the child whose token equals
+ *    that choice, i.e. the chain is walked to the first mismatch.
+ *  - TensorSharp page, section "MTP / NextN 推测解码": lossless speculative
+ *    decoding verifies all drafts in one batched forward and commits the
+ *    accepted prefix; verification follows the target greedily.
+ *
+ * Conventions fixed where the pages are silent (listed with reasons in the
+ * design notes): K/V pools are bf16 [num_blocks][H_kv][block_size][head_dim];
+ * q is bf16 [R][H_q][head_dim] with rows of sequence s at q_starts[s] ..
+ * q_starts[s+1]-1; the default GQA map is h -> h / (H_q/H_kv); the score scale
+ * multiplies q.k in float64; a sink is one logit per q head, in the units of
+ * the scaled scores, adding exp(sink) to the softmax denominator only; with the
+ * causal window, row w of a W-row window of a sequence of length L sees keys
+ * t < L - W + w + 1; a row that sees no key and has no sink outputs zeros;
+ * argmax ties go to the lowest index.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* bf16 -> float64: the 16 stored bits are the high half of an IEEE binary32;
+ * the widening is exact. */
+static double bf16_bits_to_f64(uint16_t bits)
+{
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+int oracle_version(void) { return 1; }
+
+/*
+ * Paged K/V scatter-append.  New token i of sequence s sits at absolute
+ * position p = context_lens_old[s] + i.  Its slot is block
+ * block_tables[s][p / block_size], offset p % block_size.  The K and V rows of
+ * each KV head are copied there bit for bit.
+ * Returns 0, or -1 if a position falls beyond the table, -2 for a block id
+ * outside [0, num_blocks).
+ */
+int oracle_paged_kv_append(uint16_t *k_pool, uint16_t *v_pool,
+                           int32_t num_blocks, int32_t block_size,
+                           int32_t num_kv_heads, int32_t head_dim,
+                           const int32_t *block_tables, int32_t max_blocks_per_seq,
+                           const int32_t *context_lens_old, const int32_t *new_starts,
+                           const uint16_t *k_new, const uint16_t *v_new,
+                           int32_t num_seqs)
+{
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        int32_t n_new = new_starts[s + 1] - new_starts[s];
+        for (int32_t i = 0; i < n_new; ++i) {
+            int64_t p = (int64_t)context_lens_old[s] + i;
+            int64_t logical = p / block_size;
+            int64_t offset = p % block_size;
+            if (logical >= max_blocks_per_seq)
+                return -1;
+            int32_t blk = block_tables[(int64_t)s * max_blocks_per_seq + logical];
+            if (blk < 0 || blk >= num_blocks)
+                return -2;
+            int64_t row = (int64_t)new_starts[s] + i;
+            for (int32_t h = 0; h < num_kv_heads; ++h) {
+                size_t dst = ((((size_t)blk * num_kv_heads) + h) * block_size + offset) * head_dim;
+                size_t src = (((size_t)row * num_kv_heads) + h) * head_dim;
+                memcpy(k_pool + dst, k_new + src, (size_t)head_dim * sizeof(uint16_t));
+                memcpy(v_pool + dst, v_new + src, (size_t)head_dim * sizeof(uint16_t));
+            }
+        }
+    }
+    return 0;
+}
+
+/*
+ * Attention over the paged pool, by the definition:
+ *   for each query row r of sequence s and q head h (KV head g = map[h]):
+ *     n   = causal ? L - W + w + 1 : L        (w = r - q_starts[s], W = rows of s)
+ *     x_t = scale * sum_k q[r][h][k] * K_s[t][g][k],        t < n
+ *     M   = max(max_t x_t, sink_h)                           (sink only if given)
+ *     out = sum_t e^{x_t - M} V_s[t][g] / (sum_t e^{x_t - M} + e^{sink_h - M})
+ * K_s and V_s are first materialised contiguously from the block table
+ * (logical token t -> block block_tables[s][t / B], slot t % B).
+ * Everything is float64.  out is float64 [R][H_q][head_dim].
+ * kv_head_of_q_head may be NULL (contiguous groups); sinks may be NULL.
+ * Returns 0, -1 (position beyond table), -2 (block id out of range),
+ * -3 (bad head map), -4 (out of memory).
+ */
+int oracle_paged_attention(const uint16_t *k_pool, const uint16_t *v_pool,
+                           int32_t num_blocks, int32_t block_size,
+                           int32_t num_kv_heads, int32_t head_dim,
+                           const uint16_t *q, const int32_t *q_starts,
+                           const int32_t *block_tables, int32_t max_blocks_per_seq,
+                           const int32_t *context_lens, int32_t num_seqs,
+                           int32_t num_q_heads, const int32_t *kv_head_of_q_head,
+                           const float *sinks, int32_t causal, double scale,
+                           double *out, int32_t num_threads)
+{
+    const int32_t B = block_size, D = head_dim, Hkv = num_kv_heads, Hq = num_q_heads;
+    if (Hkv <= 0 || Hq % Hkv != 0)
+        return -3;
+    const int32_t group = Hq / Hkv;
+    for (int32_t h = 0; h < Hq; ++h) {
+        int32_t g = kv_head_of_q_head ? kv_head_of_q_head[h] : h / group;
+        if (g < 0 || g >= Hkv)
+            return -3;
+    }
+    /* validate every table entry that will be read */
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        int64_t L = context_lens[s];
+        int64_t nblk = (L + B - 1) / B;
+        if (nblk > max_blocks_per_seq)
+            return -1;
+        for (int64_t j = 0; j < nblk; ++j) {
+            int32_t blk = block_tables[(int64_t)s * max_blocks_per_seq + j];
+            if (blk < 0 || blk >= num_blocks)
+                return -2;
+        }
+    }
+
+    int failed = 0;
+    const int64_t pairs = (int64_t)num_seqs * Hkv;
+#ifdef _OPENMP
+    if (num_threads <= 0)
+        num_threads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads)
+#endif
+    for (int64_t pg = 0; pg < pairs; ++pg) {
+        const int32_t s = (int32_t)(pg / Hkv), g = (int32_t)(pg % Hkv);
+        const int64_t L = context_lens[s];
+        const int32_t row0 = q_starts[s], W = q_starts[s + 1] - q_starts[s];
+        if (W <= 0)
+            continue;
+        /* step 1: materialise contiguous K_s, V_s for KV head g */
+        double *K = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * D);
+        double *V = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * D);
+        double *x = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+        if (!K || !V || !x) {
+            free(K); free(V); free(x);
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            failed = 1;
+            continue;
+        }
+        for (int64_t t = 0; t < L; ++t) {
+            int32_t blk = block_tables[(int64_t)s * max_blocks_per_seq + t / B];
+            size_t base = ((((size_t)blk * Hkv) + g) * B + (size_t)(t % B)) * D;
+            for (int32_t k = 0; k < D; ++k) {
+                K[t * D + k] = bf16_bits_to_f64(k_pool[base + k]);
+                V[t * D + k] = bf16_bits_to_f64(v_pool[base + k]);
+            }
+        }
+        /* step 2: every query row of s, every q head that reads KV head g */
+        for (int32_t w = 0; w < W; ++w) {
+            const int64_t r = (int64_t)row0 + w;
+            int64_t n = causal ? L - W + w + 1 : L;
+            if (n < 0) n = 0;
+            if (n > L) n = L;
+            for (int32_t h = 0; h < Hq; ++h) {
+                int32_t gh = kv_head_of_q_head ? kv_head_of_q_head[h] : h / group;
+                if (gh != g)
+                    continue;
+                const uint16_t *qv = q + ((size_t)r * Hq + h) * D;
+                double *o = out + ((size_t)r * Hq + h) * D;
+                double M = -INFINITY;
+                for (int64_t t = 0; t < n; ++t) {
+                    double dot = 0.0;
+                    for (int32_t k = 0; k < D; ++k)
+                        dot += bf16_bits_to_f64(qv[k]) * K[t * D + k];
+                    x[t] = scale * dot;
+                    if (x[t] > M)
+                        M = x[t];
+                }
+                const int has_sink = sinks != NULL;
+                const double sink = has_sink ? (double)sinks[h] : 0.0;
+                if (has_sink && sink > M)
+                    M = sink;
+                double den = 0.0;
+                for (int32_t k = 0; k < D; ++k)
+                    o[k] = 0.0;
+                for (int64_t t = 0; t < n; ++t) {
+                    double e = exp(x[t] - M);
+                    den += e;
+                    for (int32_t k = 0; k < D; ++k)
+                        o[k] += e * V[t * D + k];
+                }
+                if (has_sink)
+                    den += exp(sink - M);
+                for (int32_t k = 0; k < D; ++k)
+                    o[k] = den > 0.0 ? o[k] / den : 0.0;
+            }
+        }
+        free(K);
+        free(V);
+        free(x);
+    }
+    return failed ? -4 : 0;
+}
+
+/*
+ * Row argmax over the vocabulary, ties to the lowest index: scan v = 0..V-1 and
+ * replace the best only on a strictly greater value.
+ */
+void oracle_argmax_rows(const float *logits, int64_t rows, int32_t vocab, int32_t *argmax_out)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *row = logits + (size_t)r * vocab;
+        int32_t best = 0;
+        for (int32_t v = 1; v < vocab; ++v)
+            if (row[v] > row[best])
+                best = v;
+        argmax_out[r] = best;
+    }
+}
+
+/*
+ * Greedy accept over draft chains.  Sequence s owns rows q_starts[s] ..
+ * q_starts[s+1]-1 (W rows).  Row 0 is the query of the last committed token;
+ * row j >= 1 carries draft d_j = draft_tokens[q_starts[s] + j].  With a_j the
+ * target argmax of row j, draft d_j is accepted while d_i == a_{i-1} for every
+ * i <= j.  accept_len[s] = n, the number of accepted drafts; the emitted tokens
+ * are d_1..d_n followed by the target's own choice a_n (n + 1 tokens), written
+ * to out_tokens[q_starts[s] + 0 .. n]; the remaining slots of the sequence are
+ * set to -1.  A sequence with no rows gets accept_len = -1.
+ */
+void oracle_spec_accept_greedy(const float *logits, int32_t vocab,
+                               const int32_t *q_starts, const int32_t *draft_tokens,
+                               int32_t num_seqs, int32_t *argmax_out,
+                               int32_t *accept_len, int32_t *out_tokens)
+{
+    const int64_t total = q_starts[num_seqs];
+    oracle_argmax_rows(logits, total, vocab, argmax_out);
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        const int32_t r0 = q_starts[s], W = q_starts[s + 1] - q_starts[s];
+        if (W <= 0) {
+            accept_len[s] = -1;
+            continue;
+        }
+        int32_t n = 0;
+        while (n + 1 < W && draft_tokens[r0 + n + 1] == argmax_out[r0 + n])
+            ++n;
+        accept_len[s] = n;
+        for (int32_t j = 0; j < W; ++j)
+            out_tokens[r0 + j] = -1;
+        for (int32_t j = 0; j < n; ++j)
+            out_tokens[r0 + j] = draft_tokens[r0 + j + 1];
+        out_tokens[r0 + n] = argmax_out[r0 + n];
+    }
+}

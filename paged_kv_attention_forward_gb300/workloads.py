@@ -1,0 +1,388 @@
+"""Seeded synthetic inputs shaped like the serving workloads the pages describe.
+
+This module only draws random numbers and lays out buffers: block pools, block
+tables, context lengths, query rows, new K/V rows, sink logits, verify logits
+and draft chains.  It holds none of the arithmetic of attention, append or
+accept, so the float64 oracle and the CUDA path can both consume its output.
+Everything is numpy (bf16 values are carried as their uint16 bit patterns).
+
+Workloads (sizes from the continuous-batching / speculative-decoding pages):
+  tiny_decode       4 seqs, cached lengths {37,100,203,800}, 8 q / 2 kv heads,
+                    head_dim 64, block 16; append 1 token each, 1 decode row.
+  ministral_decode  4 seqs, lengths U[760,840], 32 q / 8 kv heads, head_dim
+                    128, block 16, 40 layers with independent pools.
+  cb_mix            64 seqs, cached lengths log-uniform, 48 of them sharing a
+                    2900-token prefix through the same physical full blocks,
+                    40 q / 8 kv heads, head_dim 128, block 16; append 1 token
+                    each, 1 decode row.
+  spec_verify       16 seqs, lengths U[4096,32768] including a causal verify
+                    window of U{1..16} rows whose K/V are appended first,
+                    32 q / 8 kv heads, head_dim 128; verify logits over a
+                    151936-token vocabulary and a draft chain per sequence.
+  sinks_scale       128 seqs x 8192 tokens, 64 q / 8 kv heads, head_dim 64,
+                    block 32, one fp32 sink logit per q head.
+"""
+from __future__ import annotations
+
+import math
+import os
+from concurrent.futures import ThreadPoolExecutor
+from dataclasses import dataclass, field
+from typing import Optional
+
+import numpy as np
+
+BF16_QNAN = np.uint16(0x7FC0)
+_CHUNK = 1 << 22  # elements per independently seeded chunk (fixed: results do not depend on threads)
+
+
+def _seed_seq(seed) -> np.random.SeedSequence:
+    return seed if isinstance(seed, np.random.SeedSequence) else np.random.SeedSequence(seed)
+
+
+def _workers() -> int:
+    try:
+        n = len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        n = os.cpu_count() or 1
+    return max(1, min(16, n))
+
+
+def _round_f32_to_bf16_bits(buf: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16 (nearest, ties to even); returns uint16 bits.
+
+    Only finite inputs are produced here, so the integer form of the rounding is exact.
+    """
+    u = buf.view(np.uint32)
+    lsb = (u >> 16) & np.uint32(1)
+    u += np.uint32(0x7FFF)
+    u += lsb
+    u >>= 16
+    return u.astype(np.uint16)
+
+
+def _fill_parallel(seed_seq: np.random.SeedSequence, out_flat: np.ndarray, kind: str, scale: float):
+    n = out_flat.shape[0]
+    nchunks = (n + _CHUNK - 1) // _CHUNK
+    if nchunks == 0:
+        return
+    children = seed_seq.spawn(nchunks)
+
+    def work(i):
+        lo = i * _CHUNK
+        hi = min(n, lo + _CHUNK)
+        g = np.random.Generator(np.random.PCG64(children[i]))
+        tmp = g.standard_normal(hi - lo, dtype=np.float32)
+        if scale != 1.0:
+            tmp *= np.float32(scale)
+        if kind == "bf16":
+            out_flat[lo:hi] = _round_f32_to_bf16_bits(tmp)
+        else:
+            out_flat[lo:hi] = tmp
+
+    if nchunks == 1:
+        work(0)
+    else:
+        with ThreadPoolExecutor(_workers()) as ex:
+            list(ex.map(work, range(nchunks)))
+
+
+def normal_bf16(seed_seq: np.random.SeedSequence, shape, std: float = 1.0) -> np.ndarray:
+    """N(0, std^2) samples rounded to bf16, as uint16 bits."""
+    out = np.empty(int(np.prod(shape)), dtype=np.uint16)
+    _fill_parallel(seed_seq, out, "bf16", std)
+    return out.reshape(shape)
+
+
+def normal_f32(seed_seq: np.random.SeedSequence, shape, std: float = 1.0) -> np.ndarray:
+    out = np.empty(int(np.prod(shape)), dtype=np.float32)
+    _fill_parallel(seed_seq, out, "f32", std)
+    return out.reshape(shape)
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Widen bf16 bit patterns to float32 (exact)."""
+    return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round finite float32 values to bf16 bits (nearest, ties to even)."""
+    return _round_f32_to_bf16_bits(np.array(x, dtype=np.float32, copy=True))
+
+
+@dataclass
+class PagedBatch:
+    """One batch of paged-KV work.  bf16 tensors are uint16 bit patterns.
+
+    k_pool, v_pool: [layers, num_blocks, H_kv, block_size, head_dim]; the slots of
+        the tokens that the batch appends still hold filler until the append runs.
+    block_tables: int32 [S, max_blocks_per_seq]; entries past a sequence's last
+        block are -1.
+    context_lens_old: int32 [S] tokens cached before the append.
+    context_lens: int32 [S] tokens cached after the append (what attention reads).
+    new_starts: int32 [S+1] offsets of each sequence's rows in k_new / v_new.
+    k_new, v_new: [layers, R_new, H_kv, head_dim] rows to append.
+    q_starts: int32 [S+1]; q: [layers, R, H_q, head_dim] query rows.
+    sinks: float32 [H_q] or None.
+    """
+    name: str
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    k_pool: np.ndarray
+    v_pool: np.ndarray
+    block_tables: np.ndarray
+    context_lens_old: np.ndarray
+    context_lens: np.ndarray
+    new_starts: np.ndarray
+    k_new: np.ndarray
+    v_new: np.ndarray
+    q_starts: np.ndarray
+    q: np.ndarray
+    causal: bool
+    sinks: Optional[np.ndarray] = None
+    shared_block_ids: np.ndarray = field(default_factory=lambda: np.zeros(0, np.int32))
+    sharing_seqs: np.ndarray = field(default_factory=lambda: np.zeros(0, np.int32))
+    logits: Optional[np.ndarray] = None        # float32 [R, vocab] (verify workloads)
+    draft_tokens: Optional[np.ndarray] = None  # int32 [R]; slot 0 of each sequence is -1
+    planted_targets: Optional[np.ndarray] = None  # int32 [R]: token given the planted maximum
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.context_lens.shape[0])
+
+    @property
+    def layers(self) -> int:
+        return int(self.k_pool.shape[0])
+
+    @property
+    def num_blocks(self) -> int:
+        return int(self.k_pool.shape[1])
+
+    @property
+    def total_q_rows(self) -> int:
+        return int(self.q_starts[-1])
+
+    @property
+    def max_blocks_per_seq(self) -> int:
+        return int(self.block_tables.shape[1])
+
+    @property
+    def max_context_len(self) -> int:
+        return int(self.context_lens.max()) if self.num_seqs else 0
+
+    @property
+    def max_q_rows_per_seq(self) -> int:
+        return int(np.diff(self.q_starts).max()) if self.num_seqs else 0
+
+
+def build_batch(seed, *, name: str, lens: np.ndarray, n_new: np.ndarray, q_rows: np.ndarray,
+                num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+                causal: bool, with_sinks: bool = False, layers: int = 1,
+                shared_prefix: int = 0, sharing: Optional[np.ndarray] = None,
+                filler: str = "random", slack_frac: float = 0.10,
+                extra_table_cols: int = 0) -> PagedBatch:
+    """Lay out a paged batch.
+
+    lens: final context length per sequence (after the append); n_new: tokens the
+    batch appends per sequence (the last n_new positions); q_rows: query rows per
+    sequence.  ``sharing`` marks sequences whose first ``shared_prefix`` tokens are
+    the same; their full prefix blocks are one set of physical blocks, the partial
+    prefix tail sits (with identical values) in each sequence's own block.
+    filler: "random" puts N(0,1) values in every slot no token owns (pool slack,
+    block tails, slots awaiting the append); "nan" puts bf16 NaN there instead.
+    """
+    root = _seed_seq(seed)
+    (s_struct, s_k, s_v, s_q, s_kn, s_vn, s_sink) = root.spawn(7)
+    rng = np.random.Generator(np.random.PCG64(s_struct))
+    lens = np.asarray(lens, dtype=np.int64)
+    n_new = np.asarray(n_new, dtype=np.int64)
+    q_rows = np.asarray(q_rows, dtype=np.int64)
+    S = lens.shape[0]
+    B = block_size
+    if sharing is None:
+        sharing = np.zeros(S, dtype=bool)
+    sharing = np.asarray(sharing, dtype=bool)
+    old = lens - n_new
+    assert np.all(old >= 0)
+    n_full_shared = shared_prefix // B if sharing.any() else 0
+    if sharing.any():
+        assert np.all(old[sharing] >= shared_prefix), "sharing sequences must hold the whole prefix"
+    nblk = (lens + B - 1) // B
+    private = nblk - np.where(sharing, n_full_shared, 0)
+    n_unique = int(n_full_shared + private.sum())
+    slack = max(1, int(math.ceil(slack_frac * n_unique)))
+    num_blocks = n_unique + slack
+    perm = rng.permutation(num_blocks).astype(np.int32)
+    shared_ids = perm[:n_full_shared]
+    max_blocks = int(max(1, nblk.max() if S else 1)) + extra_table_cols
+    tables = np.full((S, max_blocks), -1, dtype=np.int32)
+    cursor = n_full_shared
+    for s in range(S):
+        j0 = 0
+        if sharing[s]:
+            tables[s, :n_full_shared] = shared_ids
+            j0 = n_full_shared
+        cnt = int(nblk[s] - j0)
+        tables[s, j0:j0 + cnt] = perm[cursor:cursor + cnt]
+        cursor += cnt
+    assert cursor == n_unique
+
+    H, D = num_kv_heads, head_dim
+    shape = (layers, num_blocks, H, B, D)
+    k_pool = normal_bf16(s_k, shape)
+    v_pool = normal_bf16(s_v, shape)
+
+    # identical prefix tail tokens in every sharing sequence's own partial block
+    tail = shared_prefix - n_full_shared * B if sharing.any() else 0
+    if tail > 0:
+        idx = np.nonzero(sharing)[0]
+        src_blk = tables[idx[0], n_full_shared]
+        for s in idx[1:]:
+            dst_blk = tables[s, n_full_shared]
+            k_pool[:, dst_blk, :, :tail, :] = k_pool[:, src_blk, :, :tail, :]
+            v_pool[:, dst_blk, :, :tail, :] = v_pool[:, src_blk, :, :tail, :]
+
+    if filler == "nan":
+        owned = np.zeros((num_blocks, B), dtype=bool)
+        for s in range(S):
+            for t0 in range(0, int(old[s]), B):
+                blk = tables[s, t0 // B]
+                owned[blk, : min(B, int(old[s]) - t0)] = True
+        unowned = np.broadcast_to(~owned[:, None, :], (num_blocks, H, B))
+        k_pool[:, unowned] = BF16_QNAN
+        v_pool[:, unowned] = BF16_QNAN
+    elif filler != "random":
+        raise ValueError(filler)
+
+    new_starts = np.zeros(S + 1, dtype=np.int32)
+    new_starts[1:] = np.cumsum(n_new)
+    q_starts = np.zeros(S + 1, dtype=np.int32)
+    q_starts[1:] = np.cumsum(q_rows)
+    r_new = int(new_starts[-1])
+    R = int(q_starts[-1])
+    k_new = normal_bf16(s_kn, (layers, r_new, H, D))
+    v_new = normal_bf16(s_vn, (layers, r_new, H, D))
+    q = normal_bf16(s_q, (layers, R, num_q_heads, D))
+    sinks = normal_f32(s_sink, (num_q_heads,)) if with_sinks else None
+    return PagedBatch(name=name, num_q_heads=num_q_heads, num_kv_heads=H, head_dim=D,
+                      block_size=B, k_pool=k_pool, v_pool=v_pool, block_tables=tables,
+                      context_lens_old=old.astype(np.int32), context_lens=lens.astype(np.int32),
+                      new_starts=new_starts, k_new=k_new, v_new=v_new, q_starts=q_starts, q=q,
+                      causal=causal, sinks=sinks, shared_block_ids=shared_ids.astype(np.int32),
+                      sharing_seqs=np.nonzero(sharing)[0].astype(np.int32))
+
+
+def add_verify_logits(batch: PagedBatch, seed, vocab: int, std: float = 2.0,
+                      hit_prob: float = 0.7, planted_value: float = 20.0) -> PagedBatch:
+    """Attach verify-row logits and a draft chain to ``batch``.
+
+    Logits are N(0, std^2); one token per row (drawn uniformly) is given the value
+    ``planted_value`` (10 sigma at std 2), which makes it that row's maximum.  The
+    draft for row j >= 1 of a sequence is row j-1's planted token with probability
+    ``hit_prob``, otherwise a uniformly drawn token (which may match by chance).
+    Slot 0 of every sequence holds -1 (row 0 carries no draft).
+    """
+    s_logit, s_pick = _seed_seq(seed).spawn(2)
+    rng = np.random.Generator(np.random.PCG64(s_pick))
+    R = batch.total_q_rows
+    logits = normal_f32(s_logit, (R, vocab), std)
+    planted = rng.integers(0, vocab, size=R).astype(np.int32)
+    logits[np.arange(R), planted] = np.float32(planted_value)
+    drafts = np.full(R, -1, dtype=np.int32)
+    coins = rng.random(R)
+    randoms = rng.integers(0, vocab, size=R).astype(np.int32)
+    for s in range(batch.num_seqs):
+        r0, r1 = int(batch.q_starts[s]), int(batch.q_starts[s + 1])
+        for r in range(r0 + 1, r1):
+            drafts[r] = planted[r - 1] if coins[r] < hit_prob else randoms[r]
+    batch.logits = logits
+    batch.draft_tokens = drafts
+    batch.planted_targets = planted
+    return batch
+
+
+def _loguniform_int(rng, lo, hi, size):
+    return np.rint(np.exp(rng.uniform(math.log(lo), math.log(hi), size=size))).astype(np.int64)
+
+
+WORKLOADS = ("tiny_decode", "ministral_decode", "cb_mix", "spec_verify", "sinks_scale")
+VOCAB = 151936
+
+
+def make_workload(name: str, seed: int = 0, filler: str = "random", layers: Optional[int] = None) -> PagedBatch:
+    """Build one of the named workloads (see the module docstring)."""
+    base = np.random.SeedSequence([seed, WORKLOADS.index(name)])
+    s_shape, s_batch, s_extra = base.spawn(3)
+    rng = np.random.Generator(np.random.PCG64(s_shape))
+    if name == "tiny_decode":
+        old = np.array([37, 100, 203, 800])
+        return build_batch(s_batch, name=name, lens=old + 1, n_new=np.ones(4, np.int64),
+                           q_rows=np.ones(4, np.int64), num_q_heads=8, num_kv_heads=2,
+                           head_dim=64, block_size=16, causal=False, filler=filler)
+    if name == "ministral_decode":
+        lens = rng.integers(760, 841, size=4)
+        return build_batch(s_batch, name=name, lens=lens, n_new=np.zeros(4, np.int64),
+                           q_rows=np.ones(4, np.int64), num_q_heads=32, num_kv_heads=8,
+                           head_dim=128, block_size=16, causal=False, filler=filler,
+                           layers=40 if layers is None else layers)
+    if name == "cb_mix":
+        S, n_share, prefix = 64, 48, 2900
+        sharing = np.zeros(S, dtype=bool)
+        sharing[rng.permutation(S)[:n_share]] = True
+        old = np.where(sharing, _loguniform_int(rng, prefix + 1, 32767, S),
+                       _loguniform_int(rng, 128, 32767, S))
+        return build_batch(s_batch, name=name, lens=old + 1, n_new=np.ones(S, np.int64),
+                           q_rows=np.ones(S, np.int64), num_q_heads=40, num_kv_heads=8,
+                           head_dim=128, block_size=16, causal=False, filler=filler,
+                           shared_prefix=prefix, sharing=sharing)
+    if name == "spec_verify":
+        S = 16
+        lens = rng.integers(4096, 32769, size=S)
+        w = rng.integers(1, 17, size=S)
+        b = build_batch(s_batch, name=name, lens=lens, n_new=w, q_rows=w, num_q_heads=32,
+                        num_kv_heads=8, head_dim=128, block_size=16, causal=True, filler=filler)
+        return add_verify_logits(b, s_extra, VOCAB)
+    if name == "sinks_scale":
+        S = 128
+        return build_batch(s_batch, name=name, lens=np.full(S, 8192), n_new=np.zeros(S, np.int64),
+                           q_rows=np.ones(S, np.int64), num_q_heads=64, num_kv_heads=8,
+                           head_dim=64, block_size=32, causal=False, with_sinks=True, filler=filler)
+    raise KeyError(name)
+
+
+def select_seqs(batch: PagedBatch, seqs) -> PagedBatch:
+    """A batch holding only the listed sequences (same pool, same physical blocks).
+
+    Used to run one sequence 'alone' against the same pool, or to cut a bounded
+    sample for CPU timing.
+    """
+    seqs = np.asarray(seqs, dtype=np.int64)
+    q_rows = np.diff(batch.q_starts)[seqs]
+    n_new = np.diff(batch.new_starts)[seqs]
+    q_starts = np.zeros(len(seqs) + 1, np.int32)
+    q_starts[1:] = np.cumsum(q_rows)
+    new_starts = np.zeros(len(seqs) + 1, np.int32)
+    new_starts[1:] = np.cumsum(n_new)
+    q_idx = np.concatenate([np.arange(batch.q_starts[s], batch.q_starts[s + 1]) for s in seqs]) \
+        if len(seqs) else np.zeros(0, np.int64)
+    n_idx = np.concatenate([np.arange(batch.new_starts[s], batch.new_starts[s + 1]) for s in seqs]) \
+        if len(seqs) else np.zeros(0, np.int64)
+    sub = PagedBatch(name=batch.name + "[sel]", num_q_heads=batch.num_q_heads,
+                     num_kv_heads=batch.num_kv_heads, head_dim=batch.head_dim,
+                     block_size=batch.block_size, k_pool=batch.k_pool, v_pool=batch.v_pool,
+                     block_tables=np.ascontiguousarray(batch.block_tables[seqs]),
+                     context_lens_old=batch.context_lens_old[seqs].copy(),
+                     context_lens=batch.context_lens[seqs].copy(), new_starts=new_starts,
+                     k_new=np.ascontiguousarray(batch.k_new[:, n_idx]),
+                     v_new=np.ascontiguousarray(batch.v_new[:, n_idx]),
+                     q_starts=q_starts, q=np.ascontiguousarray(batch.q[:, q_idx]),
+                     causal=batch.causal, sinks=batch.sinks,
+                     shared_block_ids=batch.shared_block_ids,
+                     sharing_seqs=np.nonzero(np.isin(seqs, batch.sharing_seqs))[0].astype(np.int32))
+    if batch.logits is not None:
+        sub.logits = np.ascontiguousarray(batch.logits[q_idx])
+        sub.draft_tokens = batch.draft_tokens[q_idx].copy()
+        sub.planted_targets = batch.planted_targets[q_idx].copy()
+    return sub
