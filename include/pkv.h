@@ -1,0 +1,232 @@
+/*
+ * pkv.h -- C ABI of libpkv.so: batched paged-KV attention for continuous
+ * batching on NVIDIA GB300 (sm_103a).
+ *
+ * Three operations, each one or two hand-written CUDA kernels:
+ *   paged_kv_append          scatter new tokens' K/V rows into the block pool
+ *   paged_attention_forward  decode / causal verify-window attention over K/V
+ *                            gathered through per-sequence block tables, with
+ *                            optional per-head sink logits
+ *   spec_accept_greedy       per-row argmax of verify logits, then a walk of
+ *                            each draft chain to its first mismatch
+ *
+ * Conventions shared by every entry point
+ *  - Pointers are DEVICE pointers unless the argument says HOST.  The library
+ *    allocates no memory and owns no buffer: the caller owns every input,
+ *    output and workspace, and must keep them alive until the stream reaches
+ *    the launched work.
+ *  - bf16 arrays are IEEE bfloat16 (the high 16 bits of a binary32).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Every call is asynchronous on it, except pkv_device_status().
+ *  - Every call returns a pkv_status.  Argument errors are found on the host
+ *    before anything is launched; the text of the last error of the calling
+ *    thread is available from pkv_last_error_string().  Conditions that only
+ *    the device can see (a block id outside the pool, a context longer than
+ *    the table or than max_context_len, a sequence with more query rows than
+ *    max_q_rows_per_seq) never fault: the kernel clamps the access, records a
+ *    bit in a device status word and carries on; pkv_device_status() reports
+ *    and clears it.  Outputs of the affected rows are then unspecified.
+ *  - Block pool layout: K and V are separate pools, each
+ *    bf16 [num_blocks][num_kv_heads][block_size][head_dim], so one block of one
+ *    KV head is block_size * head_dim contiguous values.  Identical prefixes
+ *    may be shared by pointing several block tables at the same physical
+ *    block ids.
+ *  - Block tables: int32 [num_seqs][max_blocks_per_seq]; logical token t of
+ *    sequence s is slot t % block_size of block block_tables[s][t / block_size].
+ *
+ * Sources (page title, section): TensorSharp "高级功能" (advanced features),
+ * sections "连续批处理与分页 KV 缓存" (continuous batching and the paged KV
+ * cache: fixed-size blocks from a shared pool, full blocks content-hashed and
+ * shared across requests), "原生分页注意力" (native paged attention, gathering
+ * K/V from the paged buffers; the WithSinks variant for GPT OSS) and the
+ * "批量前向" (batched forward) paragraph (paged K/V scatter-write);
+ * TensorFold article, sections "先记住一条铁律" (every verify-window row uses the
+ * serial step's arithmetic) and "接受规则：GPU 上的 accept 内核" (the accept
+ * kernel); TensorSharp "高级功能", section "MTP / NextN 推测解码" (verify all
+ * drafts in one batched forward, commit the accepted prefix).
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_NULL = -1,        /* a required pointer is NULL                          */
+    PKV_ERR_SHAPE = -2,       /* sizes inconsistent or out of range                  */
+    PKV_ERR_UNSUPPORTED = -3, /* head_dim / block_size / group x window not built    */
+    PKV_ERR_WORKSPACE = -4,   /* workspace too small, or (device) not zero on entry  */
+    PKV_ERR_BAD_BLOCK = -5,   /* (device) block id outside the pool / table overrun  */
+    PKV_ERR_CUDA = -6,        /* a CUDA runtime call or kernel launch failed         */
+    PKV_ERR_ALIGN = -7,       /* a pointer is not 16-byte aligned                    */
+    PKV_ERR_TIMEOUT = -8      /* (device) a bounded wait inside a kernel expired     */
+} pkv_status;
+
+enum { PKV_DTYPE_BF16 = 0, PKV_DTYPE_F32 = 1 };
+
+/* Bits of the device status word (see pkv_device_status). */
+enum {
+    PKV_DEV_BAD_BLOCK = 1,     /* a block id outside [0, num_blocks)                      */
+    PKV_DEV_TABLE_OVERRUN = 2, /* a length past max_blocks_per_seq * block_size or
+                                  past max_context_len                                    */
+    PKV_DEV_TOO_MANY_ROWS = 4, /* a sequence with more rows than max_q_rows_per_seq       */
+    PKV_DEV_WORKSPACE = 8,     /* the attention workspace's counters were not zero        */
+    PKV_DEV_TIMEOUT = 16       /* a bounded wait expired                                  */
+};
+
+/* One layer's K/V block pool (host struct holding device pointers).
+ * k_pool, v_pool: bf16 [num_blocks][num_kv_heads][block_size][head_dim],
+ * 16-byte aligned. */
+typedef struct pkv_pool {
+    void *k_pool;
+    void *v_pool;
+    int32_t num_blocks;
+    int32_t block_size;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+} pkv_pool;
+
+/* Version of this ABI (incremented on any incompatible change). */
+int pkv_abi_version(void);
+
+/*
+ * Paged K/V scatter-append ("批量前向": the batched forward pairs its
+ * projections with a paged K/V scatter-write).
+ *
+ * New token i of sequence s (rows new_starts[s] .. new_starts[s+1]-1 of k_new /
+ * v_new) sits at position p = context_lens_old[s] + i and is copied, bit for
+ * bit and for every KV head, to slot p % block_size of block
+ * block_tables[s][p / block_size] of both pools.  The caller must already have
+ * placed a private block at that table entry: shared (hashed, full) blocks are
+ * never appended to.  Rollback of rejected speculative tokens needs no call:
+ * the caller simply does not advance its context length past them.
+ *
+ *   pool             HOST struct; pools as described above
+ *   block_tables     int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens_old int32 [num_seqs], tokens cached before this append
+ *   new_starts       int32 [num_seqs + 1], prefix sums of new tokens per sequence
+ *   k_new, v_new     bf16 [total_new_rows][num_kv_heads][head_dim], 16-byte aligned
+ *   total_new_rows   HOST; equals new_starts[num_seqs]
+ * head_dim must be a multiple of 8.  Launches one kernel (none if
+ * total_new_rows == 0).  Device-side checks: table overrun, bad block id.
+ */
+int paged_kv_append(const pkv_pool *pool,
+                    const int32_t *block_tables, int32_t max_blocks_per_seq,
+                    const int32_t *context_lens_old, const int32_t *new_starts,
+                    const void *k_new, const void *v_new,
+                    int32_t num_seqs, int32_t total_new_rows, void *stream);
+
+/*
+ * Bytes of workspace paged_attention_forward needs for these sizes (a
+ * multiple of 256).  The workspace holds a small counter region that must be
+ * ZERO before the first call (allocate it zeroed, or call
+ * paged_attention_workspace_init once); every call that completes leaves it
+ * zero again, so one workspace serves any sequence of calls on one stream.
+ * Calls that may overlap on the GPU need separate workspaces.
+ */
+size_t paged_attention_workspace_size(int32_t num_seqs, int32_t total_q_rows,
+                                      int32_t num_q_heads, int32_t num_kv_heads,
+                                      int32_t head_dim, int32_t max_context_len);
+
+/* Zero a workspace (cudaMemsetAsync on `stream`). */
+int paged_attention_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Batched paged attention ("原生分页注意力", with the GPT OSS sinks variant; the
+ * causal verify window per "先记住一条铁律").
+ *
+ * For query row r of sequence s (W = q_starts[s+1] - q_starts[s] rows,
+ * w = r - q_starts[s]) and q head h reading KV head g = map(h):
+ *   n   = causal ? L - W + w + 1 : L,   L = context_lens[s]
+ *   x_t = scale * q[r][h] . K_s[t][g]                      for t < n
+ *   out[r][h] = sum_t e^{x_t} V_s[t][g] / (sum_t e^{x_t} + e^{sinks[h]})
+ * (the sink term only when sinks != NULL; a row that sees no key and has no
+ * sink outputs zeros).  K_s/V_s are read through the block table.
+ *
+ *   pool               HOST struct; head_dim in {64, 128}, block_size in {16, 32}
+ *   q                  bf16 [total_q_rows][num_q_heads][head_dim]
+ *   q_starts           int32 [num_seqs + 1], rows of each sequence
+ *   block_tables       int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens       int32 [num_seqs], keys in the cache INCLUDING the tokens
+ *                      appended for this step (decode token / verify window)
+ *   max_context_len    HOST upper bound of context_lens (sizes the grid)
+ *   max_q_rows_per_seq HOST upper bound of rows per sequence; G * it <= 128
+ *                      where G = num_q_heads / num_kv_heads
+ *   kv_head_of_q_head  HOST int32 [num_q_heads] or NULL (NULL: h -> h / G).
+ *                      Each KV head must serve exactly G q heads.
+ *   sinks              float32 [num_q_heads] or NULL: one logit per q head in
+ *                      the units of the scaled scores
+ *   causal             0: every row sees all L keys; 1: verify-window mask
+ *   scale              > 0, or <= 0 for 1/sqrt(head_dim)
+ *   out                [total_q_rows][num_q_heads][head_dim], bf16 or float32
+ *                      (out_dtype = PKV_DTYPE_BF16 / PKV_DTYPE_F32)
+ *   workspace          >= paged_attention_workspace_size(...) bytes, zero on
+ *                      first use (see above), 256-byte aligned
+ * Every row's arithmetic depends only on its own sequence (its length fixes
+ * the split of the keys into fixed 512-token chunks; partials merge in chunk
+ * order), so a row computed in any batch is bit-identical to the same row
+ * computed alone, and row w of a causal window is bit-identical to a one-row
+ * decode over the first L - W + w + 1 keys.  Launches one kernel.
+ */
+int paged_attention_forward(const pkv_pool *pool,
+                            const void *q, const int32_t *q_starts,
+                            const int32_t *block_tables, int32_t max_blocks_per_seq,
+                            const int32_t *context_lens,
+                            int32_t num_seqs, int32_t total_q_rows,
+                            int32_t max_context_len, int32_t max_q_rows_per_seq,
+                            int32_t num_q_heads, const int32_t *kv_head_of_q_head,
+                            const float *sinks, int32_t causal, float scale,
+                            void *out, int32_t out_dtype,
+                            void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of workspace spec_accept_greedy needs (a multiple of 256). */
+size_t spec_accept_workspace_size(int32_t total_rows, int32_t vocab);
+
+/*
+ * Greedy speculative accept ("接受规则：GPU 上的 accept 内核": compare each draft
+ * with the target's choice and follow the chain to the first mismatch).
+ *
+ * Sequence s owns rows q_starts[s] .. q_starts[s+1]-1 (W rows).  Row 0 is the
+ * query of the last committed token; row j >= 1 carries draft token
+ * d_j = draft_tokens[q_starts[s] + j] (slot 0 is ignored).
+ *   a_j           = argmax_v logits[q_starts[s] + j][v], ties to the lowest v
+ *   accept_len[s] = n, the largest n <= W-1 with d_i == a_{i-1} for all i <= n
+ *   out_tokens    = d_1 .. d_n, a_n at q_starts[s] + 0 .. n, then -1
+ * A sequence with no rows gets accept_len = -1.  NaN logits give an
+ * unspecified argmax.
+ *
+ *   logits        float32 [total_rows][vocab], 16-byte aligned
+ *   q_starts      int32 [num_seqs + 1]; draft_tokens int32 [total_rows]
+ *   argmax_out    int32 [total_rows]; accept_len int32 [num_seqs];
+ *   out_tokens    int32 [total_rows]
+ *   workspace     >= spec_accept_workspace_size(total_rows, vocab) bytes
+ * Launches two kernels.  Results are exact (integer) and independent of the
+ * batch.
+ */
+int spec_accept_greedy(const float *logits, int32_t vocab,
+                       const int32_t *q_starts, const int32_t *draft_tokens,
+                       int32_t num_seqs, int32_t total_rows,
+                       int32_t *argmax_out, int32_t *accept_len, int32_t *out_tokens,
+                       void *workspace, size_t workspace_bytes, void *stream);
+
+/* Text of the calling thread's last error ("" if none). */
+const char *pkv_last_error_string(void);
+
+/*
+ * Synchronise `stream`, then read and clear the device status word of the
+ * current device.  Returns PKV_OK, PKV_ERR_BAD_BLOCK (bad block id or table
+ * overrun), PKV_ERR_SHAPE (too many rows), PKV_ERR_WORKSPACE, PKV_ERR_TIMEOUT,
+ * or PKV_ERR_CUDA; *bits (if not NULL) receives the raw PKV_DEV_* bits.
+ */
+int pkv_device_status(void *stream, int32_t *bits);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -1,0 +1,203 @@
+// pkv_accept.cu -- greedy speculative accept on the device.
+//
+// TensorFold article, section "接受规则：GPU 上的 accept 内核": the accept kernel
+// compares each draft token with the target's choice and follows the chain to
+// the first mismatch, writing its verdict to a small arena; TensorSharp
+// "高级功能", DFlash paragraph: the argmax runs on the device so the
+// vocabulary-wide block never crosses PCIe.
+//
+// Kernel 1 (argmax_chunks): grid (chunks, rows).  Each CTA scans one slice of one
+//   row with 16-byte loads and reduces (value, index) pairs -- larger value wins,
+//   equal values go to the lower index -- with warp shuffles, then across warps.
+//   That order is total, so the result does not depend on the slicing.
+// Kernel 2 (accept_walk): one warp per sequence merges the slices of each row
+//   (same order), writes argmax_out, finds the first mismatching draft with a
+//   ballot, and writes accept_len and out_tokens.
+#include <cfloat>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+struct Best {
+    float v;
+    int i;
+};
+
+__device__ __forceinline__ Best better(Best a, Best b)
+{
+    // b wins on a strictly larger value, or an equal value at a lower index
+    return (b.v > a.v || (b.v == a.v && b.i < a.i)) ? b : a;
+}
+
+__device__ __forceinline__ Best warp_best(Best b)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        Best o;
+        o.v = __shfl_xor_sync(0xffffffffu, b.v, off);
+        o.i = __shfl_xor_sync(0xffffffffu, b.i, off);
+        b = better(b, o);
+    }
+    return b;
+}
+
+constexpr int kArgmaxThreads = 256;
+constexpr int kNoIndex = 0x7fffffff;
+
+__global__ void __launch_bounds__(kArgmaxThreads)
+argmax_chunks_kernel(const float *__restrict__ logits, int vocab, int chunk, int n_chunks,
+                     float2 *__restrict__ part, int vec_ok)
+{
+    const int c = blockIdx.x, r = blockIdx.y;
+    const int lo = c * chunk;
+    const int hi = min(vocab, lo + chunk);
+    const float *row = logits + (size_t)r * vocab;
+    Best b = {-INFINITY, kNoIndex};
+    if (vec_ok) {
+        // lo and hi are multiples of 4 except possibly hi == vocab (vocab % 4 == 0 when vec_ok)
+        const float4 *row4 = reinterpret_cast<const float4 *>(row);
+        const int lo4 = lo >> 2, hi4 = hi >> 2;
+#pragma unroll 4
+        for (int i = lo4 + threadIdx.x; i < hi4; i += kArgmaxThreads) {
+            const float4 x = __ldcs(row4 + i);
+            const int base = i << 2;
+            b = better(b, Best{x.x, base});
+            b = better(b, Best{x.y, base + 1});
+            b = better(b, Best{x.z, base + 2});
+            b = better(b, Best{x.w, base + 3});
+        }
+    } else {
+        for (int i = lo + threadIdx.x; i < hi; i += kArgmaxThreads)
+            b = better(b, Best{__ldcs(row + i), i});
+    }
+    b = warp_best(b);
+    __shared__ Best sm[kArgmaxThreads / 32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0)
+        sm[warp] = b;
+    __syncthreads();
+    if (warp == 0) {
+        b = lane < kArgmaxThreads / 32 ? sm[lane] : Best{-INFINITY, kNoIndex};
+        b = warp_best(b);
+        if (lane == 0)
+            part[(size_t)r * n_chunks + c] = make_float2(b.v, __int_as_float(b.i));
+    }
+}
+
+__global__ void __launch_bounds__(32)
+accept_walk_kernel(const float2 *__restrict__ part, int n_chunks, const int32_t *__restrict__ q_starts,
+                   const int32_t *__restrict__ drafts, int total_rows, int32_t *__restrict__ argmax_out,
+                   int32_t *__restrict__ accept_len, int32_t *__restrict__ out_tokens,
+                   int32_t *__restrict__ status)
+{
+    const int s = blockIdx.x, lane = threadIdx.x;
+    const int r0 = q_starts[s], W = q_starts[s + 1] - r0;
+    if (W <= 0) {
+        if (lane == 0)
+            accept_len[s] = -1;
+        return;
+    }
+    if (r0 < 0 || r0 + W > total_rows) {   // q_starts inconsistent with total_rows
+        if (lane == 0) {
+            accept_len[s] = -1;
+            atomicOr(status, PKV_DEV_TOO_MANY_ROWS);
+        }
+        return;
+    }
+    int n = -1, a_n = 0;
+    for (int base = 0; base < W; base += 32) {
+        const int j = base + lane;
+        int a = 0;
+        bool stop = false;
+        if (j < W) {
+            Best b = {-INFINITY, kNoIndex};
+            const float2 *pr = part + (size_t)(r0 + j) * n_chunks;
+            for (int c = 0; c < n_chunks; ++c) {
+                const float2 x = pr[c];
+                b = better(b, Best{x.x, __float_as_int(x.y)});
+            }
+            a = b.i == kNoIndex ? 0 : b.i;
+            argmax_out[r0 + j] = a;
+            stop = (j == W - 1) || (drafts[r0 + j + 1] != a);
+        }
+        if (n < 0) {
+            const unsigned m = __ballot_sync(0xffffffffu, stop);
+            if (m) {
+                const int first = __ffs(m) - 1;
+                n = base + first;
+                a_n = __shfl_sync(0xffffffffu, a, first);
+            }
+        }
+    }
+    // n is found: every row stops at the window end at the latest
+    for (int j = lane; j < W; j += 32)
+        out_tokens[r0 + j] = j < n ? drafts[r0 + j + 1] : (j == n ? a_n : -1);
+    if (lane == 0)
+        accept_len[s] = n;
+}
+
+int accept_chunks(int32_t total_rows, int32_t vocab, int sms)
+{
+    // enough CTAs to cover the GPU about twice, slices of at least 8192 values
+    const int max_chunks = (vocab + 8191) / 8192;
+    int want = (2 * sms + total_rows - 1) / (total_rows > 0 ? total_rows : 1);
+    if (want < 1)
+        want = 1;
+    return want < max_chunks ? want : (max_chunks > 0 ? max_chunks : 1);
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" size_t spec_accept_workspace_size(int32_t total_rows, int32_t vocab)
+{
+    if (total_rows < 0 || vocab <= 0)
+        return 0;
+    const int max_chunks = (vocab + 8191) / 8192;
+    return pkv::round_up((size_t)total_rows * max_chunks * sizeof(float2), 256) + 256;
+}
+
+extern "C" int spec_accept_greedy(const float *logits, int32_t vocab, const int32_t *q_starts,
+                                  const int32_t *draft_tokens, int32_t num_seqs, int32_t total_rows,
+                                  int32_t *argmax_out, int32_t *accept_len, int32_t *out_tokens,
+                                  void *workspace, size_t workspace_bytes, void *stream)
+{
+    using namespace pkv;
+    clear_error();
+    if (num_seqs < 0 || total_rows < 0 || vocab <= 0)
+        return set_error(PKV_ERR_SHAPE, "spec_accept_greedy: bad sizes (num_seqs %d, rows %d, vocab %d)",
+                         num_seqs, total_rows, vocab);
+    if (num_seqs == 0)
+        return PKV_OK;
+    if (!q_starts || !accept_len || (total_rows > 0 && (!logits || !draft_tokens || !argmax_out ||
+                                                        !out_tokens || !workspace)))
+        return set_error(PKV_ERR_NULL, "spec_accept_greedy: a required pointer is NULL");
+    if (total_rows > 0 && !aligned16(logits))
+        return set_error(PKV_ERR_ALIGN, "spec_accept_greedy: logits must be 16-byte aligned");
+    if (workspace_bytes < spec_accept_workspace_size(total_rows, vocab))
+        return set_error(PKV_ERR_WORKSPACE, "spec_accept_greedy: workspace %zu < %zu bytes", workspace_bytes,
+                         spec_accept_workspace_size(total_rows, vocab));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int n_chunks = accept_chunks(total_rows, vocab, sm_count());
+    float2 *part = static_cast<float2 *>(workspace);
+    if (total_rows > 0) {
+        if (total_rows > 65535)
+            return set_error(PKV_ERR_SHAPE, "spec_accept_greedy: at most 65535 rows per call");
+        int chunk = (vocab + n_chunks - 1) / n_chunks;
+        chunk = (chunk + 3) & ~3;
+        const int vec_ok = (vocab % 4) == 0;
+        argmax_chunks_kernel<<<dim3(n_chunks, total_rows), kArgmaxThreads, 0, st>>>(logits, vocab, chunk,
+                                                                                   n_chunks, part, vec_ok);
+        const int rc = check_cuda(cudaGetLastError(), "spec_accept_greedy argmax launch");
+        if (rc)
+            return rc;
+    }
+    int32_t *status = device_status_word();
+    if (!status)
+        return set_error(PKV_ERR_CUDA, "spec_accept_greedy: no device status word");
+    accept_walk_kernel<<<num_seqs, 32, 0, st>>>(part, n_chunks, q_starts, draft_tokens, total_rows, argmax_out,
+                                                accept_len, out_tokens, status);
+    return check_cuda(cudaGetLastError(), "spec_accept_greedy walk launch");
+}

@@ -1,0 +1,679 @@
+// pkv_attention.cu -- batched paged-KV attention (decode rows and causal verify windows).
+//
+// What it computes: TensorSharp "高级功能", section "原生分页注意力" -- attention of
+// each sequence's query rows over K/V gathered from the paged block pool, with a
+// variant carrying one sink logit per head (GPT OSS).  The causal verify window
+// and the bit-identity rule come from the TensorFold article, section
+// "先记住一条铁律": a verify row uses exactly the serial step's arithmetic, and a
+// row computed in a batch equals the row computed alone.
+//
+// Design (one kernel per call):
+//  * Work unit = (sequence s, KV head g, split i).  Split i covers keys
+//    [512 i, 512 i + 512) of s.  The split grid depends on the sequence's own
+//    length only, never on the batch, so every row's arithmetic is fixed by
+//    its own sequence.  Grid = (num_seqs * H_kv, ceil(max_context_len / 512)),
+//    split-major, so the first splits of all sequences (where shared prefix
+//    blocks live) run together and re-read shared blocks from L2.
+//  * One producer warp: a single lane reads the block table and issues TMA
+//    tile loads (cp.async.bulk.tensor, 128-byte swizzle) of each K and V block
+//    of the split into an NST-stage shared-memory ring, completion tracked by
+//    mbarriers.
+//  * NMT consumer warps, one per 16 query rows of the (s, g) pair: the G q heads
+//    of KV head g times the W rows of s, flattened row = w * G + head_in_group.
+//    Per KV block: S = Q K^T with mma.sync m16n8k16 (bf16 in, fp32 out), scale,
+//    causal / length mask, online softmax in base 2 (running max m, running sum
+//    l of the bf16-rounded weights), O += P V with mma.sync (P rounded to bf16).
+//    Keys past a row's limit get weight exactly 0, so a verify-window row and the
+//    same row decoded alone go through identical operations.
+//  * Partials (m, l, O) of every split go to the workspace.  The last CTA of an
+//    (s, g) pair to finish (atomic counter) merges the partials of each row in
+//    split order:  M = max(m_i, sink), out = sum_i 2^{m_i-M} O_i /
+//    (sum_i 2^{m_i-M} l_i + 2^{sink-M}), and resets the counter to zero.
+//  * Bounded waits only; block ids and lengths are range-checked on the device
+//    (clamped + status bit, never a fault).
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include <cuda_bf16.h>
+
+#include "pkv_internal.h"
+#include "pkv_ptx.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct AttnParams {
+    const uint16_t *q;            // bf16 [R][Hq][D]
+    const int32_t *q_starts;      // [S+1]
+    const int32_t *block_tables;  // [S][max_blocks]
+    const int32_t *context_lens;  // [S]
+    const float *sinks;           // [Hq] or null
+    void *out;                    // [R][Hq][D] bf16 or f32
+    float2 *part_ml;              // [R*Hq*n_max] (m in log2 units, l)
+    float *part_o;                // [R*Hq*n_max][D]
+    int32_t *counters;            // [S*Hkv]
+    int32_t *status;
+    int32_t num_seqs, max_blocks_per_seq, num_blocks, num_q_heads, num_kv_heads, group;
+    int32_t n_max, max_context_len, max_rows, total_rows;
+    int32_t causal, out_f32;
+    float scale_log2;             // scale * log2(e)
+    int16_t q_head_of[kMaxQHeads];  // q head of (kv head g, member j): q_head_of[g*group + j]
+};
+
+template <int D, int BS>
+struct Tile {
+    static constexpr int kHalves = D / 64;              // 128-byte column boxes per row
+    static constexpr int kBoxBytes = BS * 128;          // one box: BS rows x 128 B
+    static constexpr int kTileBytes = BS * D * 2;       // one KV block of one head
+    static_assert(kSplitTokens % BS == 0, "split must be whole blocks");
+    static_assert(D % 64 == 0, "head_dim multiple of 64");
+    static_assert(BS % 16 == 0, "block size multiple of 16");
+};
+
+// Byte offset of logical (token, 16-byte chunk) inside a swizzled tile:
+// chunk ch of token t lives in box ch/8, row t, at chunk position (ch%8) ^ (t%8).
+template <int BS>
+__device__ __forceinline__ uint32_t tile_off(int tok, int ch)
+{
+    return (uint32_t)((ch >> 3) * (BS * 128) + tok * 128 + (((ch & 7) ^ (tok & 7)) << 4));
+}
+
+template <int D, int BS, int NMT, int NST>
+__global__ void __launch_bounds__((NMT + 1) * 32)
+paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const AttnParams p)
+{
+    using T = Tile<D, BS>;
+    constexpr int NT = BS / 8;    // score n-tiles (8 keys each) per block
+    constexpr int KS = D / 16;    // k-steps of QK^T
+    constexpr int DN = D / 8;     // output n-tiles (8 dims each)
+    constexpr int C = kSplitTokens;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    uint8_t *k_tiles = smem;
+    uint8_t *v_tiles = smem + NST * T::kTileBytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(v_tiles + NST * T::kTileBytes);
+    uint64_t *empty = full + NST;
+    volatile int32_t *s_flag = reinterpret_cast<volatile int32_t *>(empty + NST);
+    // s_flag[0]: this CTA merges; [1]: abort; [2]: blocks issued; [3]: blocks consumed
+
+    const int pair = blockIdx.x;
+    const int s = pair / p.num_kv_heads;
+    const int g = pair - s * p.num_kv_heads;
+    const int split = blockIdx.y;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    int L = __ldg(p.context_lens + s);
+    const int L_cap = (int)min((long long)p.max_context_len, (long long)p.max_blocks_per_seq * BS);
+    if (L > L_cap || L < 0) {
+        if (split == 0 && threadIdx.x == 0)
+            atomicOr(p.status, PKV_DEV_TABLE_OVERRUN);
+        L = L < 0 ? 0 : L_cap;
+    }
+    const int n_splits = (L + C - 1) / C;
+    const int row0 = __ldg(p.q_starts + s);
+    int W = __ldg(p.q_starts + s + 1) - row0;
+    if (W <= 0)
+        return;
+    if (row0 < 0 || row0 + W > p.total_rows) {   // q_starts inconsistent with total_q_rows
+        if (split == 0 && g == 0 && threadIdx.x == 0)
+            atomicOr(p.status, PKV_DEV_TOO_MANY_ROWS);
+        return;
+    }
+    if (W > p.max_rows) {
+        if (split == 0 && threadIdx.x == 0)
+            atomicOr(p.status, PKV_DEV_TOO_MANY_ROWS);
+        W = p.max_rows;
+    }
+    const int M = p.group * W;         // query rows of this (s, g)
+    const int n_mt = (M + 15) >> 4;    // consumer warps with work
+    if (split >= n_splits && !(n_splits == 0 && split == 0))
+        return;
+    // n_splits == 0 (empty context): split 0 still runs to write the (zero / sink) output.
+
+    const int t0 = split * C;
+    const int t1 = min(t0 + C, L);
+    const int blk0 = t0 / BS;
+    const int nblk = t1 > t0 ? (t1 - t0 + BS - 1) / BS : 0;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NST; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], n_mt);
+        }
+        mbar_fence_init();
+        s_flag[0] = 0;
+        s_flag[1] = 0;
+        s_flag[2] = 0;
+        s_flag[3] = 0;
+    }
+    __syncthreads();
+
+    if (warp == NMT) {
+        // ---------------- producer: block table -> TMA ----------------
+        if (lane == 0) {
+            prefetch_tensormap(&tm_k);
+            prefetch_tensormap(&tm_v);
+            const int32_t *table = p.block_tables + (size_t)s * p.max_blocks_per_seq + blk0;
+            int k = 0;
+            for (; k < nblk; ++k) {
+                const int st = k % NST;
+                if (k >= NST) {
+                    if (!mbar_wait_bounded(&empty[st], ((k / NST) + 1) & 1, kWaitLimitCycles)) {
+                        atomicOr(p.status, PKV_DEV_TIMEOUT);
+                        s_flag[1] = 1;
+                        break;
+                    }
+                }
+                if (s_flag[1])
+                    break;
+                int blk = __ldg(table + k);
+                if (blk < 0 || blk >= p.num_blocks) {
+                    atomicOr(p.status, PKV_DEV_BAD_BLOCK);
+                    blk = 0;
+                }
+                const int y = (blk * p.num_kv_heads + g) * BS;
+                mbar_arrive_expect_tx(&full[st], 2 * T::kTileBytes);
+#pragma unroll
+                for (int h = 0; h < T::kHalves; ++h) {
+                    tma_load_2d(k_tiles + st * T::kTileBytes + h * T::kBoxBytes, &tm_k, &full[st], h * 64, y);
+                    tma_load_2d(v_tiles + st * T::kTileBytes + h * T::kBoxBytes, &tm_v, &full[st], h * 64, y);
+                }
+            }
+            s_flag[2] = k;
+        }
+    } else if (warp < n_mt) {
+        // ---------------- consumers ----------------
+        const int g_row = lane >> 2;          // row within the 16-row m-tile (and +8)
+        const int q_col = (lane & 3) * 2;     // column pair within an 8/16-wide fragment
+        const int jA = warp * 16 + g_row, jB = jA + 8;
+        // Query fragments (A operand, row-major 16 x D) for rows jA / jB.
+        uint32_t qf[KS][4];
+        int limA = L, limB = L;
+        {
+            const uint32_t *qA = nullptr, *qB = nullptr;
+            if (jA < M) {
+                const int w = jA / p.group, hA = p.q_head_of[g * p.group + (jA - w * p.group)];
+                qA = reinterpret_cast<const uint32_t *>(p.q + ((size_t)(row0 + w) * p.num_q_heads + hA) * D);
+                if (p.causal)
+                    limA = L - W + w + 1;
+            }
+            if (jB < M) {
+                const int w = jB / p.group, hB = p.q_head_of[g * p.group + (jB - w * p.group)];
+                qB = reinterpret_cast<const uint32_t *>(p.q + ((size_t)(row0 + w) * p.num_q_heads + hB) * D);
+                if (p.causal)
+                    limB = L - W + w + 1;
+            }
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                const int c0 = (ks * 16 + q_col) >> 1, c1 = (ks * 16 + 8 + q_col) >> 1;
+                qf[ks][0] = qA ? __ldg(qA + c0) : 0u;
+                qf[ks][1] = qB ? __ldg(qB + c0) : 0u;
+                qf[ks][2] = qA ? __ldg(qA + c1) : 0u;
+                qf[ks][3] = qB ? __ldg(qB + c1) : 0u;
+            }
+        }
+        float o[DN][4];
+#pragma unroll
+        for (int i = 0; i < DN; ++i)
+            o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+        float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
+
+        // per-lane ldmatrix address parts
+        const int k_tok = 8 * (lane >> 4) + (lane & 7);   // K: token within a 16-key pair of n-tiles
+        const int k_chs = (lane >> 3) & 1;                 // K: chunk select within a k-step
+        const int v_tok = 8 * ((lane >> 3) & 1) + (lane & 7);
+        const int v_chs = lane >> 4;
+
+        int k = 0;
+        for (; k < nblk; ++k) {
+            const int st = k % NST;
+            if (!mbar_wait_bounded(&full[st], (k / NST) & 1, kWaitLimitCycles)) {
+                if (lane == 0) {
+                    atomicOr(p.status, PKV_DEV_TIMEOUT);
+                    s_flag[1] = 1;
+                }
+                break;
+            }
+            const uint32_t kb = smem_addr(k_tiles + st * T::kTileBytes);
+            const uint32_t vb = smem_addr(v_tiles + st * T::kTileBytes);
+            const int tbase = (blk0 + k) * BS;
+
+            // S = Q K^T for the BS keys of this block
+            float sc[NT][4];
+#pragma unroll
+            for (int i = 0; i < NT; ++i)
+                sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+#pragma unroll
+                for (int np = 0; np < NT / 2; ++np) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(kb + tile_off<BS>(np * 16 + k_tok, ks * 2 + k_chs), b0, b1, b2, b3);
+                    mma_bf16_16x8x16(sc[2 * np], qf[ks], b0, b1);
+                    mma_bf16_16x8x16(sc[2 * np + 1], qf[ks], b2, b3);
+                }
+            }
+            // scale into base-2 units, mask keys past each row's limit
+            float mxA = -INFINITY, mxB = -INFINITY;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int t = tbase + nt * 8 + q_col;
+                sc[nt][0] = (t < limA) ? sc[nt][0] * p.scale_log2 : -INFINITY;
+                sc[nt][1] = (t + 1 < limA) ? sc[nt][1] * p.scale_log2 : -INFINITY;
+                sc[nt][2] = (t < limB) ? sc[nt][2] * p.scale_log2 : -INFINITY;
+                sc[nt][3] = (t + 1 < limB) ? sc[nt][3] * p.scale_log2 : -INFINITY;
+                mxA = fmaxf(mxA, fmaxf(sc[nt][0], sc[nt][1]));
+                mxB = fmaxf(mxB, fmaxf(sc[nt][2], sc[nt][3]));
+            }
+            mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 1));
+            mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 2));
+            mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 1));
+            mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 2));
+            const float mA_new = fmaxf(mA, mxA), mB_new = fmaxf(mB, mxB);
+            const float baseA = (mA_new == -INFINITY) ? 0.f : mA_new;
+            const float baseB = (mB_new == -INFINITY) ? 0.f : mB_new;
+            const float alphaA = exp2f(mA - baseA), alphaB = exp2f(mB - baseB);
+            mA = mA_new;
+            mB = mB_new;
+
+            // P = 2^(S - m), rounded to bf16; l accumulates the rounded weights
+            uint32_t pp[NT][2];
+            float sumA = 0.f, sumB = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                pp[nt][0] = pack_bf16x2(exp2f(sc[nt][0] - baseA), exp2f(sc[nt][1] - baseA));
+                pp[nt][1] = pack_bf16x2(exp2f(sc[nt][2] - baseB), exp2f(sc[nt][3] - baseB));
+                sumA += bf16_lo_to_f32(pp[nt][0]) + bf16_hi_to_f32(pp[nt][0]);
+                sumB += bf16_lo_to_f32(pp[nt][1]) + bf16_hi_to_f32(pp[nt][1]);
+            }
+            lA = lA * alphaA + sumA;
+            lB = lB * alphaB + sumB;
+#pragma unroll
+            for (int dn = 0; dn < DN; ++dn) {
+                o[dn][0] *= alphaA;
+                o[dn][1] *= alphaA;
+                o[dn][2] *= alphaB;
+                o[dn][3] *= alphaB;
+            }
+
+            // O += P V; keys at or past L may hold anything (even NaN): zero them
+            const bool tail = tbase + BS > L;
+#pragma unroll
+            for (int kk = 0; kk < BS / 16; ++kk) {
+                const uint32_t a[4] = {pp[2 * kk][0], pp[2 * kk][1], pp[2 * kk + 1][0], pp[2 * kk + 1][1]};
+                uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+                if (tail) {
+                    const int t = tbase + kk * 16 + q_col;
+                    mlo = (t < L ? 0x0000ffffu : 0u) | (t + 1 < L ? 0xffff0000u : 0u);
+                    mhi = (t + 8 < L ? 0x0000ffffu : 0u) | (t + 9 < L ? 0xffff0000u : 0u);
+                }
+#pragma unroll
+                for (int dp = 0; dp < DN / 2; ++dp) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_trans(vb + tile_off<BS>(kk * 16 + v_tok, dp * 2 + v_chs), b0, b1, b2, b3);
+                    mma_bf16_16x8x16(o[2 * dp], a, b0 & mlo, b1 & mhi);
+                    mma_bf16_16x8x16(o[2 * dp + 1], a, b2 & mlo, b3 & mhi);
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[st]);
+        }
+        if (warp == 0 && lane == 0)
+            s_flag[3] = k;
+
+        // write this split's partial for the valid rows
+        lA += __shfl_xor_sync(0xffffffffu, lA, 1);
+        lA += __shfl_xor_sync(0xffffffffu, lA, 2);
+        lB += __shfl_xor_sync(0xffffffffu, lB, 1);
+        lB += __shfl_xor_sync(0xffffffffu, lB, 2);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int j = half ? jB : jA;
+            if (j >= M)
+                continue;
+            const int w = j / p.group;
+            const int h = p.q_head_of[g * p.group + (j - w * p.group)];
+            const size_t slot = ((size_t)(row0 + w) * p.num_q_heads + h) * p.n_max + split;
+            if ((lane & 3) == 0)
+                p.part_ml[slot] = make_float2(half ? mB : mA, half ? lB : lA);
+            float2 *dst = reinterpret_cast<float2 *>(p.part_o + slot * D);
+#pragma unroll
+            for (int dn = 0; dn < DN; ++dn)
+                dst[(dn * 8 + q_col) >> 1] = half ? make_float2(o[dn][2], o[dn][3])
+                                                  : make_float2(o[dn][0], o[dn][1]);
+        }
+    }
+
+    // ---------------- hand-off: the last split of (s, g) merges ----------------
+    __threadfence();
+    __syncthreads();
+    if (s_flag[1]) {
+        // a wait expired: drain TMA copies still in flight (bounded) and leave
+        if (threadIdx.x == 0) {
+            const int issued = s_flag[2], consumed = s_flag[3];
+            for (int kk = consumed; kk < issued; ++kk)
+                if (!mbar_wait_bounded(&full[kk % NST], (kk / NST) & 1, kWaitLimitCycles))
+                    break;
+        }
+        return;
+    }
+    const int n_arrive = n_splits > 0 ? n_splits : 1;
+    if (threadIdx.x == 0) {
+        const int old = atomicAdd(p.counters + pair, 1);
+        if (old >= n_arrive)
+            atomicOr(p.status, PKV_DEV_WORKSPACE);
+        s_flag[0] = (old == n_arrive - 1) ? 1 : 0;
+    }
+    __syncthreads();
+    if (!s_flag[0])
+        return;
+    __threadfence();
+
+    constexpr int V4 = D / 4;
+    const int n_items = M * V4;
+    for (int it = threadIdx.x; it < n_items; it += blockDim.x) {
+        const int j = it / V4, c4 = it - j * V4;
+        const int w = j / p.group;
+        const int h = p.q_head_of[g * p.group + (j - w * p.group)];
+        const int r = row0 + w;
+        const int lim = p.causal ? L - W + w + 1 : L;
+        const int nr = lim > 0 ? (lim + C - 1) / C : 0;
+        const size_t base = ((size_t)r * p.num_q_heads + h) * p.n_max;
+        float Mx = -INFINITY;
+        for (int i = 0; i < nr; ++i)
+            Mx = fmaxf(Mx, __ldcg(&p.part_ml[base + i]).x);
+        float sink2 = 0.f;
+        const bool has_sink = p.sinks != nullptr;
+        if (has_sink) {
+            sink2 = __ldg(p.sinks + h) * kLog2e;
+            Mx = fmaxf(Mx, sink2);
+        }
+        float den = 0.f;
+        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = 0; i < nr; ++i) {
+            const float2 ml = __ldcg(&p.part_ml[base + i]);
+            const float wgt = exp2f(ml.x - Mx);
+            den += wgt * ml.y;
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.part_o + (base + i) * D) + c4);
+            num.x += wgt * v.x;
+            num.y += wgt * v.y;
+            num.z += wgt * v.z;
+            num.w += wgt * v.w;
+        }
+        if (has_sink)
+            den += exp2f(sink2 - Mx);
+        float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (den > 0.f) {
+            res.x = num.x / den;
+            res.y = num.y / den;
+            res.z = num.z / den;
+            res.w = num.w / den;
+        }
+        const size_t oidx = ((size_t)r * p.num_q_heads + h) * D + c4 * 4;
+        if (p.out_f32) {
+            *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + oidx) = res;
+        } else {
+            uint2 pk;
+            pk.x = pack_bf16x2(res.x, res.y);
+            pk.y = pack_bf16x2(res.z, res.w);
+            *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.out) + oidx) = pk;
+        }
+    }
+    if (threadIdx.x == 0)
+        p.counters[pair] = 0;
+}
+
+// ---------------------------------------------------------------- host side --
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// 2-D map over a pool seen as rows of head_dim bf16: [num_blocks*H_kv*block_size][head_dim],
+// box = 64 columns (128 B, the swizzle span) x block_size rows.
+int make_pool_map(CUtensorMap *map, void *base, const pkv_pool &pool)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return set_error(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t rows = (cuuint64_t)pool.num_blocks * pool.num_kv_heads * pool.block_size;
+    cuuint64_t dims[2] = {(cuuint64_t)pool.head_dim, rows};
+    cuuint64_t strides[1] = {(cuuint64_t)pool.head_dim * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)pool.block_size};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return set_error(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return PKV_OK;
+}
+
+template <int D, int BS, int NMT>
+constexpr int kStages()
+{
+    return Tile<D, BS>::kTileBytes * 2 >= 16384 ? 3 : 4;
+}
+
+template <int D, int BS, int NMT>
+size_t smem_bytes()
+{
+    constexpr int NST = kStages<D, BS, NMT>();
+    return 1024 + (size_t)NST * 2 * Tile<D, BS>::kTileBytes + 2 * NST * sizeof(uint64_t) + 64;
+}
+
+template <int D, int BS, int NMT>
+int launch_t(const CUtensorMap &mk, const CUtensorMap &mv, const AttnParams &prm, dim3 grid,
+             cudaStream_t st)
+{
+    constexpr int NST = kStages<D, BS, NMT>();
+    auto kern = paged_attention_kernel<D, BS, NMT, NST>;
+    const size_t smem = smem_bytes<D, BS, NMT>();
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    });
+    if (attr_err != cudaSuccess)
+        return check_cuda(attr_err, "cudaFuncSetAttribute(max dynamic smem)");
+    kern<<<grid, (NMT + 1) * 32, smem, st>>>(mk, mv, prm);
+    return check_cuda(cudaGetLastError(), "paged_attention_forward launch");
+}
+
+template <int D, int BS>
+int launch_d_bs(int nmt, const CUtensorMap &mk, const CUtensorMap &mv, const AttnParams &prm,
+                dim3 grid, cudaStream_t st)
+{
+    switch (nmt) {
+    case 1: return launch_t<D, BS, 1>(mk, mv, prm, grid, st);
+    case 2: return launch_t<D, BS, 2>(mk, mv, prm, grid, st);
+    case 4: return launch_t<D, BS, 4>(mk, mv, prm, grid, st);
+    case 8: return launch_t<D, BS, 8>(mk, mv, prm, grid, st);
+    default: return set_error(PKV_ERR_UNSUPPORTED, "internal: m-tile count %d", nmt);
+    }
+}
+
+struct WsLayout {
+    size_t counters, ml, o, total;
+};
+
+WsLayout ws_layout(int32_t num_seqs, int32_t total_q_rows, int32_t num_q_heads, int32_t num_kv_heads,
+                   int32_t head_dim, int32_t max_context_len)
+{
+    const size_t n_max = (size_t)(max_context_len > 0 ? (max_context_len + kSplitTokens - 1) / kSplitTokens : 1);
+    const size_t slots = (size_t)total_q_rows * num_q_heads * n_max;
+    WsLayout w;
+    w.counters = 0;
+    w.ml = round_up((size_t)num_seqs * num_kv_heads * sizeof(int32_t), 256);
+    w.o = w.ml + round_up(slots * sizeof(float2), 256);
+    w.total = w.o + round_up(slots * head_dim * sizeof(float), 256);
+    return w;
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" size_t paged_attention_workspace_size(int32_t num_seqs, int32_t total_q_rows,
+                                                 int32_t num_q_heads, int32_t num_kv_heads,
+                                                 int32_t head_dim, int32_t max_context_len)
+{
+    if (num_seqs < 0 || total_q_rows < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+        return 0;
+    return pkv::ws_layout(num_seqs, total_q_rows, num_q_heads, num_kv_heads, head_dim, max_context_len).total;
+}
+
+extern "C" int paged_attention_workspace_init(void *workspace, size_t workspace_bytes, void *stream)
+{
+    pkv::clear_error();
+    if (!workspace)
+        return pkv::set_error(PKV_ERR_NULL, "paged_attention_workspace_init: workspace is NULL");
+    return pkv::check_cuda(cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream)),
+                           "paged_attention_workspace_init");
+}
+
+extern "C" int paged_attention_forward(const pkv_pool *pool, const void *q, const int32_t *q_starts,
+                                       const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t *context_lens, int32_t num_seqs,
+                                       int32_t total_q_rows, int32_t max_context_len,
+                                       int32_t max_q_rows_per_seq, int32_t num_q_heads,
+                                       const int32_t *kv_head_of_q_head, const float *sinks,
+                                       int32_t causal, float scale, void *out, int32_t out_dtype,
+                                       void *workspace, size_t workspace_bytes, void *stream)
+{
+    using namespace pkv;
+    clear_error();
+    if (!pool)
+        return set_error(PKV_ERR_NULL, "paged_attention_forward: pool is NULL");
+    const int D = pool->head_dim, BS = pool->block_size, Hkv = pool->num_kv_heads;
+    if (num_seqs < 0 || total_q_rows < 0 || max_context_len < 0 || max_q_rows_per_seq < 0)
+        return set_error(PKV_ERR_SHAPE, "paged_attention_forward: negative size");
+    if (pool->num_blocks <= 0 || Hkv <= 0 || max_blocks_per_seq <= 0)
+        return set_error(PKV_ERR_SHAPE, "paged_attention_forward: pool sizes and max_blocks_per_seq must be positive");
+    if (!(D == 64 || D == 128))
+        return set_error(PKV_ERR_UNSUPPORTED, "paged_attention_forward: head_dim %d (built: 64, 128)", D);
+    if (!(BS == 16 || BS == 32))
+        return set_error(PKV_ERR_UNSUPPORTED, "paged_attention_forward: block_size %d (built: 16, 32)", BS);
+    if (num_q_heads <= 0 || num_q_heads > kMaxQHeads || num_q_heads % Hkv != 0)
+        return set_error(PKV_ERR_SHAPE,
+                         "paged_attention_forward: num_q_heads %d must be a positive multiple of "
+                         "num_kv_heads %d and at most %d", num_q_heads, Hkv, kMaxQHeads);
+    if (out_dtype != PKV_DTYPE_BF16 && out_dtype != PKV_DTYPE_F32)
+        return set_error(PKV_ERR_SHAPE, "paged_attention_forward: out_dtype %d", out_dtype);
+    if ((long long)max_blocks_per_seq * BS < max_context_len)
+        return set_error(PKV_ERR_SHAPE,
+                         "paged_attention_forward: max_context_len %d exceeds max_blocks_per_seq * "
+                         "block_size = %lld", max_context_len, (long long)max_blocks_per_seq * BS);
+    if ((long long)pool->num_blocks * Hkv * BS > 0x7fffffffLL)
+        return set_error(PKV_ERR_UNSUPPORTED,
+                         "paged_attention_forward: pool too large for 32-bit TMA row coordinates");
+    const int G = num_q_heads / Hkv;
+    if (num_seqs == 0 || total_q_rows == 0)
+        return PKV_OK;
+    if (max_q_rows_per_seq <= 0)
+        return set_error(PKV_ERR_SHAPE, "paged_attention_forward: max_q_rows_per_seq must be >= 1");
+    if ((long long)G * max_q_rows_per_seq > kMaxGroupRows)
+        return set_error(PKV_ERR_UNSUPPORTED,
+                         "paged_attention_forward: group %d x max rows %d exceeds %d", G,
+                         max_q_rows_per_seq, kMaxGroupRows);
+    if (!pool->k_pool || !pool->v_pool || !q || !q_starts || !block_tables || !context_lens || !out ||
+        !workspace)
+        return set_error(PKV_ERR_NULL, "paged_attention_forward: a required pointer is NULL");
+    if (!aligned16(pool->k_pool) || !aligned16(pool->v_pool) || !aligned16(q) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return set_error(PKV_ERR_ALIGN,
+                         "paged_attention_forward: pools, q and out must be 16-byte aligned, "
+                         "workspace 256-byte aligned");
+    const WsLayout wl = ws_layout(num_seqs, total_q_rows, num_q_heads, Hkv, D, max_context_len);
+    if (workspace_bytes < wl.total)
+        return set_error(PKV_ERR_WORKSPACE, "paged_attention_forward: workspace %zu < %zu bytes",
+                         workspace_bytes, wl.total);
+
+    AttnParams prm;
+    memset(&prm, 0, sizeof prm);
+    // GQA map: q heads of each KV head, in increasing q-head order
+    {
+        int fill[kMaxQHeads] = {0};
+        for (int h = 0; h < num_q_heads; ++h) {
+            const int gg = kv_head_of_q_head ? kv_head_of_q_head[h] : h / G;
+            if (gg < 0 || gg >= Hkv || fill[gg] >= G)
+                return set_error(PKV_ERR_SHAPE,
+                                 "paged_attention_forward: kv_head_of_q_head must give each of the %d "
+                                 "KV heads exactly %d q heads (entry %d = %d)", Hkv, G, h, gg);
+            prm.q_head_of[gg * G + fill[gg]++] = (int16_t)h;
+        }
+    }
+    int32_t *status = device_status_word();
+    if (!status)
+        return set_error(PKV_ERR_CUDA, "paged_attention_forward: no device status word");
+
+    CUtensorMap mk, mv;
+    int rc = make_pool_map(&mk, pool->k_pool, *pool);
+    if (rc)
+        return rc;
+    rc = make_pool_map(&mv, pool->v_pool, *pool);
+    if (rc)
+        return rc;
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const int n_max = max_context_len > 0 ? (max_context_len + kSplitTokens - 1) / kSplitTokens : 1;
+    prm.q = static_cast<const uint16_t *>(q);
+    prm.q_starts = q_starts;
+    prm.block_tables = block_tables;
+    prm.context_lens = context_lens;
+    prm.sinks = sinks;
+    prm.out = out;
+    prm.counters = reinterpret_cast<int32_t *>(ws + wl.counters);
+    prm.part_ml = reinterpret_cast<float2 *>(ws + wl.ml);
+    prm.part_o = reinterpret_cast<float *>(ws + wl.o);
+    prm.status = status;
+    prm.num_seqs = num_seqs;
+    prm.max_blocks_per_seq = max_blocks_per_seq;
+    prm.num_blocks = pool->num_blocks;
+    prm.num_q_heads = num_q_heads;
+    prm.num_kv_heads = Hkv;
+    prm.group = G;
+    prm.n_max = n_max;
+    prm.max_context_len = max_context_len;
+    prm.max_rows = max_q_rows_per_seq;
+    prm.total_rows = total_q_rows;
+    prm.causal = causal ? 1 : 0;
+    prm.out_f32 = out_dtype == PKV_DTYPE_F32;
+    const float sc = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
+    prm.scale_log2 = sc * kLog2e;
+
+    const int rows = G * max_q_rows_per_seq;
+    const int nmt_need = (rows + 15) / 16;
+    const int nmt = nmt_need <= 1 ? 1 : nmt_need <= 2 ? 2 : nmt_need <= 4 ? 4 : 8;
+    const long long gx = (long long)num_seqs * Hkv;
+    if (gx > 0x7fffffffLL || n_max > 65535)
+        return set_error(PKV_ERR_SHAPE, "paged_attention_forward: grid too large");
+    const dim3 grid((unsigned)gx, (unsigned)n_max);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (D == 64 && BS == 16) return launch_d_bs<64, 16>(nmt, mk, mv, prm, grid, st);
+    if (D == 64 && BS == 32) return launch_d_bs<64, 32>(nmt, mk, mv, prm, grid, st);
+    if (D == 128 && BS == 16) return launch_d_bs<128, 16>(nmt, mk, mv, prm, grid, st);
+    return launch_d_bs<128, 32>(nmt, mk, mv, prm, grid, st);
+}

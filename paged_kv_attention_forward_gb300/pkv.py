@@ -1,0 +1,193 @@
+"""ctypes binding of libpkv.so: same entry points as include/pkv.h, torch tensors in.
+
+Argument marshalling only: every step runs in the library's CUDA kernels on the
+current torch CUDA stream.  There is no CPU path; if the library is missing the
+calls raise.  Buffers the library needs (workspaces, outputs) are allocated here
+with torch when the caller does not pass them.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+PKV_OK = 0
+PKV_DTYPE_BF16 = 0
+PKV_DTYPE_F32 = 1
+STATUS_NAMES = {0: "PKV_OK", -1: "PKV_ERR_NULL", -2: "PKV_ERR_SHAPE", -3: "PKV_ERR_UNSUPPORTED",
+                -4: "PKV_ERR_WORKSPACE", -5: "PKV_ERR_BAD_BLOCK", -6: "PKV_ERR_CUDA",
+                -7: "PKV_ERR_ALIGN", -8: "PKV_ERR_TIMEOUT"}
+
+# every exported symbol of include/pkv.h
+EXPORTED = ("pkv_abi_version", "paged_kv_append", "paged_attention_workspace_size",
+            "paged_attention_workspace_init", "paged_attention_forward", "spec_accept_workspace_size",
+            "spec_accept_greedy", "pkv_last_error_string", "pkv_device_status")
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class _Pool(ctypes.Structure):
+    _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+                ("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib(build_if_missing: bool = False):
+    """Load libpkv.so (raises if it is not built; no fallback exists)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if not os.path.exists(path):
+                if not build_if_missing:
+                    raise RuntimeError(f"libpkv.so is not built ({path}); run __graft_entry__.build()")
+                _build.build()
+            L = ctypes.CDLL(path)
+            P, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+            L.pkv_abi_version.argtypes = []
+            L.pkv_abi_version.restype = ctypes.c_int
+            L.paged_kv_append.argtypes = [ctypes.POINTER(_Pool), P, i32, P, P, P, P, i32, i32, P]
+            L.paged_kv_append.restype = ctypes.c_int
+            L.paged_attention_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
+            L.paged_attention_workspace_size.restype = sz
+            L.paged_attention_workspace_init.argtypes = [P, sz, P]
+            L.paged_attention_workspace_init.restype = ctypes.c_int
+            L.paged_attention_forward.argtypes = [ctypes.POINTER(_Pool), P, P, P, i32, P, i32, i32, i32,
+                                                  i32, i32, P, P, i32, ctypes.c_float, P, i32, P, sz, P]
+            L.paged_attention_forward.restype = ctypes.c_int
+            L.spec_accept_workspace_size.argtypes = [i32, i32]
+            L.spec_accept_workspace_size.restype = sz
+            L.spec_accept_greedy.argtypes = [P, i32, P, P, i32, i32, P, P, P, P, sz, P]
+            L.spec_accept_greedy.restype = ctypes.c_int
+            L.pkv_last_error_string.argtypes = []
+            L.pkv_last_error_string.restype = ctypes.c_char_p
+            L.pkv_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int32)]
+            L.pkv_device_status.restype = ctypes.c_int
+            _lib = L
+        return _lib
+
+
+def _check(rc: int):
+    if rc != PKV_OK:
+        raise PkvError(rc, lib().pkv_last_error_string().decode(errors="replace"))
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    assert t.is_cuda and t.is_contiguous(), "expected a contiguous CUDA tensor"
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _pool(k_pool: torch.Tensor, v_pool: torch.Tensor) -> _Pool:
+    assert k_pool.dtype == torch.bfloat16 and v_pool.dtype == torch.bfloat16
+    assert k_pool.shape == v_pool.shape and k_pool.dim() == 4
+    nb, hkv, bs, d = k_pool.shape
+    return _Pool(k_pool.data_ptr(), v_pool.data_ptr(), nb, bs, hkv, d)
+
+
+def paged_kv_append(k_pool, v_pool, block_tables, context_lens_old, new_starts, k_new, v_new,
+                    stream=None) -> None:
+    """Scatter k_new/v_new [R_new, H_kv, D] into the pools (see include/pkv.h)."""
+    pool = _pool(k_pool, v_pool)
+    _check(lib().paged_kv_append(ctypes.byref(pool), _dptr(block_tables), block_tables.shape[1],
+                                 _dptr(context_lens_old), _dptr(new_starts), _dptr(k_new), _dptr(v_new),
+                                 block_tables.shape[0], k_new.shape[0], _stream(stream)))
+
+
+def paged_attention_workspace_size(num_seqs, total_q_rows, num_q_heads, num_kv_heads, head_dim,
+                                   max_context_len) -> int:
+    return int(lib().paged_attention_workspace_size(num_seqs, total_q_rows, num_q_heads, num_kv_heads,
+                                                    head_dim, max_context_len))
+
+
+def new_attention_workspace(num_seqs, total_q_rows, num_q_heads, num_kv_heads, head_dim, max_context_len,
+                            device=None) -> torch.Tensor:
+    """A zeroed workspace of the right size (zero is what the first call needs)."""
+    n = paged_attention_workspace_size(num_seqs, total_q_rows, num_q_heads, num_kv_heads, head_dim,
+                                       max_context_len)
+    return torch.zeros(max(n, 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def paged_attention_forward(k_pool, v_pool, q, q_starts, block_tables, context_lens, *,
+                            max_context_len: int, max_q_rows_per_seq: int,
+                            kv_head_of_q_head=None, sinks=None, causal: bool = False,
+                            scale: float = 0.0, out: Optional[torch.Tensor] = None,
+                            out_dtype=torch.bfloat16, workspace: Optional[torch.Tensor] = None,
+                            stream=None) -> torch.Tensor:
+    """Paged attention (see include/pkv.h).  q: bf16 [R, H_q, D]; returns out [R, H_q, D].
+
+    kv_head_of_q_head is a host sequence of ints (or None); sinks a CUDA float32 [H_q] or None.
+    """
+    pool = _pool(k_pool, v_pool)
+    R, Hq, D = q.shape
+    S = block_tables.shape[0]
+    if out is None:
+        out = torch.empty((R, Hq, D), dtype=out_dtype, device=q.device)
+    dt = PKV_DTYPE_F32 if out.dtype == torch.float32 else PKV_DTYPE_BF16
+    if workspace is None:
+        workspace = new_attention_workspace(S, R, Hq, pool.num_kv_heads, D, max_context_len, q.device)
+    hmap = None
+    if kv_head_of_q_head is not None:
+        arr = (ctypes.c_int32 * Hq)(*[int(x) for x in kv_head_of_q_head])
+        hmap = ctypes.cast(arr, ctypes.c_void_p)
+    _check(lib().paged_attention_forward(
+        ctypes.byref(pool), _dptr(q), _dptr(q_starts), _dptr(block_tables), block_tables.shape[1],
+        _dptr(context_lens), S, R, int(max_context_len), int(max_q_rows_per_seq), Hq, hmap,
+        _dptr(sinks), int(bool(causal)), float(scale), _dptr(out), dt, _dptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def spec_accept_workspace_size(total_rows, vocab) -> int:
+    return int(lib().spec_accept_workspace_size(total_rows, vocab))
+
+
+def spec_accept_greedy(logits, q_starts, draft_tokens, *, argmax_out=None, accept_len=None,
+                       out_tokens=None, workspace=None, stream=None):
+    """Greedy accept (see include/pkv.h); returns (argmax [R], accept_len [S], out_tokens [R])."""
+    R, V = logits.shape
+    S = q_starts.shape[0] - 1
+    dev = logits.device
+    if argmax_out is None:
+        argmax_out = torch.empty(R, dtype=torch.int32, device=dev)
+    if accept_len is None:
+        accept_len = torch.empty(S, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty(R, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(spec_accept_workspace_size(R, V), 256), dtype=torch.uint8, device=dev)
+    _check(lib().spec_accept_greedy(_dptr(logits), V, _dptr(q_starts), _dptr(draft_tokens), S, R,
+                                    _dptr(argmax_out), _dptr(accept_len), _dptr(out_tokens),
+                                    _dptr(workspace), workspace.numel(), _stream(stream)))
+    return argmax_out, accept_len, out_tokens
+
+
+def device_status(stream=None):
+    """Synchronise and read/clear the device status word; returns (status, bits)."""
+    bits = ctypes.c_int32(0)
+    rc = lib().pkv_device_status(_stream(stream), ctypes.byref(bits))
+    return rc, bits.value
