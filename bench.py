@@ -1,0 +1,480 @@
+"""Benchmark: one decode step of the continuous-batching mix through libpkv.so.
+
+A step is the whole hot path on one batch: paged K/V append of every sequence's
+new token, then paged attention of every decode row (and, for verify workloads,
+the greedy accept).  Default workload: 64 sequences, cached lengths log-uniform
+in [128, 32767] plus one appended token, 48 of them sharing a 2900-token prefix
+through the same physical blocks, 40 q / 8 KV heads, head_dim 128, block 16.
+
+Prints ONE JSON line (rank 0).  value = algorithmic bytes of the step / device
+time of the step, in GB/s; algorithmic bytes count every distinct K/V token a
+step must read once (shared prefix blocks once), plus q, out, the block-table
+entries read, and the append's reads and writes.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--no-cpu-baseline]
+
+--impl reference times the float64 CPU oracle (the checker) on the host cores on
+a bounded sample of the same workload; it is a reported baseline, not a target.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from paged_kv_attention_forward_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "paged-attention decode: achieved HBM GB/s (frac of GB300 peak), query-rows/s"
+PROFILES = os.path.join(ROOT, "profiles")
+
+
+# ---------------------------------------------------------------- accounting --
+def algorithmic_bytes(b: wl.PagedBatch, layers: int = 1) -> dict:
+    """Bytes one step must move at least, per the workload's structure."""
+    B, H, D = b.block_size, b.num_kv_heads, b.head_dim
+    shared = set(b.shared_block_ids.tolist())
+    shared_tokens_read = 0
+    if len(b.sharing_seqs):
+        shared_tokens_read = len(shared) * B            # read once, not once per sharing sequence
+    private_tokens = 0
+    for s in range(b.num_seqs):
+        L = int(b.context_lens[s])
+        n_sh = len(shared) if s in set(b.sharing_seqs.tolist()) else 0
+        private_tokens += L - n_sh * B
+    kv = (private_tokens + shared_tokens_read) * H * D * 2 * 2
+    logical_kv = int(b.context_lens.sum()) * H * D * 2 * 2
+    R = b.total_q_rows
+    q_out = 2 * R * b.num_q_heads * D * 2
+    table = int(sum((int(L) + B - 1) // B for L in b.context_lens)) * 4 + (b.num_seqs * 2 + 1) * 4
+    r_new = int(b.new_starts[-1])
+    append = r_new * H * D * 2 * 2 * 2                  # read k_new/v_new, write the pool slots
+    attn = kv + q_out + table
+    accept = 0
+    if b.logits is not None:
+        accept = b.logits.size * 4 + R * 4 * 3
+    return dict(attention=attn * layers, append=append * layers, accept=accept,
+                step=(attn + append) * layers + accept, kv_unique=kv * layers,
+                kv_logical=logical_kv * layers, rows=R)
+
+
+def measured_peaks() -> dict:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            return json.load(fh)
+    except (OSError, ValueError):
+        return {}
+
+
+def stored_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes from a committed ncu summary, if it matches the current sources."""
+    from paged_kv_attention_forward_gb300 import build
+    path = os.path.join(PROFILES, f"{kernel}_{workload}.txt")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    vals = {}
+    for ln in lines:
+        if ":" in ln and not ln.startswith("#"):
+            k, _, v = ln.partition(":")
+            vals[k.strip()] = v.strip()
+    if vals.get("source_digest") != build.source_digest():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# -------------------------------------------------------------------- clocks --
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[4:8]):
+                if flag.lower() in ("active", "1"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm --
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from paged_kv_attention_forward_gb300 import pkv
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    layers = 40 if args.workload == "ministral_decode" else 1
+    b = wl.make_workload(args.workload, seed=args.seed + rank, layers=layers, num_seqs=args.num_seqs)
+    acct = algorithmic_bytes(b, layers)
+
+    def d_bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    def d(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    pools = [(d_bf16(b.k_pool[i]), d_bf16(b.v_pool[i])) for i in range(layers)]
+    tables, lens_old, lens = d(b.block_tables), d(b.context_lens_old), d(b.context_lens)
+    new_starts, q_starts = d(b.new_starts), d(b.q_starts)
+    k_new = [d_bf16(b.k_new[i]) for i in range(layers)]
+    v_new = [d_bf16(b.v_new[i]) for i in range(layers)]
+    qs = [d_bf16(b.q[i]) for i in range(layers)]
+    sinks = None if b.sinks is None else d(b.sinks)
+    outs = [torch.empty_like(q) for q in qs]
+    ws = pkv.new_attention_workspace(b.num_seqs, b.total_q_rows, b.num_q_heads, b.num_kv_heads,
+                                     b.head_dim, b.max_context_len, dev)
+    logits = drafts = acc_ws = None
+    acc_out = None
+    if b.logits is not None:
+        logits, drafts = d(b.logits), d(b.draft_tokens)
+        acc_ws = torch.empty(pkv.spec_accept_workspace_size(b.total_q_rows, b.logits.shape[1]),
+                             dtype=torch.uint8, device=dev)
+        acc_out = (torch.empty(b.total_q_rows, dtype=torch.int32, device=dev),
+                   torch.empty(b.num_seqs, dtype=torch.int32, device=dev),
+                   torch.empty(b.total_q_rows, dtype=torch.int32, device=dev))
+    has_append = int(b.new_starts[-1]) > 0
+    max_ctx, max_rows = b.max_context_len, b.max_q_rows_per_seq
+    stream = torch.cuda.current_stream()
+    launches_per_step = layers * (int(has_append) + 1) + (2 if logits is not None else 0)
+
+    def step(ev_pairs=None, li=None):
+        for i in range(layers):
+            if has_append:
+                pkv.paged_kv_append(pools[i][0], pools[i][1], tables, lens_old, new_starts, k_new[i], v_new[i],
+                                    stream=stream)
+            if ev_pairs is not None:
+                ev_pairs[li][0].record(stream)
+            pkv.paged_attention_forward(pools[i][0], pools[i][1], qs[i], q_starts, tables, lens,
+                                        max_context_len=max_ctx, max_q_rows_per_seq=max_rows, sinks=sinks,
+                                        causal=b.causal, out=outs[i], workspace=ws, stream=stream)
+            if ev_pairs is not None:
+                ev_pairs[li][1].record(stream)
+                li += 1
+        if logits is not None:
+            pkv.spec_accept_greedy(logits, q_starts, drafts, argmax_out=acc_out[0], accept_len=acc_out[1],
+                                   out_tokens=acc_out[2], workspace=acc_ws, stream=stream)
+        return li
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step()
+    rc, bits = pkv.device_status()
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} bits {bits:#x} after warm-up")
+
+    # ---- device-resident timed region ----
+    n_ev = args.steps * layers
+    ev_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    barrier()
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    wall0 = time.perf_counter()
+    t0.record(stream)
+    li = 0
+    for _ in range(args.steps):
+        li = step(ev_pairs, li)
+    t1.record(stream)
+    barrier()
+    wall1 = time.perf_counter()
+    clock_info = clocks.stop() if clocks else None
+    ms_total = t0.elapsed_time(t1)
+    attn_ms = [a.elapsed_time(z) for a, z in ev_pairs]
+    rc, bits = pkv.device_status()
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} bits {bits:#x} after timed steps")
+
+    # ---- end to end through the public API with host buffers ----
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    pin16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).pin_memory()  # noqa: E731
+    h_inputs = [pin(b.block_tables), pin(b.context_lens_old), pin(b.context_lens), pin(b.new_starts),
+                pin(b.q_starts)]
+    d_inputs = [tables, lens_old, lens, new_starts, q_starts]
+    h_q = [pin16(b.q[i]) for i in range(layers)]
+    h_kn = [pin16(b.k_new[i]) for i in range(layers)]
+    h_vn = [pin16(b.v_new[i]) for i in range(layers)]
+    h_out = [torch.empty(o.shape, dtype=torch.int16).pin_memory() for o in outs]
+    h2d = sum(t.numel() * t.element_size() for t in h_inputs + h_q + h_kn + h_vn)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    h_logits = h_drafts = h_acc = None
+    if logits is not None:
+        h_logits, h_drafts = pin(b.logits), pin(b.draft_tokens)
+        h_acc = [torch.empty(t.shape, dtype=torch.int32).pin_memory() for t in acc_out]
+        h2d += h_logits.numel() * 4 + h_drafts.numel() * 4
+        d2h += sum(t.numel() * 4 for t in h_acc)
+
+    def e2e_step():
+        for hsrc, ddst in zip(h_inputs, d_inputs):
+            ddst.copy_(hsrc, non_blocking=True)
+        for i in range(layers):
+            qs[i].view(torch.int16).copy_(h_q[i], non_blocking=True)
+            k_new[i].view(torch.int16).copy_(h_kn[i], non_blocking=True)
+            v_new[i].view(torch.int16).copy_(h_vn[i], non_blocking=True)
+        if logits is not None:
+            logits.copy_(h_logits, non_blocking=True)
+            drafts.copy_(h_drafts, non_blocking=True)
+        step()
+        for i in range(layers):
+            h_out[i].copy_(outs[i].view(torch.int16), non_blocking=True)
+        if logits is not None:
+            for hd, dd in zip(h_acc, acc_out):
+                hd.copy_(dd, non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    for _ in range(max(3, args.warmup // 4)):
+        e2e_step()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+
+    # ---- max over ranks ----
+    ms_per_step = ms_total / args.steps
+    e2e_ms_per_step = e2e_ms / e2e_steps
+    attn_avg_ms = statistics.fmean(attn_ms)
+    if dist is not None:
+        t = torch.tensor([ms_per_step, e2e_ms_per_step, attn_avg_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_per_step, e2e_ms_per_step, attn_avg_ms = t.tolist()
+    if rank != 0:
+        return None
+
+    peaks = measured_peaks()
+    peak = peaks.get("hbm_gbs")
+    peak_kind = "measured"
+    if peak is None:
+        peak, peak_kind = 6800.0, "fallback"
+    per_launch_bytes = acct["attention"] / layers
+    achieved = per_launch_bytes / (attn_avg_ms * 1e-3) / 1e9
+    traffic = stored_traffic("paged_attention", args.workload)
+    value = world * acct["step"] / (ms_per_step * 1e-3) / 1e9
+    e2e_value = world * acct["step"] / (e2e_ms_per_step * 1e-3) / 1e9
+    rows_per_s = world * acct["rows"] * layers / (ms_per_step * 1e-3)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_description(b, layers), "global_batch": b.num_seqs * world,
+                   "seq_len": b.max_context_len, "parallelism": f"dp{world} (independent replicas)",
+                   "l2": "inputs larger than L2 (K/V read per step >> 129 MB); no flush",
+                   "seed": args.seed},
+        "query_rows_per_s": round(rows_per_s, 1),
+        "frac_of_measured_hbm": round(value / peak, 4),
+        "frac_of_nominal_8tbs": round(value / 8000.0, 4),
+        "bytes_per_step": acct["step"], "kv_unique_bytes_per_step": acct["kv_unique"],
+        "kv_logical_bytes_per_step": acct["kv_logical"],
+        "roofline": {"kernel": "paged_attention_kernel", "bound": "hbm", "achieved": round(achieved, 2),
+                     "peak": peak, "peak_kind": f"{peak_kind} (hbm_gbs, copy kernel)", "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "bytes_per_launch": per_launch_bytes,
+                     "avg_launch_ms": round(attn_avg_ms, 5), "launches_timed": len(attn_ms),
+                     "traffic": traffic},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms_per_step, 5),
+                "steps": e2e_steps},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clock_info,
+        "wall_s_timed_region": round(wall1 - wall0, 3),
+    }
+    return line
+
+
+def workload_description(b, layers):
+    return (f"{b.name}: {b.num_seqs} seqs, context {int(b.context_lens.min())}-{int(b.context_lens.max())} "
+            f"(sum {int(b.context_lens.sum())}), {b.num_q_heads} q / {b.num_kv_heads} kv heads, "
+            f"head_dim {b.head_dim}, block {b.block_size}, rows {b.total_q_rows}, "
+            f"appended {int(b.new_starts[-1])}, shared prefix blocks {len(b.shared_block_ids)} "
+            f"x {len(b.sharing_seqs)} seqs, layers {layers}, causal {int(b.causal)}, "
+            f"sinks {int(b.sinks is not None)}")
+
+
+# ------------------------------------------------------------ oracle timing --
+def time_oracle_step(sub: wl.PagedBatch, threads: int):
+    import oracle
+    k, v = sub.k_pool[0].copy(), sub.v_pool[0].copy()
+    t = time.perf_counter()
+    if int(sub.new_starts[-1]) > 0:
+        oracle.paged_kv_append(k, v, sub.block_tables, sub.context_lens_old, sub.new_starts,
+                               sub.k_new[0], sub.v_new[0])
+    oracle.paged_attention(k, v, sub.q[0], sub.q_starts, sub.block_tables, sub.context_lens, sinks=sub.sinks,
+                           causal=sub.causal, num_threads=threads)
+    if sub.logits is not None:
+        oracle.spec_accept_greedy(sub.logits, sub.q_starts, sub.draft_tokens)
+    return time.perf_counter() - t
+
+
+def cpu_baseline(b: wl.PagedBatch, budget_s: float = 10.0, max_runs: int = 10):
+    """The oracle, as it stands, on the whole batch, repeated for about budget_s seconds."""
+    import oracle
+    oracle.build_oracle()
+    threads = len(os.sched_getaffinity(0))
+    acct = algorithmic_bytes(b)
+    times = []
+    t_start = time.perf_counter()
+    while len(times) < max_runs and (len(times) < 3 or time.perf_counter() - t_start < budget_s):
+        times.append(time_oracle_step(b, threads))
+    med = statistics.median(times)
+    return {"value": round(acct["step"] / med / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": (f"the whole batch ({b.num_seqs} seqs, {int(b.context_lens.sum())} cached tokens): "
+                       f"append + attention{' + accept' if b.logits is not None else ''} in float64, "
+                       f"median of {len(times)} runs ({med:.2f} s each, {sum(times):.1f} s in all)")}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the float64 oracle on the host cores, rank 0 only."""
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build_oracle()
+    layers = 1
+    b = wl.make_workload(args.workload, seed=args.seed, layers=layers, num_seqs=args.num_seqs)
+    threads = len(os.sched_getaffinity(0))
+    # size the per-step sample so that warm-up + timed steps take about 90 s in all
+    order = np.random.default_rng(12345).permutation(b.num_seqs)
+    cal = wl.select_seqs(b, order[:1])
+    t_cal = max(time_oracle_step(cal, threads), 1e-4)
+    tok_per_s = int(cal.context_lens.sum()) / t_cal
+    budget_tokens = tok_per_s * 90.0 / (args.steps + args.warmup)
+    chosen, tokens = [], 0
+    for s in order:
+        if chosen and tokens + int(b.context_lens[s]) > budget_tokens:
+            continue
+        chosen.append(int(s))
+        tokens += int(b.context_lens[s])
+    sub = wl.select_seqs(b, sorted(chosen))
+    acct = algorithmic_bytes(sub)
+    for _ in range(args.warmup):
+        time_oracle_step(sub, threads)
+    times = [time_oracle_step(sub, threads) for _ in range(args.steps)]
+    total = sum(times)
+    value = acct["step"] * args.steps / total / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": workload_description(b, layers), "global_batch": b.num_seqs,
+                   "seq_len": b.max_context_len, "parallelism": "host cores", "seed": args.seed},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{sub.num_seqs} of the batch's sequences ({int(sub.context_lens.sum())} "
+                                   f"cached tokens) per step, chosen in a fixed random order to fit "
+                                   f"about 90 s for all steps; append + attention in float64"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=wl.WORKLOADS, default="cb_mix")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=500)
+    ap.add_argument("--num-seqs", type=int, default=None,
+                    help="resize the batch (same per-sequence distribution); for profiling smaller cases")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    line = run_ours(args, rank, world, local_rank)
+    if line is not None:
+        if not args.no_cpu_baseline and world == 1:
+            b = wl.make_workload(args.workload, seed=args.seed, layers=1, num_seqs=args.num_seqs)
+            line["cpu_baseline"] = cpu_baseline(b)
+        else:
+            line["cpu_baseline"] = None
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

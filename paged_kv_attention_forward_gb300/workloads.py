@@ -311,8 +311,13 @@ WORKLOADS = ("tiny_decode", "ministral_decode", "cb_mix", "spec_verify", "sinks_
 VOCAB = 151936
 
 
-def make_workload(name: str, seed: int = 0, filler: str = "random", layers: Optional[int] = None) -> PagedBatch:
-    """Build one of the named workloads (see the module docstring)."""
+def make_workload(name: str, seed: int = 0, filler: str = "random", layers: Optional[int] = None,
+                  num_seqs: Optional[int] = None) -> PagedBatch:
+    """Build one of the named workloads (see the module docstring).
+
+    num_seqs shrinks or grows the batch of cb_mix / spec_verify / sinks_scale with the
+    same per-sequence distributions (cb_mix keeps three quarters of it sharing the
+    prefix); used to profile a smaller case of the same kernels."""
     base = np.random.SeedSequence([seed, WORKLOADS.index(name)])
     s_shape, s_batch, s_extra = base.spawn(3)
     rng = np.random.Generator(np.random.PCG64(s_shape))
@@ -328,7 +333,8 @@ def make_workload(name: str, seed: int = 0, filler: str = "random", layers: Opti
                            head_dim=128, block_size=16, causal=False, filler=filler,
                            layers=40 if layers is None else layers)
     if name == "cb_mix":
-        S, n_share, prefix = 64, 48, 2900
+        S = num_seqs or 64
+        n_share, prefix = (3 * S) // 4, 2900
         sharing = np.zeros(S, dtype=bool)
         sharing[rng.permutation(S)[:n_share]] = True
         old = np.where(sharing, _loguniform_int(rng, prefix + 1, 32767, S),
@@ -338,14 +344,14 @@ def make_workload(name: str, seed: int = 0, filler: str = "random", layers: Opti
                            head_dim=128, block_size=16, causal=False, filler=filler,
                            shared_prefix=prefix, sharing=sharing)
     if name == "spec_verify":
-        S = 16
+        S = num_seqs or 16
         lens = rng.integers(4096, 32769, size=S)
         w = rng.integers(1, 17, size=S)
         b = build_batch(s_batch, name=name, lens=lens, n_new=w, q_rows=w, num_q_heads=32,
                         num_kv_heads=8, head_dim=128, block_size=16, causal=True, filler=filler)
         return add_verify_logits(b, s_extra, VOCAB)
     if name == "sinks_scale":
-        S = 128
+        S = num_seqs or 128
         return build_batch(s_batch, name=name, lens=np.full(S, 8192), n_new=np.zeros(S, np.int64),
                            q_rows=np.ones(S, np.int64), num_q_heads=64, num_kv_heads=8,
                            head_dim=64, block_size=32, causal=False, with_sinks=True, filler=filler)
