@@ -214,6 +214,37 @@ int spec_accept_greedy(const float *logits, int32_t vocab,
                        int32_t *argmax_out, int32_t *accept_len, int32_t *out_tokens,
                        void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * Allocation-free paged attention: the same computation and arguments as
+ * paged_attention_forward, minus the workspace, for callers that cannot
+ * allocate device memory (a stream being captured into a CUDA graph that must
+ * not allocate, runtimes that own all device memory through their own arena,
+ * plug-in hosts whose allocator this library cannot reach).  The pages have no
+ * counterpart of this entry point; it exists for those callers only.
+ *
+ * The workspace lives in a fixed device array of PKV_NOALLOC_SCRATCH_BYTES
+ * inside the library, which every GPU that loads the library holds until the
+ * process exits.  Sizes whose paged_attention_workspace_size exceeds it are
+ * rejected with PKV_ERR_WORKSPACE before anything is launched.  The first call
+ * on a device looks the array's device address up (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.  Each
+ * call clears the array's counter region (cudaMemsetAsync on `stream`) and then
+ * launches the attention kernel; it calls no allocator.  All calls on a device
+ * share the one array, which keeps the last call's contents: calls that may
+ * overlap on the GPU (different streams without ordering) race and corrupt
+ * each other's results.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (32u << 20)
+int paged_attention_forward_noalloc(const pkv_pool *pool,
+                                    const void *q, const int32_t *q_starts,
+                                    const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                    const int32_t *context_lens,
+                                    int32_t num_seqs, int32_t total_q_rows,
+                                    int32_t max_context_len, int32_t max_q_rows_per_seq,
+                                    int32_t num_q_heads, const int32_t *kv_head_of_q_head,
+                                    const float *sinks, int32_t causal, float scale,
+                                    void *out, int32_t out_dtype, void *stream);
+
 /* Text of the calling thread's last error ("" if none). */
 const char *pkv_last_error_string(void);
 

@@ -677,3 +677,89 @@ extern "C" int paged_attention_forward(const pkv_pool *pool, const void *q, cons
     if (D == 128 && BS == 16) return launch_d_bs<128, 16>(nmt, mk, mv, prm, grid, st);
     return launch_d_bs<128, 32>(nmt, mk, mv, prm, grid, st);
 }
+
+// ------------------------------------------------ allocation-free variant --
+// Some callers cannot call cudaMalloc: code that runs inside a CUDA-graph
+// capture that must not allocate, inference runtimes that hand out all device
+// memory up front from their own arena, and plug-in hosts whose allocator is
+// not reachable from this library.  For them paged_attention_forward_noalloc
+// runs the same kernel with its workspace in this fixed device array instead of
+// a caller-provided buffer.  The array is part of the loaded module, so every
+// GPU that loads the library holds PKV_NOALLOC_SCRATCH_BYTES of it until the
+// process exits.
+static __device__ __align__(256) uint8_t g_pkv_noalloc_scratch[PKV_NOALLOC_SCRATCH_BYTES];
+
+namespace pkv {
+namespace {
+std::mutex g_noalloc_mutex;
+uint8_t *g_noalloc_ptr[64] = {nullptr};
+
+// Device address of the scratch array on the current device.  Looked up once per
+// device, with that device current: in host code the array's name is only a
+// host-side stand-in, never a device address.
+int noalloc_scratch(uint8_t **ptr)
+{
+    int dev = -1;
+    int rc = check_cuda(cudaGetDevice(&dev), "cudaGetDevice");
+    if (rc)
+        return rc;
+    if (dev < 0 || dev >= 64)
+        return set_error(PKV_ERR_CUDA, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        rc = check_cuda(cudaGetSymbolAddress(&p, g_pkv_noalloc_scratch),
+                        "cudaGetSymbolAddress of the allocation-free scratch");
+        if (rc)
+            return rc;
+        g_noalloc_ptr[dev] = static_cast<uint8_t *>(p);
+    }
+    *ptr = g_noalloc_ptr[dev];
+    return PKV_OK;
+}
+}  // namespace
+}  // namespace pkv
+
+extern "C" int paged_attention_forward_noalloc(const pkv_pool *pool, const void *q, const int32_t *q_starts,
+                                               const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                               const int32_t *context_lens, int32_t num_seqs,
+                                               int32_t total_q_rows, int32_t max_context_len,
+                                               int32_t max_q_rows_per_seq, int32_t num_q_heads,
+                                               const int32_t *kv_head_of_q_head, const float *sinks,
+                                               int32_t causal, float scale, void *out, int32_t out_dtype,
+                                               void *stream)
+{
+    using namespace pkv;
+    clear_error();
+    if (!pool)
+        return set_error(PKV_ERR_NULL, "paged_attention_forward_noalloc: pool is NULL");
+    if (num_seqs == 0 || total_q_rows == 0)
+        return paged_attention_forward(pool, q, q_starts, block_tables, max_blocks_per_seq, context_lens,
+                                       num_seqs, total_q_rows, max_context_len, max_q_rows_per_seq,
+                                       num_q_heads, kv_head_of_q_head, sinks, causal, scale, out, out_dtype,
+                                       nullptr, 0, stream);
+    const size_t need = paged_attention_workspace_size(num_seqs, total_q_rows, num_q_heads, pool->num_kv_heads,
+                                                       pool->head_dim, max_context_len);
+    if (need == 0)
+        return set_error(PKV_ERR_SHAPE, "paged_attention_forward_noalloc: invalid sizes");
+    if (need > (size_t)PKV_NOALLOC_SCRATCH_BYTES)
+        return set_error(PKV_ERR_WORKSPACE,
+                         "paged_attention_forward_noalloc: these sizes need %zu bytes of scratch but the "
+                         "built-in scratch holds %zu; use paged_attention_forward with a caller workspace",
+                         need, (size_t)PKV_NOALLOC_SCRATCH_BYTES);
+    uint8_t *scratch = nullptr;
+    int rc = noalloc_scratch(&scratch);
+    if (rc)
+        return rc;
+    // The merge counters at the start of the workspace must be zero on entry; the
+    // array keeps whatever the previous call left, so clear them on every call.
+    const size_t counter_bytes = round_up((size_t)num_seqs * pool->num_kv_heads * sizeof(int32_t), 256);
+    rc = check_cuda(cudaMemsetAsync(scratch, 0, counter_bytes, static_cast<cudaStream_t>(stream)),
+                    "clear allocation-free scratch counters");
+    if (rc)
+        return rc;
+    return paged_attention_forward(pool, q, q_starts, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                                   total_q_rows, max_context_len, max_q_rows_per_seq, num_q_heads,
+                                   kv_head_of_q_head, sinks, causal, scale, out, out_dtype, scratch,
+                                   (size_t)PKV_NOALLOC_SCRATCH_BYTES, stream);
+}

@@ -26,7 +26,8 @@ STATUS_NAMES = {0: "PKV_OK", -1: "PKV_ERR_NULL", -2: "PKV_ERR_SHAPE", -3: "PKV_E
 # every exported symbol of include/pkv.h
 EXPORTED = ("pkv_abi_version", "paged_kv_append", "paged_attention_workspace_size",
             "paged_attention_workspace_init", "paged_attention_forward", "spec_accept_workspace_size",
-            "spec_accept_greedy", "pkv_last_error_string", "pkv_device_status")
+            "spec_accept_greedy", "pkv_last_error_string", "pkv_device_status",
+            "paged_attention_forward_noalloc")
 
 
 class PkvError(RuntimeError):
@@ -72,6 +73,9 @@ def lib(build_if_missing: bool = False):
             L.paged_attention_forward.argtypes = [ctypes.POINTER(_Pool), P, P, P, i32, P, i32, i32, i32,
                                                   i32, i32, P, P, i32, ctypes.c_float, P, i32, P, sz, P]
             L.paged_attention_forward.restype = ctypes.c_int
+            L.paged_attention_forward_noalloc.argtypes = [ctypes.POINTER(_Pool), P, P, P, i32, P, i32, i32,
+                                                          i32, i32, i32, P, P, i32, ctypes.c_float, P, i32, P]
+            L.paged_attention_forward_noalloc.restype = ctypes.c_int
             L.spec_accept_workspace_size.argtypes = [i32, i32]
             L.spec_accept_workspace_size.restype = sz
             L.spec_accept_greedy.argtypes = [P, i32, P, P, i32, i32, P, P, P, P, sz, P]
