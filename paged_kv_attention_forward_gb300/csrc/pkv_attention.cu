@@ -18,11 +18,14 @@
 //    tile loads (cp.async.bulk.tensor, 128-byte swizzle) of each K and V block
 //    of the split into an NST-stage shared-memory ring, completion tracked by
 //    mbarriers.
-//  * NMT consumer warps, one per 16 query rows of the (s, g) pair: the G q heads
-//    of KV head g times the W rows of s, flattened row = w * G + head_in_group.
-//    Per KV block: S = Q K^T with mma.sync m16n8k16 (bf16 in, fp32 out), scale,
-//    causal / length mask, online softmax in base 2 (running max m, running sum
-//    l of the bf16-rounded weights), O += P V with mma.sync (P rounded to bf16).
+//  * NMT consumer warps, each owning 8 * NN query rows of the (s, g) pair: the G q
+//    heads of KV head g times the W rows of s, flattened row = w * G + head_in_group.
+//    Per KV block, on mma.sync m16n8k16 (bf16 in, fp32 out) with keys / head dims
+//    on the M side and query rows on the N side (decode has at most 8 rows per KV
+//    head, so nothing is padded to 16 rows): S^T = K q^T, scale, causal / length
+//    mask, online softmax in base 2 (running max m, running sum l of the
+//    bf16-rounded weights), P^T transposed in registers (movmatrix) and
+//    O^T += V^T P^T.
 //    Keys past a row's limit get weight exactly 0, so a verify-window row and the
 //    same row decoded alone go through identical operations.
 //  * Partials (m, l, O) of every split go to the workspace.  The last CTA of an
@@ -81,16 +84,20 @@ __device__ __forceinline__ uint32_t tile_off(int tok, int ch)
     return (uint32_t)((ch >> 3) * (BS * 128) + tok * 128 + (((ch & 7) ^ (tok & 7)) << 4));
 }
 
-template <int D, int BS, int NMT, int NST>
+// NN: n-tiles of 8 query rows per consumer warp; NMT: consumer warps.  A CTA serves
+// up to 8 * NN * NMT rows (the G q heads of one KV head times the sequence's rows).
+template <int D, int BS, int NN, int NMT, int NST>
 __global__ void __launch_bounds__((NMT + 1) * 32)
 paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const AttnParams p)
 {
     using T = Tile<D, BS>;
-    constexpr int NT = BS / 8;    // score n-tiles (8 keys each) per block
-    constexpr int KS = D / 16;    // k-steps of QK^T
-    constexpr int DN = D / 8;     // output n-tiles (8 dims each)
+    constexpr int MT = BS / 16;   // 16-key m-tiles per block
+    constexpr int KS = D / 16;    // k-steps of K q^T
+    constexpr int DM = D / 16;    // 16-dim m-tiles of V^T P^T
     constexpr int C = kSplitTokens;
+    constexpr int RPW = 8 * NN;   // rows per consumer warp
+    static_assert(C / BS <= 32, "one warp holds a split's block ids");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -100,7 +107,7 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
     uint64_t *full = reinterpret_cast<uint64_t *>(v_tiles + NST * T::kTileBytes);
     uint64_t *empty = full + NST;
     volatile int32_t *s_flag = reinterpret_cast<volatile int32_t *>(empty + NST);
-    // s_flag[0]: this CTA merges; [1]: abort; [2]: blocks issued; [3]: blocks consumed
+    // s_flag[0]: this CTA merges; [1]: abort; [2]: blocks issued
 
     const int pair = blockIdx.x;
     const int s = pair / p.num_kv_heads;
@@ -117,6 +124,8 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
         L = L < 0 ? 0 : L_cap;
     }
     const int n_splits = (L + C - 1) / C;
+    if (split >= n_splits && !(n_splits == 0 && split == 0))
+        return;   // an empty context still owns split 0 (it writes the zero / sink output)
     const int row0 = __ldg(p.q_starts + s);
     int W = __ldg(p.q_starts + s + 1) - row0;
     if (W <= 0)
@@ -131,11 +140,8 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
             atomicOr(p.status, PKV_DEV_TOO_MANY_ROWS);
         W = p.max_rows;
     }
-    const int M = p.group * W;         // query rows of this (s, g)
-    const int n_mt = (M + 15) >> 4;    // consumer warps with work
-    if (split >= n_splits && !(n_splits == 0 && split == 0))
-        return;
-    // n_splits == 0 (empty context): split 0 still runs to write the (zero / sink) output.
+    const int M = p.group * W;               // query rows of this (s, g)
+    const int n_act = (M + RPW - 1) / RPW;   // consumer warps with rows
 
     const int t0 = split * C;
     const int t1 = min(t0 + C, L);
@@ -145,91 +151,104 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
     if (threadIdx.x == 0) {
         for (int i = 0; i < NST; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], n_mt);
+            mbar_init(&empty[i], n_act);
         }
         mbar_fence_init();
         s_flag[0] = 0;
         s_flag[1] = 0;
         s_flag[2] = 0;
-        s_flag[3] = 0;
     }
     __syncthreads();
 
     if (warp == NMT) {
-        // ---------------- producer: block table -> TMA ----------------
+        // ---------------- producer warp: block table -> TMA ring ----------------
+        int my_blk = 0;   // lane j holds the id of the split's j-th block
+        if (lane < nblk) {
+            my_blk = __ldg(p.block_tables + (size_t)s * p.max_blocks_per_seq + blk0 + lane);
+            if (my_blk < 0 || my_blk >= p.num_blocks) {
+                atomicOr(p.status, PKV_DEV_BAD_BLOCK);
+                my_blk = 0;
+            }
+        }
         if (lane == 0) {
             prefetch_tensormap(&tm_k);
             prefetch_tensormap(&tm_v);
-            const int32_t *table = p.block_tables + (size_t)s * p.max_blocks_per_seq + blk0;
-            int k = 0;
-            for (; k < nblk; ++k) {
+        }
+        int k = 0;
+        for (; k < nblk; ++k) {
+            const int blk = __shfl_sync(0xffffffffu, my_blk, k);
+            bool stop = false;
+            if (lane == 0) {
                 const int st = k % NST;
-                if (k >= NST) {
-                    if (!mbar_wait_bounded(&empty[st], ((k / NST) + 1) & 1, kWaitLimitCycles)) {
-                        atomicOr(p.status, PKV_DEV_TIMEOUT);
-                        s_flag[1] = 1;
-                        break;
+                bool ok = true;
+                if (k >= NST)
+                    ok = mbar_wait_bounded(&empty[st], ((k / NST) + 1) & 1, kWaitLimitCycles);
+                if (!ok)
+                    atomicOr(p.status, PKV_DEV_TIMEOUT);
+                if (!ok || s_flag[1]) {
+                    s_flag[1] = 1;
+                    stop = true;
+                } else {
+                    const int y = (blk * p.num_kv_heads + g) * BS;
+                    mbar_arrive_expect_tx(&full[st], 2 * T::kTileBytes);
+#pragma unroll
+                    for (int h = 0; h < T::kHalves; ++h) {
+                        tma_load_2d(k_tiles + st * T::kTileBytes + h * T::kBoxBytes, &tm_k, &full[st], h * 64, y);
+                        tma_load_2d(v_tiles + st * T::kTileBytes + h * T::kBoxBytes, &tm_v, &full[st], h * 64, y);
                     }
                 }
-                if (s_flag[1])
-                    break;
-                int blk = __ldg(table + k);
-                if (blk < 0 || blk >= p.num_blocks) {
-                    atomicOr(p.status, PKV_DEV_BAD_BLOCK);
-                    blk = 0;
-                }
-                const int y = (blk * p.num_kv_heads + g) * BS;
-                mbar_arrive_expect_tx(&full[st], 2 * T::kTileBytes);
-#pragma unroll
-                for (int h = 0; h < T::kHalves; ++h) {
-                    tma_load_2d(k_tiles + st * T::kTileBytes + h * T::kBoxBytes, &tm_k, &full[st], h * 64, y);
-                    tma_load_2d(v_tiles + st * T::kTileBytes + h * T::kBoxBytes, &tm_v, &full[st], h * 64, y);
-                }
             }
-            s_flag[2] = k;
+            if (__shfl_sync(0xffffffffu, stop, 0))
+                break;
         }
-    } else if (warp < n_mt) {
-        // ---------------- consumers ----------------
-        const int g_row = lane >> 2;          // row within the 16-row m-tile (and +8)
-        const int q_col = (lane & 3) * 2;     // column pair within an 8/16-wide fragment
-        const int jA = warp * 16 + g_row, jB = jA + 8;
-        // Query fragments (A operand, row-major 16 x D) for rows jA / jB.
-        uint32_t qf[KS][4];
-        int limA = L, limB = L;
-        {
-            const uint32_t *qA = nullptr, *qB = nullptr;
-            if (jA < M) {
-                const int w = jA / p.group, hA = p.q_head_of[g * p.group + (jA - w * p.group)];
-                qA = reinterpret_cast<const uint32_t *>(p.q + ((size_t)(row0 + w) * p.num_q_heads + hA) * D);
-                if (p.causal)
-                    limA = L - W + w + 1;
-            }
-            if (jB < M) {
-                const int w = jB / p.group, hB = p.q_head_of[g * p.group + (jB - w * p.group)];
-                qB = reinterpret_cast<const uint32_t *>(p.q + ((size_t)(row0 + w) * p.num_q_heads + hB) * D);
-                if (p.causal)
-                    limB = L - W + w + 1;
+        if (lane == 0)
+            s_flag[2] = k;
+    } else if (warp < n_act) {
+        // ---------------- consumer warps ----------------
+        // S^T = K q^T and O^T += V^T P^T on mma.sync m16n8k16: keys / head dims on M,
+        // query rows on N.  Lane l owns rows 2(l%4) and 2(l%4)+1 of each n-tile for the
+        // softmax and the output, keys l/4 and l/4+8 of each 16-key m-tile.
+        const int cr = 2 * (lane & 3);   // first row of this lane within an n-tile
+        const int kr = lane >> 2;        // key (row of the C fragment) within 8
+        const int row_base = warp * RPW;
+        uint32_t qf[NN][KS][2];
+        int lim[NN][2];
+#pragma unroll
+        for (int nn = 0; nn < NN; ++nn) {
+            const int jq = row_base + nn * 8 + kr;   // B fragment: lane l carries row l/4
+            const uint32_t *qrow = nullptr;
+            if (jq < M) {
+                const int w = jq / p.group;
+                const int h = p.q_head_of[g * p.group + (jq - w * p.group)];
+                qrow = reinterpret_cast<const uint32_t *>(p.q + ((size_t)(row0 + w) * p.num_q_heads + h) * D);
             }
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
-                const int c0 = (ks * 16 + q_col) >> 1, c1 = (ks * 16 + 8 + q_col) >> 1;
-                qf[ks][0] = qA ? __ldg(qA + c0) : 0u;
-                qf[ks][1] = qB ? __ldg(qB + c0) : 0u;
-                qf[ks][2] = qA ? __ldg(qA + c1) : 0u;
-                qf[ks][3] = qB ? __ldg(qB + c1) : 0u;
+                qf[nn][ks][0] = qrow ? __ldg(qrow + ((ks * 16 + cr) >> 1)) : 0u;
+                qf[nn][ks][1] = qrow ? __ldg(qrow + ((ks * 16 + 8 + cr) >> 1)) : 0u;
+            }
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int j = row_base + nn * 8 + cr + e;
+                lim[nn][e] = (p.causal && j < M) ? L - W + j / p.group + 1 : L;
             }
         }
-        float o[DN][4];
+        float o[DM][NN][4];
 #pragma unroll
-        for (int i = 0; i < DN; ++i)
-            o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-        float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
+        for (int dm = 0; dm < DM; ++dm)
+#pragma unroll
+            for (int nn = 0; nn < NN; ++nn)
+                o[dm][nn][0] = o[dm][nn][1] = o[dm][nn][2] = o[dm][nn][3] = 0.f;
+        float mrow[NN][2], lrow[NN][2];
+#pragma unroll
+        for (int nn = 0; nn < NN; ++nn)
+            mrow[nn][0] = mrow[nn][1] = -INFINITY, lrow[nn][0] = lrow[nn][1] = 0.f;
 
-        // per-lane ldmatrix address parts
-        const int k_tok = 8 * (lane >> 4) + (lane & 7);   // K: token within a 16-key pair of n-tiles
-        const int k_chs = (lane >> 3) & 1;                 // K: chunk select within a k-step
-        const int v_tok = 8 * ((lane >> 3) & 1) + (lane & 7);
-        const int v_chs = lane >> 4;
+        // per-lane ldmatrix address parts (matrix mi = lane / 8, row lane % 8)
+        const int k_key = 8 * ((lane >> 3) & 1) + (lane & 7);   // K: keys of matrices 0/1 vs 2/3
+        const int k_chs = lane >> 4;
+        const int v_key = 8 * (lane >> 4) + (lane & 7);         // V: keys of matrices 0/1 vs 2/3
+        const int v_chs = (lane >> 3) & 1;
 
         int k = 0;
         for (; k < nblk; ++k) {
@@ -245,128 +264,172 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
             const uint32_t vb = smem_addr(v_tiles + st * T::kTileBytes);
             const int tbase = (blk0 + k) * BS;
 
-            // S = Q K^T for the BS keys of this block
-            float sc[NT][4];
+            // S^T for the BS keys of this block; even and odd k-steps in separate chains
+            float sa[MT][NN][4], sb[MT][NN][4];
 #pragma unroll
-            for (int i = 0; i < NT; ++i)
-                sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        sa[mt][nn][c] = sb[mt][nn][c] = 0.f;
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
 #pragma unroll
-                for (int np = 0; np < NT / 2; ++np) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(kb + tile_off<BS>(np * 16 + k_tok, ks * 2 + k_chs), b0, b1, b2, b3);
-                    mma_bf16_16x8x16(sc[2 * np], qf[ks], b0, b1);
-                    mma_bf16_16x8x16(sc[2 * np + 1], qf[ks], b2, b3);
+                for (int mt = 0; mt < MT; ++mt) {
+                    uint32_t a[4];
+                    ldsm_x4(kb + tile_off<BS>(mt * 16 + k_key, ks * 2 + k_chs), a[0], a[1], a[2], a[3]);
+#pragma unroll
+                    for (int nn = 0; nn < NN; ++nn) {
+                        if (ks & 1)
+                            mma_bf16_16x8x16(sb[mt][nn], a, qf[nn][ks][0], qf[nn][ks][1]);
+                        else
+                            mma_bf16_16x8x16(sa[mt][nn], a, qf[nn][ks][0], qf[nn][ks][1]);
+                    }
                 }
             }
-            // scale into base-2 units, mask keys past each row's limit
-            float mxA = -INFINITY, mxB = -INFINITY;
+            // scale into base-2 units; keys at or past a row's limit get -inf
+            float mx[NN][2];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const int t = tbase + nt * 8 + q_col;
-                sc[nt][0] = (t < limA) ? sc[nt][0] * p.scale_log2 : -INFINITY;
-                sc[nt][1] = (t + 1 < limA) ? sc[nt][1] * p.scale_log2 : -INFINITY;
-                sc[nt][2] = (t < limB) ? sc[nt][2] * p.scale_log2 : -INFINITY;
-                sc[nt][3] = (t + 1 < limB) ? sc[nt][3] * p.scale_log2 : -INFINITY;
-                mxA = fmaxf(mxA, fmaxf(sc[nt][0], sc[nt][1]));
-                mxB = fmaxf(mxB, fmaxf(sc[nt][2], sc[nt][3]));
+            for (int nn = 0; nn < NN; ++nn)
+                mx[nn][0] = mx[nn][1] = -INFINITY;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int t = tbase + mt * 16 + kr + 8 * (c >> 1);
+                        const float x = (sa[mt][nn][c] + sb[mt][nn][c]) * p.scale_log2;
+                        sa[mt][nn][c] = (t < lim[nn][c & 1]) ? x : -INFINITY;
+                        mx[nn][c & 1] = fmaxf(mx[nn][c & 1], sa[mt][nn][c]);
+                    }
+            float alpha[NN][2], base[NN][2];
+#pragma unroll
+            for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    float v = mx[nn][e];
+                    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+                    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+                    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+                    const float m_new = fmaxf(mrow[nn][e], v);
+                    base[nn][e] = (m_new == -INFINITY) ? 0.f : m_new;
+                    alpha[nn][e] = exp2f(mrow[nn][e] - base[nn][e]);
+                    mrow[nn][e] = m_new;
+                }
+            // P = 2^(S - m) rounded to bf16 (packed per 8x8 fragment); l sums the rounded weights
+            uint32_t pk[MT][NN][2];
+            float sum[NN][2];
+#pragma unroll
+            for (int nn = 0; nn < NN; ++nn)
+                sum[nn][0] = sum[nn][1] = 0.f;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int nn = 0; nn < NN; ++nn) {
+                    pk[mt][nn][0] = pack_bf16x2(exp2f(sa[mt][nn][0] - base[nn][0]), exp2f(sa[mt][nn][1] - base[nn][1]));
+                    pk[mt][nn][1] = pack_bf16x2(exp2f(sa[mt][nn][2] - base[nn][0]), exp2f(sa[mt][nn][3] - base[nn][1]));
+                    sum[nn][0] += bf16_lo_to_f32(pk[mt][nn][0]) + bf16_lo_to_f32(pk[mt][nn][1]);
+                    sum[nn][1] += bf16_hi_to_f32(pk[mt][nn][0]) + bf16_hi_to_f32(pk[mt][nn][1]);
+                }
+#pragma unroll
+            for (int nn = 0; nn < NN; ++nn) {
+                lrow[nn][0] = lrow[nn][0] * alpha[nn][0] + sum[nn][0];
+                lrow[nn][1] = lrow[nn][1] * alpha[nn][1] + sum[nn][1];
+#pragma unroll
+                for (int dm = 0; dm < DM; ++dm) {
+                    o[dm][nn][0] *= alpha[nn][0];
+                    o[dm][nn][1] *= alpha[nn][1];
+                    o[dm][nn][2] *= alpha[nn][0];
+                    o[dm][nn][3] *= alpha[nn][1];
+                }
             }
-            mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 1));
-            mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 2));
-            mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 1));
-            mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 2));
-            const float mA_new = fmaxf(mA, mxA), mB_new = fmaxf(mB, mxB);
-            const float baseA = (mA_new == -INFINITY) ? 0.f : mA_new;
-            const float baseB = (mB_new == -INFINITY) ? 0.f : mB_new;
-            const float alphaA = exp2f(mA - baseA), alphaB = exp2f(mB - baseB);
-            mA = mA_new;
-            mB = mB_new;
 
-            // P = 2^(S - m), rounded to bf16; l accumulates the rounded weights
-            uint32_t pp[NT][2];
-            float sumA = 0.f, sumB = 0.f;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                pp[nt][0] = pack_bf16x2(exp2f(sc[nt][0] - baseA), exp2f(sc[nt][1] - baseA));
-                pp[nt][1] = pack_bf16x2(exp2f(sc[nt][2] - baseB), exp2f(sc[nt][3] - baseB));
-                sumA += bf16_lo_to_f32(pp[nt][0]) + bf16_hi_to_f32(pp[nt][0]);
-                sumB += bf16_lo_to_f32(pp[nt][1]) + bf16_hi_to_f32(pp[nt][1]);
-            }
-            lA = lA * alphaA + sumA;
-            lB = lB * alphaB + sumB;
-#pragma unroll
-            for (int dn = 0; dn < DN; ++dn) {
-                o[dn][0] *= alphaA;
-                o[dn][1] *= alphaA;
-                o[dn][2] *= alphaB;
-                o[dn][3] *= alphaB;
-            }
-
-            // O += P V; keys at or past L may hold anything (even NaN): zero them
+            // O^T += V^T P^T; keys at or past L may hold anything (even NaN): zero them
             const bool tail = tbase + BS > L;
 #pragma unroll
-            for (int kk = 0; kk < BS / 16; ++kk) {
-                const uint32_t a[4] = {pp[2 * kk][0], pp[2 * kk][1], pp[2 * kk + 1][0], pp[2 * kk + 1][1]};
+            for (int kk = 0; kk < MT; ++kk) {
+                uint32_t b[NN][2];
+#pragma unroll
+                for (int nn = 0; nn < NN; ++nn) {
+                    b[nn][0] = movmatrix_trans(pk[kk][nn][0]);   // keys 0-7 of the m-tile
+                    b[nn][1] = movmatrix_trans(pk[kk][nn][1]);   // keys 8-15
+                }
                 uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
                 if (tail) {
-                    const int t = tbase + kk * 16 + q_col;
+                    const int t = tbase + kk * 16 + cr;
                     mlo = (t < L ? 0x0000ffffu : 0u) | (t + 1 < L ? 0xffff0000u : 0u);
                     mhi = (t + 8 < L ? 0x0000ffffu : 0u) | (t + 9 < L ? 0xffff0000u : 0u);
                 }
 #pragma unroll
-                for (int dp = 0; dp < DN / 2; ++dp) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_trans(vb + tile_off<BS>(kk * 16 + v_tok, dp * 2 + v_chs), b0, b1, b2, b3);
-                    mma_bf16_16x8x16(o[2 * dp], a, b0 & mlo, b1 & mhi);
-                    mma_bf16_16x8x16(o[2 * dp + 1], a, b2 & mlo, b3 & mhi);
+                for (int dm = 0; dm < DM; ++dm) {
+                    uint32_t a[4];
+                    ldsm_x4_trans(vb + tile_off<BS>(kk * 16 + v_key, dm * 2 + v_chs), a[0], a[1], a[2], a[3]);
+                    a[0] &= mlo;
+                    a[1] &= mlo;
+                    a[2] &= mhi;
+                    a[3] &= mhi;
+#pragma unroll
+                    for (int nn = 0; nn < NN; ++nn)
+                        mma_bf16_16x8x16(o[dm][nn], a, b[nn][0], b[nn][1]);
                 }
             }
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&empty[st]);
         }
-        if (warp == 0 && lane == 0)
-            s_flag[3] = k;
 
-        // write this split's partial for the valid rows
-        lA += __shfl_xor_sync(0xffffffffu, lA, 1);
-        lA += __shfl_xor_sync(0xffffffffu, lA, 2);
-        lB += __shfl_xor_sync(0xffffffffu, lB, 1);
-        lB += __shfl_xor_sync(0xffffffffu, lB, 2);
+        // this split's partial for the rows this warp owns
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int j = half ? jB : jA;
-            if (j >= M)
-                continue;
-            const int w = j / p.group;
-            const int h = p.q_head_of[g * p.group + (j - w * p.group)];
-            const size_t slot = ((size_t)(row0 + w) * p.num_q_heads + h) * p.n_max + split;
-            if ((lane & 3) == 0)
-                p.part_ml[slot] = make_float2(half ? mB : mA, half ? lB : lA);
-            float2 *dst = reinterpret_cast<float2 *>(p.part_o + slot * D);
+        for (int nn = 0; nn < NN; ++nn)
 #pragma unroll
-            for (int dn = 0; dn < DN; ++dn)
-                dst[(dn * 8 + q_col) >> 1] = half ? make_float2(o[dn][2], o[dn][3])
-                                                  : make_float2(o[dn][0], o[dn][1]);
-        }
+            for (int e = 0; e < 2; ++e) {
+                float v = lrow[nn][e];
+                v += __shfl_xor_sync(0xffffffffu, v, 4);
+                v += __shfl_xor_sync(0xffffffffu, v, 8);
+                v += __shfl_xor_sync(0xffffffffu, v, 16);
+                lrow[nn][e] = v;
+            }
+#pragma unroll
+        for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int j = row_base + nn * 8 + cr + e;
+                if (j >= M)
+                    continue;
+                const int w = j / p.group;
+                const int h = p.q_head_of[g * p.group + (j - w * p.group)];
+                const size_t slot = ((size_t)(row0 + w) * p.num_q_heads + h) * p.n_max + split;
+                if (kr == 0)
+                    p.part_ml[slot] = make_float2(mrow[nn][e], lrow[nn][e]);
+                float *dst = p.part_o + slot * D;
+#pragma unroll
+                for (int dm = 0; dm < DM; ++dm) {
+                    dst[dm * 16 + kr] = o[dm][nn][e];
+                    dst[dm * 16 + kr + 8] = o[dm][nn][2 + e];
+                }
+            }
     }
 
     // ---------------- hand-off: the last split of (s, g) merges ----------------
-    __threadfence();
+    // bar.sync orders every thread's partial writes before thread 0's cumulative fence.
     __syncthreads();
     if (s_flag[1]) {
-        // a wait expired: drain TMA copies still in flight (bounded) and leave
+        // a wait expired: wait (bounded) for the last copy issued into each stage, then leave
         if (threadIdx.x == 0) {
-            const int issued = s_flag[2], consumed = s_flag[3];
-            for (int kk = consumed; kk < issued; ++kk)
-                if (!mbar_wait_bounded(&full[kk % NST], (kk / NST) & 1, kWaitLimitCycles))
+            const int issued = s_flag[2];
+            for (int st = 0; st < NST && st < issued; ++st) {
+                const int k_last = st + ((issued - 1 - st) / NST) * NST;
+                if (!mbar_wait_bounded(&full[st], (k_last / NST) & 1, kWaitLimitCycles))
                     break;
+            }
         }
         return;
     }
     const int n_arrive = n_splits > 0 ? n_splits : 1;
     if (threadIdx.x == 0) {
+        __threadfence();
         const int old = atomicAdd(p.counters + pair, 1);
         if (old >= n_arrive)
             atomicOr(p.status, PKV_DEV_WORKSPACE);
@@ -398,6 +461,7 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
         }
         float den = 0.f;
         float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
         for (int i = 0; i < nr; ++i) {
             const float2 ml = __ldcg(&p.part_ml[base + i]);
             const float wgt = exp2f(ml.x - Mx);
@@ -472,26 +536,30 @@ int make_pool_map(CUtensorMap *map, void *base, const pkv_pool &pool)
     return PKV_OK;
 }
 
-template <int D, int BS, int NMT>
+#ifndef PKV_STAGES
+#define PKV_STAGES 0
+#endif
+template <int D, int BS>
 constexpr int kStages()
 {
-    return Tile<D, BS>::kTileBytes * 2 >= 16384 ? 3 : 4;
+    // 3 stages of >= 8 KB keep 8 KB x 3 x (8 CTAs) in flight per SM; measured best on GB300
+    return PKV_STAGES > 0 ? PKV_STAGES : (Tile<D, BS>::kTileBytes * 2 >= 8192 ? 3 : 4);
 }
 
-template <int D, int BS, int NMT>
+template <int D, int BS>
 size_t smem_bytes()
 {
-    constexpr int NST = kStages<D, BS, NMT>();
+    constexpr int NST = kStages<D, BS>();
     return 1024 + (size_t)NST * 2 * Tile<D, BS>::kTileBytes + 2 * NST * sizeof(uint64_t) + 64;
 }
 
-template <int D, int BS, int NMT>
+template <int D, int BS, int NN, int NMT>
 int launch_t(const CUtensorMap &mk, const CUtensorMap &mv, const AttnParams &prm, dim3 grid,
              cudaStream_t st)
 {
-    constexpr int NST = kStages<D, BS, NMT>();
-    auto kern = paged_attention_kernel<D, BS, NMT, NST>;
-    const size_t smem = smem_bytes<D, BS, NMT>();
+    constexpr int NST = kStages<D, BS>();
+    auto kern = paged_attention_kernel<D, BS, NN, NMT, NST>;
+    const size_t smem = smem_bytes<D, BS>();
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -503,17 +571,17 @@ int launch_t(const CUtensorMap &mk, const CUtensorMap &mv, const AttnParams &prm
     return check_cuda(cudaGetLastError(), "paged_attention_forward launch");
 }
 
+// Rows per CTA (G * max rows per sequence) -> (n-tiles per warp, consumer warps).
 template <int D, int BS>
-int launch_d_bs(int nmt, const CUtensorMap &mk, const CUtensorMap &mv, const AttnParams &prm,
+int launch_d_bs(int rows, const CUtensorMap &mk, const CUtensorMap &mv, const AttnParams &prm,
                 dim3 grid, cudaStream_t st)
 {
-    switch (nmt) {
-    case 1: return launch_t<D, BS, 1>(mk, mv, prm, grid, st);
-    case 2: return launch_t<D, BS, 2>(mk, mv, prm, grid, st);
-    case 4: return launch_t<D, BS, 4>(mk, mv, prm, grid, st);
-    case 8: return launch_t<D, BS, 8>(mk, mv, prm, grid, st);
-    default: return set_error(PKV_ERR_UNSUPPORTED, "internal: m-tile count %d", nmt);
-    }
+    if (rows <= 8) return launch_t<D, BS, 1, 1>(mk, mv, prm, grid, st);
+    if (rows <= 16) return launch_t<D, BS, 2, 1>(mk, mv, prm, grid, st);
+    if (rows <= 32) return launch_t<D, BS, 2, 2>(mk, mv, prm, grid, st);
+    if (rows <= 64) return launch_t<D, BS, 2, 4>(mk, mv, prm, grid, st);
+    if (rows <= 128) return launch_t<D, BS, 2, 8>(mk, mv, prm, grid, st);
+    return set_error(PKV_ERR_UNSUPPORTED, "internal: %d rows per CTA", rows);
 }
 
 struct WsLayout {
@@ -665,17 +733,15 @@ extern "C" int paged_attention_forward(const pkv_pool *pool, const void *q, cons
     prm.scale_log2 = sc * kLog2e;
 
     const int rows = G * max_q_rows_per_seq;
-    const int nmt_need = (rows + 15) / 16;
-    const int nmt = nmt_need <= 1 ? 1 : nmt_need <= 2 ? 2 : nmt_need <= 4 ? 4 : 8;
     const long long gx = (long long)num_seqs * Hkv;
     if (gx > 0x7fffffffLL || n_max > 65535)
         return set_error(PKV_ERR_SHAPE, "paged_attention_forward: grid too large");
     const dim3 grid((unsigned)gx, (unsigned)n_max);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (D == 64 && BS == 16) return launch_d_bs<64, 16>(nmt, mk, mv, prm, grid, st);
-    if (D == 64 && BS == 32) return launch_d_bs<64, 32>(nmt, mk, mv, prm, grid, st);
-    if (D == 128 && BS == 16) return launch_d_bs<128, 16>(nmt, mk, mv, prm, grid, st);
-    return launch_d_bs<128, 32>(nmt, mk, mv, prm, grid, st);
+    if (D == 64 && BS == 16) return launch_d_bs<64, 16>(rows, mk, mv, prm, grid, st);
+    if (D == 64 && BS == 32) return launch_d_bs<64, 32>(rows, mk, mv, prm, grid, st);
+    if (D == 128 && BS == 16) return launch_d_bs<128, 16>(rows, mk, mv, prm, grid, st);
+    return launch_d_bs<128, 32>(rows, mk, mv, prm, grid, st);
 }
 
 // ------------------------------------------------ allocation-free variant --

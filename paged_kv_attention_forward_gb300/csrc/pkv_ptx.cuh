@@ -117,6 +117,16 @@ __device__ __forceinline__ void mma_bf16_16x8x16(float (&d)[4], const uint32_t (
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Transpose an 8x8 matrix of 16-bit values held in the mma fragment layout (lane l
+// holds row l/4, columns 2(l%4) and 2(l%4)+1) -- afterwards lane l holds row l/4 of
+// the transpose.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x)
+{
+    uint32_t r;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+    return r;
+}
+
 // Two floats -> packed bf16x2 (round to nearest even); `lo` in the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
