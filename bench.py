@@ -192,7 +192,8 @@ def run_ours(args, rank, world, local_rank):
     has_append = int(b.new_starts[-1]) > 0
     max_ctx, max_rows = b.max_context_len, b.max_q_rows_per_seq
     stream = torch.cuda.current_stream()
-    launches_per_step = layers * (int(has_append) + 1) + (2 if logits is not None else 0)
+    # per layer: append (if any) + attention split kernel + attention merge kernel; accept: 2
+    launches_per_step = layers * (int(has_append) + 2) + (2 if logits is not None else 0)
 
     def step(ev_pairs=None, li=None):
         for i in range(layers):
@@ -334,7 +335,7 @@ def run_ours(args, rank, world, local_rank):
         "frac_of_nominal_8tbs": round(value / 8000.0, 4),
         "bytes_per_step": acct["step"], "kv_unique_bytes_per_step": acct["kv_unique"],
         "kv_logical_bytes_per_step": acct["kv_logical"],
-        "roofline": {"kernel": "paged_attention_kernel", "bound": "hbm", "achieved": round(achieved, 2),
+        "roofline": {"kernel": "paged attention call (split kernel + merge kernel)", "bound": "hbm", "achieved": round(achieved, 2),
                      "peak": peak, "peak_kind": f"{peak_kind} (hbm_gbs, copy kernel)", "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "bytes_per_launch": per_launch_bytes,
                      "avg_launch_ms": round(attn_avg_ms, 5), "launches_timed": len(attn_ms),

@@ -60,7 +60,7 @@ typedef enum pkv_status {
     PKV_ERR_NULL = -1,        /* a required pointer is NULL                          */
     PKV_ERR_SHAPE = -2,       /* sizes inconsistent or out of range                  */
     PKV_ERR_UNSUPPORTED = -3, /* head_dim / block_size / group x window not built    */
-    PKV_ERR_WORKSPACE = -4,   /* workspace too small, or (device) not zero on entry  */
+    PKV_ERR_WORKSPACE = -4,   /* workspace too small                                 */
     PKV_ERR_BAD_BLOCK = -5,   /* (device) block id outside the pool / table overrun  */
     PKV_ERR_CUDA = -6,        /* a CUDA runtime call or kernel launch failed         */
     PKV_ERR_ALIGN = -7,       /* a pointer is not 16-byte aligned                    */
@@ -75,7 +75,7 @@ enum {
     PKV_DEV_TABLE_OVERRUN = 2, /* a length past max_blocks_per_seq * block_size or
                                   past max_context_len                                    */
     PKV_DEV_TOO_MANY_ROWS = 4, /* a sequence with more rows than max_q_rows_per_seq       */
-    PKV_DEV_WORKSPACE = 8,     /* the attention workspace's counters were not zero        */
+    PKV_DEV_WORKSPACE = 8,     /* (reserved)                                              */
     PKV_DEV_TIMEOUT = 16       /* a bounded wait expired                                  */
 };
 
@@ -123,17 +123,17 @@ int paged_kv_append(const pkv_pool *pool,
 
 /*
  * Bytes of workspace paged_attention_forward needs for these sizes (a
- * multiple of 256).  The workspace holds a small counter region that must be
- * ZERO before the first call (allocate it zeroed, or call
- * paged_attention_workspace_init once); every call that completes leaves it
- * zero again, so one workspace serves any sequence of calls on one stream.
- * Calls that may overlap on the GPU need separate workspaces.
+ * multiple of 256): the per-split partial results (running max, sum and
+ * unnormalised output of every query row, q head and 512-token split).  Its
+ * contents on entry do not matter.  One workspace serves any sequence of calls
+ * on one stream; calls that may overlap on the GPU need separate workspaces.
  */
 size_t paged_attention_workspace_size(int32_t num_seqs, int32_t total_q_rows,
                                       int32_t num_q_heads, int32_t num_kv_heads,
                                       int32_t head_dim, int32_t max_context_len);
 
-/* Zero a workspace (cudaMemsetAsync on `stream`). */
+/* Zero a workspace (cudaMemsetAsync on `stream`); optional, kept for callers that
+ * want deterministic workspace contents. */
 int paged_attention_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
 
 /*
@@ -165,13 +165,14 @@ int paged_attention_workspace_init(void *workspace, size_t workspace_bytes, void
  *   scale              > 0, or <= 0 for 1/sqrt(head_dim)
  *   out                [total_q_rows][num_q_heads][head_dim], bf16 or float32
  *                      (out_dtype = PKV_DTYPE_BF16 / PKV_DTYPE_F32)
- *   workspace          >= paged_attention_workspace_size(...) bytes, zero on
- *                      first use (see above), 256-byte aligned
+ *   workspace          >= paged_attention_workspace_size(...) bytes, 256-byte
+ *                      aligned
  * Every row's arithmetic depends only on its own sequence (its length fixes
  * the split of the keys into fixed 512-token chunks; partials merge in chunk
  * order), so a row computed in any batch is bit-identical to the same row
  * computed alone, and row w of a causal window is bit-identical to a one-row
- * decode over the first L - W + w + 1 keys.  Launches one kernel.
+ * decode over the first L - W + w + 1 keys.  Launches two kernels: the split
+ * kernel and, as its programmatic dependent, the merge.
  */
 int paged_attention_forward(const pkv_pool *pool,
                             const void *q, const int32_t *q_starts,
@@ -228,8 +229,8 @@ int spec_accept_greedy(const float *logits, int32_t vocab,
  * rejected with PKV_ERR_WORKSPACE before anything is launched.  The first call
  * on a device looks the array's device address up (cudaGetSymbolAddress) with
  * that device current; make that first call before any stream capture.  Each
- * call clears the array's counter region (cudaMemsetAsync on `stream`) and then
- * launches the attention kernel; it calls no allocator.  All calls on a device
+ * call launches the attention kernels with the array as their workspace; it
+ * calls no allocator.  All calls on a device
  * share the one array, which keeps the last call's contents: calls that may
  * overlap on the GPU (different streams without ordering) race and corrupt
  * each other's results.

@@ -7,7 +7,7 @@
 // "先记住一条铁律": a verify row uses exactly the serial step's arithmetic, and a
 // row computed in a batch equals the row computed alone.
 //
-// Design (one kernel per call):
+// Design (two kernels per call: splits, then merge):
 //  * Work unit = (sequence s, KV head g, split i).  Split i covers keys
 //    [512 i, 512 i + 512) of s.  The split grid depends on the sequence's own
 //    length only, never on the batch, so every row's arithmetic is fixed by
@@ -28,10 +28,12 @@
 //    O^T += V^T P^T.
 //    Keys past a row's limit get weight exactly 0, so a verify-window row and the
 //    same row decoded alone go through identical operations.
-//  * Partials (m, l, O) of every split go to the workspace.  The last CTA of an
-//    (s, g) pair to finish (atomic counter) merges the partials of each row in
-//    split order:  M = max(m_i, sink), out = sum_i 2^{m_i-M} O_i /
-//    (sum_i 2^{m_i-M} l_i + 2^{sink-M}), and resets the counter to zero.
+//  * Partials (m, l, O) of every split go to the workspace.  A second kernel,
+//    one warp per (query row, q head), merges them in split order:
+//    M = max(m_i, sink), out = sum_i 2^{m_i-M} O_i / (sum_i 2^{m_i-M} l_i + 2^{sink-M}).
+//    It is launched as a programmatic dependent of the split kernel, so its launch
+//    overlaps the split grid's tail; the merge of the longest sequences is no
+//    longer serialised on one CTA at the end.
 //  * Bounded waits only; block ids and lengths are range-checked on the device
 //    (clamped + status bit, never a fault).
 #include <cmath>
@@ -57,9 +59,8 @@ struct AttnParams {
     void *out;                    // [R][Hq][D] bf16 or f32
     float2 *part_ml;              // [R*Hq*n_max] (m in log2 units, l)
     float *part_o;                // [R*Hq*n_max][D]
-    int32_t *counters;            // [S*Hkv]
     int32_t *status;
-    int32_t num_seqs, max_blocks_per_seq, num_blocks, num_q_heads, num_kv_heads, group;
+    int32_t num_seqs, max_blocks_per_seq, num_blocks, num_q_heads, num_kv_heads, group, block_size;
     int32_t n_max, max_context_len, max_rows, total_rows;
     int32_t causal, out_f32;
     float scale_log2;             // scale * log2(e)
@@ -97,7 +98,7 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
     constexpr int DM = D / 16;    // 16-dim m-tiles of V^T P^T
     constexpr int C = kSplitTokens;
     constexpr int RPW = 8 * NN;   // rows per consumer warp
-    static_assert(C / BS <= 32, "one warp holds a split's block ids");
+    constexpr int NBW = (C / BS + 31) / 32;   // block ids per producer lane
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -107,7 +108,7 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
     uint64_t *full = reinterpret_cast<uint64_t *>(v_tiles + NST * T::kTileBytes);
     uint64_t *empty = full + NST;
     volatile int32_t *s_flag = reinterpret_cast<volatile int32_t *>(empty + NST);
-    // s_flag[0]: this CTA merges; [1]: abort; [2]: blocks issued
+    // s_flag[1]: abort; [2]: blocks issued
 
     const int pair = blockIdx.x;
     const int s = pair / p.num_kv_heads;
@@ -123,9 +124,11 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
             atomicOr(p.status, PKV_DEV_TABLE_OVERRUN);
         L = L < 0 ? 0 : L_cap;
     }
+    // the dependent merge kernel may be scheduled once every CTA of this grid has started
+    asm volatile("griddepcontrol.launch_dependents;");
     const int n_splits = (L + C - 1) / C;
-    if (split >= n_splits && !(n_splits == 0 && split == 0))
-        return;   // an empty context still owns split 0 (it writes the zero / sink output)
+    if (split >= n_splits)
+        return;
     const int row0 = __ldg(p.q_starts + s);
     int W = __ldg(p.q_starts + s + 1) - row0;
     if (W <= 0)
@@ -146,7 +149,7 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
     const int t0 = split * C;
     const int t1 = min(t0 + C, L);
     const int blk0 = t0 / BS;
-    const int nblk = t1 > t0 ? (t1 - t0 + BS - 1) / BS : 0;
+    const int nblk = (t1 - t0 + BS - 1) / BS;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NST; ++i) {
@@ -154,7 +157,6 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
             mbar_init(&empty[i], n_act);
         }
         mbar_fence_init();
-        s_flag[0] = 0;
         s_flag[1] = 0;
         s_flag[2] = 0;
     }
@@ -162,12 +164,18 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
 
     if (warp == NMT) {
         // ---------------- producer warp: block table -> TMA ring ----------------
-        int my_blk = 0;   // lane j holds the id of the split's j-th block
-        if (lane < nblk) {
-            my_blk = __ldg(p.block_tables + (size_t)s * p.max_blocks_per_seq + blk0 + lane);
-            if (my_blk < 0 || my_blk >= p.num_blocks) {
-                atomicOr(p.status, PKV_DEV_BAD_BLOCK);
-                my_blk = 0;
+        // lane l holds the ids of the split's blocks l, l + 32, ... (one coalesced load each)
+        int my_blk[NBW];
+#pragma unroll
+        for (int r = 0; r < NBW; ++r) {
+            my_blk[r] = 0;
+            const int j = r * 32 + lane;
+            if (j < nblk) {
+                my_blk[r] = __ldg(p.block_tables + (size_t)s * p.max_blocks_per_seq + blk0 + j);
+                if (my_blk[r] < 0 || my_blk[r] >= p.num_blocks) {
+                    atomicOr(p.status, PKV_DEV_BAD_BLOCK);
+                    my_blk[r] = 0;
+                }
             }
         }
         if (lane == 0) {
@@ -175,31 +183,39 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
             prefetch_tensormap(&tm_v);
         }
         int k = 0;
-        for (; k < nblk; ++k) {
-            const int blk = __shfl_sync(0xffffffffu, my_blk, k);
-            bool stop = false;
-            if (lane == 0) {
-                const int st = k % NST;
-                bool ok = true;
-                if (k >= NST)
-                    ok = mbar_wait_bounded(&empty[st], ((k / NST) + 1) & 1, kWaitLimitCycles);
-                if (!ok)
-                    atomicOr(p.status, PKV_DEV_TIMEOUT);
-                if (!ok || s_flag[1]) {
-                    s_flag[1] = 1;
-                    stop = true;
-                } else {
-                    const int y = (blk * p.num_kv_heads + g) * BS;
-                    mbar_arrive_expect_tx(&full[st], 2 * T::kTileBytes);
+        bool stop = false;
 #pragma unroll
-                    for (int h = 0; h < T::kHalves; ++h) {
-                        tma_load_2d(k_tiles + st * T::kTileBytes + h * T::kBoxBytes, &tm_k, &full[st], h * 64, y);
-                        tma_load_2d(v_tiles + st * T::kTileBytes + h * T::kBoxBytes, &tm_v, &full[st], h * 64, y);
+        for (int r = 0; r < NBW; ++r) {
+            for (int jj = 0; jj < 32 && !stop; ++jj) {
+                if (k >= nblk)
+                    break;
+                const int blk = __shfl_sync(0xffffffffu, my_blk[r], jj);
+                if (lane == 0) {
+                    const int st = k % NST;
+                    bool ok = true;
+                    if (k >= NST)
+                        ok = mbar_wait_bounded(&empty[st], ((k / NST) + 1) & 1, kWaitLimitCycles);
+                    if (!ok)
+                        atomicOr(p.status, PKV_DEV_TIMEOUT);
+                    if (!ok || s_flag[1]) {
+                        s_flag[1] = 1;
+                        stop = true;
+                    } else {
+                        const int y = (blk * p.num_kv_heads + g) * BS;
+                        mbar_arrive_expect_tx(&full[st], 2 * T::kTileBytes);
+#pragma unroll
+                        for (int h = 0; h < T::kHalves; ++h) {
+                            tma_load_2d(k_tiles + st * T::kTileBytes + h * T::kBoxBytes, &tm_k, &full[st],
+                                        h * 64, y);
+                            tma_load_2d(v_tiles + st * T::kTileBytes + h * T::kBoxBytes, &tm_v, &full[st],
+                                        h * 64, y);
+                        }
                     }
                 }
+                stop = __shfl_sync(0xffffffffu, stop, 0);
+                if (!stop)
+                    ++k;
             }
-            if (__shfl_sync(0xffffffffu, stop, 0))
-                break;
         }
         if (lane == 0)
             s_flag[2] = k;
@@ -412,87 +428,159 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
             }
     }
 
-    // ---------------- hand-off: the last split of (s, g) merges ----------------
-    // bar.sync orders every thread's partial writes before thread 0's cumulative fence.
+    // a wait expired: wait (bounded) for the last copy issued into each stage before leaving
     __syncthreads();
-    if (s_flag[1]) {
-        // a wait expired: wait (bounded) for the last copy issued into each stage, then leave
-        if (threadIdx.x == 0) {
-            const int issued = s_flag[2];
-            for (int st = 0; st < NST && st < issued; ++st) {
-                const int k_last = st + ((issued - 1 - st) / NST) * NST;
-                if (!mbar_wait_bounded(&full[st], (k_last / NST) & 1, kWaitLimitCycles))
-                    break;
+    if (s_flag[1] && threadIdx.x == 0) {
+        const int issued = s_flag[2];
+        for (int st = 0; st < NST && st < issued; ++st) {
+            const int k_last = st + ((issued - 1 - st) / NST) * NST;
+            if (!mbar_wait_bounded(&full[st], (k_last / NST) & 1, kWaitLimitCycles))
+                break;
+        }
+    }
+}
+
+// Merge of the split partials of one (query row, q head) per warp, in split order,
+// with the head's sink:  M = max(m_i, sink), out = sum_i 2^{m_i - M} O_i /
+// (sum_i 2^{m_i - M} l_i + 2^{sink - M}).  Launched as a programmatic dependent of
+// the split kernel: it may start early and waits for the partials with
+// griddepcontrol.wait.
+template <int D>
+__global__ void __launch_bounds__(128)
+paged_attention_combine_kernel(const AttnParams p)
+{
+    constexpr int VEC = D / 32;   // output values per lane
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const long long wid = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (wid >= (long long)p.total_rows * p.num_q_heads)
+        return;
+    const int r = (int)(wid / p.num_q_heads);
+    const int h = (int)(wid - (long long)r * p.num_q_heads);
+    // sequence of row r: the last s with q_starts[s] <= r
+    int lo = 0, hi = p.num_seqs - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(p.q_starts + mid) <= r)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const int s = lo;
+    const int row0 = __ldg(p.q_starts + s);
+    const int W = min(__ldg(p.q_starts + s + 1) - row0, p.max_rows);
+    const int w = r - row0;
+    if (w < 0 || w >= W)
+        return;   // rows past max_q_rows_per_seq were never computed (status already set)
+    const int L_cap = (int)min((long long)p.max_context_len, (long long)p.max_blocks_per_seq * p.block_size);
+    int L = __ldg(p.context_lens + s);
+    L = L < 0 ? 0 : (L > L_cap ? L_cap : L);
+    const int lim = p.causal ? L - W + w + 1 : L;
+    const int n = lim > 0 ? (lim + kSplitTokens - 1) / kSplitTokens : 0;
+    const size_t base = ((size_t)r * p.num_q_heads + h) * p.n_max;
+
+    // lane i holds (m, l) of partials i, i + 32, ...; the sums below still run in split order
+    constexpr int MAXC = 4;   // partials cached per lane (n <= 128); longer rows reload (m, l)
+    float2 mlc[MAXC];
+#pragma unroll
+    for (int c = 0; c < MAXC; ++c) {
+        const int i = c * 32 + lane;
+        mlc[c] = i < n ? __ldcg(&p.part_ml[base + i]) : make_float2(-INFINITY, 0.f);
+    }
+    float Mx = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < MAXC; ++c)
+        Mx = fmaxf(Mx, mlc[c].x);
+    for (int i = MAXC * 32 + lane; i < n; i += 32)
+        Mx = fmaxf(Mx, __ldcg(&p.part_ml[base + i]).x);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, off));
+    float sink2 = 0.f;
+    const bool has_sink = p.sinks != nullptr;
+    if (has_sink) {
+        sink2 = __ldg(p.sinks + h) * kLog2e;
+        Mx = fmaxf(Mx, sink2);
+    }
+    float wc[MAXC], lc[MAXC];
+#pragma unroll
+    for (int c = 0; c < MAXC; ++c) {
+        wc[c] = exp2f(mlc[c].x - Mx);
+        lc[c] = mlc[c].y;
+    }
+    float den = 0.f;
+    float num[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v)
+        num[v] = 0.f;
+    const float *src0 = p.part_o + base * D + lane * VEC;
+    constexpr int BATCH = 16;   // partial rows in flight per lane
+    for (int i0 = 0; i0 < n; i0 += BATCH) {
+        float x[BATCH][VEC];
+#pragma unroll
+        for (int b = 0; b < BATCH; ++b) {
+            const int i = i0 + b;
+            if (i < n) {
+                const float *src = src0 + (size_t)i * D;
+                if constexpr (VEC == 4) {
+                    const float4 t = __ldcg(reinterpret_cast<const float4 *>(src));
+                    x[b][0] = t.x, x[b][1] = t.y, x[b][2] = t.z, x[b][3] = t.w;
+                } else {
+                    const float2 t = __ldcg(reinterpret_cast<const float2 *>(src));
+                    x[b][0] = t.x, x[b][1] = t.y;
+                }
             }
         }
-        return;
+#pragma unroll
+        for (int b = 0; b < BATCH; ++b) {
+            const int i = i0 + b;
+            if (i >= n)
+                break;
+            float wgt, l_i;
+            if (i < MAXC * 32) {
+                const int c = i >> 5, srcl = i & 31;
+                float wsel = wc[0], lsel = lc[0];
+#pragma unroll
+                for (int cc = 1; cc < MAXC; ++cc)
+                    if (c == cc)
+                        wsel = wc[cc], lsel = lc[cc];
+                wgt = __shfl_sync(0xffffffffu, wsel, srcl);
+                l_i = __shfl_sync(0xffffffffu, lsel, srcl);
+            } else {
+                const float2 ml = __ldcg(&p.part_ml[base + i]);
+                wgt = exp2f(ml.x - Mx);
+                l_i = ml.y;
+            }
+            den += wgt * l_i;
+#pragma unroll
+            for (int v = 0; v < VEC; ++v)
+                num[v] += wgt * x[b][v];
+        }
     }
-    const int n_arrive = n_splits > 0 ? n_splits : 1;
-    if (threadIdx.x == 0) {
-        __threadfence();
-        const int old = atomicAdd(p.counters + pair, 1);
-        if (old >= n_arrive)
-            atomicOr(p.status, PKV_DEV_WORKSPACE);
-        s_flag[0] = (old == n_arrive - 1) ? 1 : 0;
-    }
-    __syncthreads();
-    if (!s_flag[0])
-        return;
-    __threadfence();
-
-    constexpr int V4 = D / 4;
-    const int n_items = M * V4;
-    for (int it = threadIdx.x; it < n_items; it += blockDim.x) {
-        const int j = it / V4, c4 = it - j * V4;
-        const int w = j / p.group;
-        const int h = p.q_head_of[g * p.group + (j - w * p.group)];
-        const int r = row0 + w;
-        const int lim = p.causal ? L - W + w + 1 : L;
-        const int nr = lim > 0 ? (lim + C - 1) / C : 0;
-        const size_t base = ((size_t)r * p.num_q_heads + h) * p.n_max;
-        float Mx = -INFINITY;
-        for (int i = 0; i < nr; ++i)
-            Mx = fmaxf(Mx, __ldcg(&p.part_ml[base + i]).x);
-        float sink2 = 0.f;
-        const bool has_sink = p.sinks != nullptr;
-        if (has_sink) {
-            sink2 = __ldg(p.sinks + h) * kLog2e;
-            Mx = fmaxf(Mx, sink2);
-        }
-        float den = 0.f;
-        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-        for (int i = 0; i < nr; ++i) {
-            const float2 ml = __ldcg(&p.part_ml[base + i]);
-            const float wgt = exp2f(ml.x - Mx);
-            den += wgt * ml.y;
-            const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.part_o + (base + i) * D) + c4);
-            num.x += wgt * v.x;
-            num.y += wgt * v.y;
-            num.z += wgt * v.z;
-            num.w += wgt * v.w;
-        }
-        if (has_sink)
-            den += exp2f(sink2 - Mx);
-        float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (den > 0.f) {
-            res.x = num.x / den;
-            res.y = num.y / den;
-            res.z = num.z / den;
-            res.w = num.w / den;
-        }
-        const size_t oidx = ((size_t)r * p.num_q_heads + h) * D + c4 * 4;
-        if (p.out_f32) {
-            *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + oidx) = res;
-        } else {
+    if (has_sink)
+        den += exp2f(sink2 - Mx);
+    float res[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v)
+        res[v] = den > 0.f ? num[v] / den : 0.f;
+    const size_t oidx = ((size_t)r * p.num_q_heads + h) * D + lane * VEC;
+    if (p.out_f32) {
+        float *dst = static_cast<float *>(p.out) + oidx;
+        if constexpr (VEC == 4)
+            *reinterpret_cast<float4 *>(dst) = make_float4(res[0], res[1], res[2], res[3]);
+        else
+            *reinterpret_cast<float2 *>(dst) = make_float2(res[0], res[1]);
+    } else {
+        uint16_t *dst = static_cast<uint16_t *>(p.out) + oidx;
+        if constexpr (VEC == 4) {
             uint2 pk;
-            pk.x = pack_bf16x2(res.x, res.y);
-            pk.y = pack_bf16x2(res.z, res.w);
-            *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.out) + oidx) = pk;
+            pk.x = pack_bf16x2(res[0], res[1]);
+            pk.y = pack_bf16x2(res[2], res[3]);
+            *reinterpret_cast<uint2 *>(dst) = pk;
+        } else {
+            *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(res[0], res[1]);
         }
     }
-    if (threadIdx.x == 0)
-        p.counters[pair] = 0;
 }
 
 // ---------------------------------------------------------------- host side --
@@ -568,7 +656,23 @@ int launch_t(const CUtensorMap &mk, const CUtensorMap &mv, const AttnParams &prm
     if (attr_err != cudaSuccess)
         return check_cuda(attr_err, "cudaFuncSetAttribute(max dynamic smem)");
     kern<<<grid, (NMT + 1) * 32, smem, st>>>(mk, mv, prm);
-    return check_cuda(cudaGetLastError(), "paged_attention_forward launch");
+    int rc = check_cuda(cudaGetLastError(), "paged_attention_forward split launch");
+    if (rc)
+        return rc;
+    // merge, as a programmatic dependent launch (its launch overlaps the split grid's tail)
+    const long long warps = (long long)prm.total_rows * prm.num_q_heads;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((warps + 3) / 4));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return check_cuda(cudaLaunchKernelEx(&cfg, paged_attention_combine_kernel<D>, prm),
+                      "paged_attention_forward merge launch");
 }
 
 // Rows per CTA (G * max rows per sequence) -> (n-tiles per warp, consumer warps).
@@ -585,7 +689,7 @@ int launch_d_bs(int rows, const CUtensorMap &mk, const CUtensorMap &mv, const At
 }
 
 struct WsLayout {
-    size_t counters, ml, o, total;
+    size_t ml, o, total;
 };
 
 WsLayout ws_layout(int32_t num_seqs, int32_t total_q_rows, int32_t num_q_heads, int32_t num_kv_heads,
@@ -593,10 +697,11 @@ WsLayout ws_layout(int32_t num_seqs, int32_t total_q_rows, int32_t num_q_heads, 
 {
     const size_t n_max = (size_t)(max_context_len > 0 ? (max_context_len + kSplitTokens - 1) / kSplitTokens : 1);
     const size_t slots = (size_t)total_q_rows * num_q_heads * n_max;
+    (void)num_seqs;
+    (void)num_kv_heads;
     WsLayout w;
-    w.counters = 0;
-    w.ml = round_up((size_t)num_seqs * num_kv_heads * sizeof(int32_t), 256);
-    w.o = w.ml + round_up(slots * sizeof(float2), 256);
+    w.ml = 0;
+    w.o = round_up(slots * sizeof(float2), 256);
     w.total = w.o + round_up(slots * head_dim * sizeof(float), 256);
     return w;
 }
@@ -713,7 +818,6 @@ extern "C" int paged_attention_forward(const pkv_pool *pool, const void *q, cons
     prm.context_lens = context_lens;
     prm.sinks = sinks;
     prm.out = out;
-    prm.counters = reinterpret_cast<int32_t *>(ws + wl.counters);
     prm.part_ml = reinterpret_cast<float2 *>(ws + wl.ml);
     prm.part_o = reinterpret_cast<float *>(ws + wl.o);
     prm.status = status;
@@ -722,6 +826,7 @@ extern "C" int paged_attention_forward(const pkv_pool *pool, const void *q, cons
     prm.num_blocks = pool->num_blocks;
     prm.num_q_heads = num_q_heads;
     prm.num_kv_heads = Hkv;
+    prm.block_size = BS;
     prm.group = G;
     prm.n_max = n_max;
     prm.max_context_len = max_context_len;
@@ -815,13 +920,6 @@ extern "C" int paged_attention_forward_noalloc(const pkv_pool *pool, const void 
                          need, (size_t)PKV_NOALLOC_SCRATCH_BYTES);
     uint8_t *scratch = nullptr;
     int rc = noalloc_scratch(&scratch);
-    if (rc)
-        return rc;
-    // The merge counters at the start of the workspace must be zero on entry; the
-    // array keeps whatever the previous call left, so clear them on every call.
-    const size_t counter_bytes = round_up((size_t)num_seqs * pool->num_kv_heads * sizeof(int32_t), 256);
-    rc = check_cuda(cudaMemsetAsync(scratch, 0, counter_bytes, static_cast<cudaStream_t>(stream)),
-                    "clear allocation-free scratch counters");
     if (rc)
         return rc;
     return paged_attention_forward(pool, q, q_starts, block_tables, max_blocks_per_seq, context_lens, num_seqs,

@@ -5,7 +5,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#include "../../include/pkv.h"
+#include "pkv.h"
 
 namespace pkv {
 
@@ -28,8 +28,13 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Split-KV chunk: every sequence's keys are cut into chunks of this many tokens,
-// anchored at token 0, whatever the batch looks like.
-constexpr int kSplitTokens = 512;
+// anchored at token 0, whatever the batch looks like.  (A build-time constant: a
+// multiple of 32, at most 2048.)
+#ifndef PKV_SPLIT_TOKENS
+#define PKV_SPLIT_TOKENS 512
+#endif
+constexpr int kSplitTokens = PKV_SPLIT_TOKENS;
+static_assert(kSplitTokens % 32 == 0 && kSplitTokens <= 2048, "split size");
 constexpr int kMaxQHeads = 256;
 constexpr int kMaxGroupRows = 128;  // G * max rows per sequence
 // About two seconds of SM clock: the limit of any wait inside a kernel.
