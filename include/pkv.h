@@ -155,8 +155,9 @@ int paged_attention_workspace_init(void *workspace, size_t workspace_bytes, void
  *   context_lens       int32 [num_seqs], keys in the cache INCLUDING the tokens
  *                      appended for this step (decode token / verify window)
  *   max_context_len    HOST upper bound of context_lens (sizes the grid)
- *   max_q_rows_per_seq HOST upper bound of rows per sequence; G * it <= 128
- *                      where G = num_q_heads / num_kv_heads
+ *   max_q_rows_per_seq HOST upper bound of rows per sequence; G * it <= 8192
+ *                      where G = num_q_heads / num_kv_heads (decode: 1 row;
+ *                      verify windows: up to 16; prefill chunks: more)
  *   kv_head_of_q_head  HOST int32 [num_q_heads] or NULL (NULL: h -> h / G).
  *                      Each KV head must serve exactly G q heads.
  *   sinks              float32 [num_q_heads] or NULL: one logit per q head in

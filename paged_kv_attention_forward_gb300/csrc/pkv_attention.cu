@@ -18,8 +18,10 @@
 //    tile loads (cp.async.bulk.tensor, 128-byte swizzle) of each K and V block
 //    of the split into an NST-stage shared-memory ring, completion tracked by
 //    mbarriers.
-//  * NMT consumer warps, each owning 8 * NN query rows of the (s, g) pair: the G q
-//    heads of KV head g times the W rows of s, flattened row = w * G + head_in_group.
+//  * Consumer warps, each owning 8 * NN query rows of the (s, g) pair: the G q heads
+//    of KV head g times the W rows of s, flattened row = w * G + head_in_group.  A
+//    pair with more rows than one CTA holds is served by adjacent row-group CTAs
+//    that read the same K/V tiles (the second and later from L2).
 //    Per KV block, on mma.sync m16n8k16 (bf16 in, fp32 out) with keys / head dims
 //    on the M side and query rows on the N side (decode has at most 8 rows per KV
 //    head, so nothing is padded to 16 rows): S^T = K q^T, scale, causal / length
@@ -62,6 +64,7 @@ struct AttnParams {
     int32_t *status;
     int32_t num_seqs, max_blocks_per_seq, num_blocks, num_q_heads, num_kv_heads, group, block_size;
     int32_t n_max, max_context_len, max_rows, total_rows;
+    int32_t row_groups;           // CTAs per (s, g, split), each taking 8 * NN * NMT rows
     int32_t causal, out_f32;
     float scale_log2;             // scale * log2(e)
     int16_t q_head_of[kMaxQHeads];  // q head of (kv head g, member j): q_head_of[g*group + j]
@@ -110,7 +113,8 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
     volatile int32_t *s_flag = reinterpret_cast<volatile int32_t *>(empty + NST);
     // s_flag[1]: abort; [2]: blocks issued
 
-    const int pair = blockIdx.x;
+    const int pair = blockIdx.x / p.row_groups;
+    const int rg = blockIdx.x - pair * p.row_groups;
     const int s = pair / p.num_kv_heads;
     const int g = pair - s * p.num_kv_heads;
     const int split = blockIdx.y;
@@ -144,7 +148,10 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
         W = p.max_rows;
     }
     const int M = p.group * W;               // query rows of this (s, g)
-    const int n_act = (M + RPW - 1) / RPW;   // consumer warps with rows
+    const int r_lo = rg * RPW * NMT;         // first row of this CTA's row group
+    if (r_lo >= M)
+        return;
+    const int n_act = (min(M - r_lo, RPW * NMT) + RPW - 1) / RPW;   // consumer warps with rows
 
     const int t0 = split * C;
     const int t1 = min(t0 + C, L);
@@ -226,7 +233,7 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
         // softmax and the output, keys l/4 and l/4+8 of each 16-key m-tile.
         const int cr = 2 * (lane & 3);   // first row of this lane within an n-tile
         const int kr = lane >> 2;        // key (row of the C fragment) within 8
-        const int row_base = warp * RPW;
+        const int row_base = r_lo + warp * RPW;
         uint32_t qf[NN][KS][2];
         int lim[NN][2];
 #pragma unroll
@@ -675,17 +682,22 @@ int launch_t(const CUtensorMap &mk, const CUtensorMap &mv, const AttnParams &prm
                       "paged_attention_forward merge launch");
 }
 
-// Rows per CTA (G * max rows per sequence) -> (n-tiles per warp, consumer warps).
+// Rows of one (s, g) (G * max rows per sequence) -> one consumer warp per CTA with 8
+// rows (decode) or 16 rows in several row-group CTAs (verify windows).  Row-group CTAs
+// of one split are adjacent in launch order and share each K/V tile through L2.
 template <int D, int BS>
-int launch_d_bs(int rows, const CUtensorMap &mk, const CUtensorMap &mv, const AttnParams &prm,
-                dim3 grid, cudaStream_t st)
+int launch_d_bs(int rows, const CUtensorMap &mk, const CUtensorMap &mv, AttnParams prm,
+                long long pairs, int n_max, cudaStream_t st)
 {
-    if (rows <= 8) return launch_t<D, BS, 1, 1>(mk, mv, prm, grid, st);
-    if (rows <= 16) return launch_t<D, BS, 2, 1>(mk, mv, prm, grid, st);
-    if (rows <= 32) return launch_t<D, BS, 2, 2>(mk, mv, prm, grid, st);
-    if (rows <= 64) return launch_t<D, BS, 2, 4>(mk, mv, prm, grid, st);
-    if (rows <= 128) return launch_t<D, BS, 2, 8>(mk, mv, prm, grid, st);
-    return set_error(PKV_ERR_UNSUPPORTED, "internal: %d rows per CTA", rows);
+    const int per_cta = rows <= 8 ? 8 : 16;
+    prm.row_groups = (rows + per_cta - 1) / per_cta;
+    const long long gx = pairs * prm.row_groups;
+    if (gx > 0x7fffffffLL || n_max > 65535)
+        return set_error(PKV_ERR_SHAPE, "paged_attention_forward: grid too large");
+    const dim3 grid((unsigned)gx, (unsigned)n_max);
+    if (rows <= 8)
+        return launch_t<D, BS, 1, 1>(mk, mv, prm, grid, st);
+    return launch_t<D, BS, 2, 1>(mk, mv, prm, grid, st);
 }
 
 struct WsLayout {
@@ -838,15 +850,12 @@ extern "C" int paged_attention_forward(const pkv_pool *pool, const void *q, cons
     prm.scale_log2 = sc * kLog2e;
 
     const int rows = G * max_q_rows_per_seq;
-    const long long gx = (long long)num_seqs * Hkv;
-    if (gx > 0x7fffffffLL || n_max > 65535)
-        return set_error(PKV_ERR_SHAPE, "paged_attention_forward: grid too large");
-    const dim3 grid((unsigned)gx, (unsigned)n_max);
+    const long long pairs = (long long)num_seqs * Hkv;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (D == 64 && BS == 16) return launch_d_bs<64, 16>(rows, mk, mv, prm, grid, st);
-    if (D == 64 && BS == 32) return launch_d_bs<64, 32>(rows, mk, mv, prm, grid, st);
-    if (D == 128 && BS == 16) return launch_d_bs<128, 16>(rows, mk, mv, prm, grid, st);
-    return launch_d_bs<128, 32>(rows, mk, mv, prm, grid, st);
+    if (D == 64 && BS == 16) return launch_d_bs<64, 16>(rows, mk, mv, prm, pairs, n_max, st);
+    if (D == 64 && BS == 32) return launch_d_bs<64, 32>(rows, mk, mv, prm, pairs, n_max, st);
+    if (D == 128 && BS == 16) return launch_d_bs<128, 16>(rows, mk, mv, prm, pairs, n_max, st);
+    return launch_d_bs<128, 32>(rows, mk, mv, prm, pairs, n_max, st);
 }
 
 // ------------------------------------------------ allocation-free variant --

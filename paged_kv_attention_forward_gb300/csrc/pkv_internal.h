@@ -36,7 +36,7 @@ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 constexpr int kSplitTokens = PKV_SPLIT_TOKENS;
 static_assert(kSplitTokens % 32 == 0 && kSplitTokens <= 2048, "split size");
 constexpr int kMaxQHeads = 256;
-constexpr int kMaxGroupRows = 128;  // G * max rows per sequence
+constexpr int kMaxGroupRows = 8192;  // G * max rows per sequence (row-group CTAs of 16 rows)
 // About two seconds of SM clock: the limit of any wait inside a kernel.
 constexpr long long kWaitLimitCycles = 4000000000LL;
 

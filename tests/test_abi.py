@@ -75,7 +75,7 @@ def test_host_validation_without_device(pkv):
     assert _attn(pkv, _pool(), Hq=7) == -2
     assert _attn(pkv, _pool(), dt=5) == -2
     assert _attn(pkv, _pool(), max_ctx=64 * 16 + 1) == -2
-    assert _attn(pkv, _pool(), max_rows=17, Hq=16) == -3            # G*rows = 8*17 > 128
+    assert _attn(pkv, _pool(), max_rows=1025, Hq=16) == -3          # G*rows = 8*1025 > 8192
     assert _attn(pkv, _pool(), q=None) == -1
     assert _attn(pkv, _pool(), out=4096 + 8) == -7
     assert _attn(pkv, _pool(), ws=4096 + 16) == -7

@@ -204,6 +204,31 @@ def test_group_of_eight_with_sixteen_row_windows(pkv):
     assert_close_to_oracle(out.float().cpu().numpy(), ref, what="G8xW16")
 
 
+@pytest.mark.parametrize("d,bs", [(128, 16), (64, 32)])
+def test_chunked_prefill_windows(pkv, d, bs):
+    """Prefill chunks through the same kernel: W new rows appended, then attended causally
+    (TensorSharp advanced features, section on chunked prefill: bounded chunks of 256)."""
+    lens = np.array([256, 700, 1300, 3000])
+    W = np.array([256, 200, 256, 97])
+    b = wl.build_batch(41 + d, name="prefill", lens=lens, n_new=W, q_rows=W, num_q_heads=8, num_kv_heads=2,
+                       head_dim=d, block_size=bs, causal=True)
+    g, out = _gpu_step(pkv, b)
+    _, _, ref = _oracle_step(b)
+    assert_close_to_oracle(out.float().cpu().numpy(), ref, what=f"prefill d{d}")
+    # every prefill row equals its own one-row decode over the keys it may see
+    full = host_bits(out)
+    for s in (1, 3):
+        for w in (0, 63, int(W[s]) - 1):
+            r = int(b.q_starts[s]) + w
+            one = pkv.paged_attention_forward(
+                g["k_pool"], g["v_pool"], g["q"][r:r + 1].contiguous(), dev(np.array([0, 1], np.int32)),
+                g["block_tables"][s:s + 1].contiguous(), dev(np.array([lens[s] - W[s] + w + 1], np.int32)),
+                max_context_len=int(lens[s]), max_q_rows_per_seq=1)
+            torch.cuda.synchronize()
+            assert np.array_equal(host_bits(one)[0], full[r]), f"seq {s} row {w}"
+    _status_ok(pkv)
+
+
 def test_empty_context_and_sequences_without_rows(pkv):
     lens = np.array([0, 5, 9, 0])
     rows = np.array([1, 0, 2, 1])
