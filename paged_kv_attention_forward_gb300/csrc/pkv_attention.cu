@@ -631,20 +631,24 @@ int make_pool_map(CUtensorMap *map, void *base, const pkv_pool &pool)
     return PKV_OK;
 }
 
-#ifndef PKV_STAGES
-#define PKV_STAGES 0
+#ifndef PKV_STAGES_DECODE
+#define PKV_STAGES_DECODE 3
 #endif
-template <int D, int BS>
+#ifndef PKV_STAGES_WIDE
+#define PKV_STAGES_WIDE 4
+#endif
+// Ring depth: decode CTAs (one consumer warp) are many and small, wide-row CTAs hold
+// several consumer warps on one ring.  Chosen by measurement on GB300.
+template <int D, int BS, int NMT>
 constexpr int kStages()
 {
-    // 3 stages of >= 8 KB keep 8 KB x 3 x (8 CTAs) in flight per SM; measured best on GB300
-    return PKV_STAGES > 0 ? PKV_STAGES : (Tile<D, BS>::kTileBytes * 2 >= 8192 ? 3 : 4);
+    return NMT == 1 ? PKV_STAGES_DECODE : PKV_STAGES_WIDE;
 }
 
-template <int D, int BS>
+template <int D, int BS, int NMT>
 size_t smem_bytes()
 {
-    constexpr int NST = kStages<D, BS>();
+    constexpr int NST = kStages<D, BS, NMT>();
     return 1024 + (size_t)NST * 2 * Tile<D, BS>::kTileBytes + 2 * NST * sizeof(uint64_t) + 64;
 }
 
@@ -652,9 +656,9 @@ template <int D, int BS, int NN, int NMT>
 int launch_t(const CUtensorMap &mk, const CUtensorMap &mv, const AttnParams &prm, dim3 grid,
              cudaStream_t st)
 {
-    constexpr int NST = kStages<D, BS>();
+    constexpr int NST = kStages<D, BS, NMT>();
     auto kern = paged_attention_kernel<D, BS, NN, NMT, NST>;
-    const size_t smem = smem_bytes<D, BS>();
+    const size_t smem = smem_bytes<D, BS, NMT>();
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -685,11 +689,17 @@ int launch_t(const CUtensorMap &mk, const CUtensorMap &mv, const AttnParams &prm
 // Rows of one (s, g) (G * max rows per sequence) -> one consumer warp per CTA with 8
 // rows (decode) or 16 rows in several row-group CTAs (verify windows).  Row-group CTAs
 // of one split are adjacent in launch order and share each K/V tile through L2.
+#ifndef PKV_WIDE_NN
+#define PKV_WIDE_NN 1
+#endif
+#ifndef PKV_WIDE_NMT
+#define PKV_WIDE_NMT 3
+#endif
 template <int D, int BS>
 int launch_d_bs(int rows, const CUtensorMap &mk, const CUtensorMap &mv, AttnParams prm,
                 long long pairs, int n_max, cudaStream_t st)
 {
-    const int per_cta = rows <= 8 ? 8 : 16;
+    const int per_cta = rows <= 8 ? 8 : 8 * PKV_WIDE_NN * PKV_WIDE_NMT;
     prm.row_groups = (rows + per_cta - 1) / per_cta;
     const long long gx = pairs * prm.row_groups;
     if (gx > 0x7fffffffLL || n_max > 65535)
@@ -697,7 +707,7 @@ int launch_d_bs(int rows, const CUtensorMap &mk, const CUtensorMap &mv, AttnPara
     const dim3 grid((unsigned)gx, (unsigned)n_max);
     if (rows <= 8)
         return launch_t<D, BS, 1, 1>(mk, mv, prm, grid, st);
-    return launch_t<D, BS, 2, 1>(mk, mv, prm, grid, st);
+    return launch_t<D, BS, PKV_WIDE_NN, PKV_WIDE_NMT>(mk, mv, prm, grid, st);
 }
 
 struct WsLayout {
