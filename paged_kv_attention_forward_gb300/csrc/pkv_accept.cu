@@ -59,7 +59,7 @@ argmax_chunks_kernel(const float *__restrict__ logits, int vocab, int chunk, int
         // lo and hi are multiples of 4 except possibly hi == vocab (vocab % 4 == 0 when vec_ok)
         const float4 *row4 = reinterpret_cast<const float4 *>(row);
         const int lo4 = lo >> 2, hi4 = hi >> 2;
-#pragma unroll 4
+#pragma unroll 8
         for (int i = lo4 + threadIdx.x; i < hi4; i += kArgmaxThreads) {
             const float4 x = __ldcs(row4 + i);
             const int base = i << 2;
@@ -140,9 +140,9 @@ accept_walk_kernel(const float2 *__restrict__ part, int n_chunks, const int32_t 
 
 int accept_chunks(int32_t total_rows, int32_t vocab, int sms)
 {
-    // enough CTAs to cover the GPU about twice, slices of at least 8192 values
+    // enough CTAs to cover the GPU about four times, slices of at least 8192 values
     const int max_chunks = (vocab + 8191) / 8192;
-    int want = (2 * sms + total_rows - 1) / (total_rows > 0 ? total_rows : 1);
+    int want = (4 * sms + total_rows - 1) / (total_rows > 0 ? total_rows : 1);
     if (want < 1)
         want = 1;
     return want < max_chunks ? want : (max_chunks > 0 ? max_chunks : 1);

@@ -453,7 +453,7 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
 // the split kernel: it may start early and waits for the partials with
 // griddepcontrol.wait.
 template <int D>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(128, 7)
 paged_attention_combine_kernel(const AttnParams p)
 {
     constexpr int VEC = D / 32;   // output values per lane
@@ -486,8 +486,16 @@ paged_attention_combine_kernel(const AttnParams p)
     const int n = lim > 0 ? (lim + kSplitTokens - 1) / kSplitTokens : 0;
     const size_t base = ((size_t)r * p.num_q_heads + h) * p.n_max;
 
+    // the n partial rows of (r, h) are contiguous: ask L2 for all of them at once, so the
+    // batched loop below waits for one DRAM round trip instead of one per batch
+    {
+        const char *region = reinterpret_cast<const char *>(p.part_o + base * D);
+        const int lines = (n * D * (int)sizeof(float) + 127) / 128;
+        for (int i = lane; i < lines; i += 32)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(region + (size_t)i * 128));
+    }
     // lane i holds (m, l) of partials i, i + 32, ...; the sums below still run in split order
-    constexpr int MAXC = 4;   // partials cached per lane (n <= 128); longer rows reload (m, l)
+    constexpr int MAXC = 2;   // partials cached per lane (n <= 64); longer rows reload (m, l)
     float2 mlc[MAXC];
 #pragma unroll
     for (int c = 0; c < MAXC; ++c) {
@@ -521,7 +529,7 @@ paged_attention_combine_kernel(const AttnParams p)
     for (int v = 0; v < VEC; ++v)
         num[v] = 0.f;
     const float *src0 = p.part_o + base * D + lane * VEC;
-    constexpr int BATCH = 16;   // partial rows in flight per lane
+    constexpr int BATCH = 8;    // partial rows in flight per lane (7 CTAs of 4 warps fit per SM)
     for (int i0 = 0; i0 < n; i0 += BATCH) {
         float x[BATCH][VEC];
 #pragma unroll
