@@ -374,7 +374,7 @@ def time_oracle_step(sub: wl.PagedBatch, threads: int):
     return time.perf_counter() - t
 
 
-def cpu_baseline(b: wl.PagedBatch, budget_s: float = 10.0, max_runs: int = 10):
+def cpu_baseline(b: wl.PagedBatch, budget_s: float = 12.0, max_runs: int = 60):
     """The oracle, as it stands, on the whole batch, repeated for about budget_s seconds."""
     import oracle
     oracle.build_oracle()
