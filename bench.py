@@ -153,6 +153,27 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ------------------------------------------------------------- multi-rank --
+def replica_seed(seed: int, rank: int) -> int:
+    """Each rank runs its own replica of the workload (weak scaling): same shape, own data."""
+    return seed + rank
+
+
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise maximum of per-rank timings (the job is as slow as its slowest rank)."""
+    if dist is None:
+        return list(values)
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(units_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Units all ranks processed per second, each rank processing units_per_rank per step."""
+    return world * units_per_rank / (ms_per_step * 1e-3)
+
+
 # ------------------------------------------------------------------ our arm --
 def run_ours(args, rank, world, local_rank):
     import torch
@@ -161,7 +182,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     layers = 40 if args.workload == "ministral_decode" else 1
-    b = wl.make_workload(args.workload, seed=args.seed + rank, layers=layers, num_seqs=args.num_seqs)
+    b = wl.make_workload(args.workload, seed=replica_seed(args.seed, rank), layers=layers,
+                         num_seqs=args.num_seqs)
     acct = algorithmic_bytes(b, layers)
 
     def d_bf16(a):
@@ -304,10 +326,8 @@ def run_ours(args, rank, world, local_rank):
     ms_per_step = ms_total / args.steps
     e2e_ms_per_step = e2e_ms / e2e_steps
     attn_avg_ms = statistics.fmean(attn_ms)
-    if dist is not None:
-        t = torch.tensor([ms_per_step, e2e_ms_per_step, attn_avg_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_per_step, e2e_ms_per_step, attn_avg_ms = t.tolist()
+    ms_per_step, e2e_ms_per_step, attn_avg_ms = max_over_ranks(
+        [ms_per_step, e2e_ms_per_step, attn_avg_ms], dist, dev)
     if rank != 0:
         return None
 
@@ -319,9 +339,9 @@ def run_ours(args, rank, world, local_rank):
     per_launch_bytes = acct["attention"] / layers
     achieved = per_launch_bytes / (attn_avg_ms * 1e-3) / 1e9
     traffic = stored_traffic("paged_attention", args.workload)
-    value = world * acct["step"] / (ms_per_step * 1e-3) / 1e9
-    e2e_value = world * acct["step"] / (e2e_ms_per_step * 1e-3) / 1e9
-    rows_per_s = world * acct["rows"] * layers / (ms_per_step * 1e-3)
+    value = whole_job_rate(acct["step"], world, ms_per_step) / 1e9
+    e2e_value = whole_job_rate(acct["step"], world, e2e_ms_per_step) / 1e9
+    rows_per_s = whole_job_rate(acct["rows"] * layers, world, ms_per_step)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
