@@ -59,12 +59,14 @@ def _load():
             lib.oracle_paged_kv_append.argtypes = [P, P, i32, i32, i32, i32, P, i32, P, P, P, P, i32]
             lib.oracle_paged_kv_append.restype = ctypes.c_int
             lib.oracle_paged_attention.argtypes = [P, P, i32, i32, i32, i32, P, P, P, i32, P, i32,
-                                                   i32, P, P, i32, ctypes.c_double, P, i32]
+                                                   i32, P, P, i32, P, ctypes.c_double, P, i32]
             lib.oracle_paged_attention.restype = ctypes.c_int
             lib.oracle_argmax_rows.argtypes = [P, ctypes.c_int64, i32, P]
             lib.oracle_argmax_rows.restype = None
             lib.oracle_spec_accept_greedy.argtypes = [P, i32, P, P, i32, P, P, P]
             lib.oracle_spec_accept_greedy.restype = None
+            lib.oracle_spec_accept_tree_greedy.argtypes = [P, i32, P, P, P, i32, P, P, P, P]
+            lib.oracle_spec_accept_tree_greedy.restype = ctypes.c_int
             _lib = lib
         return _lib
 
@@ -103,13 +105,15 @@ def paged_kv_append(k_pool, v_pool, block_tables, context_lens_old, new_starts, 
 
 def paged_attention(k_pool, v_pool, q, q_starts, block_tables, context_lens,
                     kv_head_of_q_head=None, sinks=None, causal=False, scale=None,
-                    num_threads=None):
+                    num_threads=None, tree_masks=None):
     """Float64 attention over the paged pool; returns float64 [R, H_q, head_dim].
 
     q: uint16 (bf16 bits) [R, H_q, head_dim]; q_starts: int32 [S+1];
     context_lens: int32 [S] (keys in the cache, including any just appended);
     kv_head_of_q_head: int32 [H_q] or None (contiguous groups);
     sinks: float32 [H_q] or None; scale: None means 1/sqrt(head_dim).
+    tree_masks: uint32 [R] or None: bit i of row r = row r sees window token i
+    (the sequence's last W keys); overrides `causal`.
     """
     lib = _load()
     nb, hkv, bs, d = k_pool.shape
@@ -121,13 +125,14 @@ def paged_attention(k_pool, v_pool, q, q_starts, block_tables, context_lens,
     cl = _c(context_lens, np.int32)
     hm = None if kv_head_of_q_head is None else _c(kv_head_of_q_head, np.int32)
     sk = None if sinks is None else _c(sinks, np.float32)
+    tm = None if tree_masks is None else _c(tree_masks, np.uint32)
     if scale is None:
         scale = 1.0 / np.sqrt(d)
     out = np.zeros((r, hq, d), dtype=np.float64)
     rc = lib.oracle_paged_attention(
         _ptr(_c(k_pool, np.uint16)), _ptr(_c(v_pool, np.uint16)), nb, bs, hkv, d,
         _ptr(q), _ptr(qs), _ptr(bt), bt.shape[1], _ptr(cl), cl.shape[0], hq, _ptr(hm),
-        _ptr(sk), int(bool(causal)), float(scale), _ptr(out),
+        _ptr(sk), int(bool(causal)), _ptr(tm), float(scale), _ptr(out),
         int(num_threads or default_num_threads()))
     if rc != 0:
         raise ValueError(f"oracle_paged_attention failed with status {rc}")
@@ -158,3 +163,25 @@ def spec_accept_greedy(logits, q_starts, draft_tokens):
     ot = np.empty(rows, dtype=np.int32)
     lib.oracle_spec_accept_greedy(_ptr(lg), vocab, _ptr(qs), _ptr(dr), s, _ptr(am), _ptr(al), _ptr(ot))
     return am, al, ot
+
+
+def spec_accept_tree_greedy(logits, q_starts, draft_tokens, parents):
+    """Greedy accept over draft trees: returns (argmax [R], accept_len [S], out_tokens [R],
+    accepted_rows [R]), all int32.  parents[r]: parent node index of row r within its
+    sequence (row 0 of each sequence is the root; its entry is ignored)."""
+    lib = _load()
+    lg = _c(logits, np.float32)
+    rows, vocab = lg.shape
+    qs = _c(q_starts, np.int32)
+    dr = _c(draft_tokens, np.int32)
+    pa = _c(parents, np.int32)
+    s = qs.shape[0] - 1
+    am = np.empty(rows, dtype=np.int32)
+    al = np.empty(s, dtype=np.int32)
+    ot = np.empty(rows, dtype=np.int32)
+    ar = np.empty(rows, dtype=np.int32)
+    rc = lib.oracle_spec_accept_tree_greedy(_ptr(lg), vocab, _ptr(qs), _ptr(dr), _ptr(pa), s, _ptr(am),
+                                            _ptr(al), _ptr(ot), _ptr(ar))
+    if rc != 0:
+        raise ValueError(f"oracle_spec_accept_tree_greedy failed with status {rc}")
+    return am, al, ot, ar

@@ -106,8 +106,12 @@ int oracle_paged_kv_append(uint16_t *k_pool, uint16_t *v_pool,
  * (logical token t -> block block_tables[s][t / B], slot t % B).
  * Everything is float64.  out is float64 [R][H_q][head_dim].
  * kv_head_of_q_head may be NULL (contiguous groups); sinks may be NULL.
+ * Tree verify (TensorFold article, "接受规则": the verify rows may form a draft
+ * tree): with tree_masks != NULL, row w of sequence s sees every cached key
+ * t < L - W and the window key L - W + i exactly when bit i of tree_masks[r]
+ * is set (its ancestors and itself); `causal` is then ignored.
  * Returns 0, -1 (position beyond table), -2 (block id out of range),
- * -3 (bad head map), -4 (out of memory).
+ * -3 (bad head map), -4 (out of memory), -5 (tree window wider than 32).
  */
 int oracle_paged_attention(const uint16_t *k_pool, const uint16_t *v_pool,
                            int32_t num_blocks, int32_t block_size,
@@ -116,8 +120,8 @@ int oracle_paged_attention(const uint16_t *k_pool, const uint16_t *v_pool,
                            const int32_t *block_tables, int32_t max_blocks_per_seq,
                            const int32_t *context_lens, int32_t num_seqs,
                            int32_t num_q_heads, const int32_t *kv_head_of_q_head,
-                           const float *sinks, int32_t causal, double scale,
-                           double *out, int32_t num_threads)
+                           const float *sinks, int32_t causal, const uint32_t *tree_masks,
+                           double scale, double *out, int32_t num_threads)
 {
     const int32_t B = block_size, D = head_dim, Hkv = num_kv_heads, Hq = num_q_heads;
     if (Hkv <= 0 || Hq % Hkv != 0)
@@ -130,6 +134,8 @@ int oracle_paged_attention(const uint16_t *k_pool, const uint16_t *v_pool,
     }
     /* validate every table entry that will be read */
     for (int32_t s = 0; s < num_seqs; ++s) {
+        if (tree_masks && q_starts[s + 1] - q_starts[s] > 32)
+            return -5;
         int64_t L = context_lens[s];
         int64_t nblk = (L + B - 1) / B;
         if (nblk > max_blocks_per_seq)
@@ -178,8 +184,11 @@ int oracle_paged_attention(const uint16_t *k_pool, const uint16_t *v_pool,
         for (int32_t w = 0; w < W; ++w) {
             const int64_t r = (int64_t)row0 + w;
             int64_t n = causal ? L - W + w + 1 : L;
+            if (tree_masks)
+                n = L;
             if (n < 0) n = 0;
             if (n > L) n = L;
+            const int64_t win0 = L - W;   /* first key of the verify window */
             for (int32_t h = 0; h < Hq; ++h) {
                 int32_t gh = kv_head_of_q_head ? kv_head_of_q_head[h] : h / group;
                 if (gh != g)
@@ -188,6 +197,10 @@ int oracle_paged_attention(const uint16_t *k_pool, const uint16_t *v_pool,
                 double *o = out + ((size_t)r * Hq + h) * D;
                 double M = -INFINITY;
                 for (int64_t t = 0; t < n; ++t) {
+                    if (tree_masks && t >= win0 && !((tree_masks[r] >> (t - win0)) & 1u)) {
+                        x[t] = -INFINITY;   /* not an ancestor of this node: invisible */
+                        continue;
+                    }
                     double dot = 0.0;
                     for (int32_t k = 0; k < D; ++k)
                         dot += bf16_bits_to_f64(qv[k]) * K[t * D + k];
@@ -203,6 +216,8 @@ int oracle_paged_attention(const uint16_t *k_pool, const uint16_t *v_pool,
                 for (int32_t k = 0; k < D; ++k)
                     o[k] = 0.0;
                 for (int64_t t = 0; t < n; ++t) {
+                    if (x[t] == -INFINITY)
+                        continue;
                     double e = exp(x[t] - M);
                     den += e;
                     for (int32_t k = 0; k < D; ++k)
@@ -270,4 +285,59 @@ void oracle_spec_accept_greedy(const float *logits, int32_t vocab,
             out_tokens[r0 + j] = draft_tokens[r0 + j + 1];
         out_tokens[r0 + n] = argmax_out[r0 + n];
     }
+}
+
+/*
+ * Greedy accept over a draft tree (TensorFold article, "接受规则：GPU 上的 accept
+ * 内核": the verify rows form a chain or a tree; the accepted path follows, from
+ * the root, the child whose token equals the target's choice).  Sequence s owns
+ * nodes 0..W-1 (rows q_starts[s] + j); node 0 is the last committed token, node
+ * j >= 1 carries draft token d_j and has parent parents[r] (a node index < j).
+ * From u = 0: a_u = argmax of row u; the next node is the lowest-index child c
+ * of u with d_c == a_u; the walk stops at a node with no such child.
+ * accept_len[s] = the number of accepted drafts n; out_tokens holds their tokens
+ * then a_u of the final node (n + 1 tokens), then -1; accepted_rows holds the
+ * accepted node indices (n of them), then -1.  A chain is parents[j] = j - 1.
+ * Returns 0, or -1 if a parent index is not smaller than its node's index.
+ */
+int oracle_spec_accept_tree_greedy(const float *logits, int32_t vocab,
+                                   const int32_t *q_starts, const int32_t *draft_tokens,
+                                   const int32_t *parents, int32_t num_seqs,
+                                   int32_t *argmax_out, int32_t *accept_len,
+                                   int32_t *out_tokens, int32_t *accepted_rows)
+{
+    const int64_t total = q_starts[num_seqs];
+    oracle_argmax_rows(logits, total, vocab, argmax_out);
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        const int32_t r0 = q_starts[s], W = q_starts[s + 1] - q_starts[s];
+        if (W <= 0) {
+            accept_len[s] = -1;
+            continue;
+        }
+        for (int32_t j = 1; j < W; ++j)
+            if (parents[r0 + j] < 0 || parents[r0 + j] >= j)
+                return -1;
+        for (int32_t j = 0; j < W; ++j) {
+            out_tokens[r0 + j] = -1;
+            accepted_rows[r0 + j] = -1;
+        }
+        int32_t u = 0, n = 0;
+        for (;;) {
+            int32_t next = -1;
+            for (int32_t c = u + 1; c < W; ++c)
+                if (parents[r0 + c] == u && draft_tokens[r0 + c] == argmax_out[r0 + u]) {
+                    next = c;
+                    break;
+                }
+            if (next < 0)
+                break;
+            out_tokens[r0 + n] = draft_tokens[r0 + next];
+            accepted_rows[r0 + n] = next;
+            ++n;
+            u = next;
+        }
+        out_tokens[r0 + n] = argmax_out[r0 + u];
+        accept_len[s] = n;
+    }
+    return 0;
 }
