@@ -63,7 +63,7 @@ def algorithmic_bytes(b: wl.PagedBatch, layers: int = 1) -> dict:
     attn = kv + q_out + table
     accept = 0
     if b.logits is not None:
-        accept = b.logits.size * 4 + R * 4 * 3
+        accept = b.logits.size * 4 + R * 4 * (3 if b.parents is None else 5)
     return dict(attention=attn * layers, append=append * layers, accept=accept,
                 step=(attn + append) * layers + accept, kv_unique=kv * layers,
                 kv_logical=logical_kv * layers, rows=R)
@@ -204,13 +204,15 @@ def run_ours(args, rank, world, local_rank):
                                      b.head_dim, b.max_context_len, dev)
     logits = drafts = acc_ws = None
     acc_out = None
+    tree = b.tree_masks is not None
+    tree_masks = d(b.tree_masks.view(np.int32)) if tree else None
+    parents = d(b.parents) if tree else None
     if b.logits is not None:
         logits, drafts = d(b.logits), d(b.draft_tokens)
         acc_ws = torch.empty(pkv.spec_accept_workspace_size(b.total_q_rows, b.logits.shape[1]),
                              dtype=torch.uint8, device=dev)
-        acc_out = (torch.empty(b.total_q_rows, dtype=torch.int32, device=dev),
-                   torch.empty(b.num_seqs, dtype=torch.int32, device=dev),
-                   torch.empty(b.total_q_rows, dtype=torch.int32, device=dev))
+        acc_out = tuple(torch.empty(n, dtype=torch.int32, device=dev)
+                        for n in (b.total_q_rows, b.num_seqs, b.total_q_rows, b.total_q_rows))
     has_append = int(b.new_starts[-1]) > 0
     max_ctx, max_rows = b.max_context_len, b.max_q_rows_per_seq
     stream = torch.cuda.current_stream()
@@ -224,13 +226,23 @@ def run_ours(args, rank, world, local_rank):
                                     stream=stream)
             if ev_pairs is not None:
                 ev_pairs[li][0].record(stream)
-            pkv.paged_attention_forward(pools[i][0], pools[i][1], qs[i], q_starts, tables, lens,
-                                        max_context_len=max_ctx, max_q_rows_per_seq=max_rows, sinks=sinks,
-                                        causal=b.causal, out=outs[i], workspace=ws, stream=stream)
+            if tree:
+                pkv.paged_tree_attention_forward(pools[i][0], pools[i][1], qs[i], q_starts, tables, lens,
+                                                 tree_masks, max_context_len=max_ctx,
+                                                 max_q_rows_per_seq=max_rows, sinks=sinks, out=outs[i],
+                                                 workspace=ws, stream=stream)
+            else:
+                pkv.paged_attention_forward(pools[i][0], pools[i][1], qs[i], q_starts, tables, lens,
+                                            max_context_len=max_ctx, max_q_rows_per_seq=max_rows, sinks=sinks,
+                                            causal=b.causal, out=outs[i], workspace=ws, stream=stream)
             if ev_pairs is not None:
                 ev_pairs[li][1].record(stream)
                 li += 1
-        if logits is not None:
+        if logits is not None and tree:
+            pkv.spec_accept_tree_greedy(logits, q_starts, drafts, parents, argmax_out=acc_out[0],
+                                        accept_len=acc_out[1], out_tokens=acc_out[2], accepted_rows=acc_out[3],
+                                        workspace=acc_ws, stream=stream)
+        elif logits is not None:
             pkv.spec_accept_greedy(logits, q_starts, drafts, argmax_out=acc_out[0], accept_len=acc_out[1],
                                    out_tokens=acc_out[2], workspace=acc_ws, stream=stream)
         return li
@@ -292,6 +304,10 @@ def run_ours(args, rank, world, local_rank):
         h_acc = [torch.empty(t.shape, dtype=torch.int32).pin_memory() for t in acc_out]
         h2d += h_logits.numel() * 4 + h_drafts.numel() * 4
         d2h += sum(t.numel() * 4 for t in h_acc)
+    if tree:
+        h_inputs += [pin(b.tree_masks.view(np.int32)), pin(b.parents)]
+        d_inputs += [tree_masks, parents]
+        h2d += 2 * b.total_q_rows * 4
 
     def e2e_step():
         for hsrc, ddst in zip(h_inputs, d_inputs):
@@ -388,8 +404,10 @@ def time_oracle_step(sub: wl.PagedBatch, threads: int):
         oracle.paged_kv_append(k, v, sub.block_tables, sub.context_lens_old, sub.new_starts,
                                sub.k_new[0], sub.v_new[0])
     oracle.paged_attention(k, v, sub.q[0], sub.q_starts, sub.block_tables, sub.context_lens, sinks=sub.sinks,
-                           causal=sub.causal, num_threads=threads)
-    if sub.logits is not None:
+                           causal=sub.causal, num_threads=threads, tree_masks=sub.tree_masks)
+    if sub.logits is not None and sub.parents is not None:
+        oracle.spec_accept_tree_greedy(sub.logits, sub.q_starts, sub.draft_tokens, sub.parents)
+    elif sub.logits is not None:
         oracle.spec_accept_greedy(sub.logits, sub.q_starts, sub.draft_tokens)
     return time.perf_counter() - t
 

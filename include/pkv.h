@@ -2,7 +2,7 @@
  * pkv.h -- C ABI of libpkv.so: batched paged-KV attention for continuous
  * batching on NVIDIA GB300 (sm_103a).
  *
- * Three operations, each one or two hand-written CUDA kernels:
+ * Three operations (with tree variants), each one or two hand-written CUDA kernels:
  *   paged_kv_append          scatter new tokens' K/V rows into the block pool
  *   paged_attention_forward  decode / causal verify-window attention over K/V
  *                            gathered through per-sequence block tables, with
@@ -76,7 +76,8 @@ enum {
                                   past max_context_len                                    */
     PKV_DEV_TOO_MANY_ROWS = 4, /* a sequence with more rows than max_q_rows_per_seq       */
     PKV_DEV_WORKSPACE = 8,     /* (reserved)                                              */
-    PKV_DEV_TIMEOUT = 16       /* a bounded wait expired                                  */
+    PKV_DEV_TIMEOUT = 16,      /* a bounded wait expired                                  */
+    PKV_DEV_BAD_TREE = 32      /* a draft tree whose parent indices are not topological   */
 };
 
 /* One layer's K/V block pool (host struct holding device pointers).
@@ -186,6 +187,27 @@ int paged_attention_forward(const pkv_pool *pool,
                             void *out, int32_t out_dtype,
                             void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * Tree verify attention (TensorFold article, "接受规则：GPU 上的 accept 内核": the
+ * verify rows form a chain or a tree of drafts).  Same computation and
+ * arguments as paged_attention_forward, except that row w of sequence s sees
+ * every cached key t < L - W and the window key L - W + i exactly when bit i of
+ * tree_masks[q_starts[s] + w] is set (the node's ancestors and itself).  A chain
+ * is the mask (1 << (w + 1)) - 1 and gives the causal window bit for bit.
+ *   tree_masks          uint32 [total_q_rows]
+ *   max_q_rows_per_seq  at most 32
+ */
+int paged_tree_attention_forward(const pkv_pool *pool,
+                                 const void *q, const int32_t *q_starts,
+                                 const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t *context_lens,
+                                 int32_t num_seqs, int32_t total_q_rows,
+                                 int32_t max_context_len, int32_t max_q_rows_per_seq,
+                                 int32_t num_q_heads, const int32_t *kv_head_of_q_head,
+                                 const float *sinks, const uint32_t *tree_masks, float scale,
+                                 void *out, int32_t out_dtype,
+                                 void *workspace, size_t workspace_bytes, void *stream);
+
 /* Bytes of workspace spec_accept_greedy needs (a multiple of 256). */
 size_t spec_accept_workspace_size(int32_t total_rows, int32_t vocab);
 
@@ -247,13 +269,36 @@ int paged_attention_forward_noalloc(const pkv_pool *pool,
                                     const float *sinks, int32_t causal, float scale,
                                     void *out, int32_t out_dtype, void *stream);
 
+/*
+ * Greedy accept over draft trees (TensorFold article, "接受规则：GPU 上的 accept
+ * 内核": from the root, follow the child whose token equals the target's
+ * choice).  Sequence s owns nodes j = 0..W-1 at rows q_starts[s] + j; node 0 is
+ * the last committed token; node j >= 1 carries draft token d_j and has parent
+ * node parents[q_starts[s] + j] in [0, j).  From u = 0, with a_u the argmax of
+ * row u (ties to the lowest id), the walk moves to the lowest-index child c of
+ * u with d_c == a_u and stops at a node with no such child.
+ *   accept_len[s]    number of accepted drafts n (-1: no rows, or a bad tree,
+ *                    which also sets PKV_DEV_BAD_TREE)
+ *   out_tokens       the n accepted drafts, then a_u of the final node, then -1
+ *   accepted_rows    the n accepted node indices (rows to keep), then -1
+ * At most 1024 nodes per sequence.  A chain (parents[j] = j - 1) gives
+ * spec_accept_greedy's result.  Uses spec_accept_workspace_size bytes of
+ * workspace; launches two kernels.
+ */
+int spec_accept_tree_greedy(const float *logits, int32_t vocab,
+                            const int32_t *q_starts, const int32_t *draft_tokens,
+                            const int32_t *parents, int32_t num_seqs, int32_t total_rows,
+                            int32_t *argmax_out, int32_t *accept_len, int32_t *out_tokens,
+                            int32_t *accepted_rows, void *workspace, size_t workspace_bytes,
+                            void *stream);
+
 /* Text of the calling thread's last error ("" if none). */
 const char *pkv_last_error_string(void);
 
 /*
  * Synchronise `stream`, then read and clear the device status word of the
  * current device.  Returns PKV_OK, PKV_ERR_BAD_BLOCK (bad block id or table
- * overrun), PKV_ERR_SHAPE (too many rows), PKV_ERR_WORKSPACE, PKV_ERR_TIMEOUT,
+ * overrun), PKV_ERR_SHAPE (too many rows, or a bad draft tree), PKV_ERR_TIMEOUT,
  * or PKV_ERR_CUDA; *bits (if not NULL) receives the raw PKV_DEV_* bits.
  */
 int pkv_device_status(void *stream, int32_t *bits);

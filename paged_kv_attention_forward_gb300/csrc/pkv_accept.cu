@@ -138,6 +138,78 @@ accept_walk_kernel(const float2 *__restrict__ part, int n_chunks, const int32_t 
         accept_len[s] = n;
 }
 
+constexpr int kTreeMaxNodes = 1024;
+
+// Greedy accept over draft trees: one warp per sequence.  The slices of each row are
+// merged into argmax_out (and shared memory), then from the root the walk takes, at
+// node u, the lowest-index child c (parents[c] == u) whose draft equals a_u, found by
+// a ballot over 32 candidates at a time.
+__global__ void __launch_bounds__(32)
+accept_tree_walk_kernel(const float2 *__restrict__ part, int n_chunks, const int32_t *__restrict__ q_starts,
+                        const int32_t *__restrict__ drafts, const int32_t *__restrict__ parents,
+                        int total_rows, int32_t *__restrict__ argmax_out, int32_t *__restrict__ accept_len,
+                        int32_t *__restrict__ out_tokens, int32_t *__restrict__ accepted_rows,
+                        int32_t *__restrict__ status)
+{
+    __shared__ int32_t a_s[kTreeMaxNodes];
+    const int s = blockIdx.x, lane = threadIdx.x;
+    const int r0 = q_starts[s], W = q_starts[s + 1] - r0;
+    if (W <= 0) {
+        if (lane == 0)
+            accept_len[s] = -1;
+        return;
+    }
+    bool bad = r0 < 0 || r0 + W > total_rows || W > kTreeMaxNodes;
+    for (int j = 1 + lane; !bad && j < W; j += 32)
+        if (parents[r0 + j] < 0 || parents[r0 + j] >= j)
+            bad = true;
+    if (__any_sync(0xffffffffu, bad)) {
+        if (lane == 0) {
+            accept_len[s] = -1;
+            atomicOr(status, PKV_DEV_BAD_TREE);
+        }
+        return;
+    }
+    for (int j = lane; j < W; j += 32) {
+        Best b = {-INFINITY, kNoIndex};
+        const float2 *pr = part + (size_t)(r0 + j) * n_chunks;
+        for (int c = 0; c < n_chunks; ++c) {
+            const float2 x = pr[c];
+            b = better(b, Best{x.x, __float_as_int(x.y)});
+        }
+        const int a = b.i == kNoIndex ? 0 : b.i;
+        a_s[j] = a;
+        argmax_out[r0 + j] = a;
+        out_tokens[r0 + j] = -1;
+        accepted_rows[r0 + j] = -1;
+    }
+    __syncwarp();
+    int u = 0, n = 0;
+    for (;;) {
+        const int target = a_s[u];
+        int next = -1;
+        for (int base = u + 1; base < W && next < 0; base += 32) {
+            const int c = base + lane;
+            const bool hit = c < W && parents[r0 + c] == u && drafts[r0 + c] == target;
+            const unsigned m = __ballot_sync(0xffffffffu, hit);
+            if (m)
+                next = base + __ffs(m) - 1;
+        }
+        if (next < 0)
+            break;
+        if (lane == 0) {
+            out_tokens[r0 + n] = drafts[r0 + next];
+            accepted_rows[r0 + n] = next;
+        }
+        ++n;
+        u = next;
+    }
+    if (lane == 0) {
+        out_tokens[r0 + n] = a_s[u];
+        accept_len[s] = n;
+    }
+}
+
 int accept_chunks(int32_t total_rows, int32_t vocab, int sms)
 {
     // enough CTAs to cover the GPU about four times, slices of at least 8192 values
@@ -200,4 +272,47 @@ extern "C" int spec_accept_greedy(const float *logits, int32_t vocab, const int3
     accept_walk_kernel<<<num_seqs, 32, 0, st>>>(part, n_chunks, q_starts, draft_tokens, total_rows, argmax_out,
                                                 accept_len, out_tokens, status);
     return check_cuda(cudaGetLastError(), "spec_accept_greedy walk launch");
+}
+
+extern "C" int spec_accept_tree_greedy(const float *logits, int32_t vocab, const int32_t *q_starts,
+                                       const int32_t *draft_tokens, const int32_t *parents, int32_t num_seqs,
+                                       int32_t total_rows, int32_t *argmax_out, int32_t *accept_len,
+                                       int32_t *out_tokens, int32_t *accepted_rows, void *workspace,
+                                       size_t workspace_bytes, void *stream)
+{
+    using namespace pkv;
+    clear_error();
+    if (num_seqs < 0 || total_rows < 0 || vocab <= 0)
+        return set_error(PKV_ERR_SHAPE, "spec_accept_tree_greedy: bad sizes (num_seqs %d, rows %d, vocab %d)",
+                         num_seqs, total_rows, vocab);
+    if (num_seqs == 0)
+        return PKV_OK;
+    if (!q_starts || !accept_len || (total_rows > 0 && (!logits || !draft_tokens || !parents || !argmax_out ||
+                                                        !out_tokens || !accepted_rows || !workspace)))
+        return set_error(PKV_ERR_NULL, "spec_accept_tree_greedy: a required pointer is NULL");
+    if (total_rows > 0 && !aligned16(logits))
+        return set_error(PKV_ERR_ALIGN, "spec_accept_tree_greedy: logits must be 16-byte aligned");
+    if (workspace_bytes < spec_accept_workspace_size(total_rows, vocab))
+        return set_error(PKV_ERR_WORKSPACE, "spec_accept_tree_greedy: workspace %zu < %zu bytes",
+                         workspace_bytes, spec_accept_workspace_size(total_rows, vocab));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int n_chunks = accept_chunks(total_rows, vocab, sm_count());
+    float2 *part = static_cast<float2 *>(workspace);
+    if (total_rows > 0) {
+        if (total_rows > 65535)
+            return set_error(PKV_ERR_SHAPE, "spec_accept_tree_greedy: at most 65535 rows per call");
+        int chunk = (vocab + n_chunks - 1) / n_chunks;
+        chunk = (chunk + 3) & ~3;
+        argmax_chunks_kernel<<<dim3(n_chunks, total_rows), kArgmaxThreads, 0, st>>>(logits, vocab, chunk, n_chunks,
+                                                                                   part, (vocab % 4) == 0);
+        const int rc = check_cuda(cudaGetLastError(), "spec_accept_tree_greedy argmax launch");
+        if (rc)
+            return rc;
+    }
+    int32_t *status = device_status_word();
+    if (!status)
+        return set_error(PKV_ERR_CUDA, "spec_accept_tree_greedy: no device status word");
+    accept_tree_walk_kernel<<<num_seqs, 32, 0, st>>>(part, n_chunks, q_starts, draft_tokens, parents, total_rows,
+                                                     argmax_out, accept_len, out_tokens, accepted_rows, status);
+    return check_cuda(cudaGetLastError(), "spec_accept_tree_greedy walk launch");
 }

@@ -114,8 +114,8 @@ extern "C" int pkv_device_status(void *stream, int32_t *bits)
     if (host & PKV_DEV_TOO_MANY_ROWS)
         return pkv::set_error(PKV_ERR_SHAPE,
                               "a sequence had more query rows than max_q_rows_per_seq (bits 0x%x)", host);
-    if (host & PKV_DEV_WORKSPACE)
-        return pkv::set_error(PKV_ERR_WORKSPACE,
-                              "the attention workspace counters were not zero on entry (bits 0x%x)", host);
+    if (host & PKV_DEV_BAD_TREE)
+        return pkv::set_error(PKV_ERR_SHAPE,
+                              "a draft tree had a parent index outside [0, node) (bits 0x%x)", host);
     return PKV_OK;
 }

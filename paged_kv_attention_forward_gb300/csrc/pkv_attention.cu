@@ -58,6 +58,7 @@ struct AttnParams {
     const int32_t *block_tables;  // [S][max_blocks]
     const int32_t *context_lens;  // [S]
     const float *sinks;           // [Hq] or null
+    const uint32_t *tree_masks;   // [R] or null: bit i = the row sees window token i
     void *out;                    // [R][Hq][D] bf16 or f32
     float2 *part_ml;              // [R*Hq*n_max] (m in log2 units, l)
     float *part_o;                // [R*Hq*n_max][D]
@@ -90,7 +91,9 @@ __device__ __forceinline__ uint32_t tile_off(int tok, int ch)
 
 // NN: n-tiles of 8 query rows per consumer warp; NMT: consumer warps.  A CTA serves
 // up to 8 * NN * NMT rows (the G q heads of one KV head times the sequence's rows).
-template <int D, int BS, int NN, int NMT, int NST>
+// TREE: rows carry ancestor masks over the window keys (tree verify); a separate
+// instantiation so the decode / causal path carries no mask test.
+template <int D, int BS, int NN, int NMT, int NST, bool TREE>
 __global__ void __launch_bounds__((NMT + 1) * 32)
 paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const AttnParams p)
@@ -235,7 +238,8 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
         const int kr = lane >> 2;        // key (row of the C fragment) within 8
         const int row_base = r_lo + warp * RPW;
         uint32_t qf[NN][KS][2];
-        int lim[NN][2];
+        int lim[NN][2], win0[NN][2];   // keys t < lim are candidates; t >= win0 need their mask bit
+        uint32_t tmk[NN][2];
 #pragma unroll
         for (int nn = 0; nn < NN; ++nn) {
             const int jq = row_base + nn * 8 + kr;   // B fragment: lane l carries row l/4
@@ -254,6 +258,12 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
             for (int e = 0; e < 2; ++e) {
                 const int j = row_base + nn * 8 + cr + e;
                 lim[nn][e] = (p.causal && j < M) ? L - W + j / p.group + 1 : L;
+                win0[nn][e] = L;
+                tmk[nn][e] = 0u;
+                if (TREE && j < M) {   // tree verify: the window keys a row sees are its ancestors
+                    win0[nn][e] = L - W;
+                    tmk[nn][e] = __ldg(p.tree_masks + row0 + j / p.group);
+                }
             }
         }
         float o[DM][NN][4];
@@ -324,7 +334,11 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                     for (int c = 0; c < 4; ++c) {
                         const int t = tbase + mt * 16 + kr + 8 * (c >> 1);
                         const float x = (sa[mt][nn][c] + sb[mt][nn][c]) * p.scale_log2;
-                        sa[mt][nn][c] = (t < lim[nn][c & 1]) ? x : -INFINITY;
+                        const int e = c & 1;
+                        bool vis = t < lim[nn][e];
+                        if (TREE)
+                            vis = vis && (t < win0[nn][e] || ((tmk[nn][e] >> (t - win0[nn][e])) & 1u));
+                        sa[mt][nn][c] = vis ? x : -INFINITY;
                         mx[nn][c & 1] = fmaxf(mx[nn][c & 1], sa[mt][nn][c]);
                     }
             float alpha[NN][2], base[NN][2];
@@ -482,7 +496,13 @@ paged_attention_combine_kernel(const AttnParams p)
     const int L_cap = (int)min((long long)p.max_context_len, (long long)p.max_blocks_per_seq * p.block_size);
     int L = __ldg(p.context_lens + s);
     L = L < 0 ? 0 : (L > L_cap ? L_cap : L);
-    const int lim = p.causal ? L - W + w + 1 : L;
+    int lim = p.causal ? L - W + w + 1 : L;
+    if (p.tree_masks) {   // the row's last visible key is its highest visible window token
+        uint32_t m = __ldg(p.tree_masks + r);
+        if (W < 32)
+            m &= (1u << W) - 1u;
+        lim = L - W + (m ? 32 - __clz(m) : 0);
+    }
     const int n = lim > 0 ? (lim + kSplitTokens - 1) / kSplitTokens : 0;
     const size_t base = ((size_t)r * p.num_q_heads + h) * p.n_max;
 
@@ -660,12 +680,12 @@ size_t smem_bytes()
     return 1024 + (size_t)NST * 2 * Tile<D, BS>::kTileBytes + 2 * NST * sizeof(uint64_t) + 64;
 }
 
-template <int D, int BS, int NN, int NMT>
+template <int D, int BS, int NN, int NMT, bool TREE>
 int launch_t(const CUtensorMap &mk, const CUtensorMap &mv, const AttnParams &prm, dim3 grid,
              cudaStream_t st)
 {
     constexpr int NST = kStages<D, BS, NMT>();
-    auto kern = paged_attention_kernel<D, BS, NN, NMT, NST>;
+    auto kern = paged_attention_kernel<D, BS, NN, NMT, NST, TREE>;
     const size_t smem = smem_bytes<D, BS, NMT>();
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
@@ -713,9 +733,12 @@ int launch_d_bs(int rows, const CUtensorMap &mk, const CUtensorMap &mv, AttnPara
     if (gx > 0x7fffffffLL || n_max > 65535)
         return set_error(PKV_ERR_SHAPE, "paged_attention_forward: grid too large");
     const dim3 grid((unsigned)gx, (unsigned)n_max);
+    if (prm.tree_masks)
+        return rows <= 8 ? launch_t<D, BS, 1, 1, true>(mk, mv, prm, grid, st)
+                         : launch_t<D, BS, PKV_WIDE_NN, PKV_WIDE_NMT, true>(mk, mv, prm, grid, st);
     if (rows <= 8)
-        return launch_t<D, BS, 1, 1>(mk, mv, prm, grid, st);
-    return launch_t<D, BS, PKV_WIDE_NN, PKV_WIDE_NMT>(mk, mv, prm, grid, st);
+        return launch_t<D, BS, 1, 1, false>(mk, mv, prm, grid, st);
+    return launch_t<D, BS, PKV_WIDE_NN, PKV_WIDE_NMT, false>(mk, mv, prm, grid, st);
 }
 
 struct WsLayout {
@@ -757,61 +780,59 @@ extern "C" int paged_attention_workspace_init(void *workspace, size_t workspace_
                            "paged_attention_workspace_init");
 }
 
-extern "C" int paged_attention_forward(const pkv_pool *pool, const void *q, const int32_t *q_starts,
-                                       const int32_t *block_tables, int32_t max_blocks_per_seq,
-                                       const int32_t *context_lens, int32_t num_seqs,
-                                       int32_t total_q_rows, int32_t max_context_len,
-                                       int32_t max_q_rows_per_seq, int32_t num_q_heads,
-                                       const int32_t *kv_head_of_q_head, const float *sinks,
-                                       int32_t causal, float scale, void *out, int32_t out_dtype,
-                                       void *workspace, size_t workspace_bytes, void *stream)
+namespace pkv {
+namespace {
+int attention_impl(const char *who, const pkv_pool *pool, const void *q, const int32_t *q_starts,
+                   const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
+                   int32_t num_seqs, int32_t total_q_rows, int32_t max_context_len,
+                   int32_t max_q_rows_per_seq, int32_t num_q_heads, const int32_t *kv_head_of_q_head,
+                   const float *sinks, int32_t causal, const uint32_t *tree_masks, float scale, void *out,
+                   int32_t out_dtype, void *workspace, size_t workspace_bytes, void *stream)
 {
-    using namespace pkv;
-    clear_error();
     if (!pool)
-        return set_error(PKV_ERR_NULL, "paged_attention_forward: pool is NULL");
+        return set_error(PKV_ERR_NULL, "%s: pool is NULL", who);
     const int D = pool->head_dim, BS = pool->block_size, Hkv = pool->num_kv_heads;
     if (num_seqs < 0 || total_q_rows < 0 || max_context_len < 0 || max_q_rows_per_seq < 0)
-        return set_error(PKV_ERR_SHAPE, "paged_attention_forward: negative size");
+        return set_error(PKV_ERR_SHAPE, "%s: negative size", who);
     if (pool->num_blocks <= 0 || Hkv <= 0 || max_blocks_per_seq <= 0)
-        return set_error(PKV_ERR_SHAPE, "paged_attention_forward: pool sizes and max_blocks_per_seq must be positive");
+        return set_error(PKV_ERR_SHAPE, "%s: pool sizes and max_blocks_per_seq must be positive", who);
     if (!(D == 64 || D == 128))
-        return set_error(PKV_ERR_UNSUPPORTED, "paged_attention_forward: head_dim %d (built: 64, 128)", D);
+        return set_error(PKV_ERR_UNSUPPORTED, "%s: head_dim %d (built: 64, 128)", who, D);
     if (!(BS == 16 || BS == 32))
-        return set_error(PKV_ERR_UNSUPPORTED, "paged_attention_forward: block_size %d (built: 16, 32)", BS);
+        return set_error(PKV_ERR_UNSUPPORTED, "%s: block_size %d (built: 16, 32)", who, BS);
     if (num_q_heads <= 0 || num_q_heads > kMaxQHeads || num_q_heads % Hkv != 0)
         return set_error(PKV_ERR_SHAPE,
-                         "paged_attention_forward: num_q_heads %d must be a positive multiple of "
-                         "num_kv_heads %d and at most %d", num_q_heads, Hkv, kMaxQHeads);
+                         "%s: num_q_heads %d must be a positive multiple of "
+                         "num_kv_heads %d and at most %d", who, num_q_heads, Hkv, kMaxQHeads);
     if (out_dtype != PKV_DTYPE_BF16 && out_dtype != PKV_DTYPE_F32)
-        return set_error(PKV_ERR_SHAPE, "paged_attention_forward: out_dtype %d", out_dtype);
+        return set_error(PKV_ERR_SHAPE, "%s: out_dtype %d", who, out_dtype);
     if ((long long)max_blocks_per_seq * BS < max_context_len)
         return set_error(PKV_ERR_SHAPE,
-                         "paged_attention_forward: max_context_len %d exceeds max_blocks_per_seq * "
-                         "block_size = %lld", max_context_len, (long long)max_blocks_per_seq * BS);
+                         "%s: max_context_len %d exceeds max_blocks_per_seq * "
+                         "block_size = %lld", who, max_context_len, (long long)max_blocks_per_seq * BS);
     if ((long long)pool->num_blocks * Hkv * BS > 0x7fffffffLL)
         return set_error(PKV_ERR_UNSUPPORTED,
-                         "paged_attention_forward: pool too large for 32-bit TMA row coordinates");
+                         "%s: pool too large for 32-bit TMA row coordinates", who);
     const int G = num_q_heads / Hkv;
     if (num_seqs == 0 || total_q_rows == 0)
         return PKV_OK;
     if (max_q_rows_per_seq <= 0)
-        return set_error(PKV_ERR_SHAPE, "paged_attention_forward: max_q_rows_per_seq must be >= 1");
+        return set_error(PKV_ERR_SHAPE, "%s: max_q_rows_per_seq must be >= 1", who);
     if ((long long)G * max_q_rows_per_seq > kMaxGroupRows)
         return set_error(PKV_ERR_UNSUPPORTED,
-                         "paged_attention_forward: group %d x max rows %d exceeds %d", G,
+                         "%s: group %d x max rows %d exceeds %d", who, G,
                          max_q_rows_per_seq, kMaxGroupRows);
     if (!pool->k_pool || !pool->v_pool || !q || !q_starts || !block_tables || !context_lens || !out ||
         !workspace)
-        return set_error(PKV_ERR_NULL, "paged_attention_forward: a required pointer is NULL");
+        return set_error(PKV_ERR_NULL, "%s: a required pointer is NULL", who);
     if (!aligned16(pool->k_pool) || !aligned16(pool->v_pool) || !aligned16(q) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return set_error(PKV_ERR_ALIGN,
-                         "paged_attention_forward: pools, q and out must be 16-byte aligned, "
-                         "workspace 256-byte aligned");
+                         "%s: pools, q and out must be 16-byte aligned, "
+                         "workspace 256-byte aligned", who);
     const WsLayout wl = ws_layout(num_seqs, total_q_rows, num_q_heads, Hkv, D, max_context_len);
     if (workspace_bytes < wl.total)
-        return set_error(PKV_ERR_WORKSPACE, "paged_attention_forward: workspace %zu < %zu bytes",
+        return set_error(PKV_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", who,
                          workspace_bytes, wl.total);
 
     AttnParams prm;
@@ -823,14 +844,14 @@ extern "C" int paged_attention_forward(const pkv_pool *pool, const void *q, cons
             const int gg = kv_head_of_q_head ? kv_head_of_q_head[h] : h / G;
             if (gg < 0 || gg >= Hkv || fill[gg] >= G)
                 return set_error(PKV_ERR_SHAPE,
-                                 "paged_attention_forward: kv_head_of_q_head must give each of the %d "
-                                 "KV heads exactly %d q heads (entry %d = %d)", Hkv, G, h, gg);
+                                 "%s: kv_head_of_q_head must give each of the %d "
+                                 "KV heads exactly %d q heads (entry %d = %d)", who, Hkv, G, h, gg);
             prm.q_head_of[gg * G + fill[gg]++] = (int16_t)h;
         }
     }
     int32_t *status = device_status_word();
     if (!status)
-        return set_error(PKV_ERR_CUDA, "paged_attention_forward: no device status word");
+        return set_error(PKV_ERR_CUDA, "%s: no device status word", who);
 
     CUtensorMap mk, mv;
     int rc = make_pool_map(&mk, pool->k_pool, *pool);
@@ -847,6 +868,7 @@ extern "C" int paged_attention_forward(const pkv_pool *pool, const void *q, cons
     prm.block_tables = block_tables;
     prm.context_lens = context_lens;
     prm.sinks = sinks;
+    prm.tree_masks = tree_masks;
     prm.out = out;
     prm.part_ml = reinterpret_cast<float2 *>(ws + wl.ml);
     prm.part_o = reinterpret_cast<float *>(ws + wl.o);
@@ -874,6 +896,47 @@ extern "C" int paged_attention_forward(const pkv_pool *pool, const void *q, cons
     if (D == 64 && BS == 32) return launch_d_bs<64, 32>(rows, mk, mv, prm, pairs, n_max, st);
     if (D == 128 && BS == 16) return launch_d_bs<128, 16>(rows, mk, mv, prm, pairs, n_max, st);
     return launch_d_bs<128, 32>(rows, mk, mv, prm, pairs, n_max, st);
+}
+}  // namespace
+}  // namespace pkv
+
+extern "C" int paged_attention_forward(const pkv_pool *pool, const void *q, const int32_t *q_starts,
+                                       const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t *context_lens, int32_t num_seqs,
+                                       int32_t total_q_rows, int32_t max_context_len,
+                                       int32_t max_q_rows_per_seq, int32_t num_q_heads,
+                                       const int32_t *kv_head_of_q_head, const float *sinks,
+                                       int32_t causal, float scale, void *out, int32_t out_dtype,
+                                       void *workspace, size_t workspace_bytes, void *stream)
+{
+    pkv::clear_error();
+    return pkv::attention_impl("paged_attention_forward", pool, q, q_starts, block_tables, max_blocks_per_seq,
+                               context_lens, num_seqs, total_q_rows, max_context_len, max_q_rows_per_seq,
+                               num_q_heads, kv_head_of_q_head, sinks, causal, nullptr, scale, out, out_dtype,
+                               workspace, workspace_bytes, stream);
+}
+
+extern "C" int paged_tree_attention_forward(const pkv_pool *pool, const void *q, const int32_t *q_starts,
+                                            const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                            const int32_t *context_lens, int32_t num_seqs,
+                                            int32_t total_q_rows, int32_t max_context_len,
+                                            int32_t max_q_rows_per_seq, int32_t num_q_heads,
+                                            const int32_t *kv_head_of_q_head, const float *sinks,
+                                            const uint32_t *tree_masks, float scale, void *out,
+                                            int32_t out_dtype, void *workspace, size_t workspace_bytes,
+                                            void *stream)
+{
+    pkv::clear_error();
+    if (num_seqs > 0 && total_q_rows > 0 && !tree_masks)
+        return pkv::set_error(PKV_ERR_NULL, "paged_tree_attention_forward: tree_masks is NULL");
+    if (max_q_rows_per_seq > 32)
+        return pkv::set_error(PKV_ERR_UNSUPPORTED,
+                              "paged_tree_attention_forward: at most 32 verify rows per sequence (got %d)",
+                              max_q_rows_per_seq);
+    return pkv::attention_impl("paged_tree_attention_forward", pool, q, q_starts, block_tables,
+                               max_blocks_per_seq, context_lens, num_seqs, total_q_rows, max_context_len,
+                               max_q_rows_per_seq, num_q_heads, kv_head_of_q_head, sinks, 0, tree_masks, scale,
+                               out, out_dtype, workspace, workspace_bytes, stream);
 }
 
 // ------------------------------------------------ allocation-free variant --

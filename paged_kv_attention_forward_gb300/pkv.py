@@ -27,7 +27,7 @@ STATUS_NAMES = {0: "PKV_OK", -1: "PKV_ERR_NULL", -2: "PKV_ERR_SHAPE", -3: "PKV_E
 EXPORTED = ("pkv_abi_version", "paged_kv_append", "paged_attention_workspace_size",
             "paged_attention_workspace_init", "paged_attention_forward", "spec_accept_workspace_size",
             "spec_accept_greedy", "pkv_last_error_string", "pkv_device_status",
-            "paged_attention_forward_noalloc")
+            "paged_attention_forward_noalloc", "paged_tree_attention_forward", "spec_accept_tree_greedy")
 
 
 class PkvError(RuntimeError):
@@ -76,6 +76,11 @@ def lib(build_if_missing: bool = False):
             L.paged_attention_forward_noalloc.argtypes = [ctypes.POINTER(_Pool), P, P, P, i32, P, i32, i32,
                                                           i32, i32, i32, P, P, i32, ctypes.c_float, P, i32, P]
             L.paged_attention_forward_noalloc.restype = ctypes.c_int
+            L.paged_tree_attention_forward.argtypes = [ctypes.POINTER(_Pool), P, P, P, i32, P, i32, i32, i32,
+                                                       i32, i32, P, P, P, ctypes.c_float, P, i32, P, sz, P]
+            L.paged_tree_attention_forward.restype = ctypes.c_int
+            L.spec_accept_tree_greedy.argtypes = [P, i32, P, P, P, i32, i32, P, P, P, P, P, sz, P]
+            L.spec_accept_tree_greedy.restype = ctypes.c_int
             L.spec_accept_workspace_size.argtypes = [i32, i32]
             L.spec_accept_workspace_size.restype = sz
             L.spec_accept_greedy.argtypes = [P, i32, P, P, i32, i32, P, P, P, P, sz, P]
@@ -164,6 +169,53 @@ def paged_attention_forward(k_pool, v_pool, q, q_starts, block_tables, context_l
         _dptr(sinks), int(bool(causal)), float(scale), _dptr(out), dt, _dptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
     return out
+
+
+def paged_tree_attention_forward(k_pool, v_pool, q, q_starts, block_tables, context_lens, tree_masks, *,
+                                 max_context_len: int, max_q_rows_per_seq: int, kv_head_of_q_head=None,
+                                 sinks=None, scale: float = 0.0, out: Optional[torch.Tensor] = None,
+                                 out_dtype=torch.bfloat16, workspace: Optional[torch.Tensor] = None,
+                                 stream=None) -> torch.Tensor:
+    """Tree verify attention (see include/pkv.h); tree_masks: CUDA int32/uint32 [R]."""
+    pool = _pool(k_pool, v_pool)
+    R, Hq, D = q.shape
+    S = block_tables.shape[0]
+    if out is None:
+        out = torch.empty((R, Hq, D), dtype=out_dtype, device=q.device)
+    dt = PKV_DTYPE_F32 if out.dtype == torch.float32 else PKV_DTYPE_BF16
+    if workspace is None:
+        workspace = new_attention_workspace(S, R, Hq, pool.num_kv_heads, D, max_context_len, q.device)
+    hmap = None
+    if kv_head_of_q_head is not None:
+        arr = (ctypes.c_int32 * Hq)(*[int(x) for x in kv_head_of_q_head])
+        hmap = ctypes.cast(arr, ctypes.c_void_p)
+    _check(lib().paged_tree_attention_forward(
+        ctypes.byref(pool), _dptr(q), _dptr(q_starts), _dptr(block_tables), block_tables.shape[1],
+        _dptr(context_lens), S, R, int(max_context_len), int(max_q_rows_per_seq), Hq, hmap, _dptr(sinks),
+        _dptr(tree_masks), float(scale), _dptr(out), dt, _dptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def spec_accept_tree_greedy(logits, q_starts, draft_tokens, parents, *, argmax_out=None, accept_len=None,
+                            out_tokens=None, accepted_rows=None, workspace=None, stream=None):
+    """Greedy accept over draft trees (see include/pkv.h);
+    returns (argmax [R], accept_len [S], out_tokens [R], accepted_rows [R])."""
+    R, V = logits.shape
+    S = q_starts.shape[0] - 1
+    dev = logits.device
+    mk = lambda n: torch.empty(n, dtype=torch.int32, device=dev)  # noqa: E731
+    argmax_out = mk(R) if argmax_out is None else argmax_out
+    accept_len = mk(S) if accept_len is None else accept_len
+    out_tokens = mk(R) if out_tokens is None else out_tokens
+    accepted_rows = mk(R) if accepted_rows is None else accepted_rows
+    if workspace is None:
+        workspace = torch.empty(max(spec_accept_workspace_size(R, V), 256), dtype=torch.uint8, device=dev)
+    _check(lib().spec_accept_tree_greedy(_dptr(logits), V, _dptr(q_starts), _dptr(draft_tokens), _dptr(parents),
+                                         S, R, _dptr(argmax_out), _dptr(accept_len), _dptr(out_tokens),
+                                         _dptr(accepted_rows), _dptr(workspace), workspace.numel(),
+                                         _stream(stream)))
+    return argmax_out, accept_len, out_tokens, accepted_rows
 
 
 def spec_accept_workspace_size(total_rows, vocab) -> int:

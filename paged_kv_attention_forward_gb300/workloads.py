@@ -21,6 +21,8 @@ Workloads (sizes from the continuous-batching / speculative-decoding pages):
                     151936-token vocabulary and a draft chain per sequence.
   sinks_scale       128 seqs x 8192 tokens, 64 q / 8 kv heads, head_dim 64,
                     block 32, one fp32 sink logit per q head.
+  spec_tree         spec_verify's shapes with each window a random draft tree
+                    (per-row ancestor masks, parent indices, tree drafts).
 """
 from __future__ import annotations
 
@@ -147,6 +149,8 @@ class PagedBatch:
     logits: Optional[np.ndarray] = None        # float32 [R, vocab] (verify workloads)
     draft_tokens: Optional[np.ndarray] = None  # int32 [R]; slot 0 of each sequence is -1
     planted_targets: Optional[np.ndarray] = None  # int32 [R]: token given the planted maximum
+    parents: Optional[np.ndarray] = None       # int32 [R]: draft-tree parent node of each row (-1 at roots)
+    tree_masks: Optional[np.ndarray] = None    # uint32 [R]: bit i = the row sees window token i
 
     @property
     def num_seqs(self) -> int:
@@ -303,11 +307,45 @@ def add_verify_logits(batch: PagedBatch, seed, vocab: int, std: float = 2.0,
     return batch
 
 
+def add_draft_trees(batch: PagedBatch, seed, vocab: int, std: float = 2.0, hit_prob: float = 0.7,
+                    planted_value: float = 20.0) -> PagedBatch:
+    """Attach draft trees to a verify batch: node j >= 1 of each sequence takes a parent
+    drawn uniformly from nodes 0..j-1 and, with probability ``hit_prob``, the parent's
+    planted target token as its draft (else a uniform token).  Also fills the per-row
+    visibility masks (a node sees its ancestors and itself) and the verify logits (as in
+    ``add_verify_logits``)."""
+    s_logit, s_pick = _seed_seq(seed).spawn(2)
+    rng = np.random.Generator(np.random.PCG64(s_pick))
+    R = batch.total_q_rows
+    logits = normal_f32(s_logit, (R, vocab), std)
+    planted = rng.integers(0, vocab, size=R).astype(np.int32)
+    logits[np.arange(R), planted] = np.float32(planted_value)
+    parents = np.full(R, -1, dtype=np.int32)
+    drafts = np.full(R, -1, dtype=np.int32)
+    masks = np.zeros(R, dtype=np.uint32)
+    for s in range(batch.num_seqs):
+        r0, r1 = int(batch.q_starts[s]), int(batch.q_starts[s + 1])
+        for j in range(r1 - r0):
+            if j == 0:
+                masks[r0] = 1
+                continue
+            par = int(rng.integers(0, j))
+            parents[r0 + j] = par
+            drafts[r0 + j] = planted[r0 + par] if rng.random() < hit_prob else int(rng.integers(0, vocab))
+            masks[r0 + j] = masks[r0 + par] | np.uint32(1 << j)
+    batch.logits = logits
+    batch.draft_tokens = drafts
+    batch.planted_targets = planted
+    batch.parents = parents
+    batch.tree_masks = masks
+    return batch
+
+
 def _loguniform_int(rng, lo, hi, size):
     return np.rint(np.exp(rng.uniform(math.log(lo), math.log(hi), size=size))).astype(np.int64)
 
 
-WORKLOADS = ("tiny_decode", "ministral_decode", "cb_mix", "spec_verify", "sinks_scale")
+WORKLOADS = ("tiny_decode", "ministral_decode", "cb_mix", "spec_verify", "sinks_scale", "spec_tree")
 VOCAB = 151936
 
 
@@ -350,6 +388,13 @@ def make_workload(name: str, seed: int = 0, filler: str = "random", layers: Opti
         b = build_batch(s_batch, name=name, lens=lens, n_new=w, q_rows=w, num_q_heads=32,
                         num_kv_heads=8, head_dim=128, block_size=16, causal=True, filler=filler)
         return add_verify_logits(b, s_extra, VOCAB)
+    if name == "spec_tree":
+        S = num_seqs or 16
+        lens = rng.integers(4096, 32769, size=S)
+        w = rng.integers(1, 17, size=S)
+        b = build_batch(s_batch, name=name, lens=lens, n_new=w, q_rows=w, num_q_heads=32,
+                        num_kv_heads=8, head_dim=128, block_size=16, causal=False, filler=filler)
+        return add_draft_trees(b, s_extra, VOCAB)
     if name == "sinks_scale":
         S = num_seqs or 128
         return build_batch(s_batch, name=name, lens=np.full(S, 8192), n_new=np.zeros(S, np.int64),
@@ -391,4 +436,7 @@ def select_seqs(batch: PagedBatch, seqs) -> PagedBatch:
         sub.logits = np.ascontiguousarray(batch.logits[q_idx])
         sub.draft_tokens = batch.draft_tokens[q_idx].copy()
         sub.planted_targets = batch.planted_targets[q_idx].copy()
+    if batch.parents is not None:
+        sub.parents = batch.parents[q_idx].copy()
+        sub.tree_masks = batch.tree_masks[q_idx].copy()
     return sub
