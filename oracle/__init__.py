@@ -67,6 +67,13 @@ def _load():
             lib.oracle_spec_accept_greedy.restype = None
             lib.oracle_spec_accept_tree_greedy.argtypes = [P, i32, P, P, P, i32, P, P, P, P]
             lib.oracle_spec_accept_tree_greedy.restype = ctypes.c_int
+            lib.oracle_philox4x32_10.argtypes = [P, P, P]
+            lib.oracle_philox4x32_10.restype = None
+            lib.oracle_keyed_log.argtypes = [ctypes.c_float]
+            lib.oracle_keyed_log.restype = ctypes.c_float
+            lib.oracle_spec_accept_sampled.argtypes = [P, i32, P, P, P, P, ctypes.c_uint64, ctypes.c_float,
+                                                       ctypes.c_float, i32, P, P, P, P]
+            lib.oracle_spec_accept_sampled.restype = ctypes.c_int
             _lib = lib
         return _lib
 
@@ -185,3 +192,42 @@ def spec_accept_tree_greedy(logits, q_starts, draft_tokens, parents):
     if rc != 0:
         raise ValueError(f"oracle_spec_accept_tree_greedy failed with status {rc}")
     return am, al, ot, ar
+
+
+def philox4x32_10(counter, key):
+    """Philox4x32-10 of a 4-word counter and 2-word key; returns 4 uint32 words."""
+    lib = _load()
+    c = _c(counter, np.uint32)
+    k = _c(key, np.uint32)
+    out = np.empty(4, dtype=np.uint32)
+    lib.oracle_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def keyed_log(x):
+    """The sampler's float32 natural logarithm (fixed float32 operation sequence)."""
+    return np.float32(_load().oracle_keyed_log(float(x)))
+
+
+def spec_accept_sampled(logits, q_starts, draft_tokens, positions, seed, temperature, min_p=0.0,
+                        parents=None):
+    """Sampled (keyed) accept: returns (sampled [R], accept_len [S], out_tokens [R],
+    accepted_rows [R]), all int32.  parents None means chains."""
+    lib = _load()
+    lg = _c(logits, np.float32)
+    rows, vocab = lg.shape
+    qs = _c(q_starts, np.int32)
+    dr = _c(draft_tokens, np.int32)
+    po = _c(positions, np.int32)
+    pa = None if parents is None else _c(parents, np.int32)
+    s = qs.shape[0] - 1
+    sm = np.empty(rows, dtype=np.int32)
+    al = np.empty(s, dtype=np.int32)
+    ot = np.empty(rows, dtype=np.int32)
+    ar = np.empty(rows, dtype=np.int32)
+    rc = lib.oracle_spec_accept_sampled(_ptr(lg), vocab, _ptr(qs), _ptr(dr), _ptr(pa), _ptr(po), int(seed),
+                                        float(temperature), float(min_p), s, _ptr(sm), _ptr(al), _ptr(ot),
+                                        _ptr(ar))
+    if rc != 0:
+        raise ValueError(f"oracle_spec_accept_sampled failed with status {rc}")
+    return sm, al, ot, ar

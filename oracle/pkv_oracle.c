@@ -341,3 +341,173 @@ int oracle_spec_accept_tree_greedy(const float *logits, int32_t vocab,
     }
     return 0;
 }
+
+/* ---------------------------------------------------------- keyed sampling -- */
+/*
+ * Philox4x32-10, the counter-based generator of Salmon, Moraes, Dror and Shaw,
+ * "Parallel random numbers: as easy as 1, 2, 3" (SC'11): ten rounds of
+ * (hi, lo) = M * c on words 0 and 2 with M0 = 0xD2511F53, M1 = 0xCD9E8D57, the
+ * output words being (hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0); the key is bumped
+ * by the Weyl constants 0x9E3779B9, 0xBB67AE85 before every round but the first.
+ */
+void oracle_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4])
+{
+    uint32_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
+    uint32_t k0 = key_in[0], k1 = key_in[1];
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+        const uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+        const uint32_t n1 = (uint32_t)p1;
+        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+        const uint32_t n3 = (uint32_t)p0;
+        c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/*
+ * Natural logarithm in float32 by a fixed sequence of correctly rounded float32
+ * operations (no fused multiply-add), so that any IEEE implementation of the
+ * same steps gives the same bits: x = m 2^e with m in [sqrt(1/2), sqrt(2)),
+ * s = (m - 1) / (m + 1), log x = e ln 2 + 2 s (1 + s^2/3 + s^4/5 + ... + s^10/11)
+ * (the atanh series), with the coefficients rounded to float32.  x > 0, finite.
+ */
+float oracle_keyed_log(float x)
+{
+    uint32_t b;
+    memcpy(&b, &x, 4);
+    int e;
+    if ((b >> 23) == 0) {   /* subnormal: scale by 2^23 (exact) */
+        x = x * 8388608.0f;
+        memcpy(&b, &x, 4);
+        e = (int)(b >> 23) - 127 - 23;
+    } else {
+        e = (int)(b >> 23) - 127;
+    }
+    const uint32_t mb = (b & 0x7fffffu) | 0x3f800000u;
+    float m;
+    memcpy(&m, &mb, 4);
+    if (m > 0x1.6a09e6p+0f) {
+        m = m * 0.5f;
+        e += 1;
+    }
+    const float s = (m - 1.0f) / (m + 1.0f);
+    const float z = s * s;
+    float p = 0x1.745d18p-4f;        /* 1/11 */
+    p = p * z + 0x1.c71c72p-4f;      /* 1/9  */
+    p = p * z + 0x1.24924ap-3f;      /* 1/7  */
+    p = p * z + 0x1.99999ap-3f;      /* 1/5  */
+    p = p * z + 0x1.555556p-2f;      /* 1/3  */
+    p = p * z + 1.0f;
+    const float r = (s + s) * p;
+    return (float)e * 0x1.62e43p-1f + r;   /* ln 2 */
+}
+
+/*
+ * Keyed Gumbel noise of token v at absolute position pos under `seed`:
+ * u = (top 23 bits of Philox(ctr = (v, pos, 0x6b657964, 0), key = seed) + 1/2) / 2^23,
+ * g = -log(-log(u)).
+ */
+static float keyed_gumbel(uint64_t seed, int32_t pos, int32_t v)
+{
+    const uint32_t ctr[4] = {(uint32_t)v, (uint32_t)pos, 0x6b657964u, 0u};
+    const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t o[4];
+    oracle_philox4x32_10(ctr, key, o);
+    const float u = ((float)(o[0] >> 9) + 0.5f) * 0x1p-23f;
+    const float E = -oracle_keyed_log(u);
+    return -oracle_keyed_log(E);
+}
+
+/*
+ * The target's keyed draw for one row (TensorFold article, "先记住一条铁律": every
+ * draw is keyed by seed, absolute position and token id; the min_p filter is
+ * part of the keyed rule).  temperature == 0: the greedy argmax.  Otherwise, with
+ * l_max the row maximum and thr = l_max + temperature * log(min_p) (no filter
+ * when min_p <= 0), the draw is the lowest v maximising l_v / temperature +
+ * g(seed, pos, v) over the v with l_v >= thr, all in float32.  log(min_p) is the
+ * host libm's logf.
+ */
+static int32_t keyed_draw(const float *row, int32_t vocab, uint64_t seed, int32_t pos, float temperature,
+                          float min_p)
+{
+    int32_t best = 0;
+    for (int32_t v = 1; v < vocab; ++v)
+        if (row[v] > row[best])
+            best = v;
+    if (temperature == 0.0f)
+        return best;
+    const float l_max = row[best];
+    const float thr = min_p > 0.0f ? l_max + temperature * logf(min_p) : -INFINITY;
+    int32_t pick = -1;
+    float top = -INFINITY;
+    for (int32_t v = 0; v < vocab; ++v) {
+        if (!(row[v] >= thr))
+            continue;
+        const float sc = row[v] / temperature + keyed_gumbel(seed, pos, v);
+        if (pick < 0 || sc > top) {
+            top = sc;
+            pick = v;
+        }
+    }
+    return pick;
+}
+
+/*
+ * Sampled accept (TensorFold article, "先记住一条铁律" and "接受规则"): the target's
+ * token at row r is keyed_draw(row r, positions[r]); drafts are accepted along
+ * the chain (parents == NULL) or the tree exactly as in the greedy accept, with
+ * the draw in place of the argmax.  Outputs as oracle_spec_accept_tree_greedy,
+ * sampled_out holding each row's draw.  Returns 0 or -1 (bad parent index).
+ */
+int oracle_spec_accept_sampled(const float *logits, int32_t vocab, const int32_t *q_starts,
+                               const int32_t *draft_tokens, const int32_t *parents,
+                               const int32_t *positions, uint64_t seed, float temperature, float min_p,
+                               int32_t num_seqs, int32_t *sampled_out, int32_t *accept_len,
+                               int32_t *out_tokens, int32_t *accepted_rows)
+{
+    const int64_t total = q_starts[num_seqs];
+    for (int64_t r = 0; r < total; ++r)
+        sampled_out[r] = keyed_draw(logits + (size_t)r * vocab, vocab, seed, positions[r], temperature, min_p);
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        const int32_t r0 = q_starts[s], W = q_starts[s + 1] - q_starts[s];
+        if (W <= 0) {
+            accept_len[s] = -1;
+            continue;
+        }
+        for (int32_t j = 1; j < W; ++j) {
+            const int32_t par = parents ? parents[r0 + j] : j - 1;
+            if (par < 0 || par >= j)
+                return -1;
+        }
+        for (int32_t j = 0; j < W; ++j) {
+            out_tokens[r0 + j] = -1;
+            accepted_rows[r0 + j] = -1;
+        }
+        int32_t u = 0, n = 0;
+        for (;;) {
+            int32_t next = -1;
+            for (int32_t c = u + 1; c < W; ++c) {
+                const int32_t par = parents ? parents[r0 + c] : c - 1;
+                if (par == u && draft_tokens[r0 + c] == sampled_out[r0 + u]) {
+                    next = c;
+                    break;
+                }
+            }
+            if (next < 0)
+                break;
+            out_tokens[r0 + n] = draft_tokens[r0 + next];
+            accepted_rows[r0 + n] = next;
+            ++n;
+            u = next;
+        }
+        out_tokens[r0 + n] = sampled_out[r0 + u];
+        accept_len[s] = n;
+    }
+    return 0;
+}

@@ -1,0 +1,139 @@
+"""Pins for the oracle's keyed sampler and sampled accept (no GPU).
+
+TensorFold article, section "先记住一条铁律": every draw is keyed by seed, absolute position and
+token id, and a draft is accepted only when it equals the target's own draw; section
+"接受规则": min_p (and top-k/top-p) are part of the keyed rule.  Reading: Gumbel-max over
+l_v / T + g(seed, pos, v) among the tokens min_p keeps, Philox4x32-10 uniforms.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+from scipy import stats
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def test_philox_known_answers(oracle_mod):
+    n = 0
+    for line in open(os.path.join(GOLDEN, "philox4x32_10_kat.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        w = [int(x, 16) for x in line.split()]
+        assert oracle_mod.philox4x32_10(w[0:4], w[4:6]).tolist() == w[6:10]
+        n += 1
+    assert n == 3
+
+
+def test_keyed_log_accuracy(oracle_mod):
+    rng = np.random.default_rng(0)
+    xs = np.concatenate([np.exp(rng.uniform(-87, 88, 4000)), rng.uniform(0.5, 2.0, 2000),
+                         [1.0, 2.0, 0.5, 1.5e-45, 1e-40, 3.4e38, 1.0000001, 0.99999994]]).astype(np.float32)
+    for x in xs:
+        got = float(oracle_mod.keyed_log(x))
+        ref = math.log(float(x))
+        ulp = float(np.spacing(np.float32(abs(ref)))) if ref != 0 else 1e-45
+        assert abs(got - ref) <= max(4 * ulp, 1.5e-7), (x, got, ref)
+    assert float(oracle_mod.keyed_log(np.float32(1.0))) == 0.0
+
+
+def _one_chain(V, rows, seed=0):
+    rng = np.random.default_rng(seed)
+    lg = (rng.standard_normal((rows, V)) * 2).astype(np.float32)
+    qs = np.array([0, rows], np.int32)
+    return lg, qs
+
+
+def test_zero_temperature_is_greedy(oracle_mod):
+    from paged_kv_attention_forward_gb300 import workloads as wl
+    b = wl.make_workload("spec_tree", seed=1)
+    pos = np.arange(b.total_q_rows, dtype=np.int32) + 1000
+    s = oracle_mod.spec_accept_sampled(b.logits, b.q_starts, b.draft_tokens, pos, seed=5, temperature=0.0,
+                                       parents=b.parents)
+    g = oracle_mod.spec_accept_tree_greedy(b.logits, b.q_starts, b.draft_tokens, b.parents)
+    for x, y in zip(s, g):
+        assert np.array_equal(x, y)
+
+
+@pytest.mark.parametrize("temperature", [1.0, 0.5])
+def test_draws_follow_softmax(oracle_mod, temperature):
+    V, R = 6, 60000
+    row = np.array([1.0, 0.3, -0.5, 2.0, 0.0, -2.0], np.float32)
+    lg = np.tile(row, (R, 1))
+    qs = np.array([0] + list(range(1, R + 1)), np.int32)      # R one-row sequences
+    pos = np.arange(R, dtype=np.int32)
+    draws = oracle_mod.spec_accept_sampled(lg, qs, np.full(R, -1, np.int32), pos, seed=42,
+                                           temperature=temperature)[0]
+    counts = np.bincount(draws, minlength=V)
+    p = np.exp(row.astype(np.float64) / temperature)
+    p /= p.sum()
+    chi2, pval = stats.chisquare(counts, R * p)
+    assert pval > 1e-3, (counts, R * p)
+
+
+def test_min_p_filter(oracle_mod):
+    V, R = 5, 20000
+    row = np.array([2.0, 1.9, 0.0, -1.0, 1.0], np.float32)   # probs relative to max: 1, .905, .135, .05, .368
+    lg = np.tile(row, (R, 1))
+    qs = np.array([0] + list(range(1, R + 1)), np.int32)
+    pos = np.arange(R, dtype=np.int32)
+    d = oracle_mod.spec_accept_sampled(lg, qs, np.full(R, -1, np.int32), pos, seed=3, temperature=1.0,
+                                       min_p=0.3)[0]
+    assert set(np.unique(d).tolist()) == {0, 1, 4}            # tokens below 0.3 x p_max never drawn
+    kept = np.exp(row[[0, 1, 4]].astype(np.float64))
+    chi2, pval = stats.chisquare(np.bincount(d, minlength=5)[[0, 1, 4]], R * kept / kept.sum())
+    assert pval > 1e-3
+    d1 = oracle_mod.spec_accept_sampled(lg[:500], qs[:501], np.full(500, -1, np.int32), pos[:500], seed=3,
+                                        temperature=1.0, min_p=1.0)[0]
+    assert np.all(d1 == 0)
+
+
+def test_draws_are_keyed_by_seed_position_and_token(oracle_mod):
+    lg, _ = _one_chain(50, 300, seed=4)
+    R = lg.shape[0]
+    qs = np.arange(R + 1, dtype=np.int32)
+    pos = np.random.default_rng(1).permutation(10000)[:R].astype(np.int32)
+    none = np.full(R, -1, np.int32)
+    a = oracle_mod.spec_accept_sampled(lg, qs, none, pos, seed=9, temperature=1.0)[0]
+    perm = np.random.default_rng(2).permutation(R)
+    b = oracle_mod.spec_accept_sampled(lg[perm], qs, none, pos[perm], seed=9, temperature=1.0)[0]
+    assert np.array_equal(a[perm], b)                          # batch order does not matter
+    c = oracle_mod.spec_accept_sampled(lg, qs, none, pos, seed=10, temperature=1.0)[0]
+    assert (a != c).mean() > 0.5                               # another seed, other draws
+    d = oracle_mod.spec_accept_sampled(lg, qs, none, pos + 1, seed=9, temperature=1.0)[0]
+    assert (a != d).mean() > 0.5                               # another position, other draws
+
+
+def test_sampled_walk_accepts_exactly_the_matching_prefix(oracle_mod):
+    lg, qs = _one_chain(40, 9, seed=6)
+    pos = np.arange(9, dtype=np.int32) + 77
+    draws = oracle_mod.spec_accept_sampled(lg, qs, np.full(9, -1, np.int32), pos, seed=1, temperature=0.8)[0]
+    drafts = np.concatenate([[-1], draws[:-1]]).astype(np.int32)    # a perfect drafter
+    s, n, out, rows = oracle_mod.spec_accept_sampled(lg, qs, drafts, pos, seed=1, temperature=0.8)
+    assert n[0] == 8 and out.tolist() == draws.tolist() and rows[:8].tolist() == list(range(1, 9))
+    drafts[5] = (draws[4] + 1) % 40                                   # first miss at node 5
+    s, n, out, rows = oracle_mod.spec_accept_sampled(lg, qs, drafts, pos, seed=1, temperature=0.8)
+    assert n[0] == 4 and out[:5].tolist() == draws[:5].tolist() and np.all(out[5:] == -1)
+
+
+def colliding_tokens(oracle_mod, seed, pos, limit=30000):
+    """Two token ids whose keyed uniforms (top 23 bits of Philox word 0) coincide."""
+    seen = {}
+    key = [seed & 0xFFFFFFFF, seed >> 32]
+    for v in range(limit):
+        u = int(oracle_mod.philox4x32_10([v, pos, 0x6B657964, 0], key)[0]) >> 9
+        if u in seen:
+            return seen[u], v
+        seen[u] = v
+    raise AssertionError("no collision found")
+
+
+def test_exact_score_ties_go_to_the_lowest_token(oracle_mod):
+    seed, pos = 7, 11
+    v1, v2 = colliding_tokens(oracle_mod, seed, pos)
+    row = np.full((1, v2 + 5), -100.0, np.float32)
+    row[0, [v1, v2]] = 50.0                        # equal logits and equal noise: an exact tie
+    d = oracle_mod.spec_accept_sampled(row, np.array([0, 1], np.int32), np.array([-1], np.int32),
+                                       np.array([pos], np.int32), seed=seed, temperature=1.0)[0]
+    assert d[0] == v1 < v2
