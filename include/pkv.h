@@ -292,6 +292,34 @@ int spec_accept_tree_greedy(const float *logits, int32_t vocab,
                             int32_t *accepted_rows, void *workspace, size_t workspace_bytes,
                             void *stream);
 
+/*
+ * Sampled accept (TensorFold article, "先记住一条铁律": every draw is keyed by
+ * seed, absolute position and token id, and a draft is accepted only when it
+ * equals the target's own draw; "接受规则": the min_p filter is part of the
+ * keyed rule).  The target's draw at row r:
+ *   temperature == 0: the argmax (ties to the lowest id);
+ *   otherwise the lowest v maximising l_v / temperature + g(seed, positions[r], v)
+ *   over the v with l_v >= l_max + temperature * logf(min_p) (all v if min_p <= 0),
+ *   where g = -log(-log(u)), u = ((w >> 9) + 1/2) / 2^23 and w is word (v mod 4)
+ *   of Philox4x32-10(counter = (v / 4, pos, 0x6b657964, 0), key = seed); the
+ *   logs are a fixed float32 operation sequence (atanh series) and every step is
+ *   a correctly rounded float32 operation, so the draw is reproducible exactly.
+ * The walk is the greedy accept's (chain when parents is NULL, else tree) with
+ * the draw in place of the argmax; outputs as spec_accept_tree_greedy, with
+ * sampled_out holding every row's draw.
+ *   positions   int32 [total_rows]: absolute position of the token each row draws
+ *   workspace   >= 2 * spec_accept_workspace_size(total_rows, vocab) bytes
+ * Launches three kernels (two when temperature == 0).
+ */
+int spec_accept_sampled(const float *logits, int32_t vocab,
+                        const int32_t *q_starts, const int32_t *draft_tokens,
+                        const int32_t *parents, const int32_t *positions,
+                        uint64_t seed, float temperature, float min_p,
+                        int32_t num_seqs, int32_t total_rows,
+                        int32_t *sampled_out, int32_t *accept_len, int32_t *out_tokens,
+                        int32_t *accepted_rows, void *workspace, size_t workspace_bytes,
+                        void *stream);
+
 /* Text of the calling thread's last error ("" if none). */
 const char *pkv_last_error_string(void);
 

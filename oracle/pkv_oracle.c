@@ -409,17 +409,18 @@ float oracle_keyed_log(float x)
 }
 
 /*
- * Keyed Gumbel noise of token v at absolute position pos under `seed`:
- * u = (top 23 bits of Philox(ctr = (v, pos, 0x6b657964, 0), key = seed) + 1/2) / 2^23,
- * g = -log(-log(u)).
+ * Keyed Gumbel noise of token v at absolute position pos under `seed`: with
+ * w = word (v mod 4) of Philox(ctr = (v / 4, pos, 0x6b657964, 0), key = seed),
+ * u = ((w >> 9) + 1/2) / 2^23 and g = -log(-log(u)).  (One generator call keys
+ * four consecutive tokens.)
  */
 static float keyed_gumbel(uint64_t seed, int32_t pos, int32_t v)
 {
-    const uint32_t ctr[4] = {(uint32_t)v, (uint32_t)pos, 0x6b657964u, 0u};
+    const uint32_t ctr[4] = {(uint32_t)v >> 2, (uint32_t)pos, 0x6b657964u, 0u};
     const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
     uint32_t o[4];
     oracle_philox4x32_10(ctr, key, o);
-    const float u = ((float)(o[0] >> 9) + 0.5f) * 0x1p-23f;
+    const float u = ((float)(o[(uint32_t)v & 3u] >> 9) + 0.5f) * 0x1p-23f;
     const float E = -oracle_keyed_log(u);
     return -oracle_keyed_log(E);
 }

@@ -138,9 +138,125 @@ accept_walk_kernel(const float2 *__restrict__ part, int n_chunks, const int32_t 
         accept_len[s] = n;
 }
 
+// ---- keyed sampling (draws keyed by seed, absolute position and token id) ----
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): 10 rounds of multiply-xor on
+// words 0 and 2, key bumped by the Weyl constants before every round but the first.
+__device__ __forceinline__ void philox4x32_10(uint32_t (&c)[4], uint32_t k0, uint32_t k1)
+{
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint32_t lo0 = 0xD2511F53u * c[0], hi0 = __umulhi(0xD2511F53u, c[0]);
+        const uint32_t lo1 = 0xCD9E8D57u * c[2], hi1 = __umulhi(0xCD9E8D57u, c[2]);
+        const uint32_t n0 = hi1 ^ c[1] ^ k0, n2 = hi0 ^ c[3] ^ k1;
+        c[0] = n0;
+        c[1] = lo1;
+        c[2] = n2;
+        c[3] = lo0;
+    }
+}
+
+// Natural log in float32 as a fixed sequence of correctly rounded operations (no
+// contraction into FMA): x = m 2^e, m in [sqrt(1/2), sqrt(2)), s = (m-1)/(m+1),
+// log x = e ln2 + 2s (1 + s^2/3 + ... + s^10/11) with float32 coefficients.
+__device__ __forceinline__ float keyed_log(float x)
+{
+    uint32_t b = __float_as_uint(x);
+    int e;
+    if ((b >> 23) == 0) {
+        x = __fmul_rn(x, 8388608.0f);
+        b = __float_as_uint(x);
+        e = (int)(b >> 23) - 127 - 23;
+    } else {
+        e = (int)(b >> 23) - 127;
+    }
+    float m = __uint_as_float((b & 0x7fffffu) | 0x3f800000u);
+    if (m > 0x1.6a09e6p+0f) {
+        m = __fmul_rn(m, 0.5f);
+        e += 1;
+    }
+    const float sv = __fdiv_rn(__fsub_rn(m, 1.0f), __fadd_rn(m, 1.0f));
+    const float z = __fmul_rn(sv, sv);
+    float q = 0x1.745d18p-4f;
+    q = __fadd_rn(__fmul_rn(q, z), 0x1.c71c72p-4f);
+    q = __fadd_rn(__fmul_rn(q, z), 0x1.24924ap-3f);
+    q = __fadd_rn(__fmul_rn(q, z), 0x1.99999ap-3f);
+    q = __fadd_rn(__fmul_rn(q, z), 0x1.555556p-2f);
+    q = __fadd_rn(__fmul_rn(q, z), 1.0f);
+    const float rr = __fmul_rn(__fadd_rn(sv, sv), q);
+    return __fadd_rn(__fmul_rn(__int2float_rn(e), 0x1.62e43p-1f), rr);
+}
+
+// Gumbel noise from the top 23 bits of one Philox output word.
+__device__ __forceinline__ float gumbel_of(uint32_t w)
+{
+    const float u = __fmul_rn(__fadd_rn(__uint2float_rn(w >> 9), 0.5f), 0x1p-23f);
+    return -keyed_log(-keyed_log(u));
+}
+
+// Sampling pass: per (slice, row), the best l/T + g(seed, pos, v) over the tokens with
+// l >= l_max + off (off = T log(min_p), or -inf), ties to the lowest token.  The row
+// maximum comes from the argmax pass's slices.  Token v is keyed by word (v mod 4) of
+// Philox(ctr = (v / 4, pos, 0x6b657964, 0), key = seed).
+__global__ void __launch_bounds__(kArgmaxThreads)
+sample_chunks_kernel(const float *__restrict__ logits, int vocab, int chunk, int n_chunks,
+                     const float2 *__restrict__ part_max, float2 *__restrict__ part,
+                     const int32_t *__restrict__ positions, uint32_t seed_lo, uint32_t seed_hi,
+                     float temperature, float off, int vec_ok)
+{
+    const int c = blockIdx.x, r = blockIdx.y;
+    const int lo = c * chunk;
+    const int hi = min(vocab, lo + chunk);
+    const float *row = logits + (size_t)r * vocab;
+    float l_max = -INFINITY;
+    for (int i = 0; i < n_chunks; ++i)
+        l_max = fmaxf(l_max, part_max[(size_t)r * n_chunks + i].x);
+    const float thr = off == -INFINITY ? -INFINITY : __fadd_rn(l_max, off);
+    const uint32_t pos = (uint32_t)__ldg(positions + r);
+    Best b = {-INFINITY, kNoIndex};
+    if (vec_ok) {
+        const float4 *row4 = reinterpret_cast<const float4 *>(row);
+        for (int i = (lo >> 2) + threadIdx.x; i < (hi >> 2); i += kArgmaxThreads) {
+            const float4 x = __ldcs(row4 + i);
+            uint32_t w[4] = {(uint32_t)i, pos, 0x6b657964u, 0u};
+            philox4x32_10(w, seed_lo, seed_hi);
+            const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (xs[j] >= thr)
+                    b = better(b, Best{__fadd_rn(__fdiv_rn(xs[j], temperature), gumbel_of(w[j])), 4 * i + j});
+        }
+    } else {
+        for (int v = lo + threadIdx.x; v < hi; v += kArgmaxThreads) {
+            const float x = __ldcs(row + v);
+            if (!(x >= thr))
+                continue;
+            uint32_t w[4] = {(uint32_t)v >> 2, pos, 0x6b657964u, 0u};
+            philox4x32_10(w, seed_lo, seed_hi);
+            const uint32_t word = (v & 3) == 0 ? w[0] : (v & 3) == 1 ? w[1] : (v & 3) == 2 ? w[2] : w[3];
+            b = better(b, Best{__fadd_rn(__fdiv_rn(x, temperature), gumbel_of(word)), v});
+        }
+    }
+    b = warp_best(b);
+    __shared__ Best sm[kArgmaxThreads / 32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0)
+        sm[warp] = b;
+    __syncthreads();
+    if (warp == 0) {
+        b = lane < kArgmaxThreads / 32 ? sm[lane] : Best{-INFINITY, kNoIndex};
+        b = warp_best(b);
+        if (lane == 0)
+            part[(size_t)r * n_chunks + c] = make_float2(b.v, __int_as_float(b.i));
+    }
+}
+
 constexpr int kTreeMaxNodes = 1024;
 
-// Greedy accept over draft trees: one warp per sequence.  The slices of each row are
+// Accept over draft trees (or chains when parents is null): one warp per sequence.  The slices of each row are
 // merged into argmax_out (and shared memory), then from the root the walk takes, at
 // node u, the lowest-index child c (parents[c] == u) whose draft equals a_u, found by
 // a ballot over 32 candidates at a time.
@@ -160,7 +276,7 @@ accept_tree_walk_kernel(const float2 *__restrict__ part, int n_chunks, const int
         return;
     }
     bool bad = r0 < 0 || r0 + W > total_rows || W > kTreeMaxNodes;
-    for (int j = 1 + lane; !bad && j < W; j += 32)
+    for (int j = 1 + lane; parents && !bad && j < W; j += 32)
         if (parents[r0 + j] < 0 || parents[r0 + j] >= j)
             bad = true;
     if (__any_sync(0xffffffffu, bad)) {
@@ -190,7 +306,7 @@ accept_tree_walk_kernel(const float2 *__restrict__ part, int n_chunks, const int
         int next = -1;
         for (int base = u + 1; base < W && next < 0; base += 32) {
             const int c = base + lane;
-            const bool hit = c < W && parents[r0 + c] == u && drafts[r0 + c] == target;
+            const bool hit = c < W && (parents ? parents[r0 + c] : c - 1) == u && drafts[r0 + c] == target;
             const unsigned m = __ballot_sync(0xffffffffu, hit);
             if (m)
                 next = base + __ffs(m) - 1;
@@ -315,4 +431,66 @@ extern "C" int spec_accept_tree_greedy(const float *logits, int32_t vocab, const
     accept_tree_walk_kernel<<<num_seqs, 32, 0, st>>>(part, n_chunks, q_starts, draft_tokens, parents, total_rows,
                                                      argmax_out, accept_len, out_tokens, accepted_rows, status);
     return check_cuda(cudaGetLastError(), "spec_accept_tree_greedy walk launch");
+}
+
+extern "C" int spec_accept_sampled(const float *logits, int32_t vocab, const int32_t *q_starts,
+                                   const int32_t *draft_tokens, const int32_t *parents, const int32_t *positions,
+                                   uint64_t seed, float temperature, float min_p, int32_t num_seqs,
+                                   int32_t total_rows, int32_t *sampled_out, int32_t *accept_len,
+                                   int32_t *out_tokens, int32_t *accepted_rows, void *workspace,
+                                   size_t workspace_bytes, void *stream)
+{
+    using namespace pkv;
+    clear_error();
+    if (num_seqs < 0 || total_rows < 0 || vocab <= 0)
+        return set_error(PKV_ERR_SHAPE, "spec_accept_sampled: bad sizes (num_seqs %d, rows %d, vocab %d)",
+                         num_seqs, total_rows, vocab);
+    if (!(temperature >= 0.0f) || !(temperature < INFINITY) || !(min_p <= 1.0f))
+        return set_error(PKV_ERR_SHAPE, "spec_accept_sampled: temperature %g must be finite and >= 0, "
+                         "min_p %g at most 1", (double)temperature, (double)min_p);
+    if (num_seqs == 0)
+        return PKV_OK;
+    if (!q_starts || !accept_len || (total_rows > 0 && (!logits || !draft_tokens || !positions || !sampled_out ||
+                                                        !out_tokens || !accepted_rows || !workspace)))
+        return set_error(PKV_ERR_NULL, "spec_accept_sampled: a required pointer is NULL");
+    if (total_rows > 0 && !aligned16(logits))
+        return set_error(PKV_ERR_ALIGN, "spec_accept_sampled: logits must be 16-byte aligned");
+    const size_t one = spec_accept_workspace_size(total_rows, vocab);
+    if (workspace_bytes < 2 * one)
+        return set_error(PKV_ERR_WORKSPACE, "spec_accept_sampled: workspace %zu < %zu bytes", workspace_bytes,
+                         2 * one);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int n_chunks = accept_chunks(total_rows, vocab, sm_count());
+    float2 *part_max = static_cast<float2 *>(workspace);
+    float2 *part = reinterpret_cast<float2 *>(static_cast<uint8_t *>(workspace) + one);
+    if (total_rows > 0) {
+        if (total_rows > 65535)
+            return set_error(PKV_ERR_SHAPE, "spec_accept_sampled: at most 65535 rows per call");
+        int chunk = (vocab + n_chunks - 1) / n_chunks;
+        chunk = (chunk + 3) & ~3;
+        const int vec_ok = (vocab % 4) == 0;
+        argmax_chunks_kernel<<<dim3(n_chunks, total_rows), kArgmaxThreads, 0, st>>>(logits, vocab, chunk, n_chunks,
+                                                                                   part_max, vec_ok);
+        int rc = check_cuda(cudaGetLastError(), "spec_accept_sampled argmax launch");
+        if (rc)
+            return rc;
+        if (temperature > 0.0f) {
+            // the min_p threshold's offset T log(min_p), rounded once here and once in the kernel's add
+            const float off = min_p > 0.0f ? temperature * logf(min_p) : -INFINITY;
+            sample_chunks_kernel<<<dim3(n_chunks, total_rows), kArgmaxThreads, 0, st>>>(
+                logits, vocab, chunk, n_chunks, part_max, part, positions, (uint32_t)seed, (uint32_t)(seed >> 32),
+                temperature, off, vec_ok);
+            rc = check_cuda(cudaGetLastError(), "spec_accept_sampled sample launch");
+            if (rc)
+                return rc;
+        } else {
+            part = part_max;   // temperature 0: the greedy draw
+        }
+    }
+    int32_t *status = device_status_word();
+    if (!status)
+        return set_error(PKV_ERR_CUDA, "spec_accept_sampled: no device status word");
+    accept_tree_walk_kernel<<<num_seqs, 32, 0, st>>>(part, n_chunks, q_starts, draft_tokens, parents, total_rows,
+                                                     sampled_out, accept_len, out_tokens, accepted_rows, status);
+    return check_cuda(cudaGetLastError(), "spec_accept_sampled walk launch");
 }

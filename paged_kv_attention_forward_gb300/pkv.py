@@ -27,7 +27,8 @@ STATUS_NAMES = {0: "PKV_OK", -1: "PKV_ERR_NULL", -2: "PKV_ERR_SHAPE", -3: "PKV_E
 EXPORTED = ("pkv_abi_version", "paged_kv_append", "paged_attention_workspace_size",
             "paged_attention_workspace_init", "paged_attention_forward", "spec_accept_workspace_size",
             "spec_accept_greedy", "pkv_last_error_string", "pkv_device_status",
-            "paged_attention_forward_noalloc", "paged_tree_attention_forward", "spec_accept_tree_greedy")
+            "paged_attention_forward_noalloc", "paged_tree_attention_forward", "spec_accept_tree_greedy",
+            "spec_accept_sampled")
 
 
 class PkvError(RuntimeError):
@@ -81,6 +82,9 @@ def lib(build_if_missing: bool = False):
             L.paged_tree_attention_forward.restype = ctypes.c_int
             L.spec_accept_tree_greedy.argtypes = [P, i32, P, P, P, i32, i32, P, P, P, P, P, sz, P]
             L.spec_accept_tree_greedy.restype = ctypes.c_int
+            L.spec_accept_sampled.argtypes = [P, i32, P, P, P, P, ctypes.c_uint64, ctypes.c_float,
+                                              ctypes.c_float, i32, i32, P, P, P, P, P, sz, P]
+            L.spec_accept_sampled.restype = ctypes.c_int
             L.spec_accept_workspace_size.argtypes = [i32, i32]
             L.spec_accept_workspace_size.restype = sz
             L.spec_accept_greedy.argtypes = [P, i32, P, P, i32, i32, P, P, P, P, sz, P]
@@ -216,6 +220,28 @@ def spec_accept_tree_greedy(logits, q_starts, draft_tokens, parents, *, argmax_o
                                          _dptr(accepted_rows), _dptr(workspace), workspace.numel(),
                                          _stream(stream)))
     return argmax_out, accept_len, out_tokens, accepted_rows
+
+
+def spec_accept_sampled(logits, q_starts, draft_tokens, positions, *, seed: int, temperature: float,
+                        min_p: float = 0.0, parents=None, sampled_out=None, accept_len=None, out_tokens=None,
+                        accepted_rows=None, workspace=None, stream=None):
+    """Keyed sampled accept (see include/pkv.h);
+    returns (sampled [R], accept_len [S], out_tokens [R], accepted_rows [R])."""
+    R, V = logits.shape
+    S = q_starts.shape[0] - 1
+    dev = logits.device
+    mk = lambda n: torch.empty(n, dtype=torch.int32, device=dev)  # noqa: E731
+    sampled_out = mk(R) if sampled_out is None else sampled_out
+    accept_len = mk(S) if accept_len is None else accept_len
+    out_tokens = mk(R) if out_tokens is None else out_tokens
+    accepted_rows = mk(R) if accepted_rows is None else accepted_rows
+    if workspace is None:
+        workspace = torch.empty(max(2 * spec_accept_workspace_size(R, V), 256), dtype=torch.uint8, device=dev)
+    _check(lib().spec_accept_sampled(_dptr(logits), V, _dptr(q_starts), _dptr(draft_tokens), _dptr(parents),
+                                     _dptr(positions), int(seed), float(temperature), float(min_p), S, R,
+                                     _dptr(sampled_out), _dptr(accept_len), _dptr(out_tokens),
+                                     _dptr(accepted_rows), _dptr(workspace), workspace.numel(), _stream(stream)))
+    return sampled_out, accept_len, out_tokens, accepted_rows
 
 
 def spec_accept_workspace_size(total_rows, vocab) -> int:

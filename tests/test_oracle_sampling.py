@@ -122,7 +122,7 @@ def colliding_tokens(oracle_mod, seed, pos, limit=30000):
     seen = {}
     key = [seed & 0xFFFFFFFF, seed >> 32]
     for v in range(limit):
-        u = int(oracle_mod.philox4x32_10([v, pos, 0x6B657964, 0], key)[0]) >> 9
+        u = int(oracle_mod.philox4x32_10([v >> 2, pos, 0x6B657964, 0], key)[v & 3]) >> 9
         if u in seen:
             return seen[u], v
         seen[u] = v
