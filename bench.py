@@ -207,13 +207,19 @@ def run_ours(args, rank, world, local_rank):
     tree = b.tree_masks is not None
     tree_masks = d(b.tree_masks.view(np.int32)) if tree else None
     parents = d(b.parents) if tree else None
+    positions = None
     if b.logits is not None:
         logits, drafts = d(b.logits), d(b.draft_tokens)
-        acc_ws = torch.empty(pkv.spec_accept_workspace_size(b.total_q_rows, b.logits.shape[1]),
+        acc_ws = torch.empty(2 * pkv.spec_accept_workspace_size(b.total_q_rows, b.logits.shape[1]),
                              dtype=torch.uint8, device=dev)
+        # absolute position of the token each verify row draws: L - W + w + 1
+        row_seq = np.searchsorted(b.q_starts, np.arange(b.total_q_rows), side="right") - 1
+        w_of = np.arange(b.total_q_rows) - b.q_starts[row_seq]
+        positions = d((b.context_lens[row_seq] - np.diff(b.q_starts)[row_seq] + w_of + 1).astype(np.int32))
         acc_out = tuple(torch.empty(n, dtype=torch.int32, device=dev)
                         for n in (b.total_q_rows, b.num_seqs, b.total_q_rows, b.total_q_rows))
     has_append = int(b.new_starts[-1]) > 0
+    accept_mode = getattr(args, "accept", "greedy")
     max_ctx, max_rows = b.max_context_len, b.max_q_rows_per_seq
     stream = torch.cuda.current_stream()
     # per layer: append (if any) + attention split kernel + attention merge kernel; accept: 2
@@ -238,7 +244,12 @@ def run_ours(args, rank, world, local_rank):
             if ev_pairs is not None:
                 ev_pairs[li][1].record(stream)
                 li += 1
-        if logits is not None and tree:
+        if logits is not None and accept_mode == "sampled":
+            pkv.spec_accept_sampled(logits, q_starts, drafts, positions, seed=args.seed + 1, temperature=1.0,
+                                    min_p=0.05, parents=parents, sampled_out=acc_out[0], accept_len=acc_out[1],
+                                    out_tokens=acc_out[2], accepted_rows=acc_out[3], workspace=acc_ws,
+                                    stream=stream)
+        elif logits is not None and tree:
             pkv.spec_accept_tree_greedy(logits, q_starts, drafts, parents, argmax_out=acc_out[0],
                                         accept_len=acc_out[1], out_tokens=acc_out[2], accepted_rows=acc_out[3],
                                         workspace=acc_ws, stream=stream)
@@ -308,6 +319,10 @@ def run_ours(args, rank, world, local_rank):
         h_inputs += [pin(b.tree_masks.view(np.int32)), pin(b.parents)]
         d_inputs += [tree_masks, parents]
         h2d += 2 * b.total_q_rows * 4
+    if positions is not None:
+        h_inputs.append(pin(positions.cpu().numpy()))
+        d_inputs.append(positions)
+        h2d += b.total_q_rows * 4
 
     def e2e_step():
         for hsrc, ddst in zip(h_inputs, d_inputs):
@@ -365,7 +380,8 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": workload_description(b, layers), "global_batch": b.num_seqs * world,
                    "seq_len": b.max_context_len, "parallelism": f"dp{world} (independent replicas)",
                    "l2": "inputs larger than L2 (K/V read per step >> 129 MB); no flush",
-                   "seed": args.seed},
+                   "seed": args.seed,
+                   "accept": None if b.logits is None else accept_mode},
         "query_rows_per_s": round(rows_per_s, 1),
         "frac_of_measured_hbm": round(value / peak, 4),
         "frac_of_nominal_8tbs": round(value / 8000.0, 4),
@@ -484,6 +500,8 @@ def main():
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="resize the batch (same per-sequence distribution); for profiling smaller cases")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--accept", choices=("greedy", "sampled"), default="greedy",
+                    help="verify workloads: greedy accept, or keyed sampling at T = 1, min_p = 0.05")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
