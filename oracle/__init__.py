@@ -74,6 +74,12 @@ def _load():
             lib.oracle_spec_accept_sampled.argtypes = [P, i32, P, P, P, P, ctypes.c_uint64, ctypes.c_float,
                                                        ctypes.c_float, i32, P, P, P, P]
             lib.oracle_spec_accept_sampled.restype = ctypes.c_int
+            lib.oracle_fnv1a64.argtypes = [P, ctypes.c_int64]
+            lib.oracle_fnv1a64.restype = ctypes.c_uint64
+            lib.oracle_splitmix64_mix.argtypes = [ctypes.c_uint64]
+            lib.oracle_splitmix64_mix.restype = ctypes.c_uint64
+            lib.oracle_block_hashes.argtypes = [P, P, i32, i32, ctypes.c_uint64, P, P, i32]
+            lib.oracle_block_hashes.restype = ctypes.c_int
             _lib = lib
         return _lib
 
@@ -231,3 +237,27 @@ def spec_accept_sampled(logits, q_starts, draft_tokens, positions, seed, tempera
     if rc != 0:
         raise ValueError(f"oracle_spec_accept_sampled failed with status {rc}")
     return sm, al, ot, ar
+
+
+def fnv1a64(data: bytes) -> int:
+    buf = np.frombuffer(bytes(data), dtype=np.uint8) if len(data) else np.zeros(1, np.uint8)
+    return int(_load().oracle_fnv1a64(_ptr(np.ascontiguousarray(buf)), len(data)))
+
+
+def splitmix64_mix(z: int) -> int:
+    return int(_load().oracle_splitmix64_mix(z & 0xFFFFFFFFFFFFFFFF))
+
+
+def block_hashes(tokens, token_starts, block_size, seed, max_blocks_per_seq, chain_in=None):
+    """Chained keys of every full block: uint64 [S, max_blocks_per_seq] (0 past the full blocks)."""
+    lib = _load()
+    tk = _c(tokens, np.int32)
+    ts = _c(token_starts, np.int32)
+    s = ts.shape[0] - 1
+    ci = None if chain_in is None else _c(chain_in, np.uint64)
+    out = np.empty((s, max_blocks_per_seq), dtype=np.uint64)
+    rc = lib.oracle_block_hashes(_ptr(tk), _ptr(ts), s, int(block_size), int(seed),
+                                 None if ci is None else _ptr(ci), _ptr(out), int(max_blocks_per_seq))
+    if rc != 0:
+        raise ValueError(f"oracle_block_hashes failed with status {rc}")
+    return out

@@ -512,3 +512,80 @@ int oracle_spec_accept_sampled(const float *logits, int32_t vocab, const int32_t
     }
     return 0;
 }
+
+/* -------------------------------------------------------- block hashing -- */
+/*
+ * Content keys of full KV blocks for prefix sharing (TensorSharp "高级功能",
+ * "连续批处理与分页 KV 缓存": every full block is content-hashed, so identical
+ * prefixes, such as a shared system prompt, map to the same blocks).  A block is
+ * only interchangeable with another if everything before it matches too, so a
+ * block's key names its whole prefix by chaining:
+ *   c_i = FNV-1a 64 over the little-endian bytes of the block's B token ids
+ *         (offset basis 0xcbf29ce484222325, prime 0x100000001b3);
+ *   h_0 = chain_in[s] (or `seed` when chain_in is NULL);
+ *   h_{i+1} = mix(h_i ^ c_i), mix = the SplitMix64 output function
+ *         z ^= z >> 30; z *= 0xbf58476d1ce4e5b9; z ^= z >> 27;
+ *         z *= 0x94d049bb133111eb; z ^= z >> 31;
+ *   key of block i = h_{i+1}.
+ * Sequence s's tokens [token_starts[s], token_starts[s+1]) start at a block
+ * boundary; only its floor(n / B) full blocks get keys (a partial block is never
+ * shared), written to hashes_out[s][0 ..]; the rest of the row is set to 0.
+ * Passing the key of the last block already hashed as chain_in continues a chain,
+ * so a decode step hashes only the blocks that have just filled up.
+ */
+uint64_t oracle_fnv1a64(const uint8_t *bytes, int64_t n)
+{
+    uint64_t h = 0xcbf29ce484222325ull;
+    for (int64_t i = 0; i < n; ++i) {
+        h ^= bytes[i];
+        h *= 0x100000001b3ull;
+    }
+    return h;
+}
+
+uint64_t oracle_splitmix64_mix(uint64_t z)
+{
+    z ^= z >> 30;
+    z *= 0xbf58476d1ce4e5b9ull;
+    z ^= z >> 27;
+    z *= 0x94d049bb133111ebull;
+    z ^= z >> 31;
+    return z;
+}
+
+int oracle_block_hashes(const int32_t *tokens, const int32_t *token_starts, int32_t num_seqs,
+                        int32_t block_size, uint64_t seed, const uint64_t *chain_in,
+                        uint64_t *hashes_out, int32_t max_blocks_per_seq)
+{
+    if (block_size <= 0 || block_size > 1024)
+        return -2;
+    uint8_t *buf = (uint8_t *)malloc(4 * (size_t)block_size);
+    if (!buf)
+        return -3;
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        const int64_t n = (int64_t)token_starts[s + 1] - token_starts[s];
+        const int64_t full = n > 0 ? n / block_size : 0;
+        if (full > max_blocks_per_seq) {
+            free(buf);
+            return -1;
+        }
+        uint64_t *row = hashes_out + (int64_t)s * max_blocks_per_seq;
+        for (int64_t i = 0; i < max_blocks_per_seq; ++i)
+            row[i] = 0;
+        uint64_t h = chain_in ? chain_in[s] : seed;
+        for (int64_t i = 0; i < full; ++i) {
+            const int32_t *blk = tokens + token_starts[s] + i * block_size;
+            for (int32_t t = 0; t < block_size; ++t) {
+                const uint32_t v = (uint32_t)blk[t];
+                buf[4 * t + 0] = (uint8_t)(v & 0xffu);
+                buf[4 * t + 1] = (uint8_t)((v >> 8) & 0xffu);
+                buf[4 * t + 2] = (uint8_t)((v >> 16) & 0xffu);
+                buf[4 * t + 3] = (uint8_t)((v >> 24) & 0xffu);
+            }
+            h = oracle_splitmix64_mix(h ^ oracle_fnv1a64(buf, 4 * (int64_t)block_size));
+            row[i] = h;
+        }
+    }
+    free(buf);
+    return 0;
+}
