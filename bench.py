@@ -90,7 +90,7 @@ def stored_traffic(kernel: str, workload: str):
         if ":" in ln and not ln.startswith("#"):
             k, _, v = ln.partition(":")
             vals[k.strip()] = v.strip()
-    if vals.get("source_digest") != build.source_digest():
+    if vals.get("source_digest") != build.source_digest(build.ATTENTION_SOURCES):
         return None
     try:
         return float(vals["dram_bytes_per_launch"])

@@ -77,7 +77,8 @@ enum {
     PKV_DEV_TOO_MANY_ROWS = 4, /* a sequence with more rows than max_q_rows_per_seq       */
     PKV_DEV_WORKSPACE = 8,     /* (reserved)                                              */
     PKV_DEV_TIMEOUT = 16,      /* a bounded wait expired                                  */
-    PKV_DEV_BAD_TREE = 32      /* a draft tree whose parent indices are not topological   */
+    PKV_DEV_BAD_TREE = 32,     /* a draft tree whose parent indices are not topological   */
+    PKV_DEV_BAD_RANGE = 64     /* a token range outside [0, total_tokens]                 */
 };
 
 /* One layer's K/V block pool (host struct holding device pointers).
@@ -320,13 +321,40 @@ int spec_accept_sampled(const float *logits, int32_t vocab,
                         int32_t *accepted_rows, void *workspace, size_t workspace_bytes,
                         void *stream);
 
+/*
+ * Chained content keys of full KV blocks, for prefix sharing (TensorSharp
+ * "高级功能", section "连续批处理与分页 KV 缓存": every full block is
+ * content-hashed, so identical prefixes map to the same blocks).  For sequence s
+ * with tokens tokens[token_starts[s] .. token_starts[s+1]) (starting at a block
+ * boundary), block i of its floor(n / block_size) full blocks gets
+ *   c_i = FNV-1a 64 over the little-endian bytes of the block's token ids,
+ *   h_0 = chain_in[s] (seed when chain_in is NULL), h_{i+1} = mix(h_i ^ c_i),
+ *   hashes_out[s][i] = h_{i+1},
+ * mix being the SplitMix64 output function.  The rest of row s is set to 0 (a
+ * partial block is never shared).  Passing the key of the last block already
+ * hashed as chain_in[s] continues the chain, so a decode step re-hashes nothing.
+ *   tokens        int32 [total_tokens]            (device)
+ *   token_starts  int32 [num_seqs + 1]            (device)
+ *   chain_in      uint64 [num_seqs] or NULL       (device)
+ *   hashes_out    uint64 [num_seqs][max_blocks_per_seq] (device, written)
+ * block_size in [1, 1024].  A sequence with more full blocks than
+ * max_blocks_per_seq gets keys for the first max_blocks_per_seq and sets
+ * PKV_DEV_TABLE_OVERRUN; a token range outside [0, total_tokens] leaves its row
+ * zero and sets PKV_DEV_BAD_RANGE.  One kernel launch, no workspace.
+ */
+int paged_block_hashes(const int32_t *tokens, const int32_t *token_starts, int32_t num_seqs,
+                       int32_t total_tokens, int32_t block_size, uint64_t seed,
+                       const uint64_t *chain_in, uint64_t *hashes_out,
+                       int32_t max_blocks_per_seq, void *stream);
+
 /* Text of the calling thread's last error ("" if none). */
 const char *pkv_last_error_string(void);
 
 /*
  * Synchronise `stream`, then read and clear the device status word of the
  * current device.  Returns PKV_OK, PKV_ERR_BAD_BLOCK (bad block id or table
- * overrun), PKV_ERR_SHAPE (too many rows, or a bad draft tree), PKV_ERR_TIMEOUT,
+ * overrun), PKV_ERR_SHAPE (too many rows, a bad draft tree or a bad token
+ * range), PKV_ERR_TIMEOUT,
  * or PKV_ERR_CUDA; *bits (if not NULL) receives the raw PKV_DEV_* bits.
  */
 int pkv_device_status(void *stream, int32_t *bits);

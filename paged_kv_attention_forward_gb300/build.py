@@ -33,10 +33,19 @@ def sources():
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def source_digest() -> str:
-    """Hash of every source and header the library is built from."""
+# the files the attention kernels are compiled from (a profile of those kernels stays
+# valid while these are unchanged)
+ATTENTION_SOURCES = ("pkv_attention.cu", "pkv_ptx.cuh", "pkv_internal.h")
+
+
+def source_digest(names=None) -> str:
+    """Hash of every source and header the library is built from, or of the named
+    files of csrc/ only."""
     h = hashlib.sha256()
-    files = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC)) + [os.path.join(INCLUDE, "pkv.h")]
+    if names is None:
+        files = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC)) + [os.path.join(INCLUDE, "pkv.h")]
+    else:
+        files = [os.path.join(CSRC, f) for f in names]
     for f in files:
         h.update(os.path.basename(f).encode())
         with open(f, "rb") as fh:

@@ -117,5 +117,8 @@ extern "C" int pkv_device_status(void *stream, int32_t *bits)
     if (host & PKV_DEV_BAD_TREE)
         return pkv::set_error(PKV_ERR_SHAPE,
                               "a draft tree had a parent index outside [0, node) (bits 0x%x)", host);
+    if (host & PKV_DEV_BAD_RANGE)
+        return pkv::set_error(PKV_ERR_SHAPE,
+                              "a token range lay outside [0, total_tokens] (bits 0x%x)", host);
     return PKV_OK;
 }

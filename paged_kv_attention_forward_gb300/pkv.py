@@ -28,7 +28,7 @@ EXPORTED = ("pkv_abi_version", "paged_kv_append", "paged_attention_workspace_siz
             "paged_attention_workspace_init", "paged_attention_forward", "spec_accept_workspace_size",
             "spec_accept_greedy", "pkv_last_error_string", "pkv_device_status",
             "paged_attention_forward_noalloc", "paged_tree_attention_forward", "spec_accept_tree_greedy",
-            "spec_accept_sampled")
+            "spec_accept_sampled", "paged_block_hashes")
 
 
 class PkvError(RuntimeError):
@@ -85,6 +85,8 @@ def lib(build_if_missing: bool = False):
             L.spec_accept_sampled.argtypes = [P, i32, P, P, P, P, ctypes.c_uint64, ctypes.c_float,
                                               ctypes.c_float, i32, i32, P, P, P, P, P, sz, P]
             L.spec_accept_sampled.restype = ctypes.c_int
+            L.paged_block_hashes.argtypes = [P, P, i32, i32, i32, ctypes.c_uint64, P, P, i32, P]
+            L.paged_block_hashes.restype = ctypes.c_int
             L.spec_accept_workspace_size.argtypes = [i32, i32]
             L.spec_accept_workspace_size.restype = sz
             L.spec_accept_greedy.argtypes = [P, i32, P, P, i32, i32, P, P, P, P, sz, P]
@@ -266,6 +268,21 @@ def spec_accept_greedy(logits, q_starts, draft_tokens, *, argmax_out=None, accep
                                     _dptr(argmax_out), _dptr(accept_len), _dptr(out_tokens),
                                     _dptr(workspace), workspace.numel(), _stream(stream)))
     return argmax_out, accept_len, out_tokens
+
+
+def paged_block_hashes(tokens, token_starts, block_size: int, seed: int, max_blocks_per_seq: int, *,
+                       chain_in=None, out=None, stream=None):
+    """Chained content keys of full blocks (see include/pkv.h).
+
+    tokens int32 [T], token_starts int32 [S+1], chain_in int64 [S] or None (the uint64
+    key bits); returns int64 [S, max_blocks_per_seq] holding the uint64 key bits."""
+    S = token_starts.shape[0] - 1
+    if out is None:
+        out = torch.empty((S, max_blocks_per_seq), dtype=torch.int64, device=token_starts.device)
+    _check(lib().paged_block_hashes(_dptr(tokens), _dptr(token_starts), S, tokens.numel(), int(block_size),
+                                    int(seed) & 0xFFFFFFFFFFFFFFFF, _dptr(chain_in), _dptr(out),
+                                    int(max_blocks_per_seq), _stream(stream)))
+    return out
 
 
 def device_status(stream=None):

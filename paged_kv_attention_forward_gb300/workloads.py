@@ -151,6 +151,7 @@ class PagedBatch:
     planted_targets: Optional[np.ndarray] = None  # int32 [R]: token given the planted maximum
     parents: Optional[np.ndarray] = None       # int32 [R]: draft-tree parent node of each row (-1 at roots)
     tree_masks: Optional[np.ndarray] = None    # uint32 [R]: bit i = the row sees window token i
+    shared_prefix: int = 0                     # tokens the sharing sequences have in common
 
     @property
     def num_seqs(self) -> int:
@@ -275,7 +276,8 @@ def build_batch(seed, *, name: str, lens: np.ndarray, n_new: np.ndarray, q_rows:
                       context_lens_old=old.astype(np.int32), context_lens=lens.astype(np.int32),
                       new_starts=new_starts, k_new=k_new, v_new=v_new, q_starts=q_starts, q=q,
                       causal=causal, sinks=sinks, shared_block_ids=shared_ids.astype(np.int32),
-                      sharing_seqs=np.nonzero(sharing)[0].astype(np.int32))
+                      sharing_seqs=np.nonzero(sharing)[0].astype(np.int32),
+                      shared_prefix=int(shared_prefix) if sharing.any() else 0)
 
 
 def add_verify_logits(batch: PagedBatch, seed, vocab: int, std: float = 2.0,
@@ -403,6 +405,24 @@ def make_workload(name: str, seed: int = 0, filler: str = "random", layers: Opti
     raise KeyError(name)
 
 
+def context_token_ids(batch: PagedBatch, seed, vocab: int = VOCAB):
+    """Token ids of every sequence's context, for the block-key workloads.
+
+    Uniform ids in [0, vocab); the sharing sequences begin with the same
+    batch.shared_prefix ids.  Returns (tokens int32 [sum of context_lens],
+    token_starts int32 [S+1])."""
+    rng = np.random.Generator(np.random.PCG64(_seed_seq(seed)))
+    lens = batch.context_lens.astype(np.int64)
+    starts = np.zeros(len(lens) + 1, np.int64)
+    starts[1:] = np.cumsum(lens)
+    tokens = rng.integers(0, vocab, size=int(starts[-1]), dtype=np.int64).astype(np.int32)
+    if batch.shared_prefix and len(batch.sharing_seqs):
+        prefix = rng.integers(0, vocab, size=batch.shared_prefix, dtype=np.int64).astype(np.int32)
+        for s in batch.sharing_seqs:
+            tokens[starts[s]:starts[s] + batch.shared_prefix] = prefix
+    return tokens, starts.astype(np.int32)
+
+
 def select_seqs(batch: PagedBatch, seqs) -> PagedBatch:
     """A batch holding only the listed sequences (same pool, same physical blocks).
 
@@ -431,7 +451,8 @@ def select_seqs(batch: PagedBatch, seqs) -> PagedBatch:
                      q_starts=q_starts, q=np.ascontiguousarray(batch.q[:, q_idx]),
                      causal=batch.causal, sinks=batch.sinks,
                      shared_block_ids=batch.shared_block_ids,
-                     sharing_seqs=np.nonzero(np.isin(seqs, batch.sharing_seqs))[0].astype(np.int32))
+                     sharing_seqs=np.nonzero(np.isin(seqs, batch.sharing_seqs))[0].astype(np.int32),
+                     shared_prefix=batch.shared_prefix)
     if batch.logits is not None:
         sub.logits = np.ascontiguousarray(batch.logits[q_idx])
         sub.draft_tokens = batch.draft_tokens[q_idx].copy()

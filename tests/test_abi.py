@@ -93,3 +93,10 @@ def test_host_validation_without_device(pkv):
     assert lib.spec_accept_greedy(4096 + 4, 100, 4096, 4096, 1, 1, 4096, 4096, 4096, 4096, 1 << 20,
                                   None) == -7
     assert lib.spec_accept_greedy(4096, 100, 4096, 4096, 1, 1, 4096, 4096, 4096, 4096, 8, None) == -4
+    # paged_block_hashes: argument checks that return before any CUDA call
+    assert lib.paged_block_hashes(4096, None, 1, 16, 16, 0, None, 4096, 4, None) == -1
+    assert lib.paged_block_hashes(4096, 4096, 1, 16, 0, 0, None, 4096, 4, None) == -3
+    assert lib.paged_block_hashes(4096, 4096, 1, 16, 1025, 0, None, 4096, 4, None) == -3
+    assert lib.paged_block_hashes(4096, 4096, -1, 16, 16, 0, None, 4096, 4, None) == -2
+    assert lib.paged_block_hashes(4096, 4096, 1, 16, 16, 0, None, 4096 + 4, 4, None) == -7
+    assert lib.paged_block_hashes(4096, 4096, 0, 16, 16, 0, None, 4096, 4, None) == 0
