@@ -80,6 +80,19 @@ def _load():
             lib.oracle_splitmix64_mix.restype = ctypes.c_uint64
             lib.oracle_block_hashes.argtypes = [P, P, i32, i32, ctypes.c_uint64, P, P, i32]
             lib.oracle_block_hashes.restype = ctypes.c_int
+            lib.oracle_qrecord_bytes.argtypes = [i32, i32, i32]
+            lib.oracle_qrecord_bytes.restype = ctypes.c_size_t
+            lib.oracle_kv_quantize_row.argtypes = [P, i32, i32, P, P]
+            lib.oracle_kv_quantize_row.restype = ctypes.c_int
+            lib.oracle_qcode_offset.argtypes = [i32, i32, i32, i32, i32, i32, P]
+            lib.oracle_qcode_offset.restype = ctypes.c_int64
+            lib.oracle_paged_kv_append_quant.argtypes = [P, i32, i32, i32, i32, i32, P, i32, P, P, P, P, i32]
+            lib.oracle_paged_kv_append_quant.restype = ctypes.c_int
+            lib.oracle_qpool_dequant.argtypes = [P, i32, i32, i32, i32, i32, P, P]
+            lib.oracle_qpool_dequant.restype = None
+            lib.oracle_paged_attention_quant.argtypes = [P, i32, i32, i32, i32, i32, P, P, P, i32, P, i32,
+                                                         i32, P, P, i32, P, ctypes.c_double, P, i32]
+            lib.oracle_paged_attention_quant.restype = ctypes.c_int
             _lib = lib
         return _lib
 
@@ -260,4 +273,93 @@ def block_hashes(tokens, token_starts, block_size, seed, max_blocks_per_seq, cha
                                  None if ci is None else _ptr(ci), _ptr(out), int(max_blocks_per_seq))
     if rc != 0:
         raise ValueError(f"oracle_block_hashes failed with status {rc}")
+    return out
+
+
+# ------------------------------------------------------ quantised KV blocks --
+def qrecord_bytes(block_size, head_dim, bits) -> int:
+    """Bytes of one (block, KV head) record of the quantised pool."""
+    return int(_load().oracle_qrecord_bytes(int(block_size), int(head_dim), int(bits)))
+
+
+def kv_quantize_row(x_bits, bits):
+    """Quantise one bf16 row (uint16 bits [d]); returns (codes int32 [d], scale float32)."""
+    x = _c(x_bits, np.uint16)
+    codes = np.empty(x.shape[0], dtype=np.int32)
+    scale = np.zeros(1, dtype=np.float32)
+    rc = _load().oracle_kv_quantize_row(_ptr(x), x.shape[0], int(bits), _ptr(codes), _ptr(scale))
+    if rc != 0:
+        raise ValueError(f"oracle_kv_quantize_row failed with status {rc}")
+    return codes, scale[0]
+
+
+def qcode_offset(sec, t, i, head_dim, block_size, bits):
+    """(byte offset, bit shift) of the code of (section 0=K / 1=V, slot t, dim i) in a record."""
+    sh = ctypes.c_int32(0)
+    off = _load().oracle_qcode_offset(int(sec), int(t), int(i), int(head_dim), int(block_size), int(bits),
+                                      ctypes.byref(sh))
+    return int(off), int(sh.value)
+
+
+def new_qpool(num_blocks, num_kv_heads, block_size, head_dim, bits, fill=None):
+    """A record pool uint8 [num_blocks, H_kv, record_bytes] (zeros, or the given fill bytes)."""
+    rb = qrecord_bytes(block_size, head_dim, bits)
+    pool = np.zeros((num_blocks, num_kv_heads, rb), dtype=np.uint8)
+    if fill is not None:
+        pool[...] = fill
+    return pool
+
+
+def paged_kv_append_quant(records, block_size, head_dim, bits, block_tables, context_lens_old, new_starts,
+                          k_new, v_new):
+    """Quantise the new tokens' K/V rows into the record pool, in place."""
+    lib = _load()
+    assert records.dtype == np.uint8 and records.flags.c_contiguous
+    nb, hkv, rb = records.shape
+    assert rb == qrecord_bytes(block_size, head_dim, bits)
+    bt = _c(block_tables, np.int32)
+    kn = _c(k_new, np.uint16)
+    vn = _c(v_new, np.uint16)
+    rc = lib.oracle_paged_kv_append_quant(_ptr(records), nb, int(block_size), hkv, int(head_dim), int(bits),
+                                          _ptr(bt), bt.shape[1], _ptr(_c(context_lens_old, np.int32)),
+                                          _ptr(_c(new_starts, np.int32)), _ptr(kn), _ptr(vn),
+                                          len(context_lens_old))
+    if rc != 0:
+        raise ValueError(f"oracle_paged_kv_append_quant failed with status {rc}")
+
+
+def qpool_dequant(records, block_size, head_dim, bits):
+    """Every record read back: float64 K, V [num_blocks, H_kv, block_size, head_dim]."""
+    rec = _c(records, np.uint8)
+    nb, hkv, _ = rec.shape
+    k = np.empty((nb, hkv, block_size, head_dim), dtype=np.float64)
+    v = np.empty_like(k)
+    _load().oracle_qpool_dequant(_ptr(rec), nb, int(block_size), hkv, int(head_dim), int(bits), _ptr(k), _ptr(v))
+    return k, v
+
+
+def paged_attention_quant(records, block_size, head_dim, bits, q, q_starts, block_tables, context_lens,
+                          kv_head_of_q_head=None, sinks=None, causal=False, scale=None, num_threads=None,
+                          tree_masks=None):
+    """paged_attention over the quantised record pool (K, V read back as code * scale)."""
+    lib = _load()
+    rec = _c(records, np.uint8)
+    nb, hkv, _ = rec.shape
+    q = _c(q, np.uint16)
+    r, hq, dq = q.shape
+    assert dq == head_dim
+    bt = _c(block_tables, np.int32)
+    cl = _c(context_lens, np.int32)
+    hm = None if kv_head_of_q_head is None else _c(kv_head_of_q_head, np.int32)
+    sk = None if sinks is None else _c(sinks, np.float32)
+    tm = None if tree_masks is None else _c(tree_masks, np.uint32)
+    if scale is None:
+        scale = 1.0 / np.sqrt(head_dim)
+    out = np.zeros((r, hq, head_dim), dtype=np.float64)
+    rc = lib.oracle_paged_attention_quant(
+        _ptr(rec), int(bits), nb, int(block_size), hkv, int(head_dim), _ptr(q), _ptr(_c(q_starts, np.int32)),
+        _ptr(bt), bt.shape[1], _ptr(cl), cl.shape[0], hq, _ptr(hm), _ptr(sk), int(bool(causal)), _ptr(tm),
+        float(scale), _ptr(out), int(num_threads or default_num_threads()))
+    if rc != 0:
+        raise ValueError(f"oracle_paged_attention_quant failed with status {rc}")
     return out

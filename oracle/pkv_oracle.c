@@ -113,15 +113,26 @@ int oracle_paged_kv_append(uint16_t *k_pool, uint16_t *v_pool,
  * Returns 0, -1 (position beyond table), -2 (block id out of range),
  * -3 (bad head map), -4 (out of memory), -5 (tree window wider than 32).
  */
-int oracle_paged_attention(const uint16_t *k_pool, const uint16_t *v_pool,
-                           int32_t num_blocks, int32_t block_size,
-                           int32_t num_kv_heads, int32_t head_dim,
-                           const uint16_t *q, const int32_t *q_starts,
-                           const int32_t *block_tables, int32_t max_blocks_per_seq,
-                           const int32_t *context_lens, int32_t num_seqs,
-                           int32_t num_q_heads, const int32_t *kv_head_of_q_head,
-                           const float *sinks, int32_t causal, const uint32_t *tree_masks,
-                           double scale, double *out, int32_t num_threads)
+/* Where attention reads K/V rows from: bf16 pools, or quantised block records
+ * (see the quantised KV section below). */
+struct kv_source {
+    const uint16_t *k_pool, *v_pool;   /* bf16 pools, or NULL */
+    const uint8_t *records;            /* quantised records, or NULL */
+    int32_t bits;
+};
+
+static void kv_read_row(const struct kv_source *src, int32_t blk, int32_t g, int32_t off,
+                        int32_t Hkv, int32_t B, int32_t D, double *k, double *v);
+
+static int attention_core(const struct kv_source *src,
+                          int32_t num_blocks, int32_t block_size,
+                          int32_t num_kv_heads, int32_t head_dim,
+                          const uint16_t *q, const int32_t *q_starts,
+                          const int32_t *block_tables, int32_t max_blocks_per_seq,
+                          const int32_t *context_lens, int32_t num_seqs,
+                          int32_t num_q_heads, const int32_t *kv_head_of_q_head,
+                          const float *sinks, int32_t causal, const uint32_t *tree_masks,
+                          double scale, double *out, int32_t num_threads)
 {
     const int32_t B = block_size, D = head_dim, Hkv = num_kv_heads, Hq = num_q_heads;
     if (Hkv <= 0 || Hq % Hkv != 0)
@@ -174,11 +185,7 @@ int oracle_paged_attention(const uint16_t *k_pool, const uint16_t *v_pool,
         }
         for (int64_t t = 0; t < L; ++t) {
             int32_t blk = block_tables[(int64_t)s * max_blocks_per_seq + t / B];
-            size_t base = ((((size_t)blk * Hkv) + g) * B + (size_t)(t % B)) * D;
-            for (int32_t k = 0; k < D; ++k) {
-                K[t * D + k] = bf16_bits_to_f64(k_pool[base + k]);
-                V[t * D + k] = bf16_bits_to_f64(v_pool[base + k]);
-            }
+            kv_read_row(src, blk, g, (int32_t)(t % B), Hkv, B, D, K + t * D, V + t * D);
         }
         /* step 2: every query row of s, every q head that reads KV head g */
         for (int32_t w = 0; w < W; ++w) {
@@ -234,6 +241,22 @@ int oracle_paged_attention(const uint16_t *k_pool, const uint16_t *v_pool,
         free(x);
     }
     return failed ? -4 : 0;
+}
+
+int oracle_paged_attention(const uint16_t *k_pool, const uint16_t *v_pool,
+                           int32_t num_blocks, int32_t block_size,
+                           int32_t num_kv_heads, int32_t head_dim,
+                           const uint16_t *q, const int32_t *q_starts,
+                           const int32_t *block_tables, int32_t max_blocks_per_seq,
+                           const int32_t *context_lens, int32_t num_seqs,
+                           int32_t num_q_heads, const int32_t *kv_head_of_q_head,
+                           const float *sinks, int32_t causal, const uint32_t *tree_masks,
+                           double scale, double *out, int32_t num_threads)
+{
+    struct kv_source src = {k_pool, v_pool, NULL, 16};
+    return attention_core(&src, num_blocks, block_size, num_kv_heads, head_dim, q, q_starts,
+                          block_tables, max_blocks_per_seq, context_lens, num_seqs, num_q_heads,
+                          kv_head_of_q_head, sinks, causal, tree_masks, scale, out, num_threads);
 }
 
 /*
@@ -588,4 +611,264 @@ int oracle_block_hashes(const int32_t *tokens, const int32_t *token_starts, int3
     }
     free(buf);
     return 0;
+}
+
+/* ----------------------------------------------------- quantised KV blocks -- */
+/*
+ * TensorSharp "高级功能", section "内存优化", the KV block codec item: blocks may
+ * be compressed in place to 8 or 4 bits per value (Q8 / Q4, selected by
+ * --paged-kv-quant-bits), trading a small accuracy cost for half or a quarter of
+ * the footprint.  The pages give no codec internals.  The plainest codec with
+ * that footprint, and the one built here:
+ *   every (token, KV head) row x of head_dim bf16 values is quantised
+ *   symmetrically with one float32 scale,
+ *     Q = 127 (8 bits) or 7 (4 bits),
+ *     amax  = max_i |x_i|                       (float32, exact)
+ *     scale = amax / Q                          (float32 division, round to nearest)
+ *     c_i   = clamp(rint(x_i / scale), -Q, Q)   (float32 division; rint ties to even)
+ *             (c_i = 0 for every i when scale == 0),
+ *   and is read back as c_i * scale.  Every step is a correctly rounded float32
+ *   operation, so the codes are reproducible exactly.
+ *
+ * Record layout (our own; one record per (block, KV head), records of a block's
+ * heads adjacent, record = [K codes | V codes | K scales | V scales]):
+ *   C = block_size * head_dim * bits / 8 bytes of codes per section;
+ *   K scale of slot t at byte 2C + 4t, V scale at 2C + 4 block_size + 4t
+ *   (float32, little-endian).
+ *   8-bit codes are sign-magnitude bytes (bit 7 = sign, bits 0-6 = |c|);
+ *   4-bit codes are nibbles holding c + 8.
+ *   Code positions, for slot t and dim i, with 16-byte units of 4 little-endian
+ *   32-bit words:
+ *   K: mt = t/16, g = (t%16)/2, r = t%2, j = i/16, s = i%16,
+ *      c = (s%8)/2, h = s/8, e = s%2, u = 4g + c;
+ *      8-bit: byte ((mt*D/32 + j/2)*32 + u)*16 + ((j%2)*2 + r)*4 + h + 2e
+ *      4-bit: word ((mt*D/64 + j/4)*32 + u)*16 + (j%4)*4, bits 4(2r + h) + 16e
+ *   V: kk = t/16, m = (t%16)/2 + 8(t%2), h = m/8, c = (m%8)/2, e = m%2,
+ *      dm = i/16, g = i%8, r = (i%16)/8, u = 4g + c;
+ *      8-bit: byte C + ((kk*D/32 + dm/2)*32 + u)*16 + ((dm%2)*2 + r)*4 + h + 2e
+ *      4-bit: word C + ((kk*D/64 + dm/4)*32 + u)*16 + (dm%4)*4, bits 4(2h + r) + 16e
+ * Every byte holds codes of one slot only, so tokens of one block can be
+ * appended independently.
+ */
+static int qmax_of(int32_t bits) { return bits == 8 ? 127 : 7; }
+
+static float bf16_bits_to_f32(uint16_t bits)
+{
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+size_t oracle_qrecord_bytes(int32_t block_size, int32_t head_dim, int32_t bits)
+{
+    return 2 * (size_t)block_size * head_dim * bits / 8 + 8 * (size_t)block_size;
+}
+
+int oracle_kv_quantize_row(const uint16_t *x, int32_t d, int32_t bits, int32_t *codes, float *scale_out)
+{
+    if (bits != 8 && bits != 4)
+        return -1;
+    float amax = 0.0f;
+    for (int32_t i = 0; i < d; ++i) {
+        const float a = fabsf(bf16_bits_to_f32(x[i]));
+        if (a > amax)
+            amax = a;
+    }
+    const float qm = (float)qmax_of(bits);
+    const float scale = amax / qm;
+    for (int32_t i = 0; i < d; ++i) {
+        int32_t c = 0;
+        if (scale > 0.0f) {
+            float y = rintf(bf16_bits_to_f32(x[i]) / scale);
+            if (y > qm)
+                y = qm;
+            if (y < -qm)
+                y = -qm;
+            c = (y == y) ? (int32_t)y : 0;
+        }
+        codes[i] = c;
+    }
+    *scale_out = scale;
+    return 0;
+}
+
+/* byte offset of the code of (slot t, dim i) in section sec (0 = K, 1 = V), and
+ * the shift of a 4-bit code within that byte */
+static size_t qcode_pos(int sec, int32_t t, int32_t i, int32_t D, int32_t BS, int32_t bits, int *shift)
+{
+    const size_t C = (size_t)BS * D * bits / 8;
+    size_t byte;
+    if (sec == 0) {
+        const int mt = t / 16, g = (t % 16) / 2, r = t % 2;
+        const int j = i / 16, s = i % 16, c = (s % 8) / 2, h = s / 8, e = s % 2, u = 4 * g + c;
+        if (bits == 8) {
+            byte = ((size_t)(mt * (D / 32) + j / 2) * 32 + u) * 16 + (size_t)((j % 2) * 2 + r) * 4 + h + 2 * e;
+            *shift = 0;
+        } else {
+            const int bit = 4 * (2 * r + h) + 16 * e;
+            byte = ((size_t)(mt * (D / 64) + j / 4) * 32 + u) * 16 + (size_t)(j % 4) * 4 + bit / 8;
+            *shift = bit % 8;
+        }
+    } else {
+        const int kk = t / 16, m = (t % 16) / 2 + 8 * (t % 2), h = m / 8, c = (m % 8) / 2, e = m % 2;
+        const int dm = i / 16, g = i % 8, r = (i % 16) / 8, u = 4 * g + c;
+        if (bits == 8) {
+            byte = C + ((size_t)(kk * (D / 32) + dm / 2) * 32 + u) * 16 + (size_t)((dm % 2) * 2 + r) * 4 + h + 2 * e;
+            *shift = 0;
+        } else {
+            const int bit = 4 * (2 * h + r) + 16 * e;
+            byte = C + ((size_t)(kk * (D / 64) + dm / 4) * 32 + u) * 16 + (size_t)(dm % 4) * 4 + bit / 8;
+            *shift = bit % 8;
+        }
+    }
+    return byte;
+}
+
+/* offset of the code of (sec, t, i) in a record; exported so tests can check the
+ * layout is a bijection onto the code sections */
+int64_t oracle_qcode_offset(int32_t sec, int32_t t, int32_t i, int32_t head_dim, int32_t block_size,
+                            int32_t bits, int32_t *shift)
+{
+    int sh = 0;
+    const size_t b = qcode_pos(sec, t, i, head_dim, block_size, bits, &sh);
+    if (shift)
+        *shift = sh;
+    return (int64_t)b;
+}
+
+static void qrecord_put(uint8_t *rec, int sec, int32_t t, const int32_t *codes, float scale,
+                        int32_t D, int32_t BS, int32_t bits)
+{
+    for (int32_t i = 0; i < D; ++i) {
+        int shift = 0;
+        const size_t b = qcode_pos(sec, t, i, D, BS, bits, &shift);
+        if (bits == 8) {
+            const int32_t c = codes[i];
+            rec[b] = (uint8_t)((c < 0 ? 0x80 : 0) | (c < 0 ? -c : c));
+        } else {
+            const uint8_t nib = (uint8_t)(codes[i] + 8);
+            rec[b] = (uint8_t)((rec[b] & ~(0xF << shift)) | (nib << shift));
+        }
+    }
+    const size_t C = (size_t)BS * D * bits / 8;
+    memcpy(rec + 2 * C + (size_t)sec * 4 * BS + 4 * (size_t)t, &scale, sizeof scale);
+}
+
+static double qrecord_get(const uint8_t *rec, int sec, int32_t t, int32_t i, int32_t D, int32_t BS, int32_t bits)
+{
+    int shift = 0;
+    const size_t b = qcode_pos(sec, t, i, D, BS, bits, &shift);
+    int32_t c;
+    if (bits == 8)
+        c = (rec[b] & 0x80) ? -(int32_t)(rec[b] & 0x7F) : (int32_t)(rec[b] & 0x7F);
+    else
+        c = (int32_t)((rec[b] >> shift) & 0xF) - 8;
+    float scale;
+    const size_t C = (size_t)BS * D * bits / 8;
+    memcpy(&scale, rec + 2 * C + (size_t)sec * 4 * BS + 4 * (size_t)t, sizeof scale);
+    return (double)c * (double)scale;
+}
+
+static void kv_read_row(const struct kv_source *src, int32_t blk, int32_t g, int32_t off,
+                        int32_t Hkv, int32_t B, int32_t D, double *k, double *v)
+{
+    if (src->records) {
+        const size_t rb = oracle_qrecord_bytes(B, D, src->bits);
+        const uint8_t *rec = src->records + ((size_t)blk * Hkv + g) * rb;
+        for (int32_t i = 0; i < D; ++i) {
+            k[i] = qrecord_get(rec, 0, off, i, D, B, src->bits);
+            v[i] = qrecord_get(rec, 1, off, i, D, B, src->bits);
+        }
+        return;
+    }
+    const size_t base = ((((size_t)blk * Hkv) + g) * B + (size_t)off) * D;
+    for (int32_t i = 0; i < D; ++i) {
+        k[i] = bf16_bits_to_f64(src->k_pool[base + i]);
+        v[i] = bf16_bits_to_f64(src->v_pool[base + i]);
+    }
+}
+
+/*
+ * Quantising scatter-append: the slot of new token i of sequence s is found as in
+ * oracle_paged_kv_append; its K row and V row of every KV head are quantised as
+ * above and written into the record of (block, head).  Returns 0, -1 (position
+ * beyond the table), -2 (block id out of range), -3 (bits not 8 or 4).
+ */
+int oracle_paged_kv_append_quant(uint8_t *records, int32_t num_blocks, int32_t block_size,
+                                 int32_t num_kv_heads, int32_t head_dim, int32_t bits,
+                                 const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t *context_lens_old, const int32_t *new_starts,
+                                 const uint16_t *k_new, const uint16_t *v_new, int32_t num_seqs)
+{
+    if (bits != 8 && bits != 4)
+        return -3;
+    const size_t rb = oracle_qrecord_bytes(block_size, head_dim, bits);
+    int32_t *codes = (int32_t *)malloc(sizeof(int32_t) * (size_t)head_dim);
+    if (!codes)
+        return -4;
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        const int32_t n_new = new_starts[s + 1] - new_starts[s];
+        for (int32_t i = 0; i < n_new; ++i) {
+            const int64_t p = (int64_t)context_lens_old[s] + i;
+            const int64_t logical = p / block_size;
+            if (logical >= max_blocks_per_seq) {
+                free(codes);
+                return -1;
+            }
+            const int32_t blk = block_tables[(int64_t)s * max_blocks_per_seq + logical];
+            if (blk < 0 || blk >= num_blocks) {
+                free(codes);
+                return -2;
+            }
+            const int64_t row = (int64_t)new_starts[s] + i;
+            for (int32_t h = 0; h < num_kv_heads; ++h) {
+                uint8_t *rec = records + ((size_t)blk * num_kv_heads + h) * rb;
+                const size_t src = (((size_t)row * num_kv_heads) + h) * head_dim;
+                float scale;
+                oracle_kv_quantize_row(k_new + src, head_dim, bits, codes, &scale);
+                qrecord_put(rec, 0, (int32_t)(p % block_size), codes, scale, head_dim, block_size, bits);
+                oracle_kv_quantize_row(v_new + src, head_dim, bits, codes, &scale);
+                qrecord_put(rec, 1, (int32_t)(p % block_size), codes, scale, head_dim, block_size, bits);
+            }
+        }
+    }
+    free(codes);
+    return 0;
+}
+
+/* Every record read back: k_out, v_out float64 [num_blocks][H_kv][block_size][head_dim]. */
+void oracle_qpool_dequant(const uint8_t *records, int32_t num_blocks, int32_t block_size,
+                          int32_t num_kv_heads, int32_t head_dim, int32_t bits,
+                          double *k_out, double *v_out)
+{
+    struct kv_source src = {NULL, NULL, records, bits};
+    for (int32_t b = 0; b < num_blocks; ++b)
+        for (int32_t g = 0; g < num_kv_heads; ++g)
+            for (int32_t t = 0; t < block_size; ++t) {
+                const size_t o = ((((size_t)b * num_kv_heads) + g) * block_size + t) * head_dim;
+                kv_read_row(&src, b, g, t, num_kv_heads, block_size, head_dim, k_out + o, v_out + o);
+            }
+}
+
+/*
+ * Attention over quantised blocks: the definition of oracle_paged_attention with
+ * K and V read back from the records (c * scale, exact in float64).
+ */
+int oracle_paged_attention_quant(const uint8_t *records, int32_t bits,
+                                 int32_t num_blocks, int32_t block_size,
+                                 int32_t num_kv_heads, int32_t head_dim,
+                                 const uint16_t *q, const int32_t *q_starts,
+                                 const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t *context_lens, int32_t num_seqs,
+                                 int32_t num_q_heads, const int32_t *kv_head_of_q_head,
+                                 const float *sinks, int32_t causal, const uint32_t *tree_masks,
+                                 double scale, double *out, int32_t num_threads)
+{
+    if (bits != 8 && bits != 4)
+        return -6;
+    struct kv_source src = {NULL, NULL, records, bits};
+    return attention_core(&src, num_blocks, block_size, num_kv_heads, head_dim, q, q_starts,
+                          block_tables, max_blocks_per_seq, context_lens, num_seqs, num_q_heads,
+                          kv_head_of_q_head, sinks, causal, tree_masks, scale, out, num_threads);
 }
