@@ -347,6 +347,77 @@ int paged_block_hashes(const int32_t *tokens, const int32_t *token_starts, int32
                        const uint64_t *chain_in, uint64_t *hashes_out,
                        int32_t max_blocks_per_seq, void *stream);
 
+/*
+ * Quantised KV blocks (TensorSharp "高级功能", section "内存优化", the KV block
+ * codec item: blocks may be compressed in place to 8 or 4 bits per value, Q8 /
+ * Q4, for half or a quarter of the footprint at a small accuracy cost).  The
+ * pages give no codec internals; this library's codec:
+ *   each (token, KV head) row x of head_dim bf16 values is stored as one float32
+ *   scale s = max_i |x_i| / Q (Q = 127 for 8 bits, 7 for 4 bits) and codes
+ *   c_i = clamp(rint(x_i / s), -Q, Q) (all 0 when s == 0), every step a correctly
+ *   rounded float32 operation (rint ties to even); it reads back as c_i * s.
+ *   Non-finite inputs give unspecified (but in-range) codes.
+ * Pool: records uint8 [num_blocks][num_kv_heads][R], R = pkv_qrecord_bytes(),
+ * 16-byte aligned.  Record = [K codes | V codes | K scales | V scales]:
+ *   C = block_size * head_dim * bits / 8 bytes of codes per section; the K scale
+ *   of slot t at byte 2C + 4t, the V scale at 2C + 4 block_size + 4t (float32).
+ *   8-bit codes: sign-magnitude bytes (bit 7 sign, bits 0-6 |c|).
+ *   4-bit codes: nibbles holding c + 8.
+ *   Position of the code of slot t, dim i (16-byte units of 4 little-endian
+ *   32-bit words, laid out in the order the attention kernel's tensor-core
+ *   operands consume them):
+ *   K: mt = t/16, g = (t%16)/2, r = t%2, j = i/16, s = i%16,
+ *      c = (s%8)/2, h = s/8, e = s%2, u = 4g + c
+ *      8-bit: byte ((mt*(D/32) + j/2)*32 + u)*16 + ((j%2)*2 + r)*4 + h + 2e
+ *      4-bit: word ((mt*(D/64) + j/4)*32 + u)*16 + (j%4)*4, bits 4(2r + h) + 16e
+ *   V: kk = t/16, m = (t%16)/2 + 8(t%2), h = m/8, c = (m%8)/2, e = m%2,
+ *      dm = i/16, g = i%8, r = (i%16)/8, u = 4g + c
+ *      8-bit: byte C + ((kk*(D/32) + dm/2)*32 + u)*16 + ((dm%2)*2 + r)*4 + h + 2e
+ *      4-bit: word C + ((kk*(D/64) + dm/4)*32 + u)*16 + (dm%4)*4, bits 4(2h + r) + 16e
+ *   (D = head_dim).  A byte never holds codes of two slots.
+ * Built for head_dim 64 / 128 and block_size 16 / 32.
+ */
+typedef struct pkv_qpool {
+    void *records;
+    int32_t num_blocks;
+    int32_t block_size;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t bits;   /* 8 or 4 */
+} pkv_qpool;
+
+/* Bytes of one (block, KV head) record; 0 for unsupported arguments. */
+size_t pkv_qrecord_bytes(int32_t block_size, int32_t head_dim, int32_t bits);
+
+/*
+ * paged_kv_append with quantisation: the slot of every new row is found as in
+ * paged_kv_append and its K and V rows (bf16 [total_new_rows][num_kv_heads]
+ * [head_dim], any 2-byte alignment) are quantised into that slot of the
+ * record of (block, KV head).  Other slots are untouched; rows of one call may
+ * share a block.  Device-side errors as paged_kv_append.  One kernel launch.
+ */
+int paged_kv_append_quant(const pkv_qpool *pool, const int32_t *block_tables,
+                          int32_t max_blocks_per_seq, const int32_t *context_lens_old,
+                          const int32_t *new_starts, const void *k_new, const void *v_new,
+                          int32_t num_seqs, int32_t total_new_rows, void *stream);
+
+/*
+ * paged_attention_forward over a quantised pool: the same definition with K
+ * and V read back as c * s; every other argument, the workspace
+ * (paged_attention_workspace_size), the split / merge structure and the
+ * batch-invariance rules are those of paged_attention_forward.  Within one
+ * codec the arithmetic is fixed by the row's own sequence, so a row computed
+ * in a batch equals the row alone, bit for bit.
+ */
+int paged_attention_forward_quant(const pkv_qpool *pool, const void *q, const int32_t *q_starts,
+                                  const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t *context_lens, int32_t num_seqs, int32_t total_q_rows,
+                                  int32_t max_context_len, int32_t max_q_rows_per_seq,
+                                  int32_t num_q_heads, const int32_t *kv_head_of_q_head,
+                                  const float *sinks, int32_t causal, float scale, void *out,
+                                  int32_t out_dtype, void *workspace, size_t workspace_bytes,
+                                  void *stream);
+
 /* Text of the calling thread's last error ("" if none). */
 const char *pkv_last_error_string(void);
 

@@ -1,0 +1,1009 @@
+// pkv_attention_impl.cuh -- the paged-attention kernels (split + merge) and the host
+// checks shared by the bf16 and the quantised-KV entry points.
+//
+// What it computes: TensorSharp "高级功能", section "原生分页注意力" -- attention of
+// each sequence's query rows over K/V gathered from the paged block pool, with a
+// variant carrying one sink logit per head (GPT OSS).  The causal verify window
+// and the bit-identity rule come from the TensorFold article, section
+// "先记住一条铁律": a verify row uses exactly the serial step's arithmetic, and a
+// row computed in a batch equals the row computed alone.
+//
+// Design (two kernels per call: splits, then merge):
+//  * Work unit = (sequence s, KV head g, split i).  Split i covers keys
+//    [512 i, 512 i + 512) of s.  The split grid depends on the sequence's own
+//    length only, never on the batch, so every row's arithmetic is fixed by
+//    its own sequence.  Grid = (num_seqs * H_kv, ceil(max_context_len / 512)),
+//    split-major, so the first splits of all sequences (where shared prefix
+//    blocks live) run together and re-read shared blocks from L2.
+//  * One producer warp: a single lane reads the block table and issues TMA
+//    tile loads (cp.async.bulk.tensor, 128-byte swizzle) of each K and V block
+//    of the split into an NST-stage shared-memory ring, completion tracked by
+//    mbarriers.
+//  * Consumer warps, each owning 8 * NN query rows of the (s, g) pair: the G q heads
+//    of KV head g times the W rows of s, flattened row = w * G + head_in_group.  A
+//    pair with more rows than one CTA holds is served by adjacent row-group CTAs
+//    that read the same K/V tiles (the second and later from L2).
+//    Per KV block, on mma.sync m16n8k16 (bf16 in, fp32 out) with keys / head dims
+//    on the M side and query rows on the N side (decode has at most 8 rows per KV
+//    head, so nothing is padded to 16 rows): S^T = K q^T, scale, causal / length
+//    mask, online softmax in base 2 (running max m, running sum l of the
+//    bf16-rounded weights), P^T transposed in registers (movmatrix) and
+//    O^T += V^T P^T.
+//    Keys past a row's limit get weight exactly 0, so a verify-window row and the
+//    same row decoded alone go through identical operations.
+//  * Partials (m, l, O) of every split go to the workspace.  A second kernel,
+//    one warp per (query row, q head), merges them in split order:
+//    M = max(m_i, sink), out = sum_i 2^{m_i-M} O_i / (sum_i 2^{m_i-M} l_i + 2^{sink-M}).
+//    It is launched as a programmatic dependent of the split kernel, so its launch
+//    overlaps the split grid's tail; the merge of the longest sequences is no
+//    longer serialised on one CTA at the end.
+//  * Bounded waits only; block ids and lengths are range-checked on the device
+//    (clamped + status bit, never a fault).
+//  * Quantised KV blocks (TensorSharp "高级功能", section "内存优化", the KV block
+//    codec item): the same kernel with BITS = 8 or 4 reads one record per
+//    (block, KV head) with a single bulk copy (codes of K and V + per-key
+//    scales), widens the codes to bf16 in registers, folds each key's K scale
+//    into its score and its V scale into its weight.
+#pragma once
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include <cuda_bf16.h>
+
+#include "pkv_internal.h"
+#include "pkv_ptx.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct AttnParams {
+    const uint16_t *q;            // bf16 [R][Hq][D]
+    const int32_t *q_starts;      // [S+1]
+    const int32_t *block_tables;  // [S][max_blocks]
+    const int32_t *context_lens;  // [S]
+    const float *sinks;           // [Hq] or null
+    const uint32_t *tree_masks;   // [R] or null: bit i = the row sees window token i
+    void *out;                    // [R][Hq][D] bf16 or f32
+    float2 *part_ml;              // [R*Hq*n_max] (m in log2 units, l)
+    float *part_o;                // [R*Hq*n_max][D]
+    const uint8_t *qrec;          // quantised pool: records [num_blocks][H_kv][QRec::kBytes], or null
+    int32_t *status;
+    int32_t num_seqs, max_blocks_per_seq, num_blocks, num_q_heads, num_kv_heads, group, block_size;
+    int32_t n_max, max_context_len, max_rows, total_rows;
+    int32_t row_groups;           // CTAs per (s, g, split), each taking 8 * NN * NMT rows
+    int32_t causal, out_f32;
+    float scale_log2;             // scale * log2(e)
+    int16_t q_head_of[kMaxQHeads];  // q head of (kv head g, member j): q_head_of[g*group + j]
+};
+
+template <int D, int BS>
+struct Tile {
+    static constexpr int kHalves = D / 64;              // 128-byte column boxes per row
+    static constexpr int kBoxBytes = BS * 128;          // one box: BS rows x 128 B
+    static constexpr int kTileBytes = BS * D * 2;       // one KV block of one head
+    static_assert(kSplitTokens % BS == 0, "split must be whole blocks");
+    static_assert(D % 64 == 0, "head_dim multiple of 64");
+    static_assert(BS % 16 == 0, "block size multiple of 16");
+};
+
+// Byte offset of logical (token, 16-byte chunk) inside a swizzled tile:
+// chunk ch of token t lives in box ch/8, row t, at chunk position (ch%8) ^ (t%8).
+template <int BS>
+__device__ __forceinline__ uint32_t tile_off(int tok, int ch)
+{
+    return (uint32_t)((ch >> 3) * (BS * 128) + tok * 128 + (((ch & 7) ^ (tok & 7)) << 4));
+}
+
+// ---- quantised records ------------------------------------------------------
+// One record per (block, KV head): [K codes | V codes | K scales | V scales], the
+// codes of each section in "fragment order": 16-byte units, unit (tile16, u, lane)
+// holding exactly the 4 words lane `lane` feeds to the mma A operand, so a warp
+// reads a section with conflict-free 16-byte loads.  For the 16-key tile mt, A row
+// g + 8r of K is key 16 mt + 2g + r and A column s is dim s of the k-step; the V^T
+// operand uses column s = key 16 kk + (s < 8 ? 2s : 2(s - 8) + 1), the order in
+// which the transposed P^T fragment of K's S^T arrives.  8-bit codes are
+// sign-magnitude bytes (word bytes 0, 2 feed a0/a1, bytes 1, 3 feed a2/a3); 4-bit
+// codes are nibbles holding c + 8.  Full byte-level formula in pkv.h.
+template <int D, int BS, int BITS>
+struct QRec {
+    static constexpr int kCodeBytes = BS * D * BITS / 8;          // one section
+    static constexpr int kK = 0, kV = kCodeBytes;
+    static constexpr int kKs = 2 * kCodeBytes, kVs = 2 * kCodeBytes + 4 * BS;
+    static constexpr int kBytes = 2 * kCodeBytes + 8 * BS;
+    static constexpr int kUnits = BITS == 8 ? D / 32 : D / 64;    // 16-byte units per lane per 16 keys
+    static_assert(BITS == 8 || BITS == 4, "codec width");
+    static_assert(kBytes % 16 == 0, "record must stay 16-byte aligned");
+};
+
+__device__ __forceinline__ uint32_t word_of(const uint4 &u, int i)
+{
+    return i == 0 ? u.x : i == 1 ? u.y : i == 2 ? u.z : u.w;
+}
+
+__device__ __forceinline__ uint32_t sub_bf16x2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// bf16 128 + m is exact for 0 <= m <= 127 (bits 0x4300 | m); subtracting 128 leaves m.
+// Sign-magnitude bytes 0 and 2 of w -> bf16x2 (byte 0 in the low half).
+__device__ __forceinline__ uint32_t q8_lo(uint32_t w)
+{
+    const uint32_t m = sub_bf16x2((w & 0x007F007Fu) | 0x43004300u, 0x43004300u);
+    return m | ((w << 8) & 0x80008000u);
+}
+// bytes 1 and 3 of w -> bf16x2 (byte 1 in the low half)
+__device__ __forceinline__ uint32_t q8_hi(uint32_t w)
+{
+    const uint32_t m = sub_bf16x2(((w >> 8) & 0x007F007Fu) | 0x43004300u, 0x43004300u);
+    return m | (w & 0x80008000u);
+}
+// nibbles at bits 4p and 16 + 4p of w (each c + 8) -> bf16x2 of c: 128 + n - 136
+template <int P>
+__device__ __forceinline__ uint32_t q4_pair(uint32_t w)
+{
+    return sub_bf16x2(((w >> (4 * P)) & 0x000F000Fu) | 0x43004300u, 0x43084308u);
+}
+
+// A operand of k-step ks of a K tile (or of 16-dim m-tile ks of a V^T tile) from the
+// lane's units of that 16-key group.
+template <int BITS, bool IS_V>
+__device__ __forceinline__ void q_frag(const uint4 *un, int ks, uint32_t (&a)[4])
+{
+    if constexpr (BITS == 8) {
+        const uint4 &u = un[ks >> 1];
+        const uint32_t w0 = word_of(u, (ks & 1) * 2), w1 = word_of(u, (ks & 1) * 2 + 1);
+        a[0] = q8_lo(w0);
+        a[1] = q8_lo(w1);
+        a[2] = q8_hi(w0);
+        a[3] = q8_hi(w1);
+    } else {
+        const uint32_t w = word_of(un[ks >> 2], ks & 3);
+        // K: nibble pair p = 2r + h; V: p = 2h + r (r: A row half, h: A column half)
+        a[0] = q4_pair<0>(w);
+        a[1] = q4_pair<IS_V ? 1 : 2>(w);
+        a[2] = q4_pair<IS_V ? 2 : 1>(w);
+        a[3] = q4_pair<3>(w);
+    }
+}
+
+// NN: n-tiles of 8 query rows per consumer warp; NMT: consumer warps.  A CTA serves
+// up to 8 * NN * NMT rows (the G q heads of one KV head times the sequence's rows).
+// TREE: rows carry ancestor masks over the window keys (tree verify); a separate
+// instantiation so the decode / causal path carries no mask test.
+// BITS: 16 = bf16 pools read by TMA tiles; 8 / 4 = quantised records, one bulk copy
+// per (block, KV head), codes widened to bf16 in registers.
+template <int D, int BS, int NN, int NMT, int NST, bool TREE, int BITS>
+__global__ void __launch_bounds__((NMT + 1) * 32)
+paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const AttnParams p)
+{
+    using T = Tile<D, BS>;
+    constexpr int MT = BS / 16;   // 16-key m-tiles per block
+    constexpr int KS = D / 16;    // k-steps of K q^T
+    constexpr int DM = D / 16;    // 16-dim m-tiles of V^T P^T
+    constexpr int C = kSplitTokens;
+    constexpr int RPW = 8 * NN;   // rows per consumer warp
+    constexpr int NBW = (C / BS + 31) / 32;   // block ids per producer lane
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    constexpr int STAGE = BITS == 16 ? 2 * T::kTileBytes : QRec<D, BS, (BITS == 16 ? 8 : BITS)>::kBytes;
+    uint8_t *k_tiles = smem;                          // bf16: K tiles of every stage, then V tiles
+    uint8_t *v_tiles = smem + NST * T::kTileBytes;    // quantised: one record per stage
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + NST * STAGE);
+    uint64_t *empty = full + NST;
+    volatile int32_t *s_flag = reinterpret_cast<volatile int32_t *>(empty + NST);
+    // s_flag[1]: abort; [2]: blocks issued
+
+    const int pair = blockIdx.x / p.row_groups;
+    const int rg = blockIdx.x - pair * p.row_groups;
+    const int s = pair / p.num_kv_heads;
+    const int g = pair - s * p.num_kv_heads;
+    const int split = blockIdx.y;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    int L = __ldg(p.context_lens + s);
+    const int L_cap = (int)min((long long)p.max_context_len, (long long)p.max_blocks_per_seq * BS);
+    if (L > L_cap || L < 0) {
+        if (split == 0 && threadIdx.x == 0)
+            atomicOr(p.status, PKV_DEV_TABLE_OVERRUN);
+        L = L < 0 ? 0 : L_cap;
+    }
+    // the dependent merge kernel may be scheduled once every CTA of this grid has started
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int n_splits = (L + C - 1) / C;
+    if (split >= n_splits)
+        return;
+    const int row0 = __ldg(p.q_starts + s);
+    int W = __ldg(p.q_starts + s + 1) - row0;
+    if (W <= 0)
+        return;
+    if (row0 < 0 || row0 + W > p.total_rows) {   // q_starts inconsistent with total_q_rows
+        if (split == 0 && g == 0 && threadIdx.x == 0)
+            atomicOr(p.status, PKV_DEV_TOO_MANY_ROWS);
+        return;
+    }
+    if (W > p.max_rows) {
+        if (split == 0 && threadIdx.x == 0)
+            atomicOr(p.status, PKV_DEV_TOO_MANY_ROWS);
+        W = p.max_rows;
+    }
+    const int M = p.group * W;               // query rows of this (s, g)
+    const int r_lo = rg * RPW * NMT;         // first row of this CTA's row group
+    if (r_lo >= M)
+        return;
+    const int n_act = (min(M - r_lo, RPW * NMT) + RPW - 1) / RPW;   // consumer warps with rows
+
+    const int t0 = split * C;
+    const int t1 = min(t0 + C, L);
+    const int blk0 = t0 / BS;
+    const int nblk = (t1 - t0 + BS - 1) / BS;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NST; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], n_act);
+        }
+        mbar_fence_init();
+        s_flag[1] = 0;
+        s_flag[2] = 0;
+    }
+    __syncthreads();
+
+    if (warp == NMT) {
+        // ---------------- producer warp: block table -> TMA ring ----------------
+        // lane l holds the ids of the split's blocks l, l + 32, ... (one coalesced load each)
+        int my_blk[NBW];
+#pragma unroll
+        for (int r = 0; r < NBW; ++r) {
+            my_blk[r] = 0;
+            const int j = r * 32 + lane;
+            if (j < nblk) {
+                my_blk[r] = __ldg(p.block_tables + (size_t)s * p.max_blocks_per_seq + blk0 + j);
+                if (my_blk[r] < 0 || my_blk[r] >= p.num_blocks) {
+                    atomicOr(p.status, PKV_DEV_BAD_BLOCK);
+                    my_blk[r] = 0;
+                }
+            }
+        }
+        if (BITS == 16 && lane == 0) {
+            prefetch_tensormap(&tm_k);
+            prefetch_tensormap(&tm_v);
+        }
+        int k = 0;
+        bool stop = false;
+#pragma unroll
+        for (int r = 0; r < NBW; ++r) {
+            for (int jj = 0; jj < 32 && !stop; ++jj) {
+                if (k >= nblk)
+                    break;
+                const int blk = __shfl_sync(0xffffffffu, my_blk[r], jj);
+                if (lane == 0) {
+                    const int st = k % NST;
+                    bool ok = true;
+                    if (k >= NST)
+                        ok = mbar_wait_bounded(&empty[st], ((k / NST) + 1) & 1, kWaitLimitCycles);
+                    if (!ok)
+                        atomicOr(p.status, PKV_DEV_TIMEOUT);
+                    if (!ok || s_flag[1]) {
+                        s_flag[1] = 1;
+                        stop = true;
+                    } else if constexpr (BITS == 16) {
+                        const int y = (blk * p.num_kv_heads + g) * BS;
+                        mbar_arrive_expect_tx(&full[st], 2 * T::kTileBytes);
+#pragma unroll
+                        for (int h = 0; h < T::kHalves; ++h) {
+                            tma_load_2d(k_tiles + st * T::kTileBytes + h * T::kBoxBytes, &tm_k, &full[st],
+                                        h * 64, y);
+                            tma_load_2d(v_tiles + st * T::kTileBytes + h * T::kBoxBytes, &tm_v, &full[st],
+                                        h * 64, y);
+                        }
+                    } else {
+                        constexpr int RB = QRec<D, BS, BITS>::kBytes;
+                        mbar_arrive_expect_tx(&full[st], RB);
+                        bulk_load(smem + st * RB, p.qrec + ((size_t)blk * p.num_kv_heads + g) * RB, RB,
+                                  &full[st]);
+                    }
+                }
+                stop = __shfl_sync(0xffffffffu, stop, 0);
+                if (!stop)
+                    ++k;
+            }
+        }
+        if (lane == 0)
+            s_flag[2] = k;
+    } else if (warp < n_act) {
+        // ---------------- consumer warps ----------------
+        // S^T = K q^T and O^T += V^T P^T on mma.sync m16n8k16: keys / head dims on M,
+        // query rows on N.  Lane l owns rows 2(l%4) and 2(l%4)+1 of each n-tile for the
+        // softmax and the output, keys l/4 and l/4+8 of each 16-key m-tile.
+        const int cr = 2 * (lane & 3);   // first row of this lane within an n-tile
+        const int kr = lane >> 2;        // key (row of the C fragment) within 8
+        const int row_base = r_lo + warp * RPW;
+        uint32_t qf[NN][KS][2];
+        int lim[NN][2], win0[NN][2];   // keys t < lim are candidates; t >= win0 need their mask bit
+        uint32_t tmk[NN][2];
+#pragma unroll
+        for (int nn = 0; nn < NN; ++nn) {
+            const int jq = row_base + nn * 8 + kr;   // B fragment: lane l carries row l/4
+            const uint32_t *qrow = nullptr;
+            if (jq < M) {
+                const int w = jq / p.group;
+                const int h = p.q_head_of[g * p.group + (jq - w * p.group)];
+                qrow = reinterpret_cast<const uint32_t *>(p.q + ((size_t)(row0 + w) * p.num_q_heads + h) * D);
+            }
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                qf[nn][ks][0] = qrow ? __ldg(qrow + ((ks * 16 + cr) >> 1)) : 0u;
+                qf[nn][ks][1] = qrow ? __ldg(qrow + ((ks * 16 + 8 + cr) >> 1)) : 0u;
+            }
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int j = row_base + nn * 8 + cr + e;
+                lim[nn][e] = (p.causal && j < M) ? L - W + j / p.group + 1 : L;
+                win0[nn][e] = L;
+                tmk[nn][e] = 0u;
+                if (TREE && j < M) {   // tree verify: the window keys a row sees are its ancestors
+                    win0[nn][e] = L - W;
+                    tmk[nn][e] = __ldg(p.tree_masks + row0 + j / p.group);
+                }
+            }
+        }
+        float o[DM][NN][4];
+#pragma unroll
+        for (int dm = 0; dm < DM; ++dm)
+#pragma unroll
+            for (int nn = 0; nn < NN; ++nn)
+                o[dm][nn][0] = o[dm][nn][1] = o[dm][nn][2] = o[dm][nn][3] = 0.f;
+        float mrow[NN][2], lrow[NN][2];
+#pragma unroll
+        for (int nn = 0; nn < NN; ++nn)
+            mrow[nn][0] = mrow[nn][1] = -INFINITY, lrow[nn][0] = lrow[nn][1] = 0.f;
+
+        // per-lane ldmatrix address parts (matrix mi = lane / 8, row lane % 8)
+        const int k_key = 8 * ((lane >> 3) & 1) + (lane & 7);   // K: keys of matrices 0/1 vs 2/3
+        const int k_chs = lane >> 4;
+        const int v_key = 8 * (lane >> 4) + (lane & 7);         // V: keys of matrices 0/1 vs 2/3
+        const int v_chs = (lane >> 3) & 1;
+
+        int k = 0;
+        for (; k < nblk; ++k) {
+            const int st = k % NST;
+            if (!mbar_wait_bounded(&full[st], (k / NST) & 1, kWaitLimitCycles)) {
+                if (lane == 0) {
+                    atomicOr(p.status, PKV_DEV_TIMEOUT);
+                    s_flag[1] = 1;
+                }
+                break;
+            }
+            const uint32_t kb = smem_addr(k_tiles + st * T::kTileBytes);
+            const uint32_t vb = smem_addr(v_tiles + st * T::kTileBytes);
+            const uint8_t *rec = smem + st * STAGE;   // quantised record of this stage
+            const int tbase = (blk0 + k) * BS;
+
+            // S^T for the BS keys of this block; even and odd k-steps in separate chains
+            float sa[MT][NN][4], sb[MT][NN][4];
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        sa[mt][nn][c] = sb[mt][nn][c] = 0.f;
+            float2 kscale[MT], vscale[MT];   // quantised: scales of this lane's keys 2 kr, 2 kr + 1
+            if constexpr (BITS == 16) {
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt) {
+                        uint32_t a[4];
+                        ldsm_x4(kb + tile_off<BS>(mt * 16 + k_key, ks * 2 + k_chs), a[0], a[1], a[2], a[3]);
+#pragma unroll
+                        for (int nn = 0; nn < NN; ++nn) {
+                            if (ks & 1)
+                                mma_bf16_16x8x16(sb[mt][nn], a, qf[nn][ks][0], qf[nn][ks][1]);
+                            else
+                                mma_bf16_16x8x16(sa[mt][nn], a, qf[nn][ks][0], qf[nn][ks][1]);
+                        }
+                    }
+                }
+            } else {
+                using QR = QRec<D, BS, BITS>;
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    kscale[mt] = *reinterpret_cast<const float2 *>(rec + QR::kKs + (mt * 16 + 2 * kr) * 4);
+                    vscale[mt] = *reinterpret_cast<const float2 *>(rec + QR::kVs + (mt * 16 + 2 * kr) * 4);
+                    uint4 un[QR::kUnits];
+#pragma unroll
+                    for (int u = 0; u < QR::kUnits; ++u)
+                        un[u] = *reinterpret_cast<const uint4 *>(rec + QR::kK + ((mt * QR::kUnits + u) * 32 + lane) * 16);
+#pragma unroll
+                    for (int ks = 0; ks < KS; ++ks) {
+                        uint32_t a[4];
+                        q_frag<BITS, false>(un, ks, a);
+#pragma unroll
+                        for (int nn = 0; nn < NN; ++nn) {
+                            if (ks & 1)
+                                mma_bf16_16x8x16(sb[mt][nn], a, qf[nn][ks][0], qf[nn][ks][1]);
+                            else
+                                mma_bf16_16x8x16(sa[mt][nn], a, qf[nn][ks][0], qf[nn][ks][1]);
+                        }
+                    }
+                }
+            }
+            // scale into base-2 units; keys at or past a row's limit get -inf
+            float mx[NN][2];
+#pragma unroll
+            for (int nn = 0; nn < NN; ++nn)
+                mx[nn][0] = mx[nn][1] = -INFINITY;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        // bf16 tiles: A row kr + 8 j is key kr + 8 j; quantised: key 2 kr + j
+                        const int t = BITS == 16 ? tbase + mt * 16 + kr + 8 * (c >> 1)
+                                                 : tbase + mt * 16 + 2 * kr + (c >> 1);
+                        float x = (sa[mt][nn][c] + sb[mt][nn][c]);
+                        if constexpr (BITS != 16)
+                            x *= (c >> 1) ? kscale[mt].y : kscale[mt].x;
+                        x *= p.scale_log2;
+                        const int e = c & 1;
+                        bool vis = t < lim[nn][e];
+                        if (TREE)
+                            vis = vis && (t < win0[nn][e] || ((tmk[nn][e] >> (t - win0[nn][e])) & 1u));
+                        sa[mt][nn][c] = vis ? x : -INFINITY;
+                        mx[nn][c & 1] = fmaxf(mx[nn][c & 1], sa[mt][nn][c]);
+                    }
+            float alpha[NN][2], base[NN][2];
+#pragma unroll
+            for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    float v = mx[nn][e];
+                    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+                    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+                    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+                    const float m_new = fmaxf(mrow[nn][e], v);
+                    base[nn][e] = (m_new == -INFINITY) ? 0.f : m_new;
+                    alpha[nn][e] = exp2f(mrow[nn][e] - base[nn][e]);
+                    mrow[nn][e] = m_new;
+                }
+            const bool tail = tbase + BS > L;
+            // P = 2^(S - m) rounded to bf16 (packed per 8x8 fragment); l sums the rounded weights.
+            // Quantised: P carries each key's V scale (P v = (p s_v) c) and l sums p itself;
+            // keys at or past L get weight exactly 0 whatever their stored scale holds.
+            uint32_t pk[MT][NN][2];
+            float sum[NN][2];
+#pragma unroll
+            for (int nn = 0; nn < NN; ++nn)
+                sum[nn][0] = sum[nn][1] = 0.f;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int nn = 0; nn < NN; ++nn) {
+                    if constexpr (BITS == 16) {
+                        pk[mt][nn][0] = pack_bf16x2(exp2f(sa[mt][nn][0] - base[nn][0]), exp2f(sa[mt][nn][1] - base[nn][1]));
+                        pk[mt][nn][1] = pack_bf16x2(exp2f(sa[mt][nn][2] - base[nn][0]), exp2f(sa[mt][nn][3] - base[nn][1]));
+                        sum[nn][0] += bf16_lo_to_f32(pk[mt][nn][0]) + bf16_lo_to_f32(pk[mt][nn][1]);
+                        sum[nn][1] += bf16_hi_to_f32(pk[mt][nn][0]) + bf16_hi_to_f32(pk[mt][nn][1]);
+                    } else {
+                        const float p0 = exp2f(sa[mt][nn][0] - base[nn][0]), p1 = exp2f(sa[mt][nn][1] - base[nn][1]);
+                        const float p2 = exp2f(sa[mt][nn][2] - base[nn][0]), p3 = exp2f(sa[mt][nn][3] - base[nn][1]);
+                        float w0 = p0 * vscale[mt].x, w1 = p1 * vscale[mt].x;
+                        float w2 = p2 * vscale[mt].y, w3 = p3 * vscale[mt].y;
+                        if (tail) {
+                            const int t = tbase + mt * 16 + 2 * kr;
+                            if (t >= L)
+                                w0 = w1 = 0.f;
+                            if (t + 1 >= L)
+                                w2 = w3 = 0.f;
+                        }
+                        pk[mt][nn][0] = pack_bf16x2(w0, w1);
+                        pk[mt][nn][1] = pack_bf16x2(w2, w3);
+                        sum[nn][0] += p0 + p2;
+                        sum[nn][1] += p1 + p3;
+                    }
+                }
+#pragma unroll
+            for (int nn = 0; nn < NN; ++nn) {
+                lrow[nn][0] = lrow[nn][0] * alpha[nn][0] + sum[nn][0];
+                lrow[nn][1] = lrow[nn][1] * alpha[nn][1] + sum[nn][1];
+#pragma unroll
+                for (int dm = 0; dm < DM; ++dm) {
+                    o[dm][nn][0] *= alpha[nn][0];
+                    o[dm][nn][1] *= alpha[nn][1];
+                    o[dm][nn][2] *= alpha[nn][0];
+                    o[dm][nn][3] *= alpha[nn][1];
+                }
+            }
+
+            // O^T += V^T P^T; keys at or past L may hold anything (even NaN): zero them
+#pragma unroll
+            for (int kk = 0; kk < MT; ++kk) {
+                uint32_t b[NN][2];
+#pragma unroll
+                for (int nn = 0; nn < NN; ++nn) {
+                    b[nn][0] = movmatrix_trans(pk[kk][nn][0]);   // keys 0-7 of the m-tile
+                    b[nn][1] = movmatrix_trans(pk[kk][nn][1]);   // keys 8-15
+                }
+                if constexpr (BITS != 16) {
+                    using QR = QRec<D, BS, BITS>;
+                    uint4 un[QR::kUnits];
+#pragma unroll
+                    for (int u = 0; u < QR::kUnits; ++u)
+                        un[u] = *reinterpret_cast<const uint4 *>(rec + QR::kV + ((kk * QR::kUnits + u) * 32 + lane) * 16);
+#pragma unroll
+                    for (int dm = 0; dm < DM; ++dm) {
+                        uint32_t a[4];
+                        q_frag<BITS, true>(un, dm, a);
+#pragma unroll
+                        for (int nn = 0; nn < NN; ++nn)
+                            mma_bf16_16x8x16(o[dm][nn], a, b[nn][0], b[nn][1]);
+                    }
+                } else {
+                    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+                    if (tail) {
+                        const int t = tbase + kk * 16 + cr;
+                        mlo = (t < L ? 0x0000ffffu : 0u) | (t + 1 < L ? 0xffff0000u : 0u);
+                        mhi = (t + 8 < L ? 0x0000ffffu : 0u) | (t + 9 < L ? 0xffff0000u : 0u);
+                    }
+#pragma unroll
+                    for (int dm = 0; dm < DM; ++dm) {
+                        uint32_t a[4];
+                        ldsm_x4_trans(vb + tile_off<BS>(kk * 16 + v_key, dm * 2 + v_chs), a[0], a[1], a[2], a[3]);
+                        a[0] &= mlo;
+                        a[1] &= mlo;
+                        a[2] &= mhi;
+                        a[3] &= mhi;
+#pragma unroll
+                        for (int nn = 0; nn < NN; ++nn)
+                            mma_bf16_16x8x16(o[dm][nn], a, b[nn][0], b[nn][1]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[st]);
+        }
+
+        // this split's partial for the rows this warp owns
+#pragma unroll
+        for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float v = lrow[nn][e];
+                v += __shfl_xor_sync(0xffffffffu, v, 4);
+                v += __shfl_xor_sync(0xffffffffu, v, 8);
+                v += __shfl_xor_sync(0xffffffffu, v, 16);
+                lrow[nn][e] = v;
+            }
+#pragma unroll
+        for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int j = row_base + nn * 8 + cr + e;
+                if (j >= M)
+                    continue;
+                const int w = j / p.group;
+                const int h = p.q_head_of[g * p.group + (j - w * p.group)];
+                const size_t slot = ((size_t)(row0 + w) * p.num_q_heads + h) * p.n_max + split;
+                if (kr == 0)
+                    p.part_ml[slot] = make_float2(mrow[nn][e], lrow[nn][e]);
+                float *dst = p.part_o + slot * D;
+#pragma unroll
+                for (int dm = 0; dm < DM; ++dm) {
+                    dst[dm * 16 + kr] = o[dm][nn][e];
+                    dst[dm * 16 + kr + 8] = o[dm][nn][2 + e];
+                }
+            }
+    }
+
+    // a wait expired: wait (bounded) for the last copy issued into each stage before leaving
+    __syncthreads();
+    if (s_flag[1] && threadIdx.x == 0) {
+        const int issued = s_flag[2];
+        for (int st = 0; st < NST && st < issued; ++st) {
+            const int k_last = st + ((issued - 1 - st) / NST) * NST;
+            if (!mbar_wait_bounded(&full[st], (k_last / NST) & 1, kWaitLimitCycles))
+                break;
+        }
+    }
+}
+
+// Merge of the split partials of one (query row, q head) per warp, in split order,
+// with the head's sink:  M = max(m_i, sink), out = sum_i 2^{m_i - M} O_i /
+// (sum_i 2^{m_i - M} l_i + 2^{sink - M}).  Launched as a programmatic dependent of
+// the split kernel: it may start early and waits for the partials with
+// griddepcontrol.wait.
+template <int D>
+__global__ void __launch_bounds__(128, 7)
+paged_attention_combine_kernel(const AttnParams p)
+{
+    constexpr int VEC = D / 32;   // output values per lane
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const long long wid = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (wid >= (long long)p.total_rows * p.num_q_heads)
+        return;
+    const int r = (int)(wid / p.num_q_heads);
+    const int h = (int)(wid - (long long)r * p.num_q_heads);
+    // sequence of row r: the last s with q_starts[s] <= r
+    int lo = 0, hi = p.num_seqs - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(p.q_starts + mid) <= r)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const int s = lo;
+    const int row0 = __ldg(p.q_starts + s);
+    const int W = min(__ldg(p.q_starts + s + 1) - row0, p.max_rows);
+    const int w = r - row0;
+    if (w < 0 || w >= W)
+        return;   // rows past max_q_rows_per_seq were never computed (status already set)
+    const int L_cap = (int)min((long long)p.max_context_len, (long long)p.max_blocks_per_seq * p.block_size);
+    int L = __ldg(p.context_lens + s);
+    L = L < 0 ? 0 : (L > L_cap ? L_cap : L);
+    int lim = p.causal ? L - W + w + 1 : L;
+    if (p.tree_masks) {   // the row's last visible key is its highest visible window token
+        uint32_t m = __ldg(p.tree_masks + r);
+        if (W < 32)
+            m &= (1u << W) - 1u;
+        lim = L - W + (m ? 32 - __clz(m) : 0);
+    }
+    const int n = lim > 0 ? (lim + kSplitTokens - 1) / kSplitTokens : 0;
+    const size_t base = ((size_t)r * p.num_q_heads + h) * p.n_max;
+
+    // the n partial rows of (r, h) are contiguous: ask L2 for all of them at once, so the
+    // batched loop below waits for one DRAM round trip instead of one per batch
+    {
+        const char *region = reinterpret_cast<const char *>(p.part_o + base * D);
+        const int lines = (n * D * (int)sizeof(float) + 127) / 128;
+        for (int i = lane; i < lines; i += 32)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(region + (size_t)i * 128));
+    }
+    // lane i holds (m, l) of partials i, i + 32, ...; the sums below still run in split order
+    constexpr int MAXC = 2;   // partials cached per lane (n <= 64); longer rows reload (m, l)
+    float2 mlc[MAXC];
+#pragma unroll
+    for (int c = 0; c < MAXC; ++c) {
+        const int i = c * 32 + lane;
+        mlc[c] = i < n ? __ldcg(&p.part_ml[base + i]) : make_float2(-INFINITY, 0.f);
+    }
+    float Mx = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < MAXC; ++c)
+        Mx = fmaxf(Mx, mlc[c].x);
+    for (int i = MAXC * 32 + lane; i < n; i += 32)
+        Mx = fmaxf(Mx, __ldcg(&p.part_ml[base + i]).x);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, off));
+    float sink2 = 0.f;
+    const bool has_sink = p.sinks != nullptr;
+    if (has_sink) {
+        sink2 = __ldg(p.sinks + h) * kLog2e;
+        Mx = fmaxf(Mx, sink2);
+    }
+    float wc[MAXC], lc[MAXC];
+#pragma unroll
+    for (int c = 0; c < MAXC; ++c) {
+        wc[c] = exp2f(mlc[c].x - Mx);
+        lc[c] = mlc[c].y;
+    }
+    float den = 0.f;
+    float num[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v)
+        num[v] = 0.f;
+    const float *src0 = p.part_o + base * D + lane * VEC;
+    constexpr int BATCH = 8;    // partial rows in flight per lane (7 CTAs of 4 warps fit per SM)
+    for (int i0 = 0; i0 < n; i0 += BATCH) {
+        float x[BATCH][VEC];
+#pragma unroll
+        for (int b = 0; b < BATCH; ++b) {
+            const int i = i0 + b;
+            if (i < n) {
+                const float *src = src0 + (size_t)i * D;
+                if constexpr (VEC == 4) {
+                    const float4 t = __ldcg(reinterpret_cast<const float4 *>(src));
+                    x[b][0] = t.x, x[b][1] = t.y, x[b][2] = t.z, x[b][3] = t.w;
+                } else {
+                    const float2 t = __ldcg(reinterpret_cast<const float2 *>(src));
+                    x[b][0] = t.x, x[b][1] = t.y;
+                }
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < BATCH; ++b) {
+            const int i = i0 + b;
+            if (i >= n)
+                break;
+            float wgt, l_i;
+            if (i < MAXC * 32) {
+                const int c = i >> 5, srcl = i & 31;
+                float wsel = wc[0], lsel = lc[0];
+#pragma unroll
+                for (int cc = 1; cc < MAXC; ++cc)
+                    if (c == cc)
+                        wsel = wc[cc], lsel = lc[cc];
+                wgt = __shfl_sync(0xffffffffu, wsel, srcl);
+                l_i = __shfl_sync(0xffffffffu, lsel, srcl);
+            } else {
+                const float2 ml = __ldcg(&p.part_ml[base + i]);
+                wgt = exp2f(ml.x - Mx);
+                l_i = ml.y;
+            }
+            den += wgt * l_i;
+#pragma unroll
+            for (int v = 0; v < VEC; ++v)
+                num[v] += wgt * x[b][v];
+        }
+    }
+    if (has_sink)
+        den += exp2f(sink2 - Mx);
+    float res[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v)
+        res[v] = den > 0.f ? num[v] / den : 0.f;
+    const size_t oidx = ((size_t)r * p.num_q_heads + h) * D + lane * VEC;
+    if (p.out_f32) {
+        float *dst = static_cast<float *>(p.out) + oidx;
+        if constexpr (VEC == 4)
+            *reinterpret_cast<float4 *>(dst) = make_float4(res[0], res[1], res[2], res[3]);
+        else
+            *reinterpret_cast<float2 *>(dst) = make_float2(res[0], res[1]);
+    } else {
+        uint16_t *dst = static_cast<uint16_t *>(p.out) + oidx;
+        if constexpr (VEC == 4) {
+            uint2 pk;
+            pk.x = pack_bf16x2(res[0], res[1]);
+            pk.y = pack_bf16x2(res[2], res[3]);
+            *reinterpret_cast<uint2 *>(dst) = pk;
+        } else {
+            *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(res[0], res[1]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- host side --
+#ifndef PKV_STAGES_DECODE
+#define PKV_STAGES_DECODE 3
+#endif
+#ifndef PKV_STAGES_WIDE
+#define PKV_STAGES_WIDE 4
+#endif
+#ifndef PKV_STAGES_QUANT
+#define PKV_STAGES_QUANT 4
+#endif
+// Ring depth: decode CTAs (one consumer warp) are many and small, wide-row CTAs hold
+// several consumer warps on one ring; a quantised record is half or a quarter of a bf16
+// stage, so its ring can be deeper at the same shared memory.  Chosen by measurement.
+template <int D, int BS, int NMT, int BITS>
+constexpr int kStages()
+{
+    return BITS != 16 ? PKV_STAGES_QUANT : NMT == 1 ? PKV_STAGES_DECODE : PKV_STAGES_WIDE;
+}
+
+template <int D, int BS, int NMT, int BITS>
+size_t smem_bytes()
+{
+    constexpr int NST = kStages<D, BS, NMT, BITS>();
+    constexpr size_t stage = BITS == 16 ? 2 * (size_t)Tile<D, BS>::kTileBytes
+                                        : (size_t)QRec<D, BS, (BITS == 16 ? 8 : BITS)>::kBytes;
+    return 1024 + (size_t)NST * stage + 2 * NST * sizeof(uint64_t) + 64;
+}
+
+template <int D, int BS, int NN, int NMT, bool TREE, int BITS>
+int launch_t(const CUtensorMap &mk, const CUtensorMap &mv, const AttnParams &prm, dim3 grid,
+             cudaStream_t st)
+{
+    constexpr int NST = kStages<D, BS, NMT, BITS>();
+    auto kern = paged_attention_kernel<D, BS, NN, NMT, NST, TREE, BITS>;
+    const size_t smem = smem_bytes<D, BS, NMT, BITS>();
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    });
+    if (attr_err != cudaSuccess)
+        return check_cuda(attr_err, "cudaFuncSetAttribute(max dynamic smem)");
+    kern<<<grid, (NMT + 1) * 32, smem, st>>>(mk, mv, prm);
+    int rc = check_cuda(cudaGetLastError(), "paged attention split launch");
+    if (rc)
+        return rc;
+    // merge, as a programmatic dependent launch (its launch overlaps the split grid's tail)
+    const long long warps = (long long)prm.total_rows * prm.num_q_heads;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((warps + 3) / 4));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return check_cuda(cudaLaunchKernelEx(&cfg, paged_attention_combine_kernel<D>, prm),
+                      "paged attention merge launch");
+}
+
+// Rows of one (s, g) (G * max rows per sequence) -> one consumer warp per CTA with 8
+// rows (decode) or several consumer warps in several row-group CTAs (verify windows).
+// Row-group CTAs of one split are adjacent in launch order and share each K/V tile
+// through L2.
+#ifndef PKV_WIDE_NN
+#define PKV_WIDE_NN 1
+#endif
+#ifndef PKV_WIDE_NMT
+#define PKV_WIDE_NMT 3
+#endif
+template <int D, int BS, int BITS, bool WITH_TREE>
+int launch_d_bs(int rows, const CUtensorMap &mk, const CUtensorMap &mv, AttnParams prm,
+                long long pairs, int n_max, cudaStream_t st)
+{
+    const int per_cta = rows <= 8 ? 8 : 8 * PKV_WIDE_NN * PKV_WIDE_NMT;
+    prm.row_groups = (rows + per_cta - 1) / per_cta;
+    const long long gx = pairs * prm.row_groups;
+    if (gx > 0x7fffffffLL || n_max > 65535)
+        return set_error(PKV_ERR_SHAPE, "paged attention: grid too large");
+    const dim3 grid((unsigned)gx, (unsigned)n_max);
+    if constexpr (WITH_TREE) {
+        if (prm.tree_masks)
+            return rows <= 8 ? launch_t<D, BS, 1, 1, true, BITS>(mk, mv, prm, grid, st)
+                             : launch_t<D, BS, PKV_WIDE_NN, PKV_WIDE_NMT, true, BITS>(mk, mv, prm, grid, st);
+    }
+    if (rows <= 8)
+        return launch_t<D, BS, 1, 1, false, BITS>(mk, mv, prm, grid, st);
+    return launch_t<D, BS, PKV_WIDE_NN, PKV_WIDE_NMT, false, BITS>(mk, mv, prm, grid, st);
+}
+
+struct WsLayout {
+    size_t ml, o, total;
+};
+
+WsLayout ws_layout(int32_t num_seqs, int32_t total_q_rows, int32_t num_q_heads, int32_t num_kv_heads,
+                   int32_t head_dim, int32_t max_context_len)
+{
+    const size_t n_max = (size_t)(max_context_len > 0 ? (max_context_len + kSplitTokens - 1) / kSplitTokens : 1);
+    const size_t slots = (size_t)total_q_rows * num_q_heads * n_max;
+    (void)num_seqs;
+    (void)num_kv_heads;
+    WsLayout w;
+    w.ml = 0;
+    w.o = round_up(slots * sizeof(float2), 256);
+    w.total = w.o + round_up(slots * head_dim * sizeof(float), 256);
+    return w;
+}
+
+
+// What a pool gives the attention: geometry, and either bf16 K/V pools or records.
+struct PoolView {
+    int32_t num_blocks, block_size, num_kv_heads, head_dim, bits;   // bits: 16, 8 or 4
+    const void *k_pool, *v_pool;   // bits == 16
+    const void *records;           // bits 8 / 4
+};
+
+// Called with validated parameters: launches the split and merge kernels.
+using LaunchFn = int (*)(const PoolView &pv, AttnParams &prm, int rows, long long pairs, int n_max,
+                         cudaStream_t st);
+
+// Argument checks shared by every attention entry point, then the launch.
+inline int attention_run(const char *who, const PoolView &pv, const void *q, const int32_t *q_starts,
+                         const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
+                         int32_t num_seqs, int32_t total_q_rows, int32_t max_context_len,
+                         int32_t max_q_rows_per_seq, int32_t num_q_heads, const int32_t *kv_head_of_q_head,
+                         const float *sinks, int32_t causal, const uint32_t *tree_masks, float scale, void *out,
+                         int32_t out_dtype, void *workspace, size_t workspace_bytes, void *stream, LaunchFn launch)
+{
+    const int D = pv.head_dim, BS = pv.block_size, Hkv = pv.num_kv_heads;
+    if (num_seqs < 0 || total_q_rows < 0 || max_context_len < 0 || max_q_rows_per_seq < 0)
+        return set_error(PKV_ERR_SHAPE, "%s: negative size", who);
+    if (pv.num_blocks <= 0 || Hkv <= 0 || max_blocks_per_seq <= 0)
+        return set_error(PKV_ERR_SHAPE, "%s: pool sizes and max_blocks_per_seq must be positive", who);
+    if (!(D == 64 || D == 128))
+        return set_error(PKV_ERR_UNSUPPORTED, "%s: head_dim %d (built: 64, 128)", who, D);
+    if (!(BS == 16 || BS == 32))
+        return set_error(PKV_ERR_UNSUPPORTED, "%s: block_size %d (built: 16, 32)", who, BS);
+    if (num_q_heads <= 0 || num_q_heads > kMaxQHeads || num_q_heads % Hkv != 0)
+        return set_error(PKV_ERR_SHAPE,
+                         "%s: num_q_heads %d must be a positive multiple of "
+                         "num_kv_heads %d and at most %d", who, num_q_heads, Hkv, kMaxQHeads);
+    if (out_dtype != PKV_DTYPE_BF16 && out_dtype != PKV_DTYPE_F32)
+        return set_error(PKV_ERR_SHAPE, "%s: out_dtype %d", who, out_dtype);
+    if ((long long)max_blocks_per_seq * BS < max_context_len)
+        return set_error(PKV_ERR_SHAPE,
+                         "%s: max_context_len %d exceeds max_blocks_per_seq * "
+                         "block_size = %lld", who, max_context_len, (long long)max_blocks_per_seq * BS);
+    if ((long long)pv.num_blocks * Hkv * BS > 0x7fffffffLL)
+        return set_error(PKV_ERR_UNSUPPORTED,
+                         "%s: pool too large for 32-bit TMA row coordinates", who);
+    const int G = num_q_heads / Hkv;
+    if (num_seqs == 0 || total_q_rows == 0)
+        return PKV_OK;
+    if (max_q_rows_per_seq <= 0)
+        return set_error(PKV_ERR_SHAPE, "%s: max_q_rows_per_seq must be >= 1", who);
+    if ((long long)G * max_q_rows_per_seq > kMaxGroupRows)
+        return set_error(PKV_ERR_UNSUPPORTED,
+                         "%s: group %d x max rows %d exceeds %d", who, G,
+                         max_q_rows_per_seq, kMaxGroupRows);
+    const bool pools_ok = pv.bits == 16 ? (pv.k_pool && pv.v_pool) : pv.records != nullptr;
+    if (!pools_ok || !q || !q_starts || !block_tables || !context_lens || !out || !workspace)
+        return set_error(PKV_ERR_NULL, "%s: a required pointer is NULL", who);
+    const bool pools_aligned = pv.bits == 16 ? (aligned16(pv.k_pool) && aligned16(pv.v_pool))
+                                             : aligned16(pv.records);
+    if (!pools_aligned || !aligned16(q) || !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return set_error(PKV_ERR_ALIGN,
+                         "%s: pools, q and out must be 16-byte aligned, "
+                         "workspace 256-byte aligned", who);
+    const WsLayout wl = ws_layout(num_seqs, total_q_rows, num_q_heads, Hkv, D, max_context_len);
+    if (workspace_bytes < wl.total)
+        return set_error(PKV_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", who,
+                         workspace_bytes, wl.total);
+
+    AttnParams prm;
+    memset(&prm, 0, sizeof prm);
+    // GQA map: q heads of each KV head, in increasing q-head order
+    {
+        int fill[kMaxQHeads] = {0};
+        for (int h = 0; h < num_q_heads; ++h) {
+            const int gg = kv_head_of_q_head ? kv_head_of_q_head[h] : h / G;
+            if (gg < 0 || gg >= Hkv || fill[gg] >= G)
+                return set_error(PKV_ERR_SHAPE,
+                                 "%s: kv_head_of_q_head must give each of the %d "
+                                 "KV heads exactly %d q heads (entry %d = %d)", who, Hkv, G, h, gg);
+            prm.q_head_of[gg * G + fill[gg]++] = (int16_t)h;
+        }
+    }
+    int32_t *status = device_status_word();
+    if (!status)
+        return set_error(PKV_ERR_CUDA, "%s: no device status word", who);
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const int n_max = max_context_len > 0 ? (max_context_len + kSplitTokens - 1) / kSplitTokens : 1;
+    prm.q = static_cast<const uint16_t *>(q);
+    prm.q_starts = q_starts;
+    prm.block_tables = block_tables;
+    prm.context_lens = context_lens;
+    prm.sinks = sinks;
+    prm.tree_masks = tree_masks;
+    prm.out = out;
+    prm.part_ml = reinterpret_cast<float2 *>(ws + wl.ml);
+    prm.part_o = reinterpret_cast<float *>(ws + wl.o);
+    prm.qrec = static_cast<const uint8_t *>(pv.records);
+    prm.status = status;
+    prm.num_seqs = num_seqs;
+    prm.max_blocks_per_seq = max_blocks_per_seq;
+    prm.num_blocks = pv.num_blocks;
+    prm.num_q_heads = num_q_heads;
+    prm.num_kv_heads = Hkv;
+    prm.block_size = BS;
+    prm.group = G;
+    prm.n_max = n_max;
+    prm.max_context_len = max_context_len;
+    prm.max_rows = max_q_rows_per_seq;
+    prm.total_rows = total_q_rows;
+    prm.causal = causal ? 1 : 0;
+    prm.out_f32 = out_dtype == PKV_DTYPE_F32;
+    const float sc = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
+    prm.scale_log2 = sc * kLog2e;
+
+    const int rows = G * max_q_rows_per_seq;
+    const long long pairs = (long long)num_seqs * Hkv;
+    return launch(pv, prm, rows, pairs, n_max, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+}  // namespace pkv

@@ -1,6 +1,6 @@
 // pkv_ptx.cuh -- inline-PTX wrappers used by the kernels (sm_103a).
 //
-// mbarrier + TMA (cp.async.bulk.tensor) for the K/V staging pipeline, and
+// mbarrier + TMA (cp.async.bulk.tensor, cp.async.bulk) for the K/V staging pipeline, and
 // ldmatrix + mma.sync (bf16 in, fp32 accumulate) for the small QK^T / PV tiles.
 #pragma once
 
@@ -81,6 +81,17 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_addr(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+
+// 1-D bulk copy global -> shared (both 16-byte aligned, size a multiple of 16),
+// completion counted on `bar`.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar))
         : "memory");
 }
 

@@ -28,7 +28,8 @@ EXPORTED = ("pkv_abi_version", "paged_kv_append", "paged_attention_workspace_siz
             "paged_attention_workspace_init", "paged_attention_forward", "spec_accept_workspace_size",
             "spec_accept_greedy", "pkv_last_error_string", "pkv_device_status",
             "paged_attention_forward_noalloc", "paged_tree_attention_forward", "spec_accept_tree_greedy",
-            "spec_accept_sampled", "paged_block_hashes")
+            "spec_accept_sampled", "paged_block_hashes", "pkv_qrecord_bytes", "paged_kv_append_quant",
+            "paged_attention_forward_quant")
 
 
 class PkvError(RuntimeError):
@@ -41,6 +42,11 @@ class _Pool(ctypes.Structure):
     _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
                 ("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+
+
+class _QPool(ctypes.Structure):
+    _fields_ = [("records", ctypes.c_void_p), ("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("bits", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -87,6 +93,13 @@ def lib(build_if_missing: bool = False):
             L.spec_accept_sampled.restype = ctypes.c_int
             L.paged_block_hashes.argtypes = [P, P, i32, i32, i32, ctypes.c_uint64, P, P, i32, P]
             L.paged_block_hashes.restype = ctypes.c_int
+            L.pkv_qrecord_bytes.argtypes = [i32, i32, i32]
+            L.pkv_qrecord_bytes.restype = sz
+            L.paged_kv_append_quant.argtypes = [ctypes.POINTER(_QPool), P, i32, P, P, P, P, i32, i32, P]
+            L.paged_kv_append_quant.restype = ctypes.c_int
+            L.paged_attention_forward_quant.argtypes = [ctypes.POINTER(_QPool), P, P, P, i32, P, i32, i32, i32,
+                                                        i32, i32, P, P, i32, ctypes.c_float, P, i32, P, sz, P]
+            L.paged_attention_forward_quant.restype = ctypes.c_int
             L.spec_accept_workspace_size.argtypes = [i32, i32]
             L.spec_accept_workspace_size.restype = sz
             L.spec_accept_greedy.argtypes = [P, i32, P, P, i32, i32, P, P, P, P, sz, P]
@@ -170,6 +183,52 @@ def paged_attention_forward(k_pool, v_pool, q, q_starts, block_tables, context_l
         arr = (ctypes.c_int32 * Hq)(*[int(x) for x in kv_head_of_q_head])
         hmap = ctypes.cast(arr, ctypes.c_void_p)
     _check(lib().paged_attention_forward(
+        ctypes.byref(pool), _dptr(q), _dptr(q_starts), _dptr(block_tables), block_tables.shape[1],
+        _dptr(context_lens), S, R, int(max_context_len), int(max_q_rows_per_seq), Hq, hmap,
+        _dptr(sinks), int(bool(causal)), float(scale), _dptr(out), dt, _dptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def qrecord_bytes(block_size: int, head_dim: int, bits: int) -> int:
+    return int(lib().pkv_qrecord_bytes(int(block_size), int(head_dim), int(bits)))
+
+
+def _qpool(records: torch.Tensor, block_size: int, head_dim: int, bits: int) -> _QPool:
+    assert records.dtype == torch.uint8 and records.dim() == 3 and records.is_contiguous()
+    nb, hkv, rb = records.shape
+    assert rb == qrecord_bytes(block_size, head_dim, bits), "record size does not match the codec"
+    return _QPool(records.data_ptr(), nb, int(block_size), hkv, int(head_dim), int(bits))
+
+
+def paged_kv_append_quant(records, block_size, head_dim, bits, block_tables, context_lens_old, new_starts,
+                          k_new, v_new, stream=None) -> None:
+    """Quantise k_new/v_new [R_new, H_kv, D] (bf16) into the record pool uint8 [nb, H_kv, R]."""
+    pool = _qpool(records, block_size, head_dim, bits)
+    _check(lib().paged_kv_append_quant(ctypes.byref(pool), _dptr(block_tables), block_tables.shape[1],
+                                       _dptr(context_lens_old), _dptr(new_starts), _dptr(k_new), _dptr(v_new),
+                                       block_tables.shape[0], k_new.shape[0], _stream(stream)))
+
+
+def paged_attention_forward_quant(records, block_size, head_dim, bits, q, q_starts, block_tables, context_lens, *,
+                                  max_context_len: int, max_q_rows_per_seq: int, kv_head_of_q_head=None,
+                                  sinks=None, causal: bool = False, scale: float = 0.0,
+                                  out: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16,
+                                  workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Paged attention over a quantised record pool (see include/pkv.h)."""
+    pool = _qpool(records, block_size, head_dim, bits)
+    R, Hq, D = q.shape
+    S = block_tables.shape[0]
+    if out is None:
+        out = torch.empty((R, Hq, D), dtype=out_dtype, device=q.device)
+    dt = PKV_DTYPE_F32 if out.dtype == torch.float32 else PKV_DTYPE_BF16
+    if workspace is None:
+        workspace = new_attention_workspace(S, R, Hq, pool.num_kv_heads, D, max_context_len, q.device)
+    hmap = None
+    if kv_head_of_q_head is not None:
+        arr = (ctypes.c_int32 * Hq)(*[int(x) for x in kv_head_of_q_head])
+        hmap = ctypes.cast(arr, ctypes.c_void_p)
+    _check(lib().paged_attention_forward_quant(
         ctypes.byref(pool), _dptr(q), _dptr(q_starts), _dptr(block_tables), block_tables.shape[1],
         _dptr(context_lens), S, R, int(max_context_len), int(max_q_rows_per_seq), Hq, hmap,
         _dptr(sinks), int(bool(causal)), float(scale), _dptr(out), dt, _dptr(workspace),

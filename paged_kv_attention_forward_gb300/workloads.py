@@ -405,6 +405,42 @@ def make_workload(name: str, seed: int = 0, filler: str = "random", layers: Opti
     raise KeyError(name)
 
 
+def record_bytes(block_size: int, head_dim: int, bits: int) -> int:
+    """Size of one (block, KV head) record of a quantised pool: K codes, V codes, K and V scales."""
+    return 2 * block_size * head_dim * bits // 8 + 8 * block_size
+
+
+def random_records(seed, batch: PagedBatch, bits: int, layers: int = 1, filler: str = "random"):
+    """A quantised pool with the batch's geometry: uint8 [layers, num_blocks, H_kv, record].
+
+    Every code byte is uniform (any byte is a valid sign-magnitude code, any nibble a
+    valid offset code); every scale is float32 uniform in [0.5, 1.5) * 3 / Q, so values
+    span about +-3 like the bf16 workloads.  filler "nan" stores NaN scales in every
+    slot no cached token owns (pool slack, block tails, slots awaiting the append)."""
+    s_codes, s_scales = _seed_seq(seed).spawn(2)
+    B, D, H = batch.block_size, batch.head_dim, batch.num_kv_heads
+    nb = batch.k_pool.shape[1] if batch.k_pool is not None else int(batch.block_tables.max()) + 1
+    C = B * D * bits // 8
+    rb = record_bytes(B, D, bits)
+    rec = np.empty((layers, nb, H, rb), dtype=np.uint8)
+    rng = np.random.Generator(np.random.PCG64(s_codes))
+    rec[..., :2 * C] = rng.integers(0, 256, size=(layers, nb, H, 2 * C), dtype=np.uint8)
+    rng = np.random.Generator(np.random.PCG64(s_scales))
+    q = 127.0 if bits == 8 else 7.0
+    scales = ((0.5 + rng.random((layers, nb, H, 2, B))) * (3.0 / q)).astype(np.float32)
+    if filler == "nan":
+        owned = np.zeros((nb, B), dtype=bool)
+        for sq in range(batch.num_seqs):
+            old = int(batch.context_lens_old[sq])
+            for t0 in range(0, old, B):
+                owned[batch.block_tables[sq, t0 // B], : min(B, old - t0)] = True
+        scales[:, ~owned[:, None, None, :].repeat(H, 1).repeat(2, 2)] = np.nan
+    elif filler != "random":
+        raise ValueError(filler)
+    rec[..., 2 * C:] = scales.reshape(layers, nb, H, 2 * B).view(np.uint8).reshape(layers, nb, H, 8 * B)
+    return rec
+
+
 def context_token_ids(batch: PagedBatch, seed, vocab: int = VOCAB):
     """Token ids of every sequence's context, for the block-key workloads.
 

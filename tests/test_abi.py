@@ -100,3 +100,17 @@ def test_host_validation_without_device(pkv):
     assert lib.paged_block_hashes(4096, 4096, -1, 16, 16, 0, None, 4096, 4, None) == -2
     assert lib.paged_block_hashes(4096, 4096, 1, 16, 16, 0, None, 4096 + 4, 4, None) == -7
     assert lib.paged_block_hashes(4096, 4096, 0, 16, 16, 0, None, 4096, 4, None) == 0
+    # quantised pool: record size and the checks made before any CUDA call
+    assert lib.pkv_qrecord_bytes(16, 128, 8) == 2 * 16 * 128 + 8 * 16
+    assert lib.pkv_qrecord_bytes(32, 64, 4) == 2 * 32 * 32 + 8 * 32
+    assert lib.pkv_qrecord_bytes(16, 128, 5) == 0
+    qp = pkv._QPool(4096, 10, 16, 2, 128, 6)
+    assert lib.paged_kv_append_quant(ctypes.byref(qp), 4096, 4, 4096, 4096, 4096, 4096, 1, 1, None) == -3
+    qp.bits, qp.head_dim = 8, 96
+    assert lib.paged_kv_append_quant(ctypes.byref(qp), 4096, 4, 4096, 4096, 4096, 4096, 1, 1, None) == -3
+    qp.head_dim = 128
+    assert lib.paged_kv_append_quant(ctypes.byref(qp), 4096, 4, 4096, 4096, 4096, 4096, 1, 0, None) == 0
+    qp.records = 4096 + 8
+    assert lib.paged_kv_append_quant(ctypes.byref(qp), 4096, 4, 4096, 4096, 4096, 4096, 1, 1, None) == -7
+    assert lib.paged_attention_forward_quant(None, None, None, None, 0, None, 0, 0, 0, 0, 0, None, None, 0,
+                                             0.0, None, 0, None, 0, None) == -1
