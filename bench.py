@@ -41,9 +41,16 @@ PROFILES = os.path.join(ROOT, "profiles")
 
 
 # ---------------------------------------------------------------- accounting --
-def algorithmic_bytes(b: wl.PagedBatch, layers: int = 1) -> dict:
+def kv_bytes_per_token_head(head_dim: int, bits: int) -> int:
+    """K and V of one cached token of one KV head: bf16 rows, or its share of a
+    quantised record (codes of K and V plus two float32 scales)."""
+    return head_dim * 2 * 2 if bits == 16 else 2 * head_dim * bits // 8 + 8
+
+
+def algorithmic_bytes(b: wl.PagedBatch, layers: int = 1, bits: int = 16) -> dict:
     """Bytes one step must move at least, per the workload's structure."""
     B, H, D = b.block_size, b.num_kv_heads, b.head_dim
+    per_tok = kv_bytes_per_token_head(D, bits)
     shared = set(b.shared_block_ids.tolist())
     shared_tokens_read = 0
     if len(b.sharing_seqs):
@@ -53,13 +60,13 @@ def algorithmic_bytes(b: wl.PagedBatch, layers: int = 1) -> dict:
         L = int(b.context_lens[s])
         n_sh = len(shared) if s in set(b.sharing_seqs.tolist()) else 0
         private_tokens += L - n_sh * B
-    kv = (private_tokens + shared_tokens_read) * H * D * 2 * 2
-    logical_kv = int(b.context_lens.sum()) * H * D * 2 * 2
+    kv = (private_tokens + shared_tokens_read) * H * per_tok
+    logical_kv = int(b.context_lens.sum()) * H * per_tok
     R = b.total_q_rows
     q_out = 2 * R * b.num_q_heads * D * 2
     table = int(sum((int(L) + B - 1) // B for L in b.context_lens)) * 4 + (b.num_seqs * 2 + 1) * 4
     r_new = int(b.new_starts[-1])
-    append = r_new * H * D * 2 * 2 * 2                  # read k_new/v_new, write the pool slots
+    append = r_new * H * (D * 2 * 2 + per_tok)          # read k_new/v_new, write the pool slots
     attn = kv + q_out + table
     accept = 0
     if b.logits is not None:
@@ -184,7 +191,9 @@ def run_ours(args, rank, world, local_rank):
     layers = 40 if args.workload == "ministral_decode" else 1
     b = wl.make_workload(args.workload, seed=replica_seed(args.seed, rank), layers=layers,
                          num_seqs=args.num_seqs)
-    acct = algorithmic_bytes(b, layers)
+    bits = args.kv_bits
+    quant = bits != 16
+    acct = algorithmic_bytes(b, layers, bits)
 
     def d_bf16(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
@@ -192,7 +201,12 @@ def run_ours(args, rank, world, local_rank):
     def d(a):
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
-    pools = [(d_bf16(b.k_pool[i]), d_bf16(b.v_pool[i])) for i in range(layers)]
+    if quant:
+        recs = wl.random_records(replica_seed(args.seed, rank) + 7, b, bits, layers)
+        records = [d(recs[i]) for i in range(layers)]
+        del recs
+    else:
+        pools = [(d_bf16(b.k_pool[i]), d_bf16(b.v_pool[i])) for i in range(layers)]
     tables, lens_old, lens = d(b.block_tables), d(b.context_lens_old), d(b.context_lens)
     new_starts, q_starts = d(b.new_starts), d(b.q_starts)
     k_new = [d_bf16(b.k_new[i]) for i in range(layers)]
@@ -227,12 +241,20 @@ def run_ours(args, rank, world, local_rank):
 
     def step(ev_pairs=None, li=None):
         for i in range(layers):
-            if has_append:
+            if has_append and quant:
+                pkv.paged_kv_append_quant(records[i], b.block_size, b.head_dim, bits, tables, lens_old, new_starts,
+                                          k_new[i], v_new[i], stream=stream)
+            elif has_append:
                 pkv.paged_kv_append(pools[i][0], pools[i][1], tables, lens_old, new_starts, k_new[i], v_new[i],
                                     stream=stream)
             if ev_pairs is not None:
                 ev_pairs[li][0].record(stream)
-            if tree:
+            if quant:
+                pkv.paged_attention_forward_quant(records[i], b.block_size, b.head_dim, bits, qs[i], q_starts, tables,
+                                                  lens, max_context_len=max_ctx, max_q_rows_per_seq=max_rows,
+                                                  sinks=sinks, causal=b.causal, out=outs[i], workspace=ws,
+                                                  stream=stream)
+            elif tree:
                 pkv.paged_tree_attention_forward(pools[i][0], pools[i][1], qs[i], q_starts, tables, lens,
                                                  tree_masks, max_context_len=max_ctx,
                                                  max_q_rows_per_seq=max_rows, sinks=sinks, out=outs[i],
@@ -369,7 +391,8 @@ def run_ours(args, rank, world, local_rank):
         peak, peak_kind = 6800.0, "fallback"
     per_launch_bytes = acct["attention"] / layers
     achieved = per_launch_bytes / (attn_avg_ms * 1e-3) / 1e9
-    traffic = stored_traffic("paged_attention", args.workload)
+    kernel_tag = "paged_attention" if not quant else f"paged_attention_q{bits}"
+    traffic = stored_traffic(kernel_tag, args.workload)
     value = whole_job_rate(acct["step"], world, ms_per_step) / 1e9
     e2e_value = whole_job_rate(acct["step"], world, e2e_ms_per_step) / 1e9
     rows_per_s = whole_job_rate(acct["rows"] * layers, world, ms_per_step)
@@ -381,13 +404,15 @@ def run_ours(args, rank, world, local_rank):
                    "seq_len": b.max_context_len, "parallelism": f"dp{world} (independent replicas)",
                    "l2": "inputs larger than L2 (K/V read per step >> 129 MB); no flush",
                    "seed": args.seed,
-                   "accept": None if b.logits is None else accept_mode},
+                   "accept": None if b.logits is None else accept_mode,
+                   "kv_codec": "bf16" if not quant else f"q{bits} (per-row float32 scale)"},
         "query_rows_per_s": round(rows_per_s, 1),
         "frac_of_measured_hbm": round(value / peak, 4),
         "frac_of_nominal_8tbs": round(value / 8000.0, 4),
         "bytes_per_step": acct["step"], "kv_unique_bytes_per_step": acct["kv_unique"],
         "kv_logical_bytes_per_step": acct["kv_logical"],
-        "roofline": {"kernel": "paged attention call (split kernel + merge kernel)", "bound": "hbm", "achieved": round(achieved, 2),
+        "roofline": {"kernel": "paged attention call (split kernel + merge kernel)"
+                     + ("" if not quant else f", q{bits} records"), "bound": "hbm", "achieved": round(achieved, 2),
                      "peak": peak, "peak_kind": f"{peak_kind} (hbm_gbs, copy kernel)", "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "bytes_per_launch": per_launch_bytes,
                      "avg_launch_ms": round(attn_avg_ms, 5), "launches_timed": len(attn_ms),
@@ -412,8 +437,18 @@ def workload_description(b, layers):
 
 
 # ------------------------------------------------------------ oracle timing --
-def time_oracle_step(sub: wl.PagedBatch, threads: int):
+def time_oracle_step(sub: wl.PagedBatch, threads: int, records=None, bits: int = 16):
     import oracle
+    if records is not None:
+        rec = records.copy()
+        t = time.perf_counter()
+        if int(sub.new_starts[-1]) > 0:
+            oracle.paged_kv_append_quant(rec, sub.block_size, sub.head_dim, bits, sub.block_tables,
+                                         sub.context_lens_old, sub.new_starts, sub.k_new[0], sub.v_new[0])
+        oracle.paged_attention_quant(rec, sub.block_size, sub.head_dim, bits, sub.q[0], sub.q_starts,
+                                     sub.block_tables, sub.context_lens, sinks=sub.sinks, causal=sub.causal,
+                                     num_threads=threads)
+        return time.perf_counter() - t
     k, v = sub.k_pool[0].copy(), sub.v_pool[0].copy()
     t = time.perf_counter()
     if int(sub.new_starts[-1]) > 0:
@@ -428,16 +463,17 @@ def time_oracle_step(sub: wl.PagedBatch, threads: int):
     return time.perf_counter() - t
 
 
-def cpu_baseline(b: wl.PagedBatch, budget_s: float = 12.0, max_runs: int = 60):
+def cpu_baseline(b: wl.PagedBatch, budget_s: float = 12.0, max_runs: int = 60, bits: int = 16, seed: int = 0):
     """The oracle, as it stands, on the whole batch, repeated for about budget_s seconds."""
     import oracle
     oracle.build_oracle()
     threads = len(os.sched_getaffinity(0))
-    acct = algorithmic_bytes(b)
+    acct = algorithmic_bytes(b, 1, bits)
+    records = wl.random_records(seed + 7, b, bits)[0] if bits != 16 else None
     times = []
     t_start = time.perf_counter()
     while len(times) < max_runs and (len(times) < 3 or time.perf_counter() - t_start < budget_s):
-        times.append(time_oracle_step(b, threads))
+        times.append(time_oracle_step(b, threads, records, bits))
     med = statistics.median(times)
     return {"value": round(acct["step"] / med / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": (f"the whole batch ({b.num_seqs} seqs, {int(b.context_lens.sum())} cached tokens): "
@@ -500,6 +536,8 @@ def main():
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="resize the batch (same per-sequence distribution); for profiling smaller cases")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kv-bits", type=int, choices=(16, 8, 4), default=16,
+                    help="16: bf16 K/V pools; 8 / 4: quantised KV blocks (Q8 / Q4 records)")
     ap.add_argument("--accept", choices=("greedy", "sampled"), default="greedy",
                     help="verify workloads: greedy accept, or keyed sampling at T = 1, min_p = 0.05")
     args = ap.parse_args()
@@ -524,7 +562,7 @@ def main():
     if line is not None:
         if not args.no_cpu_baseline and world == 1:
             b = wl.make_workload(args.workload, seed=args.seed, layers=1, num_seqs=args.num_seqs)
-            line["cpu_baseline"] = cpu_baseline(b)
+            line["cpu_baseline"] = cpu_baseline(b, bits=args.kv_bits, seed=args.seed)
         else:
             line["cpu_baseline"] = None
         print(json.dumps(line), flush=True)

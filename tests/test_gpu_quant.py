@@ -65,9 +65,15 @@ def _oracle_qstep(b, rec, bits, layer=0):
 
 @pytest.mark.parametrize("bits", BITS)
 @pytest.mark.parametrize("name,filler", [("tiny_decode", "random"), ("spec_verify", "nan"),
-                                         ("sinks_scale", "random")])
+                                         ("cb_mix", "random"), ("window_d64_b32", "nan")])
 def test_append_quant_bit_exact(pkv, bits, name, filler):
-    b = wl.make_workload(name, seed=0, filler=filler, num_seqs=4 if name != "tiny_decode" else None)
+    if name == "window_d64_b32":
+        lens = np.array([5, 32, 33, 70, 100])
+        W = np.array([5, 16, 2, 16, 9])
+        b = wl.build_batch(9, name=name, lens=lens, n_new=W, q_rows=W, num_q_heads=8, num_kv_heads=2,
+                           head_dim=64, block_size=32, causal=True, filler=filler)
+    else:
+        b = wl.make_workload(name, seed=0, filler=filler, num_seqs=4 if name != "tiny_decode" else None)
     b.k_new[0][0, 0, :] = 0                   # a zero row: scale 0, every code 0
     rec = wl.random_records(1, b, bits, filler=filler)[0]
     g, _ = _gpu_qstep(pkv, b, rec, bits)
