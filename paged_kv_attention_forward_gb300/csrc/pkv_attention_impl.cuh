@@ -124,52 +124,64 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &u, int i)
     return i == 0 ? u.x : i == 1 ? u.y : i == 2 ? u.z : u.w;
 }
 
-__device__ __forceinline__ uint32_t sub_bf16x2(uint32_t a, uint32_t b)
+// Codes are widened exactly to 16-bit floats with a magic constant: bf16 0x4300 | m is
+// 128 + m and f16 0x6400 | m is 1024 + m (0 <= m <= 127); subtracting the constant
+// leaves m.  K codes go to bf16 (q stays exact in bf16), V codes to f16 (the weights
+// that multiply them carry 11 significant bits instead of 8).
+template <bool F16>
+__device__ __forceinline__ uint32_t sub_x2(uint32_t a, uint32_t b)
 {
     uint32_t d;
-    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    if constexpr (F16)
+        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    else
+        asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
 }
 
-// bf16 128 + m is exact for 0 <= m <= 127 (bits 0x4300 | m); subtracting 128 leaves m.
-// Sign-magnitude bytes 0 and 2 of w -> bf16x2 (byte 0 in the low half).
+template <bool F16>
+constexpr uint32_t kMagic = F16 ? 0x64006400u : 0x43004300u;
+
+// sign-magnitude bytes 0 and 2 of w -> x2 (byte 0 in the low half)
+template <bool F16>
 __device__ __forceinline__ uint32_t q8_lo(uint32_t w)
 {
-    const uint32_t m = sub_bf16x2((w & 0x007F007Fu) | 0x43004300u, 0x43004300u);
+    const uint32_t m = sub_x2<F16>((w & 0x007F007Fu) | kMagic<F16>, kMagic<F16>);
     return m | ((w << 8) & 0x80008000u);
 }
-// bytes 1 and 3 of w -> bf16x2 (byte 1 in the low half)
+// bytes 1 and 3 of w -> x2 (byte 1 in the low half)
+template <bool F16>
 __device__ __forceinline__ uint32_t q8_hi(uint32_t w)
 {
-    const uint32_t m = sub_bf16x2(((w >> 8) & 0x007F007Fu) | 0x43004300u, 0x43004300u);
+    const uint32_t m = sub_x2<F16>(((w >> 8) & 0x007F007Fu) | kMagic<F16>, kMagic<F16>);
     return m | (w & 0x80008000u);
 }
-// nibbles at bits 4p and 16 + 4p of w (each c + 8) -> bf16x2 of c: 128 + n - 136
-template <int P>
+// nibbles at bits 4p and 16 + 4p of w (each c + 8) -> x2 of c: (magic + n) - (magic + 8)
+template <int P, bool F16>
 __device__ __forceinline__ uint32_t q4_pair(uint32_t w)
 {
-    return sub_bf16x2(((w >> (4 * P)) & 0x000F000Fu) | 0x43004300u, 0x43084308u);
+    return sub_x2<F16>(((w >> (4 * P)) & 0x000F000Fu) | kMagic<F16>, kMagic<F16> | 0x00080008u);
 }
 
-// A operand of k-step ks of a K tile (or of 16-dim m-tile ks of a V^T tile) from the
-// lane's units of that 16-key group.
+// A operand of k-step ks of a K tile (bf16), or of 16-dim m-tile ks of a V^T tile
+// (f16), from the lane's units of that 16-key group.
 template <int BITS, bool IS_V>
 __device__ __forceinline__ void q_frag(const uint4 *un, int ks, uint32_t (&a)[4])
 {
     if constexpr (BITS == 8) {
         const uint4 &u = un[ks >> 1];
         const uint32_t w0 = word_of(u, (ks & 1) * 2), w1 = word_of(u, (ks & 1) * 2 + 1);
-        a[0] = q8_lo(w0);
-        a[1] = q8_lo(w1);
-        a[2] = q8_hi(w0);
-        a[3] = q8_hi(w1);
+        a[0] = q8_lo<IS_V>(w0);
+        a[1] = q8_lo<IS_V>(w1);
+        a[2] = q8_hi<IS_V>(w0);
+        a[3] = q8_hi<IS_V>(w1);
     } else {
         const uint32_t w = word_of(un[ks >> 2], ks & 3);
         // K: nibble pair p = 2r + h; V: p = 2h + r (r: A row half, h: A column half)
-        a[0] = q4_pair<0>(w);
-        a[1] = q4_pair<IS_V ? 1 : 2>(w);
-        a[2] = q4_pair<IS_V ? 2 : 1>(w);
-        a[3] = q4_pair<3>(w);
+        a[0] = q4_pair<0, IS_V>(w);
+        a[1] = q4_pair<IS_V ? 1 : 2, IS_V>(w);
+        a[2] = q4_pair<IS_V ? 2 : 1, IS_V>(w);
+        a[3] = q4_pair<3, IS_V>(w);
     }
 }
 
@@ -481,8 +493,25 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                 }
             const bool tail = tbase + BS > L;
             // P = 2^(S - m) rounded to bf16 (packed per 8x8 fragment); l sums the rounded weights.
-            // Quantised: P carries each key's V scale (P v = (p s_v) c) and l sums p itself;
-            // keys at or past L get weight exactly 0 whatever their stored scale holds.
+            // Quantised: P carries each key's V scale relative to the block's largest,
+            // p * (s_v / s_max), in f16, the block's P V is scaled by s_max as it is added,
+            // and l sums p itself; keys at or past L get weight exactly 0 and take no part
+            // in s_max, whatever their stored scale holds.
+            float vmax = 0.f, vinv = 0.f;
+            if constexpr (BITS != 16) {
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    const int t = tbase + mt * 16 + 2 * kr;
+                    if (!tail || t < L)
+                        vmax = fmaxf(vmax, vscale[mt].x);
+                    if (!tail || t + 1 < L)
+                        vmax = fmaxf(vmax, vscale[mt].y);
+                }
+                vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 4));
+                vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 8));
+                vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 16));
+                vinv = vmax > 0.f ? 1.0f / vmax : 0.f;
+            }
             uint32_t pk[MT][NN][2];
             float sum[NN][2];
 #pragma unroll
@@ -500,8 +529,8 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                     } else {
                         const float p0 = exp2f(sa[mt][nn][0] - base[nn][0]), p1 = exp2f(sa[mt][nn][1] - base[nn][1]);
                         const float p2 = exp2f(sa[mt][nn][2] - base[nn][0]), p3 = exp2f(sa[mt][nn][3] - base[nn][1]);
-                        float w0 = p0 * vscale[mt].x, w1 = p1 * vscale[mt].x;
-                        float w2 = p2 * vscale[mt].y, w3 = p3 * vscale[mt].y;
+                        const float rx = vscale[mt].x * vinv, ry = vscale[mt].y * vinv;
+                        float w0 = p0 * rx, w1 = p1 * rx, w2 = p2 * ry, w3 = p3 * ry;
                         if (tail) {
                             const int t = tbase + mt * 16 + 2 * kr;
                             if (t >= L)
@@ -509,8 +538,8 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                             if (t + 1 >= L)
                                 w2 = w3 = 0.f;
                         }
-                        pk[mt][nn][0] = pack_bf16x2(w0, w1);
-                        pk[mt][nn][1] = pack_bf16x2(w2, w3);
+                        pk[mt][nn][0] = pack_f16x2(w0, w1);
+                        pk[mt][nn][1] = pack_f16x2(w2, w3);
                         sum[nn][0] += p0 + p2;
                         sum[nn][1] += p1 + p3;
                     }
@@ -548,8 +577,13 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                         uint32_t a[4];
                         q_frag<BITS, true>(un, dm, a);
 #pragma unroll
-                        for (int nn = 0; nn < NN; ++nn)
-                            mma_bf16_16x8x16(o[dm][nn], a, b[nn][0], b[nn][1]);
+                        for (int nn = 0; nn < NN; ++nn) {
+                            float part[4] = {0.f, 0.f, 0.f, 0.f};
+                            mma_f16_16x8x16(part, a, b[nn][0], b[nn][1]);
+#pragma unroll
+                            for (int c = 0; c < 4; ++c)
+                                o[dm][nn][c] = fmaf(vmax, part[c], o[dm][nn][c]);
+                        }
                     }
                 } else {
                     uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
