@@ -196,6 +196,7 @@ __global__ void __launch_bounds__((NMT + 1) * 32)
 paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const AttnParams p)
 {
+    static_assert(!(TREE && BITS != 16), "tree masks are built for bf16 pools only");
     using T = Tile<D, BS>;
     constexpr int MT = BS / 16;   // 16-key m-tiles per block
     constexpr int KS = D / 16;    // k-steps of K q^T
@@ -493,24 +494,32 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                 }
             const bool tail = tbase + BS > L;
             // P = 2^(S - m) rounded to bf16 (packed per 8x8 fragment); l sums the rounded weights.
-            // Quantised: P carries each key's V scale relative to the block's largest,
-            // p * (s_v / s_max), in f16, the block's P V is scaled by s_max as it is added,
-            // and l sums p itself; keys at or past L get weight exactly 0 and take no part
-            // in s_max, whatever their stored scale holds.
-            float vmax = 0.f, vinv = 0.f;
+            // Quantised: P carries each key's V scale relative to the largest V scale among
+            // the block's keys the row sees, p * (s_v / s_max), in f16; the block's P V is
+            // scaled by s_max as it is added, and l sums p itself.  s_max depends only on
+            // the keys the row sees, so a verify row and the same row decoded alone agree;
+            // keys at or past L get weight exactly 0 whatever their stored scale holds.
+            float vmax[NN][2], vinv[NN][2];
             if constexpr (BITS != 16) {
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    const int t = tbase + mt * 16 + 2 * kr;
-                    if (!tail || t < L)
-                        vmax = fmaxf(vmax, vscale[mt].x);
-                    if (!tail || t + 1 < L)
-                        vmax = fmaxf(vmax, vscale[mt].y);
-                }
-                vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 4));
-                vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 8));
-                vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 16));
-                vinv = vmax > 0.f ? 1.0f / vmax : 0.f;
+                for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        float v = 0.f;
+#pragma unroll
+                        for (int mt = 0; mt < MT; ++mt) {
+                            const int t = tbase + mt * 16 + 2 * kr;
+                            if (t < lim[nn][e])
+                                v = fmaxf(v, vscale[mt].x);
+                            if (t + 1 < lim[nn][e])
+                                v = fmaxf(v, vscale[mt].y);
+                        }
+                        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+                        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+                        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+                        vmax[nn][e] = v;
+                        vinv[nn][e] = v > 0.f ? __frcp_rn(v) : 0.f;
+                    }
             }
             uint32_t pk[MT][NN][2];
             float sum[NN][2];
@@ -529,8 +538,8 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                     } else {
                         const float p0 = exp2f(sa[mt][nn][0] - base[nn][0]), p1 = exp2f(sa[mt][nn][1] - base[nn][1]);
                         const float p2 = exp2f(sa[mt][nn][2] - base[nn][0]), p3 = exp2f(sa[mt][nn][3] - base[nn][1]);
-                        const float rx = vscale[mt].x * vinv, ry = vscale[mt].y * vinv;
-                        float w0 = p0 * rx, w1 = p1 * rx, w2 = p2 * ry, w3 = p3 * ry;
+                        float w0 = p0 * (vscale[mt].x * vinv[nn][0]), w1 = p1 * (vscale[mt].x * vinv[nn][1]);
+                        float w2 = p2 * (vscale[mt].y * vinv[nn][0]), w3 = p3 * (vscale[mt].y * vinv[nn][1]);
                         if (tail) {
                             const int t = tbase + mt * 16 + 2 * kr;
                             if (t >= L)
@@ -582,7 +591,7 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                             mma_f16_16x8x16(part, a, b[nn][0], b[nn][1]);
 #pragma unroll
                             for (int c = 0; c < 4; ++c)
-                                o[dm][nn][c] = fmaf(vmax, part[c], o[dm][nn][c]);
+                                o[dm][nn][c] = fmaf(vmax[nn][c & 1], part[c], o[dm][nn][c]);
                         }
                     }
                 } else {
