@@ -291,9 +291,9 @@ def run_ours(args, rank, world, local_rank):
 
     for _ in range(args.warmup):
         step()
-    rc, bits = pkv.device_status()
+    rc, dev_bits = pkv.device_status()
     if rc != 0:
-        raise RuntimeError(f"device status {rc} bits {bits:#x} after warm-up")
+        raise RuntimeError(f"device status {rc} bits {dev_bits:#x} after warm-up")
 
     # ---- device-resident timed region ----
     n_ev = args.steps * layers
@@ -315,9 +315,9 @@ def run_ours(args, rank, world, local_rank):
     clock_info = clocks.stop() if clocks else None
     ms_total = t0.elapsed_time(t1)
     attn_ms = [a.elapsed_time(z) for a, z in ev_pairs]
-    rc, bits = pkv.device_status()
+    rc, dev_bits = pkv.device_status()
     if rc != 0:
-        raise RuntimeError(f"device status {rc} bits {bits:#x} after timed steps")
+        raise RuntimeError(f"device status {rc} bits {dev_bits:#x} after timed steps")
 
     # ---- end to end through the public API with host buffers ----
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
