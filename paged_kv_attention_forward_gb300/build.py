@@ -35,7 +35,8 @@ def sources():
 
 # the files the attention kernels are compiled from (a profile of those kernels stays
 # valid while these are unchanged)
-ATTENTION_SOURCES = ("pkv_attention.cu", "pkv_ptx.cuh", "pkv_internal.h")
+ATTENTION_SOURCES = ("pkv_attention_impl.cuh", "pkv_attention.cu", "pkv_attention_quant.cu", "pkv_ptx.cuh",
+                     "pkv_internal.h")
 
 
 def source_digest(names=None) -> str:
