@@ -361,8 +361,7 @@ int paged_block_hashes(const int32_t *tokens, const int32_t *token_starts, int32
  * 16-byte aligned.  Record = [K codes | V codes | K scales | V scales]:
  *   C = block_size * head_dim * bits / 8 bytes of codes per section; the K scale
  *   of slot t at byte 2C + 4t, the V scale at 2C + 4 block_size + 4t (float32).
- *   8-bit codes: sign-magnitude bytes (bit 7 sign, bits 0-6 |c|).
- *   4-bit codes: nibbles holding c + 8.
+ *   8-bit codes: bytes holding c + 128.  4-bit codes: nibbles holding c + 8.
  *   Position of the code of slot t, dim i (16-byte units of 4 little-endian
  *   32-bit words, laid out in the order the attention kernel's tensor-core
  *   operands consume them):

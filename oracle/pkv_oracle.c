@@ -635,8 +635,7 @@ int oracle_block_hashes(const int32_t *tokens, const int32_t *token_starts, int3
  *   C = block_size * head_dim * bits / 8 bytes of codes per section;
  *   K scale of slot t at byte 2C + 4t, V scale at 2C + 4 block_size + 4t
  *   (float32, little-endian).
- *   8-bit codes are sign-magnitude bytes (bit 7 = sign, bits 0-6 = |c|);
- *   4-bit codes are nibbles holding c + 8.
+ *   8-bit codes are bytes holding c + 128; 4-bit codes are nibbles holding c + 8.
  *   Code positions, for slot t and dim i, with 16-byte units of 4 little-endian
  *   32-bit words:
  *   K: mt = t/16, g = (t%16)/2, r = t%2, j = i/16, s = i%16,
@@ -744,8 +743,7 @@ static void qrecord_put(uint8_t *rec, int sec, int32_t t, const int32_t *codes, 
         int shift = 0;
         const size_t b = qcode_pos(sec, t, i, D, BS, bits, &shift);
         if (bits == 8) {
-            const int32_t c = codes[i];
-            rec[b] = (uint8_t)((c < 0 ? 0x80 : 0) | (c < 0 ? -c : c));
+            rec[b] = (uint8_t)(codes[i] + 128);
         } else {
             const uint8_t nib = (uint8_t)(codes[i] + 8);
             rec[b] = (uint8_t)((rec[b] & ~(0xF << shift)) | (nib << shift));
@@ -761,7 +759,7 @@ static double qrecord_get(const uint8_t *rec, int sec, int32_t t, int32_t i, int
     const size_t b = qcode_pos(sec, t, i, D, BS, bits, &shift);
     int32_t c;
     if (bits == 8)
-        c = (rec[b] & 0x80) ? -(int32_t)(rec[b] & 0x7F) : (int32_t)(rec[b] & 0x7F);
+        c = (int32_t)rec[b] - 128;
     else
         c = (int32_t)((rec[b] >> shift) & 0xF) - 8;
     float scale;

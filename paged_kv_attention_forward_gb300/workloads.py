@@ -414,7 +414,7 @@ def random_records(seed, batch: PagedBatch, bits: int, layers: int = 1, filler: 
     """A quantised pool with the batch's geometry: uint8 [layers, num_blocks, H_kv, record].
 
     Codes are independent draws of a rounded N(0, (Q/3)^2) clipped to [-Q, Q] (Q = 127 or
-    7), stored in the codec's byte encoding (8 bits: sign-magnitude bytes; 4 bits: two
+    7), stored in the codec's byte encoding (8 bits: bytes of c + 128; 4 bits: two
     nibbles of c + 8 per byte); since every code is drawn alike, where a code sits in
     the record does not matter.  Scales are float32 uniform in [0.5, 1.5) * 3 / Q, so
     values are about N(0, 1) like the bf16 workloads.  filler "nan" stores NaN scales
@@ -430,7 +430,7 @@ def random_records(seed, batch: PagedBatch, bits: int, layers: int = 1, filler: 
     codes = normal_f32(s_codes, (layers, nb, H, 2 * C * (8 // bits)), std=q / 3.0)
     codes = np.clip(np.rint(codes), -q, q).astype(np.int16)
     if bits == 8:
-        rec[..., :2 * C] = np.where(codes < 0, 0x80 | -codes, codes).astype(np.uint8)
+        rec[..., :2 * C] = (codes + 128).astype(np.uint8)
     else:
         nib = (codes + 8).astype(np.uint8)
         rec[..., :2 * C] = nib[..., 0::2] | (nib[..., 1::2] << 4)
