@@ -105,9 +105,9 @@ __device__ __forceinline__ uint32_t tile_off(int tok, int ch)
 // reads a section with conflict-free 16-byte loads.  For the 16-key tile mt, A row
 // g + 8r of K is key 16 mt + 2g + r and A column s is dim s of the k-step; the V^T
 // operand uses column s = key 16 kk + (s < 8 ? 2s : 2(s - 8) + 1), the order in
-// which the transposed P^T fragment of K's S^T arrives.  8-bit codes are
-// sign-magnitude bytes (word bytes 0, 2 feed a0/a1, bytes 1, 3 feed a2/a3); 4-bit
-// codes are nibbles holding c + 8.  Full byte-level formula in pkv.h.
+// which the transposed P^T fragment of K's S^T arrives.  8-bit codes are bytes of
+// c + 128 (word bytes 0, 2 feed a0/a1, bytes 1, 3 feed a2/a3); 4-bit codes are
+// nibbles holding c + 8.  Full byte-level formula in pkv.h.
 template <int D, int BS, int BITS>
 struct QRec {
     static constexpr int kCodeBytes = BS * D * BITS / 8;          // one section
@@ -124,64 +124,43 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &u, int i)
     return i == 0 ? u.x : i == 1 ? u.y : i == 2 ? u.z : u.w;
 }
 
-// Codes are widened exactly to 16-bit floats with a magic constant: bf16 0x4300 | m is
-// 128 + m and f16 0x6400 | m is 1024 + m (0 <= m <= 127); subtracting the constant
-// leaves m.  K codes go to bf16 (q stays exact in bf16), V codes to f16 (the weights
-// that multiply them carry 11 significant bits instead of 8).
-template <bool F16>
-__device__ __forceinline__ uint32_t sub_x2(uint32_t a, uint32_t b)
+// Codes become f16 operands without arithmetic: f16 bits 0x6400 | u are 1024 + u for a
+// byte u (0..255), and bits 0x4C00 | (u << 6) are 16 + u for a nibble u (0..15), so
+// putting a stored u = c + 128 (or c + 8) under those exponent bits yields c + kBias
+// exactly.  The tensor core then computes q . (c + kBias) and P . (c + kBias); the
+// kernel removes kBias * sum(q) from each score and kBias * sum(P) from each output
+// row, in fp32.
+template <int BITS>
+constexpr float kBias = BITS == 8 ? 1152.f : 24.f;   // 1024 + 128, 16 + 8
+
+// nibble pair P (bits 4P and 16 + 4P of w) -> f16x2 of 16 + u
+template <int P>
+__device__ __forceinline__ uint32_t nib_pair(uint32_t w)
 {
-    uint32_t d;
-    if constexpr (F16)
-        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    else
-        asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
+    const uint32_t x = P == 0 ? w << 6 : P == 1 ? w << 2 : P == 2 ? w >> 2 : w >> 6;
+    return (x & 0x03C003C0u) | 0x4C004C00u;
 }
 
-template <bool F16>
-constexpr uint32_t kMagic = F16 ? 0x64006400u : 0x43004300u;
-
-// sign-magnitude bytes 0 and 2 of w -> x2 (byte 0 in the low half)
-template <bool F16>
-__device__ __forceinline__ uint32_t q8_lo(uint32_t w)
-{
-    const uint32_t m = sub_x2<F16>((w & 0x007F007Fu) | kMagic<F16>, kMagic<F16>);
-    return m | ((w << 8) & 0x80008000u);
-}
-// bytes 1 and 3 of w -> x2 (byte 1 in the low half)
-template <bool F16>
-__device__ __forceinline__ uint32_t q8_hi(uint32_t w)
-{
-    const uint32_t m = sub_x2<F16>(((w >> 8) & 0x007F007Fu) | kMagic<F16>, kMagic<F16>);
-    return m | (w & 0x80008000u);
-}
-// nibbles at bits 4p and 16 + 4p of w (each c + 8) -> x2 of c: (magic + n) - (magic + 8)
-template <int P, bool F16>
-__device__ __forceinline__ uint32_t q4_pair(uint32_t w)
-{
-    return sub_x2<F16>(((w >> (4 * P)) & 0x000F000Fu) | kMagic<F16>, kMagic<F16> | 0x00080008u);
-}
-
-// A operand of k-step ks of a K tile (bf16), or of 16-dim m-tile ks of a V^T tile
-// (f16), from the lane's units of that 16-key group.
+// A operand of k-step ks of a K tile, or of 16-dim m-tile ks of a V^T tile, from the
+// lane's units of that 16-key group.
 template <int BITS, bool IS_V>
 __device__ __forceinline__ void q_frag(const uint4 *un, int ks, uint32_t (&a)[4])
 {
     if constexpr (BITS == 8) {
         const uint4 &u = un[ks >> 1];
         const uint32_t w0 = word_of(u, (ks & 1) * 2), w1 = word_of(u, (ks & 1) * 2 + 1);
-        a[0] = q8_lo<IS_V>(w0);
-        a[1] = q8_lo<IS_V>(w1);
-        a[2] = q8_hi<IS_V>(w0);
-        a[3] = q8_hi<IS_V>(w1);
+        a[0] = __byte_perm(w0, 0x64646464u, 0x4240);   // bytes 0, 2
+        a[1] = __byte_perm(w1, 0x64646464u, 0x4240);
+        a[2] = __byte_perm(w0, 0x64646464u, 0x4341);   // bytes 1, 3
+        a[3] = __byte_perm(w1, 0x64646464u, 0x4341);
     } else {
         const uint32_t w = word_of(un[ks >> 2], ks & 3);
-        // K: nibble pair p = 2r + h; V: p = 2h + r (r: A row half, h: A column half)
-        a[0] = q4_pair<0, IS_V>(w);
-        a[1] = q4_pair<IS_V ? 1 : 2, IS_V>(w);
-        a[2] = q4_pair<IS_V ? 2 : 1, IS_V>(w);
-        a[3] = q4_pair<3, IS_V>(w);
+        // nibble pair p sits at bits 4p and 16 + 4p; K: p = 2r + h, V: p = 2h + r
+        // (r: A row half, h: A column half)
+        a[0] = nib_pair<0>(w);
+        a[1] = nib_pair<IS_V ? 1 : 2>(w);
+        a[2] = nib_pair<IS_V ? 2 : 1>(w);
+        a[3] = nib_pair<3>(w);
     }
 }
 
@@ -371,6 +350,49 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                 }
             }
         }
+        // Quantised: q goes to f16, scaled per row by the power of two 2^e that puts its
+        // largest |value| in [2^14, 2^15) (exact: a bf16 value has 8 significant bits);
+        // qbias = kBias * sum(q') is the code offset's share of every score, qscale =
+        // scale * log2(e) * 2^-e.  Both are needed for the rows cr, cr + 1 of this lane's
+        // S^T elements, so they are taken from the lanes that hold those rows' q.
+        float qbias[NN][2], qscale[NN][2], cacc[NN][2];
+        if constexpr (BITS != 16) {
+#pragma unroll
+            for (int nn = 0; nn < NN; ++nn) {
+                float amax = 0.f;
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+                        amax = fmaxf(amax, fmaxf(fabsf(bf16_lo_to_f32(qf[nn][ks][j])),
+                                                 fabsf(bf16_hi_to_f32(qf[nn][ks][j]))));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                const int ex = (__float_as_int(amax) >> 23) & 0xFF;
+                const int e2 = amax > 0.f ? min(141 - ex, 126) : 0;   // amax * 2^e2 in [2^14, 2^15)
+                const float up = __int_as_float((127 + e2) << 23);
+                float qsum = 0.f;
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const uint32_t h2 = pack_f16x2(bf16_lo_to_f32(qf[nn][ks][j]) * up,
+                                                       bf16_hi_to_f32(qf[nn][ks][j]) * up);
+                        qf[nn][ks][j] = h2;
+                        qsum += f16_lo_to_f32(h2) + f16_hi_to_f32(h2);
+                    }
+                qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+                qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
+                const float bias_r = kBias<(BITS == 16 ? 8 : BITS)> * qsum;
+                const float scale_r = p.scale_log2 * __int_as_float((127 - e2) << 23);
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    qbias[nn][e] = __shfl_sync(0xffffffffu, bias_r, 4 * (cr + e));
+                    qscale[nn][e] = __shfl_sync(0xffffffffu, scale_r, 4 * (cr + e));
+                    cacc[nn][e] = 0.f;
+                }
+            }
+        }
         float o[DM][NN][4];
 #pragma unroll
         for (int dm = 0; dm < DM; ++dm)
@@ -446,9 +468,9 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
                         for (int nn = 0; nn < NN; ++nn) {
                             if (ks & 1)
-                                mma_bf16_16x8x16(sb[mt][nn], a, qf[nn][ks][0], qf[nn][ks][1]);
+                                mma_f16_16x8x16(sb[mt][nn], a, qf[nn][ks][0], qf[nn][ks][1]);
                             else
-                                mma_bf16_16x8x16(sa[mt][nn], a, qf[nn][ks][0], qf[nn][ks][1]);
+                                mma_f16_16x8x16(sa[mt][nn], a, qf[nn][ks][0], qf[nn][ks][1]);
                         }
                     }
                 }
@@ -467,10 +489,12 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                         // bf16 tiles: A row kr + 8 j is key kr + 8 j; quantised: key 2 kr + j
                         const int t = BITS == 16 ? tbase + mt * 16 + kr + 8 * (c >> 1)
                                                  : tbase + mt * 16 + 2 * kr + (c >> 1);
-                        float x = (sa[mt][nn][c] + sb[mt][nn][c]);
-                        if constexpr (BITS != 16)
-                            x *= (c >> 1) ? kscale[mt].y : kscale[mt].x;
-                        x *= p.scale_log2;
+                        float x;
+                        if constexpr (BITS == 16)
+                            x = (sa[mt][nn][c] + sb[mt][nn][c]) * p.scale_log2;
+                        else
+                            x = ((sa[mt][nn][c] + sb[mt][nn][c]) - qbias[nn][c & 1]) *
+                                (((c >> 1) ? kscale[mt].y : kscale[mt].x) * qscale[nn][c & 1]);
                         const int e = c & 1;
                         bool vis = t < lim[nn][e];
                         if (TREE)
@@ -522,10 +546,10 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                     }
             }
             uint32_t pk[MT][NN][2];
-            float sum[NN][2];
+            float sum[NN][2], psum[NN][2];
 #pragma unroll
             for (int nn = 0; nn < NN; ++nn)
-                sum[nn][0] = sum[nn][1] = 0.f;
+                sum[nn][0] = sum[nn][1] = psum[nn][0] = psum[nn][1] = 0.f;
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -551,12 +575,19 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                         pk[mt][nn][1] = pack_f16x2(w2, w3);
                         sum[nn][0] += p0 + p2;
                         sum[nn][1] += p1 + p3;
+                        // the rounded weights, for the code offset's share of the output
+                        psum[nn][0] += f16_lo_to_f32(pk[mt][nn][0]) + f16_lo_to_f32(pk[mt][nn][1]);
+                        psum[nn][1] += f16_hi_to_f32(pk[mt][nn][0]) + f16_hi_to_f32(pk[mt][nn][1]);
                     }
                 }
 #pragma unroll
             for (int nn = 0; nn < NN; ++nn) {
                 lrow[nn][0] = lrow[nn][0] * alpha[nn][0] + sum[nn][0];
                 lrow[nn][1] = lrow[nn][1] * alpha[nn][1] + sum[nn][1];
+                if constexpr (BITS != 16) {
+                    cacc[nn][0] = cacc[nn][0] * alpha[nn][0] + vmax[nn][0] * psum[nn][0];
+                    cacc[nn][1] = cacc[nn][1] * alpha[nn][1] + vmax[nn][1] * psum[nn][1];
+                }
 #pragma unroll
                 for (int dm = 0; dm < DM; ++dm) {
                     o[dm][nn][0] *= alpha[nn][0];
@@ -631,6 +662,24 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                 v += __shfl_xor_sync(0xffffffffu, v, 16);
                 lrow[nn][e] = v;
             }
+        if constexpr (BITS != 16) {
+            // remove the code offset: o -= kBias * sum over keys of the weights used
+#pragma unroll
+            for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    float v = cacc[nn][e];
+                    v += __shfl_xor_sync(0xffffffffu, v, 4);
+                    v += __shfl_xor_sync(0xffffffffu, v, 8);
+                    v += __shfl_xor_sync(0xffffffffu, v, 16);
+                    const float corr = kBias<(BITS == 16 ? 8 : BITS)> * v;
+#pragma unroll
+                    for (int dm = 0; dm < DM; ++dm) {
+                        o[dm][nn][e] -= corr;
+                        o[dm][nn][2 + e] -= corr;
+                    }
+                }
+        }
 #pragma unroll
         for (int nn = 0; nn < NN; ++nn)
 #pragma unroll

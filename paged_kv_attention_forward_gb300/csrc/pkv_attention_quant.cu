@@ -53,7 +53,7 @@ __device__ __forceinline__ int quant_code(float x, float s, float Q)
     return y == y ? (int)y : 0;
 }
 
-__device__ __forceinline__ uint8_t q8_byte(int c) { return (uint8_t)((c < 0 ? 0x80 : 0) | (c < 0 ? -c : c)); }
+__device__ __forceinline__ uint8_t q8_byte(int c) { return (uint8_t)(c + 128); }
 
 __device__ __forceinline__ int find_seq(const int32_t *__restrict__ starts, int num_seqs, int row)
 {

@@ -165,6 +165,20 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
     return r;
 }
 
+__device__ __forceinline__ float f16_lo_to_f32(uint32_t v)
+{
+    float f;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, lo;\n\t}" : "=f"(f) : "r"(v));
+    return f;
+}
+
+__device__ __forceinline__ float f16_hi_to_f32(uint32_t v)
+{
+    float f;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, hi;\n\t}" : "=f"(f) : "r"(v));
+    return f;
+}
+
 __device__ __forceinline__ float bf16_lo_to_f32(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi_to_f32(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
