@@ -169,13 +169,18 @@ __device__ __forceinline__ void q_frag(const uint4 *un, int ks, uint32_t (&a)[4]
 // TREE: rows carry ancestor masks over the window keys (tree verify); a separate
 // instantiation so the decode / causal path carries no mask test.
 // BITS: 16 = bf16 pools read by TMA tiles; 8 / 4 = quantised records, one bulk copy
-// per (block, KV head), codes widened to bf16 in registers.
-template <int D, int BS, int NN, int NMT, int NST, bool TREE, int BITS>
-__global__ void __launch_bounds__((NMT + 1) * 32)
+// per (block, KV head), codes widened to f16 in registers.
+// KW: consumer warps that share one row group's keys (decode only): warp kw takes the
+// split's blocks kw, kw + KW, ... with its own softmax state; the KW states are merged
+// in kw order at the end.  Which warp sees which key depends only on the key's
+// position, so a row's arithmetic is still fixed by its own sequence.
+template <int D, int BS, int NN, int NMT, int NST, bool TREE, int BITS, int KW>
+__global__ void __launch_bounds__((NMT * KW + 1) * 32)
 paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const AttnParams p)
 {
     static_assert(!(TREE && BITS != 16), "tree masks are built for bf16 pools only");
+    static_assert(KW == 1 || NMT == 1, "key-split consumer warps are built for decode CTAs");
     using T = Tile<D, BS>;
     constexpr int MT = BS / 16;   // 16-key m-tiles per block
     constexpr int KS = D / 16;    // k-steps of K q^T
@@ -251,7 +256,7 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
     }
     __syncthreads();
 
-    if (warp == NMT) {
+    if (warp == NMT * KW) {
         // ---------------- producer warp: block table -> TMA ring ----------------
         // lane l holds the ids of the split's blocks l, l + 32, ... (one coalesced load each)
         int my_blk[NBW];
@@ -313,14 +318,15 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
         }
         if (lane == 0)
             s_flag[2] = k;
-    } else if (warp < n_act) {
+    } else if (warp % NMT < n_act) {
         // ---------------- consumer warps ----------------
         // S^T = K q^T and O^T += V^T P^T on mma.sync m16n8k16: keys / head dims on M,
         // query rows on N.  Lane l owns rows 2(l%4) and 2(l%4)+1 of each n-tile for the
         // softmax and the output, keys l/4 and l/4+8 of each 16-key m-tile.
         const int cr = 2 * (lane & 3);   // first row of this lane within an n-tile
         const int kr = lane >> 2;        // key (row of the C fragment) within 8
-        const int row_base = r_lo + warp * RPW;
+        const int kw = warp / NMT;        // key share of this warp
+        const int row_base = r_lo + (warp % NMT) * RPW;
         uint32_t qf[NN][KS][2];
         int lim[NN][2], win0[NN][2];   // keys t < lim are candidates; t >= win0 need their mask bit
         uint32_t tmk[NN][2];
@@ -410,8 +416,7 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
         const int v_key = 8 * (lane >> 4) + (lane & 7);         // V: keys of matrices 0/1 vs 2/3
         const int v_chs = (lane >> 3) & 1;
 
-        int k = 0;
-        for (; k < nblk; ++k) {
+        for (int k = kw; k < nblk; k += KW) {
             const int st = k % NST;
             if (!mbar_wait_bounded(&full[st], (k / NST) & 1, kWaitLimitCycles)) {
                 if (lane == 0) {
@@ -651,7 +656,81 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                 mbar_arrive(&empty[st]);
         }
 
+        bool write_out = true;
+        if constexpr (KW > 1) {
+            // merge the KW key shares in kw order, through the (now idle) stage ring
+            asm volatile("bar.sync 1, %0;" ::"r"(KW * 32) : "memory");
+            constexpr int NV = DM * NN * 4 + 6 * NN;
+            static_assert((size_t)(KW - 1) * NV * 32 * 4 <= (size_t)NST * STAGE, "merge needs the ring");
+            float *xs = reinterpret_cast<float *>(smem);
+            const bool aborted = s_flag[1] != 0;
+            if (!aborted && kw > 0) {
+                float *dst = xs + (size_t)(kw - 1) * NV * 32 + lane;
+                int v = 0;
+#pragma unroll
+                for (int dm = 0; dm < DM; ++dm)
+#pragma unroll
+                    for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            dst[(v++) * 32] = o[dm][nn][c];
+#pragma unroll
+                for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        dst[(v++) * 32] = mrow[nn][e];
+                        dst[(v++) * 32] = lrow[nn][e];
+                        dst[(v++) * 32] = BITS != 16 ? cacc[nn][e] : 0.f;
+                    }
+            }
+            asm volatile("bar.sync 1, %0;" ::"r"(KW * 32) : "memory");
+            write_out = !aborted && kw == 0;
+        }
+        if (KW > 1 && write_out) {
+            constexpr int NV = DM * NN * 4 + 6 * NN;
+            const float *xs = reinterpret_cast<const float *>(smem);
+            float f[KW][NN][2];
+#pragma unroll
+            for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    float mx = mrow[nn][e];
+#pragma unroll
+                    for (int j = 1; j < KW; ++j)
+                        mx = fmaxf(mx, xs[((size_t)(j - 1) * NV + DM * NN * 4 + nn * 6 + e * 3) * 32 + lane]);
+                    f[0][nn][e] = mrow[nn][e] == -INFINITY ? 0.f : exp2f(mrow[nn][e] - mx);
+#pragma unroll
+                    for (int j = 1; j < KW; ++j) {
+                        const float mj = xs[((size_t)(j - 1) * NV + DM * NN * 4 + nn * 6 + e * 3) * 32 + lane];
+                        f[j][nn][e] = mj == -INFINITY ? 0.f : exp2f(mj - mx);
+                    }
+                    lrow[nn][e] *= f[0][nn][e];
+                    if constexpr (BITS != 16)
+                        cacc[nn][e] *= f[0][nn][e];
+#pragma unroll
+                    for (int j = 1; j < KW; ++j) {
+                        const float *src = xs + ((size_t)(j - 1) * NV + DM * NN * 4 + nn * 6 + e * 3) * 32 + lane;
+                        lrow[nn][e] += f[j][nn][e] * src[32];
+                        if constexpr (BITS != 16)
+                            cacc[nn][e] += f[j][nn][e] * src[64];
+                    }
+                    mrow[nn][e] = mx;
+                }
+#pragma unroll
+            for (int dm = 0; dm < DM; ++dm)
+#pragma unroll
+                for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        float acc = o[dm][nn][c] * f[0][nn][c & 1];
+#pragma unroll
+                        for (int j = 1; j < KW; ++j)
+                            acc += f[j][nn][c & 1] * xs[((size_t)(j - 1) * NV + (dm * NN + nn) * 4 + c) * 32 + lane];
+                        o[dm][nn][c] = acc;
+                    }
+        }
         // this split's partial for the rows this warp owns
+        if (write_out) {
 #pragma unroll
         for (int nn = 0; nn < NN; ++nn)
 #pragma unroll
@@ -699,6 +778,7 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                     dst[dm * 16 + kr + 8] = o[dm][nn][2 + e];
                 }
             }
+        }
     }
 
     // a wait expired: wait (bounded) for the last copy issued into each stage before leaving
@@ -878,7 +958,13 @@ paged_attention_combine_kernel(const AttnParams p)
 #define PKV_STAGES_WIDE 4
 #endif
 #ifndef PKV_STAGES_QUANT
-#define PKV_STAGES_QUANT 4
+#define PKV_STAGES_QUANT 8
+#endif
+#ifndef PKV_KW_BF16
+#define PKV_KW_BF16 1
+#endif
+#ifndef PKV_KW_QUANT
+#define PKV_KW_QUANT 4
 #endif
 // Ring depth: decode CTAs (one consumer warp) are many and small, wide-row CTAs hold
 // several consumer warps on one ring; a quantised record is half or a quarter of a bf16
@@ -887,6 +973,13 @@ template <int D, int BS, int NMT, int BITS>
 constexpr int kStages()
 {
     return BITS != 16 ? PKV_STAGES_QUANT : NMT == 1 ? PKV_STAGES_DECODE : PKV_STAGES_WIDE;
+}
+
+// consumer warps sharing one decode row group's keys
+template <int NMT, int BITS>
+constexpr int kKeyWarps()
+{
+    return NMT != 1 ? 1 : BITS != 16 ? PKV_KW_QUANT : PKV_KW_BF16;
 }
 
 template <int D, int BS, int NMT, int BITS>
@@ -903,7 +996,8 @@ int launch_t(const CUtensorMap &mk, const CUtensorMap &mv, const AttnParams &prm
              cudaStream_t st)
 {
     constexpr int NST = kStages<D, BS, NMT, BITS>();
-    auto kern = paged_attention_kernel<D, BS, NN, NMT, NST, TREE, BITS>;
+    constexpr int KW = kKeyWarps<NMT, BITS>();
+    auto kern = paged_attention_kernel<D, BS, NN, NMT, NST, TREE, BITS, KW>;
     const size_t smem = smem_bytes<D, BS, NMT, BITS>();
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
@@ -912,7 +1006,7 @@ int launch_t(const CUtensorMap &mk, const CUtensorMap &mv, const AttnParams &prm
     });
     if (attr_err != cudaSuccess)
         return check_cuda(attr_err, "cudaFuncSetAttribute(max dynamic smem)");
-    kern<<<grid, (NMT + 1) * 32, smem, st>>>(mk, mv, prm);
+    kern<<<grid, (NMT * KW + 1) * 32, smem, st>>>(mk, mv, prm);
     int rc = check_cuda(cudaGetLastError(), "paged attention split launch");
     if (rc)
         return rc;
