@@ -170,17 +170,17 @@ __device__ __forceinline__ void q_frag(const uint4 *un, int ks, uint32_t (&a)[4]
 // instantiation so the decode / causal path carries no mask test.
 // BITS: 16 = bf16 pools read by TMA tiles; 8 / 4 = quantised records, one bulk copy
 // per (block, KV head), codes widened to f16 in registers.
-// KW: consumer warps that share one row group's keys (decode only): warp kw takes the
-// split's blocks kw, kw + KW, ... with its own softmax state; the KW states are merged
-// in kw order at the end.  Which warp sees which key depends only on the key's
-// position, so a row's arithmetic is still fixed by its own sequence.
+// KW: consumer warps that share each row group's keys: warp (kw, mw) takes the split's
+// blocks kw, kw + KW, ... for the rows of row warp mw, with its own softmax state; the
+// KW states are merged in kw order at the end.  KW depends only on the codec, and
+// which warp sees which key only on the key's position, so a row's arithmetic is
+// still fixed by its own sequence, whatever the CTA shape.
 template <int D, int BS, int NN, int NMT, int NST, bool TREE, int BITS, int KW>
 __global__ void __launch_bounds__((NMT * KW + 1) * 32)
 paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const AttnParams p)
 {
     static_assert(!(TREE && BITS != 16), "tree masks are built for bf16 pools only");
-    static_assert(KW == 1 || NMT == 1, "key-split consumer warps are built for decode CTAs");
     using T = Tile<D, BS>;
     constexpr int MT = BS / 16;   // 16-key m-tiles per block
     constexpr int KS = D / 16;    // k-steps of K q^T
@@ -318,7 +318,12 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
         }
         if (lane == 0)
             s_flag[2] = k;
-    } else if (warp % NMT < n_act) {
+    } else if (warp % NMT >= n_act) {
+        if constexpr (KW > 1) {   // row warps without rows still take part in the merge barriers
+            asm volatile("bar.sync 1, %0;" ::"r"(NMT * KW * 32) : "memory");
+            asm volatile("bar.sync 1, %0;" ::"r"(NMT * KW * 32) : "memory");
+        }
+    } else {
         // ---------------- consumer warps ----------------
         // S^T = K q^T and O^T += V^T P^T on mma.sync m16n8k16: keys / head dims on M,
         // query rows on N.  Lane l owns rows 2(l%4) and 2(l%4)+1 of each n-tile for the
@@ -326,7 +331,8 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
         const int cr = 2 * (lane & 3);   // first row of this lane within an n-tile
         const int kr = lane >> 2;        // key (row of the C fragment) within 8
         const int kw = warp / NMT;        // key share of this warp
-        const int row_base = r_lo + (warp % NMT) * RPW;
+        const int mw = warp % NMT;        // row warp
+        const int row_base = r_lo + mw * RPW;
         uint32_t qf[NN][KS][2];
         int lim[NN][2], win0[NN][2];   // keys t < lim are candidates; t >= win0 need their mask bit
         uint32_t tmk[NN][2];
@@ -659,13 +665,13 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
         bool write_out = true;
         if constexpr (KW > 1) {
             // merge the KW key shares in kw order, through the (now idle) stage ring
-            asm volatile("bar.sync 1, %0;" ::"r"(KW * 32) : "memory");
+            asm volatile("bar.sync 1, %0;" ::"r"(NMT * KW * 32) : "memory");
             constexpr int NV = DM * NN * 4 + 6 * NN;
-            static_assert((size_t)(KW - 1) * NV * 32 * 4 <= (size_t)NST * STAGE, "merge needs the ring");
+            static_assert((size_t)(KW - 1) * NMT * NV * 32 * 4 <= (size_t)NST * STAGE, "merge needs the ring");
             float *xs = reinterpret_cast<float *>(smem);
             const bool aborted = s_flag[1] != 0;
             if (!aborted && kw > 0) {
-                float *dst = xs + (size_t)(kw - 1) * NV * 32 + lane;
+                float *dst = xs + (size_t)((kw - 1) * NMT + mw) * NV * 32 + lane;
                 int v = 0;
 #pragma unroll
                 for (int dm = 0; dm < DM; ++dm)
@@ -683,7 +689,7 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                         dst[(v++) * 32] = BITS != 16 ? cacc[nn][e] : 0.f;
                     }
             }
-            asm volatile("bar.sync 1, %0;" ::"r"(KW * 32) : "memory");
+            asm volatile("bar.sync 1, %0;" ::"r"(NMT * KW * 32) : "memory");
             write_out = !aborted && kw == 0;
         }
         if (KW > 1 && write_out) {
@@ -697,11 +703,11 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                     float mx = mrow[nn][e];
 #pragma unroll
                     for (int j = 1; j < KW; ++j)
-                        mx = fmaxf(mx, xs[((size_t)(j - 1) * NV + DM * NN * 4 + nn * 6 + e * 3) * 32 + lane]);
+                        mx = fmaxf(mx, xs[((size_t)((j - 1) * NMT + mw) * NV + DM * NN * 4 + nn * 6 + e * 3) * 32 + lane]);
                     f[0][nn][e] = mrow[nn][e] == -INFINITY ? 0.f : exp2f(mrow[nn][e] - mx);
 #pragma unroll
                     for (int j = 1; j < KW; ++j) {
-                        const float mj = xs[((size_t)(j - 1) * NV + DM * NN * 4 + nn * 6 + e * 3) * 32 + lane];
+                        const float mj = xs[((size_t)((j - 1) * NMT + mw) * NV + DM * NN * 4 + nn * 6 + e * 3) * 32 + lane];
                         f[j][nn][e] = mj == -INFINITY ? 0.f : exp2f(mj - mx);
                     }
                     lrow[nn][e] *= f[0][nn][e];
@@ -709,7 +715,7 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                         cacc[nn][e] *= f[0][nn][e];
 #pragma unroll
                     for (int j = 1; j < KW; ++j) {
-                        const float *src = xs + ((size_t)(j - 1) * NV + DM * NN * 4 + nn * 6 + e * 3) * 32 + lane;
+                        const float *src = xs + ((size_t)((j - 1) * NMT + mw) * NV + DM * NN * 4 + nn * 6 + e * 3) * 32 + lane;
                         lrow[nn][e] += f[j][nn][e] * src[32];
                         if constexpr (BITS != 16)
                             cacc[nn][e] += f[j][nn][e] * src[64];
@@ -725,7 +731,7 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                         float acc = o[dm][nn][c] * f[0][nn][c & 1];
 #pragma unroll
                         for (int j = 1; j < KW; ++j)
-                            acc += f[j][nn][c & 1] * xs[((size_t)(j - 1) * NV + (dm * NN + nn) * 4 + c) * 32 + lane];
+                            acc += f[j][nn][c & 1] * xs[((size_t)((j - 1) * NMT + mw) * NV + (dm * NN + nn) * 4 + c) * 32 + lane];
                         o[dm][nn][c] = acc;
                     }
         }
@@ -964,22 +970,30 @@ paged_attention_combine_kernel(const AttnParams p)
 #define PKV_KW_BF16 1
 #endif
 #ifndef PKV_KW_QUANT
-#define PKV_KW_QUANT 4
+#define PKV_KW_QUANT 2
 #endif
 // Ring depth: decode CTAs (one consumer warp) are many and small, wide-row CTAs hold
 // several consumer warps on one ring; a quantised record is half or a quarter of a bf16
 // stage, so its ring can be deeper at the same shared memory.  Chosen by measurement.
+template <int BITS>
+constexpr int kKeyWarps();
+
 template <int D, int BS, int NMT, int BITS>
 constexpr int kStages()
 {
-    return BITS != 16 ? PKV_STAGES_QUANT : NMT == 1 ? PKV_STAGES_DECODE : PKV_STAGES_WIDE;
+    constexpr int base = BITS != 16 ? PKV_STAGES_QUANT : NMT == 1 ? PKV_STAGES_DECODE : PKV_STAGES_WIDE;
+    // the KW - 1 key shares' states pass through the ring at the end: make it big enough
+    constexpr int stage = BITS == 16 ? 2 * Tile<D, BS>::kTileBytes : QRec<D, BS, (BITS == 16 ? 8 : BITS)>::kBytes;
+    constexpr int merge = (kKeyWarps<BITS>() - 1) * NMT * (D / 16 * 4 + 6) * 32 * 4;
+    constexpr int need = (merge + stage - 1) / stage;
+    return base > need ? base : need;
 }
 
-// consumer warps sharing one decode row group's keys
-template <int NMT, int BITS>
+// consumer warps sharing each row group's keys (the same for every CTA shape of a codec)
+template <int BITS>
 constexpr int kKeyWarps()
 {
-    return NMT != 1 ? 1 : BITS != 16 ? PKV_KW_QUANT : PKV_KW_BF16;
+    return BITS != 16 ? PKV_KW_QUANT : PKV_KW_BF16;
 }
 
 template <int D, int BS, int NMT, int BITS>
@@ -996,7 +1010,7 @@ int launch_t(const CUtensorMap &mk, const CUtensorMap &mv, const AttnParams &prm
              cudaStream_t st)
 {
     constexpr int NST = kStages<D, BS, NMT, BITS>();
-    constexpr int KW = kKeyWarps<NMT, BITS>();
+    constexpr int KW = kKeyWarps<BITS>();
     auto kern = paged_attention_kernel<D, BS, NN, NMT, NST, TREE, BITS, KW>;
     const size_t smem = smem_bytes<D, BS, NMT, BITS>();
     static std::once_flag once;
