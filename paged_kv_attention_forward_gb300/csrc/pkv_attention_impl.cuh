@@ -591,6 +591,7 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                         psum[nn][1] += f16_hi_to_f32(pk[mt][nn][0]) + f16_hi_to_f32(pk[mt][nn][1]);
                     }
                 }
+            bool moved = false;   // did any row's running max change?
 #pragma unroll
             for (int nn = 0; nn < NN; ++nn) {
                 lrow[nn][0] = lrow[nn][0] * alpha[nn][0] + sum[nn][0];
@@ -599,13 +600,19 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                     cacc[nn][0] = cacc[nn][0] * alpha[nn][0] + vmax[nn][0] * psum[nn][0];
                     cacc[nn][1] = cacc[nn][1] * alpha[nn][1] + vmax[nn][1] * psum[nn][1];
                 }
+                moved = moved || alpha[nn][0] != 1.f || alpha[nn][1] != 1.f;
+            }
+            // o *= alpha; skipped when every alpha is exactly 1 (then it changes no bit)
+            if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll
-                for (int dm = 0; dm < DM; ++dm) {
-                    o[dm][nn][0] *= alpha[nn][0];
-                    o[dm][nn][1] *= alpha[nn][1];
-                    o[dm][nn][2] *= alpha[nn][0];
-                    o[dm][nn][3] *= alpha[nn][1];
-                }
+                for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+                    for (int dm = 0; dm < DM; ++dm) {
+                        o[dm][nn][0] *= alpha[nn][0];
+                        o[dm][nn][1] *= alpha[nn][1];
+                        o[dm][nn][2] *= alpha[nn][0];
+                        o[dm][nn][3] *= alpha[nn][1];
+                    }
             }
 
             // O^T += V^T P^T; keys at or past L may hold anything (even NaN): zero them
@@ -958,7 +965,7 @@ paged_attention_combine_kernel(const AttnParams p)
 
 // ---------------------------------------------------------------- host side --
 #ifndef PKV_STAGES_DECODE
-#define PKV_STAGES_DECODE 3
+#define PKV_STAGES_DECODE 4
 #endif
 #ifndef PKV_STAGES_WIDE
 #define PKV_STAGES_WIDE 4
@@ -967,7 +974,7 @@ paged_attention_combine_kernel(const AttnParams p)
 #define PKV_STAGES_QUANT 8
 #endif
 #ifndef PKV_KW_BF16
-#define PKV_KW_BF16 1
+#define PKV_KW_BF16 2
 #endif
 #ifndef PKV_KW_QUANT
 #define PKV_KW_QUANT 2
