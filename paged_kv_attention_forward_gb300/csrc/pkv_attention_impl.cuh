@@ -181,6 +181,11 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const AttnParams p)
 {
     static_assert(!(TREE && BITS != 16), "tree masks are built for bf16 pools only");
+    // Every use of a stage must belong to one key-share warp: stage st holds blocks
+    // st, st + NST, ..., all of share st % KW only when KW divides NST.  Otherwise a
+    // warp could wait for a stage's next phase while another warp's phase of it is
+    // still pending, and a parity wait cannot tell those phases apart.
+    static_assert(NST % KW == 0, "ring depth must be a multiple of the key-share warps");
     using T = Tile<D, BS>;
     constexpr int MT = BS / 16;   // 16-key m-tiles per block
     constexpr int KS = D / 16;    // k-steps of K q^T
@@ -993,7 +998,9 @@ constexpr int kStages()
     constexpr int stage = BITS == 16 ? 2 * Tile<D, BS>::kTileBytes : QRec<D, BS, (BITS == 16 ? 8 : BITS)>::kBytes;
     constexpr int merge = (kKeyWarps<BITS>() - 1) * NMT * (D / 16 * 4 + 6) * 32 * 4;
     constexpr int need = (merge + stage - 1) / stage;
-    return base > need ? base : need;
+    constexpr int kw = kKeyWarps<BITS>();
+    constexpr int n = base > need ? base : need;
+    return (n + kw - 1) / kw * kw;   // a multiple of the key-share warps (see the kernel)
 }
 
 // consumer warps sharing each row group's keys (the same for every CTA shape of a codec)
