@@ -970,7 +970,7 @@ paged_attention_combine_kernel(const AttnParams p)
 
 // ---------------------------------------------------------------- host side --
 #ifndef PKV_STAGES_DECODE
-#define PKV_STAGES_DECODE 4
+#define PKV_STAGES_DECODE 3
 #endif
 #ifndef PKV_STAGES_WIDE
 #define PKV_STAGES_WIDE 4
@@ -979,14 +979,17 @@ paged_attention_combine_kernel(const AttnParams p)
 #define PKV_STAGES_QUANT 8
 #endif
 #ifndef PKV_KW_BF16
-#define PKV_KW_BF16 2
+#define PKV_KW_BF16 1
 #endif
 #ifndef PKV_KW_QUANT
 #define PKV_KW_QUANT 2
 #endif
-// Ring depth: decode CTAs (one consumer warp) are many and small, wide-row CTAs hold
-// several consumer warps on one ring; a quantised record is half or a quarter of a bf16
-// stage, so its ring can be deeper at the same shared memory.  Chosen by measurement.
+// Ring depth and key-share warps, chosen by measurement on GB300: decode CTAs are many
+// and small, wide-row CTAs hold several consumer warps on one ring; a quantised record
+// is half or a quarter of a bf16 stage, so its ring can be deeper at the same shared
+// memory.  Two key-share warps pay off for quantised records (their per-block work is
+// longer: 394 -> 309 us for a Q8 cb_mix call) but not for bf16 pools, whose verify
+// windows lose a third of their speed with them while decode gains 1 %.
 template <int BITS>
 constexpr int kKeyWarps();
 
