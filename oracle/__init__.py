@@ -72,7 +72,11 @@ def _load():
             lib.oracle_keyed_log.argtypes = [ctypes.c_float]
             lib.oracle_keyed_log.restype = ctypes.c_float
             lib.oracle_spec_accept_sampled.argtypes = [P, i32, P, P, P, P, ctypes.c_uint64, ctypes.c_float,
-                                                       ctypes.c_float, i32, P, P, P, P]
+                                                       i32, ctypes.c_float, ctypes.c_float, i32, P, P, P, P]
+            lib.oracle_keyed_exp2.argtypes = [ctypes.c_float]
+            lib.oracle_keyed_exp2.restype = ctypes.c_float
+            lib.oracle_topkp_kept.argtypes = [P, i32, ctypes.c_float, i32, ctypes.c_float, P]
+            lib.oracle_topkp_kept.restype = i32
             lib.oracle_spec_accept_sampled.restype = ctypes.c_int
             lib.oracle_fnv1a64.argtypes = [P, ctypes.c_int64]
             lib.oracle_fnv1a64.restype = ctypes.c_uint64
@@ -229,9 +233,10 @@ def keyed_log(x):
 
 
 def spec_accept_sampled(logits, q_starts, draft_tokens, positions, seed, temperature, min_p=0.0,
-                        parents=None):
+                        parents=None, top_k=0, top_p=1.0):
     """Sampled (keyed) accept: returns (sampled [R], accept_len [S], out_tokens [R],
-    accepted_rows [R]), all int32.  parents None means chains."""
+    accepted_rows [R]), all int32.  parents None means chains; top_k <= 0 and
+    top_p >= 1 switch those filters off."""
     lib = _load()
     lg = _c(logits, np.float32)
     rows, vocab = lg.shape
@@ -245,11 +250,27 @@ def spec_accept_sampled(logits, q_starts, draft_tokens, positions, seed, tempera
     ot = np.empty(rows, dtype=np.int32)
     ar = np.empty(rows, dtype=np.int32)
     rc = lib.oracle_spec_accept_sampled(_ptr(lg), vocab, _ptr(qs), _ptr(dr), _ptr(pa), _ptr(po), int(seed),
-                                        float(temperature), float(min_p), s, _ptr(sm), _ptr(al), _ptr(ot),
-                                        _ptr(ar))
+                                        float(temperature), int(top_k), float(top_p), float(min_p), s, _ptr(sm),
+                                        _ptr(al), _ptr(ot), _ptr(ar))
     if rc != 0:
         raise ValueError(f"oracle_spec_accept_sampled failed with status {rc}")
     return sm, al, ot, ar
+
+
+def keyed_exp2(y: float) -> float:
+    """The fixed float32 2^y (y <= 0) the top-p weights are built from."""
+    return float(_load().oracle_keyed_exp2(float(y)))
+
+
+def topkp_kept(row, temperature, top_k=0, top_p=1.0):
+    """(n, order): the top-k / top-p filters keep the first n tokens of `order`
+    (logit descending, id ascending)."""
+    r = _c(row, np.float32)
+    order = np.empty(r.shape[0], dtype=np.int32)
+    n = _load().oracle_topkp_kept(_ptr(r), r.shape[0], float(temperature), int(top_k), float(top_p), _ptr(order))
+    if n < 0:
+        raise MemoryError("oracle_topkp_kept")
+    return int(n), order
 
 
 def fnv1a64(data: bytes) -> int:

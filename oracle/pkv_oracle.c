@@ -449,16 +449,115 @@ static float keyed_gumbel(uint64_t seed, int32_t pos, int32_t v)
 }
 
 /*
+ * 2^y for y <= 0 as a fixed float32 operation sequence, so that every platform
+ * computes the same bits: y < -32 gives 0 (such a weight is below the 2^-32
+ * resolution of the integer weights below); otherwise n = floor(y), f = y - n in
+ * [0, 1), and 2^f = e^{f ln 2} is the Taylor polynomial of degree 8,
+ * sum_k (ln 2)^k / k! f^k, with float32 coefficients, evaluated by Horner's rule
+ * with separately rounded multiplies and adds; the result is scaled by 2^n exactly.
+ */
+float oracle_keyed_exp2(float y)
+{
+    static const float c[9] = {0x1p+0f, 0x1.62e430p-1f, 0x1.ebfbe0p-3f, 0x1.c6b08ep-5f, 0x1.3b2ab6p-7f,
+                               0x1.5d87fep-10f, 0x1.430912p-13f, 0x1.ffcbfcp-17f, 0x1.62c022p-20f};
+    if (!(y >= -32.0f))
+        return 0.0f;
+    if (y >= 0.0f)
+        return 1.0f;
+    const float n = floorf(y);
+    const float f = y - n;
+    float p = c[8];
+    for (int k = 7; k >= 0; --k) {
+        const float t = p * f;
+        p = t + c[k];
+    }
+    return ldexpf(p, (int)n);
+}
+
+/* Integer weight of token v in a row with maximum l_max at temperature T:
+ * floor(2^32 * keyed_exp2(((l_v - l_max) / T) * log2(e))), every step a correctly
+ * rounded float32 operation.  The probability of v is its weight over the row's
+ * total; integer weights make every sum exact, whatever the order. */
+static uint64_t keyed_weight(float l, float l_max, float temperature)
+{
+    const float d = l - l_max;
+    const float z = d / temperature;
+    const float y = z * 0x1.715476p+0f;
+    const float w = oracle_keyed_exp2(y);
+    return (uint64_t)(w * 4294967296.0f);
+}
+
+/* the order tokens are filtered in: logit descending, then token id ascending */
+static const float *g_sort_row;
+static int order_cmp(const void *a, const void *b)
+{
+    const int32_t x = *(const int32_t *)a, y = *(const int32_t *)b;
+    const float lx = g_sort_row[x], ly = g_sort_row[y];
+    if (lx > ly)
+        return -1;
+    if (lx < ly)
+        return 1;
+    return x < y ? -1 : (x > y ? 1 : 0);
+}
+
+/*
+ * Tokens kept by top-k and top-p, as a count n: the kept tokens are the first n of
+ * the order (logit descending, id ascending).  top-k keeps k tokens (k <= 0 or
+ * k >= vocab: all).  top-p keeps the shortest prefix whose weight reaches
+ * ceil(p_fix * total / 2^32), p_fix = floor(p * 2^32), total = the row's weight
+ * (0 < p < 1; otherwise all).  n = min of the two.  order_out (vocab entries) may
+ * be NULL; it receives the order.  Returns n, or -1 when out of memory.
+ */
+int32_t oracle_topkp_kept(const float *row, int32_t vocab, float temperature, int32_t top_k, float top_p,
+                          int32_t *order_out)
+{
+    int32_t *order = order_out ? order_out : (int32_t *)malloc(sizeof(int32_t) * (size_t)vocab);
+    if (!order)
+        return -1;
+    for (int32_t v = 0; v < vocab; ++v)
+        order[v] = v;
+    g_sort_row = row;
+    qsort(order, (size_t)vocab, sizeof(int32_t), order_cmp);
+    int32_t n = vocab;
+    if (top_k > 0 && top_k < n)
+        n = top_k;
+    if (top_p > 0.0f && top_p < 1.0f) {
+        const float l_max = row[order[0]];
+        uint64_t total = 0;
+        for (int32_t v = 0; v < vocab; ++v)
+            total += keyed_weight(row[v], l_max, temperature);
+        const uint64_t p_fix = (uint64_t)(top_p * 4294967296.0f);
+        const unsigned __int128 prod = (unsigned __int128)p_fix * total;
+        const uint64_t thr = (uint64_t)((prod + 0xFFFFFFFFu) >> 32);
+        uint64_t cum = 0;
+        int32_t np = vocab;
+        for (int32_t i = 0; i < vocab; ++i) {
+            cum += keyed_weight(row[order[i]], l_max, temperature);
+            if (cum >= thr) {
+                np = i + 1;
+                break;
+            }
+        }
+        if (np < n)
+            n = np;
+    }
+    if (!order_out)
+        free(order);
+    return n;
+}
+
+/*
  * The target's keyed draw for one row (TensorFold article, "先记住一条铁律": every
- * draw is keyed by seed, absolute position and token id; the min_p filter is
- * part of the keyed rule).  temperature == 0: the greedy argmax.  Otherwise, with
- * l_max the row maximum and thr = l_max + temperature * log(min_p) (no filter
- * when min_p <= 0), the draw is the lowest v maximising l_v / temperature +
- * g(seed, pos, v) over the v with l_v >= thr, all in float32.  log(min_p) is the
- * host libm's logf.
+ * draw is keyed by seed, absolute position and token id; "接受规则": the top-k,
+ * top-p and min_p filters are part of the keyed rule).  temperature == 0: the
+ * greedy argmax.  Otherwise the kept tokens are those that pass all three filters,
+ * each defined on the whole row: the first n of the order by oracle_topkp_kept, and
+ * l_v >= thr with thr = l_max + temperature * log(min_p) (no filter when min_p <= 0;
+ * log(min_p) is the host libm's logf).  The draw is the lowest v maximising
+ * l_v / temperature + g(seed, pos, v) over the kept v, all in float32.
  */
 static int32_t keyed_draw(const float *row, int32_t vocab, uint64_t seed, int32_t pos, float temperature,
-                          float min_p)
+                          int32_t top_k, float top_p, float min_p, uint8_t *kept)
 {
     int32_t best = 0;
     for (int32_t v = 1; v < vocab; ++v)
@@ -468,10 +567,23 @@ static int32_t keyed_draw(const float *row, int32_t vocab, uint64_t seed, int32_
         return best;
     const float l_max = row[best];
     const float thr = min_p > 0.0f ? l_max + temperature * logf(min_p) : -INFINITY;
+    const int filtered = (top_k > 0 && top_k < vocab) || (top_p > 0.0f && top_p < 1.0f);
+    if (filtered) {
+        int32_t *order = (int32_t *)malloc(sizeof(int32_t) * (size_t)vocab);
+        if (!order)
+            return -1;
+        const int32_t n = oracle_topkp_kept(row, vocab, temperature, top_k, top_p, order);
+        memset(kept, 0, (size_t)vocab);
+        for (int32_t i = 0; i < n; ++i)
+            kept[order[i]] = 1;
+        free(order);
+    }
     int32_t pick = -1;
     float top = -INFINITY;
     for (int32_t v = 0; v < vocab; ++v) {
         if (!(row[v] >= thr))
+            continue;
+        if (filtered && !kept[v])
             continue;
         const float sc = row[v] / temperature + keyed_gumbel(seed, pos, v);
         if (pick < 0 || sc > top) {
@@ -491,13 +603,19 @@ static int32_t keyed_draw(const float *row, int32_t vocab, uint64_t seed, int32_
  */
 int oracle_spec_accept_sampled(const float *logits, int32_t vocab, const int32_t *q_starts,
                                const int32_t *draft_tokens, const int32_t *parents,
-                               const int32_t *positions, uint64_t seed, float temperature, float min_p,
+                               const int32_t *positions, uint64_t seed, float temperature,
+                               int32_t top_k, float top_p, float min_p,
                                int32_t num_seqs, int32_t *sampled_out, int32_t *accept_len,
                                int32_t *out_tokens, int32_t *accepted_rows)
 {
     const int64_t total = q_starts[num_seqs];
+    uint8_t *kept = (uint8_t *)malloc((size_t)vocab);
+    if (!kept)
+        return -2;
     for (int64_t r = 0; r < total; ++r)
-        sampled_out[r] = keyed_draw(logits + (size_t)r * vocab, vocab, seed, positions[r], temperature, min_p);
+        sampled_out[r] = keyed_draw(logits + (size_t)r * vocab, vocab, seed, positions[r], temperature, top_k,
+                                    top_p, min_p, kept);
+    free(kept);
     for (int32_t s = 0; s < num_seqs; ++s) {
         const int32_t r0 = q_starts[s], W = q_starts[s + 1] - q_starts[s];
         if (W <= 0) {

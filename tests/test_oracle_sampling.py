@@ -137,3 +137,82 @@ def test_exact_score_ties_go_to_the_lowest_token(oracle_mod):
     d = oracle_mod.spec_accept_sampled(row, np.array([0, 1], np.int32), np.array([-1], np.int32),
                                        np.array([pos], np.int32), seed=seed, temperature=1.0)[0]
     assert d[0] == v1 < v2
+
+
+# ------------------------------------------------------------- top-k / top-p --
+def test_keyed_exp2_accuracy_and_exact_points(oracle_mod):
+    import math
+    ys = np.concatenate([np.linspace(-32, 0, 4001), -np.random.default_rng(3).random(2000) * 32])
+    for y in ys.astype(np.float32):
+        got = oracle_mod.keyed_exp2(float(y))
+        ref = 2.0 ** float(y)
+        assert abs(got - ref) <= 4e-7 * ref, (float(y), got, ref)
+    for k in range(33):                      # integers: the polynomial is 1 at f = 0, scaling is exact
+        assert oracle_mod.keyed_exp2(-float(k)) == 2.0 ** -k
+    assert oracle_mod.keyed_exp2(0.0) == 1.0
+    assert oracle_mod.keyed_exp2(-32.5) == 0.0 and oracle_mod.keyed_exp2(float("-inf")) == 0.0
+
+
+def _weights(oracle_mod, row, T):
+    """Integer weights of a row, from the oracle's exp2 and numpy float32 arithmetic."""
+    r = np.asarray(row, np.float32)
+    lmax = r.max()
+    y = ((r - lmax) / np.float32(T)) * np.float32(1.4426950408889634)
+    return [int(np.float32(oracle_mod.keyed_exp2(float(v))) * np.float32(2.0 ** 32)) for v in y.astype(np.float32)]
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_topkp_kept_is_the_defined_prefix(oracle_mod, seed):
+    rng = np.random.default_rng(seed)
+    V = 500
+    row = (rng.standard_normal(V) * 2).astype(np.float32)
+    row[rng.integers(0, V, 40)] = row[7]                  # ties, broken by token id
+    T = 0.8
+    n, order = oracle_mod.topkp_kept(row, T)
+    assert n == V
+    ref_order = np.lexsort((np.arange(V), -row.astype(np.float64)))
+    assert np.array_equal(order, ref_order)
+    assert oracle_mod.topkp_kept(row, T, top_k=17)[0] == 17
+    W = _weights(oracle_mod, row, T)
+    total = sum(W)
+    for p in (0.05, 0.3, 0.5, 0.9, 0.99):
+        n, _ = oracle_mod.topkp_kept(row, T, top_p=p)
+        p_fix = int(np.float32(p) * np.float32(2.0 ** 32))
+        thr = -(-(p_fix * total) // 2 ** 32)              # ceil, exact integers
+        cum = np.cumsum([W[i] for i in ref_order], dtype=object)
+        assert cum[n - 1] >= thr and (n == 1 or cum[n - 2] < thr), (p, n)
+        assert oracle_mod.topkp_kept(row, T, top_k=n + 5, top_p=p)[0] == n
+        assert oracle_mod.topkp_kept(row, T, top_k=max(1, n - 3), top_p=p)[0] == max(1, n - 3)
+    assert oracle_mod.topkp_kept(row, T, top_p=1e-9)[0] == 1
+    assert oracle_mod.topkp_kept(row, T, top_p=1.0)[0] == V
+
+
+def test_topkp_draws(oracle_mod):
+    rng = np.random.default_rng(9)
+    V, R = 300, 400
+    logits = np.tile((rng.standard_normal(V) * 1.5).astype(np.float32), (R, 1))
+    qs = np.arange(R + 1, dtype=np.int32)
+    drafts = np.full(R, -1, np.int32)
+    pos = np.arange(R, dtype=np.int32) + 1000
+    amax = int(np.argmax(logits[0]))
+    # top-k 1 and a vanishing top-p leave only the argmax, whatever the noise
+    s1, *_ = oracle_mod.spec_accept_sampled(logits, qs, drafts, pos, seed=5, temperature=1.0, top_k=1)
+    s2, *_ = oracle_mod.spec_accept_sampled(logits, qs, drafts, pos, seed=5, temperature=1.0, top_p=1e-9)
+    assert np.all(s1 == amax) and np.all(s2 == amax)
+    # top-k 6: every draw is among the 6 largest; all 6 are drawn; frequencies follow the
+    # renormalised softmax of those 6 (loose statistical check)
+    s3, *_ = oracle_mod.spec_accept_sampled(logits, qs, drafts, pos, seed=5, temperature=1.0, top_k=6)
+    top6 = np.argsort(-logits[0].astype(np.float64), kind="stable")[:6]
+    assert set(s3.tolist()) <= set(top6.tolist()) and len(set(s3.tolist())) == 6
+    pr = np.exp(logits[0][top6].astype(np.float64))
+    pr /= pr.sum()
+    cnt = np.array([np.sum(s3 == t) for t in top6])
+    assert np.all(np.abs(cnt / R - pr) < 5 * np.sqrt(pr * (1 - pr) / R) + 0.01)
+    # top-p keeps the prefix the kept-set function names
+    n, order = oracle_mod.topkp_kept(logits[0], 1.0, top_p=0.6)
+    s4, *_ = oracle_mod.spec_accept_sampled(logits, qs, drafts, pos, seed=6, temperature=1.0, top_p=0.6)
+    assert set(s4.tolist()) <= set(order[:n].tolist())
+    # no filter: the same draws as before the filters existed
+    s5, *_ = oracle_mod.spec_accept_sampled(logits, qs, drafts, pos, seed=5, temperature=1.0)
+    s6, *_ = oracle_mod.spec_accept_sampled(logits, qs, drafts, pos, seed=5, temperature=1.0, top_k=V, top_p=1.0)
+    assert np.array_equal(s5, s6)
