@@ -224,7 +224,7 @@ def run_ours(args, rank, world, local_rank):
     positions = None
     if b.logits is not None:
         logits, drafts = d(b.logits), d(b.draft_tokens)
-        acc_ws = torch.empty(2 * pkv.spec_accept_workspace_size(b.total_q_rows, b.logits.shape[1]),
+        acc_ws = torch.empty(pkv.sampled_accept_workspace_size(b.total_q_rows, b.logits.shape[1]),
                              dtype=torch.uint8, device=dev)
         # absolute position of the token each verify row draws: L - W + w + 1
         row_seq = np.searchsorted(b.q_starts, np.arange(b.total_q_rows), side="right") - 1
@@ -237,7 +237,8 @@ def run_ours(args, rank, world, local_rank):
     max_ctx, max_rows = b.max_context_len, b.max_q_rows_per_seq
     stream = torch.cuda.current_stream()
     # per layer: append (if any) + attention split kernel + attention merge kernel; accept: 2
-    launches_per_step = layers * (int(has_append) + 2) + (2 if logits is not None else 0)
+    accept_launches = {"greedy": 2, "sampled": 3, "sampled-topkp": 4}[accept_mode] if logits is not None else 0
+    launches_per_step = layers * (int(has_append) + 2) + accept_launches
 
     def step(ev_pairs=None, li=None):
         for i in range(layers):
@@ -266,9 +267,10 @@ def run_ours(args, rank, world, local_rank):
             if ev_pairs is not None:
                 ev_pairs[li][1].record(stream)
                 li += 1
-        if logits is not None and accept_mode == "sampled":
+        if logits is not None and accept_mode in ("sampled", "sampled-topkp"):
+            filt = dict(top_k=50, top_p=0.9) if accept_mode == "sampled-topkp" else {}
             pkv.spec_accept_sampled(logits, q_starts, drafts, positions, seed=args.seed + 1, temperature=1.0,
-                                    min_p=0.05, parents=parents, sampled_out=acc_out[0], accept_len=acc_out[1],
+                                    min_p=0.05, **filt, parents=parents, sampled_out=acc_out[0], accept_len=acc_out[1],
                                     out_tokens=acc_out[2], accepted_rows=acc_out[3], workspace=acc_ws,
                                     stream=stream)
         elif logits is not None and tree:
@@ -538,8 +540,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kv-bits", type=int, choices=(16, 8, 4), default=16,
                     help="16: bf16 K/V pools; 8 / 4: quantised KV blocks (Q8 / Q4 records)")
-    ap.add_argument("--accept", choices=("greedy", "sampled"), default="greedy",
-                    help="verify workloads: greedy accept, or keyed sampling at T = 1, min_p = 0.05")
+    ap.add_argument("--accept", choices=("greedy", "sampled", "sampled-topkp"), default="greedy",
+                    help="verify workloads: greedy accept, keyed sampling at T = 1, min_p = 0.05, or the same "
+                         "with top_k = 50 and top_p = 0.9")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

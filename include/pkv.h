@@ -296,12 +296,21 @@ int spec_accept_tree_greedy(const float *logits, int32_t vocab,
 /*
  * Sampled accept (TensorFold article, "先记住一条铁律": every draw is keyed by
  * seed, absolute position and token id, and a draft is accepted only when it
- * equals the target's own draw; "接受规则": the min_p filter is part of the
- * keyed rule).  The target's draw at row r:
+ * equals the target's own draw; "接受规则": the top-k, top-p and min_p filters
+ * are part of the keyed rule).  The target's draw at row r:
  *   temperature == 0: the argmax (ties to the lowest id);
  *   otherwise the lowest v maximising l_v / temperature + g(seed, positions[r], v)
- *   over the v with l_v >= l_max + temperature * logf(min_p) (all v if min_p <= 0),
- *   where g = -log(-log(u)), u = ((w >> 9) + 1/2) / 2^23 and w is word (v mod 4)
+ *   over the kept v: those passing all three filters, each defined on the whole
+ *   row.  With the order "logit descending, token id ascending": top-k keeps the
+ *   first top_k tokens (off when top_k <= 0 or >= vocab); top-p keeps the
+ *   shortest prefix whose integer weight reaches ceil(p_fix * total / 2^32),
+ *   p_fix = floor(top_p * 2^32), total = the row's weight (off unless
+ *   0 < top_p < 1), the weight of v being floor(2^32 * exp2(((l_v - l_max) / T)
+ *   * log2 e)) with exp2 a fixed float32 sequence (0 below 2^-32; else the
+ *   degree-8 Taylor polynomial of 2^f, f the fraction, by Horner's rule, times
+ *   2^floor); min_p keeps l_v >= l_max + temperature * logf(min_p) (off when
+ *   min_p <= 0);
+ *   g = -log(-log(u)), u = ((w >> 9) + 1/2) / 2^23 and w is word (v mod 4)
  *   of Philox4x32-10(counter = (v / 4, pos, 0x6b657964, 0), key = seed); the
  *   logs are a fixed float32 operation sequence (atanh series) and every step is
  *   a correctly rounded float32 operation, so the draw is reproducible exactly.
@@ -309,13 +318,14 @@ int spec_accept_tree_greedy(const float *logits, int32_t vocab,
  * the draw in place of the argmax; outputs as spec_accept_tree_greedy, with
  * sampled_out holding every row's draw.
  *   positions   int32 [total_rows]: absolute position of the token each row draws
- *   workspace   >= 2 * spec_accept_workspace_size(total_rows, vocab) bytes
- * Launches three kernels (two when temperature == 0).
+ *   workspace   >= 2 * spec_accept_workspace_size(total_rows, vocab) + 8 * total_rows
+ *               bytes (the last part rounded up to 256)
+ * Launches three kernels (two when temperature == 0), four with top-k / top-p.
  */
 int spec_accept_sampled(const float *logits, int32_t vocab,
                         const int32_t *q_starts, const int32_t *draft_tokens,
                         const int32_t *parents, const int32_t *positions,
-                        uint64_t seed, float temperature, float min_p,
+                        uint64_t seed, float temperature, int32_t top_k, float top_p, float min_p,
                         int32_t num_seqs, int32_t total_rows,
                         int32_t *sampled_out, int32_t *accept_len, int32_t *out_tokens,
                         int32_t *accepted_rows, void *workspace, size_t workspace_bytes,

@@ -197,15 +197,172 @@ __device__ __forceinline__ float gumbel_of(uint32_t w)
     return -keyed_log(-keyed_log(u));
 }
 
-// Sampling pass: per (slice, row), the best l/T + g(seed, pos, v) over the tokens with
-// l >= l_max + off (off = T log(min_p), or -inf), ties to the lowest token.  The row
-// maximum comes from the argmax pass's slices.  Token v is keyed by word (v mod 4) of
-// Philox(ctr = (v / 4, pos, 0x6b657964, 0), key = seed).
+// ---- top-k / top-p: the kept tokens are a prefix of the order (logit descending,
+// token id ascending).  A token's place in that order is its 64-bit key
+// (~ascending-float-bits(l) << 32) | v, so the kept set is {v : key_v <= cut}.
+__device__ __forceinline__ uint64_t order_key(float l, int v)
+{
+    uint32_t b = __float_as_uint(l == 0.f ? 0.f : l);   // -0 and +0 are one logit
+    b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);     // ascending with the float
+    return ((uint64_t)~b << 32) | (uint32_t)v;
+}
+
+// 2^y for y <= 0 as a fixed float32 sequence: 0 below -32; else n = floor(y),
+// f = y - n, the degree-8 Taylor polynomial of e^{f ln 2} (float32 coefficients
+// (ln 2)^k / k!) by Horner's rule with separately rounded steps, times 2^n.
+__device__ __forceinline__ float keyed_exp2(float y)
+{
+    if (!(y >= -32.0f))
+        return 0.0f;
+    if (y >= 0.0f)
+        return 1.0f;
+    const float n = floorf(y);
+    const float f = __fsub_rn(y, n);
+    float p = 0x1.62c022p-20f;
+    p = __fadd_rn(__fmul_rn(p, f), 0x1.ffcbfcp-17f);
+    p = __fadd_rn(__fmul_rn(p, f), 0x1.430912p-13f);
+    p = __fadd_rn(__fmul_rn(p, f), 0x1.5d87fep-10f);
+    p = __fadd_rn(__fmul_rn(p, f), 0x1.3b2ab6p-7f);
+    p = __fadd_rn(__fmul_rn(p, f), 0x1.c6b08ep-5f);
+    p = __fadd_rn(__fmul_rn(p, f), 0x1.ebfbe0p-3f);
+    p = __fadd_rn(__fmul_rn(p, f), 0x1.62e430p-1f);
+    p = __fadd_rn(__fmul_rn(p, f), 1.0f);
+    return __fmul_rn(p, __int_as_float((127 + (int)n) << 23));
+}
+
+// Integer weight floor(2^32 * 2^(((l - l_max) / T) log2 e)): sums of weights are exact.
+__device__ __forceinline__ uint64_t keyed_weight(float l, float l_max, float temperature)
+{
+    const float y = __fmul_rn(__fdiv_rn(__fsub_rn(l, l_max), temperature), 0x1.715476p+0f);
+    return __float2ull_rz(__fmul_rn(keyed_exp2(y), 4294967296.0f));
+}
+
+constexpr int kSelThreads = 512;
+constexpr int kSelWarps = kSelThreads / 32;
+
+// Smallest key K with (sum of w_v over key_v <= K) >= need (w_v = the weight, or 1 when
+// COUNT): eight passes of 8 bits from the top, each a per-warp histogram of the
+// candidates that match the bits found so far.
+template <bool COUNT>
+__device__ uint64_t select_key(const float *__restrict__ row, int vocab, float l_max, float temperature,
+                               uint64_t need, unsigned long long (*hist)[256], uint64_t *bcast)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint64_t prefix = 0;
+    for (int pass = 0; pass < 8; ++pass) {
+        const int shift = 56 - 8 * pass;
+        for (int i = threadIdx.x; i < kSelWarps * 256; i += kSelThreads)
+            (&hist[0][0])[i] = 0ull;
+        __syncthreads();
+        for (int v = threadIdx.x; v < vocab; v += kSelThreads) {
+            const float l = __ldg(row + v);
+            const uint64_t key = order_key(l, v);
+            if (pass > 0 && (key >> (shift + 8)) != prefix)
+                continue;
+            const uint64_t w = COUNT ? 1ull : keyed_weight(l, l_max, temperature);
+            if (w)
+                atomicAdd(&hist[warp][(key >> shift) & 255], (unsigned long long)w);
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // lane j owns bins 8j .. 8j + 7
+            uint64_t bins[8], own = 0;
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+                uint64_t t = 0;
+                for (int w = 0; w < kSelWarps; ++w)
+                    t += hist[w][8 * lane + b];
+                bins[b] = t;
+                own += t;
+            }
+            uint64_t incl = own;   // inclusive scan over lanes
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const uint64_t o = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off)
+                    incl += o;
+            }
+            const uint64_t before = incl - own;
+            const bool mine = before < need && incl >= need;
+            const unsigned who = __ballot_sync(0xffffffffu, mine);
+            if (mine && lane == __ffs(who) - 1) {
+                uint64_t cum = before;
+                int b = 0;
+                for (; b < 7; ++b) {
+                    if (cum + bins[b] >= need)
+                        break;
+                    cum += bins[b];
+                }
+                bcast[0] = (prefix << 8) | (uint64_t)(8 * lane + b);
+                bcast[1] = need - cum;
+            }
+            if (!who && lane == 0) {   // need beyond the total (cannot happen for valid filters)
+                bcast[0] = (prefix << 8) | 255ull;
+                bcast[1] = 1;
+            }
+        }
+        __syncthreads();
+        prefix = bcast[0];
+        need = bcast[1];
+        __syncthreads();
+    }
+    return prefix;
+}
+
+// One CTA per row: the cut key of top-k (k tokens) and of top-p (the shortest prefix
+// whose weight reaches ceil(p_fix * total / 2^32)); the kept set is key <= min of the two.
+__global__ void __launch_bounds__(kSelThreads)
+topkp_cut_kernel(const float *__restrict__ logits, int vocab, const float2 *__restrict__ part_max, int n_chunks,
+                 float temperature, int top_k, int use_p, unsigned long long p_fix,
+                 unsigned long long *__restrict__ cut)
+{
+    __shared__ unsigned long long hist[kSelWarps][256];
+    __shared__ uint64_t bcast[2];
+    __shared__ unsigned long long total_sh;
+    const int r = blockIdx.x;
+    const float *row = logits + (size_t)r * vocab;
+    float l_max = -INFINITY;
+    for (int i = 0; i < n_chunks; ++i)
+        l_max = fmaxf(l_max, part_max[(size_t)r * n_chunks + i].x);
+    uint64_t c = ~0ull;
+    if (top_k > 0 && top_k < vocab)
+        c = select_key<true>(row, vocab, l_max, temperature, (uint64_t)top_k, hist, bcast);
+    if (use_p) {
+        if (threadIdx.x == 0)
+            total_sh = 0ull;
+        __syncthreads();
+        unsigned long long t = 0;
+        for (int v = threadIdx.x; v < vocab; v += kSelThreads)
+            t += keyed_weight(__ldg(row + v), l_max, temperature);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            t += __shfl_xor_sync(0xffffffffu, t, off);
+        if ((threadIdx.x & 31) == 0)
+            atomicAdd(&total_sh, t);
+        __syncthreads();
+        const uint64_t total = total_sh;
+        // ceil(p_fix * total / 2^32) with the 128-bit product
+        const uint64_t lo = p_fix * total, hi = __umul64hi(p_fix, total);
+        const uint64_t lo2 = lo + 0xFFFFFFFFull;
+        uint64_t thr = ((hi + (lo2 < lo ? 1ull : 0ull)) << 32) | (lo2 >> 32);
+        thr = thr ? thr : 1ull;   // a zero threshold keeps the first token, as a threshold of 1 does
+        const uint64_t cp = select_key<false>(row, vocab, l_max, temperature, thr, hist, bcast);
+        c = cp < c ? cp : c;
+    }
+    if (threadIdx.x == 0)
+        cut[r] = c;
+}
+
+// Sampling pass: per (slice, row), the best l/T + g(seed, pos, v) over the kept tokens
+// (l >= l_max + off, off = T log(min_p) or -inf, and key_v <= cut[r] when top-k / top-p
+// are on), ties to the lowest token.  The row maximum comes from the argmax pass's
+// slices.  Token v is keyed by word (v mod 4) of Philox(ctr = (v / 4, pos,
+// 0x6b657964, 0), key = seed).
 __global__ void __launch_bounds__(kArgmaxThreads)
 sample_chunks_kernel(const float *__restrict__ logits, int vocab, int chunk, int n_chunks,
                      const float2 *__restrict__ part_max, float2 *__restrict__ part,
                      const int32_t *__restrict__ positions, uint32_t seed_lo, uint32_t seed_hi,
-                     float temperature, float off, int vec_ok)
+                     float temperature, float off, int vec_ok, const unsigned long long *__restrict__ cut)
 {
     const int c = blockIdx.x, r = blockIdx.y;
     const int lo = c * chunk;
@@ -215,6 +372,7 @@ sample_chunks_kernel(const float *__restrict__ logits, int vocab, int chunk, int
     for (int i = 0; i < n_chunks; ++i)
         l_max = fmaxf(l_max, part_max[(size_t)r * n_chunks + i].x);
     const float thr = off == -INFINITY ? -INFINITY : __fadd_rn(l_max, off);
+    const uint64_t kcut = cut ? cut[r] : ~0ull;
     const uint32_t pos = (uint32_t)__ldg(positions + r);
     Best b = {-INFINITY, kNoIndex};
     if (vec_ok) {
@@ -226,13 +384,13 @@ sample_chunks_kernel(const float *__restrict__ logits, int vocab, int chunk, int
             const float xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                if (xs[j] >= thr)
+                if (xs[j] >= thr && order_key(xs[j], 4 * i + j) <= kcut)
                     b = better(b, Best{__fadd_rn(__fdiv_rn(xs[j], temperature), gumbel_of(w[j])), 4 * i + j});
         }
     } else {
         for (int v = lo + threadIdx.x; v < hi; v += kArgmaxThreads) {
             const float x = __ldcs(row + v);
-            if (!(x >= thr))
+            if (!(x >= thr) || order_key(x, v) > kcut)
                 continue;
             uint32_t w[4] = {(uint32_t)v >> 2, pos, 0x6b657964u, 0u};
             philox4x32_10(w, seed_lo, seed_hi);
@@ -435,7 +593,8 @@ extern "C" int spec_accept_tree_greedy(const float *logits, int32_t vocab, const
 
 extern "C" int spec_accept_sampled(const float *logits, int32_t vocab, const int32_t *q_starts,
                                    const int32_t *draft_tokens, const int32_t *parents, const int32_t *positions,
-                                   uint64_t seed, float temperature, float min_p, int32_t num_seqs,
+                                   uint64_t seed, float temperature, int32_t top_k, float top_p, float min_p,
+                                   int32_t num_seqs,
                                    int32_t total_rows, int32_t *sampled_out, int32_t *accept_len,
                                    int32_t *out_tokens, int32_t *accepted_rows, void *workspace,
                                    size_t workspace_bytes, void *stream)
@@ -445,9 +604,10 @@ extern "C" int spec_accept_sampled(const float *logits, int32_t vocab, const int
     if (num_seqs < 0 || total_rows < 0 || vocab <= 0)
         return set_error(PKV_ERR_SHAPE, "spec_accept_sampled: bad sizes (num_seqs %d, rows %d, vocab %d)",
                          num_seqs, total_rows, vocab);
-    if (!(temperature >= 0.0f) || !(temperature < INFINITY) || !(min_p <= 1.0f))
+    if (!(temperature >= 0.0f) || !(temperature < INFINITY) || !(min_p <= 1.0f) || !(top_p == top_p))
         return set_error(PKV_ERR_SHAPE, "spec_accept_sampled: temperature %g must be finite and >= 0, "
-                         "min_p %g at most 1", (double)temperature, (double)min_p);
+                         "min_p %g at most 1, top_p %g a number", (double)temperature, (double)min_p,
+                         (double)top_p);
     if (num_seqs == 0)
         return PKV_OK;
     if (!q_starts || !accept_len || (total_rows > 0 && (!logits || !draft_tokens || !positions || !sampled_out ||
@@ -456,9 +616,10 @@ extern "C" int spec_accept_sampled(const float *logits, int32_t vocab, const int
     if (total_rows > 0 && !aligned16(logits))
         return set_error(PKV_ERR_ALIGN, "spec_accept_sampled: logits must be 16-byte aligned");
     const size_t one = spec_accept_workspace_size(total_rows, vocab);
-    if (workspace_bytes < 2 * one)
+    const size_t need_ws = 2 * one + round_up((size_t)total_rows * 8, 256);
+    if (workspace_bytes < need_ws)
         return set_error(PKV_ERR_WORKSPACE, "spec_accept_sampled: workspace %zu < %zu bytes", workspace_bytes,
-                         2 * one);
+                         need_ws);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int n_chunks = accept_chunks(total_rows, vocab, sm_count());
     float2 *part_max = static_cast<float2 *>(workspace);
@@ -477,9 +638,21 @@ extern "C" int spec_accept_sampled(const float *logits, int32_t vocab, const int
         if (temperature > 0.0f) {
             // the min_p threshold's offset T log(min_p), rounded once here and once in the kernel's add
             const float off = min_p > 0.0f ? temperature * logf(min_p) : -INFINITY;
+            unsigned long long *cut = nullptr;
+            const bool use_k = top_k > 0 && top_k < vocab;
+            const bool use_p = top_p > 0.0f && top_p < 1.0f;
+            if (use_k || use_p) {
+                cut = reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(workspace) + 2 * one);
+                const unsigned long long p_fix = use_p ? (unsigned long long)(top_p * 4294967296.0f) : 0ull;
+                topkp_cut_kernel<<<total_rows, kSelThreads, 0, st>>>(logits, vocab, part_max, n_chunks, temperature,
+                                                                     use_k ? top_k : 0, use_p ? 1 : 0, p_fix, cut);
+                rc = check_cuda(cudaGetLastError(), "spec_accept_sampled top-k / top-p launch");
+                if (rc)
+                    return rc;
+            }
             sample_chunks_kernel<<<dim3(n_chunks, total_rows), kArgmaxThreads, 0, st>>>(
                 logits, vocab, chunk, n_chunks, part_max, part, positions, (uint32_t)seed, (uint32_t)(seed >> 32),
-                temperature, off, vec_ok);
+                temperature, off, vec_ok, cut);
             rc = check_cuda(cudaGetLastError(), "spec_accept_sampled sample launch");
             if (rc)
                 return rc;

@@ -78,7 +78,7 @@ int sm_count()
 
 }  // namespace pkv
 
-extern "C" int pkv_abi_version(void) { return 1; }
+extern "C" int pkv_abi_version(void) { return 2; }
 
 extern "C" const char *pkv_last_error_string(void) { return pkv::t_last_error; }
 

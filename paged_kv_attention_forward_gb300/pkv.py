@@ -88,8 +88,8 @@ def lib(build_if_missing: bool = False):
             L.paged_tree_attention_forward.restype = ctypes.c_int
             L.spec_accept_tree_greedy.argtypes = [P, i32, P, P, P, i32, i32, P, P, P, P, P, sz, P]
             L.spec_accept_tree_greedy.restype = ctypes.c_int
-            L.spec_accept_sampled.argtypes = [P, i32, P, P, P, P, ctypes.c_uint64, ctypes.c_float,
-                                              ctypes.c_float, i32, i32, P, P, P, P, P, sz, P]
+            L.spec_accept_sampled.argtypes = [P, i32, P, P, P, P, ctypes.c_uint64, ctypes.c_float, i32,
+                                              ctypes.c_float, ctypes.c_float, i32, i32, P, P, P, P, P, sz, P]
             L.spec_accept_sampled.restype = ctypes.c_int
             L.paged_block_hashes.argtypes = [P, P, i32, i32, i32, ctypes.c_uint64, P, P, i32, P]
             L.paged_block_hashes.restype = ctypes.c_int
@@ -284,8 +284,8 @@ def spec_accept_tree_greedy(logits, q_starts, draft_tokens, parents, *, argmax_o
 
 
 def spec_accept_sampled(logits, q_starts, draft_tokens, positions, *, seed: int, temperature: float,
-                        min_p: float = 0.0, parents=None, sampled_out=None, accept_len=None, out_tokens=None,
-                        accepted_rows=None, workspace=None, stream=None):
+                        min_p: float = 0.0, top_k: int = 0, top_p: float = 1.0, parents=None, sampled_out=None,
+                        accept_len=None, out_tokens=None, accepted_rows=None, workspace=None, stream=None):
     """Keyed sampled accept (see include/pkv.h);
     returns (sampled [R], accept_len [S], out_tokens [R], accepted_rows [R])."""
     R, V = logits.shape
@@ -297,9 +297,10 @@ def spec_accept_sampled(logits, q_starts, draft_tokens, positions, *, seed: int,
     out_tokens = mk(R) if out_tokens is None else out_tokens
     accepted_rows = mk(R) if accepted_rows is None else accepted_rows
     if workspace is None:
-        workspace = torch.empty(max(2 * spec_accept_workspace_size(R, V), 256), dtype=torch.uint8, device=dev)
+        workspace = torch.empty(sampled_accept_workspace_size(R, V), dtype=torch.uint8, device=dev)
     _check(lib().spec_accept_sampled(_dptr(logits), V, _dptr(q_starts), _dptr(draft_tokens), _dptr(parents),
-                                     _dptr(positions), int(seed), float(temperature), float(min_p), S, R,
+                                     _dptr(positions), int(seed), float(temperature), int(top_k), float(top_p),
+                                     float(min_p), S, R,
                                      _dptr(sampled_out), _dptr(accept_len), _dptr(out_tokens),
                                      _dptr(accepted_rows), _dptr(workspace), workspace.numel(), _stream(stream)))
     return sampled_out, accept_len, out_tokens, accepted_rows
@@ -307,6 +308,11 @@ def spec_accept_sampled(logits, q_starts, draft_tokens, positions, *, seed: int,
 
 def spec_accept_workspace_size(total_rows, vocab) -> int:
     return int(lib().spec_accept_workspace_size(total_rows, vocab))
+
+
+def sampled_accept_workspace_size(total_rows, vocab) -> int:
+    """Workspace bytes spec_accept_sampled needs (see include/pkv.h)."""
+    return 2 * spec_accept_workspace_size(total_rows, vocab) + (total_rows * 8 + 255) // 256 * 256
 
 
 def spec_accept_greedy(logits, q_starts, draft_tokens, *, argmax_out=None, accept_len=None,

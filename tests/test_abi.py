@@ -32,7 +32,7 @@ def test_header_declarations_are_exported(pkv):
     for n in names:
         assert hasattr(lib, n), f"{n} declared in pkv.h but not exported"
     assert sorted(pkv.EXPORTED) == names
-    assert lib.pkv_abi_version() == 1
+    assert lib.pkv_abi_version() == 2
 
 
 def test_workspace_sizes(pkv):

@@ -18,12 +18,14 @@ def pkv():
     return m
 
 
-def _check(pkv, logits, q_starts, drafts, positions, seed, temperature, min_p=0.0, parents=None):
+def _check(pkv, logits, q_starts, drafts, positions, seed, temperature, min_p=0.0, parents=None, top_k=0,
+           top_p=1.0):
     got = pkv.spec_accept_sampled(dev(logits), dev(q_starts), dev(drafts), dev(positions), seed=seed,
-                                  temperature=temperature, min_p=min_p,
+                                  temperature=temperature, min_p=min_p, top_k=top_k, top_p=top_p,
                                   parents=None if parents is None else dev(parents))
     torch.cuda.synchronize()
-    ref = oracle.spec_accept_sampled(logits, q_starts, drafts, positions, seed, temperature, min_p, parents)
+    ref = oracle.spec_accept_sampled(logits, q_starts, drafts, positions, seed, temperature, min_p, parents,
+                                     top_k=top_k, top_p=top_p)
     for g, r, what in zip(got, ref, ("draws", "accept_len", "out_tokens", "accepted_rows")):
         assert np.array_equal(g.cpu().numpy(), r), what
     rc, bits = pkv.device_status()
@@ -76,3 +78,35 @@ def test_exact_ties_go_to_the_lowest_token(pkv):
     ref = _check(pkv, row, np.array([0, 1], np.int32), np.array([-1], np.int32), np.array([pos], np.int32),
                  seed=seed, temperature=1.0)
     assert ref[0][0] == v1
+
+
+@pytest.mark.parametrize("top_k,top_p,min_p,T", [(40, 1.0, 0.0, 1.0), (0, 0.9, 0.0, 1.0), (0, 0.3, 0.0, 0.6),
+                                                 (50, 0.95, 0.02, 0.8), (1, 1.0, 0.0, 1.0), (0, 1e-9, 0.0, 1.0),
+                                                 (0, 1e-12, 0.0, 1.0), (151935, 0.999, 0.0, 1.5)])
+def test_top_k_top_p_bit_exact(pkv, top_k, top_p, min_p, T):
+    # full vocabulary (151936) spec_verify rows; chains
+    b = wl.make_workload("spec_verify", seed=3, num_seqs=6)
+    pos = (np.arange(b.total_q_rows) * 3 + 100).astype(np.int32)
+    _check(pkv, b.logits, b.q_starts, b.draft_tokens, pos, seed=77, temperature=T, min_p=min_p, top_k=top_k,
+           top_p=top_p)
+
+
+def test_top_p_with_ties_and_signed_zeros(pkv):
+    # equal logits at the cut are ordered by token id; -0 and +0 are one logit
+    rng = np.random.default_rng(4)
+    V = 4099
+    lg = np.round(rng.standard_normal((6, V)) * 2).astype(np.float32)   # many exact ties
+    lg[:, ::7] = -0.0
+    lg[:, 3::7] = 0.0
+    qs = np.array([0, 2, 6], np.int32)
+    drafts = rng.integers(0, V, 6).astype(np.int32)
+    pos = rng.integers(0, 1 << 20, 6).astype(np.int32)
+    for top_k, top_p in ((100, 1.0), (0, 0.5), (0, 0.97), (33, 0.8)):
+        _check(pkv, lg, qs, drafts, pos, seed=12, temperature=1.0, top_k=top_k, top_p=top_p)
+
+
+def test_top_k_top_p_trees(pkv):
+    b = wl.make_workload("spec_tree", seed=5, num_seqs=4)
+    pos = (np.arange(b.total_q_rows) * 5 + 3).astype(np.int32)
+    _check(pkv, b.logits, b.q_starts, b.draft_tokens, pos, seed=8, temperature=1.0, parents=b.parents, top_k=20,
+           top_p=0.8)
