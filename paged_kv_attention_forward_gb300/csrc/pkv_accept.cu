@@ -14,6 +14,7 @@
 //   (same order), writes argmax_out, finds the first mismatching draft with a
 //   ballot, and writes accept_len and out_tokens.
 #include <cfloat>
+#include <mutex>
 
 #include "pkv_internal.h"
 
@@ -239,40 +240,75 @@ __device__ __forceinline__ uint64_t keyed_weight(float l, float l_max, float tem
 
 constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kSelCap = 4096;   // candidates kept in shared memory once they are this few
 
-// Smallest key K with (sum of w_v over key_v <= K) >= need (w_v = the weight, or 1 when
-// COUNT): eight passes of 8 bits from the top, each a per-warp histogram of the
-// candidates that match the bits found so far.
+struct SelSmem {
+    unsigned long long hw[kSelWarps][256];   // per-warp weight (or count) histograms
+    unsigned int hc[kSelWarps][256];         // per-warp candidate counts
+    float cl[kSelCap];                       // compacted candidates: logit, token
+    int cv[kSelCap];
+    uint64_t bcast[3];
+    unsigned int n_list;
+};
+
+// Smallest key K with (sum of w_v over key_v <= K) >= need, w_v = the token's weight
+// (or 1 when COUNT).  Eight passes of 8 bits from the top, each a per-warp histogram of
+// the candidates that match the bits found so far; once the candidates are at most
+// kSelCap they are copied to shared memory and later passes read only them.  For the
+// weighted select `need` is derived from the row total, found in pass 0:
+// ceil(p_fix * total / 2^32) (at least 1).  Integer sums make the result independent
+// of the order in which threads add.
 template <bool COUNT>
 __device__ uint64_t select_key(const float *__restrict__ row, int vocab, float l_max, float temperature,
-                               uint64_t need, unsigned long long (*hist)[256], uint64_t *bcast)
+                               uint64_t need, uint64_t p_fix, SelSmem &sm)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint64_t prefix = 0;
+    bool listed = false;            // candidates live in sm.cl / sm.cv
+    uint32_t n_cand = (uint32_t)vocab;
+    if (threadIdx.x == 0)
+        sm.n_list = 0;
     for (int pass = 0; pass < 8; ++pass) {
         const int shift = 56 - 8 * pass;
-        for (int i = threadIdx.x; i < kSelWarps * 256; i += kSelThreads)
-            (&hist[0][0])[i] = 0ull;
+        const bool compact = !listed && n_cand <= (uint32_t)kSelCap;
+        for (int i = threadIdx.x; i < kSelWarps * 256; i += kSelThreads) {
+            (&sm.hw[0][0])[i] = 0ull;
+            (&sm.hc[0][0])[i] = 0u;
+        }
         __syncthreads();
-        for (int v = threadIdx.x; v < vocab; v += kSelThreads) {
-            const float l = __ldg(row + v);
+        const int n_iter = listed ? (int)sm.n_list : vocab;
+        for (int i = threadIdx.x; i < n_iter; i += kSelThreads) {
+            const float l = listed ? sm.cl[i] : __ldg(row + i);
+            const int v = listed ? sm.cv[i] : i;
             const uint64_t key = order_key(l, v);
             if (pass > 0 && (key >> (shift + 8)) != prefix)
                 continue;
+            if (compact) {
+                const unsigned int at = atomicAdd(&sm.n_list, 1u);
+                sm.cl[at] = l;
+                sm.cv[at] = v;
+            }
             const uint64_t w = COUNT ? 1ull : keyed_weight(l, l_max, temperature);
+            const int bin = (int)((key >> shift) & 255);
             if (w)
-                atomicAdd(&hist[warp][(key >> shift) & 255], (unsigned long long)w);
+                atomicAdd(&sm.hw[warp][bin], (unsigned long long)w);
+            atomicAdd(&sm.hc[warp][bin], 1u);
         }
         __syncthreads();
         if (warp == 0) {
             // lane j owns bins 8j .. 8j + 7
             uint64_t bins[8], own = 0;
+            uint32_t cnts[8];
 #pragma unroll
             for (int b = 0; b < 8; ++b) {
                 uint64_t t = 0;
-                for (int w = 0; w < kSelWarps; ++w)
-                    t += hist[w][8 * lane + b];
+                uint32_t c = 0;
+                for (int w = 0; w < kSelWarps; ++w) {
+                    t += sm.hw[w][8 * lane + b];
+                    c += sm.hc[w][8 * lane + b];
+                }
                 bins[b] = t;
+                cnts[b] = c;
                 own += t;
             }
             uint64_t incl = own;   // inclusive scan over lanes
@@ -281,6 +317,14 @@ __device__ uint64_t select_key(const float *__restrict__ row, int vocab, float l
                 const uint64_t o = __shfl_up_sync(0xffffffffu, incl, off);
                 if (lane >= off)
                     incl += o;
+            }
+            if (!COUNT && pass == 0) {
+                // the row total is the sum of every bin: the top-p threshold
+                const uint64_t total = __shfl_sync(0xffffffffu, incl, 31);
+                const uint64_t lo = p_fix * total, hi = __umul64hi(p_fix, total);
+                const uint64_t lo2 = lo + 0xFFFFFFFFull;
+                need = ((hi + (lo2 < lo ? 1ull : 0ull)) << 32) | (lo2 >> 32);
+                need = need ? need : 1ull;   // a zero threshold keeps the first token, as 1 does
             }
             const uint64_t before = incl - own;
             const bool mine = before < need && incl >= need;
@@ -293,17 +337,21 @@ __device__ uint64_t select_key(const float *__restrict__ row, int vocab, float l
                         break;
                     cum += bins[b];
                 }
-                bcast[0] = (prefix << 8) | (uint64_t)(8 * lane + b);
-                bcast[1] = need - cum;
+                sm.bcast[0] = (prefix << 8) | (uint64_t)(8 * lane + b);
+                sm.bcast[1] = need - cum;
+                sm.bcast[2] = cnts[b];
             }
             if (!who && lane == 0) {   // need beyond the total (cannot happen for valid filters)
-                bcast[0] = (prefix << 8) | 255ull;
-                bcast[1] = 1;
+                sm.bcast[0] = (prefix << 8) | 255ull;
+                sm.bcast[1] = 1;
+                sm.bcast[2] = 0;
             }
         }
         __syncthreads();
-        prefix = bcast[0];
-        need = bcast[1];
+        prefix = sm.bcast[0];
+        need = sm.bcast[1];
+        n_cand = (uint32_t)sm.bcast[2];
+        listed = listed || compact;
         __syncthreads();
     }
     return prefix;
@@ -316,9 +364,8 @@ topkp_cut_kernel(const float *__restrict__ logits, int vocab, const float2 *__re
                  float temperature, int top_k, int use_p, unsigned long long p_fix,
                  unsigned long long *__restrict__ cut)
 {
-    __shared__ unsigned long long hist[kSelWarps][256];
-    __shared__ uint64_t bcast[2];
-    __shared__ unsigned long long total_sh;
+    extern __shared__ __align__(16) uint8_t sel_raw[];
+    SelSmem &sm = *reinterpret_cast<SelSmem *>(sel_raw);
     const int r = blockIdx.x;
     const float *row = logits + (size_t)r * vocab;
     float l_max = -INFINITY;
@@ -326,27 +373,9 @@ topkp_cut_kernel(const float *__restrict__ logits, int vocab, const float2 *__re
         l_max = fmaxf(l_max, part_max[(size_t)r * n_chunks + i].x);
     uint64_t c = ~0ull;
     if (top_k > 0 && top_k < vocab)
-        c = select_key<true>(row, vocab, l_max, temperature, (uint64_t)top_k, hist, bcast);
+        c = select_key<true>(row, vocab, l_max, temperature, (uint64_t)top_k, 0ull, sm);
     if (use_p) {
-        if (threadIdx.x == 0)
-            total_sh = 0ull;
-        __syncthreads();
-        unsigned long long t = 0;
-        for (int v = threadIdx.x; v < vocab; v += kSelThreads)
-            t += keyed_weight(__ldg(row + v), l_max, temperature);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-            t += __shfl_xor_sync(0xffffffffu, t, off);
-        if ((threadIdx.x & 31) == 0)
-            atomicAdd(&total_sh, t);
-        __syncthreads();
-        const uint64_t total = total_sh;
-        // ceil(p_fix * total / 2^32) with the 128-bit product
-        const uint64_t lo = p_fix * total, hi = __umul64hi(p_fix, total);
-        const uint64_t lo2 = lo + 0xFFFFFFFFull;
-        uint64_t thr = ((hi + (lo2 < lo ? 1ull : 0ull)) << 32) | (lo2 >> 32);
-        thr = thr ? thr : 1ull;   // a zero threshold keeps the first token, as a threshold of 1 does
-        const uint64_t cp = select_key<false>(row, vocab, l_max, temperature, thr, hist, bcast);
+        const uint64_t cp = select_key<false>(row, vocab, l_max, temperature, 0ull, p_fix, sm);
         c = cp < c ? cp : c;
     }
     if (threadIdx.x == 0)
@@ -644,8 +673,17 @@ extern "C" int spec_accept_sampled(const float *logits, int32_t vocab, const int
             if (use_k || use_p) {
                 cut = reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(workspace) + 2 * one);
                 const unsigned long long p_fix = use_p ? (unsigned long long)(top_p * 4294967296.0f) : 0ull;
-                topkp_cut_kernel<<<total_rows, kSelThreads, 0, st>>>(logits, vocab, part_max, n_chunks, temperature,
-                                                                     use_k ? top_k : 0, use_p ? 1 : 0, p_fix, cut);
+                static std::once_flag once;
+                static cudaError_t attr_err = cudaSuccess;
+                std::call_once(once, [] {
+                    attr_err = cudaFuncSetAttribute(topkp_cut_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                    (int)sizeof(SelSmem));
+                });
+                rc = check_cuda(attr_err, "spec_accept_sampled: shared memory attribute");
+                if (rc)
+                    return rc;
+                topkp_cut_kernel<<<total_rows, kSelThreads, sizeof(SelSmem), st>>>(
+                    logits, vocab, part_max, n_chunks, temperature, use_k ? top_k : 0, use_p ? 1 : 0, p_fix, cut);
                 rc = check_cuda(cudaGetLastError(), "spec_accept_sampled top-k / top-p launch");
                 if (rc)
                     return rc;
