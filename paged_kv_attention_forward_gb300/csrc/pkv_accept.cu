@@ -276,13 +276,10 @@ __device__ uint64_t select_key(const float *__restrict__ row, int vocab, float l
             (&sm.hc[0][0])[i] = 0u;
         }
         __syncthreads();
-        const int n_iter = listed ? (int)sm.n_list : vocab;
-        for (int i = threadIdx.x; i < n_iter; i += kSelThreads) {
-            const float l = listed ? sm.cl[i] : __ldg(row + i);
-            const int v = listed ? sm.cv[i] : i;
+        auto visit = [&](float l, int v) {
             const uint64_t key = order_key(l, v);
             if (pass > 0 && (key >> (shift + 8)) != prefix)
-                continue;
+                return;
             if (compact) {
                 const unsigned int at = atomicAdd(&sm.n_list, 1u);
                 sm.cl[at] = l;
@@ -293,6 +290,36 @@ __device__ uint64_t select_key(const float *__restrict__ row, int vocab, float l
             if (w)
                 atomicAdd(&sm.hw[warp][bin], (unsigned long long)w);
             atomicAdd(&sm.hc[warp][bin], 1u);
+        };
+        if (listed) {
+            const int n = (int)sm.n_list;
+            for (int i = threadIdx.x; i < n; i += kSelThreads)
+                visit(sm.cl[i], sm.cv[i]);
+        } else if ((vocab & 3) == 0) {
+            // the whole row: four 16-byte loads in flight per thread
+            const float4 *row4 = reinterpret_cast<const float4 *>(row);
+            const int n4 = vocab >> 2;
+            for (int i0 = threadIdx.x; i0 < n4; i0 += 4 * kSelThreads) {
+                float4 x[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = i0 + u * kSelThreads;
+                    x[u] = i < n4 ? __ldg(row4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = i0 + u * kSelThreads;
+                    if (i < n4) {
+                        visit(x[u].x, 4 * i);
+                        visit(x[u].y, 4 * i + 1);
+                        visit(x[u].z, 4 * i + 2);
+                        visit(x[u].w, 4 * i + 3);
+                    }
+                }
+            }
+        } else {
+            for (int i = threadIdx.x; i < vocab; i += kSelThreads)
+                visit(__ldg(row + i), i);
         }
         __syncthreads();
         if (warp == 0) {
