@@ -241,65 +241,70 @@ __device__ __forceinline__ uint64_t keyed_weight(float l, float l_max, float tem
 constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelCap = 4096;   // candidates kept in shared memory once they are this few
+constexpr int kSelBins = 16;    // 4-bit digits: every thread keeps its own histogram
+static_assert(kSelWarps == kSelBins, "one warp sums each bin");
 
 struct SelSmem {
-    unsigned long long hw[kSelWarps][256];   // per-warp weight (or count) histograms
-    unsigned int hc[kSelWarps][256];         // per-warp candidate counts
-    float cl[kSelCap];                       // compacted candidates: logit, token
+    unsigned long long hw[kSelBins][kSelThreads];   // per-thread weight histograms
+    unsigned int hc[kSelBins][kSelThreads];         // per-thread candidate counts
+    float cl[kSelCap];                               // compacted candidates: logit, token
     int cv[kSelCap];
+    unsigned long long bw[kSelBins];                 // the pass's totals per bin
+    unsigned int bc[kSelBins];
     uint64_t bcast[3];
     unsigned int n_list;
 };
 
 // Smallest key K with (sum of w_v over key_v <= K) >= need, w_v = the token's weight
-// (or 1 when COUNT).  Eight passes of 8 bits from the top, each a per-warp histogram of
-// the candidates that match the bits found so far; once the candidates are at most
-// kSelCap they are copied to shared memory and later passes read only them.  For the
-// weighted select `need` is derived from the row total, found in pass 0:
-// ceil(p_fix * total / 2^32) (at least 1).  Integer sums make the result independent
-// of the order in which threads add.
+// (or 1 when COUNT).  Sixteen passes of 4 bits from the top; in each, every thread
+// histograms the candidates it visits into its own row of shared memory (no atomics),
+// and the 16 bins are then summed.  Once the candidates are at most kSelCap they are
+// copied to shared memory and later passes read only them.  For the weighted select
+// `need` comes from the row total, found in pass 0: ceil(p_fix * total / 2^32) (at
+// least 1).  Integer sums make the result independent of the order of the adds.
 template <bool COUNT>
 __device__ uint64_t select_key(const float *__restrict__ row, int vocab, float l_max, float temperature,
                                uint64_t need, uint64_t p_fix, SelSmem &sm)
 {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     uint64_t prefix = 0;
     bool listed = false;            // candidates live in sm.cl / sm.cv
     uint32_t n_cand = (uint32_t)vocab;
-    if (threadIdx.x == 0)
+    if (t == 0)
         sm.n_list = 0;
-    for (int pass = 0; pass < 8; ++pass) {
-        const int shift = 56 - 8 * pass;
+    for (int pass = 0; pass < 16; ++pass) {
+        const int shift = 60 - 4 * pass;
         const bool compact = !listed && n_cand <= (uint32_t)kSelCap;
-        for (int i = threadIdx.x; i < kSelWarps * 256; i += kSelThreads) {
-            (&sm.hw[0][0])[i] = 0ull;
-            (&sm.hc[0][0])[i] = 0u;
+#pragma unroll
+        for (int b = 0; b < kSelBins; ++b) {
+            if (!COUNT)
+                sm.hw[b][t] = 0ull;
+            sm.hc[b][t] = 0u;
         }
         __syncthreads();
         auto visit = [&](float l, int v) {
             const uint64_t key = order_key(l, v);
-            if (pass > 0 && (key >> (shift + 8)) != prefix)
+            if (pass > 0 && (key >> (shift + 4)) != prefix)
                 return;
             if (compact) {
                 const unsigned int at = atomicAdd(&sm.n_list, 1u);
                 sm.cl[at] = l;
                 sm.cv[at] = v;
             }
-            const uint64_t w = COUNT ? 1ull : keyed_weight(l, l_max, temperature);
-            const int bin = (int)((key >> shift) & 255);
-            if (w)
-                atomicAdd(&sm.hw[warp][bin], (unsigned long long)w);
-            atomicAdd(&sm.hc[warp][bin], 1u);
+            const int bin = (int)((key >> shift) & 15);
+            if (!COUNT)
+                sm.hw[bin][t] += keyed_weight(l, l_max, temperature);
+            sm.hc[bin][t] += 1u;
         };
         if (listed) {
             const int n = (int)sm.n_list;
-            for (int i = threadIdx.x; i < n; i += kSelThreads)
+            for (int i = t; i < n; i += kSelThreads)
                 visit(sm.cl[i], sm.cv[i]);
         } else if ((vocab & 3) == 0) {
             // the whole row: four 16-byte loads in flight per thread
             const float4 *row4 = reinterpret_cast<const float4 *>(row);
             const int n4 = vocab >> 2;
-            for (int i0 = threadIdx.x; i0 < n4; i0 += 4 * kSelThreads) {
+            for (int i0 = t; i0 < n4; i0 += 4 * kSelThreads) {
                 float4 x[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
@@ -318,61 +323,51 @@ __device__ uint64_t select_key(const float *__restrict__ row, int vocab, float l
                 }
             }
         } else {
-            for (int i = threadIdx.x; i < vocab; i += kSelThreads)
+            for (int i = t; i < vocab; i += kSelThreads)
                 visit(__ldg(row + i), i);
         }
         __syncthreads();
-        if (warp == 0) {
-            // lane j owns bins 8j .. 8j + 7
-            uint64_t bins[8], own = 0;
-            uint32_t cnts[8];
-#pragma unroll
-            for (int b = 0; b < 8; ++b) {
-                uint64_t t = 0;
-                uint32_t c = 0;
-                for (int w = 0; w < kSelWarps; ++w) {
-                    t += sm.hw[w][8 * lane + b];
-                    c += sm.hc[w][8 * lane + b];
-                }
-                bins[b] = t;
-                cnts[b] = c;
-                own += t;
+        // warp w sums bin w over the threads (kSelWarps == kSelBins)
+        {
+            unsigned long long sw = 0;
+            unsigned int sc = 0;
+            for (int i = lane; i < kSelThreads; i += 32) {
+                if (!COUNT)
+                    sw += sm.hw[warp][i];
+                sc += sm.hc[warp][i];
             }
-            uint64_t incl = own;   // inclusive scan over lanes
 #pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const uint64_t o = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off)
-                    incl += o;
+            for (int off = 16; off > 0; off >>= 1) {
+                sw += __shfl_xor_sync(0xffffffffu, sw, off);
+                sc += __shfl_xor_sync(0xffffffffu, sc, off);
             }
+            if (lane == 0) {
+                sm.bw[warp] = COUNT ? (unsigned long long)sc : sw;
+                sm.bc[warp] = sc;
+            }
+        }
+        __syncthreads();
+        if (t == 0) {
             if (!COUNT && pass == 0) {
                 // the row total is the sum of every bin: the top-p threshold
-                const uint64_t total = __shfl_sync(0xffffffffu, incl, 31);
+                uint64_t total = 0;
+                for (int b = 0; b < kSelBins; ++b)
+                    total += sm.bw[b];
                 const uint64_t lo = p_fix * total, hi = __umul64hi(p_fix, total);
                 const uint64_t lo2 = lo + 0xFFFFFFFFull;
                 need = ((hi + (lo2 < lo ? 1ull : 0ull)) << 32) | (lo2 >> 32);
                 need = need ? need : 1ull;   // a zero threshold keeps the first token, as 1 does
             }
-            const uint64_t before = incl - own;
-            const bool mine = before < need && incl >= need;
-            const unsigned who = __ballot_sync(0xffffffffu, mine);
-            if (mine && lane == __ffs(who) - 1) {
-                uint64_t cum = before;
-                int b = 0;
-                for (; b < 7; ++b) {
-                    if (cum + bins[b] >= need)
-                        break;
-                    cum += bins[b];
-                }
-                sm.bcast[0] = (prefix << 8) | (uint64_t)(8 * lane + b);
-                sm.bcast[1] = need - cum;
-                sm.bcast[2] = cnts[b];
+            uint64_t cum = 0;
+            int b = 0;
+            for (; b < kSelBins - 1; ++b) {
+                if (cum + sm.bw[b] >= need)
+                    break;
+                cum += sm.bw[b];
             }
-            if (!who && lane == 0) {   // need beyond the total (cannot happen for valid filters)
-                sm.bcast[0] = (prefix << 8) | 255ull;
-                sm.bcast[1] = 1;
-                sm.bcast[2] = 0;
-            }
+            sm.bcast[0] = (prefix << 4) | (uint64_t)b;
+            sm.bcast[1] = need - cum;
+            sm.bcast[2] = sm.bc[b];
         }
         __syncthreads();
         prefix = sm.bcast[0];
