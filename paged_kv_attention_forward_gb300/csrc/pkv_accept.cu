@@ -238,17 +238,19 @@ __device__ __forceinline__ uint64_t keyed_weight(float l, float l_max, float tem
     return __float2ull_rz(__fmul_rn(keyed_exp2(y), 4294967296.0f));
 }
 
-constexpr int kSelThreads = 512;
+constexpr int kSelThreads = 1024;
 constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kSelCap = 4096;   // candidates kept in shared memory once they are this few
+constexpr int kSelCap = 2048;   // candidates kept in shared memory once they are this few
 constexpr int kSelBins = 16;    // 4-bit digits: every thread keeps its own histogram
-static_assert(kSelWarps == kSelBins, "one warp sums each bin");
+static_assert(kSelWarps % kSelBins == 0, "whole warps sum each bin");
 
 struct SelSmem {
     unsigned long long hw[kSelBins][kSelThreads];   // per-thread weight histograms
     unsigned int hc[kSelBins][kSelThreads];         // per-thread candidate counts
     float cl[kSelCap];                               // compacted candidates: logit, token
     int cv[kSelCap];
+    unsigned long long pw[kSelWarps];                // per-warp shares of the bin sums
+    unsigned int pc[kSelWarps];
     unsigned long long bw[kSelBins];                 // the pass's totals per bin
     unsigned int bc[kSelBins];
     uint64_t bcast[3];
@@ -262,15 +264,17 @@ struct SelSmem {
 // copied to shared memory and later passes read only them.  For the weighted select
 // `need` comes from the row total, found in pass 0: ceil(p_fix * total / 2^32) (at
 // least 1).  Integer sums make the result independent of the order of the adds.
+// prelisted: the candidates are already in sm.cl / sm.cv and `need` is final.
 template <bool COUNT>
 __device__ uint64_t select_key(const float *__restrict__ row, int vocab, float l_max, float temperature,
-                               uint64_t need, uint64_t p_fix, SelSmem &sm)
+                               uint64_t need, uint64_t p_fix, SelSmem &sm, bool prelisted = false)
 {
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     uint64_t prefix = 0;
-    bool listed = false;            // candidates live in sm.cl / sm.cv
-    uint32_t n_cand = (uint32_t)vocab;
-    if (t == 0)
+    bool listed = prelisted;        // candidates live in sm.cl / sm.cv
+    uint32_t n_cand = prelisted ? sm.n_list : (uint32_t)vocab;
+    __syncthreads();
+    if (t == 0 && !prelisted)
         sm.n_list = 0;
     for (int pass = 0; pass < 16; ++pass) {
         const int shift = 60 - 4 * pass;
@@ -327,14 +331,16 @@ __device__ uint64_t select_key(const float *__restrict__ row, int vocab, float l
                 visit(__ldg(row + i), i);
         }
         __syncthreads();
-        // warp w sums bin w over the threads (kSelWarps == kSelBins)
+        // the warps of group w sum bin w over the threads, each warp a share of them
         {
+            constexpr int kPer = kSelWarps / kSelBins;
+            const int bin = warp / kPer, part = warp % kPer;
             unsigned long long sw = 0;
             unsigned int sc = 0;
-            for (int i = lane; i < kSelThreads; i += 32) {
+            for (int i = part * 32 + lane; i < kSelThreads; i += 32 * kPer) {
                 if (!COUNT)
-                    sw += sm.hw[warp][i];
-                sc += sm.hc[warp][i];
+                    sw += sm.hw[bin][i];
+                sc += sm.hc[bin][i];
             }
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) {
@@ -342,13 +348,25 @@ __device__ uint64_t select_key(const float *__restrict__ row, int vocab, float l
                 sc += __shfl_xor_sync(0xffffffffu, sc, off);
             }
             if (lane == 0) {
-                sm.bw[warp] = COUNT ? (unsigned long long)sc : sw;
-                sm.bc[warp] = sc;
+                sm.pw[warp] = COUNT ? (unsigned long long)sc : sw;
+                sm.pc[warp] = sc;
             }
         }
         __syncthreads();
+        if (t < kSelBins) {
+            constexpr int kPer = kSelWarps / kSelBins;
+            unsigned long long sw = 0;
+            unsigned int sc = 0;
+            for (int q = 0; q < kPer; ++q) {
+                sw += sm.pw[t * kPer + q];
+                sc += sm.pc[t * kPer + q];
+            }
+            sm.bw[t] = sw;
+            sm.bc[t] = sc;
+        }
+        __syncthreads();
         if (t == 0) {
-            if (!COUNT && pass == 0) {
+            if (!COUNT && pass == 0 && !prelisted) {
                 // the row total is the sum of every bin: the top-p threshold
                 uint64_t total = 0;
                 for (int b = 0; b < kSelBins; ++b)
@@ -396,7 +414,49 @@ topkp_cut_kernel(const float *__restrict__ logits, int vocab, const float2 *__re
     uint64_t c = ~0ull;
     if (top_k > 0 && top_k < vocab)
         c = select_key<true>(row, vocab, l_max, temperature, (uint64_t)top_k, 0ull, sm);
-    if (use_p) {
+    if (use_p && top_k > 0 && top_k <= kSelCap && c != ~0ull) {
+        // top-p can only cut inside the k kept tokens: one scan for the row total and those
+        // tokens, then the weighted select over them alone
+        __shared__ unsigned long long tot_sh, kept_sh;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            tot_sh = 0ull;
+            kept_sh = 0ull;
+            sm.n_list = 0;
+        }
+        __syncthreads();
+        unsigned long long tot = 0, kept = 0;
+        for (int v = threadIdx.x; v < vocab; v += kSelThreads) {
+            const float l = __ldg(row + v);
+            const uint64_t w = keyed_weight(l, l_max, temperature);
+            tot += w;
+            if (order_key(l, v) <= c) {
+                kept += w;
+                const unsigned int at = atomicAdd(&sm.n_list, 1u);
+                sm.cl[at] = l;
+                sm.cv[at] = v;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            tot += __shfl_xor_sync(0xffffffffu, tot, off);
+            kept += __shfl_xor_sync(0xffffffffu, kept, off);
+        }
+        if ((threadIdx.x & 31) == 0) {
+            atomicAdd(&tot_sh, tot);
+            atomicAdd(&kept_sh, kept);
+        }
+        __syncthreads();
+        const uint64_t total = tot_sh;
+        const uint64_t lo = p_fix * total, hi = __umul64hi(p_fix, total);
+        const uint64_t lo2 = lo + 0xFFFFFFFFull;
+        uint64_t need = ((hi + (lo2 < lo ? 1ull : 0ull)) << 32) | (lo2 >> 32);
+        need = need ? need : 1ull;
+        if (need <= (uint64_t)kept_sh) {   // else top-p keeps all k tokens
+            const uint64_t cp = select_key<false>(row, vocab, l_max, temperature, need, p_fix, sm, true);
+            c = cp < c ? cp : c;
+        }
+    } else if (use_p) {
         const uint64_t cp = select_key<false>(row, vocab, l_max, temperature, 0ull, p_fix, sm);
         c = cp < c ? cp : c;
     }
