@@ -73,6 +73,9 @@ def _load():
             lib.oracle_keyed_log.restype = ctypes.c_float
             lib.oracle_spec_accept_sampled.argtypes = [P, i32, P, P, P, P, ctypes.c_uint64, ctypes.c_float,
                                                        i32, ctypes.c_float, ctypes.c_float, i32, P, P, P, P]
+            lib.oracle_paged_attention_sparse.argtypes = [P, P, i32, i32, i32, i32, P, P, P, i32, P, i32, P, P,
+                                                          i32, i32, P, P, ctypes.c_double, P]
+            lib.oracle_paged_attention_sparse.restype = ctypes.c_int
             lib.oracle_keyed_exp2.argtypes = [ctypes.c_float]
             lib.oracle_keyed_exp2.restype = ctypes.c_float
             lib.oracle_topkp_kept.argtypes = [P, i32, ctypes.c_float, i32, ctypes.c_float, P]
@@ -383,4 +386,32 @@ def paged_attention_quant(records, block_size, head_dim, bits, q, q_starts, bloc
         float(scale), _ptr(out), int(num_threads or default_num_threads()))
     if rc != 0:
         raise ValueError(f"oracle_paged_attention_quant failed with status {rc}")
+    return out
+
+
+def paged_attention_sparse(k_pool, v_pool, q, q_starts, block_tables, context_lens, key_idx, key_counts,
+                           kv_head_of_q_head=None, sinks=None, scale=None):
+    """Attention of every row over its own list of key positions: float64 [R, H_q, D].
+
+    key_idx int32 [R, max_keys] (positions within the row's sequence), key_counts int32 [R]."""
+    lib = _load()
+    nb, hkv, bs, d = k_pool.shape
+    q = _c(q, np.uint16)
+    r, hq, dq = q.shape
+    assert dq == d
+    bt = _c(block_tables, np.int32)
+    ki = _c(key_idx, np.int32)
+    kc = _c(key_counts, np.int32)
+    hm = None if kv_head_of_q_head is None else _c(kv_head_of_q_head, np.int32)
+    sk = None if sinks is None else _c(sinks, np.float32)
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    out = np.zeros((r, hq, d), dtype=np.float64)
+    rc = lib.oracle_paged_attention_sparse(
+        _ptr(_c(k_pool, np.uint16)), _ptr(_c(v_pool, np.uint16)), nb, bs, hkv, d, _ptr(q),
+        _ptr(_c(q_starts, np.int32)), _ptr(bt), bt.shape[1], _ptr(_c(context_lens, np.int32)),
+        len(context_lens), _ptr(ki), _ptr(kc), ki.shape[1] if ki.ndim == 2 else 0, hq, _ptr(hm), _ptr(sk),
+        float(scale), _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle_paged_attention_sparse failed with status {rc}")
     return out

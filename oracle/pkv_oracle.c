@@ -988,3 +988,118 @@ int oracle_paged_attention_quant(const uint8_t *records, int32_t bits,
                           block_tables, max_blocks_per_seq, context_lens, num_seqs, num_q_heads,
                           kv_head_of_q_head, sinks, causal, tree_masks, scale, out, num_threads);
 }
+
+/* ------------------------------------------------- index-list (sparse) gather -- */
+/*
+ * Attention over an explicit list of key positions (TensorSharp "高级功能", the
+ * DeepSeek V4 executor item: decode attention takes a compact [ring | top-512]
+ * set of keys through a fused index-gather instead of scanning the whole
+ * context).  Query row r of sequence s, q head h (KV head g = map[h]) attends to
+ * the keys at positions key_idx[r][0 .. key_counts[r]-1] of s, each read through
+ * the block table (block_tables[s][t / B], slot t % B):
+ *   x_j = scale * q[r][h] . K_s[key_idx[r][j]][g]
+ *   out = sum_j e^{x_j - M} V_s[key_idx[r][j]][g] / (sum_j e^{x_j - M} + e^{sink_h - M})
+ * over j in list order (a position listed twice counts twice); M = max(x_j, sink_h).
+ * No causal mask: the list says what the row sees.  key_idx is int32
+ * [R][max_keys]; rows of s are q_starts[s] .. q_starts[s+1]-1.  Every position must
+ * lie in [0, context_lens[s]).  Returns 0, -1 (a position outside [0, L) or past
+ * the table), -2 (block id out of range), -3 (bad head map), -4 (out of memory),
+ * -6 (a count outside [0, max_keys]).
+ */
+int oracle_paged_attention_sparse(const uint16_t *k_pool, const uint16_t *v_pool,
+                                  int32_t num_blocks, int32_t block_size,
+                                  int32_t num_kv_heads, int32_t head_dim,
+                                  const uint16_t *q, const int32_t *q_starts,
+                                  const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t *context_lens, int32_t num_seqs,
+                                  const int32_t *key_idx, const int32_t *key_counts, int32_t max_keys,
+                                  int32_t num_q_heads, const int32_t *kv_head_of_q_head,
+                                  const float *sinks, double scale, double *out)
+{
+    const int32_t B = block_size, D = head_dim, Hkv = num_kv_heads, Hq = num_q_heads;
+    if (Hkv <= 0 || Hq % Hkv != 0)
+        return -3;
+    const int32_t group = Hq / Hkv;
+    for (int32_t h = 0; h < Hq; ++h) {
+        const int32_t g = kv_head_of_q_head ? kv_head_of_q_head[h] : h / group;
+        if (g < 0 || g >= Hkv)
+            return -3;
+    }
+    double *K = (double *)malloc(sizeof(double) * (size_t)(max_keys > 0 ? max_keys : 1) * D);
+    double *V = (double *)malloc(sizeof(double) * (size_t)(max_keys > 0 ? max_keys : 1) * D);
+    double *x = (double *)malloc(sizeof(double) * (size_t)(max_keys > 0 ? max_keys : 1));
+    if (!K || !V || !x) {
+        free(K); free(V); free(x);
+        return -4;
+    }
+    int rc = 0;
+    for (int32_t s = 0; s < num_seqs && rc == 0; ++s) {
+        const int64_t L = context_lens[s];
+        for (int64_t r = q_starts[s]; r < q_starts[s + 1] && rc == 0; ++r) {
+            const int32_t n = key_counts[r];
+            if (n < 0 || n > max_keys) {
+                rc = -6;
+                break;
+            }
+            for (int32_t g = 0; g < Hkv && rc == 0; ++g) {
+                /* gather this row's keys for KV head g */
+                for (int32_t j = 0; j < n; ++j) {
+                    const int64_t t = key_idx[r * (int64_t)max_keys + j];
+                    if (t < 0 || t >= L || t / B >= max_blocks_per_seq) {
+                        rc = -1;
+                        break;
+                    }
+                    const int32_t blk = block_tables[(int64_t)s * max_blocks_per_seq + t / B];
+                    if (blk < 0 || blk >= num_blocks) {
+                        rc = -2;
+                        break;
+                    }
+                    const size_t base = ((((size_t)blk * Hkv) + g) * B + (size_t)(t % B)) * D;
+                    for (int32_t i = 0; i < D; ++i) {
+                        K[(size_t)j * D + i] = bf16_bits_to_f64(k_pool[base + i]);
+                        V[(size_t)j * D + i] = bf16_bits_to_f64(v_pool[base + i]);
+                    }
+                }
+                if (rc)
+                    break;
+                for (int32_t h = 0; h < Hq; ++h) {
+                    const int32_t gh = kv_head_of_q_head ? kv_head_of_q_head[h] : h / group;
+                    if (gh != g)
+                        continue;
+                    const uint16_t *qv = q + ((size_t)r * Hq + h) * D;
+                    double *o = out + ((size_t)r * Hq + h) * D;
+                    double M = -INFINITY;
+                    for (int32_t j = 0; j < n; ++j) {
+                        double dot = 0.0;
+                        for (int32_t i = 0; i < D; ++i)
+                            dot += bf16_bits_to_f64(qv[i]) * K[(size_t)j * D + i];
+                        x[j] = scale * dot;
+                        if (x[j] > M)
+                            M = x[j];
+                    }
+                    const int has_sink = sinks != NULL;
+                    const double sink = has_sink ? (double)sinks[h] : 0.0;
+                    if (has_sink && sink > M)
+                        M = sink;
+                    double den = 0.0;
+                    for (int32_t i = 0; i < D; ++i)
+                        o[i] = 0.0;
+                    for (int32_t j = 0; j < n; ++j) {
+                        const double e = exp(x[j] - M);
+                        den += e;
+                        for (int32_t i = 0; i < D; ++i)
+                            o[i] += e * V[(size_t)j * D + i];
+                    }
+                    if (has_sink)
+                        den += exp(sink - M);
+                    for (int32_t i = 0; i < D; ++i)
+                        o[i] = den > 0.0 ? o[i] / den : 0.0;
+                }
+            }
+        }
+    }
+    free(K);
+    free(V);
+    free(x);
+    return rc;
+}

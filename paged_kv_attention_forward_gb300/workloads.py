@@ -152,6 +152,8 @@ class PagedBatch:
     parents: Optional[np.ndarray] = None       # int32 [R]: draft-tree parent node of each row (-1 at roots)
     tree_masks: Optional[np.ndarray] = None    # uint32 [R]: bit i = the row sees window token i
     shared_prefix: int = 0                     # tokens the sharing sequences have in common
+    key_idx: Optional[np.ndarray] = None       # int32 [sets, R, max_keys]: per-row key positions (-1 pad)
+    key_counts: Optional[np.ndarray] = None    # int32 [sets, R]
 
     @property
     def num_seqs(self) -> int:
@@ -343,11 +345,43 @@ def add_draft_trees(batch: PagedBatch, seed, vocab: int, std: float = 2.0, hit_p
     return batch
 
 
+def add_key_lists(batch: PagedBatch, seed, ring: int = 128, top: int = 512, sets: int = 1) -> PagedBatch:
+    """Per-row key lists for the index-list gather: the row's last `ring` cached keys
+    followed by `top` distinct positions drawn uniformly from the keys before them (in
+    random order, as an indexer's top-k would arrive), padded with -1.  `sets`
+    independent list sets let a benchmark change the lists every step."""
+    rng = np.random.Generator(np.random.PCG64(_seed_seq(seed)))
+    R = batch.total_q_rows
+    width = ring + top
+    idx = np.full((sets, R, width), -1, dtype=np.int32)
+    cnt = np.zeros((sets, R), dtype=np.int32)
+    row_seq = np.searchsorted(batch.q_starts, np.arange(R), side="right") - 1
+    W = np.diff(batch.q_starts)
+    for k in range(sets):
+        for r in range(R):
+            s = row_seq[r]
+            # the keys row r may see: up to its own position in a causal window
+            L = int(batch.context_lens[s] - W[s] + (r - batch.q_starts[s]) + 1) if batch.causal \
+                else int(batch.context_lens[s])
+            nr = min(ring, L)
+            recent = np.arange(L - nr, L, dtype=np.int32)
+            pool = L - nr
+            nt = min(top, pool)
+            older = rng.choice(pool, size=nt, replace=False).astype(np.int32) if nt > 0 else np.zeros(0, np.int32)
+            lst = np.concatenate([recent, older])
+            idx[k, r, :len(lst)] = lst
+            cnt[k, r] = len(lst)
+    batch.key_idx = idx
+    batch.key_counts = cnt
+    return batch
+
+
 def _loguniform_int(rng, lo, hi, size):
     return np.rint(np.exp(rng.uniform(math.log(lo), math.log(hi), size=size))).astype(np.int64)
 
 
-WORKLOADS = ("tiny_decode", "ministral_decode", "cb_mix", "spec_verify", "sinks_scale", "spec_tree")
+WORKLOADS = ("tiny_decode", "ministral_decode", "cb_mix", "spec_verify", "sinks_scale", "spec_tree",
+             "sparse_gather")
 VOCAB = 151936
 
 
@@ -383,6 +417,19 @@ def make_workload(name: str, seed: int = 0, filler: str = "random", layers: Opti
                            q_rows=np.ones(S, np.int64), num_q_heads=40, num_kv_heads=8,
                            head_dim=128, block_size=16, causal=False, filler=filler,
                            shared_prefix=prefix, sharing=sharing)
+    if name == "sparse_gather":
+        # cb_mix's sequences, each decode row reading [its last 128 keys | 512 older keys]
+        S = num_seqs or 64
+        n_share, prefix = (3 * S) // 4, 2900
+        sharing = np.zeros(S, dtype=bool)
+        sharing[rng.permutation(S)[:n_share]] = True
+        old = np.where(sharing, _loguniform_int(rng, prefix + 1, 32767, S),
+                       _loguniform_int(rng, 128, 32767, S))
+        b = build_batch(s_batch, name=name, lens=old + 1, n_new=np.ones(S, np.int64),
+                        q_rows=np.ones(S, np.int64), num_q_heads=40, num_kv_heads=8,
+                        head_dim=128, block_size=16, causal=False, filler=filler,
+                        shared_prefix=prefix, sharing=sharing)
+        return add_key_lists(b, s_extra, ring=128, top=512, sets=4)
     if name == "spec_verify":
         S = num_seqs or 16
         lens = rng.integers(4096, 32769, size=S)
@@ -505,4 +552,7 @@ def select_seqs(batch: PagedBatch, seqs) -> PagedBatch:
     if batch.parents is not None:
         sub.parents = batch.parents[q_idx].copy()
         sub.tree_masks = batch.tree_masks[q_idx].copy()
+    if batch.key_idx is not None:
+        sub.key_idx = np.ascontiguousarray(batch.key_idx[:, q_idx])
+        sub.key_counts = np.ascontiguousarray(batch.key_counts[:, q_idx])
     return sub
