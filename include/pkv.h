@@ -358,6 +358,33 @@ int paged_block_hashes(const int32_t *tokens, const int32_t *token_starts, int32
                        int32_t max_blocks_per_seq, void *stream);
 
 /*
+ * Index-list gather (TensorSharp "高级功能", the DeepSeek V4 executor item: decode
+ * attention reads a compact [ring | top-k] set of keys through an index-gather
+ * instead of the whole context).  Query row r of sequence s attends to the keys
+ * at positions key_idx[r][0 .. key_counts[r]-1] of s, read through the block
+ * table; a position listed twice counts twice; there is no causal mask (the list
+ * says what the row sees); sinks as in paged_attention_forward.
+ *   key_idx     int32 [total_q_rows][max_keys] (device); entries past a row's
+ *               count are not read
+ *   key_counts  int32 [total_q_rows] (device), each in [0, max_keys]
+ *   max_keys    at most max_blocks_per_seq * block_size
+ * A listed position outside [0, context_lens[s]) contributes a zero key and value
+ * and sets PKV_DEV_TABLE_OVERRUN (the row's output is then not meaningful); a
+ * count outside [0, max_keys] is clamped and sets the same bit.  Workspace:
+ * paged_attention_workspace_size(num_seqs, total_q_rows, num_q_heads,
+ * num_kv_heads, head_dim, max_keys).  Within a row the arithmetic depends only
+ * on its own list, so a row computed in a batch equals the row alone.  Launches
+ * two kernels.
+ */
+int paged_attention_forward_gather(const pkv_pool *pool, const void *q, const int32_t *q_starts,
+                                   const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t *context_lens, int32_t num_seqs, int32_t total_q_rows,
+                                   const int32_t *key_idx, const int32_t *key_counts, int32_t max_keys,
+                                   int32_t num_q_heads, const int32_t *kv_head_of_q_head,
+                                   const float *sinks, float scale, void *out, int32_t out_dtype,
+                                   void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Quantised KV blocks (TensorSharp "高级功能", section "内存优化", the KV block
  * codec item: blocks may be compressed in place to 8 or 4 bits per value, Q8 /
  * Q4, for half or a quarter of the footprint at a small accuracy cost).  The

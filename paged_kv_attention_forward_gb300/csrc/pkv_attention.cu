@@ -74,6 +74,32 @@ int launch_bf16(const PoolView &pv, AttnParams &prm, int rows, long long pairs, 
     return launch_d_bs<128, 32, 16, true>(rows, mk, mv, prm, pairs, n_max, st);
 }
 
+// Index-list gather: one unit per (query row, KV head); the grid's second dimension
+// runs over 512-entry slices of the longest list.
+template <int D>
+int launch_gather_d(int rows, AttnParams prm, long long pairs, int n_max, cudaStream_t st)
+{
+    CUtensorMap none;   // the gather copies rows with cp.async, not tensor maps
+    memset(&none, 0, sizeof none);
+    const int per_cta = rows <= 8 ? 8 : 8 * PKV_WIDE_NN * PKV_WIDE_NMT;
+    prm.row_groups = (rows + per_cta - 1) / per_cta;
+    const long long gx = pairs * prm.row_groups;
+    if (gx > 0x7fffffffLL || n_max > 65535)
+        return set_error(PKV_ERR_SHAPE, "paged_attention_forward_gather: grid too large");
+    const dim3 grid((unsigned)gx, (unsigned)n_max);
+    if (rows <= 8)
+        return launch_t<D, 16, 1, 1, false, 16, true>(none, none, prm, grid, st);
+    return launch_t<D, 16, PKV_WIDE_NN, PKV_WIDE_NMT, false, 16, true>(none, none, prm, grid, st);
+}
+
+int launch_gather(const PoolView &pv, AttnParams &prm, int rows, long long /*pairs*/, int n_max, cudaStream_t st)
+{
+    const long long pairs = (long long)prm.total_rows * pv.num_kv_heads;
+    if (pv.head_dim == 64)
+        return launch_gather_d<64>(rows, prm, pairs, n_max, st);
+    return launch_gather_d<128>(rows, prm, pairs, n_max, st);
+}
+
 int attention_impl(const char *who, const pkv_pool *pool, const void *q, const int32_t *q_starts,
                    const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
                    int32_t num_seqs, int32_t total_q_rows, int32_t max_context_len,
@@ -228,4 +254,33 @@ extern "C" int paged_attention_forward_noalloc(const pkv_pool *pool, const void 
                                    total_q_rows, max_context_len, max_q_rows_per_seq, num_q_heads,
                                    kv_head_of_q_head, sinks, causal, scale, out, out_dtype, scratch,
                                    (size_t)PKV_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+extern "C" int paged_attention_forward_gather(const pkv_pool *pool, const void *q, const int32_t *q_starts,
+                                              const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                              const int32_t *context_lens, int32_t num_seqs, int32_t total_q_rows,
+                                              const int32_t *key_idx, const int32_t *key_counts, int32_t max_keys,
+                                              int32_t num_q_heads, const int32_t *kv_head_of_q_head,
+                                              const float *sinks, float scale, void *out, int32_t out_dtype,
+                                              void *workspace, size_t workspace_bytes, void *stream)
+{
+    using namespace pkv;
+    clear_error();
+    const char *who = "paged_attention_forward_gather";
+    if (!pool)
+        return set_error(PKV_ERR_NULL, "%s: pool is NULL", who);
+    if (max_keys < 0)
+        return set_error(PKV_ERR_SHAPE, "%s: max_keys %d is negative", who, max_keys);
+    if (num_seqs > 0 && total_q_rows > 0 && max_keys > 0 && (!key_idx || !key_counts))
+        return set_error(PKV_ERR_NULL, "%s: key_idx and key_counts are required", who);
+    if (num_seqs > 0 && total_q_rows > 0 && max_keys == 0)
+        return set_error(PKV_ERR_SHAPE, "%s: max_keys must be positive", who);
+    PoolView pv = {pool->num_blocks, pool->block_size, pool->num_kv_heads, pool->head_dim, 16,
+                   pool->k_pool, pool->v_pool, nullptr};
+    pv.key_idx = key_idx;
+    pv.key_counts = key_counts;
+    pv.max_keys = max_keys;
+    return attention_run(who, pv, q, q_starts, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                         total_q_rows, max_keys, 1, num_q_heads, kv_head_of_q_head, sinks, 0, nullptr, scale, out,
+                         out_dtype, workspace, workspace_bytes, stream, launch_gather);
 }

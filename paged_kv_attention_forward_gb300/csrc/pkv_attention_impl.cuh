@@ -71,6 +71,10 @@ struct AttnParams {
     float2 *part_ml;              // [R*Hq*n_max] (m in log2 units, l)
     float *part_o;                // [R*Hq*n_max][D]
     const uint8_t *qrec;          // quantised pool: records [num_blocks][H_kv][QRec::kBytes], or null
+    const uint16_t *kpool, *vpool;   // bf16 pools, read by the index-list gather
+    const int32_t *key_idx;       // [R][max_keys] key positions of each row (index-list gather), or null
+    const int32_t *key_counts;    // [R]
+    int32_t max_keys;
     int32_t *status;
     int32_t num_seqs, max_blocks_per_seq, num_blocks, num_q_heads, num_kv_heads, group, block_size;
     int32_t n_max, max_context_len, max_rows, total_rows;
@@ -175,11 +179,15 @@ __device__ __forceinline__ void q_frag(const uint4 *un, int ks, uint32_t (&a)[4]
 // KW states are merged in kw order at the end.  KW depends only on the codec, and
 // which warp sees which key only on the key's position, so a row's arithmetic is
 // still fixed by its own sequence, whatever the CTA shape.
-template <int D, int BS, int NN, int NMT, int NST, bool TREE, int BITS, int KW>
+// GATHER: the index-list gather.  The work unit is (query row, KV head); its keys are
+// the row's list entries, 16 per stage, each row fetched through the block table with
+// 16-byte cp.async copies into the same swizzled tile layout the TMA path fills.
+template <int D, int BS, int NN, int NMT, int NST, bool TREE, int BITS, int KW, bool GATHER = false>
 __global__ void __launch_bounds__((NMT * KW + 1) * 32)
 paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const AttnParams p)
 {
+    static_assert(!GATHER || (BITS == 16 && !TREE && KW == 1 && BS == 16), "index-list gather: bf16, 16-key tiles");
     static_assert(!(TREE && BITS != 16), "tree masks are built for bf16 pools only");
     // Every use of a stage must belong to one key-share warp: stage st holds blocks
     // st, st + NST, ..., all of share st % KW only when KW divides NST.  Otherwise a
@@ -213,20 +221,40 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    int L = __ldg(p.context_lens + s);
-    const int L_cap = (int)min((long long)p.max_context_len, (long long)p.max_blocks_per_seq * BS);
-    if (L > L_cap || L < 0) {
-        if (split == 0 && threadIdx.x == 0)
-            atomicOr(p.status, PKV_DEV_TABLE_OVERRUN);
-        L = L < 0 ? 0 : L_cap;
+    int L;        // keys of the unit: the context length, or (gather) the row's list length
+    int seq = s;  // (gather) the sequence of query row s
+    if constexpr (GATHER) {
+        int lo = 0, hi = p.num_seqs - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(p.q_starts + mid) <= s)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        seq = lo;
+        L = s < p.total_rows ? __ldg(p.key_counts + s) : 0;
+        if (L > p.max_keys || L < 0) {
+            if (split == 0 && threadIdx.x == 0)
+                atomicOr(p.status, PKV_DEV_TABLE_OVERRUN);
+            L = L < 0 ? 0 : p.max_keys;
+        }
+    } else {
+        L = __ldg(p.context_lens + s);
+        const int L_cap = (int)min((long long)p.max_context_len, (long long)p.max_blocks_per_seq * BS);
+        if (L > L_cap || L < 0) {
+            if (split == 0 && threadIdx.x == 0)
+                atomicOr(p.status, PKV_DEV_TABLE_OVERRUN);
+            L = L < 0 ? 0 : L_cap;
+        }
     }
     // the dependent merge kernel may be scheduled once every CTA of this grid has started
     asm volatile("griddepcontrol.launch_dependents;");
     const int n_splits = (L + C - 1) / C;
     if (split >= n_splits)
         return;
-    const int row0 = __ldg(p.q_starts + s);
-    int W = __ldg(p.q_starts + s + 1) - row0;
+    const int row0 = GATHER ? s : __ldg(p.q_starts + s);
+    int W = GATHER ? 1 : __ldg(p.q_starts + s + 1) - row0;
     if (W <= 0)
         return;
     if (row0 < 0 || row0 + W > p.total_rows) {   // q_starts inconsistent with total_q_rows
@@ -252,7 +280,7 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NST; ++i) {
-            mbar_init(&full[i], 1);
+            mbar_init(&full[i], GATHER ? 32 : 1);   // gather: every producer lane arrives
             mbar_init(&empty[i], n_act);
         }
         mbar_fence_init();
@@ -261,7 +289,66 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
     }
     __syncthreads();
 
-    if (warp == NMT * KW) {
+    if (GATHER && warp == NMT * KW) {
+        // ---------------- producer warp (gather): list -> block table -> cp.async ----------------
+        constexpr int CH = D / 8;             // 16-byte chunks per key row
+        constexpr int KSTEP = 32 / CH;        // keys a lane steps over
+        constexpr int KPL = 16 / KSTEP;       // keys per lane per tile
+        const int ch = lane % CH, kq = lane / CH;
+        const long long ctx_cap = (long long)p.max_blocks_per_seq * p.block_size;
+        long long ctx = __ldg(p.context_lens + seq);
+        ctx = ctx < 0 ? 0 : (ctx > ctx_cap ? ctx_cap : ctx);
+        const int32_t *lst = p.key_idx + (size_t)s * p.max_keys;
+        int k = 0;
+        for (; k < nblk; ++k) {
+            const int st = k % NST;
+            bool ok = true;
+            if (k >= NST)
+                ok = mbar_wait_bounded(&empty[st], ((k / NST) + 1) & 1, kWaitLimitCycles);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok || s_flag[1]) {
+                if (lane == 0) {
+                    if (!ok)
+                        atomicOr(p.status, PKV_DEV_TIMEOUT);
+                    s_flag[1] = 1;
+                }
+                break;
+            }
+            // lane j < 16 resolves entry j of this tile
+            const int e = t0 + k * 16 + (lane & 15);
+            unsigned long long off = 0;
+            int valid = 0;
+            if (lane < 16 && e < t1) {
+                const int pos = __ldg(lst + e);
+                if (pos >= 0 && pos < ctx) {
+                    const int blk = __ldg(p.block_tables + (size_t)seq * p.max_blocks_per_seq + pos / p.block_size);
+                    if (blk >= 0 && blk < p.num_blocks) {
+                        off = ((((unsigned long long)blk * p.num_kv_heads) + g) * p.block_size + pos % p.block_size) * D;
+                        valid = 1;
+                    } else {
+                        atomicOr(p.status, PKV_DEV_BAD_BLOCK);
+                    }
+                } else {
+                    atomicOr(p.status, PKV_DEV_TABLE_OVERRUN);   // a listed position outside the context
+                }
+            }
+            uint8_t *kt = k_tiles + st * T::kTileBytes;
+            uint8_t *vt = v_tiles + st * T::kTileBytes;
+#pragma unroll
+            for (int i = 0; i < KPL; ++i) {
+                const int key = kq + i * KSTEP;
+                const unsigned long long o = __shfl_sync(0xffffffffu, off, key);
+                const int vld = __shfl_sync(0xffffffffu, valid, key);
+                if (t0 + k * 16 + key < t1) {   // entries past the list's end are masked, not copied
+                    cp_async_16(kt + tile_off<16>(key, ch), p.kpool + o + ch * 8, vld ? 16u : 0u);
+                    cp_async_16(vt + tile_off<16>(key, ch), p.vpool + o + ch * 8, vld ? 16u : 0u);
+                }
+            }
+            cp_async_arrive(&full[st]);
+        }
+        if (lane == 0)
+            s_flag[2] = k;
+    } else if (!GATHER && warp == NMT * KW) {
         // ---------------- producer warp: block table -> TMA ring ----------------
         // lane l holds the ids of the split's blocks l, l + 32, ... (one coalesced load each)
         int my_blk[NBW];
@@ -841,7 +928,7 @@ paged_attention_combine_kernel(const AttnParams p)
     const int row0 = __ldg(p.q_starts + s);
     const int W = min(__ldg(p.q_starts + s + 1) - row0, p.max_rows);
     const int w = r - row0;
-    if (w < 0 || w >= W)
+    if (!p.key_counts && (w < 0 || w >= W))
         return;   // rows past max_q_rows_per_seq were never computed (status already set)
     const int L_cap = (int)min((long long)p.max_context_len, (long long)p.max_blocks_per_seq * p.block_size);
     int L = __ldg(p.context_lens + s);
@@ -852,6 +939,10 @@ paged_attention_combine_kernel(const AttnParams p)
         if (W < 32)
             m &= (1u << W) - 1u;
         lim = L - W + (m ? 32 - __clz(m) : 0);
+    }
+    if (p.key_counts) {   // index-list gather: the row's list length
+        const int c = __ldg(p.key_counts + r);
+        lim = c < 0 ? 0 : (c > p.max_keys ? p.max_keys : c);
     }
     const int n = lim > 0 ? (lim + kSplitTokens - 1) / kSplitTokens : 0;
     const size_t base = ((size_t)r * p.num_q_heads + h) * p.n_max;
@@ -1022,13 +1113,13 @@ size_t smem_bytes()
     return 1024 + (size_t)NST * stage + 2 * NST * sizeof(uint64_t) + 64;
 }
 
-template <int D, int BS, int NN, int NMT, bool TREE, int BITS>
+template <int D, int BS, int NN, int NMT, bool TREE, int BITS, bool GATHER = false>
 int launch_t(const CUtensorMap &mk, const CUtensorMap &mv, const AttnParams &prm, dim3 grid,
              cudaStream_t st)
 {
     constexpr int NST = kStages<D, BS, NMT, BITS>();
-    constexpr int KW = kKeyWarps<BITS>();
-    auto kern = paged_attention_kernel<D, BS, NN, NMT, NST, TREE, BITS, KW>;
+    constexpr int KW = GATHER ? 1 : kKeyWarps<BITS>();
+    auto kern = paged_attention_kernel<D, BS, NN, NMT, NST, TREE, BITS, KW, GATHER>;
     const size_t smem = smem_bytes<D, BS, NMT, BITS>();
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
@@ -1111,6 +1202,9 @@ struct PoolView {
     int32_t num_blocks, block_size, num_kv_heads, head_dim, bits;   // bits: 16, 8 or 4
     const void *k_pool, *v_pool;   // bits == 16
     const void *records;           // bits 8 / 4
+    const int32_t *key_idx = nullptr;      // index-list gather: [R][max_keys], or null
+    const int32_t *key_counts = nullptr;   // [R]
+    int32_t max_keys = 0;
 };
 
 // Called with validated parameters: launches the split and merge kernels.
@@ -1200,6 +1294,11 @@ inline int attention_run(const char *who, const PoolView &pv, const void *q, con
     prm.part_ml = reinterpret_cast<float2 *>(ws + wl.ml);
     prm.part_o = reinterpret_cast<float *>(ws + wl.o);
     prm.qrec = static_cast<const uint8_t *>(pv.records);
+    prm.kpool = static_cast<const uint16_t *>(pv.k_pool);
+    prm.vpool = static_cast<const uint16_t *>(pv.v_pool);
+    prm.key_idx = pv.key_idx;
+    prm.key_counts = pv.key_counts;
+    prm.max_keys = pv.max_keys;
     prm.status = status;
     prm.num_seqs = num_seqs;
     prm.max_blocks_per_seq = max_blocks_per_seq;

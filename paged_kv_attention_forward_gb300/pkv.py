@@ -29,7 +29,7 @@ EXPORTED = ("pkv_abi_version", "paged_kv_append", "paged_attention_workspace_siz
             "spec_accept_greedy", "pkv_last_error_string", "pkv_device_status",
             "paged_attention_forward_noalloc", "paged_tree_attention_forward", "spec_accept_tree_greedy",
             "spec_accept_sampled", "paged_block_hashes", "pkv_qrecord_bytes", "paged_kv_append_quant",
-            "paged_attention_forward_quant")
+            "paged_attention_forward_quant", "paged_attention_forward_gather")
 
 
 class PkvError(RuntimeError):
@@ -100,6 +100,9 @@ def lib(build_if_missing: bool = False):
             L.paged_attention_forward_quant.argtypes = [ctypes.POINTER(_QPool), P, P, P, i32, P, i32, i32, i32,
                                                         i32, i32, P, P, i32, ctypes.c_float, P, i32, P, sz, P]
             L.paged_attention_forward_quant.restype = ctypes.c_int
+            L.paged_attention_forward_gather.argtypes = [ctypes.POINTER(_Pool), P, P, P, i32, P, i32, i32, P, P,
+                                                         i32, i32, P, P, ctypes.c_float, P, i32, P, sz, P]
+            L.paged_attention_forward_gather.restype = ctypes.c_int
             L.spec_accept_workspace_size.argtypes = [i32, i32]
             L.spec_accept_workspace_size.restype = sz
             L.spec_accept_greedy.argtypes = [P, i32, P, P, i32, i32, P, P, P, P, sz, P]
@@ -187,6 +190,34 @@ def paged_attention_forward(k_pool, v_pool, q, q_starts, block_tables, context_l
         _dptr(context_lens), S, R, int(max_context_len), int(max_q_rows_per_seq), Hq, hmap,
         _dptr(sinks), int(bool(causal)), float(scale), _dptr(out), dt, _dptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def paged_attention_forward_gather(k_pool, v_pool, q, q_starts, block_tables, context_lens, key_idx, key_counts, *,
+                                   kv_head_of_q_head=None, sinks=None, scale: float = 0.0,
+                                   out: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16,
+                                   workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Attention of each row over its own key list (see include/pkv.h).
+
+    key_idx: CUDA int32 [R, max_keys]; key_counts: CUDA int32 [R]."""
+    pool = _pool(k_pool, v_pool)
+    R, Hq, D = q.shape
+    S = block_tables.shape[0]
+    max_keys = key_idx.shape[1]
+    if out is None:
+        out = torch.empty((R, Hq, D), dtype=out_dtype, device=q.device)
+    dt = PKV_DTYPE_F32 if out.dtype == torch.float32 else PKV_DTYPE_BF16
+    if workspace is None:
+        workspace = new_attention_workspace(S, R, Hq, pool.num_kv_heads, D, max_keys, q.device)
+    hmap = None
+    if kv_head_of_q_head is not None:
+        arr = (ctypes.c_int32 * Hq)(*[int(x) for x in kv_head_of_q_head])
+        hmap = ctypes.cast(arr, ctypes.c_void_p)
+    _check(lib().paged_attention_forward_gather(
+        ctypes.byref(pool), _dptr(q), _dptr(q_starts), _dptr(block_tables), block_tables.shape[1],
+        _dptr(context_lens), S, R, _dptr(key_idx), _dptr(key_counts), int(max_keys), Hq, hmap, _dptr(sinks),
+        float(scale), _dptr(out), dt, _dptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
     return out
 
 
