@@ -62,9 +62,23 @@ def algorithmic_bytes(b: wl.PagedBatch, layers: int = 1, bits: int = 16) -> dict
         private_tokens += L - n_sh * B
     kv = (private_tokens + shared_tokens_read) * H * per_tok
     logical_kv = int(b.context_lens.sum()) * H * per_tok
+    list_bytes = 0
+    if b.key_idx is not None:
+        # index-list gather: every distinct physical (block, slot) the step's lists name, once
+        row_seq = np.searchsorted(b.q_starts, np.arange(b.total_q_rows), side="right") - 1
+        slots = set()
+        for r in range(b.total_q_rows):
+            s_ = row_seq[r]
+            for t in b.key_idx[0, r, :b.key_counts[0, r]]:
+                slots.add(int(b.block_tables[s_, t // B]) * B + int(t % B))
+        kv = len(slots) * H * per_tok
+        logical_kv = int(b.key_counts[0].sum()) * H * per_tok
+        list_bytes = int(b.key_counts[0].sum()) * (4 + 4)    # the list entries and their table entries
     R = b.total_q_rows
     q_out = 2 * R * b.num_q_heads * D * 2
     table = int(sum((int(L) + B - 1) // B for L in b.context_lens)) * 4 + (b.num_seqs * 2 + 1) * 4
+    if b.key_idx is not None:
+        table = list_bytes + (b.num_seqs * 2 + 1) * 4 + b.total_q_rows * 4
     r_new = int(b.new_starts[-1])
     append = r_new * H * (D * 2 * 2 + per_tok)          # read k_new/v_new, write the pool slots
     attn = kv + q_out + table
@@ -215,7 +229,7 @@ def run_ours(args, rank, world, local_rank):
     sinks = None if b.sinks is None else d(b.sinks)
     outs = [torch.empty_like(q) for q in qs]
     ws = pkv.new_attention_workspace(b.num_seqs, b.total_q_rows, b.num_q_heads, b.num_kv_heads,
-                                     b.head_dim, b.max_context_len, dev)
+                                     b.head_dim, b.max_context_len if b.key_idx is None else b.key_idx.shape[2], dev)
     logits = drafts = acc_ws = None
     acc_out = None
     tree = b.tree_masks is not None
@@ -233,6 +247,11 @@ def run_ours(args, rank, world, local_rank):
         acc_out = tuple(torch.empty(n, dtype=torch.int32, device=dev)
                         for n in (b.total_q_rows, b.num_seqs, b.total_q_rows, b.total_q_rows))
     has_append = int(b.new_starts[-1]) > 0
+    gather = b.key_idx is not None
+    if gather:
+        key_sets = [d(b.key_idx[k]) for k in range(b.key_idx.shape[0])]
+        key_counts = d(b.key_counts[0])
+        step_no = [0]
     accept_mode = getattr(args, "accept", "greedy")
     max_ctx, max_rows = b.max_context_len, b.max_q_rows_per_seq
     stream = torch.cuda.current_stream()
@@ -250,7 +269,13 @@ def run_ours(args, rank, world, local_rank):
                                     stream=stream)
             if ev_pairs is not None:
                 ev_pairs[li][0].record(stream)
-            if quant:
+            if gather:
+                k_set = key_sets[step_no[0] % len(key_sets)]   # the lists change every step
+                step_no[0] += 1
+                pkv.paged_attention_forward_gather(pools[i][0], pools[i][1], qs[i], q_starts, tables, lens, k_set,
+                                                   key_counts, sinks=sinks, out=outs[i], workspace=ws,
+                                                   stream=stream)
+            elif quant:
                 pkv.paged_attention_forward_quant(records[i], b.block_size, b.head_dim, bits, qs[i], q_starts, tables,
                                                   lens, max_context_len=max_ctx, max_q_rows_per_seq=max_rows,
                                                   sinks=sinks, causal=b.causal, out=outs[i], workspace=ws,
@@ -347,6 +372,10 @@ def run_ours(args, rank, world, local_rank):
         h_inputs.append(pin(positions.cpu().numpy()))
         d_inputs.append(positions)
         h2d += b.total_q_rows * 4
+    if gather:   # this step's lists come from the host too
+        h_inputs.append(pin(b.key_idx[0]))
+        d_inputs.append(key_sets[0])
+        h2d += b.key_idx[0].nbytes
 
     def e2e_step():
         for hsrc, ddst in zip(h_inputs, d_inputs):
@@ -402,7 +431,10 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_description(b, layers), "global_batch": b.num_seqs * world,
+        "config": {"workload": workload_description(b, layers)
+                   + ("" if not gather else f", index-list gather: [last 128 | 512 older] keys per row, "
+                                            f"{b.key_idx.shape[0]} list sets used in turn"),
+                   "global_batch": b.num_seqs * world,
                    "seq_len": b.max_context_len, "parallelism": f"dp{world} (independent replicas)",
                    "l2": "inputs larger than L2 (K/V read per step >> 129 MB); no flush",
                    "seed": args.seed,
@@ -456,8 +488,12 @@ def time_oracle_step(sub: wl.PagedBatch, threads: int, records=None, bits: int =
     if int(sub.new_starts[-1]) > 0:
         oracle.paged_kv_append(k, v, sub.block_tables, sub.context_lens_old, sub.new_starts,
                                sub.k_new[0], sub.v_new[0])
-    oracle.paged_attention(k, v, sub.q[0], sub.q_starts, sub.block_tables, sub.context_lens, sinks=sub.sinks,
-                           causal=sub.causal, num_threads=threads, tree_masks=sub.tree_masks)
+    if sub.key_idx is not None:
+        oracle.paged_attention_sparse(k, v, sub.q[0], sub.q_starts, sub.block_tables, sub.context_lens,
+                                      sub.key_idx[0], sub.key_counts[0], sinks=sub.sinks)
+    else:
+        oracle.paged_attention(k, v, sub.q[0], sub.q_starts, sub.block_tables, sub.context_lens, sinks=sub.sinks,
+                               causal=sub.causal, num_threads=threads, tree_masks=sub.tree_masks)
     if sub.logits is not None and sub.parents is not None:
         oracle.spec_accept_tree_greedy(sub.logits, sub.q_starts, sub.draft_tokens, sub.parents)
     elif sub.logits is not None:
