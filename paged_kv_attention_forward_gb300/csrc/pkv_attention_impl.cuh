@@ -616,7 +616,7 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                     v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
                     const float m_new = fmaxf(mrow[nn][e], v);
                     base[nn][e] = (m_new == -INFINITY) ? 0.f : m_new;
-                    alpha[nn][e] = exp2f(mrow[nn][e] - base[nn][e]);
+                    alpha[nn][e] = fast_exp2(mrow[nn][e] - base[nn][e]);
                     mrow[nn][e] = m_new;
                 }
             const bool tail = tbase + BS > L;
@@ -658,13 +658,13 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
                 for (int nn = 0; nn < NN; ++nn) {
                     if constexpr (BITS == 16) {
-                        pk[mt][nn][0] = pack_bf16x2(exp2f(sa[mt][nn][0] - base[nn][0]), exp2f(sa[mt][nn][1] - base[nn][1]));
-                        pk[mt][nn][1] = pack_bf16x2(exp2f(sa[mt][nn][2] - base[nn][0]), exp2f(sa[mt][nn][3] - base[nn][1]));
+                        pk[mt][nn][0] = pack_bf16x2(fast_exp2(sa[mt][nn][0] - base[nn][0]), fast_exp2(sa[mt][nn][1] - base[nn][1]));
+                        pk[mt][nn][1] = pack_bf16x2(fast_exp2(sa[mt][nn][2] - base[nn][0]), fast_exp2(sa[mt][nn][3] - base[nn][1]));
                         sum[nn][0] += bf16_lo_to_f32(pk[mt][nn][0]) + bf16_lo_to_f32(pk[mt][nn][1]);
                         sum[nn][1] += bf16_hi_to_f32(pk[mt][nn][0]) + bf16_hi_to_f32(pk[mt][nn][1]);
                     } else {
-                        const float p0 = exp2f(sa[mt][nn][0] - base[nn][0]), p1 = exp2f(sa[mt][nn][1] - base[nn][1]);
-                        const float p2 = exp2f(sa[mt][nn][2] - base[nn][0]), p3 = exp2f(sa[mt][nn][3] - base[nn][1]);
+                        const float p0 = fast_exp2(sa[mt][nn][0] - base[nn][0]), p1 = fast_exp2(sa[mt][nn][1] - base[nn][1]);
+                        const float p2 = fast_exp2(sa[mt][nn][2] - base[nn][0]), p3 = fast_exp2(sa[mt][nn][3] - base[nn][1]);
                         float w0 = p0 * (vscale[mt].x * vinv[nn][0]), w1 = p1 * (vscale[mt].x * vinv[nn][1]);
                         float w2 = p2 * (vscale[mt].y * vinv[nn][0]), w3 = p3 * (vscale[mt].y * vinv[nn][1]);
                         if (tail) {
@@ -803,11 +803,11 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
                     for (int j = 1; j < KW; ++j)
                         mx = fmaxf(mx, xs[((size_t)((j - 1) * NMT + mw) * NV + DM * NN * 4 + nn * 6 + e * 3) * 32 + lane]);
-                    f[0][nn][e] = mrow[nn][e] == -INFINITY ? 0.f : exp2f(mrow[nn][e] - mx);
+                    f[0][nn][e] = mrow[nn][e] == -INFINITY ? 0.f : fast_exp2(mrow[nn][e] - mx);
 #pragma unroll
                     for (int j = 1; j < KW; ++j) {
                         const float mj = xs[((size_t)((j - 1) * NMT + mw) * NV + DM * NN * 4 + nn * 6 + e * 3) * 32 + lane];
-                        f[j][nn][e] = mj == -INFINITY ? 0.f : exp2f(mj - mx);
+                        f[j][nn][e] = mj == -INFINITY ? 0.f : fast_exp2(mj - mx);
                     }
                     lrow[nn][e] *= f[0][nn][e];
                     if constexpr (BITS != 16)
@@ -981,7 +981,7 @@ paged_attention_combine_kernel(const AttnParams p)
     float wc[MAXC], lc[MAXC];
 #pragma unroll
     for (int c = 0; c < MAXC; ++c) {
-        wc[c] = exp2f(mlc[c].x - Mx);
+        wc[c] = fast_exp2(mlc[c].x - Mx);
         lc[c] = mlc[c].y;
     }
     float den = 0.f;
@@ -1024,7 +1024,7 @@ paged_attention_combine_kernel(const AttnParams p)
                 l_i = __shfl_sync(0xffffffffu, lsel, srcl);
             } else {
                 const float2 ml = __ldcg(&p.part_ml[base + i]);
-                wgt = exp2f(ml.x - Mx);
+                wgt = fast_exp2(ml.x - Mx);
                 l_i = ml.y;
             }
             den += wgt * l_i;
@@ -1034,7 +1034,7 @@ paged_attention_combine_kernel(const AttnParams p)
         }
     }
     if (has_sink)
-        den += exp2f(sink2 - Mx);
+        den += fast_exp2(sink2 - Mx);
     float res[VEC];
 #pragma unroll
     for (int v = 0; v < VEC; ++v)

@@ -180,6 +180,15 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
     return r;
 }
 
+// 2^x by the SFU's approximate exp2 (relative error about 2^-22; results below the
+// normal range flush to zero, 2^-inf = 0).  The softmax weights only need this.
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ float f16_lo_to_f32(uint32_t v)
 {
     float f;
