@@ -60,6 +60,13 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// accumulation chains of the S^T = K q^T k-steps (2 or 4), a build-time choice
+#ifndef PKV_QK_CHAINS
+#define PKV_QK_CHAINS 2
+#endif
+constexpr int kQkChains = PKV_QK_CHAINS;
+static_assert(kQkChains == 2 || kQkChains == 4, "QK chains");
+
 struct AttnParams {
     const uint16_t *q;            // bf16 [R][Hq][D]
     const int32_t *q_starts;      // [S+1]
@@ -529,14 +536,15 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
             const int tbase = (blk0 + k) * BS;
 
             // S^T for the BS keys of this block; even and odd k-steps in separate chains
-            float sa[MT][NN][4], sb[MT][NN][4];
+            // (PKV_QK_CHAINS = 4: k-steps ks % 4 in four chains, summed (a + b) + (c + d))
+            float sa[MT][NN][4], sb[MT][NN][4], sc[MT][NN][4], sd[MT][NN][4];
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
                 for (int nn = 0; nn < NN; ++nn)
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
-                        sa[mt][nn][c] = sb[mt][nn][c] = 0.f;
+                        sa[mt][nn][c] = sb[mt][nn][c] = sc[mt][nn][c] = sd[mt][nn][c] = 0.f;
             float2 kscale[MT], vscale[MT];   // quantised: scales of this lane's keys 2 kr, 2 kr + 1
             if constexpr (BITS == 16) {
 #pragma unroll
@@ -547,10 +555,9 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                         ldsm_x4(kb + tile_off<BS>(mt * 16 + k_key, ks * 2 + k_chs), a[0], a[1], a[2], a[3]);
 #pragma unroll
                         for (int nn = 0; nn < NN; ++nn) {
-                            if (ks & 1)
-                                mma_bf16_16x8x16(sb[mt][nn], a, qf[nn][ks][0], qf[nn][ks][1]);
-                            else
-                                mma_bf16_16x8x16(sa[mt][nn], a, qf[nn][ks][0], qf[nn][ks][1]);
+                            const int chain = ks % kQkChains;
+                            mma_bf16_16x8x16(chain == 0 ? sa[mt][nn] : chain == 1 ? sb[mt][nn] : chain == 2 ? sc[mt][nn] : sd[mt][nn],
+                                             a, qf[nn][ks][0], qf[nn][ks][1]);
                         }
                     }
                 }
@@ -570,10 +577,9 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                         q_frag<BITS, false>(un, ks, a);
 #pragma unroll
                         for (int nn = 0; nn < NN; ++nn) {
-                            if (ks & 1)
-                                mma_f16_16x8x16(sb[mt][nn], a, qf[nn][ks][0], qf[nn][ks][1]);
-                            else
-                                mma_f16_16x8x16(sa[mt][nn], a, qf[nn][ks][0], qf[nn][ks][1]);
+                            const int chain = ks % kQkChains;
+                            mma_f16_16x8x16(chain == 0 ? sa[mt][nn] : chain == 1 ? sb[mt][nn] : chain == 2 ? sc[mt][nn] : sd[mt][nn],
+                                            a, qf[nn][ks][0], qf[nn][ks][1]);
                         }
                     }
                 }
@@ -592,11 +598,13 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                         // bf16 tiles: A row kr + 8 j is key kr + 8 j; quantised: key 2 kr + j
                         const int t = BITS == 16 ? tbase + mt * 16 + kr + 8 * (c >> 1)
                                                  : tbase + mt * 16 + 2 * kr + (c >> 1);
+                        const float qk = kQkChains == 4 ? (sa[mt][nn][c] + sb[mt][nn][c]) + (sc[mt][nn][c] + sd[mt][nn][c])
+                                                        : sa[mt][nn][c] + sb[mt][nn][c];
                         float x;
                         if constexpr (BITS == 16)
-                            x = (sa[mt][nn][c] + sb[mt][nn][c]) * p.scale_log2;
+                            x = qk * p.scale_log2;
                         else
-                            x = ((sa[mt][nn][c] + sb[mt][nn][c]) - qbias[nn][c & 1]) *
+                            x = (qk - qbias[nn][c & 1]) *
                                 (((c >> 1) ? kscale[mt].y : kscale[mt].x) * qscale[nn][c & 1]);
                         const int e = c & 1;
                         bool vis = t < lim[nn][e];
@@ -1084,13 +1092,13 @@ paged_attention_combine_kernel(const AttnParams p)
 template <int BITS>
 constexpr int kKeyWarps();
 
-template <int D, int BS, int NMT, int BITS>
+template <int D, int BS, int NN, int NMT, int BITS>
 constexpr int kStages()
 {
     constexpr int base = BITS != 16 ? PKV_STAGES_QUANT : NMT == 1 ? PKV_STAGES_DECODE : PKV_STAGES_WIDE;
     // the KW - 1 key shares' states pass through the ring at the end: make it big enough
     constexpr int stage = BITS == 16 ? 2 * Tile<D, BS>::kTileBytes : QRec<D, BS, (BITS == 16 ? 8 : BITS)>::kBytes;
-    constexpr int merge = (kKeyWarps<BITS>() - 1) * NMT * (D / 16 * 4 + 6) * 32 * 4;
+    constexpr int merge = (kKeyWarps<BITS>() - 1) * NMT * (D / 16 * 4 + 6) * NN * 32 * 4;
     constexpr int need = (merge + stage - 1) / stage;
     constexpr int kw = kKeyWarps<BITS>();
     constexpr int n = base > need ? base : need;
@@ -1104,10 +1112,10 @@ constexpr int kKeyWarps()
     return BITS != 16 ? PKV_KW_QUANT : PKV_KW_BF16;
 }
 
-template <int D, int BS, int NMT, int BITS>
+template <int D, int BS, int NN, int NMT, int BITS>
 size_t smem_bytes()
 {
-    constexpr int NST = kStages<D, BS, NMT, BITS>();
+    constexpr int NST = kStages<D, BS, NN, NMT, BITS>();
     constexpr size_t stage = BITS == 16 ? 2 * (size_t)Tile<D, BS>::kTileBytes
                                         : (size_t)QRec<D, BS, (BITS == 16 ? 8 : BITS)>::kBytes;
     return 1024 + (size_t)NST * stage + 2 * NST * sizeof(uint64_t) + 64;
@@ -1117,10 +1125,10 @@ template <int D, int BS, int NN, int NMT, bool TREE, int BITS, bool GATHER = fal
 int launch_t(const CUtensorMap &mk, const CUtensorMap &mv, const AttnParams &prm, dim3 grid,
              cudaStream_t st)
 {
-    constexpr int NST = kStages<D, BS, NMT, BITS>();
+    constexpr int NST = kStages<D, BS, NN, NMT, BITS>();
     constexpr int KW = GATHER ? 1 : kKeyWarps<BITS>();
     auto kern = paged_attention_kernel<D, BS, NN, NMT, NST, TREE, BITS, KW, GATHER>;
-    const size_t smem = smem_bytes<D, BS, NMT, BITS>();
+    const size_t smem = smem_bytes<D, BS, NN, NMT, BITS>();
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
