@@ -60,12 +60,19 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-// accumulation chains of the S^T = K q^T k-steps (2 or 4), a build-time choice
-#ifndef PKV_QK_CHAINS
-#define PKV_QK_CHAINS 2
+// Accumulation chains of the S^T = K q^T k-steps, per codec (chosen by measurement:
+// four chains gain 12 % on Q8 records, whose k-steps carry more latency, and lose 1 %
+// on bf16 pools).  One value per codec keeps every CTA shape on one arithmetic.
+#ifndef PKV_QK_CHAINS_BF16
+#define PKV_QK_CHAINS_BF16 2
 #endif
-constexpr int kQkChains = PKV_QK_CHAINS;
-static_assert(kQkChains == 2 || kQkChains == 4, "QK chains");
+#ifndef PKV_QK_CHAINS_QUANT
+#define PKV_QK_CHAINS_QUANT 4
+#endif
+template <int BITS>
+constexpr int kQkChainsOf = BITS == 16 ? PKV_QK_CHAINS_BF16 : PKV_QK_CHAINS_QUANT;
+static_assert((PKV_QK_CHAINS_BF16 == 2 || PKV_QK_CHAINS_BF16 == 4) &&
+              (PKV_QK_CHAINS_QUANT == 2 || PKV_QK_CHAINS_QUANT == 4), "QK chains");
 
 struct AttnParams {
     const uint16_t *q;            // bf16 [R][Hq][D]
@@ -201,6 +208,7 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
     // warp could wait for a stage's next phase while another warp's phase of it is
     // still pending, and a parity wait cannot tell those phases apart.
     static_assert(NST % KW == 0, "ring depth must be a multiple of the key-share warps");
+    constexpr int kQkChains = kQkChainsOf<BITS>;
     using T = Tile<D, BS>;
     constexpr int MT = BS / 16;   // 16-key m-tiles per block
     constexpr int KS = D / 16;    // k-steps of K q^T
@@ -536,7 +544,7 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
             const int tbase = (blk0 + k) * BS;
 
             // S^T for the BS keys of this block; even and odd k-steps in separate chains
-            // (PKV_QK_CHAINS = 4: k-steps ks % 4 in four chains, summed (a + b) + (c + d))
+            // (four chains: k-steps ks % 4, summed (a + b) + (c + d))
             float sa[MT][NN][4], sb[MT][NN][4], sc[MT][NN][4], sd[MT][NN][4];
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
