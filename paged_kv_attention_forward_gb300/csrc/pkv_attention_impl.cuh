@@ -71,6 +71,12 @@ constexpr float kLog2e = 1.4426950408889634f;
 #endif
 template <int BITS>
 constexpr int kQkChainsOf = BITS == 16 ? PKV_QK_CHAINS_BF16 : PKV_QK_CHAINS_QUANT;
+
+// 16-key quantised records fetched per ring stage (1 or 2)
+#ifndef PKV_QUANT_RECS_PER_STAGE
+#define PKV_QUANT_RECS_PER_STAGE 1
+#endif
+static_assert(PKV_QUANT_RECS_PER_STAGE == 1 || PKV_QUANT_RECS_PER_STAGE == 2, "records per stage");
 static_assert((PKV_QK_CHAINS_BF16 == 2 || PKV_QK_CHAINS_BF16 == 4) &&
               (PKV_QK_CHAINS_QUANT == 2 || PKV_QK_CHAINS_QUANT == 4), "QK chains");
 
@@ -211,6 +217,10 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
     constexpr int kQkChains = kQkChainsOf<BITS>;
     using T = Tile<D, BS>;
     constexpr int MT = BS / 16;   // 16-key m-tiles per block
+    // blocks per ring stage: quantised 16-key records go two at a time, so the per-stage
+    // softmax bookkeeping is paid once per 32 keys
+    constexpr int TB = (BITS != 16 && BS == 16) ? PKV_QUANT_RECS_PER_STAGE : 1;
+    constexpr int MTE = MT * TB;  // 16-key m-tiles per stage
     constexpr int KS = D / 16;    // k-steps of K q^T
     constexpr int DM = D / 16;    // 16-dim m-tiles of V^T P^T
     constexpr int C = kSplitTokens;
@@ -220,13 +230,14 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
-    constexpr int STAGE = BITS == 16 ? 2 * T::kTileBytes : QRec<D, BS, (BITS == 16 ? 8 : BITS)>::kBytes;
+    constexpr int RECB = QRec<D, BS, (BITS == 16 ? 8 : BITS)>::kBytes;
+    constexpr int STAGE = BITS == 16 ? 2 * T::kTileBytes : TB * RECB;
     uint8_t *k_tiles = smem;                          // bf16: K tiles of every stage, then V tiles
     uint8_t *v_tiles = smem + NST * T::kTileBytes;    // quantised: one record per stage
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + NST * STAGE);
     uint64_t *empty = full + NST;
     volatile int32_t *s_flag = reinterpret_cast<volatile int32_t *>(empty + NST);
-    // s_flag[1]: abort; [2]: blocks issued
+    // s_flag[1]: abort; [2]: stages issued
 
     const int pair = blockIdx.x / p.row_groups;
     const int rg = blockIdx.x - pair * p.row_groups;
@@ -292,6 +303,7 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
     const int t1 = min(t0 + C, L);
     const int blk0 = t0 / BS;
     const int nblk = (t1 - t0 + BS - 1) / BS;
+    const int nstage = (nblk + TB - 1) / TB;   // ring stages of this split
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NST; ++i) {
@@ -383,45 +395,54 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
             prefetch_tensormap(&tm_k);
             prefetch_tensormap(&tm_v);
         }
-        int k = 0;
-        bool stop = false;
+        int k = 0;   // stages issued
+        for (; k < nstage; ++k) {
+            int blks[TB];
 #pragma unroll
-        for (int r = 0; r < NBW; ++r) {
-            for (int jj = 0; jj < 32 && !stop; ++jj) {
-                if (k >= nblk)
-                    break;
-                const int blk = __shfl_sync(0xffffffffu, my_blk[r], jj);
-                if (lane == 0) {
-                    const int st = k % NST;
-                    bool ok = true;
-                    if (k >= NST)
-                        ok = mbar_wait_bounded(&empty[st], ((k / NST) + 1) & 1, kWaitLimitCycles);
-                    if (!ok)
-                        atomicOr(p.status, PKV_DEV_TIMEOUT);
-                    if (!ok || s_flag[1]) {
-                        s_flag[1] = 1;
-                        stop = true;
-                    } else if constexpr (BITS == 16) {
-                        const int y = (blk * p.num_kv_heads + g) * BS;
-                        mbar_arrive_expect_tx(&full[st], 2 * T::kTileBytes);
+            for (int i = 0; i < TB; ++i) {
+                const int idx = k * TB + i;
+                int mine = 0;
 #pragma unroll
-                        for (int h = 0; h < T::kHalves; ++h) {
-                            tma_load_2d(k_tiles + st * T::kTileBytes + h * T::kBoxBytes, &tm_k, &full[st],
-                                        h * 64, y);
-                            tma_load_2d(v_tiles + st * T::kTileBytes + h * T::kBoxBytes, &tm_v, &full[st],
-                                        h * 64, y);
-                        }
-                    } else {
-                        constexpr int RB = QRec<D, BS, BITS>::kBytes;
-                        mbar_arrive_expect_tx(&full[st], RB);
-                        bulk_load(smem + st * RB, p.qrec + ((size_t)blk * p.num_kv_heads + g) * RB, RB,
-                                  &full[st]);
-                    }
-                }
-                stop = __shfl_sync(0xffffffffu, stop, 0);
-                if (!stop)
-                    ++k;
+                for (int r = 0; r < NBW; ++r)
+                    if (r == (idx >> 5))
+                        mine = my_blk[r];
+                const int b = __shfl_sync(0xffffffffu, mine, idx & 31);
+                blks[i] = idx < nblk ? b : -1;
             }
+            bool stop = false;
+            if (lane == 0) {
+                const int st = k % NST;
+                bool ok = true;
+                if (k >= NST)
+                    ok = mbar_wait_bounded(&empty[st], ((k / NST) + 1) & 1, kWaitLimitCycles);
+                if (!ok)
+                    atomicOr(p.status, PKV_DEV_TIMEOUT);
+                if (!ok || s_flag[1]) {
+                    s_flag[1] = 1;
+                    stop = true;
+                } else if constexpr (BITS == 16) {
+                    const int y = (blks[0] * p.num_kv_heads + g) * BS;
+                    mbar_arrive_expect_tx(&full[st], 2 * T::kTileBytes);
+#pragma unroll
+                    for (int h = 0; h < T::kHalves; ++h) {
+                        tma_load_2d(k_tiles + st * T::kTileBytes + h * T::kBoxBytes, &tm_k, &full[st], h * 64, y);
+                        tma_load_2d(v_tiles + st * T::kTileBytes + h * T::kBoxBytes, &tm_v, &full[st], h * 64, y);
+                    }
+                } else {
+                    uint32_t bytes = 0;
+#pragma unroll
+                    for (int i = 0; i < TB; ++i)
+                        bytes += blks[i] >= 0 ? RECB : 0;
+                    mbar_arrive_expect_tx(&full[st], bytes);
+#pragma unroll
+                    for (int i = 0; i < TB; ++i)
+                        if (blks[i] >= 0)
+                            bulk_load(smem + st * STAGE + i * RECB,
+                                      p.qrec + ((size_t)blks[i] * p.num_kv_heads + g) * RECB, RECB, &full[st]);
+                }
+            }
+            if (__shfl_sync(0xffffffffu, stop, 0))
+                break;
         }
         if (lane == 0)
             s_flag[2] = k;
@@ -529,7 +550,7 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
         const int v_key = 8 * (lane >> 4) + (lane & 7);         // V: keys of matrices 0/1 vs 2/3
         const int v_chs = (lane >> 3) & 1;
 
-        for (int k = kw; k < nblk; k += KW) {
+        for (int k = kw; k < nstage; k += KW) {
             const int st = k % NST;
             if (!mbar_wait_bounded(&full[st], (k / NST) & 1, kWaitLimitCycles)) {
                 if (lane == 0) {
@@ -541,24 +562,24 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
             const uint32_t kb = smem_addr(k_tiles + st * T::kTileBytes);
             const uint32_t vb = smem_addr(v_tiles + st * T::kTileBytes);
             const uint8_t *rec = smem + st * STAGE;   // quantised record of this stage
-            const int tbase = (blk0 + k) * BS;
+            const int tbase = (blk0 + k * TB) * BS;
 
             // S^T for the BS keys of this block; even and odd k-steps in separate chains
             // (four chains: k-steps ks % 4, summed (a + b) + (c + d))
-            float sa[MT][NN][4], sb[MT][NN][4], sc[MT][NN][4], sd[MT][NN][4];
+            float sa[MTE][NN][4], sb[MTE][NN][4], sc[MTE][NN][4], sd[MTE][NN][4];
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt)
+            for (int mt = 0; mt < MTE; ++mt)
 #pragma unroll
                 for (int nn = 0; nn < NN; ++nn)
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
                         sa[mt][nn][c] = sb[mt][nn][c] = sc[mt][nn][c] = sd[mt][nn][c] = 0.f;
-            float2 kscale[MT], vscale[MT];   // quantised: scales of this lane's keys 2 kr, 2 kr + 1
+            float2 kscale[MTE], vscale[MTE];   // quantised: scales of this lane's keys 2 kr, 2 kr + 1
             if constexpr (BITS == 16) {
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) {
 #pragma unroll
-                    for (int mt = 0; mt < MT; ++mt) {
+                    for (int mt = 0; mt < MTE; ++mt) {
                         uint32_t a[4];
                         ldsm_x4(kb + tile_off<BS>(mt * 16 + k_key, ks * 2 + k_chs), a[0], a[1], a[2], a[3]);
 #pragma unroll
@@ -572,13 +593,15 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
             } else {
                 using QR = QRec<D, BS, BITS>;
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    kscale[mt] = *reinterpret_cast<const float2 *>(rec + QR::kKs + (mt * 16 + 2 * kr) * 4);
-                    vscale[mt] = *reinterpret_cast<const float2 *>(rec + QR::kVs + (mt * 16 + 2 * kr) * 4);
+                for (int mt = 0; mt < MTE; ++mt) {
+                    const uint8_t *rm = rec + (mt / MT) * RECB;   // the record holding m-tile mt
+                    const int mi = mt % MT;
+                    kscale[mt] = *reinterpret_cast<const float2 *>(rm + QR::kKs + (mi * 16 + 2 * kr) * 4);
+                    vscale[mt] = *reinterpret_cast<const float2 *>(rm + QR::kVs + (mi * 16 + 2 * kr) * 4);
                     uint4 un[QR::kUnits];
 #pragma unroll
                     for (int u = 0; u < QR::kUnits; ++u)
-                        un[u] = *reinterpret_cast<const uint4 *>(rec + QR::kK + ((mt * QR::kUnits + u) * 32 + lane) * 16);
+                        un[u] = *reinterpret_cast<const uint4 *>(rm + QR::kK + ((mi * QR::kUnits + u) * 32 + lane) * 16);
 #pragma unroll
                     for (int ks = 0; ks < KS; ++ks) {
                         uint32_t a[4];
@@ -598,7 +621,7 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
             for (int nn = 0; nn < NN; ++nn)
                 mx[nn][0] = mx[nn][1] = -INFINITY;
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt)
+            for (int mt = 0; mt < MTE; ++mt)
 #pragma unroll
                 for (int nn = 0; nn < NN; ++nn)
 #pragma unroll
@@ -635,7 +658,7 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                     alpha[nn][e] = fast_exp2(mrow[nn][e] - base[nn][e]);
                     mrow[nn][e] = m_new;
                 }
-            const bool tail = tbase + BS > L;
+            const bool tail = tbase + BS * TB > L;
             // P = 2^(S - m) rounded to bf16 (packed per 8x8 fragment); l sums the rounded weights.
             // Quantised: P carries each key's V scale relative to the largest V scale among
             // the block's keys the row sees, p * (s_v / s_max), in f16; the block's P V is
@@ -650,7 +673,7 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                     for (int e = 0; e < 2; ++e) {
                         float v = 0.f;
 #pragma unroll
-                        for (int mt = 0; mt < MT; ++mt) {
+                        for (int mt = 0; mt < MTE; ++mt) {
                             const int t = tbase + mt * 16 + 2 * kr;
                             if (t < lim[nn][e])
                                 v = fmaxf(v, vscale[mt].x);
@@ -664,13 +687,13 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                         vinv[nn][e] = v > 0.f ? __frcp_rn(v) : 0.f;
                     }
             }
-            uint32_t pk[MT][NN][2];
+            uint32_t pk[MTE][NN][2];
             float sum[NN][2], psum[NN][2];
 #pragma unroll
             for (int nn = 0; nn < NN; ++nn)
                 sum[nn][0] = sum[nn][1] = psum[nn][0] = psum[nn][1] = 0.f;
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt)
+            for (int mt = 0; mt < MTE; ++mt)
 #pragma unroll
                 for (int nn = 0; nn < NN; ++nn) {
                     if constexpr (BITS == 16) {
@@ -725,7 +748,7 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
 
             // O^T += V^T P^T; keys at or past L may hold anything (even NaN): zero them
 #pragma unroll
-            for (int kk = 0; kk < MT; ++kk) {
+            for (int kk = 0; kk < MTE; ++kk) {
                 uint32_t b[NN][2];
 #pragma unroll
                 for (int nn = 0; nn < NN; ++nn) {
@@ -737,7 +760,8 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                     uint4 un[QR::kUnits];
 #pragma unroll
                     for (int u = 0; u < QR::kUnits; ++u)
-                        un[u] = *reinterpret_cast<const uint4 *>(rec + QR::kV + ((kk * QR::kUnits + u) * 32 + lane) * 16);
+                        un[u] = *reinterpret_cast<const uint4 *>(rec + (kk / MT) * RECB + QR::kV +
+                                                                 (((kk % MT) * QR::kUnits + u) * 32 + lane) * 16);
 #pragma unroll
                     for (int dm = 0; dm < DM; ++dm) {
                         uint32_t a[4];
@@ -1105,7 +1129,8 @@ constexpr int kStages()
 {
     constexpr int base = BITS != 16 ? PKV_STAGES_QUANT : NMT == 1 ? PKV_STAGES_DECODE : PKV_STAGES_WIDE;
     // the KW - 1 key shares' states pass through the ring at the end: make it big enough
-    constexpr int stage = BITS == 16 ? 2 * Tile<D, BS>::kTileBytes : QRec<D, BS, (BITS == 16 ? 8 : BITS)>::kBytes;
+    constexpr int tb = (BITS != 16 && BS == 16) ? PKV_QUANT_RECS_PER_STAGE : 1;
+    constexpr int stage = BITS == 16 ? 2 * Tile<D, BS>::kTileBytes : tb * QRec<D, BS, (BITS == 16 ? 8 : BITS)>::kBytes;
     constexpr int merge = (kKeyWarps<BITS>() - 1) * NMT * (D / 16 * 4 + 6) * NN * 32 * 4;
     constexpr int need = (merge + stage - 1) / stage;
     constexpr int kw = kKeyWarps<BITS>();
@@ -1124,8 +1149,9 @@ template <int D, int BS, int NN, int NMT, int BITS>
 size_t smem_bytes()
 {
     constexpr int NST = kStages<D, BS, NN, NMT, BITS>();
+    constexpr size_t tb = (BITS != 16 && BS == 16) ? PKV_QUANT_RECS_PER_STAGE : 1;
     constexpr size_t stage = BITS == 16 ? 2 * (size_t)Tile<D, BS>::kTileBytes
-                                        : (size_t)QRec<D, BS, (BITS == 16 ? 8 : BITS)>::kBytes;
+                                        : tb * (size_t)QRec<D, BS, (BITS == 16 ? 8 : BITS)>::kBytes;
     return 1024 + (size_t)NST * stage + 2 * NST * sizeof(uint64_t) + 64;
 }
 
