@@ -1126,10 +1126,17 @@ paged_attention_combine_kernel(const AttnParams p)
 template <int BITS>
 constexpr int kKeyWarps();
 
-template <int D, int BS, int NN, int NMT, int BITS>
+#ifndef PKV_STAGES_DEEP
+#define PKV_STAGES_DEEP 8
+#endif
+// DEEP: a grid of at most two CTAs per SM (a few long sequences, e.g. one layer of a
+// 4-sequence decode) is bound by the bytes each CTA keeps in flight, not by occupancy:
+// such calls get a deeper ring.  Ring depth does not change any row's arithmetic.
+template <int D, int BS, int NN, int NMT, int BITS, bool DEEP = false>
 constexpr int kStages()
 {
-    constexpr int base = BITS != 16 ? PKV_STAGES_QUANT : NMT == 1 ? PKV_STAGES_DECODE : PKV_STAGES_WIDE;
+    constexpr int base = DEEP ? PKV_STAGES_DEEP
+                              : BITS != 16 ? PKV_STAGES_QUANT : NMT == 1 ? PKV_STAGES_DECODE : PKV_STAGES_WIDE;
     // the KW - 1 key shares' states pass through the ring at the end: make it big enough
     constexpr int tb = (BITS != 16 && BS == 16) ? PKV_QUANT_RECS_PER_STAGE : 1;
     constexpr int stage = BITS == 16 ? 2 * Tile<D, BS>::kTileBytes : tb * QRec<D, BS, (BITS == 16 ? 8 : BITS)>::kBytes;
@@ -1147,24 +1154,24 @@ constexpr int kKeyWarps()
     return BITS != 16 ? PKV_KW_QUANT : PKV_KW_BF16;
 }
 
-template <int D, int BS, int NN, int NMT, int BITS>
+template <int D, int BS, int NN, int NMT, int BITS, bool DEEP = false>
 size_t smem_bytes()
 {
-    constexpr int NST = kStages<D, BS, NN, NMT, BITS>();
+    constexpr int NST = kStages<D, BS, NN, NMT, BITS, DEEP>();
     constexpr size_t tb = (BITS != 16 && BS == 16) ? PKV_QUANT_RECS_PER_STAGE : 1;
     constexpr size_t stage = BITS == 16 ? 2 * (size_t)Tile<D, BS>::kTileBytes
                                         : tb * (size_t)QRec<D, BS, (BITS == 16 ? 8 : BITS)>::kBytes;
     return 1024 + (size_t)NST * stage + 2 * NST * sizeof(uint64_t) + 64;
 }
 
-template <int D, int BS, int NN, int NMT, bool TREE, int BITS, bool GATHER = false>
+template <int D, int BS, int NN, int NMT, bool TREE, int BITS, bool GATHER = false, bool DEEP = false>
 int launch_t(const CUtensorMap &mk, const CUtensorMap &mv, const AttnParams &prm, dim3 grid,
              cudaStream_t st)
 {
-    constexpr int NST = kStages<D, BS, NN, NMT, BITS>();
+    constexpr int NST = kStages<D, BS, NN, NMT, BITS, DEEP>();
     constexpr int KW = GATHER ? 1 : kKeyWarps<BITS>();
     auto kern = paged_attention_kernel<D, BS, NN, NMT, NST, TREE, BITS, KW, GATHER>;
-    const size_t smem = smem_bytes<D, BS, NN, NMT, BITS>();
+    const size_t smem = smem_bytes<D, BS, NN, NMT, BITS, DEEP>();
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -1212,13 +1219,15 @@ int launch_d_bs(int rows, const CUtensorMap &mk, const CUtensorMap &mv, AttnPara
     if (gx > 0x7fffffffLL || n_max > 65535)
         return set_error(PKV_ERR_SHAPE, "paged attention: grid too large");
     const dim3 grid((unsigned)gx, (unsigned)n_max);
+    const bool deep = gx * n_max <= 2LL * sm_count();   // few, long CTAs: keep more bytes in flight
     if constexpr (WITH_TREE) {
         if (prm.tree_masks)
             return rows <= 8 ? launch_t<D, BS, 1, 1, true, BITS>(mk, mv, prm, grid, st)
                              : launch_t<D, BS, PKV_WIDE_NN, PKV_WIDE_NMT, true, BITS>(mk, mv, prm, grid, st);
     }
     if (rows <= 8)
-        return launch_t<D, BS, 1, 1, false, BITS>(mk, mv, prm, grid, st);
+        return deep ? launch_t<D, BS, 1, 1, false, BITS, false, true>(mk, mv, prm, grid, st)
+                    : launch_t<D, BS, 1, 1, false, BITS>(mk, mv, prm, grid, st);
     return launch_t<D, BS, PKV_WIDE_NN, PKV_WIDE_NMT, false, BITS>(mk, mv, prm, grid, st);
 }
 
