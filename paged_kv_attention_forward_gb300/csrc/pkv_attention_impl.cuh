@@ -59,6 +59,7 @@ namespace pkv {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr unsigned long long kGatherBad = ~0ull;
 
 // Accumulation chains of the S^T = K q^T k-steps, per codec (chosen by measurement:
 // four chains gain 12 % on Q8 records, whose k-steps carry more latency, and lose 1 %
@@ -240,6 +241,8 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
     uint64_t *empty = full + NST;
     volatile int32_t *s_flag = reinterpret_cast<volatile int32_t *>(empty + NST);
     // s_flag[1]: abort; [2]: stages issued
+    // (gather) the slice's resolved row offsets, in elements; kGatherBad marks a bad entry
+    unsigned long long *g_off = reinterpret_cast<unsigned long long *>(empty + NST + 8);
 
     const int pair = blockIdx.x / p.row_groups;
     const int rg = blockIdx.x - pair * p.row_groups;
@@ -328,6 +331,27 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
         long long ctx = __ldg(p.context_lens + seq);
         ctx = ctx < 0 ? 0 : (ctx > ctx_cap ? ctx_cap : ctx);
         const int32_t *lst = p.key_idx + (size_t)s * p.max_keys;
+        // resolve every entry of the slice first, all loads in flight at once (an entry's
+        // block-table load depends on its list load; per tile that chain would serialise)
+#pragma unroll 4
+        for (int i = lane; i < C; i += 32) {
+            const int e = t0 + i;
+            if (e >= t1)
+                break;
+            const int pos = __ldg(lst + e);
+            unsigned long long off = kGatherBad;
+            if (pos >= 0 && pos < ctx) {
+                const int blk = __ldg(p.block_tables + (size_t)seq * p.max_blocks_per_seq + pos / p.block_size);
+                if (blk >= 0 && blk < p.num_blocks)
+                    off = ((((unsigned long long)blk * p.num_kv_heads) + g) * p.block_size + pos % p.block_size) * D;
+                else
+                    atomicOr(p.status, PKV_DEV_BAD_BLOCK);
+            } else {
+                atomicOr(p.status, PKV_DEV_TABLE_OVERRUN);   // a listed position outside the context
+            }
+            g_off[i] = off;
+        }
+        __syncwarp();
         int k = 0;
         for (; k < nblk; ++k) {
             const int st = k % NST;
@@ -343,34 +367,16 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                 }
                 break;
             }
-            // lane j < 16 resolves entry j of this tile
-            const int e = t0 + k * 16 + (lane & 15);
-            unsigned long long off = 0;
-            int valid = 0;
-            if (lane < 16 && e < t1) {
-                const int pos = __ldg(lst + e);
-                if (pos >= 0 && pos < ctx) {
-                    const int blk = __ldg(p.block_tables + (size_t)seq * p.max_blocks_per_seq + pos / p.block_size);
-                    if (blk >= 0 && blk < p.num_blocks) {
-                        off = ((((unsigned long long)blk * p.num_kv_heads) + g) * p.block_size + pos % p.block_size) * D;
-                        valid = 1;
-                    } else {
-                        atomicOr(p.status, PKV_DEV_BAD_BLOCK);
-                    }
-                } else {
-                    atomicOr(p.status, PKV_DEV_TABLE_OVERRUN);   // a listed position outside the context
-                }
-            }
             uint8_t *kt = k_tiles + st * T::kTileBytes;
             uint8_t *vt = v_tiles + st * T::kTileBytes;
 #pragma unroll
             for (int i = 0; i < KPL; ++i) {
                 const int key = kq + i * KSTEP;
-                const unsigned long long o = __shfl_sync(0xffffffffu, off, key);
-                const int vld = __shfl_sync(0xffffffffu, valid, key);
                 if (t0 + k * 16 + key < t1) {   // entries past the list's end are masked, not copied
-                    cp_async_16(kt + tile_off<16>(key, ch), p.kpool + o + ch * 8, vld ? 16u : 0u);
-                    cp_async_16(vt + tile_off<16>(key, ch), p.vpool + o + ch * 8, vld ? 16u : 0u);
+                    const unsigned long long o = g_off[k * 16 + key];
+                    const bool vld = o != kGatherBad;   // a bad entry copies zeros from the pool's start
+                    cp_async_16(kt + tile_off<16>(key, ch), p.kpool + (vld ? o : 0ull) + ch * 8, vld ? 16u : 0u);
+                    cp_async_16(vt + tile_off<16>(key, ch), p.vpool + (vld ? o : 0ull) + ch * 8, vld ? 16u : 0u);
                 }
             }
             cp_async_arrive(&full[st]);
@@ -1154,14 +1160,15 @@ constexpr int kKeyWarps()
     return BITS != 16 ? PKV_KW_QUANT : PKV_KW_BF16;
 }
 
-template <int D, int BS, int NN, int NMT, int BITS, bool DEEP = false>
+template <int D, int BS, int NN, int NMT, int BITS, bool DEEP = false, bool GATHER = false>
 size_t smem_bytes()
 {
     constexpr int NST = kStages<D, BS, NN, NMT, BITS, DEEP>();
     constexpr size_t tb = (BITS != 16 && BS == 16) ? PKV_QUANT_RECS_PER_STAGE : 1;
     constexpr size_t stage = BITS == 16 ? 2 * (size_t)Tile<D, BS>::kTileBytes
                                         : tb * (size_t)QRec<D, BS, (BITS == 16 ? 8 : BITS)>::kBytes;
-    return 1024 + (size_t)NST * stage + 2 * NST * sizeof(uint64_t) + 64;
+    // + the flags (64 B) and, for the index-list gather, a split's row offsets
+    return 1024 + (size_t)NST * stage + 2 * NST * sizeof(uint64_t) + 64 + (GATHER ? (size_t)kSplitTokens * 8 : 0);
 }
 
 template <int D, int BS, int NN, int NMT, bool TREE, int BITS, bool GATHER = false, bool DEEP = false>
@@ -1171,7 +1178,7 @@ int launch_t(const CUtensorMap &mk, const CUtensorMap &mv, const AttnParams &prm
     constexpr int NST = kStages<D, BS, NN, NMT, BITS, DEEP>();
     constexpr int KW = GATHER ? 1 : kKeyWarps<BITS>();
     auto kern = paged_attention_kernel<D, BS, NN, NMT, NST, TREE, BITS, KW, GATHER>;
-    const size_t smem = smem_bytes<D, BS, NN, NMT, BITS, DEEP>();
+    const size_t smem = smem_bytes<D, BS, NN, NMT, BITS, DEEP, GATHER>();
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
