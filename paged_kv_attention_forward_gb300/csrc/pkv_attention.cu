@@ -75,7 +75,7 @@ int launch_bf16(const PoolView &pv, AttnParams &prm, int rows, long long pairs, 
 }
 
 #ifndef PKV_GATHER_DEEP
-#define PKV_GATHER_DEEP 1
+#define PKV_GATHER_DEEP 0
 #endif
 // Index-list gather: one unit per (query row, KV head); the grid's second dimension
 // runs over 512-entry slices of the longest list.
@@ -90,8 +90,8 @@ int launch_gather_d(int rows, AttnParams prm, long long pairs, int n_max, cudaSt
     if (gx > 0x7fffffffLL || n_max > 65535)
         return set_error(PKV_ERR_SHAPE, "paged_attention_forward_gather: grid too large");
     const dim3 grid((unsigned)gx, (unsigned)n_max);
-    // scattered 16-byte row copies carry more latency than TMA tiles: the gather keeps a
-    // deeper ring by default
+    // (a deeper ring was measured slower here: 1024 CTAs need the occupancy more than the
+    // bytes in flight; PKV_GATHER_DEEP=1 selects it)
     if (rows <= 8)
         return launch_t<D, 16, 1, 1, false, 16, true, PKV_GATHER_DEEP != 0>(none, none, prm, grid, st);
     return launch_t<D, 16, PKV_WIDE_NN, PKV_WIDE_NMT, false, 16, true, PKV_GATHER_DEEP != 0>(none, none, prm, grid, st);
