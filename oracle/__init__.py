@@ -76,6 +76,8 @@ def _load():
             lib.oracle_paged_attention_sparse.argtypes = [P, P, i32, i32, i32, i32, P, P, P, i32, P, i32, P, P,
                                                           i32, i32, P, P, ctypes.c_double, P]
             lib.oracle_paged_attention_sparse.restype = ctypes.c_int
+            lib.oracle_topp_threshold.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
+            lib.oracle_topp_threshold.restype = ctypes.c_uint64
             lib.oracle_keyed_exp2.argtypes = [ctypes.c_float]
             lib.oracle_keyed_exp2.restype = ctypes.c_float
             lib.oracle_topkp_kept.argtypes = [P, i32, ctypes.c_float, i32, ctypes.c_float, P]
@@ -258,6 +260,11 @@ def spec_accept_sampled(logits, q_starts, draft_tokens, positions, seed, tempera
     if rc != 0:
         raise ValueError(f"oracle_spec_accept_sampled failed with status {rc}")
     return sm, al, ot, ar
+
+
+def topp_threshold(p_fix: int, total: int) -> int:
+    """ceil(p_fix * total / 2^32): the weight a top-p prefix must reach."""
+    return int(_load().oracle_topp_threshold(int(p_fix), int(total)))
 
 
 def keyed_exp2(y: float) -> float:

@@ -487,6 +487,14 @@ static uint64_t keyed_weight(float l, float l_max, float temperature)
     return (uint64_t)(w * 4294967296.0f);
 }
 
+/* The weight the top-p prefix must reach: ceil(p_fix * total / 2^32), with the
+ * product taken exactly (128 bits). */
+uint64_t oracle_topp_threshold(uint64_t p_fix, uint64_t total)
+{
+    const unsigned __int128 prod = (unsigned __int128)p_fix * total;
+    return (uint64_t)((prod + 0xFFFFFFFFu) >> 32);
+}
+
 /* the order tokens are filtered in: logit descending, then token id ascending */
 static const float *g_sort_row;
 static int order_cmp(const void *a, const void *b)
@@ -526,9 +534,7 @@ int32_t oracle_topkp_kept(const float *row, int32_t vocab, float temperature, in
         uint64_t total = 0;
         for (int32_t v = 0; v < vocab; ++v)
             total += keyed_weight(row[v], l_max, temperature);
-        const uint64_t p_fix = (uint64_t)(top_p * 4294967296.0f);
-        const unsigned __int128 prod = (unsigned __int128)p_fix * total;
-        const uint64_t thr = (uint64_t)((prod + 0xFFFFFFFFu) >> 32);
+        const uint64_t thr = oracle_topp_threshold((uint64_t)(top_p * 4294967296.0f), total);
         uint64_t cum = 0;
         int32_t np = vocab;
         for (int32_t i = 0; i < vocab; ++i) {

@@ -216,3 +216,17 @@ def test_topkp_draws(oracle_mod):
     s5, *_ = oracle_mod.spec_accept_sampled(logits, qs, drafts, pos, seed=5, temperature=1.0)
     s6, *_ = oracle_mod.spec_accept_sampled(logits, qs, drafts, pos, seed=5, temperature=1.0, top_k=V, top_p=1.0)
     assert np.array_equal(s5, s6)
+
+
+def test_topp_threshold_is_a_ceiling(oracle_mod):
+    # exact integers: the threshold rounds p_fix * total / 2^32 up, never down
+    rng = np.random.default_rng(11)
+    assert oracle_mod.topp_threshold(1 << 31, 3) == 2            # 1.5 -> 2
+    assert oracle_mod.topp_threshold(1 << 31, 4) == 2            # 2 exactly
+    assert oracle_mod.topp_threshold(1, 1) == 1                  # 2^-32 -> 1
+    assert oracle_mod.topp_threshold(0, 12345) == 0
+    for _ in range(2000):
+        p_fix = int(rng.integers(0, 1 << 32))
+        total = int(rng.integers(1 << 32, 1 << 50))
+        x = p_fix * total
+        assert oracle_mod.topp_threshold(p_fix, total) == -(-x // (1 << 32))
