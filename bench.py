@@ -27,6 +27,7 @@ import subprocess
 import sys
 import threading
 import time
+import types
 
 import numpy as np
 
@@ -259,52 +260,62 @@ def run_ours(args, rank, world, local_rank):
     accept_launches = {"greedy": 2, "sampled": 3, "sampled-topkp": 4}[accept_mode] if logits is not None else 0
     launches_per_step = layers * (int(has_append) + 2) + accept_launches
 
-    def step(ev_pairs=None, li=None):
+    # the tensors a step reads and writes: one set for the device-timed region; the end-to-end
+    # pass alternates two sets so that one step's copies overlap the other's compute
+    io = types.SimpleNamespace(tables=tables, lens_old=lens_old, lens=lens, new_starts=new_starts,
+                               q_starts=q_starts, k_new=k_new, v_new=v_new, qs=qs, outs=outs, logits=logits,
+                               drafts=drafts, acc_out=acc_out, tree_masks=tree_masks, parents=parents,
+                               positions=positions, keys=None)
+
+    def step(ev_pairs=None, li=None, io=io, st=None):
+        st = stream if st is None else st
         for i in range(layers):
             if has_append and quant:
-                pkv.paged_kv_append_quant(records[i], b.block_size, b.head_dim, bits, tables, lens_old, new_starts,
-                                          k_new[i], v_new[i], stream=stream)
+                pkv.paged_kv_append_quant(records[i], b.block_size, b.head_dim, bits, io.tables, io.lens_old,
+                                          io.new_starts, io.k_new[i], io.v_new[i], stream=st)
             elif has_append:
-                pkv.paged_kv_append(pools[i][0], pools[i][1], tables, lens_old, new_starts, k_new[i], v_new[i],
-                                    stream=stream)
+                pkv.paged_kv_append(pools[i][0], pools[i][1], io.tables, io.lens_old, io.new_starts, io.k_new[i],
+                                    io.v_new[i], stream=st)
             if ev_pairs is not None:
-                ev_pairs[li][0].record(stream)
+                ev_pairs[li][0].record(st)
             if gather:
-                k_set = key_sets[step_no[0] % len(key_sets)]   # the lists change every step
-                step_no[0] += 1
-                pkv.paged_attention_forward_gather(pools[i][0], pools[i][1], qs[i], q_starts, tables, lens, k_set,
-                                                   key_counts, sinks=sinks, out=outs[i], workspace=ws,
-                                                   stream=stream)
+                k_set = io.keys
+                if k_set is None:   # device-timed region: the lists change every step
+                    k_set = key_sets[step_no[0] % len(key_sets)]
+                    step_no[0] += 1
+                pkv.paged_attention_forward_gather(pools[i][0], pools[i][1], io.qs[i], io.q_starts, io.tables,
+                                                   io.lens, k_set, key_counts, sinks=sinks, out=io.outs[i],
+                                                   workspace=ws, stream=st)
             elif quant:
-                pkv.paged_attention_forward_quant(records[i], b.block_size, b.head_dim, bits, qs[i], q_starts, tables,
-                                                  lens, max_context_len=max_ctx, max_q_rows_per_seq=max_rows,
-                                                  sinks=sinks, causal=b.causal, out=outs[i], workspace=ws,
-                                                  stream=stream)
+                pkv.paged_attention_forward_quant(records[i], b.block_size, b.head_dim, bits, io.qs[i], io.q_starts,
+                                                  io.tables, io.lens, max_context_len=max_ctx,
+                                                  max_q_rows_per_seq=max_rows, sinks=sinks, causal=b.causal,
+                                                  out=io.outs[i], workspace=ws, stream=st)
             elif tree:
-                pkv.paged_tree_attention_forward(pools[i][0], pools[i][1], qs[i], q_starts, tables, lens,
-                                                 tree_masks, max_context_len=max_ctx,
-                                                 max_q_rows_per_seq=max_rows, sinks=sinks, out=outs[i],
-                                                 workspace=ws, stream=stream)
+                pkv.paged_tree_attention_forward(pools[i][0], pools[i][1], io.qs[i], io.q_starts, io.tables, io.lens,
+                                                 io.tree_masks, max_context_len=max_ctx,
+                                                 max_q_rows_per_seq=max_rows, sinks=sinks, out=io.outs[i],
+                                                 workspace=ws, stream=st)
             else:
-                pkv.paged_attention_forward(pools[i][0], pools[i][1], qs[i], q_starts, tables, lens,
+                pkv.paged_attention_forward(pools[i][0], pools[i][1], io.qs[i], io.q_starts, io.tables, io.lens,
                                             max_context_len=max_ctx, max_q_rows_per_seq=max_rows, sinks=sinks,
-                                            causal=b.causal, out=outs[i], workspace=ws, stream=stream)
+                                            causal=b.causal, out=io.outs[i], workspace=ws, stream=st)
             if ev_pairs is not None:
-                ev_pairs[li][1].record(stream)
+                ev_pairs[li][1].record(st)
                 li += 1
-        if logits is not None and accept_mode in ("sampled", "sampled-topkp"):
+        if io.logits is not None and accept_mode in ("sampled", "sampled-topkp"):
             filt = dict(top_k=50, top_p=0.9) if accept_mode == "sampled-topkp" else {}
-            pkv.spec_accept_sampled(logits, q_starts, drafts, positions, seed=args.seed + 1, temperature=1.0,
-                                    min_p=0.05, **filt, parents=parents, sampled_out=acc_out[0], accept_len=acc_out[1],
-                                    out_tokens=acc_out[2], accepted_rows=acc_out[3], workspace=acc_ws,
-                                    stream=stream)
-        elif logits is not None and tree:
-            pkv.spec_accept_tree_greedy(logits, q_starts, drafts, parents, argmax_out=acc_out[0],
-                                        accept_len=acc_out[1], out_tokens=acc_out[2], accepted_rows=acc_out[3],
-                                        workspace=acc_ws, stream=stream)
-        elif logits is not None:
-            pkv.spec_accept_greedy(logits, q_starts, drafts, argmax_out=acc_out[0], accept_len=acc_out[1],
-                                   out_tokens=acc_out[2], workspace=acc_ws, stream=stream)
+            pkv.spec_accept_sampled(io.logits, io.q_starts, io.drafts, io.positions, seed=args.seed + 1,
+                                    temperature=1.0, min_p=0.05, **filt, parents=io.parents,
+                                    sampled_out=io.acc_out[0], accept_len=io.acc_out[1], out_tokens=io.acc_out[2],
+                                    accepted_rows=io.acc_out[3], workspace=acc_ws, stream=st)
+        elif io.logits is not None and tree:
+            pkv.spec_accept_tree_greedy(io.logits, io.q_starts, io.drafts, io.parents, argmax_out=io.acc_out[0],
+                                        accept_len=io.acc_out[1], out_tokens=io.acc_out[2],
+                                        accepted_rows=io.acc_out[3], workspace=acc_ws, stream=st)
+        elif io.logits is not None:
+            pkv.spec_accept_greedy(io.logits, io.q_starts, io.drafts, argmax_out=io.acc_out[0],
+                                   accept_len=io.acc_out[1], out_tokens=io.acc_out[2], workspace=acc_ws, stream=st)
         return li
 
     dist = None
@@ -347,62 +358,88 @@ def run_ours(args, rank, world, local_rank):
         raise RuntimeError(f"device status {rc} bits {dev_bits:#x} after timed steps")
 
     # ---- end to end through the public API with host buffers ----
+    # Every step copies its inputs from pinned host memory and its results back.  Two sets of
+    # device buffers let step i + 1's input copies (on a copy stream) overlap step i's kernels,
+    # and step i's result copies overlap step i + 1's kernels, as a serving loop would.
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
     pin16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).pin_memory()  # noqa: E731
-    h_inputs = [pin(b.block_tables), pin(b.context_lens_old), pin(b.context_lens), pin(b.new_starts),
-                pin(b.q_starts)]
-    d_inputs = [tables, lens_old, lens, new_starts, q_starts]
-    h_q = [pin16(b.q[i]) for i in range(layers)]
-    h_kn = [pin16(b.k_new[i]) for i in range(layers)]
-    h_vn = [pin16(b.v_new[i]) for i in range(layers)]
-    h_out = [torch.empty(o.shape, dtype=torch.int16).pin_memory() for o in outs]
-    h2d = sum(t.numel() * t.element_size() for t in h_inputs + h_q + h_kn + h_vn)
-    d2h = sum(t.numel() * t.element_size() for t in h_out)
-    h_logits = h_drafts = h_acc = None
+
+    def clone_set(src):
+        dup = lambda t: None if t is None else t.clone()  # noqa: E731
+        return types.SimpleNamespace(
+            tables=dup(src.tables), lens_old=dup(src.lens_old), lens=dup(src.lens), new_starts=dup(src.new_starts),
+            q_starts=dup(src.q_starts), k_new=[dup(t) for t in src.k_new], v_new=[dup(t) for t in src.v_new],
+            qs=[dup(t) for t in src.qs], outs=[torch.empty_like(t) for t in src.outs], logits=dup(src.logits),
+            drafts=dup(src.drafts), acc_out=None if src.acc_out is None else tuple(torch.empty_like(t) for t in src.acc_out),
+            tree_masks=dup(src.tree_masks), parents=dup(src.parents), positions=dup(src.positions),
+            keys=None if not gather else key_sets[0].clone())
+
+    sets = [clone_set(io), clone_set(io)]
+    # host side of the inputs (name, host tensor) and of the results
+    h_in = [("tables", pin(b.block_tables)), ("lens_old", pin(b.context_lens_old)), ("lens", pin(b.context_lens)),
+            ("new_starts", pin(b.new_starts)), ("q_starts", pin(b.q_starts))]
+    h_layer = [("qs", [pin16(b.q[i]) for i in range(layers)]), ("k_new", [pin16(b.k_new[i]) for i in range(layers)]),
+               ("v_new", [pin16(b.v_new[i]) for i in range(layers)])]
     if logits is not None:
-        h_logits, h_drafts = pin(b.logits), pin(b.draft_tokens)
-        h_acc = [torch.empty(t.shape, dtype=torch.int32).pin_memory() for t in acc_out]
-        h2d += h_logits.numel() * 4 + h_drafts.numel() * 4
-        d2h += sum(t.numel() * 4 for t in h_acc)
+        h_in += [("logits", pin(b.logits)), ("drafts", pin(b.draft_tokens)), ("positions", pin(positions.cpu().numpy()))]
     if tree:
-        h_inputs += [pin(b.tree_masks.view(np.int32)), pin(b.parents)]
-        d_inputs += [tree_masks, parents]
-        h2d += 2 * b.total_q_rows * 4
-    if positions is not None:
-        h_inputs.append(pin(positions.cpu().numpy()))
-        d_inputs.append(positions)
-        h2d += b.total_q_rows * 4
+        h_in += [("tree_masks", pin(b.tree_masks.view(np.int32))), ("parents", pin(b.parents))]
     if gather:   # this step's lists come from the host too
-        h_inputs.append(pin(b.key_idx[0]))
-        d_inputs.append(key_sets[0])
-        h2d += b.key_idx[0].nbytes
+        h_in.append(("keys", pin(b.key_idx[0])))
+    h_out = [[torch.empty(o.shape, dtype=torch.int16).pin_memory() for o in outs] for _ in range(2)]
+    h_acc = None if acc_out is None else [[torch.empty(t.shape, dtype=torch.int32).pin_memory() for t in acc_out]
+                                          for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for _, t in h_in) + \
+        sum(t.numel() * t.element_size() for _, ts in h_layer for t in ts)
+    d2h = sum(t.numel() * t.element_size() for t in h_out[0]) + \
+        (0 if h_acc is None else sum(t.numel() * t.element_size() for t in h_acc[0]))
+    copy_stream = torch.cuda.Stream()
 
-    def e2e_step():
-        for hsrc, ddst in zip(h_inputs, d_inputs):
-            ddst.copy_(hsrc, non_blocking=True)
-        for i in range(layers):
-            qs[i].view(torch.int16).copy_(h_q[i], non_blocking=True)
-            k_new[i].view(torch.int16).copy_(h_kn[i], non_blocking=True)
-            v_new[i].view(torch.int16).copy_(h_vn[i], non_blocking=True)
-        if logits is not None:
-            logits.copy_(h_logits, non_blocking=True)
-            drafts.copy_(h_drafts, non_blocking=True)
-        step()
-        for i in range(layers):
-            h_out[i].copy_(outs[i].view(torch.int16), non_blocking=True)
-        if logits is not None:
-            for hd, dd in zip(h_acc, acc_out):
-                hd.copy_(dd, non_blocking=True)
+    def copy_in(k):
+        dst = sets[k]
+        for name, h in h_in:
+            getattr(dst, name).copy_(h, non_blocking=True)
+        for name, hs in h_layer:
+            for t, h in zip(getattr(dst, name), hs):
+                t.view(torch.int16).copy_(h, non_blocking=True)
 
-    e2e_steps = max(1, min(args.steps, args.e2e_steps))
-    for _ in range(max(3, args.warmup // 4)):
-        e2e_step()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    def copy_out(k):
+        for h, t in zip(h_out[k], sets[k].outs):
+            h.copy_(t.view(torch.int16), non_blocking=True)
+        if h_acc is not None:
+            for h, t in zip(h_acc[k], sets[k].acc_out):
+                h.copy_(t, non_blocking=True)
+
+    def e2e_run(n):
+        ready = [torch.cuda.Event(), torch.cuda.Event()]
+        done = [torch.cuda.Event(), torch.cuda.Event()]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        copy_stream.wait_stream(stream)
+        e0.record(copy_stream)
+        with torch.cuda.stream(copy_stream):
+            copy_in(0)
+        ready[0].record(copy_stream)
+        for i in range(n):
+            k, o = i % 2, 1 - i % 2
+            stream.wait_event(ready[k])
+            step(io=sets[k])
+            done[k].record(stream)
+            with torch.cuda.stream(copy_stream):
+                if i + 1 < n:
+                    if i >= 1:
+                        copy_stream.wait_event(done[o])   # step i - 1 has finished with set o
+                    copy_in(o)
+                    ready[o].record(copy_stream)
+                copy_stream.wait_event(done[k])
+                copy_out(k)
+        e1.record(copy_stream)
+        return e0, e1
+
+    e2e_steps = max(2, min(args.steps, args.e2e_steps))
+    e2e_run(max(3, args.warmup // 4))
     barrier()
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
+    e0, e1 = e2e_run(e2e_steps)
+    torch.cuda.synchronize()
     barrier()
     e2e_ms = e0.elapsed_time(e1)
 
