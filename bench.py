@@ -361,54 +361,76 @@ def run_ours(args, rank, world, local_rank):
     # Every step copies its inputs from pinned host memory and its results back.  Two sets of
     # device buffers let step i + 1's input copies (on a copy stream) overlap step i's kernels,
     # and step i's result copies overlap step i + 1's kernels, as a serving loop would.
-    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
-    pin16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).pin_memory()  # noqa: E731
-
-    def clone_set(src):
-        dup = lambda t: None if t is None else t.clone()  # noqa: E731
-        return types.SimpleNamespace(
-            tables=dup(src.tables), lens_old=dup(src.lens_old), lens=dup(src.lens), new_starts=dup(src.new_starts),
-            q_starts=dup(src.q_starts), k_new=[dup(t) for t in src.k_new], v_new=[dup(t) for t in src.v_new],
-            qs=[dup(t) for t in src.qs], outs=[torch.empty_like(t) for t in src.outs], logits=dup(src.logits),
-            drafts=dup(src.drafts), acc_out=None if src.acc_out is None else tuple(torch.empty_like(t) for t in src.acc_out),
-            tree_masks=dup(src.tree_masks), parents=dup(src.parents), positions=dup(src.positions),
-            keys=None if not gather else key_sets[0].clone())
-
-    sets = [clone_set(io), clone_set(io)]
-    # host side of the inputs (name, host tensor) and of the results
-    h_in = [("tables", pin(b.block_tables)), ("lens_old", pin(b.context_lens_old)), ("lens", pin(b.context_lens)),
-            ("new_starts", pin(b.new_starts)), ("q_starts", pin(b.q_starts))]
-    h_layer = [("qs", [pin16(b.q[i]) for i in range(layers)]), ("k_new", [pin16(b.k_new[i]) for i in range(layers)]),
-               ("v_new", [pin16(b.v_new[i]) for i in range(layers)])]
+    # Each set's inputs live in one packed device buffer (and its results in another), so
+    # a step moves its inputs with one host-to-device copy and its results with one copy back.
+    in_items = [("tables", b.block_tables), ("lens_old", b.context_lens_old), ("lens", b.context_lens),
+                ("new_starts", b.new_starts), ("q_starts", b.q_starts)]
+    in_items += [(("qs", li), np.ascontiguousarray(b.q[li]).view(np.int16)) for li in range(layers)]
+    in_items += [(("k_new", li), np.ascontiguousarray(b.k_new[li]).view(np.int16)) for li in range(layers)]
+    in_items += [(("v_new", li), np.ascontiguousarray(b.v_new[li]).view(np.int16)) for li in range(layers)]
     if logits is not None:
-        h_in += [("logits", pin(b.logits)), ("drafts", pin(b.draft_tokens)), ("positions", pin(positions.cpu().numpy()))]
+        in_items += [("logits", b.logits), ("drafts", b.draft_tokens), ("positions", positions.cpu().numpy())]
     if tree:
-        h_in += [("tree_masks", pin(b.tree_masks.view(np.int32))), ("parents", pin(b.parents))]
+        in_items += [("tree_masks", b.tree_masks.view(np.int32)), ("parents", b.parents)]
     if gather:   # this step's lists come from the host too
-        h_in.append(("keys", pin(b.key_idx[0])))
-    h_out = [[torch.empty(o.shape, dtype=torch.int16).pin_memory() for o in outs] for _ in range(2)]
-    h_acc = None if acc_out is None else [[torch.empty(t.shape, dtype=torch.int32).pin_memory() for t in acc_out]
-                                          for _ in range(2)]
-    h2d = sum(t.numel() * t.element_size() for _, t in h_in) + \
-        sum(t.numel() * t.element_size() for _, ts in h_layer for t in ts)
-    d2h = sum(t.numel() * t.element_size() for t in h_out[0]) + \
-        (0 if h_acc is None else sum(t.numel() * t.element_size() for t in h_acc[0]))
+        in_items.append(("keys", b.key_idx[0]))
+    out_items = [(("outs", li), (b.total_q_rows, b.num_q_heads, b.head_dim), np.int16) for li in range(layers)]
+    if acc_out is not None:
+        out_items += [(("acc_out", n), tuple(t.shape), np.int32) for n, t in enumerate(acc_out)]
+
+    def layout(sizes):
+        offs, at = [], 0
+        for nbytes in sizes:
+            offs.append(at)
+            at += (nbytes + 255) // 256 * 256
+        return offs, at
+
+    in_offs, in_total = layout([np.asarray(a).nbytes for _, a in in_items])
+    out_offs, out_total = layout([int(np.prod(shape)) * np.dtype(dt).itemsize for _, shape, dt in out_items])
+    h_in = torch.empty(in_total, dtype=torch.uint8).pin_memory()
+    h_in_np = h_in.numpy()
+    for (_, a), off in zip(in_items, in_offs):
+        raw = np.ascontiguousarray(a).view(np.uint8).reshape(-1)
+        h_in_np[off:off + raw.size] = raw
+    h_out = [torch.empty(out_total, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    d_in = [torch.empty(in_total, dtype=torch.uint8, device=dev) for _ in range(2)]
+    d_out = [torch.empty(out_total, dtype=torch.uint8, device=dev) for _ in range(2)]
+    to_torch = {np.dtype(np.int32): torch.int32, np.dtype(np.int16): torch.int16}
+
+    def view(buf, off, a_dtype, shape, bf16=False):
+        n = int(np.prod(shape)) * np.dtype(a_dtype).itemsize
+        t = buf[off:off + n].view(to_torch[np.dtype(a_dtype)]).view(shape)
+        return t.view(torch.bfloat16) if bf16 else t
+
+    def make_set(k):
+        st_ = types.SimpleNamespace(qs=[None] * layers, k_new=[None] * layers, v_new=[None] * layers,
+                                    outs=[None] * layers, acc_out=None if acc_out is None else [None] * len(acc_out),
+                                    logits=None, drafts=None, positions=None, tree_masks=None, parents=None,
+                                    keys=None)
+        for (name, a), off in zip(in_items, in_offs):
+            a = np.asarray(a)
+            if isinstance(name, tuple):
+                getattr(st_, name[0])[name[1]] = view(d_in[k], off, np.int16, a.shape, bf16=True)
+            elif name == "logits":
+                st_.logits = d_in[k][off:off + a.nbytes].view(torch.float32).view(a.shape)
+            else:
+                setattr(st_, name, view(d_in[k], off, np.int32, a.shape))
+        for (name, shape, dt), off in zip(out_items, out_offs):
+            getattr(st_, name[0])[name[1]] = view(d_out[k], off, dt, shape, bf16=name[0] == "outs")
+        if st_.acc_out is not None:
+            st_.acc_out = tuple(st_.acc_out)
+        return st_
+
+    sets = [make_set(0), make_set(1)]
+    h2d = in_total
+    d2h = out_total
     copy_stream = torch.cuda.Stream()
 
     def copy_in(k):
-        dst = sets[k]
-        for name, h in h_in:
-            getattr(dst, name).copy_(h, non_blocking=True)
-        for name, hs in h_layer:
-            for t, h in zip(getattr(dst, name), hs):
-                t.view(torch.int16).copy_(h, non_blocking=True)
+        d_in[k].copy_(h_in, non_blocking=True)
 
     def copy_out(k):
-        for h, t in zip(h_out[k], sets[k].outs):
-            h.copy_(t.view(torch.int16), non_blocking=True)
-        if h_acc is not None:
-            for h, t in zip(h_acc[k], sets[k].acc_out):
-                h.copy_(t, non_blocking=True)
+        h_out[k].copy_(d_out[k], non_blocking=True)
 
     def e2e_run(n):
         ready = [torch.cuda.Event(), torch.cuda.Event()]
