@@ -205,11 +205,8 @@ __device__ __forceinline__ void q_frag(const uint4 *un, int ks, uint32_t (&a)[4]
 // GATHER: the index-list gather.  The work unit is (query row, KV head); its keys are
 // the row's list entries, 16 per stage, each row fetched through the block table with
 // 16-byte cp.async copies into the same swizzled tile layout the TMA path fills.
-#ifndef PKV_WIDE_MIN_BLOCKS
-#define PKV_WIDE_MIN_BLOCKS 1
-#endif
 template <int D, int BS, int NN, int NMT, int NST, bool TREE, int BITS, int KW, bool GATHER = false>
-__global__ void __launch_bounds__((NMT * KW + 1) * 32, NMT > 1 ? PKV_WIDE_MIN_BLOCKS : 1)
+__global__ void __launch_bounds__((NMT * KW + 1) * 32)
 paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const AttnParams p)
 {
