@@ -951,6 +951,9 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
 // (sum_i 2^{m_i - M} l_i + 2^{sink - M}).  Launched as a programmatic dependent of
 // the split kernel: it may start early and waits for the partials with
 // griddepcontrol.wait.
+#ifndef PKV_MERGE_BATCH
+#define PKV_MERGE_BATCH 8
+#endif
 template <int D>
 __global__ void __launch_bounds__(128, 7)
 paged_attention_combine_kernel(const AttnParams p)
@@ -1038,7 +1041,7 @@ paged_attention_combine_kernel(const AttnParams p)
     for (int v = 0; v < VEC; ++v)
         num[v] = 0.f;
     const float *src0 = p.part_o + base * D + lane * VEC;
-    constexpr int BATCH = 8;    // partial rows in flight per lane (7 CTAs of 4 warps fit per SM)
+    constexpr int BATCH = PKV_MERGE_BATCH;   // partial rows in flight per lane
     for (int i0 = 0; i0 < n; i0 += BATCH) {
         float x[BATCH][VEC];
 #pragma unroll
