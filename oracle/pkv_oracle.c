@@ -740,13 +740,13 @@ int oracle_block_hashes(const int32_t *tokens, const int32_t *token_starts, int3
 /* ----------------------------------------------------- quantised KV blocks -- */
 /*
  * TensorSharp "高级功能", section "内存优化", the KV block codec item: blocks may
- * be compressed in place to 8 or 4 bits per value (Q8 / Q4, selected by
+ * be compressed in place to 8, 4 or 2 bits per value (Q8 / Q4 / Q2, selected by
  * --paged-kv-quant-bits), trading a small accuracy cost for half or a quarter of
  * the footprint.  The pages give no codec internals.  The plainest codec with
  * that footprint, and the one built here:
  *   every (token, KV head) row x of head_dim bf16 values is quantised
  *   symmetrically with one float32 scale,
- *     Q = 127 (8 bits) or 7 (4 bits),
+ *     Q = 2^(bits-1) - 1: 127 (8 bits), 7 (4 bits) or 1 (2 bits: codes -1, 0, 1),
  *     amax  = max_i |x_i|                       (float32, exact)
  *     scale = amax / Q                          (float32 division, round to nearest)
  *     c_i   = clamp(rint(x_i / scale), -Q, Q)   (float32 division; rint ties to even)
@@ -759,21 +759,27 @@ int oracle_block_hashes(const int32_t *tokens, const int32_t *token_starts, int3
  *   C = block_size * head_dim * bits / 8 bytes of codes per section;
  *   K scale of slot t at byte 2C + 4t, V scale at 2C + 4 block_size + 4t
  *   (float32, little-endian).
- *   8-bit codes are bytes holding c + 128; 4-bit codes are nibbles holding c + 8.
+ *   8-bit codes are bytes holding c + 128; 4-bit codes are nibbles holding c + 8;
+ *   2-bit codes are bit pairs holding c + 2.
  *   Code positions, for slot t and dim i, with 16-byte units of 4 little-endian
  *   32-bit words:
  *   K: mt = t/16, g = (t%16)/2, r = t%2, j = i/16, s = i%16,
  *      c = (s%8)/2, h = s/8, e = s%2, u = 4g + c;
  *      8-bit: byte ((mt*D/32 + j/2)*32 + u)*16 + ((j%2)*2 + r)*4 + h + 2e
  *      4-bit: word ((mt*D/64 + j/4)*32 + u)*16 + (j%4)*4, bits 4(2r + h) + 16e
+ *      2-bit: word (mt*32 + u)*(D/8) + (j/2)*4, bits 8r + 2(2(j%2) + h) + 16e
  *   V: kk = t/16, m = (t%16)/2 + 8(t%2), h = m/8, c = (m%8)/2, e = m%2,
  *      dm = i/16, g = i%8, r = (i%16)/8, u = 4g + c;
  *      8-bit: byte C + ((kk*D/32 + dm/2)*32 + u)*16 + ((dm%2)*2 + r)*4 + h + 2e
  *      4-bit: word C + ((kk*D/64 + dm/4)*32 + u)*16 + (dm%4)*4, bits 4(2h + r) + 16e
+ *      2-bit: word C + (kk*32 + u)*(D/8) + (dm/2)*4, bits 8h + 2(2(dm%2) + r) + 16e
+ *   (the 2-bit units are D/8 bytes: 8 at head_dim 64, 16 at 128).
  * Every byte holds codes of one slot only, so tokens of one block can be
  * appended independently.
  */
-static int qmax_of(int32_t bits) { return bits == 8 ? 127 : 7; }
+static int qmax_of(int32_t bits) { return (1 << (bits - 1)) - 1; }
+
+static int bits_ok(int32_t bits) { return bits == 8 || bits == 4 || bits == 2; }
 
 static float bf16_bits_to_f32(uint16_t bits)
 {
@@ -790,7 +796,7 @@ size_t oracle_qrecord_bytes(int32_t block_size, int32_t head_dim, int32_t bits)
 
 int oracle_kv_quantize_row(const uint16_t *x, int32_t d, int32_t bits, int32_t *codes, float *scale_out)
 {
-    if (bits != 8 && bits != 4)
+    if (!bits_ok(bits))
         return -1;
     float amax = 0.0f;
     for (int32_t i = 0; i < d; ++i) {
@@ -828,6 +834,10 @@ static size_t qcode_pos(int sec, int32_t t, int32_t i, int32_t D, int32_t BS, in
         if (bits == 8) {
             byte = ((size_t)(mt * (D / 32) + j / 2) * 32 + u) * 16 + (size_t)((j % 2) * 2 + r) * 4 + h + 2 * e;
             *shift = 0;
+        } else if (bits == 2) {
+            const int bit = 8 * r + 2 * (2 * (j % 2) + h) + 16 * e;
+            byte = (size_t)(mt * 32 + u) * (D / 8) + (size_t)(j / 2) * 4 + bit / 8;
+            *shift = bit % 8;
         } else {
             const int bit = 4 * (2 * r + h) + 16 * e;
             byte = ((size_t)(mt * (D / 64) + j / 4) * 32 + u) * 16 + (size_t)(j % 4) * 4 + bit / 8;
@@ -839,6 +849,10 @@ static size_t qcode_pos(int sec, int32_t t, int32_t i, int32_t D, int32_t BS, in
         if (bits == 8) {
             byte = C + ((size_t)(kk * (D / 32) + dm / 2) * 32 + u) * 16 + (size_t)((dm % 2) * 2 + r) * 4 + h + 2 * e;
             *shift = 0;
+        } else if (bits == 2) {
+            const int bit = 8 * h + 2 * (2 * (dm % 2) + r) + 16 * e;
+            byte = C + (size_t)(kk * 32 + u) * (D / 8) + (size_t)(dm / 2) * 4 + bit / 8;
+            *shift = bit % 8;
         } else {
             const int bit = 4 * (2 * h + r) + 16 * e;
             byte = C + ((size_t)(kk * (D / 64) + dm / 4) * 32 + u) * 16 + (size_t)(dm % 4) * 4 + bit / 8;
@@ -869,8 +883,9 @@ static void qrecord_put(uint8_t *rec, int sec, int32_t t, const int32_t *codes, 
         if (bits == 8) {
             rec[b] = (uint8_t)(codes[i] + 128);
         } else {
-            const uint8_t nib = (uint8_t)(codes[i] + 8);
-            rec[b] = (uint8_t)((rec[b] & ~(0xF << shift)) | (nib << shift));
+            const int q = qmax_of(bits) + 1, mask = 2 * q - 1;   /* field c + q: 0xF or 0x3 */
+            const uint8_t field = (uint8_t)(codes[i] + q);
+            rec[b] = (uint8_t)((rec[b] & ~(mask << shift)) | (field << shift));
         }
     }
     const size_t C = (size_t)BS * D * bits / 8;
@@ -882,10 +897,12 @@ static double qrecord_get(const uint8_t *rec, int sec, int32_t t, int32_t i, int
     int shift = 0;
     const size_t b = qcode_pos(sec, t, i, D, BS, bits, &shift);
     int32_t c;
-    if (bits == 8)
+    if (bits == 8) {
         c = (int32_t)rec[b] - 128;
-    else
-        c = (int32_t)((rec[b] >> shift) & 0xF) - 8;
+    } else {
+        const int q = qmax_of(bits) + 1;
+        c = (int32_t)((rec[b] >> shift) & (2 * q - 1)) - q;
+    }
     float scale;
     const size_t C = (size_t)BS * D * bits / 8;
     memcpy(&scale, rec + 2 * C + (size_t)sec * 4 * BS + 4 * (size_t)t, sizeof scale);
@@ -915,7 +932,7 @@ static void kv_read_row(const struct kv_source *src, int32_t blk, int32_t g, int
  * Quantising scatter-append: the slot of new token i of sequence s is found as in
  * oracle_paged_kv_append; its K row and V row of every KV head are quantised as
  * above and written into the record of (block, head).  Returns 0, -1 (position
- * beyond the table), -2 (block id out of range), -3 (bits not 8 or 4).
+ * beyond the table), -2 (block id out of range), -3 (bits not 8, 4 or 2).
  */
 int oracle_paged_kv_append_quant(uint8_t *records, int32_t num_blocks, int32_t block_size,
                                  int32_t num_kv_heads, int32_t head_dim, int32_t bits,
@@ -923,7 +940,7 @@ int oracle_paged_kv_append_quant(uint8_t *records, int32_t num_blocks, int32_t b
                                  const int32_t *context_lens_old, const int32_t *new_starts,
                                  const uint16_t *k_new, const uint16_t *v_new, int32_t num_seqs)
 {
-    if (bits != 8 && bits != 4)
+    if (!bits_ok(bits))
         return -3;
     const size_t rb = oracle_qrecord_bytes(block_size, head_dim, bits);
     int32_t *codes = (int32_t *)malloc(sizeof(int32_t) * (size_t)head_dim);
@@ -987,7 +1004,7 @@ int oracle_paged_attention_quant(const uint8_t *records, int32_t bits,
                                  const float *sinks, int32_t causal, const uint32_t *tree_masks,
                                  double scale, double *out, int32_t num_threads)
 {
-    if (bits != 8 && bits != 4)
+    if (!bits_ok(bits))
         return -6;
     struct kv_source src = {NULL, NULL, records, bits};
     return attention_core(&src, num_blocks, block_size, num_kv_heads, head_dim, q, q_starts,

@@ -1,7 +1,7 @@
-"""Oracle pins for quantised KV blocks (Q8 / Q4 codec, record layout, attention).
+"""Oracle pins for quantised KV blocks (Q8 / Q4 / Q2 codec, record layout, attention).
 
 TensorSharp "高级功能", section "内存优化", the KV block codec item: blocks are
-compressed in place to 8 or 4 bits per value at a small accuracy cost.  The codec
+compressed in place to 8, 4 or 2 bits per value at a small accuracy cost.  The codec
 (per-row symmetric integer codes with one float32 scale) and the record layout
 are this library's reading; they are pinned by hand-worked examples, the
 rounding error bound, a layout bijection, and by exactly representable data on
@@ -12,7 +12,7 @@ import pytest
 
 from paged_kv_attention_forward_gb300 import workloads as wl
 
-QMAX = {8: 127, 4: 7}
+QMAX = {8: 127, 4: 7, 2: 1}
 
 
 def bf(vals):
@@ -35,12 +35,16 @@ def test_quantize_worked_examples(oracle_mod):
     codes, scale = oracle_mod.kv_quantize_row(bf([2, 0.5, -1, 0]), 4)
     assert scale == np.float32(2) / np.float32(7)
     assert codes.tolist() == [7, 2, -3, 0]
+    # 2 bits: Q = 1, amax 3 -> scale 3; x / 3 rounds to -1, 0 or 1 (+-0.5 ties go to 0)
+    codes, scale = oracle_mod.kv_quantize_row(bf([3, -1.5, 1.5, 2, -3, 1, -2, 0]), 2)
+    assert scale == 3.0
+    assert codes.tolist() == [1, 0, 0, 1, -1, 0, -1, 0]
     # a zero row: scale 0, every code 0
     codes, scale = oracle_mod.kv_quantize_row(bf([0, -0.0, 0, 0]), 8)
     assert scale == 0.0 and not codes.any()
 
 
-@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("bits", [8, 4, 2])
 def test_quantize_error_bound_and_range(oracle_mod, bits):
     rng = np.random.default_rng(bits)
     Q = QMAX[bits]
@@ -58,7 +62,8 @@ def test_quantize_error_bound_and_range(oracle_mod, bits):
         assert np.all(err <= np.float64(scale) * (0.5 + Q * 2 ** -23))
 
 
-@pytest.mark.parametrize("bits,D,BS", [(8, 128, 16), (8, 64, 32), (4, 128, 16), (4, 64, 32)])
+@pytest.mark.parametrize("bits,D,BS", [(8, 128, 16), (8, 64, 32), (4, 128, 16), (4, 64, 32),
+                                        (2, 128, 16), (2, 64, 16), (2, 64, 32)])
 def test_record_layout_is_a_bijection(oracle_mod, bits, D, BS):
     C = BS * D * bits // 8
     assert oracle_mod.qrecord_bytes(BS, D, bits) == 2 * C + 8 * BS
@@ -86,9 +91,19 @@ def test_record_layout_worked_offsets(oracle_mod):
     assert oracle_mod.qcode_offset(1, 3, 37, 128, 16, 4) == (1024 + 331, 0)
     assert oracle_mod.qcode_offset(0, 0, 8, 128, 16, 4) == (0, 4)       # h = 1: high nibble
     assert oracle_mod.qcode_offset(1, 0, 8, 128, 16, 4) == (1024, 4)    # r = 1: high nibble
+    # 2 bits (units of D/8 = 16 bytes): K slot 3 (g 1, r 1), dim 37 (j 2, c 2, h 0, e 1) -> u 6,
+    # word 96 + 4, bit 8 + 0 + 16 = 24; V slot 3 (m 9: h 1, c 0, e 1), dim 37 (dm 2, g 5,
+    # r 0) -> u 20, word 512 + 320 + 4, bit 8 + 16 = 24
+    assert oracle_mod.qcode_offset(0, 3, 37, 128, 16, 2) == (103, 0)
+    assert oracle_mod.qcode_offset(1, 3, 37, 128, 16, 2) == (512 + 327, 0)
+    assert oracle_mod.qcode_offset(0, 0, 8, 128, 16, 2) == (0, 2)       # h = 1
+    assert oracle_mod.qcode_offset(0, 0, 16, 128, 16, 2) == (0, 4)      # j = 1: second k-step
+    assert oracle_mod.qcode_offset(1, 0, 8, 128, 16, 2) == (512, 2)     # r = 1
+    assert oracle_mod.qcode_offset(1, 0, 16, 128, 16, 2) == (512, 4)    # dm = 1
+    assert oracle_mod.qcode_offset(0, 16, 0, 64, 32, 2) == (32 * 8, 0)  # head_dim 64: 8-byte units
 
 
-@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("bits", [8, 4, 2])
 def test_append_writes_only_its_slots(oracle_mod, bits):
     rng = np.random.default_rng(20 + bits)
     H, D, BS, nb = 2, 64, 16, 6
@@ -113,7 +128,8 @@ def test_append_writes_only_its_slots(oracle_mod, bits):
     mask = np.ones((nb, H, BS), bool)
     for (blk, slot) in written:
         mask[blk, :, slot] = False
-    assert np.array_equal(k[mask], k0[mask]) and np.array_equal(v[mask], v0[mask])
+    # untouched slots are byte-for-byte the filler (whose scales may decode to NaN)
+    assert np.array_equal(k[mask], k0[mask], equal_nan=True) and np.array_equal(v[mask], v0[mask], equal_nan=True)
 
 
 def _exact_batch(rng, bits, S=3, H=2, Hq=4, D=64, BS=16):
@@ -136,7 +152,7 @@ def _exact_batch(rng, bits, S=3, H=2, Hq=4, D=64, BS=16):
     return lens, bt, kv, nb
 
 
-@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("bits", [8, 4, 2])
 def test_quantised_attention_equals_bf16_attention_on_exact_data(oracle_mod, bits):
     rng = np.random.default_rng(30 + bits)
     H, Hq, D, BS = 2, 4, 64, 16
@@ -160,9 +176,11 @@ def test_quantised_attention_equals_bf16_attention_on_exact_data(oracle_mod, bit
         assert np.array_equal(got, ref)
 
 
-@pytest.mark.parametrize("bits,bound", [(8, 0.05), (4, 0.6)])
+@pytest.mark.parametrize("bits,bound", [(8, 0.05), (4, 0.6), (2, 3.5)])
 def test_quantised_attention_accuracy_cost(oracle_mod, bits, bound):
-    # random N(0,1) K/V: the codec's cost on the output stays small (loose, informative bound)
+    # random N(0,1) K/V: the codec's cost on the output (loose, informative bounds; ternary
+    # 2-bit codes with one scale per row keep only a Gaussian row's largest entries, so
+    # their cost is of the order of the output itself)
     rng = np.random.default_rng(40 + bits)
     H, Hq, D, BS, S, L = 2, 8, 128, 16, 2, 300
     nb = S * ((L + BS - 1) // BS)
