@@ -633,8 +633,8 @@ def main():
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="resize the batch (same per-sequence distribution); for profiling smaller cases")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kv-bits", type=int, choices=(16, 8, 4), default=16,
-                    help="16: bf16 K/V pools; 8 / 4: quantised KV blocks (Q8 / Q4 records)")
+    ap.add_argument("--kv-bits", type=int, choices=(16, 8, 4, 2), default=16,
+                    help="16: bf16 K/V pools; 8 / 4 / 2: quantised KV blocks (Q8 / Q4 / Q2 records)")
     ap.add_argument("--accept", choices=("greedy", "sampled", "sampled-topkp"), default="greedy",
                     help="verify workloads: greedy accept, keyed sampling at T = 1, min_p = 0.05, or the same "
                          "with top_k = 50 and top_p = 0.9")

@@ -386,11 +386,12 @@ int paged_attention_forward_gather(const pkv_pool *pool, const void *q, const in
 
 /*
  * Quantised KV blocks (TensorSharp "高级功能", section "内存优化", the KV block
- * codec item: blocks may be compressed in place to 8 or 4 bits per value, Q8 /
- * Q4, for half or a quarter of the footprint at a small accuracy cost).  The
+ * codec item: blocks may be compressed in place to 8, 4 or 2 bits per value,
+ * Q8 / Q4 / Q2, for a fraction of the footprint at an accuracy cost).  The
  * pages give no codec internals; this library's codec:
  *   each (token, KV head) row x of head_dim bf16 values is stored as one float32
- *   scale s = max_i |x_i| / Q (Q = 127 for 8 bits, 7 for 4 bits) and codes
+ *   scale s = max_i |x_i| / Q (Q = 2^(bits-1) - 1: 127 for 8 bits, 7 for 4 bits,
+ *   1 for 2 bits, whose codes are -1, 0, 1) and codes
  *   c_i = clamp(rint(x_i / s), -Q, Q) (all 0 when s == 0), every step a correctly
  *   rounded float32 operation (rint ties to even); it reads back as c_i * s.
  *   Non-finite inputs give unspecified (but in-range) codes.
@@ -399,6 +400,7 @@ int paged_attention_forward_gather(const pkv_pool *pool, const void *q, const in
  *   C = block_size * head_dim * bits / 8 bytes of codes per section; the K scale
  *   of slot t at byte 2C + 4t, the V scale at 2C + 4 block_size + 4t (float32).
  *   8-bit codes: bytes holding c + 128.  4-bit codes: nibbles holding c + 8.
+ *   2-bit codes: bit pairs holding c + 2.
  *   Position of the code of slot t, dim i (16-byte units of 4 little-endian
  *   32-bit words, laid out in the order the attention kernel's tensor-core
  *   operands consume them):
@@ -406,10 +408,12 @@ int paged_attention_forward_gather(const pkv_pool *pool, const void *q, const in
  *      c = (s%8)/2, h = s/8, e = s%2, u = 4g + c
  *      8-bit: byte ((mt*(D/32) + j/2)*32 + u)*16 + ((j%2)*2 + r)*4 + h + 2e
  *      4-bit: word ((mt*(D/64) + j/4)*32 + u)*16 + (j%4)*4, bits 4(2r + h) + 16e
+ *      2-bit: word (mt*32 + u)*(D/8) + (j/2)*4, bits 8r + 2(2(j%2) + h) + 16e
  *   V: kk = t/16, m = (t%16)/2 + 8(t%2), h = m/8, c = (m%8)/2, e = m%2,
  *      dm = i/16, g = i%8, r = (i%16)/8, u = 4g + c
  *      8-bit: byte C + ((kk*(D/32) + dm/2)*32 + u)*16 + ((dm%2)*2 + r)*4 + h + 2e
  *      4-bit: word C + ((kk*(D/64) + dm/4)*32 + u)*16 + (dm%4)*4, bits 4(2h + r) + 16e
+ *      2-bit: word C + (kk*32 + u)*(D/8) + (dm/2)*4, bits 8h + 2(2(dm%2) + r) + 16e
  *   (D = head_dim).  A byte never holds codes of two slots.
  * Built for head_dim 64 / 128 and block_size 16 / 32.
  */
@@ -419,7 +423,7 @@ typedef struct pkv_qpool {
     int32_t block_size;
     int32_t num_kv_heads;
     int32_t head_dim;
-    int32_t bits;   /* 8 or 4 */
+    int32_t bits;   /* 8, 4 or 2 */
 } pkv_qpool;
 
 /* Bytes of one (block, KV head) record; 0 for unsupported arguments. */

@@ -40,9 +40,9 @@
 //  * Bounded waits only; block ids and lengths are range-checked on the device
 //    (clamped + status bit, never a fault).
 //  * Quantised KV blocks (TensorSharp "高级功能", section "内存优化", the KV block
-//    codec item): the same kernel with BITS = 8 or 4 reads one record per
+//    codec item): the same kernel with BITS = 8, 4 or 2 reads one record per
 //    (block, KV head) with a single bulk copy (codes of K and V + per-key
-//    scales), widens the codes to bf16 in registers, folds each key's K scale
+//    scales), widens the codes to f16 in registers, folds each key's K scale
 //    into its score and its V scale into its weight.
 #pragma once
 
@@ -134,31 +134,51 @@ __device__ __forceinline__ uint32_t tile_off(int tok, int ch)
 // operand uses column s = key 16 kk + (s < 8 ? 2s : 2(s - 8) + 1), the order in
 // which the transposed P^T fragment of K's S^T arrives.  8-bit codes are bytes of
 // c + 128 (word bytes 0, 2 feed a0/a1, bytes 1, 3 feed a2/a3); 4-bit codes are
-// nibbles holding c + 8.  Full byte-level formula in pkv.h.
+// nibbles holding c + 8; 2-bit codes are bit pairs holding c + 2, one lane's codes
+// of a 16-key group in D / 8 contiguous bytes (two k-steps per word, a byte per
+// key).  Full byte-level formula in pkv.h.
 template <int D, int BS, int BITS>
 struct QRec {
     static constexpr int kCodeBytes = BS * D * BITS / 8;          // one section
     static constexpr int kK = 0, kV = kCodeBytes;
     static constexpr int kKs = 2 * kCodeBytes, kVs = 2 * kCodeBytes + 4 * BS;
     static constexpr int kBytes = 2 * kCodeBytes + 8 * BS;
-    static constexpr int kUnits = BITS == 8 ? D / 32 : D / 64;    // 16-byte units per lane per 16 keys
-    static_assert(BITS == 8 || BITS == 4, "codec width");
+    static constexpr int kWords = D * BITS / 64;                  // 32-bit words per lane per 16 keys
+    static constexpr int kGroupBytes = kWords * 4 * 32;           // a 16-key group of one section
+    static_assert(BITS == 8 || BITS == 4 || BITS == 2, "codec width");
     static_assert(kBytes % 16 == 0, "record must stay 16-byte aligned");
 };
 
-__device__ __forceinline__ uint32_t word_of(const uint4 &u, int i)
+// The lane's words of one 16-key group (g: the group's first byte): 16-byte units
+// interleaved across the warp for 8 / 4 bits, one contiguous run for 2 bits.
+template <int D, int BITS>
+__device__ __forceinline__ void load_group(const uint8_t *g, int lane, uint32_t (&w)[D * BITS / 64])
 {
-    return i == 0 ? u.x : i == 1 ? u.y : i == 2 ? u.z : u.w;
+    constexpr int NW = D * BITS / 64;
+    if constexpr (BITS == 2 && NW == 2) {
+        const uint2 u = *reinterpret_cast<const uint2 *>(g + lane * 8);
+        w[0] = u.x;
+        w[1] = u.y;
+    } else {
+#pragma unroll
+        for (int k = 0; k < NW / 4; ++k) {
+            const uint4 u = *reinterpret_cast<const uint4 *>(g + (BITS == 2 ? lane * 16 : (k * 32 + lane) * 16));
+            w[4 * k] = u.x;
+            w[4 * k + 1] = u.y;
+            w[4 * k + 2] = u.z;
+            w[4 * k + 3] = u.w;
+        }
+    }
 }
 
 // Codes become f16 operands without arithmetic: f16 bits 0x6400 | u are 1024 + u for a
-// byte u (0..255), and bits 0x4C00 | (u << 6) are 16 + u for a nibble u (0..15), so
-// putting a stored u = c + 128 (or c + 8) under those exponent bits yields c + kBias
-// exactly.  The tensor core then computes q . (c + kBias) and P . (c + kBias); the
+// byte u (0..255), and bits 0x4C00 | (u << 6) are 16 + u for a nibble or bit pair u
+// (0..15), so putting a stored u = c + 128 (c + 8, c + 2) under those exponent bits
+// yields c + kBias exactly.  The tensor core then computes q . (c + kBias) and P . (c + kBias); the
 // kernel removes kBias * sum(q) from each score and kBias * sum(P) from each output
 // row, in fp32.
 template <int BITS>
-constexpr float kBias = BITS == 8 ? 1152.f : 24.f;   // 1024 + 128, 16 + 8
+constexpr float kBias = BITS == 8 ? 1152.f : BITS == 4 ? 24.f : 18.f;   // 1024 + 128, 16 + 8, 16 + 2
 
 // nibble pair P (bits 4P and 16 + 4P of w) -> f16x2 of 16 + u
 template <int P>
@@ -168,20 +188,35 @@ __device__ __forceinline__ uint32_t nib_pair(uint32_t w)
     return (x & 0x03C003C0u) | 0x4C004C00u;
 }
 
+// bit pair at bits b and 16 + b of w -> f16x2 of 16 + u
+__device__ __forceinline__ uint32_t bit_pair(uint32_t w, int b)
+{
+    const uint32_t x = b <= 6 ? w << (6 - b) : w >> (b - 6);
+    return (x & 0x00C000C0u) | 0x4C004C00u;
+}
+
 // A operand of k-step ks of a K tile, or of 16-dim m-tile ks of a V^T tile, from the
-// lane's units of that 16-key group.
-template <int BITS, bool IS_V>
-__device__ __forceinline__ void q_frag(const uint4 *un, int ks, uint32_t (&a)[4])
+// lane's words of that 16-key group.
+template <int BITS, bool IS_V, int NW>
+__device__ __forceinline__ void q_frag(const uint32_t (&cw)[NW], int ks, uint32_t (&a)[4])
 {
     if constexpr (BITS == 8) {
-        const uint4 &u = un[ks >> 1];
-        const uint32_t w0 = word_of(u, (ks & 1) * 2), w1 = word_of(u, (ks & 1) * 2 + 1);
+        const uint32_t w0 = cw[2 * ks], w1 = cw[2 * ks + 1];
         a[0] = __byte_perm(w0, 0x64646464u, 0x4240);   // bytes 0, 2
         a[1] = __byte_perm(w1, 0x64646464u, 0x4240);
         a[2] = __byte_perm(w0, 0x64646464u, 0x4341);   // bytes 1, 3
         a[3] = __byte_perm(w1, 0x64646464u, 0x4341);
+    } else if constexpr (BITS == 2) {
+        // k-step parity q picks bits 4q..4q+3 of each byte; K: byte r (A row half), pair
+        // h (A column half); V: byte h, pair r
+        const uint32_t w = cw[ks >> 1];
+        const int q4 = 4 * (ks & 1);
+        a[0] = bit_pair(w, q4);
+        a[1] = bit_pair(w, IS_V ? q4 + 2 : q4 + 8);
+        a[2] = bit_pair(w, IS_V ? q4 + 8 : q4 + 2);
+        a[3] = bit_pair(w, q4 + 10);
     } else {
-        const uint32_t w = word_of(un[ks >> 2], ks & 3);
+        const uint32_t w = cw[ks];
         // nibble pair p sits at bits 4p and 16 + 4p; K: p = 2r + h, V: p = 2h + r
         // (r: A row half, h: A column half)
         a[0] = nib_pair<0>(w);
@@ -195,7 +230,7 @@ __device__ __forceinline__ void q_frag(const uint4 *un, int ks, uint32_t (&a)[4]
 // up to 8 * NN * NMT rows (the G q heads of one KV head times the sequence's rows).
 // TREE: rows carry ancestor masks over the window keys (tree verify); a separate
 // instantiation so the decode / causal path carries no mask test.
-// BITS: 16 = bf16 pools read by TMA tiles; 8 / 4 = quantised records, one bulk copy
+// BITS: 16 = bf16 pools read by TMA tiles; 8 / 4 / 2 = quantised records, one bulk copy
 // per (block, KV head), codes widened to f16 in registers.
 // KW: consumer warps that share each row group's keys: warp (kw, mw) takes the split's
 // blocks kw, kw + KW, ... for the rows of row warp mw, with its own softmax state; the
@@ -606,14 +641,12 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                     const int mi = mt % MT;
                     kscale[mt] = *reinterpret_cast<const float2 *>(rm + QR::kKs + (mi * 16 + 2 * kr) * 4);
                     vscale[mt] = *reinterpret_cast<const float2 *>(rm + QR::kVs + (mi * 16 + 2 * kr) * 4);
-                    uint4 un[QR::kUnits];
-#pragma unroll
-                    for (int u = 0; u < QR::kUnits; ++u)
-                        un[u] = *reinterpret_cast<const uint4 *>(rm + QR::kK + ((mi * QR::kUnits + u) * 32 + lane) * 16);
+                    uint32_t cw[QR::kWords];
+                    load_group<D, BITS>(rm + QR::kK + mi * QR::kGroupBytes, lane, cw);
 #pragma unroll
                     for (int ks = 0; ks < KS; ++ks) {
                         uint32_t a[4];
-                        q_frag<BITS, false>(un, ks, a);
+                        q_frag<BITS, false>(cw, ks, a);
 #pragma unroll
                         for (int nn = 0; nn < NN; ++nn) {
                             const int chain = ks % kQkChains;
@@ -765,15 +798,12 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                 }
                 if constexpr (BITS != 16) {
                     using QR = QRec<D, BS, BITS>;
-                    uint4 un[QR::kUnits];
-#pragma unroll
-                    for (int u = 0; u < QR::kUnits; ++u)
-                        un[u] = *reinterpret_cast<const uint4 *>(rec + (kk / MT) * RECB + QR::kV +
-                                                                 (((kk % MT) * QR::kUnits + u) * 32 + lane) * 16);
+                    uint32_t cw[QR::kWords];
+                    load_group<D, BITS>(rec + (kk / MT) * RECB + QR::kV + (kk % MT) * QR::kGroupBytes, lane, cw);
 #pragma unroll
                     for (int dm = 0; dm < DM; ++dm) {
                         uint32_t a[4];
-                        q_frag<BITS, true>(un, dm, a);
+                        q_frag<BITS, true>(cw, dm, a);
 #pragma unroll
                         for (int nn = 0; nn < NN; ++nn) {
                             float part[4] = {0.f, 0.f, 0.f, 0.f};

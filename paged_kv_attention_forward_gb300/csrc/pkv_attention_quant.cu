@@ -2,10 +2,10 @@
 // attention over the record pool.
 //
 // TensorSharp "高级功能", section "内存优化", the KV block codec item: blocks may be
-// compressed in place to 8 or 4 bits per value (Q8 / Q4), trading a small accuracy
-// cost for half or a quarter of the footprint.  The codec built here (the pages give
-// none): each (token, KV head) row of head_dim values gets one float32 scale
-// s = max|x| / Q (Q = 127 or 7) and codes c = clamp(rint(x / s), -Q, Q), every step
+// compressed in place to 8, 4 or 2 bits per value (Q8 / Q4 / Q2), trading a small
+// accuracy cost for the footprint.  The codec built here (the pages give none): each
+// (token, KV head) row of head_dim values gets one float32 scale s = max|x| / Q
+// (Q = 2^(bits-1) - 1: 127, 7 or 1) and codes c = clamp(rint(x / s), -Q, Q), every step
 // a correctly rounded float32 operation; the value read back is c * s.  The record
 // layout (pkv.h) keeps each (block, KV head) in one contiguous record, so the
 // attention kernel fetches a block with a single bulk copy.
@@ -15,7 +15,9 @@ namespace pkv {
 namespace {
 
 // Byte of a record holding the code of (slot t, dim i): K section, then V section
-// (for 4-bit codes the byte of the nibble; the nibble pairs dims i and i + 8).
+// (for 4-bit codes the byte of the nibble; the nibble pairs dims i and i + 8; for
+// 2-bit codes the byte of the bit pair, shared by dims i, i + 8, i + 16, i + 24 for K
+// and by dims i, i + 8, i + 16, i + 24 of the same row half for V).
 template <int BITS>
 __device__ __forceinline__ uint32_t k_code_byte(int t, int i, int D)
 {
@@ -23,6 +25,8 @@ __device__ __forceinline__ uint32_t k_code_byte(int t, int i, int D)
     const int j = i >> 4, s = i & 15, c = (s & 7) >> 1, h = s >> 3, e = s & 1, u = 4 * g + c;
     if constexpr (BITS == 8)
         return ((mt * (D / 32) + (j >> 1)) * 32 + u) * 16 + ((j & 1) * 2 + r) * 4 + h + 2 * e;
+    else if constexpr (BITS == 2)
+        return (mt * 32 + u) * (D / 8) + (j >> 1) * 4 + r + 2 * e;
     else
         return ((mt * (D / 64) + (j >> 2)) * 32 + u) * 16 + (j & 3) * 4 + ((4 * (2 * r + h) + 16 * e) >> 3);
 }
@@ -36,6 +40,8 @@ __device__ __forceinline__ uint32_t v_code_byte(int t, int i, int D, int BS)
     const uint32_t C = (uint32_t)BS * D * BITS / 8;
     if constexpr (BITS == 8)
         return C + ((kk * (D / 32) + (dm >> 1)) * 32 + u) * 16 + ((dm & 1) * 2 + r) * 4 + h + 2 * e;
+    else if constexpr (BITS == 2)
+        return C + (kk * 32 + u) * (D / 8) + (dm >> 1) * 4 + h + 2 * e;
     else
         return C + ((kk * (D / 64) + (dm >> 2)) * 32 + u) * 16 + (dm & 3) * 4 + ((4 * (2 * h + r) + 16 * e) >> 3);
 }
@@ -119,7 +125,7 @@ paged_kv_append_quant_kernel(uint8_t *__restrict__ records, const uint16_t *__re
         av = fmaxf(av, __shfl_xor_sync(0xffffffffu, av, off));
     }
     __syncwarp();
-    const float Q = BITS == 8 ? 127.f : 7.f;
+    const float Q = BITS == 8 ? 127.f : BITS == 4 ? 7.f : 1.f;
     const float sk = __fdiv_rn(ak, Q), sv = __fdiv_rn(av, Q);
     uint8_t *rec = records + ((size_t)blk * num_kv_heads + h) * rec_bytes;
     const int t = (int)(p % block_size);
@@ -127,6 +133,23 @@ paged_kv_append_quant_kernel(uint8_t *__restrict__ records, const uint16_t *__re
         for (int i = lane; i < D; i += 32) {
             rec[k_code_byte<8>(t, i, D)] = q8_byte(quant_code(xs[wib][0][i], sk, Q));
             rec[v_code_byte<8>(t, i, D, block_size)] = q8_byte(quant_code(xs[wib][1][i], sv, Q));
+        }
+    } else if constexpr (BITS == 2) {
+        // byte task k: K dims 32 (k/8) + 2 ((k%8)/2) + k%2 + {0, 8, 16, 24} (the k-step pair's
+        // h and parity, bit pairs 2 (2q + h)); V dims 32 (k/8) + k%8 + {0, 8, 16, 24} (r and
+        // parity, bit pairs 2 (2q + r))
+        for (int k = lane; k < D / 4; k += 32) {
+            const int ik = 32 * (k >> 3) + 2 * ((k & 7) >> 1) + (k & 1);
+            const int iv = 32 * (k >> 3) + (k & 7);
+            uint32_t bk = 0, bv = 0;
+#pragma unroll
+            for (int f = 0; f < 4; ++f) {   // f = 2q + (h or r): dim offset 16 q + 8 (h or r)
+                const int off = 16 * (f >> 1) + 8 * (f & 1);
+                bk |= (uint32_t)(quant_code(xs[wib][0][ik + off], sk, Q) + 2) << (2 * f);
+                bv |= (uint32_t)(quant_code(xs[wib][1][iv + off], sv, Q) + 2) << (2 * f);
+            }
+            rec[k_code_byte<2>(t, ik, D)] = (uint8_t)bk;
+            rec[v_code_byte<2>(t, iv, D, block_size)] = (uint8_t)bv;
         }
     } else {
         // byte task k: K dims (16 (k/8) + 2 ((k%8)/2) + k%2, + 8); V dims (16 (k/8) + k%8, + 8)
@@ -157,6 +180,12 @@ int launch_quant(const PoolView &pv, AttnParams &prm, int rows, long long pairs,
         if (D == 128 && BS == 16) return launch_d_bs<128, 16, 8, false>(rows, none, none, prm, pairs, n_max, st);
         return launch_d_bs<128, 32, 8, false>(rows, none, none, prm, pairs, n_max, st);
     }
+    if (pv.bits == 2) {
+        if (D == 64 && BS == 16) return launch_d_bs<64, 16, 2, false>(rows, none, none, prm, pairs, n_max, st);
+        if (D == 64 && BS == 32) return launch_d_bs<64, 32, 2, false>(rows, none, none, prm, pairs, n_max, st);
+        if (D == 128 && BS == 16) return launch_d_bs<128, 16, 2, false>(rows, none, none, prm, pairs, n_max, st);
+        return launch_d_bs<128, 32, 2, false>(rows, none, none, prm, pairs, n_max, st);
+    }
     if (D == 64 && BS == 16) return launch_d_bs<64, 16, 4, false>(rows, none, none, prm, pairs, n_max, st);
     if (D == 64 && BS == 32) return launch_d_bs<64, 32, 4, false>(rows, none, none, prm, pairs, n_max, st);
     if (D == 128 && BS == 16) return launch_d_bs<128, 16, 4, false>(rows, none, none, prm, pairs, n_max, st);
@@ -168,7 +197,7 @@ int launch_quant(const PoolView &pv, AttnParams &prm, int rows, long long pairs,
 
 extern "C" size_t pkv_qrecord_bytes(int32_t block_size, int32_t head_dim, int32_t bits)
 {
-    if (block_size <= 0 || head_dim <= 0 || (bits != 8 && bits != 4))
+    if (block_size <= 0 || head_dim <= 0 || (bits != 8 && bits != 4 && bits != 2))
         return 0;
     return 2 * (size_t)block_size * head_dim * bits / 8 + 8 * (size_t)block_size;
 }
@@ -186,8 +215,8 @@ extern "C" int paged_kv_append_quant(const pkv_qpool *pool, const int32_t *block
         return set_error(PKV_ERR_SHAPE, "paged_kv_append_quant: negative sizes or max_blocks_per_seq <= 0");
     if (pool->num_blocks <= 0 || pool->num_kv_heads <= 0)
         return set_error(PKV_ERR_SHAPE, "paged_kv_append_quant: pool dimensions must be positive");
-    if (pool->bits != 8 && pool->bits != 4)
-        return set_error(PKV_ERR_UNSUPPORTED, "paged_kv_append_quant: bits %d (built: 8, 4)", pool->bits);
+    if (pool->bits != 8 && pool->bits != 4 && pool->bits != 2)
+        return set_error(PKV_ERR_UNSUPPORTED, "paged_kv_append_quant: bits %d (built: 8, 4, 2)", pool->bits);
     if (!(pool->head_dim == 64 || pool->head_dim == 128) || !(pool->block_size == 16 || pool->block_size == 32))
         return set_error(PKV_ERR_UNSUPPORTED,
                          "paged_kv_append_quant: head_dim %d / block_size %d (built: 64 or 128 / 16 or 32)",
@@ -208,7 +237,8 @@ extern "C" int paged_kv_append_quant(const pkv_qpool *pool, const int32_t *block
         return set_error(PKV_ERR_SHAPE, "paged_kv_append_quant: too many rows");
     const int rb = (int)pkv_qrecord_bytes(pool->block_size, pool->head_dim, pool->bits);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    auto kern = pool->bits == 8 ? paged_kv_append_quant_kernel<8> : paged_kv_append_quant_kernel<4>;
+    auto kern = pool->bits == 8 ? paged_kv_append_quant_kernel<8>
+              : pool->bits == 4 ? paged_kv_append_quant_kernel<4> : paged_kv_append_quant_kernel<2>;
     kern<<<(unsigned)blocks, 128, 0, st>>>(static_cast<uint8_t *>(pool->records),
                                            static_cast<const uint16_t *>(k_new), static_cast<const uint16_t *>(v_new),
                                            block_tables, max_blocks_per_seq, context_lens_old, new_starts, num_seqs,
@@ -231,8 +261,8 @@ extern "C" int paged_attention_forward_quant(const pkv_qpool *pool, const void *
     const char *who = "paged_attention_forward_quant";
     if (!pool)
         return set_error(PKV_ERR_NULL, "%s: pool is NULL", who);
-    if (pool->bits != 8 && pool->bits != 4)
-        return set_error(PKV_ERR_UNSUPPORTED, "%s: bits %d (built: 8, 4)", who, pool->bits);
+    if (pool->bits != 8 && pool->bits != 4 && pool->bits != 2)
+        return set_error(PKV_ERR_UNSUPPORTED, "%s: bits %d (built: 8, 4, 2)", who, pool->bits);
     PoolView pv = {pool->num_blocks, pool->block_size, pool->num_kv_heads, pool->head_dim, pool->bits,
                    nullptr, nullptr, pool->records};
     return attention_run(who, pv, q, q_starts, block_tables, max_blocks_per_seq, context_lens, num_seqs,

@@ -460,10 +460,10 @@ def record_bytes(block_size: int, head_dim: int, bits: int) -> int:
 def random_records(seed, batch: PagedBatch, bits: int, layers: int = 1, filler: str = "random"):
     """A quantised pool with the batch's geometry: uint8 [layers, num_blocks, H_kv, record].
 
-    Codes are independent draws of a rounded N(0, (Q/3)^2) clipped to [-Q, Q] (Q = 127 or
-    7), stored in the codec's byte encoding (8 bits: bytes of c + 128; 4 bits: two
-    nibbles of c + 8 per byte); since every code is drawn alike, where a code sits in
-    the record does not matter.  Scales are float32 uniform in [0.5, 1.5) * 3 / Q, so
+    Codes are independent draws of a rounded N(0, (Q/3)^2) clipped to [-Q, Q] (Q = 127, 7
+    or 1), stored in the codec's byte encoding (8 bits: bytes of c + 128; 4 bits: two
+    nibbles of c + 8 per byte; 2 bits: four bit pairs of c + 2 per byte); since every
+    code is drawn alike, where a code sits in the record does not matter.  Scales are float32 uniform in [0.5, 1.5) * 3 / Q, so
     values are about N(0, 1) like the bf16 workloads.  filler "nan" stores NaN scales
     in every slot no cached token owns (pool slack, block tails, slots awaiting the
     append)."""
@@ -472,15 +472,18 @@ def random_records(seed, batch: PagedBatch, bits: int, layers: int = 1, filler: 
     nb = batch.k_pool.shape[1] if batch.k_pool is not None else int(batch.block_tables.max()) + 1
     C = B * D * bits // 8
     rb = record_bytes(B, D, bits)
-    q = 127 if bits == 8 else 7
+    q = (1 << (bits - 1)) - 1
     rec = np.empty((layers, nb, H, rb), dtype=np.uint8)
     codes = normal_f32(s_codes, (layers, nb, H, 2 * C * (8 // bits)), std=q / 3.0)
     codes = np.clip(np.rint(codes), -q, q).astype(np.int16)
     if bits == 8:
         rec[..., :2 * C] = (codes + 128).astype(np.uint8)
-    else:
+    elif bits == 4:
         nib = (codes + 8).astype(np.uint8)
         rec[..., :2 * C] = nib[..., 0::2] | (nib[..., 1::2] << 4)
+    else:
+        f = (codes + 2).astype(np.uint8)
+        rec[..., :2 * C] = f[..., 0::4] | (f[..., 1::4] << 2) | (f[..., 2::4] << 4) | (f[..., 3::4] << 6)
     del codes
     rng = np.random.Generator(np.random.PCG64(s_scales))
     scales = ((0.5 + rng.random((layers, nb, H, 2, B))) * (3.0 / q)).astype(np.float32)

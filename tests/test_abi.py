@@ -103,6 +103,8 @@ def test_host_validation_without_device(pkv):
     # quantised pool: record size and the checks made before any CUDA call
     assert lib.pkv_qrecord_bytes(16, 128, 8) == 2 * 16 * 128 + 8 * 16
     assert lib.pkv_qrecord_bytes(32, 64, 4) == 2 * 32 * 32 + 8 * 32
+    assert lib.pkv_qrecord_bytes(16, 64, 2) == 2 * 16 * 16 + 8 * 16
+    assert lib.pkv_qrecord_bytes(16, 128, 2) == 2 * 16 * 32 + 8 * 16
     assert lib.pkv_qrecord_bytes(16, 128, 5) == 0
     qp = pkv._QPool(4096, 10, 16, 2, 128, 6)
     assert lib.paged_kv_append_quant(ctypes.byref(qp), 4096, 4, 4096, 4096, 4096, 4096, 1, 1, None) == -3

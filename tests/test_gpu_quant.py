@@ -1,4 +1,4 @@
-"""GPU parity of the quantised KV path (Q8 / Q4 records) against the float64 oracle.
+"""GPU parity of the quantised KV path (Q8 / Q4 / Q2 records) against the float64 oracle.
 
 TensorSharp "高级功能", section "内存优化", the KV block codec item.  Bars: the
 quantising append bit-exact (codes and scales, byte for byte); attention max-abs
@@ -16,7 +16,7 @@ from _helpers import assert_close_to_oracle, dev, dev_bf16, host_bits
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
-BITS = [8, 4]
+BITS = [8, 4, 2]
 
 
 @pytest.fixture(scope="module")
