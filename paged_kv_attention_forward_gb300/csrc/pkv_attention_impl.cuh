@@ -80,6 +80,16 @@ constexpr int kQkChainsOf = BITS == 16 ? PKV_QK_CHAINS_BF16 : PKV_QK_CHAINS_QUAN
 #define PKV_QUANT_RECS_PER_STAGE 2
 #endif
 static_assert(PKV_QUANT_RECS_PER_STAGE == 1 || PKV_QUANT_RECS_PER_STAGE == 2, "records per stage");
+// 16-key bf16 blocks per ring stage (1 or 2).  This sets the granularity of the online
+// softmax update, so it is one constant for every CTA shape (decode, verify, prefill,
+// gather): a verify row must take the same steps as the same row decoded alone.
+#ifndef PKV_BF16_BLOCKS_PER_STAGE
+#define PKV_BF16_BLOCKS_PER_STAGE 1
+#endif
+static_assert(PKV_BF16_BLOCKS_PER_STAGE == 1 || PKV_BF16_BLOCKS_PER_STAGE == 2, "bf16 blocks per stage");
+// blocks per ring stage: 32-key blocks always go one at a time
+template <int BITS, int BS>
+constexpr int kBlocksPerStage = BS != 16 ? 1 : BITS != 16 ? PKV_QUANT_RECS_PER_STAGE : PKV_BF16_BLOCKS_PER_STAGE;
 static_assert((PKV_QK_CHAINS_BF16 == 2 || PKV_QK_CHAINS_BF16 == 4) &&
               (PKV_QK_CHAINS_QUANT == 2 || PKV_QK_CHAINS_QUANT == 4), "QK chains");
 
@@ -255,9 +265,9 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
     constexpr int kQkChains = kQkChainsOf<BITS>;
     using T = Tile<D, BS>;
     constexpr int MT = BS / 16;   // 16-key m-tiles per block
-    // blocks per ring stage: quantised 16-key records go two at a time, so the per-stage
+    // blocks per ring stage: 16-key blocks may go two at a time, so the per-stage
     // softmax bookkeeping is paid once per 32 keys
-    constexpr int TB = (BITS != 16 && BS == 16) ? PKV_QUANT_RECS_PER_STAGE : 1;
+    constexpr int TB = kBlocksPerStage<BITS, BS>;
     constexpr int MTE = MT * TB;  // 16-key m-tiles per stage
     constexpr int KS = D / 16;    // k-steps of K q^T
     constexpr int DM = D / 16;    // 16-dim m-tiles of V^T P^T
@@ -269,9 +279,9 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
     constexpr int RECB = QRec<D, BS, (BITS == 16 ? 8 : BITS)>::kBytes;
-    constexpr int STAGE = BITS == 16 ? 2 * T::kTileBytes : TB * RECB;
-    uint8_t *k_tiles = smem;                          // bf16: K tiles of every stage, then V tiles
-    uint8_t *v_tiles = smem + NST * T::kTileBytes;    // quantised: one record per stage
+    constexpr int STAGE = BITS == 16 ? 2 * TB * T::kTileBytes : TB * RECB;
+    uint8_t *k_tiles = smem;                              // bf16: the TB K tiles of every stage,
+    uint8_t *v_tiles = smem + NST * TB * T::kTileBytes;   // then the V tiles; quantised: TB records per stage
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + NST * STAGE);
     uint64_t *empty = full + NST;
     volatile int32_t *s_flag = reinterpret_cast<volatile int32_t *>(empty + NST);
@@ -388,7 +398,7 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
         }
         __syncwarp();
         int k = 0;
-        for (; k < nblk; ++k) {
+        for (; k < nstage; ++k) {
             const int st = k % NST;
             bool ok = true;
             if (k >= NST)
@@ -402,16 +412,20 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                 }
                 break;
             }
-            uint8_t *kt = k_tiles + st * T::kTileBytes;
-            uint8_t *vt = v_tiles + st * T::kTileBytes;
 #pragma unroll
-            for (int i = 0; i < KPL; ++i) {
-                const int key = kq + i * KSTEP;
-                if (t0 + k * 16 + key < t1) {   // entries past the list's end are masked, not copied
-                    const unsigned long long o = g_off[k * 16 + key];
-                    const bool vld = o != kGatherBad;   // a bad entry copies zeros from the pool's start
-                    cp_async_16(kt + tile_off<16>(key, ch), p.kpool + (vld ? o : 0ull) + ch * 8, vld ? 16u : 0u);
-                    cp_async_16(vt + tile_off<16>(key, ch), p.vpool + (vld ? o : 0ull) + ch * 8, vld ? 16u : 0u);
+            for (int b = 0; b < TB; ++b) {
+                const int tt = k * TB + b;   // 16-entry tile of the slice
+                uint8_t *kt = k_tiles + (st * TB + b) * T::kTileBytes;
+                uint8_t *vt = v_tiles + (st * TB + b) * T::kTileBytes;
+#pragma unroll
+                for (int i = 0; i < KPL; ++i) {
+                    const int key = kq + i * KSTEP;
+                    if (t0 + tt * 16 + key < t1) {   // entries past the list's end are masked, not copied
+                        const unsigned long long o = g_off[tt * 16 + key];
+                        const bool vld = o != kGatherBad;   // a bad entry copies zeros from the pool's start
+                        cp_async_16(kt + tile_off<16>(key, ch), p.kpool + (vld ? o : 0ull) + ch * 8, vld ? 16u : 0u);
+                        cp_async_16(vt + tile_off<16>(key, ch), p.vpool + (vld ? o : 0ull) + ch * 8, vld ? 16u : 0u);
+                    }
                 }
             }
             cp_async_arrive(&full[st]);
@@ -464,12 +478,23 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                     s_flag[1] = 1;
                     stop = true;
                 } else if constexpr (BITS == 16) {
-                    const int y = (blks[0] * p.num_kv_heads + g) * BS;
-                    mbar_arrive_expect_tx(&full[st], 2 * T::kTileBytes);
+                    uint32_t bytes = 0;
 #pragma unroll
-                    for (int h = 0; h < T::kHalves; ++h) {
-                        tma_load_2d(k_tiles + st * T::kTileBytes + h * T::kBoxBytes, &tm_k, &full[st], h * 64, y);
-                        tma_load_2d(v_tiles + st * T::kTileBytes + h * T::kBoxBytes, &tm_v, &full[st], h * 64, y);
+                    for (int i = 0; i < TB; ++i)
+                        bytes += blks[i] >= 0 ? 2 * T::kTileBytes : 0;
+                    mbar_arrive_expect_tx(&full[st], bytes);
+#pragma unroll
+                    for (int i = 0; i < TB; ++i) {
+                        if (blks[i] < 0)   // past the split's last block: the keys are masked
+                            continue;
+                        const int y = (blks[i] * p.num_kv_heads + g) * BS;
+                        uint8_t *kt = k_tiles + (st * TB + i) * T::kTileBytes;
+                        uint8_t *vt = v_tiles + (st * TB + i) * T::kTileBytes;
+#pragma unroll
+                        for (int h = 0; h < T::kHalves; ++h) {
+                            tma_load_2d(kt + h * T::kBoxBytes, &tm_k, &full[st], h * 64, y);
+                            tma_load_2d(vt + h * T::kBoxBytes, &tm_v, &full[st], h * 64, y);
+                        }
                     }
                 } else {
                     uint32_t bytes = 0;
@@ -602,8 +627,8 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                 }
                 break;
             }
-            const uint32_t kb = smem_addr(k_tiles + st * T::kTileBytes);
-            const uint32_t vb = smem_addr(v_tiles + st * T::kTileBytes);
+            const uint32_t kb = smem_addr(k_tiles + st * TB * T::kTileBytes);   // m-tile mt: tile mt / MT
+            const uint32_t vb = smem_addr(v_tiles + st * TB * T::kTileBytes);
             const uint8_t *rec = smem + st * STAGE;   // quantised record of this stage
             const int tbase = (blk0 + k * TB) * BS;
 
@@ -624,7 +649,8 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
                     for (int mt = 0; mt < MTE; ++mt) {
                         uint32_t a[4];
-                        ldsm_x4(kb + tile_off<BS>(mt * 16 + k_key, ks * 2 + k_chs), a[0], a[1], a[2], a[3]);
+                        ldsm_x4(kb + (mt / MT) * T::kTileBytes + tile_off<BS>((mt % MT) * 16 + k_key, ks * 2 + k_chs),
+                                a[0], a[1], a[2], a[3]);
 #pragma unroll
                         for (int nn = 0; nn < NN; ++nn) {
                             const int chain = ks % kQkChains;
@@ -823,7 +849,8 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
                     for (int dm = 0; dm < DM; ++dm) {
                         uint32_t a[4];
-                        ldsm_x4_trans(vb + tile_off<BS>(kk * 16 + v_key, dm * 2 + v_chs), a[0], a[1], a[2], a[3]);
+                        ldsm_x4_trans(vb + (kk / MT) * T::kTileBytes + tile_off<BS>((kk % MT) * 16 + v_key, dm * 2 + v_chs),
+                                      a[0], a[1], a[2], a[3]);
                         a[0] &= mlo;
                         a[1] &= mlo;
                         a[2] &= mhi;
@@ -1177,8 +1204,8 @@ constexpr int kStages()
     constexpr int base = DEEP ? PKV_STAGES_DEEP
                               : BITS != 16 ? PKV_STAGES_QUANT : NMT == 1 ? PKV_STAGES_DECODE : PKV_STAGES_WIDE;
     // the KW - 1 key shares' states pass through the ring at the end: make it big enough
-    constexpr int tb = (BITS != 16 && BS == 16) ? PKV_QUANT_RECS_PER_STAGE : 1;
-    constexpr int stage = BITS == 16 ? 2 * Tile<D, BS>::kTileBytes : tb * QRec<D, BS, (BITS == 16 ? 8 : BITS)>::kBytes;
+    constexpr int tb = kBlocksPerStage<BITS, BS>;
+    constexpr int stage = BITS == 16 ? 2 * tb * Tile<D, BS>::kTileBytes : tb * QRec<D, BS, (BITS == 16 ? 8 : BITS)>::kBytes;
     constexpr int merge = (kKeyWarps<BITS>() - 1) * NMT * (D / 16 * 4 + 6) * NN * 32 * 4;
     constexpr int need = (merge + stage - 1) / stage;
     constexpr int kw = kKeyWarps<BITS>();
@@ -1197,8 +1224,8 @@ template <int D, int BS, int NN, int NMT, int BITS, bool DEEP = false, bool GATH
 size_t smem_bytes()
 {
     constexpr int NST = kStages<D, BS, NN, NMT, BITS, DEEP>();
-    constexpr size_t tb = (BITS != 16 && BS == 16) ? PKV_QUANT_RECS_PER_STAGE : 1;
-    constexpr size_t stage = BITS == 16 ? 2 * (size_t)Tile<D, BS>::kTileBytes
+    constexpr size_t tb = kBlocksPerStage<BITS, BS>;
+    constexpr size_t stage = BITS == 16 ? 2 * tb * (size_t)Tile<D, BS>::kTileBytes
                                         : tb * (size_t)QRec<D, BS, (BITS == 16 ? 8 : BITS)>::kBytes;
     // + the flags (64 B) and, for the index-list gather, a split's row offsets
     return 1024 + (size_t)NST * stage + 2 * NST * sizeof(uint64_t) + 64 + (GATHER ? (size_t)kSplitTokens * 8 : 0);
