@@ -250,8 +250,16 @@ __device__ __forceinline__ void q_frag(const uint32_t (&cw)[NW], int ks, uint32_
 // GATHER: the index-list gather.  The work unit is (query row, KV head); its keys are
 // the row's list entries, 16 per stage, each row fetched through the block table with
 // 16-byte cp.async copies into the same swizzled tile layout the TMA path fills.
+// Residency hints: by default the compiler picks the register count (93-96 for the
+// bf16 kernels at d 128); PKV_MIN_CTAS_WIDE / PKV_MIN_CTAS_DECODE request that many
+// resident CTAs of the wide-row / decode shapes, capping the registers to fit.
+#if defined(PKV_MIN_CTAS_WIDE) && defined(PKV_MIN_CTAS_DECODE)
+#define PKV_KERNEL_BOUNDS(NMT, KW) __launch_bounds__(((NMT) * (KW) + 1) * 32, (NMT) > 1 ? PKV_MIN_CTAS_WIDE : PKV_MIN_CTAS_DECODE)
+#else
+#define PKV_KERNEL_BOUNDS(NMT, KW) __launch_bounds__(((NMT) * (KW) + 1) * 32)
+#endif
 template <int D, int BS, int NN, int NMT, int NST, bool TREE, int BITS, int KW, bool GATHER = false>
-__global__ void __launch_bounds__((NMT * KW + 1) * 32)
+__global__ void PKV_KERNEL_BOUNDS(NMT, KW)
 paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const AttnParams p)
 {
@@ -376,19 +384,29 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
         long long ctx = __ldg(p.context_lens + seq);
         ctx = ctx < 0 ? 0 : (ctx > ctx_cap ? ctx_cap : ctx);
         const int32_t *lst = p.key_idx + (size_t)s * p.max_keys;
-        // resolve every entry of the slice first, all loads in flight at once (an entry's
-        // block-table load depends on its list load; per tile that chain would serialise)
-#pragma unroll 4
-        for (int i = lane; i < C; i += 32) {
-            const int e = t0 + i;
-            if (e >= t1)
+        // resolve every entry of the slice first: all of the lane's list loads, then all
+        // of its (dependent) block-table loads, so the slice costs two round trips
+        constexpr int EPL = C / 32;   // entries per lane
+        int pos[EPL], blk[EPL];
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) {
+            const int e = t0 + j * 32 + lane;
+            pos[j] = e < t1 ? __ldg(lst + e) : -1;
+        }
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) {
+            const bool in = pos[j] >= 0 && pos[j] < ctx;
+            blk[j] = in ? __ldg(p.block_tables + (size_t)seq * p.max_blocks_per_seq + pos[j] / p.block_size) : -1;
+        }
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) {
+            const int i = j * 32 + lane;
+            if (t0 + i >= t1)
                 break;
-            const int pos = __ldg(lst + e);
             unsigned long long off = kGatherBad;
-            if (pos >= 0 && pos < ctx) {
-                const int blk = __ldg(p.block_tables + (size_t)seq * p.max_blocks_per_seq + pos / p.block_size);
-                if (blk >= 0 && blk < p.num_blocks)
-                    off = ((((unsigned long long)blk * p.num_kv_heads) + g) * p.block_size + pos % p.block_size) * D;
+            if (pos[j] >= 0 && pos[j] < ctx) {
+                if (blk[j] >= 0 && blk[j] < p.num_blocks)
+                    off = ((((unsigned long long)blk[j] * p.num_kv_heads) + g) * p.block_size + pos[j] % p.block_size) * D;
                 else
                     atomicOr(p.status, PKV_DEV_BAD_BLOCK);
             } else {
@@ -1198,14 +1216,20 @@ constexpr int kKeyWarps();
 // DEEP: a grid of at most two CTAs per SM (a few long sequences, e.g. one layer of a
 // 4-sequence decode) is bound by the bytes each CTA keeps in flight, not by occupancy:
 // such calls get a deeper ring.  Ring depth does not change any row's arithmetic.
+// Quantised rings hold at least PKV_QUANT_RING_BYTES: a record of fewer bits gets more
+// stages, so each CTA keeps as many bytes in flight as a Q8 one.
+#ifndef PKV_QUANT_RING_BYTES
+#define PKV_QUANT_RING_BYTES 0
+#endif
 template <int D, int BS, int NN, int NMT, int BITS, bool DEEP = false>
 constexpr int kStages()
 {
-    constexpr int base = DEEP ? PKV_STAGES_DEEP
-                              : BITS != 16 ? PKV_STAGES_QUANT : NMT == 1 ? PKV_STAGES_DECODE : PKV_STAGES_WIDE;
-    // the KW - 1 key shares' states pass through the ring at the end: make it big enough
     constexpr int tb = kBlocksPerStage<BITS, BS>;
     constexpr int stage = BITS == 16 ? 2 * tb * Tile<D, BS>::kTileBytes : tb * QRec<D, BS, (BITS == 16 ? 8 : BITS)>::kBytes;
+    constexpr int by_bytes = BITS != 16 ? (PKV_QUANT_RING_BYTES + stage - 1) / stage : 0;
+    constexpr int quant = PKV_STAGES_QUANT > by_bytes ? PKV_STAGES_QUANT : by_bytes;
+    constexpr int base = DEEP ? PKV_STAGES_DEEP : BITS != 16 ? quant : NMT == 1 ? PKV_STAGES_DECODE : PKV_STAGES_WIDE;
+    // the KW - 1 key shares' states pass through the ring at the end: make it big enough
     constexpr int merge = (kKeyWarps<BITS>() - 1) * NMT * (D / 16 * 4 + 6) * NN * 32 * 4;
     constexpr int need = (merge + stage - 1) / stage;
     constexpr int kw = kKeyWarps<BITS>();
