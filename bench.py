@@ -334,9 +334,42 @@ def run_ours(args, rank, world, local_rank):
         raise RuntimeError(f"device status {rc} bits {dev_bits:#x} after warm-up")
 
     # ---- device-resident timed region ----
-    n_ev = args.steps * layers
-    ev_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
+    # By default the step is captured as a CUDA graph and replayed, as a serving loop replays
+    # its decode step (its launches then cost one graph launch); the per-call kernel
+    # durations for the roofline come from an eager pass beforehand, since a graph changes
+    # the gaps between kernels, not the kernels.  The index-list gather, whose lists change
+    # every step, captures one graph per list set and replays them in turn.  --eager: plain
+    # launches throughout.
+    graph = not getattr(args, "eager", False)
+
+    def capture(io_):
+        g_ = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step(io=io_, st=side)
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g_):
+            step(io=io_, st=torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        return g_
+
+    n_eager = min(args.steps, 200) if graph else args.steps
+    ev_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(n_eager * layers)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if graph:
+        li = 0
+        for _ in range(n_eager):
+            li = step(ev_pairs, li)
+        torch.cuda.synchronize()
+        if gather:
+            g_steps = [capture(types.SimpleNamespace(**{**vars(io), "keys": ks})) for ks in key_sets]
+        else:
+            g_steps = [capture(io)]
+        for k in range(3):
+            g_steps[k % len(g_steps)].replay()
     clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     barrier()
     if clocks:
@@ -345,8 +378,11 @@ def run_ours(args, rank, world, local_rank):
     wall0 = time.perf_counter()
     t0.record(stream)
     li = 0
-    for _ in range(args.steps):
-        li = step(ev_pairs, li)
+    for i in range(args.steps):
+        if graph:
+            g_steps[i % len(g_steps)].replay()
+        else:
+            li = step(ev_pairs, li)
     t1.record(stream)
     barrier()
     wall1 = time.perf_counter()
@@ -422,6 +458,7 @@ def run_ours(args, rank, world, local_rank):
         return st_
 
     sets = [make_set(0), make_set(1)]
+    g_sets = [capture(sets[0]), capture(sets[1])] if graph else None
     h2d = in_total
     d2h = out_total
     copy_stream = torch.cuda.Stream()
@@ -444,7 +481,10 @@ def run_ours(args, rank, world, local_rank):
         for i in range(n):
             k, o = i % 2, 1 - i % 2
             stream.wait_event(ready[k])
-            step(io=sets[k])
+            if graph:
+                g_sets[k].replay()
+            else:
+                step(io=sets[k])
             done[k].record(stream)
             with torch.cuda.stream(copy_stream):
                 if i + 1 < n:
@@ -498,6 +538,7 @@ def run_ours(args, rank, world, local_rank):
                    "l2": "inputs larger than L2 (K/V read per step >> 129 MB); no flush",
                    "seed": args.seed,
                    "accept": None if b.logits is None else accept_mode,
+                   "launch": "cuda graph (one captured step, replayed)" if graph else "eager",
                    "kv_codec": "bf16" if not quant else f"q{bits} (per-row float32 scale)"},
         "query_rows_per_s": round(rows_per_s, 1),
         "frac_of_measured_hbm": round(value / peak, 4),
@@ -509,6 +550,7 @@ def run_ours(args, rank, world, local_rank):
                      "peak": peak, "peak_kind": f"{peak_kind} (hbm_gbs, copy kernel)", "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "bytes_per_launch": per_launch_bytes,
                      "avg_launch_ms": round(attn_avg_ms, 5), "launches_timed": len(attn_ms),
+                     "launches_timed_mode": "eager pass before the graph replays" if graph else "timed region",
                      "traffic": traffic},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms_per_step, 5),
@@ -633,6 +675,8 @@ def main():
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="resize the batch (same per-sequence distribution); for profiling smaller cases")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="launch every kernel of every step directly instead of replaying a captured CUDA graph")
     ap.add_argument("--kv-bits", type=int, choices=(16, 8, 4, 2), default=16,
                     help="16: bf16 K/V pools; 8 / 4 / 2: quantised KV blocks (Q8 / Q4 / Q2 records)")
     ap.add_argument("--accept", choices=("greedy", "sampled", "sampled-topkp"), default="greedy",

@@ -157,7 +157,7 @@ def paged_attention_workspace_size(num_seqs, total_q_rows, num_q_heads, num_kv_h
 
 def new_attention_workspace(num_seqs, total_q_rows, num_q_heads, num_kv_heads, head_dim, max_context_len,
                             device=None) -> torch.Tensor:
-    """A zeroed workspace of the right size (zero is what the first call needs)."""
+    """A workspace of the right size, zeroed (the calls do not depend on its contents)."""
     n = paged_attention_workspace_size(num_seqs, total_q_rows, num_q_heads, num_kv_heads, head_dim,
                                        max_context_len)
     return torch.zeros(max(n, 256), dtype=torch.uint8, device=device or "cuda")
