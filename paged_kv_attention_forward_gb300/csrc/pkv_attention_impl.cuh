@@ -1021,34 +1021,48 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
     }
 }
 
-// Merge of the split partials of one (query row, q head) per warp, in split order,
-// with the head's sink:  M = max(m_i, sink), out = sum_i 2^{m_i - M} O_i /
-// (sum_i 2^{m_i - M} l_i + 2^{sink - M}).  Launched as a programmatic dependent of
-// the split kernel: it may start early and waits for the partials with
-// griddepcontrol.wait.
+// Merge of the split partials of one (query row, q head) with the head's sink:
+// M = max(m_i, sink), out = sum_i 2^{m_i - M} O_i / (sum_i 2^{m_i - M} l_i + 2^{sink - M}).
+// Two warps serve a (row, head): warp h sums, in split order, the partials of its half
+// [0, n0) or [n0, n) (n0 = ceil(n / 2)), and the second half's sums are added to the
+// first's.  The order depends only on n, i.e. on the row's own length.  Launched as a
+// programmatic dependent of the split kernel: it may start early and waits for the
+// partials with griddepcontrol.wait.
 #ifndef PKV_MERGE_BATCH
 #define PKV_MERGE_BATCH 8
 #endif
+#ifndef PKV_MERGE_MIN_CTAS
+#define PKV_MERGE_MIN_CTAS 7
+#endif
 template <int D>
-__global__ void __launch_bounds__(128, 7)
+__global__ void __launch_bounds__(128, PKV_MERGE_MIN_CTAS)
 paged_attention_combine_kernel(const AttnParams p)
 {
     constexpr int VEC = D / 32;   // output values per lane
+    __shared__ float hand[2][VEC + 1][32];   // per pair: the second half's numerators and denominator
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const long long wid = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int pr = warp >> 1, half = warp & 1;
+    const long long wid = (long long)blockIdx.x * 2 + pr;
     if (wid >= (long long)p.total_rows * p.num_q_heads)
-        return;
+        return;   // both warps of the pair leave together
     const int r = (int)(wid / p.num_q_heads);
     const int h = (int)(wid - (long long)r * p.num_q_heads);
-    // sequence of row r: the last s with q_starts[s] <= r
+    // sequence of row r: the last s with q_starts[s] <= r, by a 32-way search (the table
+    // is non-decreasing; q_starts[lo] <= r holds throughout)
     int lo = 0, hi = p.num_seqs - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(p.q_starts + mid) <= r)
-            lo = mid;
-        else
-            hi = mid - 1;
+    while (hi - lo >= 32) {
+        const int step = (hi - lo + 32) / 32;
+        const int j = lo + lane * step;
+        const unsigned m = __ballot_sync(0xffffffffu, j <= hi && __ldg(p.q_starts + j) <= r);
+        const int last = m ? 31 - __clz(m) : 0;
+        lo += last * step;
+        hi = min(hi, lo + step - 1);
+    }
+    {
+        const int j = lo + lane;
+        const unsigned m = __ballot_sync(0xffffffffu, j <= hi && __ldg(p.q_starts + j) <= r);
+        lo += m ? 31 - __clz(m) : 0;
     }
     const int s = lo;
     const int row0 = __ldg(p.q_starts + s);
@@ -1071,17 +1085,29 @@ paged_attention_combine_kernel(const AttnParams p)
         lim = c < 0 ? 0 : (c > p.max_keys ? p.max_keys : c);
     }
     const int n = lim > 0 ? (lim + kSplitTokens - 1) / kSplitTokens : 0;
+    const int n0 = (n + 1) / 2;
+    const int i_begin = half ? n0 : 0, i_end = half ? n : n0;
     const size_t base = ((size_t)r * p.num_q_heads + h) * p.n_max;
+    const float *src0 = p.part_o + base * D + lane * VEC;
+    constexpr int BATCH = PKV_MERGE_BATCH;   // partial rows in flight per lane
 
-    // the n partial rows of (r, h) are contiguous: ask L2 for all of them at once, so the
-    // batched loop below waits for one DRAM round trip instead of one per batch
-    {
-        const char *region = reinterpret_cast<const char *>(p.part_o + base * D);
-        const int lines = (n * D * (int)sizeof(float) + 127) / 128;
-        for (int i = lane; i < lines; i += 32)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(region + (size_t)i * 128));
+    // the first batch of this half's partial rows goes out with the (m, l) loads
+    float x0[BATCH][VEC];
+#pragma unroll
+    for (int b = 0; b < BATCH; ++b) {
+        const int i = i_begin + b;
+        if (i < i_end) {
+            const float *src = src0 + (size_t)i * D;
+            if constexpr (VEC == 4) {
+                const float4 t = __ldcg(reinterpret_cast<const float4 *>(src));
+                x0[b][0] = t.x, x0[b][1] = t.y, x0[b][2] = t.z, x0[b][3] = t.w;
+            } else {
+                const float2 t = __ldcg(reinterpret_cast<const float2 *>(src));
+                x0[b][0] = t.x, x0[b][1] = t.y;
+            }
+        }
     }
-    // lane i holds (m, l) of partials i, i + 32, ...; the sums below still run in split order
+    // lane i holds (m, l) of partials i, i + 32, ...; both warps find the same M
     constexpr int MAXC = 2;   // partials cached per lane (n <= 64); longer rows reload (m, l)
     float2 mlc[MAXC];
 #pragma unroll
@@ -1115,14 +1141,37 @@ paged_attention_combine_kernel(const AttnParams p)
 #pragma unroll
     for (int v = 0; v < VEC; ++v)
         num[v] = 0.f;
-    const float *src0 = p.part_o + base * D + lane * VEC;
-    constexpr int BATCH = PKV_MERGE_BATCH;   // partial rows in flight per lane
-    for (int i0 = 0; i0 < n; i0 += BATCH) {
+    auto accumulate = [&](int i, const float (&xv)[VEC]) {
+        float wgt, l_i;
+        if (i < MAXC * 32) {
+            const int c = i >> 5, srcl = i & 31;
+            float wsel = wc[0], lsel = lc[0];
+#pragma unroll
+            for (int cc = 1; cc < MAXC; ++cc)
+                if (c == cc)
+                    wsel = wc[cc], lsel = lc[cc];
+            wgt = __shfl_sync(0xffffffffu, wsel, srcl);
+            l_i = __shfl_sync(0xffffffffu, lsel, srcl);
+        } else {
+            const float2 ml = __ldcg(&p.part_ml[base + i]);
+            wgt = fast_exp2(ml.x - Mx);
+            l_i = ml.y;
+        }
+        den += wgt * l_i;
+#pragma unroll
+        for (int v = 0; v < VEC; ++v)
+            num[v] += wgt * xv[v];
+    };
+#pragma unroll
+    for (int b = 0; b < BATCH; ++b)
+        if (i_begin + b < i_end)
+            accumulate(i_begin + b, x0[b]);
+    for (int i0 = i_begin + BATCH; i0 < i_end; i0 += BATCH) {
         float x[BATCH][VEC];
 #pragma unroll
         for (int b = 0; b < BATCH; ++b) {
             const int i = i0 + b;
-            if (i < n) {
+            if (i < i_end) {
                 const float *src = src0 + (size_t)i * D;
                 if constexpr (VEC == 4) {
                     const float4 t = __ldcg(reinterpret_cast<const float4 *>(src));
@@ -1134,31 +1183,27 @@ paged_attention_combine_kernel(const AttnParams p)
             }
         }
 #pragma unroll
-        for (int b = 0; b < BATCH; ++b) {
-            const int i = i0 + b;
-            if (i >= n)
-                break;
-            float wgt, l_i;
-            if (i < MAXC * 32) {
-                const int c = i >> 5, srcl = i & 31;
-                float wsel = wc[0], lsel = lc[0];
-#pragma unroll
-                for (int cc = 1; cc < MAXC; ++cc)
-                    if (c == cc)
-                        wsel = wc[cc], lsel = lc[cc];
-                wgt = __shfl_sync(0xffffffffu, wsel, srcl);
-                l_i = __shfl_sync(0xffffffffu, lsel, srcl);
-            } else {
-                const float2 ml = __ldcg(&p.part_ml[base + i]);
-                wgt = fast_exp2(ml.x - Mx);
-                l_i = ml.y;
-            }
-            den += wgt * l_i;
-#pragma unroll
-            for (int v = 0; v < VEC; ++v)
-                num[v] += wgt * x[b][v];
-        }
+        for (int b = 0; b < BATCH; ++b)
+            if (i0 + b < i_end)
+                accumulate(i0 + b, x[b]);
     }
+    // the second half hands its sums to the first, which adds them after its own
+    if (half) {
+#pragma unroll
+        for (int v = 0; v < VEC; ++v)
+            hand[pr][v][lane] = num[v];
+        hand[pr][VEC][lane] = den;
+    }
+    if (pr == 0)   // one named barrier per pair of warps
+        asm volatile("bar.sync 1, 64;" ::: "memory");
+    else
+        asm volatile("bar.sync 2, 64;" ::: "memory");
+    if (half)
+        return;
+#pragma unroll
+    for (int v = 0; v < VEC; ++v)
+        num[v] += hand[pr][v][lane];
+    den += hand[pr][VEC][lane];
     if (has_sink)
         den += fast_exp2(sink2 - Mx);
     float res[VEC];
@@ -1274,10 +1319,11 @@ int launch_t(const CUtensorMap &mk, const CUtensorMap &mv, const AttnParams &prm
     int rc = check_cuda(cudaGetLastError(), "paged attention split launch");
     if (rc)
         return rc;
-    // merge, as a programmatic dependent launch (its launch overlaps the split grid's tail)
-    const long long warps = (long long)prm.total_rows * prm.num_q_heads;
+    // merge, as a programmatic dependent launch (its launch overlaps the split grid's tail);
+    // a CTA of four warps serves two (row, q head) units
+    const long long units = (long long)prm.total_rows * prm.num_q_heads;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((warps + 3) / 4));
+    cfg.gridDim = dim3((unsigned)((units + 1) / 2));
     cfg.blockDim = dim3(128);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;

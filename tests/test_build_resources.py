@@ -2,8 +2,8 @@
 
 The occupancy the design relies on (eight 64-thread decode CTAs and five 128-thread
 verify CTAs per SM for head_dim 128) holds only while these kernels stay within 96
-registers per thread without spills; a change that raises them slows every verify step
-without failing any numeric test.
+registers per thread without spills, and the merge kernel (seven 128-thread CTAs per SM)
+within 72; a change that raises them slows every call without failing any numeric test.
 """
 import os
 import re
@@ -37,8 +37,13 @@ def _ptxas_usage(src):
     return usage
 
 
-def test_bf16_attention_kernels_fit_their_register_budget():
-    usage = _ptxas_usage("pkv_attention.cu")
+@pytest.fixture(scope="module")
+def attention_usage():
+    return _ptxas_usage("pkv_attention.cu")
+
+
+def test_bf16_attention_kernels_fit_their_register_budget(attention_usage):
+    usage = attention_usage
     # head_dim 128, block 16, bf16, no tree, no gather: the decode (1 row warp) and verify
     # (3 row warps) shapes of the cb_mix and spec_verify workloads
     pat = re.compile(r"paged_attention_kernelILi128ELi16ELi1ELi([13])ELi\d+ELb0ELi16ELi1ELb0E")
@@ -47,3 +52,10 @@ def test_bf16_attention_kernels_fit_their_register_budget():
     for shape, u in found.items():
         assert u["regs"] <= 96, f"{shape} row warps: {u['regs']} registers"
         assert u.get("spill", 0) == 0, f"{shape} row warps spill {u['spill']} bytes"
+
+
+def test_merge_kernel_fits_its_register_budget(attention_usage):
+    found = {name: u for name, u in attention_usage.items() if "paged_attention_combine_kernel" in name}
+    assert len(found) == 2, sorted(attention_usage)[:5]   # head_dim 64 and 128
+    for name, u in found.items():
+        assert u["regs"] <= 72 and u.get("spill", 0) == 0, (name, u)
