@@ -96,6 +96,8 @@ def test_record_layout_worked_offsets(oracle_mod):
     # r 0) -> u 20, word 512 + 320 + 4, bit 8 + 16 = 24
     assert oracle_mod.qcode_offset(0, 3, 37, 128, 16, 2) == (103, 0)
     assert oracle_mod.qcode_offset(1, 3, 37, 128, 16, 2) == (512 + 327, 0)
+    assert oracle_mod.qcode_offset(0, 1, 0, 128, 16, 2) == (1, 0)       # r = 1, e = 0: byte 1
+    assert oracle_mod.qcode_offset(0, 0, 1, 128, 16, 2) == (2, 0)       # r = 0, e = 1: byte 2
     assert oracle_mod.qcode_offset(0, 0, 8, 128, 16, 2) == (0, 2)       # h = 1
     assert oracle_mod.qcode_offset(0, 0, 16, 128, 16, 2) == (0, 4)      # j = 1: second k-step
     assert oracle_mod.qcode_offset(1, 0, 8, 128, 16, 2) == (512, 2)     # r = 1
