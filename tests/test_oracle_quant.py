@@ -89,6 +89,10 @@ def test_record_layout_worked_offsets(oracle_mod):
     assert oracle_mod.qcode_offset(1, 3, 37, 128, 16, 8) == (2048 + 835, 0)
     assert oracle_mod.qcode_offset(0, 3, 37, 128, 16, 4) == (107, 0)
     assert oracle_mod.qcode_offset(1, 3, 37, 128, 16, 4) == (1024 + 331, 0)
+    assert oracle_mod.qcode_offset(0, 1, 0, 128, 16, 8) == (4, 0)       # key parity 1, column parity 0
+    assert oracle_mod.qcode_offset(0, 0, 1, 128, 16, 8) == (2, 0)       # key parity 0, column parity 1
+    assert oracle_mod.qcode_offset(0, 1, 0, 128, 16, 4) == (1, 0)       # bit 8
+    assert oracle_mod.qcode_offset(0, 0, 1, 128, 16, 4) == (2, 0)       # bit 16
     assert oracle_mod.qcode_offset(0, 0, 8, 128, 16, 4) == (0, 4)       # h = 1: high nibble
     assert oracle_mod.qcode_offset(1, 0, 8, 128, 16, 4) == (1024, 4)    # r = 1: high nibble
     # 2 bits (units of D/8 = 16 bytes): K slot 3 (g 1, r 1), dim 37 (j 2, c 2, h 0, e 1) -> u 6,
@@ -101,6 +105,8 @@ def test_record_layout_worked_offsets(oracle_mod):
     assert oracle_mod.qcode_offset(0, 0, 8, 128, 16, 2) == (0, 2)       # h = 1
     assert oracle_mod.qcode_offset(0, 0, 16, 128, 16, 2) == (0, 4)      # j = 1: second k-step
     assert oracle_mod.qcode_offset(1, 0, 8, 128, 16, 2) == (512, 2)     # r = 1
+    assert oracle_mod.qcode_offset(1, 1, 0, 128, 16, 2) == (513, 0)     # slot 1: m 8, h 1, e 0
+    assert oracle_mod.qcode_offset(1, 2, 0, 128, 16, 2) == (514, 0)     # slot 2: m 1, h 0, e 1
     assert oracle_mod.qcode_offset(1, 0, 16, 128, 16, 2) == (512, 4)    # dm = 1
     assert oracle_mod.qcode_offset(0, 16, 0, 64, 32, 2) == (32 * 8, 0)  # head_dim 64: 8-byte units
 
