@@ -8,6 +8,7 @@ from __future__ import annotations
 
 import hashlib
 import os
+import re
 import shutil
 import subprocess
 from concurrent.futures import ThreadPoolExecutor
@@ -39,9 +40,19 @@ ATTENTION_SOURCES = ("pkv_attention_impl.cuh", "pkv_attention.cu", "pkv_attentio
                      "pkv_internal.h")
 
 
+_COMMENT = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)
+
+
+def code_text(text: str) -> str:
+    """C/C++/CUDA source with its comments removed and whitespace runs collapsed: what
+    the compiler sees, up to line positions."""
+    return " ".join(_COMMENT.sub(" ", text).split())
+
+
 def source_digest(names=None) -> str:
-    """Hash of every source and header the library is built from, or of the named
-    files of csrc/ only."""
+    """Hash of every source and header the library is built from (the rebuild stamp), or,
+    for the named files of csrc/, of their code alone (comments and layout do not count,
+    so a profile of the kernels stays valid across comment edits)."""
     h = hashlib.sha256()
     if names is None:
         files = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC)) + [os.path.join(INCLUDE, "pkv.h")]
@@ -50,7 +61,8 @@ def source_digest(names=None) -> str:
     for f in files:
         h.update(os.path.basename(f).encode())
         with open(f, "rb") as fh:
-            h.update(fh.read())
+            data = fh.read()
+        h.update(data if names is None else code_text(data.decode("utf-8")).encode())
     return h.hexdigest()[:16]
 
 

@@ -32,11 +32,11 @@
 //    Keys past a row's limit get weight exactly 0, so a verify-window row and the
 //    same row decoded alone go through identical operations.
 //  * Partials (m, l, O) of every split go to the workspace.  A second kernel,
-//    one warp per (query row, q head), merges them in split order:
+//    two warps per (query row, q head), merges them in an order fixed by the
+//    row's own length (each warp one half in split order, then the halves):
 //    M = max(m_i, sink), out = sum_i 2^{m_i-M} O_i / (sum_i 2^{m_i-M} l_i + 2^{sink-M}).
 //    It is launched as a programmatic dependent of the split kernel, so its launch
-//    overlaps the split grid's tail; the merge of the longest sequences is no
-//    longer serialised on one CTA at the end.
+//    overlaps the split grid's tail.
 //  * Bounded waits only; block ids and lengths are range-checked on the device
 //    (clamped + status bit, never a fault).
 //  * Quantised KV blocks (TensorSharp "高级功能", section "内存优化", the KV block
