@@ -23,6 +23,11 @@ Workloads (sizes from the continuous-batching / speculative-decoding pages):
                     block 32, one fp32 sink logit per q head.
   spec_tree         spec_verify's shapes with each window a random draft tree
                     (per-row ancestor masks, parent indices, tree drafts).
+  sparse_gather     cb_mix's sequences, each decode row attending over a list of
+                    [its last 128 | 512 older] key positions.
+  prefill_mix       16 seqs, cached lengths U[1024,8192], each appending a
+                    256-token prefill chunk with causal rows, 32 q / 8 kv heads,
+                    head_dim 128, block 16.
 """
 from __future__ import annotations
 
@@ -381,7 +386,7 @@ def _loguniform_int(rng, lo, hi, size):
 
 
 WORKLOADS = ("tiny_decode", "ministral_decode", "cb_mix", "spec_verify", "sinks_scale", "spec_tree",
-             "sparse_gather")
+             "sparse_gather", "prefill_mix")
 VOCAB = 151936
 
 
@@ -430,6 +435,14 @@ def make_workload(name: str, seed: int = 0, filler: str = "random", layers: Opti
                         head_dim=128, block_size=16, causal=False, filler=filler,
                         shared_prefix=prefix, sharing=sharing)
         return add_key_lists(b, s_extra, ring=128, top=512, sets=4)
+    if name == "prefill_mix":
+        # chunked prefill in bounded 256-token chunks: the chunk's K/V are appended first and
+        # its rows attend causally over the cached context and the chunk
+        S = num_seqs or 16
+        old = rng.integers(1024, 8193, size=S)
+        chunk = np.full(S, 256, np.int64)
+        return build_batch(s_batch, name=name, lens=old + chunk, n_new=chunk, q_rows=chunk, num_q_heads=32,
+                           num_kv_heads=8, head_dim=128, block_size=16, causal=True, filler=filler)
     if name == "spec_verify":
         S = num_seqs or 16
         lens = rng.integers(4096, 32769, size=S)

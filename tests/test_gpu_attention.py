@@ -80,7 +80,7 @@ def test_append_bit_exact(pkv, name, filler):
 
 @pytest.mark.parametrize("name,seed", [("tiny_decode", 0), ("tiny_decode", 1), ("tiny_decode", 2),
                                        ("cb_mix", 0), ("spec_verify", 0), ("sinks_scale", 0),
-                                       ("cb_mix", 1), ("spec_verify", 2)])
+                                       ("cb_mix", 1), ("spec_verify", 2), ("prefill_mix", 0)])
 def test_attention_matches_oracle(pkv, name, seed):
     b = wl.make_workload(name, seed=seed)
     _, out = _gpu_step(pkv, b)
@@ -109,7 +109,7 @@ def test_float32_output(pkv, name):
     assert_close_to_oracle(out.cpu().numpy(), ref, what=name)
 
 
-@pytest.mark.parametrize("name", ["cb_mix", "spec_verify", "sinks_scale"])
+@pytest.mark.parametrize("name", ["cb_mix", "spec_verify", "sinks_scale", "prefill_mix"])
 def test_batch_vs_solo_bit_identical(pkv, name):
     b = wl.make_workload(name, seed=4)
     g, out = _gpu_step(pkv, b)
