@@ -194,6 +194,25 @@ def test_ragged_lengths_all_variants(pkv, d, bs, causal):
     _status_ok(pkv)
 
 
+def test_contexts_beyond_sixty_four_splits(pkv):
+    # 79, 137, 2 and 65 splits of 512 keys: the merge reloads (m, l) past 64 partials, and
+    # both of its halves (odd and even split counts) are exercised
+    lens = np.array([40001, 70000, 1000, 33000])
+    W = np.array([1, 16, 1, 5])
+    b = wl.build_batch(77, name="long", lens=lens, n_new=W, q_rows=W, num_q_heads=8, num_kv_heads=2,
+                       head_dim=128, block_size=16, causal=True, with_sinks=True)
+    g, out = _gpu_step(pkv, b)
+    _, _, ref = _oracle_step(b)
+    assert_close_to_oracle(out.float().cpu().numpy(), ref, what="long contexts")
+    full = host_bits(out)
+    for s in (0, 1):
+        sub = wl.select_seqs(b, [s])
+        one = _attn_only(pkv, g, sub, tables=dev(sub.block_tables), lens=dev(sub.context_lens),
+                         q=dev_bf16(sub.q[0]), q_starts=dev(sub.q_starts))
+        assert np.array_equal(host_bits(one), full[b.q_starts[s]:b.q_starts[s + 1]]), f"sequence {s} alone"
+    _status_ok(pkv)
+
+
 def test_group_of_eight_with_sixteen_row_windows(pkv):
     lens = np.array([40, 700, 2049])
     W = np.array([16, 16, 9])
@@ -204,7 +223,7 @@ def test_group_of_eight_with_sixteen_row_windows(pkv):
     assert_close_to_oracle(out.float().cpu().numpy(), ref, what="G8xW16")
 
 
-@pytest.mark.parametrize("d,bs", [(128, 16), (64, 32)])
+@pytest.mark.parametrize("d,bs", [(128, 16), (64, 32), (64, 16), (128, 32)])
 def test_chunked_prefill_windows(pkv, d, bs):
     """Prefill chunks through the same kernel: W new rows appended, then attended causally
     (TensorSharp advanced features, section on chunked prefill: bounded chunks of 256)."""
