@@ -181,28 +181,23 @@ __device__ __forceinline__ void load_group(const uint8_t *g, int lane, uint32_t 
     }
 }
 
-// Codes become f16 operands without arithmetic: f16 bits 0x6400 | u are 1024 + u for a
-// byte u (0..255), and bits 0x4C00 | (u << 6) are 16 + u for a nibble or bit pair u
-// (0..15), so putting a stored u = c + 128 (c + 8, c + 2) under those exponent bits
-// yields c + kBias exactly.  The tensor core then computes q . (c + kBias) and P . (c + kBias); the
-// kernel removes kBias * sum(q) from each score and kBias * sum(P) from each output
-// row, in fp32.
+// Codes become f16 operands with one logic op: a field u at bits p .. of the low byte
+// of each 16-bit half, under the exponent bits 0x6400, is the f16 1024 + u * 2^p
+// exactly.  A byte code (u = c + 128, p = 0) is 1024 + u; a nibble (c + 8) or bit pair
+// (c + 2) sits at p = fpos(step, half) of its byte (bytes 1 and 3 are first moved down by
+// one prmt), so its operand is 1024 + 2^p (c + off).  The factor 2^p is taken out exactly
+// (K: the matching q dims are scaled by 2^-p; V: the PV product by 2^-p), leaving the
+// offset 1024 * 2^-p + off, which the kernel removes in fp32: sum(q' * (1024 + 2^p off))
+// from each score and (1024 * 2^-p + off) * sum(P) from each output element.
 template <int BITS>
-constexpr float kBias = BITS == 8 ? 1152.f : BITS == 4 ? 24.f : 18.f;   // 1024 + 128, 16 + 8, 16 + 2
+constexpr int kCodeOff = 1 << (BITS - 1);   // 128, 8, 2: the stored field is c + off
 
-// nibble pair P (bits 4P and 16 + 4P of w) -> f16x2 of 16 + u
-template <int P>
-__device__ __forceinline__ uint32_t nib_pair(uint32_t w)
+// bit position, within its byte, of the field that feeds k-step (K) or dim m-tile (V)
+// `step`, column half (K) or row half (V) `half`
+template <int BITS>
+__device__ __forceinline__ constexpr int fpos(int step, int half)
 {
-    const uint32_t x = P == 0 ? w << 6 : P == 1 ? w << 2 : P == 2 ? w >> 2 : w >> 6;
-    return (x & 0x03C003C0u) | 0x4C004C00u;
-}
-
-// bit pair at bits b and 16 + b of w -> f16x2 of 16 + u
-__device__ __forceinline__ uint32_t bit_pair(uint32_t w, int b)
-{
-    const uint32_t x = b <= 6 ? w << (6 - b) : w >> (b - 6);
-    return (x & 0x00C000C0u) | 0x4C004C00u;
+    return BITS == 8 ? 0 : BITS == 4 ? 4 * half : 4 * (step & 1) + 2 * half;
 }
 
 // A operand of k-step ks of a K tile, or of 16-dim m-tile ks of a V^T tile, from the
@@ -216,23 +211,24 @@ __device__ __forceinline__ void q_frag(const uint32_t (&cw)[NW], int ks, uint32_
         a[1] = __byte_perm(w1, 0x64646464u, 0x4240);
         a[2] = __byte_perm(w0, 0x64646464u, 0x4341);   // bytes 1, 3
         a[3] = __byte_perm(w1, 0x64646464u, 0x4341);
-    } else if constexpr (BITS == 2) {
-        // k-step parity q picks bits 4q..4q+3 of each byte; K: byte r (A row half), pair
-        // h (A column half); V: byte h, pair r
-        const uint32_t w = cw[ks >> 1];
-        const int q4 = 4 * (ks & 1);
-        a[0] = bit_pair(w, q4);
-        a[1] = bit_pair(w, IS_V ? q4 + 2 : q4 + 8);
-        a[2] = bit_pair(w, IS_V ? q4 + 8 : q4 + 2);
-        a[3] = bit_pair(w, q4 + 10);
     } else {
-        const uint32_t w = cw[ks];
-        // nibble pair p sits at bits 4p and 16 + 4p; K: p = 2r + h, V: p = 2h + r
-        // (r: A row half, h: A column half)
-        a[0] = nib_pair<0>(w);
-        a[1] = nib_pair<IS_V ? 1 : 2>(w);
-        a[2] = nib_pair<IS_V ? 2 : 1>(w);
-        a[3] = nib_pair<3>(w);
+        // K: byte = A row half r, field = A column half h; V: byte = A column half h,
+        // field = A row half r (the fields of one k-step / m-tile sit at fpos(step, 0 / 1))
+        const uint32_t lo = BITS == 4 ? cw[ks] : cw[ks >> 1];
+        const uint32_t hi = __byte_perm(lo, 0u, 0x3311);   // bytes 1, 3 -> 0, 2
+        constexpr uint32_t f = BITS == 4 ? 0x000F000Fu : 0x00030003u;
+        const uint32_t m0 = f << fpos<BITS>(ks, 0), m1 = f << fpos<BITS>(ks, 1);
+        if constexpr (!IS_V) {
+            a[0] = (lo & m0) | 0x64006400u;   // r 0, h 0
+            a[1] = (hi & m0) | 0x64006400u;   // r 1, h 0
+            a[2] = (lo & m1) | 0x64006400u;   // r 0, h 1
+            a[3] = (hi & m1) | 0x64006400u;   // r 1, h 1
+        } else {
+            a[0] = (lo & m0) | 0x64006400u;   // r 0, h 0
+            a[1] = (lo & m1) | 0x64006400u;   // r 1, h 0
+            a[2] = (hi & m0) | 0x64006400u;   // r 0, h 1
+            a[3] = (hi & m1) | 0x64006400u;   // r 1, h 1
+        }
     }
 }
 
@@ -577,8 +573,9 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
             }
         }
         // Quantised: q goes to f16, scaled per row by the power of two 2^e that puts its
-        // largest |value| in [2^14, 2^15) (exact: a bf16 value has 8 significant bits);
-        // qbias = kBias * sum(q') is the code offset's share of every score, qscale =
+        // largest |value| in [2^14, 2^15) (exact: a bf16 value has 8 significant bits), and
+        // by 2^-fpos more where its codes carry 2^fpos; qbias is the code offset's share of
+        // every score (see q_frag), qscale =
         // scale * log2(e) * 2^-e.  Both are needed for the rows cr, cr + 1 of this lane's
         // S^T elements, so they are taken from the lanes that hold those rows' q.
         float qbias[NN][2], qscale[NN][2], cacc[NN][2];
@@ -596,20 +593,34 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                 amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
                 const int ex = (__float_as_int(amax) >> 23) & 0xFF;
                 const int e2 = amax > 0.f ? min(141 - ex, 126) : 0;   // amax * 2^e2 in [2^14, 2^15)
-                const float up = __int_as_float((127 + e2) << 23);
-                float qsum = 0.f;
+                // dims of column half j of k-step ks meet codes scaled by 2^fpos: q' takes 2^-fpos
+                constexpr int QB = BITS == 16 ? 8 : BITS;
+                float qsum[4] = {0.f, 0.f, 0.f, 0.f};   // per field position class
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
+                        const float up = __int_as_float((127 + e2 - fpos<QB>(ks, j)) << 23);
                         const uint32_t h2 = pack_f16x2(bf16_lo_to_f32(qf[nn][ks][j]) * up,
                                                        bf16_hi_to_f32(qf[nn][ks][j]) * up);
                         qf[nn][ks][j] = h2;
-                        qsum += f16_lo_to_f32(h2) + f16_hi_to_f32(h2);
+                        qsum[QB == 2 ? 2 * (ks & 1) + j : QB == 4 ? j : 0] += f16_lo_to_f32(h2) + f16_hi_to_f32(h2);
                     }
-                qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
-                qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
-                const float bias_r = kBias<(BITS == 16 ? 8 : BITS)> * qsum;
+                // the code offset's share of the score: sum over dims of q' (1024 + 2^fpos off)
+                float bias_r;
+                if constexpr (QB == 8) {
+                    float q0 = qsum[0];
+                    q0 += __shfl_xor_sync(0xffffffffu, q0, 1);
+                    q0 += __shfl_xor_sync(0xffffffffu, q0, 2);
+                    bias_r = (1024.f + kCodeOff<8>) * q0;
+                } else {
+                    bias_r = 0.f;
+#pragma unroll
+                    for (int c = 0; c < (QB == 2 ? 4 : 2); ++c)
+                        bias_r += qsum[c] * (1024.f + (float)((1 << fpos<QB>(c >> 1, c & 1)) * kCodeOff<QB>));
+                    bias_r += __shfl_xor_sync(0xffffffffu, bias_r, 1);
+                    bias_r += __shfl_xor_sync(0xffffffffu, bias_r, 2);
+                }
                 const float scale_r = p.scale_log2 * __int_as_float((127 - e2) << 23);
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
@@ -853,8 +864,9 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                             float part[4] = {0.f, 0.f, 0.f, 0.f};
                             mma_f16_16x8x16(part, a, b[nn][0], b[nn][1]);
 #pragma unroll
-                            for (int c = 0; c < 4; ++c)
-                                o[dm][nn][c] = fmaf(vmax[nn][c & 1], part[c], o[dm][nn][c]);
+                            for (int c = 0; c < 4; ++c)   // row half c >> 1: codes scaled by 2^fpos
+                                o[dm][nn][c] = fmaf(vmax[nn][c & 1] * __int_as_float((127 - fpos<BITS>(dm, c >> 1)) << 23),
+                                                    part[c], o[dm][nn][c]);
                         }
                     }
                 } else {
@@ -970,7 +982,7 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                 lrow[nn][e] = v;
             }
         if constexpr (BITS != 16) {
-            // remove the code offset: o -= kBias * sum over keys of the weights used
+            // remove the code offset: o -= (1024 * 2^-fpos + off) * sum over keys of the weights used
 #pragma unroll
             for (int nn = 0; nn < NN; ++nn)
 #pragma unroll
@@ -979,11 +991,11 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                     v += __shfl_xor_sync(0xffffffffu, v, 4);
                     v += __shfl_xor_sync(0xffffffffu, v, 8);
                     v += __shfl_xor_sync(0xffffffffu, v, 16);
-                    const float corr = kBias<(BITS == 16 ? 8 : BITS)> * v;
+                    constexpr int QB = BITS == 16 ? 8 : BITS;
 #pragma unroll
-                    for (int dm = 0; dm < DM; ++dm) {
-                        o[dm][nn][e] -= corr;
-                        o[dm][nn][2 + e] -= corr;
+                    for (int dm = 0; dm < DM; ++dm) {   // (1024 * 2^-fpos + off) * sum of the weights
+                        o[dm][nn][e] -= (1024.f * __int_as_float((127 - fpos<QB>(dm, 0)) << 23) + kCodeOff<QB>) * v;
+                        o[dm][nn][2 + e] -= (1024.f * __int_as_float((127 - fpos<QB>(dm, 1)) << 23) + kCodeOff<QB>) * v;
                     }
                 }
         }
