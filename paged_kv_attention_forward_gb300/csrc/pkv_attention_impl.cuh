@@ -297,7 +297,9 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
     const int rg = blockIdx.x - pair * p.row_groups;
     const int s = pair / p.num_kv_heads;
     const int g = pair - s * p.num_kv_heads;
-    const int split = blockIdx.y;
+    // highest split indices first: only the longest sequences have them, so the grid ends
+    // on every sequence's first split (uniform, and sharing the prefix blocks through L2)
+    const int split = gridDim.y - 1 - blockIdx.y;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
