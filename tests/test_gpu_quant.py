@@ -117,6 +117,27 @@ def test_quant_ragged_lengths_all_variants(pkv, bits, d, bs, causal):
 
 
 @pytest.mark.parametrize("bits", BITS)
+def test_quant_wide_dynamic_range_queries(pkv, bits):
+    # q entries spanning 2^-24 .. 2^8 (the kernel scales some dims by 2^-fpos before rounding
+    # to f16, so its tiniest entries go subnormal), an all-zero row and a single-spike row
+    lens = np.array([300, 1200, 77])
+    W = np.array([1, 4, 2])
+    b = wl.build_batch(61 + bits, name="qrange", lens=lens, n_new=W, q_rows=W, num_q_heads=8, num_kv_heads=2,
+                       head_dim=128, block_size=16, causal=True, with_sinks=True)
+    rng = np.random.default_rng(62 + bits)
+    q = rng.standard_normal(b.q[0].shape) * 2.0 ** rng.uniform(-24, 8, size=b.q[0].shape)
+    q[0] = 0.0
+    q[1] = 0.0
+    q[1, :, 5] = 37.0
+    b.q[0] = wl.f32_to_bf16_bits(q.astype(np.float32))
+    rec = wl.random_records(70 + bits, b, bits)[0]
+    _, out = _gpu_qstep(pkv, b, rec, bits)
+    _, ref = _oracle_qstep(b, rec, bits)
+    assert_close_to_oracle(out.float().cpu().numpy(), ref, what=f"q{bits} wide-range q")
+    _status_ok(pkv)
+
+
+@pytest.mark.parametrize("bits", BITS)
 @pytest.mark.parametrize("name", ["cb_mix", "spec_verify"])
 def test_quant_batch_vs_solo_bit_identical(pkv, bits, name):
     b = wl.make_workload(name, seed=4)
