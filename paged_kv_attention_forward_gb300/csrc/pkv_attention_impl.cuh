@@ -1367,12 +1367,18 @@ int launch_t(const CUtensorMap &mk, const CUtensorMap &mv, const AttnParams &prm
 #ifndef PKV_PREFILL_ROWS
 #define PKV_PREFILL_ROWS 64
 #endif
+// row warps of a wide-row CTA over quantised records, each with PKV_KW_QUANT key shares
+// (2: a Q8 verify call 408 -> 358 us against 3; 1: 418 us)
+#ifndef PKV_WIDE_NMT_QUANT
+#define PKV_WIDE_NMT_QUANT 2
+#endif
 template <int D, int BS, int BITS, bool WITH_TREE>
 int launch_d_bs(int rows, const CUtensorMap &mk, const CUtensorMap &mv, AttnParams prm,
                 long long pairs, int n_max, cudaStream_t st)
 {
+    constexpr int WIDE_NMT = BITS == 16 ? PKV_WIDE_NMT : PKV_WIDE_NMT_QUANT;
     const bool prefill = BITS == 16 && !prm.tree_masks && rows > PKV_PREFILL_ROWS;
-    const int per_cta = rows <= 8 ? 8 : prefill ? 8 * 2 * PKV_WIDE_NMT : 8 * PKV_WIDE_NN * PKV_WIDE_NMT;
+    const int per_cta = rows <= 8 ? 8 : prefill ? 8 * 2 * PKV_WIDE_NMT : 8 * PKV_WIDE_NN * WIDE_NMT;
     prm.row_groups = (rows + per_cta - 1) / per_cta;
     const long long gx = pairs * prm.row_groups;
     if (gx > 0x7fffffffLL || n_max > 65535)
@@ -1391,7 +1397,7 @@ int launch_d_bs(int rows, const CUtensorMap &mk, const CUtensorMap &mv, AttnPara
         if (prefill)
             return launch_t<D, BS, 2, PKV_WIDE_NMT, false, BITS>(mk, mv, prm, grid, st);
     }
-    return launch_t<D, BS, PKV_WIDE_NN, PKV_WIDE_NMT, false, BITS>(mk, mv, prm, grid, st);
+    return launch_t<D, BS, PKV_WIDE_NN, WIDE_NMT, false, BITS>(mk, mv, prm, grid, st);
 }
 
 struct WsLayout {
