@@ -608,8 +608,10 @@ def workload_description(b, layers):
 # ------------------------------------------------------------ oracle timing --
 def time_oracle_step(sub: wl.PagedBatch, threads: int, records=None, bits: int = 16):
     import oracle
+    # the append writes the same values into the same slots on every call, so the pool is
+    # used in place (copying a whole pool per step would cost more than the step)
     if records is not None:
-        rec = records.copy()
+        rec = records
         t = time.perf_counter()
         if int(sub.new_starts[-1]) > 0:
             oracle.paged_kv_append_quant(rec, sub.block_size, sub.head_dim, bits, sub.block_tables,
@@ -618,7 +620,7 @@ def time_oracle_step(sub: wl.PagedBatch, threads: int, records=None, bits: int =
                                      sub.block_tables, sub.context_lens, sinks=sub.sinks, causal=sub.causal,
                                      num_threads=threads)
         return time.perf_counter() - t
-    k, v = sub.k_pool[0].copy(), sub.v_pool[0].copy()
+    k, v = sub.k_pool[0], sub.v_pool[0]
     t = time.perf_counter()
     if int(sub.new_starts[-1]) > 0:
         oracle.paged_kv_append(k, v, sub.block_tables, sub.context_lens_old, sub.new_starts,
@@ -671,10 +673,12 @@ def run_reference(args, rank, world):
     budget_tokens = tok_per_s * 90.0 / (args.steps + args.warmup)
     chosen, tokens = [], 0
     for s in order:
-        if chosen and tokens + int(b.context_lens[s]) > budget_tokens:
+        if tokens + int(b.context_lens[s]) > budget_tokens:
             continue
         chosen.append(int(s))
         tokens += int(b.context_lens[s])
+    if not chosen:   # nothing fits: the shortest sequence alone
+        chosen = [int(np.argmin(b.context_lens))]
     sub = wl.select_seqs(b, sorted(chosen))
     acct = algorithmic_bytes(sub)
     for _ in range(args.warmup):
