@@ -1260,6 +1260,11 @@ paged_attention_combine_kernel(const AttnParams p)
 #ifndef PKV_KW_QUANT
 #define PKV_KW_QUANT 2
 #endif
+// key-share warps over 4- and 2-bit records (their per-block work is longer still:
+// a Q4 cb_mix call 273 -> 255 us with three)
+#ifndef PKV_KW_QUANT_NARROW
+#define PKV_KW_QUANT_NARROW 3
+#endif
 // Ring depth and key-share warps, chosen by measurement on GB300: decode CTAs are many
 // and small, wide-row CTAs hold several consumer warps on one ring; a quantised record
 // is half or a quarter of a bf16 stage, so its ring can be deeper at the same shared
@@ -1300,7 +1305,7 @@ constexpr int kStages()
 template <int BITS>
 constexpr int kKeyWarps()
 {
-    return BITS != 16 ? PKV_KW_QUANT : PKV_KW_BF16;
+    return BITS == 16 ? PKV_KW_BF16 : BITS == 8 ? PKV_KW_QUANT : PKV_KW_QUANT_NARROW;
 }
 
 template <int D, int BS, int NN, int NMT, int BITS, bool DEEP = false, bool GATHER = false>
@@ -1367,16 +1372,20 @@ int launch_t(const CUtensorMap &mk, const CUtensorMap &mv, const AttnParams &prm
 #ifndef PKV_PREFILL_ROWS
 #define PKV_PREFILL_ROWS 64
 #endif
-// row warps of a wide-row CTA over quantised records, each with PKV_KW_QUANT key shares
-// (2: a Q8 verify call 408 -> 358 us against 3; 1: 418 us)
+// row warps of a wide-row CTA over quantised records, each with the codec's key shares
+// (Q8, two key shares: 2 row warps -> a verify call 358 us, 3 -> 408 us, 1 -> 418 us;
+// Q4 / Q2, three key shares: 1 row warp -> a Q4 verify call 442 us, 2 -> 514 us)
 #ifndef PKV_WIDE_NMT_QUANT
 #define PKV_WIDE_NMT_QUANT 2
+#endif
+#ifndef PKV_WIDE_NMT_QUANT_NARROW
+#define PKV_WIDE_NMT_QUANT_NARROW 1
 #endif
 template <int D, int BS, int BITS, bool WITH_TREE>
 int launch_d_bs(int rows, const CUtensorMap &mk, const CUtensorMap &mv, AttnParams prm,
                 long long pairs, int n_max, cudaStream_t st)
 {
-    constexpr int WIDE_NMT = BITS == 16 ? PKV_WIDE_NMT : PKV_WIDE_NMT_QUANT;
+    constexpr int WIDE_NMT = BITS == 16 ? PKV_WIDE_NMT : BITS == 8 ? PKV_WIDE_NMT_QUANT : PKV_WIDE_NMT_QUANT_NARROW;
     const bool prefill = BITS == 16 && !prm.tree_masks && rows > PKV_PREFILL_ROWS;
     const int per_cta = rows <= 8 ? 8 : prefill ? 8 * 2 * PKV_WIDE_NMT : 8 * PKV_WIDE_NN * WIDE_NMT;
     prm.row_groups = (rows + per_cta - 1) / per_cta;
