@@ -1268,9 +1268,10 @@ paged_attention_combine_kernel(const AttnParams p)
 // Ring depth and key-share warps, chosen by measurement on GB300: decode CTAs are many
 // and small, wide-row CTAs hold several consumer warps on one ring; a quantised record
 // is half or a quarter of a bf16 stage, so its ring can be deeper at the same shared
-// memory.  Two key-share warps pay off for quantised records (their per-block work is
-// longer: 394 -> 309 us for a Q8 cb_mix call) but not for bf16 pools, whose verify
-// windows lose a third of their speed with them while decode gains 1 %.
+// memory.  Key-share warps pay off for quantised records (their per-block work is
+// longer: two took a Q8 cb_mix call 394 -> 309 us; 4- and 2-bit records take three) but
+// not for bf16 pools, whose verify windows lose a third of their speed with two while
+// decode gains 1 %.
 template <int BITS>
 constexpr int kKeyWarps();
 
