@@ -488,15 +488,38 @@ sample_chunks_kernel(const float *__restrict__ logits, int vocab, int chunk, int
     Best b = {-INFINITY, kNoIndex};
     if (vec_ok) {
         const float4 *row4 = reinterpret_cast<const float4 *>(row);
-        for (int i = (lo >> 2) + threadIdx.x; i < (hi >> 2); i += kArgmaxThreads) {
-            const float4 x = __ldcs(row4 + i);
-            uint32_t w[4] = {(uint32_t)i, pos, 0x6b657964u, 0u};
-            philox4x32_10(w, seed_lo, seed_hi);
-            const float xs[4] = {x.x, x.y, x.z, x.w};
+        // four float4 loads in flight per thread, then the (rare) kept tokens; the result does
+        // not depend on the visiting order (better() is a total order on (value, index))
+        constexpr int U = 4;
+        const int hi4 = hi >> 2;
+        for (int i0 = (lo >> 2) + threadIdx.x; i0 < hi4; i0 += U * kArgmaxThreads) {
+            float4 xv[U];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (xs[j] >= thr && order_key(xs[j], 4 * i + j) <= kcut)
-                    b = better(b, Best{__fadd_rn(__fdiv_rn(xs[j], temperature), gumbel_of(w[j])), 4 * i + j});
+            for (int u = 0; u < U; ++u) {
+                const int i = i0 + u * kArgmaxThreads;
+                xv[u] = i < hi4 ? __ldcs(row4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int i = i0 + u * kArgmaxThreads;
+                if (i >= hi4)
+                    break;
+                const float xs[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
+                bool keep[4], any = false;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    keep[j] = xs[j] >= thr && order_key(xs[j], 4 * i + j) <= kcut;
+                    any = any || keep[j];
+                }
+                if (!any)   // a token's draw depends only on (seed, position, token): skip unkept groups
+                    continue;
+                uint32_t w[4] = {(uint32_t)i, pos, 0x6b657964u, 0u};
+                philox4x32_10(w, seed_lo, seed_hi);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (keep[j])
+                        b = better(b, Best{__fadd_rn(__fdiv_rn(xs[j], temperature), gumbel_of(w[j])), 4 * i + j});
+            }
         }
     } else {
         for (int v = lo + threadIdx.x; v < hi; v += kArgmaxThreads) {
