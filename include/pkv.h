@@ -171,8 +171,8 @@ int paged_attention_workspace_init(void *workspace, size_t workspace_bytes, void
  *   workspace          >= paged_attention_workspace_size(...) bytes, 256-byte
  *                      aligned
  * Every row's arithmetic depends only on its own sequence (its length fixes
- * the split of the keys into fixed 512-token chunks; partials merge in chunk
- * order), so a row computed in any batch is bit-identical to the same row
+ * the split of the keys into fixed 512-token chunks and the order in which the
+ * chunks' partials merge), so a row computed in any batch is bit-identical to the same row
  * computed alone, and row w of a causal window is bit-identical to a one-row
  * decode over the first L - W + w + 1 keys.  Launches two kernels: the split
  * kernel and, as its programmatic dependent, the merge.
