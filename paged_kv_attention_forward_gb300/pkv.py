@@ -129,13 +129,19 @@ def _stream(stream) -> ctypes.c_void_p:
 def _dptr(t: Optional[torch.Tensor]):
     if t is None:
         return None
-    assert t.is_cuda and t.is_contiguous(), "expected a contiguous CUDA tensor"
+    if not (isinstance(t, torch.Tensor) and t.is_cuda and t.is_contiguous()):
+        raise ValueError("expected a contiguous CUDA tensor")
     return ctypes.c_void_p(t.data_ptr())
 
 
 def _pool(k_pool: torch.Tensor, v_pool: torch.Tensor) -> _Pool:
-    assert k_pool.dtype == torch.bfloat16 and v_pool.dtype == torch.bfloat16
-    assert k_pool.shape == v_pool.shape and k_pool.dim() == 4
+    for t in (k_pool, v_pool):
+        if not (isinstance(t, torch.Tensor) and t.is_cuda and t.is_contiguous()):
+            raise ValueError("K / V pools must be contiguous CUDA tensors")
+    if k_pool.dtype != torch.bfloat16 or v_pool.dtype != torch.bfloat16:
+        raise TypeError("K / V pools must be bfloat16")
+    if k_pool.shape != v_pool.shape or k_pool.dim() != 4:
+        raise ValueError("K / V pools must share one shape [num_blocks, H_kv, block_size, head_dim]")
     nb, hkv, bs, d = k_pool.shape
     return _Pool(k_pool.data_ptr(), v_pool.data_ptr(), nb, bs, hkv, d)
 
@@ -226,9 +232,13 @@ def qrecord_bytes(block_size: int, head_dim: int, bits: int) -> int:
 
 
 def _qpool(records: torch.Tensor, block_size: int, head_dim: int, bits: int) -> _QPool:
-    assert records.dtype == torch.uint8 and records.dim() == 3 and records.is_contiguous()
+    if not (isinstance(records, torch.Tensor) and records.is_cuda and records.is_contiguous()):
+        raise ValueError("records must be a contiguous CUDA tensor")
+    if records.dtype != torch.uint8 or records.dim() != 3:
+        raise TypeError("records must be uint8 [num_blocks, H_kv, record_bytes]")
     nb, hkv, rb = records.shape
-    assert rb == qrecord_bytes(block_size, head_dim, bits), "record size does not match the codec"
+    if rb != qrecord_bytes(block_size, head_dim, bits):
+        raise ValueError("record size does not match the codec")
     return _QPool(records.data_ptr(), nb, int(block_size), hkv, int(head_dim), int(bits))
 
 

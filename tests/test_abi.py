@@ -116,3 +116,20 @@ def test_host_validation_without_device(pkv):
     assert lib.paged_kv_append_quant(ctypes.byref(qp), 4096, 4, 4096, 4096, 4096, 4096, 1, 1, None) == -7
     assert lib.paged_attention_forward_quant(None, None, None, None, 0, None, 0, 0, 0, 0, 0, None, None, 0,
                                              0.0, None, 0, None, 0, None) == -1
+
+
+def test_binding_refuses_host_tensors():
+    # a host tensor must never reach the library as a device pointer
+    import torch
+    from paged_kv_attention_forward_gb300 import pkv
+    k = torch.zeros(2, 1, 16, 64, dtype=torch.bfloat16)
+    i32 = torch.zeros(2, dtype=torch.int32)
+    with pytest.raises(ValueError):
+        pkv.paged_kv_append(k, k, i32.view(2, 1), i32, torch.zeros(3, dtype=torch.int32), k[0], k[0])
+    with pytest.raises(ValueError):
+        pkv.paged_attention_forward(k, k, torch.zeros(1, 2, 64, dtype=torch.bfloat16), i32, i32.view(2, 1), i32,
+                                    max_context_len=16, max_q_rows_per_seq=1)
+    with pytest.raises(ValueError):
+        pkv.paged_attention_forward_quant(torch.zeros(2, 1, pkv.qrecord_bytes(16, 64, 8), dtype=torch.uint8),
+                                          16, 64, 8, torch.zeros(1, 2, 64, dtype=torch.bfloat16), i32,
+                                          i32.view(2, 1), i32, max_context_len=16, max_q_rows_per_seq=1)
