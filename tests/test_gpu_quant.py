@@ -204,5 +204,5 @@ def test_quant_host_side_argument_errors(pkv):
                                    pkv._dptr(g["context_lens_old"]), pkv._dptr(g["new_starts"]),
                                    pkv._dptr(g["k_new"]), pkv._dptr(g["v_new"]), b.num_seqs, 4, None)
     assert rc == -7
-    with pytest.raises(AssertionError):
+    with pytest.raises(ValueError):
         pkv._qpool(g["rec"], b.block_size, b.head_dim, 4)   # record size of another codec
