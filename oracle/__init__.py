@@ -71,6 +71,10 @@ def _load():
             lib.oracle_philox4x32_10.restype = None
             lib.oracle_keyed_log.argtypes = [ctypes.c_float]
             lib.oracle_keyed_log.restype = ctypes.c_float
+            lib.oracle_keyed_uniform_bits.argtypes = [ctypes.c_uint64, i32, i32]
+            lib.oracle_keyed_uniform_bits.restype = ctypes.c_uint32
+            lib.oracle_keyed_gumbel.argtypes = [ctypes.c_uint64, i32, i32]
+            lib.oracle_keyed_gumbel.restype = ctypes.c_float
             lib.oracle_spec_accept_sampled.argtypes = [P, i32, P, P, P, P, ctypes.c_uint64, ctypes.c_float,
                                                        i32, ctypes.c_float, ctypes.c_float, i32, P, P, P, P]
             lib.oracle_paged_attention_sparse.argtypes = [P, P, i32, i32, i32, i32, P, P, P, i32, P, i32, P, P,
@@ -265,6 +269,16 @@ def spec_accept_sampled(logits, q_starts, draft_tokens, positions, seed, tempera
 def topp_threshold(p_fix: int, total: int) -> int:
     """ceil(p_fix * total / 2^32): the weight a top-p prefix must reach."""
     return int(_load().oracle_topp_threshold(int(p_fix), int(total)))
+
+
+def keyed_uniform_bits(seed: int, pos: int, v: int) -> int:
+    """The 23-bit uniform code the keyed sampler gives token v at position pos under seed."""
+    return int(_load().oracle_keyed_uniform_bits(int(seed), int(pos), int(v)))
+
+
+def keyed_gumbel(seed: int, pos: int, v: int) -> float:
+    """Keyed Gumbel noise g = -log(-log(u)) of token v at position pos under seed (float32)."""
+    return float(_load().oracle_keyed_gumbel(int(seed), int(pos), int(v)))
 
 
 def keyed_exp2(y: float) -> float:

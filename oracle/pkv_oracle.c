@@ -432,18 +432,29 @@ float oracle_keyed_log(float x)
 }
 
 /*
- * Keyed Gumbel noise of token v at absolute position pos under `seed`: with
- * w = word (v mod 4) of Philox(ctr = (v / 4, pos, 0x6b657964, 0), key = seed),
- * u = ((w >> 9) + 1/2) / 2^23 and g = -log(-log(u)).  (One generator call keys
- * four consecutive tokens.)
+ * The 23-bit uniform code of token v at absolute position pos under `seed`: the top
+ * 23 bits (w >> 9) of word (v mod 4) of Philox4x32-10 with counter
+ * (v / 4, pos, 0x6b657964, 0) and key (seed low word, seed high word).  One generator
+ * call keys four consecutive tokens, which lets a GPU thread draw a group of four
+ * tokens with one call.  (TensorFold article, section "先记住一条铁律": a draw depends
+ * on seed, absolute position and token id only.)
  */
-static float keyed_gumbel(uint64_t seed, int32_t pos, int32_t v)
+uint32_t oracle_keyed_uniform_bits(uint64_t seed, int32_t pos, int32_t v)
 {
     const uint32_t ctr[4] = {(uint32_t)v >> 2, (uint32_t)pos, 0x6b657964u, 0u};
     const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
     uint32_t o[4];
     oracle_philox4x32_10(ctr, key, o);
-    const float u = ((float)(o[(uint32_t)v & 3u] >> 9) + 0.5f) * 0x1p-23f;
+    return o[(uint32_t)v & 3u] >> 9;
+}
+
+/*
+ * Keyed Gumbel noise of token v at position pos under `seed`: u = (code + 1/2) / 2^23
+ * with the code above, and g = -log(-log(u)) with the fixed float32 log.
+ */
+float oracle_keyed_gumbel(uint64_t seed, int32_t pos, int32_t v)
+{
+    const float u = ((float)oracle_keyed_uniform_bits(seed, pos, v) + 0.5f) * 0x1p-23f;
     const float E = -oracle_keyed_log(u);
     return -oracle_keyed_log(E);
 }
@@ -591,7 +602,7 @@ static int32_t keyed_draw(const float *row, int32_t vocab, uint64_t seed, int32_
             continue;
         if (filtered && !kept[v])
             continue;
-        const float sc = row[v] / temperature + keyed_gumbel(seed, pos, v);
+        const float sc = row[v] / temperature + oracle_keyed_gumbel(seed, pos, v);
         if (pick < 0 || sc > top) {
             top = sc;
             pick = v;

@@ -15,15 +15,71 @@ from scipy import stats
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
-def test_philox_known_answers(oracle_mod):
-    n = 0
+_M0, _M1 = 0xD2511F53, 0xCD9E8D57      # Philox4x32 round multipliers (Salmon et al., SC'11)
+_W0, _W1 = 0x9E3779B9, 0xBB67AE85      # key schedule (Weyl) increments
+
+
+def _philox_ref(ctr, key):
+    """Philox4x32-10 in plain Python integers, written from the generator's published
+    definition: ten rounds of two 32x32->64 multiplies with the key bumped between rounds."""
+    c = [int(x) & 0xFFFFFFFF for x in ctr]
+    k0, k1 = int(key[0]) & 0xFFFFFFFF, int(key[1]) & 0xFFFFFFFF
+    for rnd in range(10):
+        if rnd:
+            k0, k1 = (k0 + _W0) & 0xFFFFFFFF, (k1 + _W1) & 0xFFFFFFFF
+        p0, p1 = _M0 * c[0], _M1 * c[2]
+        c = [(p1 >> 32) ^ c[1] ^ k0, p1 & 0xFFFFFFFF, (p0 >> 32) ^ c[3] ^ k1, p0 & 0xFFFFFFFF]
+    return c
+
+
+def _kat_lines():
     for line in open(os.path.join(GOLDEN, "philox4x32_10_kat.txt")):
         if line.startswith("#") or not line.strip():
             continue
-        w = [int(x, 16) for x in line.split()]
+        yield [int(x, 16) for x in line.split()]
+
+
+def test_philox_known_answers(oracle_mod):
+    n = 0
+    for w in _kat_lines():
         assert oracle_mod.philox4x32_10(w[0:4], w[4:6]).tolist() == w[6:10]
+        assert _philox_ref(w[0:4], w[4:6]) == w[6:10]      # the test's own generator, same answers
         n += 1
     assert n == 3
+
+
+# (seed, position, token) cases for the counter layout: tokens 0-3 share counter 0 and
+# take words 0-3; token 4 starts counter 1; large positions, ids and 64-bit seeds reach
+# the high counter and key words.
+_KEYED_CASES = [(0, 0, v) for v in range(9)] + [
+    (0x243F6A8885A308D3, 123456, 151935), (0xFFFFFFFFFFFFFFFF, 0x7FFFFFFF, 0x7FFFFFFF),
+    (1, 2, 3), (7, 11, 4097), (0x13198A2E03707344, 99, 77), (42, 0, 151932)]
+
+
+@pytest.mark.parametrize("seed,pos,v", _KEYED_CASES)
+def test_keyed_uniform_counter_layout(oracle_mod, seed, pos, v):
+    """The draw of token v at position pos under seed is the top 23 bits of word v mod 4 of
+    Philox4x32-10 with counter (v / 4, pos, 0x6b657964, 0) and key (seed low, seed high)
+    (one generator call keys four consecutive tokens).  The expected word comes from the
+    test's own Philox, which the published known answers pin; swapping the word index or
+    the counter packing in the oracle fails here."""
+    words = _philox_ref([v >> 2, pos, 0x6B657964, 0], [seed & 0xFFFFFFFF, seed >> 32])
+    code = words[v & 3] >> 9
+    assert oracle_mod.keyed_uniform_bits(seed, pos, v) == code
+    # the Gumbel noise built on it: g = -log(-log(u)), u = (code + 1/2) / 2^23
+    u = (code + 0.5) / 2.0 ** 23
+    g_ref = -math.log(-math.log(u))
+    g = oracle_mod.keyed_gumbel(seed, pos, v)
+    assert abs(g - g_ref) <= 2e-6 * max(1.0, abs(g_ref)), (g, g_ref)
+
+
+def test_keyed_uniform_words_of_one_call_are_distinct_tokens(oracle_mod):
+    """Tokens 4c .. 4c+3 read the four different words of one generator call."""
+    for seed, pos in ((0, 0), (5, 1000)):
+        for c in range(4):
+            words = _philox_ref([c, pos, 0x6B657964, 0], [seed, 0])
+            got = [oracle_mod.keyed_uniform_bits(seed, pos, 4 * c + j) for j in range(4)]
+            assert got == [w >> 9 for w in words]
 
 
 def test_keyed_log_accuracy(oracle_mod):
@@ -118,11 +174,10 @@ def test_sampled_walk_accepts_exactly_the_matching_prefix(oracle_mod):
 
 
 def colliding_tokens(oracle_mod, seed, pos, limit=30000):
-    """Two token ids whose keyed uniforms (top 23 bits of Philox word 0) coincide."""
+    """Two token ids whose keyed uniform codes (as the oracle draws them) coincide."""
     seen = {}
-    key = [seed & 0xFFFFFFFF, seed >> 32]
     for v in range(limit):
-        u = int(oracle_mod.philox4x32_10([v >> 2, pos, 0x6B657964, 0], key)[v & 3]) >> 9
+        u = oracle_mod.keyed_uniform_bits(seed, pos, v)
         if u in seen:
             return seen[u], v
         seen[u] = v
