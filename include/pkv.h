@@ -250,11 +250,15 @@ int spec_accept_greedy(const float *logits, int32_t vocab,
  * The workspace lives in a fixed device array of PKV_NOALLOC_SCRATCH_BYTES
  * inside the library, which every GPU that loads the library holds until the
  * process exits.  Sizes whose paged_attention_workspace_size exceeds it are
- * rejected with PKV_ERR_WORKSPACE before anything is launched.  The first call
- * on a device looks the array's device address up (cudaGetSymbolAddress) with
- * that device current; make that first call before any stream capture.  Each
- * call launches the attention kernels with the array as their workspace; it
- * calls no allocator.  All calls on a device
+ * rejected with PKV_ERR_WORKSPACE before anything is launched.  Every call
+ * looks the array's device address up (cudaGetSymbolAddress) in the caller's
+ * current device and context, so a context created after cudaDeviceReset, or a
+ * driver-API context other than the primary one, gets its own copy of the
+ * array; the first call in a context may load the library's module there, so
+ * make that first call before any stream capture.  Each call launches the
+ * attention kernels with the array as their workspace (whose contents on entry
+ * do not matter: every partial is written before it is read); it calls no
+ * allocator.  All calls in a context
  * share the one array, which keeps the last call's contents: calls that may
  * overlap on the GPU (different streams without ordering) race and corrupt
  * each other's results.
@@ -469,6 +473,21 @@ const char *pkv_last_error_string(void);
  * or PKV_ERR_CUDA; *bits (if not NULL) receives the raw PKV_DEV_* bits.
  */
 int pkv_device_status(void *stream, int32_t *bits);
+
+/*
+ * Test hook for the failure path of the attention kernels' bounded waits.  Sets
+ * the limit, in SM clock cycles, that each stage wait of the attention pipeline
+ * (the consumer's wait for a staged tile, the producer's wait for a free stage)
+ * may take in the calls launched after it, process-wide.  0 makes every such wait
+ * give up at once, without testing its barrier: the kernel then records
+ * PKV_DEV_TIMEOUT, stops issuing copies, waits for the copies it already issued
+ * (that final wait always keeps the default limit) and returns, so the copies
+ * land and the context stays usable; the call's output is undefined.  A negative
+ * value restores the default (about two seconds of SM clock).  Not thread-safe
+ * with respect to calls launched concurrently from other threads.  Returns PKV_OK.
+ * (No passage of the pages; it exists to test the library's own error path.)
+ */
+int pkv_debug_set_wait_limit(long long cycles);
 
 #ifdef __cplusplus
 }

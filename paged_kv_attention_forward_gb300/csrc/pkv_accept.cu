@@ -778,13 +778,10 @@ extern "C" int spec_accept_sampled(const float *logits, int32_t vocab, const int
             if (use_k || use_p) {
                 cut = reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(workspace) + 2 * one);
                 const unsigned long long p_fix = use_p ? (unsigned long long)(top_p * 4294967296.0f) : 0ull;
-                static std::once_flag once;
-                static cudaError_t attr_err = cudaSuccess;
-                std::call_once(once, [] {
-                    attr_err = cudaFuncSetAttribute(topkp_cut_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                    (int)sizeof(SelSmem));
-                });
-                rc = check_cuda(attr_err, "spec_accept_sampled: shared memory attribute");
+                // set before every launch: the attribute belongs to the current context
+                rc = check_cuda(cudaFuncSetAttribute(topkp_cut_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     (int)sizeof(SelSmem)),
+                                "spec_accept_sampled: shared memory attribute");
                 if (rc)
                     return rc;
                 topkp_cut_kernel<<<total_rows, kSelThreads, sizeof(SelSmem), st>>>(

@@ -1,4 +1,5 @@
 // pkv_api.cu -- error reporting, the device status word and small shared host helpers.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -16,7 +17,6 @@ namespace {
 thread_local char t_last_error[512] = {0};
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
-int32_t *g_status_addr[kMaxDevices] = {nullptr};
 int g_sm_count[kMaxDevices] = {0};
 
 int current_device()
@@ -46,19 +46,22 @@ int check_cuda(cudaError_t e, const char *what)
     return set_error(PKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+namespace {
+std::atomic<long long> g_wait_limit{kWaitLimitCycles};
+}
+
+long long pipeline_wait_limit() { return g_wait_limit.load(std::memory_order_relaxed); }
+
 int32_t *device_status_word()
 {
-    const int dev = current_device();
-    if (dev < 0)
+    // Looked up on every call, in the caller's current context: a cached address
+    // would outlive a cudaDeviceReset or belong to another context of the same device
+    // (the module, and the word with it, is loaded again in each context).  The
+    // lookup is a host-side table query, not a stream operation.
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_pkv_device_status) != cudaSuccess)
         return nullptr;
-    std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_status_addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_pkv_device_status) != cudaSuccess)
-            return nullptr;
-        g_status_addr[dev] = static_cast<int32_t *>(p);
-    }
-    return g_status_addr[dev];
+    return static_cast<int32_t *>(p);
 }
 
 int sm_count()
@@ -81,6 +84,13 @@ int sm_count()
 extern "C" int pkv_abi_version(void) { return 2; }
 
 extern "C" const char *pkv_last_error_string(void) { return pkv::t_last_error; }
+
+extern "C" int pkv_debug_set_wait_limit(long long cycles)
+{
+    pkv::clear_error();
+    pkv::g_wait_limit.store(cycles < 0 ? pkv::kWaitLimitCycles : cycles, std::memory_order_relaxed);
+    return PKV_OK;
+}
 
 extern "C" int pkv_device_status(void *stream, int32_t *bits)
 {

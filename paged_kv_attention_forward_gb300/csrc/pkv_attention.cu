@@ -195,30 +195,21 @@ static __device__ __align__(256) uint8_t g_pkv_noalloc_scratch[PKV_NOALLOC_SCRAT
 
 namespace pkv {
 namespace {
-std::mutex g_noalloc_mutex;
-uint8_t *g_noalloc_ptr[64] = {nullptr};
-
-// Device address of the scratch array on the current device.  Looked up once per
-// device, with that device current: in host code the array's name is only a
-// host-side stand-in, never a device address.
+// Device address of the scratch array in the caller's current context.  In host code
+// the array's name is only a host-side stand-in, never a device address, so it is
+// looked up with cudaGetSymbolAddress -- on every call, with the caller's device and
+// context current: each context (a new one after cudaDeviceReset, or a driver-API
+// context other than the primary one) loads the module, and the array with it, at its
+// own address, so an address kept from an earlier call could name unmapped memory.
+// The lookup is a host-side query, not a stream operation.
 int noalloc_scratch(uint8_t **ptr)
 {
-    int dev = -1;
-    int rc = check_cuda(cudaGetDevice(&dev), "cudaGetDevice");
+    void *p = nullptr;
+    const int rc = check_cuda(cudaGetSymbolAddress(&p, g_pkv_noalloc_scratch),
+                              "cudaGetSymbolAddress of the allocation-free scratch");
     if (rc)
         return rc;
-    if (dev < 0 || dev >= 64)
-        return set_error(PKV_ERR_CUDA, "device ordinal %d out of range", dev);
-    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_ptr[dev]) {
-        void *p = nullptr;
-        rc = check_cuda(cudaGetSymbolAddress(&p, g_pkv_noalloc_scratch),
-                        "cudaGetSymbolAddress of the allocation-free scratch");
-        if (rc)
-            return rc;
-        g_noalloc_ptr[dev] = static_cast<uint8_t *>(p);
-    }
-    *ptr = g_noalloc_ptr[dev];
+    *ptr = static_cast<uint8_t *>(p);
     return PKV_OK;
 }
 }  // namespace

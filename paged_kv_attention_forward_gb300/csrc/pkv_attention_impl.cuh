@@ -109,6 +109,7 @@ struct AttnParams {
     const int32_t *key_counts;    // [R]
     int32_t max_keys;
     int32_t *status;
+    long long wait_limit;         // SM cycles a pipeline stage wait may take (<= 0: give up at once)
     int32_t num_seqs, max_blocks_per_seq, num_blocks, num_q_heads, num_kv_heads, group, block_size;
     int32_t n_max, max_context_len, max_rows, total_rows;
     int32_t row_groups;           // CTAs per (s, g, split), each taking 8 * NN * NMT rows
@@ -418,7 +419,7 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
             const int st = k % NST;
             bool ok = true;
             if (k >= NST)
-                ok = mbar_wait_bounded(&empty[st], ((k / NST) + 1) & 1, kWaitLimitCycles);
+                ok = mbar_wait_bounded(&empty[st], ((k / NST) + 1) & 1, p.wait_limit);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok || s_flag[1]) {
                 if (lane == 0) {
@@ -487,7 +488,7 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                 const int st = k % NST;
                 bool ok = true;
                 if (k >= NST)
-                    ok = mbar_wait_bounded(&empty[st], ((k / NST) + 1) & 1, kWaitLimitCycles);
+                    ok = mbar_wait_bounded(&empty[st], ((k / NST) + 1) & 1, p.wait_limit);
                 if (!ok)
                     atomicOr(p.status, PKV_DEV_TIMEOUT);
                 if (!ok || s_flag[1]) {
@@ -651,7 +652,7 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
 
         for (int k = kw; k < nstage; k += KW) {
             const int st = k % NST;
-            if (!mbar_wait_bounded(&full[st], (k / NST) & 1, kWaitLimitCycles)) {
+            if (!mbar_wait_bounded(&full[st], (k / NST) & 1, p.wait_limit)) {
                 if (lane == 0) {
                     atomicOr(p.status, PKV_DEV_TIMEOUT);
                     s_flag[1] = 1;
@@ -1328,11 +1329,9 @@ int launch_t(const CUtensorMap &mk, const CUtensorMap &mv, const AttnParams &prm
     constexpr int KW = GATHER ? 1 : kKeyWarps<BITS>();
     auto kern = paged_attention_kernel<D, BS, NN, NMT, NST, TREE, BITS, KW, GATHER>;
     const size_t smem = smem_bytes<D, BS, NN, NMT, BITS, DEEP, GATHER>();
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    });
+    // A function attribute belongs to a context: set it before every launch, so that a
+    // second device, or a context created after a reset, gets it too (the call is cheap).
+    const cudaError_t attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (attr_err != cudaSuccess)
         return check_cuda(attr_err, "cudaFuncSetAttribute(max dynamic smem)");
     kern<<<grid, (NMT * KW + 1) * 32, smem, st>>>(mk, mv, prm);
@@ -1532,6 +1531,7 @@ inline int attention_run(const char *who, const PoolView &pv, const void *q, con
     prm.key_counts = pv.key_counts;
     prm.max_keys = pv.max_keys;
     prm.status = status;
+    prm.wait_limit = pipeline_wait_limit();
     prm.num_seqs = num_seqs;
     prm.max_blocks_per_seq = max_blocks_per_seq;
     prm.num_blocks = pv.num_blocks;

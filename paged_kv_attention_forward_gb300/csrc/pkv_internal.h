@@ -13,8 +13,8 @@ namespace pkv {
 int set_error(int status, const char *fmt, ...);
 void clear_error();
 
-// Device address of the library's device status word on the current device
-// (looked up once per device with cudaGetSymbolAddress).  NULL on failure.
+// Device address of the library's device status word in the current context
+// (looked up with cudaGetSymbolAddress on every call).  NULL on failure.
 int32_t *device_status_word();
 
 // Streaming-multiprocessor count of the current device (cached per device).
@@ -39,5 +39,9 @@ constexpr int kMaxQHeads = 256;
 constexpr int kMaxGroupRows = 8192;  // G * max rows per sequence (row-group CTAs of 16 rows)
 // About two seconds of SM clock: the limit of any wait inside a kernel.
 constexpr long long kWaitLimitCycles = 4000000000LL;
+// Limit of the attention pipeline's stage waits for the next launches:
+// kWaitLimitCycles unless pkv_debug_set_wait_limit() changed it.  (The final wait
+// for a kernel's own copies in flight always uses kWaitLimitCycles.)
+long long pipeline_wait_limit();
 
 }  // namespace pkv

@@ -29,7 +29,7 @@ EXPORTED = ("pkv_abi_version", "paged_kv_append", "paged_attention_workspace_siz
             "spec_accept_greedy", "pkv_last_error_string", "pkv_device_status",
             "paged_attention_forward_noalloc", "paged_tree_attention_forward", "spec_accept_tree_greedy",
             "spec_accept_sampled", "paged_block_hashes", "pkv_qrecord_bytes", "paged_kv_append_quant",
-            "paged_attention_forward_quant", "paged_attention_forward_gather")
+            "paged_attention_forward_quant", "paged_attention_forward_gather", "pkv_debug_set_wait_limit")
 
 
 class PkvError(RuntimeError):
@@ -110,6 +110,8 @@ def lib(build_if_missing: bool = False):
             L.pkv_last_error_string.argtypes = []
             L.pkv_last_error_string.restype = ctypes.c_char_p
             L.pkv_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int32)]
+            L.pkv_debug_set_wait_limit.argtypes = [ctypes.c_longlong]
+            L.pkv_debug_set_wait_limit.restype = ctypes.c_int
             L.pkv_device_status.restype = ctypes.c_int
             _lib = L
         return _lib
@@ -396,3 +398,9 @@ def device_status(stream=None):
     bits = ctypes.c_int32(0)
     rc = lib().pkv_device_status(_stream(stream), ctypes.byref(bits))
     return rc, bits.value
+
+
+def debug_set_wait_limit(cycles: int):
+    """Test hook: the SM-cycle limit of the attention pipeline's stage waits in later calls
+    (0: give up at once, taking the kernels' timeout path; negative: the default)."""
+    _check(lib().pkv_debug_set_wait_limit(int(cycles)))
