@@ -93,6 +93,8 @@ def _load():
             lib.oracle_splitmix64_mix.restype = ctypes.c_uint64
             lib.oracle_block_hashes.argtypes = [P, P, i32, i32, ctypes.c_uint64, P, P, i32]
             lib.oracle_block_hashes.restype = ctypes.c_int
+            lib.oracle_block_allocate.argtypes = [P, P, P, P, i32, P, P, P, P, P, i32, i32, i32, P, P, P]
+            lib.oracle_block_allocate.restype = ctypes.c_int
             lib.oracle_qrecord_bytes.argtypes = [i32, i32, i32]
             lib.oracle_qrecord_bytes.restype = ctypes.c_size_t
             lib.oracle_kv_quantize_row.argtypes = [P, i32, i32, P, P]
@@ -322,6 +324,50 @@ def block_hashes(tokens, token_starts, block_size, seed, max_blocks_per_seq, cha
 
 
 # ------------------------------------------------------ quantised KV blocks --
+class BlockIndex:
+    """The prefix-sharing index of the block allocator as a plain list of entries:
+    keys uint64 [n], ids int32 [n] (-1: a key whose allocation failed), refs int32 [n]."""
+
+    def __init__(self, keys=(), ids=(), refs=()):
+        self.keys = np.asarray(keys, np.uint64).copy()
+        self.ids = np.asarray(ids, np.int32).copy()
+        self.refs = np.asarray(refs, np.int32).copy()
+
+    def as_dict(self):
+        return {int(k): (int(i), int(r)) for k, i, r in zip(self.keys, self.ids, self.refs)}
+
+
+def block_allocate(index: BlockIndex, free_ids, free_count: int, block_keys, context_lens, first_block,
+                   block_size: int, block_tables):
+    """Sequential block allocation with prefix sharing (see oracle_block_allocate).
+
+    block_keys uint64 [S, max_blocks]; block_tables int32 [S, max_blocks] (entries before
+    first_block are kept).  Returns (new BlockIndex, block_tables, fresh int32 [S, max_blocks],
+    free_count, status_bits)."""
+    lib = _load()
+    keys = _c(block_keys, np.uint64)
+    S, mb = keys.shape
+    tables = _c(block_tables, np.int32).copy()
+    fresh = np.zeros((S, mb), np.int32)
+    n0 = len(index.keys)
+    cap = n0 + S * mb + 1
+    ik = np.zeros(cap, np.uint64)
+    ii = np.zeros(cap, np.int32)
+    ir = np.zeros(cap, np.int32)
+    ik[:n0], ii[:n0], ir[:n0] = index.keys, index.ids, index.refs
+    n = np.array([n0], np.int32)
+    fc = np.array([free_count], np.int32)
+    bits = np.zeros(1, np.int32)
+    fids = _c(free_ids, np.int32)
+    rc = lib.oracle_block_allocate(_ptr(ik), _ptr(ii), _ptr(ir), _ptr(n), cap, _ptr(fids), _ptr(fc), _ptr(keys),
+                                   _ptr(_c(context_lens, np.int32)), _ptr(_c(first_block, np.int32)), S,
+                                   int(block_size), mb, _ptr(tables), _ptr(fresh), _ptr(bits))
+    if rc != 0:
+        raise RuntimeError("oracle_block_allocate failed")
+    k = int(n[0])
+    return BlockIndex(ik[:k], ii[:k], ir[:k]), tables, fresh, int(fc[0]), int(bits[0])
+
+
 def qrecord_bytes(block_size, head_dim, bits) -> int:
     """Bytes of one (block, KV head) record of the quantised pool."""
     return int(_load().oracle_qrecord_bytes(int(block_size), int(head_dim), int(bits)))

@@ -1137,3 +1137,119 @@ int oracle_paged_attention_sparse(const uint16_t *k_pool, const uint16_t *v_pool
     free(x);
     return rc;
 }
+
+/*
+ * Block allocation with prefix sharing (TensorSharp "高级功能", section "连续批处理与分页
+ * KV 缓存": KV blocks of fixed size come from one shared pool, and every full block is
+ * content-hashed so that identical prefixes share physical blocks; a partial block is
+ * never shared).  This is the sequential engine step the GPU call replaces, written as a
+ * plain loop over the sequences in order and, within a sequence, over its blocks in order:
+ *
+ *   sequence s holds L = context_lens[s] tokens in nb = ceil(L / B) blocks, of which the
+ *   first nk = floor(L / B) are full and carry the keys block_keys[s][j] (the chained
+ *   keys of paged_block_hashes); blocks j < first_block[s] are already allocated and
+ *   are left alone.  For j = first_block[s] .. nb - 1:
+ *     - a full block whose key is in the index with a block id: that block is shared
+ *       (table entry = its id, its reference count + 1, not fresh);
+ *     - a full block whose key is not (or whose earlier allocation failed in a previous
+ *       call): the key enters the index and takes a block popped from the free stack
+ *       (reference count 1, fresh: the caller must fill it); later blocks with that key
+ *       in this call share it;
+ *     - a partial block, or a full block whose key equals the reserved empty key
+ *       (all bits set), takes a private block popped from the stack (fresh).
+ *   The free stack holds free_ids[0 .. F-1]; the k-th pop of the call (k = 0, 1, ...)
+ *   takes free_ids[F - 1 - k].  A pop past the stack's end gives -1 and sets the
+ *   out-of-blocks bit (128); a key whose pop failed stays in the index without a block
+ *   (id -1) and its later occurrences in this call get -1 too.  A length needing more
+ *   than max_blocks blocks is cut to max_blocks and sets the table-overrun bit (2).
+ *
+ * The index is a list of n entries (key, id, refcount) with room for cap; it is searched
+ * linearly (this is the definition, not a fast map).  fresh [S][max_blocks] is set to 1
+ * for every block this call allocated and 0 elsewhere.  Returns 0, or -1 when the index
+ * has no room (cap entries) for a new key.
+ */
+int oracle_block_allocate(uint64_t *ix_keys, int32_t *ix_ids, int32_t *ix_refs, int32_t *n_entries, int32_t cap,
+                          const int32_t *free_ids, int32_t *free_count, const uint64_t *block_keys,
+                          const int32_t *context_lens, const int32_t *first_block, int32_t num_seqs,
+                          int32_t block_size, int32_t max_blocks, int32_t *block_tables, int32_t *fresh,
+                          int32_t *status_bits)
+{
+    const uint64_t kEmpty = ~0ull;
+    const int32_t F = *free_count;
+    int64_t pops = 0;
+    int32_t n = *n_entries;
+    int32_t bits = 0;
+    uint8_t *touched = (uint8_t *)calloc((size_t)(cap > 0 ? cap : 1), 1);
+    if (!touched)
+        return -1;
+    for (int64_t e = 0; e < (int64_t)num_seqs * max_blocks; ++e)
+        fresh[e] = 0;
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        const int64_t L = context_lens[s] < 0 ? 0 : context_lens[s];
+        int64_t nb = (L + block_size - 1) / block_size;
+        int64_t nk = L / block_size;
+        if (nb > max_blocks) {
+            nb = max_blocks;
+            bits |= 2;
+        }
+        if (nk > nb)
+            nk = nb;
+        const int64_t j0 = first_block[s] < 0 ? 0 : first_block[s];
+        for (int64_t j = j0; j < nb; ++j) {
+            const int64_t e = (int64_t)s * max_blocks + j;
+            int32_t id = -1;
+            int32_t is_fresh = 0;
+            const uint64_t key = block_keys[e];
+            if (j < nk && key != kEmpty) {
+                int32_t i = -1;
+                for (int32_t k = 0; k < n; ++k)
+                    if (ix_keys[k] == key) {
+                        i = k;
+                        break;
+                    }
+                if (i >= 0 && ix_ids[i] >= 0) {          /* shared: an earlier allocation of this key */
+                    id = ix_ids[i];
+                    ix_refs[i] += 1;
+                } else if (i >= 0 && touched[i]) {       /* its allocation failed earlier in this call */
+                    id = -1;
+                } else {                                 /* a new key: pop a block for it */
+                    if (i < 0) {
+                        if (n >= cap) {
+                            free(touched);
+                            return -1;
+                        }
+                        i = n++;
+                        ix_keys[i] = key;
+                        ix_ids[i] = -1;
+                        ix_refs[i] = 0;
+                    }
+                    touched[i] = 1;
+                    if (pops < F) {
+                        id = free_ids[F - 1 - pops];
+                        ix_ids[i] = id;
+                        ix_refs[i] = 1;
+                        is_fresh = 1;
+                    } else {
+                        bits |= 128;
+                    }
+                    ++pops;
+                }
+            } else {                                     /* a private block */
+                if (pops < F) {
+                    id = free_ids[F - 1 - pops];
+                    is_fresh = 1;
+                } else {
+                    bits |= 128;
+                }
+                ++pops;
+            }
+            block_tables[e] = id;
+            fresh[e] = is_fresh;
+        }
+    }
+    *free_count = pops < F ? (int32_t)(F - pops) : 0;
+    *n_entries = n;
+    *status_bits = bits;
+    free(touched);
+    return 0;
+}
