@@ -64,7 +64,8 @@ typedef enum pkv_status {
     PKV_ERR_BAD_BLOCK = -5,   /* (device) block id outside the pool / table overrun  */
     PKV_ERR_CUDA = -6,        /* a CUDA runtime call or kernel launch failed         */
     PKV_ERR_ALIGN = -7,       /* a pointer is not 16-byte aligned                    */
-    PKV_ERR_TIMEOUT = -8      /* (device) a bounded wait inside a kernel expired     */
+    PKV_ERR_TIMEOUT = -8,     /* (device) a bounded wait inside a kernel expired     */
+    PKV_ERR_OUT_OF_BLOCKS = -9 /* (device) the free stack or the block index ran out */
 } pkv_status;
 
 enum { PKV_DTYPE_BF16 = 0, PKV_DTYPE_F32 = 1 };
@@ -78,7 +79,9 @@ enum {
     PKV_DEV_WORKSPACE = 8,     /* (reserved)                                              */
     PKV_DEV_TIMEOUT = 16,      /* a bounded wait expired                                  */
     PKV_DEV_BAD_TREE = 32,     /* a draft tree whose parent indices are not topological   */
-    PKV_DEV_BAD_RANGE = 64     /* a token range outside [0, total_tokens]                 */
+    PKV_DEV_BAD_RANGE = 64,    /* a token range outside [0, total_tokens]                 */
+    PKV_DEV_OUT_OF_BLOCKS = 128, /* the block allocator's free stack ran out               */
+    PKV_DEV_INDEX_FULL = 256   /* the block index had no free slot for a new key          */
 };
 
 /* One layer's K/V block pool (host struct holding device pointers).
@@ -462,6 +465,73 @@ int paged_attention_forward_quant(const pkv_qpool *pool, const void *q, const in
                                   int32_t out_dtype, void *workspace, size_t workspace_bytes,
                                   void *stream);
 
+/*
+ * Block allocation with prefix sharing (TensorSharp "高级功能", section "连续批处理与分页
+ * KV 缓存": KV blocks of a fixed size come from one shared pool; every full block is
+ * content-hashed so that identical prefixes map to the same physical blocks; a partial
+ * block is never shared).
+ *
+ * The index (all arrays device memory, owned by the caller):
+ *   keys       uint64 [capacity]: a block key (from paged_block_hashes), or
+ *              PKV_BLOCK_KEY_EMPTY in a free slot
+ *   block_ids  int32 [capacity]: the physical block holding the key's contents
+ *              (negative: the key has no block, e.g. its allocation ran out)
+ *   refcounts  int32 [capacity]: how many block-table entries name that block
+ *   capacity   slots, a power of two; keep the index at most about half full
+ *              (open addressing with linear probing)
+ *   free_ids   int32 [...]: a stack of free physical block ids, free_ids[0 .. *free_count)
+ *   free_count int32 [1]: ids on the stack
+ * The caller fills free_ids; paged_block_index_init empties every slot and sets
+ * *free_count.  A key equal to PKV_BLOCK_KEY_EMPTY cannot be indexed: its block is
+ * allocated as a private one.
+ */
+#define PKV_BLOCK_KEY_EMPTY 0xFFFFFFFFFFFFFFFFull
+typedef struct pkv_block_index {
+    uint64_t *keys;
+    int32_t *block_ids;
+    int32_t *refcounts;
+    int32_t capacity;
+    int32_t *free_ids;
+    int32_t *free_count;
+} pkv_block_index;
+
+/* Empty every slot of the index and set *free_count = num_free.  One launch. */
+int paged_block_index_init(const pkv_block_index *index, int32_t num_free, void *stream);
+
+/* Workspace bytes paged_block_allocate needs for num_seqs x max_blocks_per_seq entries. */
+size_t paged_block_allocate_workspace_size(int32_t num_seqs, int32_t max_blocks_per_seq);
+
+/*
+ * Fill block tables from the index and the free stack.  Sequence s holds
+ * L = context_lens[s] tokens in nb = ceil(L / block_size) blocks; the first
+ * nk = floor(L / block_size) are full and carry the keys block_keys[s][j] (the layout
+ * paged_block_hashes writes); entries j < first_block[s] are already allocated and
+ * are left alone.  For j = first_block[s] .. nb - 1:
+ *   - a full block whose key has a block in the index shares it (table entry = that
+ *     id, its reference count + 1, fresh 0);
+ *   - a full block whose key has none takes a block from the free stack; later blocks
+ *     with the same key in this call share it (fresh 1 for the first, 0 for the rest);
+ *   - a partial block takes a private block from the free stack (fresh 1).
+ * The result is the sequential engine step: sequences in order, blocks in order, the
+ * k-th pop of the call taking free_ids[F - 1 - k] (F = *free_count on entry), however
+ * the kernels' threads interleave.  fresh[s][j] (may be NULL) is set for every entry:
+ * 1 where this call allocated a block the caller must fill, else 0.  A pop past the
+ * stack's end gives -1 (the key, if any, stays without a block) and sets
+ * PKV_DEV_OUT_OF_BLOCKS; a key that finds no free slot gets a private block and sets
+ * PKV_DEV_INDEX_FULL (the results are then not the sequential ones); a length past
+ * max_blocks_per_seq * block_size is cut there and sets PKV_DEV_TABLE_OVERRUN.
+ *   block_keys    uint64 [num_seqs][max_blocks_per_seq] (device, 8-byte aligned)
+ *   context_lens, first_block   int32 [num_seqs] (device)
+ *   block_tables  int32 [num_seqs][max_blocks_per_seq] (device, in / out)
+ *   workspace     paged_block_allocate_workspace_size bytes, 256-byte aligned; its
+ *                 contents on entry do not matter
+ * Calls that use one index must be ordered on the GPU (one stream).  Three launches.
+ */
+int paged_block_allocate(const pkv_block_index *index, const uint64_t *block_keys,
+                         const int32_t *context_lens, const int32_t *first_block, int32_t num_seqs,
+                         int32_t block_size, int32_t max_blocks_per_seq, int32_t *block_tables,
+                         int32_t *fresh, void *workspace, size_t workspace_bytes, void *stream);
+
 /* Text of the calling thread's last error ("" if none). */
 const char *pkv_last_error_string(void);
 
@@ -469,7 +539,7 @@ const char *pkv_last_error_string(void);
  * Synchronise `stream`, then read and clear the device status word of the
  * current device.  Returns PKV_OK, PKV_ERR_BAD_BLOCK (bad block id or table
  * overrun), PKV_ERR_SHAPE (too many rows, a bad draft tree or a bad token
- * range), PKV_ERR_TIMEOUT,
+ * range), PKV_ERR_TIMEOUT, PKV_ERR_OUT_OF_BLOCKS (the allocator ran out),
  * or PKV_ERR_CUDA; *bits (if not NULL) receives the raw PKV_DEV_* bits.
  */
 int pkv_device_status(void *stream, int32_t *bits);

@@ -117,6 +117,9 @@ extern "C" int pkv_device_status(void *stream, int32_t *bits)
         *bits = host;
     if (host & PKV_DEV_TIMEOUT)
         return pkv::set_error(PKV_ERR_TIMEOUT, "a bounded wait inside a kernel expired (bits 0x%x)", host);
+    if (host & (PKV_DEV_OUT_OF_BLOCKS | PKV_DEV_INDEX_FULL))
+        return pkv::set_error(PKV_ERR_OUT_OF_BLOCKS,
+                              "the block allocator ran out of free blocks or index slots (bits 0x%x)", host);
     if (host & (PKV_DEV_BAD_BLOCK | PKV_DEV_TABLE_OVERRUN))
         return pkv::set_error(PKV_ERR_BAD_BLOCK,
                               "a kernel met a block id outside the pool or a length past the "

@@ -21,7 +21,8 @@ PKV_DTYPE_BF16 = 0
 PKV_DTYPE_F32 = 1
 STATUS_NAMES = {0: "PKV_OK", -1: "PKV_ERR_NULL", -2: "PKV_ERR_SHAPE", -3: "PKV_ERR_UNSUPPORTED",
                 -4: "PKV_ERR_WORKSPACE", -5: "PKV_ERR_BAD_BLOCK", -6: "PKV_ERR_CUDA",
-                -7: "PKV_ERR_ALIGN", -8: "PKV_ERR_TIMEOUT"}
+                -7: "PKV_ERR_ALIGN", -8: "PKV_ERR_TIMEOUT", -9: "PKV_ERR_OUT_OF_BLOCKS"}
+PKV_BLOCK_KEY_EMPTY = 0xFFFFFFFFFFFFFFFF
 
 # every exported symbol of include/pkv.h
 EXPORTED = ("pkv_abi_version", "paged_kv_append", "paged_attention_workspace_size",
@@ -29,7 +30,8 @@ EXPORTED = ("pkv_abi_version", "paged_kv_append", "paged_attention_workspace_siz
             "spec_accept_greedy", "pkv_last_error_string", "pkv_device_status",
             "paged_attention_forward_noalloc", "paged_tree_attention_forward", "spec_accept_tree_greedy",
             "spec_accept_sampled", "paged_block_hashes", "pkv_qrecord_bytes", "paged_kv_append_quant",
-            "paged_attention_forward_quant", "paged_attention_forward_gather", "pkv_debug_set_wait_limit")
+            "paged_attention_forward_quant", "paged_attention_forward_gather", "pkv_debug_set_wait_limit",
+            "paged_block_index_init", "paged_block_allocate_workspace_size", "paged_block_allocate")
 
 
 class PkvError(RuntimeError):
@@ -47,6 +49,11 @@ class _Pool(ctypes.Structure):
 class _QPool(ctypes.Structure):
     _fields_ = [("records", ctypes.c_void_p), ("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("bits", ctypes.c_int32)]
+
+
+class _BlockIndexC(ctypes.Structure):
+    _fields_ = [("keys", ctypes.c_void_p), ("block_ids", ctypes.c_void_p), ("refcounts", ctypes.c_void_p),
+                ("capacity", ctypes.c_int32), ("free_ids", ctypes.c_void_p), ("free_count", ctypes.c_void_p)]
 
 
 _lock = threading.Lock()
@@ -110,6 +117,12 @@ def lib(build_if_missing: bool = False):
             L.pkv_last_error_string.argtypes = []
             L.pkv_last_error_string.restype = ctypes.c_char_p
             L.pkv_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int32)]
+            L.paged_block_index_init.argtypes = [ctypes.POINTER(_BlockIndexC), i32, P]
+            L.paged_block_index_init.restype = ctypes.c_int
+            L.paged_block_allocate_workspace_size.argtypes = [i32, i32]
+            L.paged_block_allocate_workspace_size.restype = sz
+            L.paged_block_allocate.argtypes = [ctypes.POINTER(_BlockIndexC), P, P, P, i32, i32, i32, P, P, P, sz, P]
+            L.paged_block_allocate.restype = ctypes.c_int
             L.pkv_debug_set_wait_limit.argtypes = [ctypes.c_longlong]
             L.pkv_debug_set_wait_limit.restype = ctypes.c_int
             L.pkv_device_status.restype = ctypes.c_int
@@ -404,3 +417,51 @@ def debug_set_wait_limit(cycles: int):
     """Test hook: the SM-cycle limit of the attention pipeline's stage waits in later calls
     (0: give up at once, taking the kernels' timeout path; negative: the default)."""
     _check(lib().pkv_debug_set_wait_limit(int(cycles)))
+
+
+class BlockIndex:
+    """Device block index and free stack for paged_block_allocate (see include/pkv.h).
+
+    keys int64 [capacity] (the uint64 keys' bits), block_ids / refcounts int32 [capacity],
+    free_ids int32 [n], free_count int32 [1]; all CUDA tensors owned here."""
+
+    def __init__(self, capacity: int, free_ids: torch.Tensor, device="cuda", stream=None):
+        if capacity < 1 or capacity & (capacity - 1):
+            raise ValueError("capacity must be a positive power of two")
+        self.keys = torch.empty(capacity, dtype=torch.int64, device=device)
+        self.block_ids = torch.empty(capacity, dtype=torch.int32, device=device)
+        self.refcounts = torch.empty(capacity, dtype=torch.int32, device=device)
+        self.free_ids = free_ids.to(device=device, dtype=torch.int32).contiguous()
+        self.free_count = torch.empty(1, dtype=torch.int32, device=device)
+        _check(lib().paged_block_index_init(ctypes.byref(self._c()), self.free_ids.numel(), _stream(stream)))
+
+    def _c(self) -> _BlockIndexC:
+        return _BlockIndexC(self.keys.data_ptr(), self.block_ids.data_ptr(), self.refcounts.data_ptr(),
+                            self.keys.numel(), self.free_ids.data_ptr(), self.free_count.data_ptr())
+
+    def entries(self):
+        """The index as {key (uint64 int): (block id, refcount)} (host copy of the occupied slots)."""
+        k = self.keys.cpu().numpy().view("uint64")
+        i = self.block_ids.cpu().numpy()
+        r = self.refcounts.cpu().numpy()
+        return {int(a): (int(b) if b >= 0 else -1, int(c)) for a, b, c in zip(k, i, r)
+                if int(a) != PKV_BLOCK_KEY_EMPTY}
+
+
+def paged_block_allocate(index: BlockIndex, block_keys, context_lens, first_block, block_size: int, block_tables,
+                         *, fresh: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                         stream=None) -> torch.Tensor:
+    """Fill block_tables [S, max_blocks] in place from the index (see include/pkv.h); returns
+    fresh int32 [S, max_blocks] (1 where a block was allocated that the caller must fill)."""
+    S, mb = block_tables.shape
+    if block_keys.dtype not in (torch.int64, torch.uint64) or tuple(block_keys.shape) != (S, mb):
+        raise ValueError("block_keys must be 64-bit [num_seqs, max_blocks_per_seq]")
+    if fresh is None:
+        fresh = torch.empty((S, mb), dtype=torch.int32, device=block_tables.device)
+    if workspace is None:
+        n = lib().paged_block_allocate_workspace_size(S, mb)
+        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=block_tables.device)
+    _check(lib().paged_block_allocate(ctypes.byref(index._c()), _dptr(block_keys), _dptr(context_lens),
+                                      _dptr(first_block), S, int(block_size), mb, _dptr(block_tables), _dptr(fresh),
+                                      _dptr(workspace), workspace.numel(), _stream(stream)))
+    return fresh

@@ -100,6 +100,20 @@ def test_host_validation_without_device(pkv):
     assert lib.paged_block_hashes(4096, 4096, -1, 16, 16, 0, None, 4096, 4, None) == -2
     assert lib.paged_block_hashes(4096, 4096, 1, 16, 16, 0, None, 4096 + 4, 4, None) == -7
     assert lib.paged_block_hashes(4096, 4096, 0, 16, 16, 0, None, 4096, 4, None) == 0
+    # block allocation: checks made before any CUDA call
+    bi = pkv._BlockIndexC(4096, 4096, 4096, 48, 4096, 4096)       # capacity not a power of two
+    assert lib.paged_block_allocate(ctypes.byref(bi), 4096, 4096, 4096, 1, 16, 4, 4096, None, 4096, 1 << 20,
+                                    None) == -2
+    assert lib.paged_block_allocate(None, 4096, 4096, 4096, 1, 16, 4, 4096, None, 4096, 1 << 20, None) == -1
+    bi.capacity = 64
+    assert lib.paged_block_allocate(ctypes.byref(bi), 4096, 4096, 4096, 1, 16, 4, 4096, None, 4096, 8,
+                                    None) == -4
+    assert lib.paged_block_allocate(ctypes.byref(bi), 4096 + 4, 4096, 4096, 1, 16, 4, 4096, None, 4096, 1 << 20,
+                                    None) == -7
+    assert lib.paged_block_allocate(ctypes.byref(bi), 4096, 4096, 4096, 0, 16, 4, 4096, None, 4096, 1 << 20,
+                                    None) == 0
+    assert lib.paged_block_allocate_workspace_size(3, 5) == 256
+    assert lib.paged_block_index_init(ctypes.byref(bi), -1, None) == -2
     # quantised pool: record size and the checks made before any CUDA call
     assert lib.pkv_qrecord_bytes(16, 128, 8) == 2 * 16 * 128 + 8 * 16
     assert lib.pkv_qrecord_bytes(32, 64, 4) == 2 * 32 * 32 + 8 * 32
