@@ -224,6 +224,8 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
+    if getattr(args, "kernel", "mma") == "tcgen05":
+        pkv.set_attention_kernel(pkv.PKV_KERNEL_TCGEN05)
     layers = 40 if args.workload == "ministral_decode" else 1
     b = wl.make_workload(args.workload, seed=replica_seed(args.seed, rank), layers=layers,
                          num_seqs=args.num_seqs)
@@ -544,7 +546,8 @@ def run_ours(args, rank, world, local_rank):
     achieved = per_launch_bytes / (attn_avg_ms * 1e-3) / 1e9
     flops = algorithmic_flops(b)
     attn_tflops = flops / (attn_avg_ms * 1e-3) / 1e12
-    kernel_tag = "paged_attention" if not quant else f"paged_attention_q{bits}"
+    kernel_tag = ("paged_attention" if not quant else f"paged_attention_q{bits}") + (
+        "_tcgen05" if getattr(args, "kernel", "mma") == "tcgen05" and not quant else "")
     traffic = stored_traffic(kernel_tag, args.workload)
     value = whole_job_rate(acct["step"], world, ms_per_step) / 1e9
     e2e_value = whole_job_rate(acct["step"], world, e2e_ms_per_step) / 1e9
@@ -562,7 +565,8 @@ def run_ours(args, rank, world, local_rank):
                    "seed": args.seed,
                    "accept": None if b.logits is None else accept_mode,
                    "launch": "cuda graph (one captured step, replayed)" if graph else "eager",
-                   "kv_codec": "bf16" if not quant else f"q{bits} (per-row float32 scale)"},
+                   "kv_codec": "bf16" if not quant else f"q{bits} (per-row float32 scale)",
+                   "kernel": "tcgen05" if getattr(args, "kernel", "mma") == "tcgen05" and not quant else "mma.sync"},
         "query_rows_per_s": round(rows_per_s, 1),
         "frac_of_measured_hbm": round(value / peak, 4),
         "frac_of_nominal_8tbs": round(value / 8000.0, 4),
@@ -713,6 +717,8 @@ def main():
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="resize the batch (same per-sequence distribution); for profiling smaller cases")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", choices=("mma", "tcgen05"), default="mma",
+                    help="kernel of the bf16 attention calls (pkv_set_attention_kernel)")
     ap.add_argument("--eager", action="store_true",
                     help="launch every kernel of every step directly instead of replaying a captured CUDA graph")
     ap.add_argument("--kv-bits", type=int, choices=(16, 8, 4, 2), default=16,

@@ -545,6 +545,24 @@ const char *pkv_last_error_string(void);
 int pkv_device_status(void *stream, int32_t *bits);
 
 /*
+ * The kernel that serves the bf16 attention calls (paged_attention_forward and its
+ * allocation-free variant, paged_tree_attention_forward, paged_attention_forward_gather),
+ * process-wide, for the calls launched after it:
+ *   PKV_KERNEL_MMA_SYNC (the default): warp-level mma.sync tiles of 16 keys, many small
+ *     CTAs per SM;
+ *   PKV_KERNEL_TCGEN05: 5th-generation tensor cores (tcgen05.mma, accumulators in tensor
+ *     memory), 128-key tiles, one persistent CTA per SM fed by a one-CTA unit pass.
+ * Both give results within the same tolerance of the exact attention, and with either a
+ * row's arithmetic depends only on its own sequence (batch / solo and verify-row / decode
+ * invariance hold), but the two kernels round differently: switch only between workloads,
+ * never between calls whose rows must agree bit for bit.  The quantised pools always use
+ * the mma.sync kernel.  Returns PKV_OK, or PKV_ERR_SHAPE for an unknown value.  (No passage
+ * of the pages; it selects between two implementations of the same operation.)
+ */
+enum { PKV_KERNEL_MMA_SYNC = 0, PKV_KERNEL_TCGEN05 = 1 };
+int pkv_set_attention_kernel(int32_t which);
+
+/*
  * Test hook for the failure path of the attention kernels' bounded waits.  Sets
  * the limit, in SM clock cycles, that each stage wait of the attention pipeline
  * (the consumer's wait for a staged tile, the producer's wait for a free stage)

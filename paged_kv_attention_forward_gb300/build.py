@@ -37,7 +37,7 @@ def sources():
 # the files the attention kernels are compiled from (a profile of those kernels stays
 # valid while these are unchanged)
 ATTENTION_SOURCES = ("pkv_attention_impl.cuh", "pkv_attention.cu", "pkv_attention_quant.cu", "pkv_ptx.cuh",
-                     "pkv_internal.h")
+                     "pkv_internal.h", "pkv_attention_tc.cuh", "pkv_tc.cuh")
 
 
 _COMMENT = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)

@@ -5,10 +5,59 @@
 // variant), and the TensorFold article, section "先记住一条铁律" (verify rows use
 // the serial step's arithmetic; a batched row equals the row alone).  The kernels
 // and the shared argument checks are in pkv_attention_impl.cuh.
-#include "pkv_attention_impl.cuh"
+#include <atomic>
+
+#include "pkv_attention_tc.cuh"
+
+// Which kernel serves the bf16 paths (decode, verify windows, draft trees, prefill chunks,
+// the index-list gather): pkv_set_attention_kernel() chooses, process-wide, between the
+// mma.sync kernel (the default) and the tcgen05 kernel of pkv_attention_tc.cuh.  Each keeps
+// every row's arithmetic a function of its own sequence, but their arithmetic differs, so a
+// row computed by one is not bit-identical to the row computed by the other.  The mma.sync
+// kernel is the default because it is faster at these row counts: a tcgen05 MMA of 128 keys
+// costs about 55 SM cycles for any N up to 64, and one softmax pipeline per SM (its 64 KB
+// K / V stages leave room for no second) cannot hide the latency that many small mma.sync
+// CTAs hide.  The quantised pools always use the mma.sync kernel.
+static std::atomic<int> g_attention_kernel{PKV_KERNEL_MMA_SYNC};
 
 namespace pkv {
 namespace {
+
+// Unit-pass arguments of an attention call; num_src = sequences, or query rows for the
+// index-list gather.
+UnitPassParams unit_pass_params(const AttnParams &prm, int num_src)
+{
+    UnitPassParams up;
+    memset(&up, 0, sizeof up);
+    up.q_starts = prm.q_starts;
+    up.context_lens = prm.context_lens;
+    up.key_counts = prm.key_counts;
+    up.units = const_cast<int4 *>(prm.units);
+    up.ctl = prm.unit_ctl;
+    up.status = prm.status;
+    up.num_src = num_src;
+    up.num_seqs = prm.num_seqs;
+    up.total_rows = prm.total_rows;
+    up.max_rows = prm.max_rows;
+    up.group = prm.group;
+    up.num_kv_heads = prm.num_kv_heads;
+    up.max_keys = prm.max_keys;
+    up.L_cap = (int)std::min<long long>(prm.max_context_len, (long long)prm.max_blocks_per_seq * prm.block_size);
+    up.n_max = prm.n_max;
+    up.unit_cap = prm.unit_cap;
+    return up;
+}
+
+int tc_limits(const char *who, int num_src, int n_max)
+{
+    if (num_src > kTcMaxSeqs)
+        return set_error(PKV_ERR_UNSUPPORTED, "%s: %d sequences (or gather rows) in one call; at most %d", who,
+                         num_src, kTcMaxSeqs);
+    if (n_max > kTcMaxSplits)
+        return set_error(PKV_ERR_UNSUPPORTED, "%s: contexts up to %d tokens in one call", who,
+                         kTcMaxSplits * kSplitTokens);
+    return PKV_OK;
+}
 
 // ---------------------------------------------------------------- host side --
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -68,6 +117,16 @@ int launch_bf16(const PoolView &pv, AttnParams &prm, int rows, long long pairs, 
     if (rc)
         return rc;
     const int D = pv.head_dim, BS = pv.block_size;
+    if (g_attention_kernel.load(std::memory_order_relaxed) == PKV_KERNEL_TCGEN05) {
+        rc = tc_limits("paged attention", prm.num_seqs, n_max);
+        if (rc)
+            return rc;
+        const UnitPassParams up = unit_pass_params(prm, prm.num_seqs);
+        if (D == 64 && BS == 16) return launch_tc<64, 16, false>(rows, mk, mv, prm, up, st);
+        if (D == 64 && BS == 32) return launch_tc<64, 32, false>(rows, mk, mv, prm, up, st);
+        if (D == 128 && BS == 16) return launch_tc<128, 16, false>(rows, mk, mv, prm, up, st);
+        return launch_tc<128, 32, false>(rows, mk, mv, prm, up, st);
+    }
     if (D == 64 && BS == 16) return launch_d_bs<64, 16, 16, true>(rows, mk, mv, prm, pairs, n_max, st);
     if (D == 64 && BS == 32) return launch_d_bs<64, 32, 16, true>(rows, mk, mv, prm, pairs, n_max, st);
     if (D == 128 && BS == 16) return launch_d_bs<128, 16, 16, true>(rows, mk, mv, prm, pairs, n_max, st);
@@ -100,6 +159,17 @@ int launch_gather_d(int rows, AttnParams prm, long long pairs, int n_max, cudaSt
 int launch_gather(const PoolView &pv, AttnParams &prm, int rows, long long /*pairs*/, int n_max, cudaStream_t st)
 {
     const long long pairs = (long long)prm.total_rows * pv.num_kv_heads;
+    if (g_attention_kernel.load(std::memory_order_relaxed) == PKV_KERNEL_TCGEN05) {
+        int rc = tc_limits("paged_attention_forward_gather", prm.total_rows, n_max);
+        if (rc)
+            return rc;
+        CUtensorMap none;
+        memset(&none, 0, sizeof none);
+        const UnitPassParams up = unit_pass_params(prm, prm.total_rows);
+        if (pv.head_dim == 64)
+            return launch_tc<64, 16, true>(rows, none, none, prm, up, st);
+        return launch_tc<128, 16, true>(rows, none, none, prm, up, st);
+    }
     if (pv.head_dim == 64)
         return launch_gather_d<64>(rows, prm, pairs, n_max, st);
     return launch_gather_d<128>(rows, prm, pairs, n_max, st);
@@ -279,4 +349,13 @@ extern "C" int paged_attention_forward_gather(const pkv_pool *pool, const void *
     return attention_run(who, pv, q, q_starts, block_tables, max_blocks_per_seq, context_lens, num_seqs,
                          total_q_rows, max_keys, 1, num_q_heads, kv_head_of_q_head, sinks, 0, nullptr, scale, out,
                          out_dtype, workspace, workspace_bytes, stream, launch_gather);
+}
+
+extern "C" int pkv_set_attention_kernel(int32_t which)
+{
+    pkv::clear_error();
+    if (which != PKV_KERNEL_MMA_SYNC && which != PKV_KERNEL_TCGEN05)
+        return pkv::set_error(PKV_ERR_SHAPE, "pkv_set_attention_kernel: unknown kernel %d", which);
+    g_attention_kernel.store(which, std::memory_order_relaxed);
+    return PKV_OK;
 }

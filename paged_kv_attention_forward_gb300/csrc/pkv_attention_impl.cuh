@@ -110,6 +110,9 @@ struct AttnParams {
     int32_t max_keys;
     int32_t *status;
     long long wait_limit;         // SM cycles a pipeline stage wait may take (<= 0: give up at once)
+    const int4 *units;            // (tensor-core path) the unit list: (s, split, KV head, row group)
+    int32_t *unit_ctl;            // [0] work counter, [1] unit count
+    long long unit_cap;           // entries the unit list has room for
     int32_t num_seqs, max_blocks_per_seq, num_blocks, num_q_heads, num_kv_heads, group, block_size;
     int32_t n_max, max_context_len, max_rows, total_rows;
     int32_t row_groups;           // CTAs per (s, g, split), each taking 8 * NN * NMT rows
@@ -1410,20 +1413,27 @@ int launch_d_bs(int rows, const CUtensorMap &mk, const CUtensorMap &mv, AttnPara
 }
 
 struct WsLayout {
-    size_t ml, o, total;
+    size_t ml, o, units, ctl, total;
 };
 
+// Workspace: the split partials (m, l) and O, then (tensor-core path) the unit list and its
+// counters.  A sequence of W rows has ceil(G W / 16) row groups at most, so the units of a
+// split number at most H_kv (G R / 16 + S') with S' = max(S, R) (the index-list gather
+// lists rows, not sequences).
 WsLayout ws_layout(int32_t num_seqs, int32_t total_q_rows, int32_t num_q_heads, int32_t num_kv_heads,
                    int32_t head_dim, int32_t max_context_len)
 {
     const size_t n_max = (size_t)(max_context_len > 0 ? (max_context_len + kSplitTokens - 1) / kSplitTokens : 1);
     const size_t slots = (size_t)total_q_rows * num_q_heads * n_max;
-    (void)num_seqs;
-    (void)num_kv_heads;
+    const size_t G = (size_t)(num_q_heads / (num_kv_heads > 0 ? num_kv_heads : 1));
+    const size_t src = (size_t)(num_seqs > total_q_rows ? num_seqs : total_q_rows);
+    const size_t units = n_max * (size_t)num_kv_heads * ((G * total_q_rows + 15) / 16 + src);
     WsLayout w;
     w.ml = 0;
     w.o = round_up(slots * sizeof(float2), 256);
-    w.total = w.o + round_up(slots * head_dim * sizeof(float), 256);
+    w.units = w.o + round_up(slots * head_dim * sizeof(float), 256);
+    w.ctl = w.units + round_up(units * 16, 256);
+    w.total = w.ctl + 256;
     return w;
 }
 
@@ -1524,6 +1534,9 @@ inline int attention_run(const char *who, const PoolView &pv, const void *q, con
     prm.out = out;
     prm.part_ml = reinterpret_cast<float2 *>(ws + wl.ml);
     prm.part_o = reinterpret_cast<float *>(ws + wl.o);
+    prm.units = reinterpret_cast<const int4 *>(ws + wl.units);
+    prm.unit_ctl = reinterpret_cast<int32_t *>(ws + wl.ctl);
+    prm.unit_cap = (long long)((wl.ctl - wl.units) / 16);
     prm.qrec = static_cast<const uint8_t *>(pv.records);
     prm.kpool = static_cast<const uint16_t *>(pv.k_pool);
     prm.vpool = static_cast<const uint16_t *>(pv.v_pool);

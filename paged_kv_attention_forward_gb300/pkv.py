@@ -31,7 +31,10 @@ EXPORTED = ("pkv_abi_version", "paged_kv_append", "paged_attention_workspace_siz
             "paged_attention_forward_noalloc", "paged_tree_attention_forward", "spec_accept_tree_greedy",
             "spec_accept_sampled", "paged_block_hashes", "pkv_qrecord_bytes", "paged_kv_append_quant",
             "paged_attention_forward_quant", "paged_attention_forward_gather", "pkv_debug_set_wait_limit",
-            "paged_block_index_init", "paged_block_allocate_workspace_size", "paged_block_allocate")
+            "paged_block_index_init", "paged_block_allocate_workspace_size", "paged_block_allocate",
+            "pkv_set_attention_kernel")
+PKV_KERNEL_MMA_SYNC = 0
+PKV_KERNEL_TCGEN05 = 1
 
 
 class PkvError(RuntimeError):
@@ -123,6 +126,8 @@ def lib(build_if_missing: bool = False):
             L.paged_block_allocate_workspace_size.restype = sz
             L.paged_block_allocate.argtypes = [ctypes.POINTER(_BlockIndexC), P, P, P, i32, i32, i32, P, P, P, sz, P]
             L.paged_block_allocate.restype = ctypes.c_int
+            L.pkv_set_attention_kernel.argtypes = [i32]
+            L.pkv_set_attention_kernel.restype = ctypes.c_int
             L.pkv_debug_set_wait_limit.argtypes = [ctypes.c_longlong]
             L.pkv_debug_set_wait_limit.restype = ctypes.c_int
             L.pkv_device_status.restype = ctypes.c_int
@@ -465,3 +470,8 @@ def paged_block_allocate(index: BlockIndex, block_keys, context_lens, first_bloc
                                       _dptr(first_block), S, int(block_size), mb, _dptr(block_tables), _dptr(fresh),
                                       _dptr(workspace), workspace.numel(), _stream(stream)))
     return fresh
+
+
+def set_attention_kernel(which: int):
+    """Choose the kernel of the bf16 attention calls (PKV_KERNEL_MMA_SYNC or PKV_KERNEL_TCGEN05)."""
+    _check(lib().pkv_set_attention_kernel(int(which)))
