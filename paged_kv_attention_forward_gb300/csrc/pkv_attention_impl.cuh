@@ -43,7 +43,8 @@
 //    codec item): the same kernel with BITS = 8, 4 or 2 reads one record per
 //    (block, KV head) with a single bulk copy (codes of K and V + per-key
 //    scales), widens the codes to f16 in registers, folds each key's K scale
-//    into its score and its V scale into its weight.
+//    into its score and log2 of its V scale into its logit, so the weights meet the
+//    raw codes and P V accumulates straight into O.
 #pragma once
 
 #include <cmath>
@@ -196,6 +197,10 @@ __device__ __forceinline__ void load_group(const uint8_t *g, int lane, uint32_t 
 template <int BITS>
 constexpr int kCodeOff = 1 << (BITS - 1);   // 128, 8, 2: the stored field is c + off
 
+// Floor of log2 of a V scale folded into a logit: keeps p = 2^(x - m) below 2^100 for a
+// key whose V row is zero (scale 0) or tiny, so the denominator stays finite.
+constexpr float kVlogFloor = -100.f;
+
 // bit position, within its byte, of the field that feeds k-step (K) or dim m-tile (V)
 // `step`, column half (K) or row half (V) `half`
 template <int BITS>
@@ -253,15 +258,31 @@ __device__ __forceinline__ void q_frag(const uint32_t (&cw)[NW], int ks, uint32_
 // Residency hints: by default the compiler picks the register count (93-96 for the
 // bf16 kernels at d 128); PKV_MIN_CTAS_WIDE / PKV_MIN_CTAS_DECODE request that many
 // resident CTAs of the wide-row / decode shapes, capping the registers to fit.
+// Quantised records: PKV_MIN_CTAS_Q8 / PKV_MIN_CTAS_QNARROW (decode shapes of 8-bit /
+// 4- and 2-bit records) and PKV_MIN_CTAS_QWIDE (their wide-row shapes), when above 0,
+// launch through a second entry point that asks for that many resident CTAs.  (A
+// minimum of 1 is not the same as none: it changes the compiler's register choice.)
+#ifndef PKV_MIN_CTAS_Q8
+#define PKV_MIN_CTAS_Q8 0
+#endif
+#ifndef PKV_MIN_CTAS_QNARROW
+#define PKV_MIN_CTAS_QNARROW 0
+#endif
+#ifndef PKV_MIN_CTAS_QWIDE
+#define PKV_MIN_CTAS_QWIDE 0
+#endif
+template <int BITS, int NMT>
+constexpr int kMinCtas()
+{
+    return BITS == 16 ? 0 : NMT > 1 ? PKV_MIN_CTAS_QWIDE : BITS == 8 ? PKV_MIN_CTAS_Q8 : PKV_MIN_CTAS_QNARROW;
+}
 #if defined(PKV_MIN_CTAS_WIDE) && defined(PKV_MIN_CTAS_DECODE)
 #define PKV_KERNEL_BOUNDS(NMT, KW) __launch_bounds__(((NMT) * (KW) + 1) * 32, (NMT) > 1 ? PKV_MIN_CTAS_WIDE : PKV_MIN_CTAS_DECODE)
 #else
 #define PKV_KERNEL_BOUNDS(NMT, KW) __launch_bounds__(((NMT) * (KW) + 1) * 32)
 #endif
-template <int D, int BS, int NN, int NMT, int NST, bool TREE, int BITS, int KW, bool GATHER = false>
-__global__ void PKV_KERNEL_BOUNDS(NMT, KW)
-paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, const AttnParams p)
+template <int D, int BS, int NN, int NMT, int NST, bool TREE, int BITS, int KW, bool GATHER>
+__device__ __forceinline__ void split_kernel_body(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const AttnParams &p)
 {
     static_assert(!GATHER || (BITS == 16 && !TREE && KW == 1 && BS == 16), "index-list gather: bf16, 16-key tiles");
     static_assert(!(TREE && BITS != 16), "tree masks are built for bf16 pools only");
@@ -669,15 +690,20 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
 
             // S^T for the BS keys of this block; even and odd k-steps in separate chains
             // (four chains: k-steps ks % 4, summed (a + b) + (c + d))
+            // (quantised: the first chain starts at minus the code offset's share of the score)
             float sa[MTE][NN][4], sb[MTE][NN][4], sc[MTE][NN][4], sd[MTE][NN][4];
 #pragma unroll
             for (int mt = 0; mt < MTE; ++mt)
 #pragma unroll
                 for (int nn = 0; nn < NN; ++nn)
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        sa[mt][nn][c] = sb[mt][nn][c] = sc[mt][nn][c] = sd[mt][nn][c] = 0.f;
-            float2 kscale[MTE], vscale[MTE];   // quantised: scales of this lane's keys 2 kr, 2 kr + 1
+                    for (int c = 0; c < 4; ++c) {
+                        sa[mt][nn][c] = BITS != 16 ? -qbias[nn][c & 1] : 0.f;
+                        sb[mt][nn][c] = sc[mt][nn][c] = sd[mt][nn][c] = 0.f;
+                    }
+            // quantised: scales of this lane's keys 2 kr, 2 kr + 1, log2 of their V scales
+            // (floored) and 2^-log2
+            float2 kscale[MTE], vlog[MTE], vunlog[MTE];
             if constexpr (BITS == 16) {
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) {
@@ -701,7 +727,9 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                     const uint8_t *rm = rec + (mt / MT) * RECB;   // the record holding m-tile mt
                     const int mi = mt % MT;
                     kscale[mt] = *reinterpret_cast<const float2 *>(rm + QR::kKs + (mi * 16 + 2 * kr) * 4);
-                    vscale[mt] = *reinterpret_cast<const float2 *>(rm + QR::kVs + (mi * 16 + 2 * kr) * 4);
+                    const float2 vs = *reinterpret_cast<const float2 *>(rm + QR::kVs + (mi * 16 + 2 * kr) * 4);
+                    vlog[mt] = make_float2(fmaxf(__log2f(vs.x), kVlogFloor), fmaxf(__log2f(vs.y), kVlogFloor));
+                    vunlog[mt] = make_float2(fast_exp2(-vlog[mt].x), fast_exp2(-vlog[mt].y));
                     uint32_t cw[QR::kWords];
                     load_group<D, BITS>(rm + QR::kK + mi * QR::kGroupBytes, lane, cw);
 #pragma unroll
@@ -736,9 +764,9 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                         float x;
                         if constexpr (BITS == 16)
                             x = qk * p.scale_log2;
-                        else
-                            x = (qk - qbias[nn][c & 1]) *
-                                (((c >> 1) ? kscale[mt].y : kscale[mt].x) * qscale[nn][c & 1]);
+                        else   // the logit plus log2 of the key's V scale (see below)
+                            x = fmaf(qk, ((c >> 1) ? kscale[mt].y : kscale[mt].x) * qscale[nn][c & 1],
+                                     (c >> 1) ? vlog[mt].y : vlog[mt].x);
                         const int e = c & 1;
                         bool vis = t < lim[nn][e];
                         if (TREE)
@@ -762,33 +790,14 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                 }
             const bool tail = tbase + BS * TB > L;
             // P = 2^(S - m) rounded to bf16 (packed per 8x8 fragment); l sums the rounded weights.
-            // Quantised: P carries each key's V scale relative to the largest V scale among
-            // the block's keys the row sees, p * (s_v / s_max), in f16; the block's P V is
-            // scaled by s_max as it is added, and l sums p itself.  s_max depends only on
-            // the keys the row sees, so a verify row and the same row decoded alone agree;
-            // keys at or past L get weight exactly 0 whatever their stored scale holds.
-            float vmax[NN][2], vinv[NN][2];
-            if constexpr (BITS != 16) {
-#pragma unroll
-                for (int nn = 0; nn < NN; ++nn)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        float v = 0.f;
-#pragma unroll
-                        for (int mt = 0; mt < MTE; ++mt) {
-                            const int t = tbase + mt * 16 + 2 * kr;
-                            if (t < lim[nn][e])
-                                v = fmaxf(v, vscale[mt].x);
-                            if (t + 1 < lim[nn][e])
-                                v = fmaxf(v, vscale[mt].y);
-                        }
-                        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
-                        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
-                        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
-                        vmax[nn][e] = v;
-                        vinv[nn][e] = v > 0.f ? __frcp_rn(v) : 0.f;
-                    }
-            }
+            // Quantised: each logit x carries log2 of its key's V scale s_v (floored at
+            // kVlogFloor), so the running max m is taken over x + log2 s_v and
+            // P = 2^(x + log2 s_v - m) <= 1 is the key's weight times its V scale.  P in f16
+            // meets the raw codes in the MMA, which accumulates straight into O; l sums the
+            // softmax weights 2^(x - m) = P * 2^-log2 s_v on the same reference.  Every step
+            // depends only on the keys the row sees, so a verify row and the same row
+            // decoded alone agree; keys at or past L get P exactly 0 whatever their stored
+            // scale holds.
             uint32_t pk[MTE][NN][2];
             float sum[NN][2], psum[NN][2];
 #pragma unroll
@@ -804,21 +813,14 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                         sum[nn][0] += bf16_lo_to_f32(pk[mt][nn][0]) + bf16_lo_to_f32(pk[mt][nn][1]);
                         sum[nn][1] += bf16_hi_to_f32(pk[mt][nn][0]) + bf16_hi_to_f32(pk[mt][nn][1]);
                     } else {
-                        const float p0 = fast_exp2(sa[mt][nn][0] - base[nn][0]), p1 = fast_exp2(sa[mt][nn][1] - base[nn][1]);
-                        const float p2 = fast_exp2(sa[mt][nn][2] - base[nn][0]), p3 = fast_exp2(sa[mt][nn][3] - base[nn][1]);
-                        float w0 = p0 * (vscale[mt].x * vinv[nn][0]), w1 = p1 * (vscale[mt].x * vinv[nn][1]);
-                        float w2 = p2 * (vscale[mt].y * vinv[nn][0]), w3 = p3 * (vscale[mt].y * vinv[nn][1]);
-                        if (tail) {
-                            const int t = tbase + mt * 16 + 2 * kr;
-                            if (t >= L)
-                                w0 = w1 = 0.f;
-                            if (t + 1 >= L)
-                                w2 = w3 = 0.f;
-                        }
+                        // P = 2^(x + log2 s_v - m) (keys past a row's limit: exactly 0); the
+                        // softmax weight 2^(x - m) = P * 2^-log2 s_v goes to l
+                        const float w0 = fast_exp2(sa[mt][nn][0] - base[nn][0]), w1 = fast_exp2(sa[mt][nn][1] - base[nn][1]);
+                        const float w2 = fast_exp2(sa[mt][nn][2] - base[nn][0]), w3 = fast_exp2(sa[mt][nn][3] - base[nn][1]);
                         pk[mt][nn][0] = pack_f16x2(w0, w1);
                         pk[mt][nn][1] = pack_f16x2(w2, w3);
-                        sum[nn][0] += p0 + p2;
-                        sum[nn][1] += p1 + p3;
+                        sum[nn][0] = fmaf(w0, vunlog[mt].x, fmaf(w2, vunlog[mt].y, sum[nn][0]));
+                        sum[nn][1] = fmaf(w1, vunlog[mt].x, fmaf(w3, vunlog[mt].y, sum[nn][1]));
                         // the rounded weights, for the code offset's share of the output
                         psum[nn][0] += f16_lo_to_f32(pk[mt][nn][0]) + f16_lo_to_f32(pk[mt][nn][1]);
                         psum[nn][1] += f16_hi_to_f32(pk[mt][nn][0]) + f16_hi_to_f32(pk[mt][nn][1]);
@@ -830,8 +832,8 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                 lrow[nn][0] = lrow[nn][0] * alpha[nn][0] + sum[nn][0];
                 lrow[nn][1] = lrow[nn][1] * alpha[nn][1] + sum[nn][1];
                 if constexpr (BITS != 16) {
-                    cacc[nn][0] = cacc[nn][0] * alpha[nn][0] + vmax[nn][0] * psum[nn][0];
-                    cacc[nn][1] = cacc[nn][1] * alpha[nn][1] + vmax[nn][1] * psum[nn][1];
+                    cacc[nn][0] = cacc[nn][0] * alpha[nn][0] + psum[nn][0];
+                    cacc[nn][1] = cacc[nn][1] * alpha[nn][1] + psum[nn][1];
                 }
                 moved = moved || alpha[nn][0] != 1.f || alpha[nn][1] != 1.f;
             }
@@ -866,14 +868,8 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                         uint32_t a[4];
                         q_frag<BITS, true>(cw, dm, a);
 #pragma unroll
-                        for (int nn = 0; nn < NN; ++nn) {
-                            float part[4] = {0.f, 0.f, 0.f, 0.f};
-                            mma_f16_16x8x16(part, a, b[nn][0], b[nn][1]);
-#pragma unroll
-                            for (int c = 0; c < 4; ++c)   // row half c >> 1: codes scaled by 2^fpos
-                                o[dm][nn][c] = fmaf(vmax[nn][c & 1] * __int_as_float((127 - fpos<BITS>(dm, c >> 1)) << 23),
-                                                    part[c], o[dm][nn][c]);
-                        }
+                        for (int nn = 0; nn < NN; ++nn)   // row half c >> 1 carries 2^fpos, taken out at the end
+                            mma_f16_16x8x16(o[dm][nn], a, b[nn][0], b[nn][1]);
                     }
                 } else {
                     uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
@@ -988,7 +984,8 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                 lrow[nn][e] = v;
             }
         if constexpr (BITS != 16) {
-            // remove the code offset: o -= (1024 * 2^-fpos + off) * sum over keys of the weights used
+            // take out the fields' 2^fpos (exact) and remove the code offset:
+            // o = o * 2^-fpos - (1024 * 2^-fpos + off) * sum over keys of the weights used
 #pragma unroll
             for (int nn = 0; nn < NN; ++nn)
 #pragma unroll
@@ -999,9 +996,11 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                     v += __shfl_xor_sync(0xffffffffu, v, 16);
                     constexpr int QB = BITS == 16 ? 8 : BITS;
 #pragma unroll
-                    for (int dm = 0; dm < DM; ++dm) {   // (1024 * 2^-fpos + off) * sum of the weights
-                        o[dm][nn][e] -= (1024.f * __int_as_float((127 - fpos<QB>(dm, 0)) << 23) + kCodeOff<QB>) * v;
-                        o[dm][nn][2 + e] -= (1024.f * __int_as_float((127 - fpos<QB>(dm, 1)) << 23) + kCodeOff<QB>) * v;
+                    for (int dm = 0; dm < DM; ++dm) {
+                        const float u0 = __int_as_float((127 - fpos<QB>(dm, 0)) << 23);
+                        const float u1 = __int_as_float((127 - fpos<QB>(dm, 1)) << 23);
+                        o[dm][nn][e] = o[dm][nn][e] * u0 - (1024.f * u0 + kCodeOff<QB>) * v;
+                        o[dm][nn][2 + e] = o[dm][nn][2 + e] * u1 - (1024.f * u1 + kCodeOff<QB>) * v;
                     }
                 }
         }
@@ -1037,6 +1036,22 @@ paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                 break;
         }
     }
+}
+
+template <int D, int BS, int NN, int NMT, int NST, bool TREE, int BITS, int KW, bool GATHER = false>
+__global__ void PKV_KERNEL_BOUNDS(NMT, KW)
+paged_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ AttnParams p)
+{
+    split_kernel_body<D, BS, NN, NMT, NST, TREE, BITS, KW, GATHER>(tm_k, tm_v, p);
+}
+
+template <int D, int BS, int NN, int NMT, int NST, bool TREE, int BITS, int KW, bool GATHER = false>
+__global__ void __launch_bounds__((NMT * KW + 1) * 32, kMinCtas<BITS, NMT>() > 0 ? kMinCtas<BITS, NMT>() : 1)
+paged_attention_kernel_bounded(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                             const __grid_constant__ AttnParams p)
+{
+    split_kernel_body<D, BS, NN, NMT, NST, TREE, BITS, KW, GATHER>(tm_k, tm_v, p);
 }
 
 // Merge of the split partials of one (query row, q head) with the head's sink:
@@ -1256,7 +1271,10 @@ paged_attention_combine_kernel(const AttnParams p)
 #define PKV_STAGES_WIDE 4
 #endif
 #ifndef PKV_STAGES_QUANT
-#define PKV_STAGES_QUANT 4
+#define PKV_STAGES_QUANT 6
+#endif
+#ifndef PKV_STAGES_QUANT_WIDE
+#define PKV_STAGES_QUANT_WIDE 6
 #endif
 #ifndef PKV_KW_BF16
 #define PKV_KW_BF16 1
@@ -1285,10 +1303,13 @@ constexpr int kKeyWarps();
 // DEEP: a grid of at most two CTAs per SM (a few long sequences, e.g. one layer of a
 // 4-sequence decode) is bound by the bytes each CTA keeps in flight, not by occupancy:
 // such calls get a deeper ring.  Ring depth does not change any row's arithmetic.
-// Quantised rings hold at least PKV_QUANT_RING_BYTES: a record of fewer bits gets more
-// stages, so each CTA keeps as many bytes in flight as a Q8 one.
+// Quantised rings take six stages (from four: a Q8 verify call 366 -> 324 us, a Q8
+// cb_mix call 244 -> 233 us; eight cost cb_mix a CTA per SM) and hold at least
+// PKV_QUANT_RING_BYTES: a record of fewer bits gets more stages, so each CTA keeps as
+// many bytes in flight as a Q8 one (48 KB: Q4 cb_mix 239 -> 236 us, Q2 234 -> 230 us).
+// A deep ring is never shallower than that.
 #ifndef PKV_QUANT_RING_BYTES
-#define PKV_QUANT_RING_BYTES 0
+#define PKV_QUANT_RING_BYTES 49152
 #endif
 template <int D, int BS, int NN, int NMT, int BITS, bool DEEP = false>
 constexpr int kStages()
@@ -1296,8 +1317,10 @@ constexpr int kStages()
     constexpr int tb = kBlocksPerStage<BITS, BS>;
     constexpr int stage = BITS == 16 ? 2 * tb * Tile<D, BS>::kTileBytes : tb * QRec<D, BS, (BITS == 16 ? 8 : BITS)>::kBytes;
     constexpr int by_bytes = BITS != 16 ? (PKV_QUANT_RING_BYTES + stage - 1) / stage : 0;
-    constexpr int quant = PKV_STAGES_QUANT > by_bytes ? PKV_STAGES_QUANT : by_bytes;
-    constexpr int base = DEEP ? PKV_STAGES_DEEP : BITS != 16 ? quant : NMT == 1 ? PKV_STAGES_DECODE : PKV_STAGES_WIDE;
+    constexpr int quant_base = NMT > 1 ? PKV_STAGES_QUANT_WIDE : PKV_STAGES_QUANT;
+    constexpr int quant = quant_base > by_bytes ? quant_base : by_bytes;
+    constexpr int deep = BITS != 16 && quant > PKV_STAGES_DEEP ? quant : PKV_STAGES_DEEP;
+    constexpr int base = DEEP ? deep : BITS != 16 ? quant : NMT == 1 ? PKV_STAGES_DECODE : PKV_STAGES_WIDE;
     // the KW - 1 key shares' states pass through the ring at the end: make it big enough
     constexpr int merge = (kKeyWarps<BITS>() - 1) * NMT * (D / 16 * 4 + 6) * NN * 32 * 4;
     constexpr int need = (merge + stage - 1) / stage;
@@ -1314,7 +1337,7 @@ constexpr int kKeyWarps()
 }
 
 template <int D, int BS, int NN, int NMT, int BITS, bool DEEP = false, bool GATHER = false>
-size_t smem_bytes()
+constexpr size_t smem_bytes()
 {
     constexpr int NST = kStages<D, BS, NN, NMT, BITS, DEEP>();
     constexpr size_t tb = kBlocksPerStage<BITS, BS>;
@@ -1330,8 +1353,13 @@ int launch_t(const CUtensorMap &mk, const CUtensorMap &mv, const AttnParams &prm
 {
     constexpr int NST = kStages<D, BS, NN, NMT, BITS, DEEP>();
     constexpr int KW = GATHER ? 1 : kKeyWarps<BITS>();
-    auto kern = paged_attention_kernel<D, BS, NN, NMT, NST, TREE, BITS, KW, GATHER>;
-    const size_t smem = smem_bytes<D, BS, NN, NMT, BITS, DEEP, GATHER>();
+    void (*kern)(const CUtensorMap, const CUtensorMap, const AttnParams);
+    if constexpr (kMinCtas<BITS, NMT>() > 0)
+        kern = paged_attention_kernel_bounded<D, BS, NN, NMT, NST, TREE, BITS, KW, GATHER>;
+    else
+        kern = paged_attention_kernel<D, BS, NN, NMT, NST, TREE, BITS, KW, GATHER>;
+    constexpr size_t smem = smem_bytes<D, BS, NN, NMT, BITS, DEEP, GATHER>();
+    static_assert(smem <= 232448, "split kernel: shared memory per CTA");
     // A function attribute belongs to a context: set it before every launch, so that a
     // second device, or a context created after a reset, gets it too (the call is cheap).
     const cudaError_t attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
