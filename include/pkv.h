@@ -451,10 +451,12 @@ int paged_kv_append_quant(const pkv_qpool *pool, const int32_t *block_tables,
 /*
  * paged_attention_forward over a quantised pool: the same definition with K
  * and V read back as c * s; every other argument, the workspace
- * (paged_attention_workspace_size), the split / merge structure and the
- * batch-invariance rules are those of paged_attention_forward.  Within one
- * codec the arithmetic is fixed by the row's own sequence, so a row computed
- * in a batch equals the row alone, bit for bit.
+ * (paged_attention_workspace_size, of which it uses at most that much), the
+ * split / merge structure and the batch-invariance rules are those of
+ * paged_attention_forward, except that the keys split into fixed 1024-token
+ * chunks.  Within one codec the arithmetic is fixed by the row's own sequence,
+ * so a row computed in a batch equals the row alone, bit for bit, and row w of
+ * a causal window equals the one-row decode over its keys.
  */
 int paged_attention_forward_quant(const pkv_qpool *pool, const void *q, const int32_t *q_starts,
                                   const int32_t *block_tables, int32_t max_blocks_per_seq,

@@ -50,6 +50,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include <cuda_bf16.h>
 
@@ -191,11 +192,19 @@ __device__ __forceinline__ void load_group(const uint8_t *g, int lane, uint32_t 
 // exactly.  A byte code (u = c + 128, p = 0) is 1024 + u; a nibble (c + 8) or bit pair
 // (c + 2) sits at p = fpos(step, half) of its byte (bytes 1 and 3 are first moved down by
 // one prmt), so its operand is 1024 + 2^p (c + off).  The factor 2^p is taken out exactly
-// (K: the matching q dims are scaled by 2^-p; V: the PV product by 2^-p), leaving the
-// offset 1024 * 2^-p + off, which the kernel removes in fp32: sum(q' * (1024 + 2^p off))
-// from each score and (1024 * 2^-p + off) * sum(P) from each output element.
+// (K: the matching q dims are scaled by 2^-p; V: the PV product by 2^-p at the end), and
+// the kernel removes the offset in fp32: sum(q' * (1024 + 2^p off)) from each score (the
+// first accumulation chain starts there) and, every ring stage, (1024 + 2^p off) * sum(P)
+// over the stage's weights from each output element.
 template <int BITS>
 constexpr int kCodeOff = 1 << (BITS - 1);   // 128, 8, 2: the stored field is c + off
+
+// Ring stages of quantised records between two removals of the code offset from the
+// output accumulators (the weights' sum of the stages in between is carried, rescaled
+// with the running max like every other part of the state).
+#ifndef PKV_QUANT_OFFSET_STAGES
+#define PKV_QUANT_OFFSET_STAGES 1
+#endif
 
 // Floor of log2 of a V scale folded into a logit: keeps p = 2^(x - m) below 2^100 for a
 // key whose V row is zero (scale 0) or tiny, so the denominator stays finite.
@@ -599,13 +608,22 @@ __device__ __forceinline__ void split_kernel_body(const CUtensorMap &tm_k, const
                 }
             }
         }
+        // keys below every row's limit (and, for a tree, below every window) need no mask: a
+        // stage entirely below it skips the per-key test (warp-uniform)
+        int vis_all = 0x7fffffff;
+#pragma unroll
+        for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+                vis_all = min(vis_all, TREE ? min(lim[nn][e], win0[nn][e]) : lim[nn][e]);
+        vis_all = __reduce_min_sync(0xffffffffu, vis_all);
         // Quantised: q goes to f16, scaled per row by the power of two 2^e that puts its
         // largest |value| in [2^14, 2^15) (exact: a bf16 value has 8 significant bits), and
         // by 2^-fpos more where its codes carry 2^fpos; qbias is the code offset's share of
         // every score (see q_frag), qscale =
         // scale * log2(e) * 2^-e.  Both are needed for the rows cr, cr + 1 of this lane's
         // S^T elements, so they are taken from the lanes that hold those rows' q.
-        float qbias[NN][2], qscale[NN][2], cacc[NN][2];
+        float qbias[NN][2], qscale[NN][2], opend[NN][2];   // opend: weights whose offset is pending
         if constexpr (BITS != 16) {
 #pragma unroll
             for (int nn = 0; nn < NN; ++nn) {
@@ -653,7 +671,7 @@ __device__ __forceinline__ void split_kernel_body(const CUtensorMap &tm_k, const
                 for (int e = 0; e < 2; ++e) {
                     qbias[nn][e] = __shfl_sync(0xffffffffu, bias_r, 4 * (cr + e));
                     qscale[nn][e] = __shfl_sync(0xffffffffu, scale_r, 4 * (cr + e));
-                    cacc[nn][e] = 0.f;
+                    opend[nn][e] = 0.f;
                 }
             }
         }
@@ -750,30 +768,39 @@ __device__ __forceinline__ void split_kernel_body(const CUtensorMap &tm_k, const
 #pragma unroll
             for (int nn = 0; nn < NN; ++nn)
                 mx[nn][0] = mx[nn][1] = -INFINITY;
+            auto scale_scores = [&](auto masked) {
 #pragma unroll
-            for (int mt = 0; mt < MTE; ++mt)
+                for (int mt = 0; mt < MTE; ++mt)
 #pragma unroll
-                for (int nn = 0; nn < NN; ++nn)
+                    for (int nn = 0; nn < NN; ++nn)
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        // bf16 tiles: A row kr + 8 j is key kr + 8 j; quantised: key 2 kr + j
-                        const int t = BITS == 16 ? tbase + mt * 16 + kr + 8 * (c >> 1)
-                                                 : tbase + mt * 16 + 2 * kr + (c >> 1);
-                        const float qk = kQkChains == 4 ? (sa[mt][nn][c] + sb[mt][nn][c]) + (sc[mt][nn][c] + sd[mt][nn][c])
-                                                        : sa[mt][nn][c] + sb[mt][nn][c];
-                        float x;
-                        if constexpr (BITS == 16)
-                            x = qk * p.scale_log2;
-                        else   // the logit plus log2 of the key's V scale (see below)
-                            x = fmaf(qk, ((c >> 1) ? kscale[mt].y : kscale[mt].x) * qscale[nn][c & 1],
-                                     (c >> 1) ? vlog[mt].y : vlog[mt].x);
-                        const int e = c & 1;
-                        bool vis = t < lim[nn][e];
-                        if (TREE)
-                            vis = vis && (t < win0[nn][e] || ((tmk[nn][e] >> (t - win0[nn][e])) & 1u));
-                        sa[mt][nn][c] = vis ? x : -INFINITY;
-                        mx[nn][c & 1] = fmaxf(mx[nn][c & 1], sa[mt][nn][c]);
-                    }
+                        for (int c = 0; c < 4; ++c) {
+                            const float qk = kQkChains == 4 ? (sa[mt][nn][c] + sb[mt][nn][c]) + (sc[mt][nn][c] + sd[mt][nn][c])
+                                                            : sa[mt][nn][c] + sb[mt][nn][c];
+                            float x;
+                            if constexpr (BITS == 16)
+                                x = qk * p.scale_log2;
+                            else   // the logit plus log2 of the key's V scale (see below)
+                                x = fmaf(qk, ((c >> 1) ? kscale[mt].y : kscale[mt].x) * qscale[nn][c & 1],
+                                         (c >> 1) ? vlog[mt].y : vlog[mt].x);
+                            if constexpr (decltype(masked)::value) {
+                                // bf16 tiles: A row kr + 8 j is key kr + 8 j; quantised: key 2 kr + j
+                                const int t = BITS == 16 ? tbase + mt * 16 + kr + 8 * (c >> 1)
+                                                         : tbase + mt * 16 + 2 * kr + (c >> 1);
+                                const int e = c & 1;
+                                bool vis = t < lim[nn][e];
+                                if (TREE)
+                                    vis = vis && (t < win0[nn][e] || ((tmk[nn][e] >> (t - win0[nn][e])) & 1u));
+                                x = vis ? x : -INFINITY;
+                            }
+                            sa[mt][nn][c] = x;
+                            mx[nn][c & 1] = fmaxf(mx[nn][c & 1], x);
+                        }
+            };
+            if (tbase + BS * TB <= vis_all)
+                scale_scores(std::false_type{});
+            else
+                scale_scores(std::true_type{});
             float alpha[NN][2], base[NN][2];
 #pragma unroll
             for (int nn = 0; nn < NN; ++nn)
@@ -821,7 +848,7 @@ __device__ __forceinline__ void split_kernel_body(const CUtensorMap &tm_k, const
                         pk[mt][nn][1] = pack_f16x2(w2, w3);
                         sum[nn][0] = fmaf(w0, vunlog[mt].x, fmaf(w2, vunlog[mt].y, sum[nn][0]));
                         sum[nn][1] = fmaf(w1, vunlog[mt].x, fmaf(w3, vunlog[mt].y, sum[nn][1]));
-                        // the rounded weights, for the code offset's share of the output
+                        // the rounded weights, for the code offset's share of this stage's P V
                         psum[nn][0] += f16_lo_to_f32(pk[mt][nn][0]) + f16_lo_to_f32(pk[mt][nn][1]);
                         psum[nn][1] += f16_hi_to_f32(pk[mt][nn][0]) + f16_hi_to_f32(pk[mt][nn][1]);
                     }
@@ -832,8 +859,8 @@ __device__ __forceinline__ void split_kernel_body(const CUtensorMap &tm_k, const
                 lrow[nn][0] = lrow[nn][0] * alpha[nn][0] + sum[nn][0];
                 lrow[nn][1] = lrow[nn][1] * alpha[nn][1] + sum[nn][1];
                 if constexpr (BITS != 16) {
-                    cacc[nn][0] = cacc[nn][0] * alpha[nn][0] + psum[nn][0];
-                    cacc[nn][1] = cacc[nn][1] * alpha[nn][1] + psum[nn][1];
+                    opend[nn][0] = opend[nn][0] * alpha[nn][0] + psum[nn][0];
+                    opend[nn][1] = opend[nn][1] * alpha[nn][1] + psum[nn][1];
                 }
                 moved = moved || alpha[nn][0] != 1.f || alpha[nn][1] != 1.f;
             }
@@ -850,7 +877,7 @@ __device__ __forceinline__ void split_kernel_body(const CUtensorMap &tm_k, const
                     }
             }
 
-            // O^T += V^T P^T; keys at or past L may hold anything (even NaN): zero them
+            // O^T += V^T P^T
 #pragma unroll
             for (int kk = 0; kk < MTE; ++kk) {
                 uint32_t b[NN][2];
@@ -872,25 +899,58 @@ __device__ __forceinline__ void split_kernel_body(const CUtensorMap &tm_k, const
                             mma_f16_16x8x16(o[dm][nn], a, b[nn][0], b[nn][1]);
                     }
                 } else {
-                    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-                    if (tail) {
-                        const int t = tbase + kk * 16 + cr;
-                        mlo = (t < L ? 0x0000ffffu : 0u) | (t + 1 < L ? 0xffff0000u : 0u);
-                        mhi = (t + 8 < L ? 0x0000ffffu : 0u) | (t + 9 < L ? 0xffff0000u : 0u);
-                    }
+                    // keys at or past L may hold anything (even NaN): a tail stage zeroes them
+                    auto pv_tiles = [&](auto in_tail) {
+                        uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+                        if constexpr (decltype(in_tail)::value) {
+                            const int t = tbase + kk * 16 + cr;
+                            mlo = (t < L ? 0x0000ffffu : 0u) | (t + 1 < L ? 0xffff0000u : 0u);
+                            mhi = (t + 8 < L ? 0x0000ffffu : 0u) | (t + 9 < L ? 0xffff0000u : 0u);
+                        }
 #pragma unroll
-                    for (int dm = 0; dm < DM; ++dm) {
-                        uint32_t a[4];
-                        ldsm_x4_trans(vb + (kk / MT) * T::kTileBytes + tile_off<BS>((kk % MT) * 16 + v_key, dm * 2 + v_chs),
-                                      a[0], a[1], a[2], a[3]);
-                        a[0] &= mlo;
-                        a[1] &= mlo;
-                        a[2] &= mhi;
-                        a[3] &= mhi;
+                        for (int dm = 0; dm < DM; ++dm) {
+                            uint32_t a[4];
+                            ldsm_x4_trans(vb + (kk / MT) * T::kTileBytes + tile_off<BS>((kk % MT) * 16 + v_key, dm * 2 + v_chs),
+                                          a[0], a[1], a[2], a[3]);
+                            if constexpr (decltype(in_tail)::value) {
+                                a[0] &= mlo;
+                                a[1] &= mlo;
+                                a[2] &= mhi;
+                                a[3] &= mhi;
+                            }
 #pragma unroll
-                        for (int nn = 0; nn < NN; ++nn)
-                            mma_bf16_16x8x16(o[dm][nn], a, b[nn][0], b[nn][1]);
-                    }
+                            for (int nn = 0; nn < NN; ++nn)
+                                mma_bf16_16x8x16(o[dm][nn], a, b[nn][0], b[nn][1]);
+                        }
+                    };
+                    if (tail)
+                        pv_tiles(std::true_type{});
+                    else
+                        pv_tiles(std::false_type{});
+                }
+            }
+            // Remove the code offset: each weight P met 1024 + 2^fpos (c + off), so the O^T
+            // elements of dims whose field sits at fpos also gained (1024 + 2^fpos off) * sum(P).
+            // Removed every PKV_QUANT_OFFSET_STAGES stages of this warp (and after its last), the
+            // offset never builds up in the accumulator against the far smaller sum of P c.
+            if constexpr (BITS != 16) {
+                if ((k / KW) % PKV_QUANT_OFFSET_STAGES == PKV_QUANT_OFFSET_STAGES - 1 || k + KW >= nstage) {
+#pragma unroll
+                    for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            float v = opend[nn][e];
+                            opend[nn][e] = 0.f;
+                            v += __shfl_xor_sync(0xffffffffu, v, 4);
+                            v += __shfl_xor_sync(0xffffffffu, v, 8);
+                            v += __shfl_xor_sync(0xffffffffu, v, 16);
+#pragma unroll
+                            for (int dm = 0; dm < DM; ++dm) {
+                                o[dm][nn][e] = fmaf(-(1024.f + (float)((1 << fpos<BITS>(dm, 0)) * kCodeOff<BITS>)), v, o[dm][nn][e]);
+                                o[dm][nn][2 + e] =
+                                    fmaf(-(1024.f + (float)((1 << fpos<BITS>(dm, 1)) * kCodeOff<BITS>)), v, o[dm][nn][2 + e]);
+                            }
+                        }
                 }
             }
             __syncwarp();
@@ -902,7 +962,7 @@ __device__ __forceinline__ void split_kernel_body(const CUtensorMap &tm_k, const
         if constexpr (KW > 1) {
             // merge the KW key shares in kw order, through the (now idle) stage ring
             asm volatile("bar.sync 1, %0;" ::"r"(NMT * KW * 32) : "memory");
-            constexpr int NV = DM * NN * 4 + 6 * NN;
+            constexpr int NV = DM * NN * 4 + 4 * NN;
             static_assert((size_t)(KW - 1) * NMT * NV * 32 * 4 <= (size_t)NST * STAGE, "merge needs the ring");
             float *xs = reinterpret_cast<float *>(smem);
             const bool aborted = s_flag[1] != 0;
@@ -922,14 +982,13 @@ __device__ __forceinline__ void split_kernel_body(const CUtensorMap &tm_k, const
                     for (int e = 0; e < 2; ++e) {
                         dst[(v++) * 32] = mrow[nn][e];
                         dst[(v++) * 32] = lrow[nn][e];
-                        dst[(v++) * 32] = BITS != 16 ? cacc[nn][e] : 0.f;
                     }
             }
             asm volatile("bar.sync 1, %0;" ::"r"(NMT * KW * 32) : "memory");
             write_out = !aborted && kw == 0;
         }
         if (KW > 1 && write_out) {
-            constexpr int NV = DM * NN * 4 + 6 * NN;
+            constexpr int NV = DM * NN * 4 + 4 * NN;
             const float *xs = reinterpret_cast<const float *>(smem);
             float f[KW][NN][2];
 #pragma unroll
@@ -939,22 +998,18 @@ __device__ __forceinline__ void split_kernel_body(const CUtensorMap &tm_k, const
                     float mx = mrow[nn][e];
 #pragma unroll
                     for (int j = 1; j < KW; ++j)
-                        mx = fmaxf(mx, xs[((size_t)((j - 1) * NMT + mw) * NV + DM * NN * 4 + nn * 6 + e * 3) * 32 + lane]);
+                        mx = fmaxf(mx, xs[((size_t)((j - 1) * NMT + mw) * NV + DM * NN * 4 + nn * 4 + e * 2) * 32 + lane]);
                     f[0][nn][e] = mrow[nn][e] == -INFINITY ? 0.f : fast_exp2(mrow[nn][e] - mx);
 #pragma unroll
                     for (int j = 1; j < KW; ++j) {
-                        const float mj = xs[((size_t)((j - 1) * NMT + mw) * NV + DM * NN * 4 + nn * 6 + e * 3) * 32 + lane];
+                        const float mj = xs[((size_t)((j - 1) * NMT + mw) * NV + DM * NN * 4 + nn * 4 + e * 2) * 32 + lane];
                         f[j][nn][e] = mj == -INFINITY ? 0.f : fast_exp2(mj - mx);
                     }
                     lrow[nn][e] *= f[0][nn][e];
-                    if constexpr (BITS != 16)
-                        cacc[nn][e] *= f[0][nn][e];
 #pragma unroll
                     for (int j = 1; j < KW; ++j) {
-                        const float *src = xs + ((size_t)((j - 1) * NMT + mw) * NV + DM * NN * 4 + nn * 6 + e * 3) * 32 + lane;
+                        const float *src = xs + ((size_t)((j - 1) * NMT + mw) * NV + DM * NN * 4 + nn * 4 + e * 2) * 32 + lane;
                         lrow[nn][e] += f[j][nn][e] * src[32];
-                        if constexpr (BITS != 16)
-                            cacc[nn][e] += f[j][nn][e] * src[64];
                     }
                     mrow[nn][e] = mx;
                 }
@@ -984,24 +1039,18 @@ __device__ __forceinline__ void split_kernel_body(const CUtensorMap &tm_k, const
                 lrow[nn][e] = v;
             }
         if constexpr (BITS != 16) {
-            // take out the fields' 2^fpos (exact) and remove the code offset:
-            // o = o * 2^-fpos - (1024 * 2^-fpos + off) * sum over keys of the weights used
+            // take out the fields' 2^fpos (exact)
+            constexpr int QB = BITS == 16 ? 8 : BITS;
 #pragma unroll
             for (int nn = 0; nn < NN; ++nn)
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    float v = cacc[nn][e];
-                    v += __shfl_xor_sync(0xffffffffu, v, 4);
-                    v += __shfl_xor_sync(0xffffffffu, v, 8);
-                    v += __shfl_xor_sync(0xffffffffu, v, 16);
-                    constexpr int QB = BITS == 16 ? 8 : BITS;
-#pragma unroll
-                    for (int dm = 0; dm < DM; ++dm) {
-                        const float u0 = __int_as_float((127 - fpos<QB>(dm, 0)) << 23);
-                        const float u1 = __int_as_float((127 - fpos<QB>(dm, 1)) << 23);
-                        o[dm][nn][e] = o[dm][nn][e] * u0 - (1024.f * u0 + kCodeOff<QB>) * v;
-                        o[dm][nn][2 + e] = o[dm][nn][2 + e] * u1 - (1024.f * u1 + kCodeOff<QB>) * v;
-                    }
+                for (int dm = 0; dm < DM; ++dm) {
+                    const float u0 = __int_as_float((127 - fpos<QB>(dm, 0)) << 23);
+                    const float u1 = __int_as_float((127 - fpos<QB>(dm, 1)) << 23);
+                    o[dm][nn][0] *= u0;
+                    o[dm][nn][1] *= u0;
+                    o[dm][nn][2] *= u1;
+                    o[dm][nn][3] *= u1;
                 }
         }
 #pragma unroll
@@ -1322,7 +1371,7 @@ constexpr int kStages()
     constexpr int deep = BITS != 16 && quant > PKV_STAGES_DEEP ? quant : PKV_STAGES_DEEP;
     constexpr int base = DEEP ? deep : BITS != 16 ? quant : NMT == 1 ? PKV_STAGES_DECODE : PKV_STAGES_WIDE;
     // the KW - 1 key shares' states pass through the ring at the end: make it big enough
-    constexpr int merge = (kKeyWarps<BITS>() - 1) * NMT * (D / 16 * 4 + 6) * NN * 32 * 4;
+    constexpr int merge = (kKeyWarps<BITS>() - 1) * NMT * (D / 16 * 4 + 4) * NN * 32 * 4;
     constexpr int need = (merge + stage - 1) / stage;
     constexpr int kw = kKeyWarps<BITS>();
     constexpr int n = base > need ? base : need;

@@ -9,6 +9,20 @@
 // a correctly rounded float32 operation; the value read back is c * s.  The record
 // layout (pkv.h) keeps each (block, KV head) in one contiguous record, so the
 // attention kernel fetches a block with a single bulk copy.
+// Splits of quantised records are 1024 keys (a build-time constant of this file,
+// PKV_QUANT_SPLIT_TOKENS): a record's split CTA pays its start-up (length, block
+// table and q loads, the first copies) and its key-share merge once per 1024 keys
+// instead of per 512.  Measured on GB300 against 512-key splits: a Q8 cb_mix call
+// 233 -> 225 us, Q4 236 -> 214 us, Q8 verify windows 325 -> 294 us, sinks_scale
+// Q8 253 -> 217 us; the smallest calls (4 sequences of about 800 keys) lose about
+// a microsecond.  Verify rows and decode rows of a codec share it, so every rule of
+// bit identity holds within the codec; the workspace needed is at most what
+// paged_attention_workspace_size returns.
+#ifndef PKV_QUANT_SPLIT_TOKENS
+#define PKV_QUANT_SPLIT_TOKENS 1024
+#endif
+#undef PKV_SPLIT_TOKENS
+#define PKV_SPLIT_TOKENS PKV_QUANT_SPLIT_TOKENS
 #include "pkv_attention_impl.cuh"
 
 namespace pkv {

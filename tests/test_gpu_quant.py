@@ -103,8 +103,9 @@ def test_attention_quant_matches_oracle(pkv, bits, name, seed, filler):
 @pytest.mark.parametrize("d,bs", [(64, 16), (64, 32), (128, 16), (128, 32)])
 @pytest.mark.parametrize("causal", [False, True])
 def test_quant_ragged_lengths_all_variants(pkv, bits, d, bs, causal):
-    lens = np.array([1, 15, 16, 17, 31, 32, 33, 511, 512, 513, 1025, 2049])
-    W = np.array([1, 1, 3, 2, 16, 1, 5, 16, 1, 7, 16, 9]) if causal else np.ones(len(lens), np.int64)
+    # every block and split boundary (quantised splits are 1024 keys) and one past it
+    lens = np.array([1, 15, 16, 17, 31, 32, 33, 511, 512, 513, 1023, 1024, 1025, 2048, 2049, 3073])
+    W = np.array([1, 1, 3, 2, 16, 1, 5, 16, 1, 7, 16, 1, 16, 3, 9, 12]) if causal else np.ones(len(lens), np.int64)
     W = np.minimum(W, lens)
     b = wl.build_batch(31 + d + bs + bits, name="ragged", lens=lens, n_new=W, q_rows=W, num_q_heads=16,
                        num_kv_heads=2, head_dim=d, block_size=bs, causal=causal, with_sinks=causal,
@@ -172,6 +173,32 @@ def test_quant_window_rows_equal_single_row_decodes(pkv, bits):
                 dev(np.array([L - W + w + 1], np.int32)), max_context_len=L, max_q_rows_per_seq=1, causal=False)
             torch.cuda.synchronize()
             assert np.array_equal(host_bits(one)[0], full[r]), f"seq {s} row {w}"
+
+
+@pytest.mark.parametrize("bits", BITS)
+def test_quant_window_rows_straddling_split_boundaries(pkv, bits):
+    # causal windows of 16 rows whose rows end on both sides of a 512-, 1024- and 2048-key
+    # boundary: every row equals the one-row decode over its own keys, bit for bit
+    lens = np.array([520, 1030, 2056, 1031, 3080])
+    W = np.array([16, 16, 16, 9, 16])
+    b = wl.build_batch(90 + bits, name="straddle", lens=lens, n_new=W, q_rows=W, num_q_heads=32, num_kv_heads=8,
+                       head_dim=128, block_size=16, causal=True, filler="nan")
+    rec = wl.random_records(91 + bits, b, bits, filler="nan")[0]
+    g, out = _gpu_qstep(pkv, b, rec, bits)
+    full = host_bits(out)
+    _, ref = _oracle_qstep(b, rec, bits)
+    assert_close_to_oracle(out.float().cpu().numpy(), ref, what=f"q{bits} straddling windows")
+    for s in range(b.num_seqs):
+        w_s, L = int(W[s]), int(b.context_lens[s])
+        for w in range(w_s):
+            r = int(b.q_starts[s]) + w
+            one = pkv.paged_attention_forward_quant(
+                g["rec"], b.block_size, b.head_dim, bits, g["q"][r:r + 1].contiguous(),
+                dev(np.array([0, 1], np.int32)), g["block_tables"][s:s + 1].contiguous(),
+                dev(np.array([L - w_s + w + 1], np.int32)), max_context_len=L, max_q_rows_per_seq=1, causal=False)
+            torch.cuda.synchronize()
+            assert np.array_equal(host_bits(one)[0], full[r]), f"seq {s} row {w}"
+    _status_ok(pkv)
 
 
 @pytest.mark.parametrize("bits", BITS)
