@@ -1461,13 +1461,23 @@ int launch_t(const CUtensorMap &mk, const CUtensorMap &mv, const AttnParams &prm
 #ifndef PKV_WIDE_NMT_QUANT_NARROW
 #define PKV_WIDE_NMT_QUANT_NARROW 1
 #endif
+// 8-row n-tiles per row warp of a wide CTA over Q8 / Q4 and Q2 records: a 4- or 2-bit
+// warp widens each code for two n-tiles (Q4 verify call 365 -> 331 us, Q2 349 -> 328 us;
+// Q8 300 -> 401 us, so it keeps one)
+#ifndef PKV_WIDE_NN_QUANT
+#define PKV_WIDE_NN_QUANT 1
+#endif
+#ifndef PKV_WIDE_NN_QUANT_NARROW
+#define PKV_WIDE_NN_QUANT_NARROW 2
+#endif
 template <int D, int BS, int BITS, bool WITH_TREE>
 int launch_d_bs(int rows, const CUtensorMap &mk, const CUtensorMap &mv, AttnParams prm,
                 long long pairs, int n_max, cudaStream_t st)
 {
     constexpr int WIDE_NMT = BITS == 16 ? PKV_WIDE_NMT : BITS == 8 ? PKV_WIDE_NMT_QUANT : PKV_WIDE_NMT_QUANT_NARROW;
+    constexpr int WIDE_NN = BITS == 16 ? PKV_WIDE_NN : BITS == 8 ? PKV_WIDE_NN_QUANT : PKV_WIDE_NN_QUANT_NARROW;
     const bool prefill = BITS == 16 && !prm.tree_masks && rows > PKV_PREFILL_ROWS;
-    const int per_cta = rows <= 8 ? 8 : prefill ? 8 * 2 * PKV_WIDE_NMT : 8 * PKV_WIDE_NN * WIDE_NMT;
+    const int per_cta = rows <= 8 ? 8 : prefill ? 8 * 2 * PKV_WIDE_NMT : 8 * WIDE_NN * WIDE_NMT;
     prm.row_groups = (rows + per_cta - 1) / per_cta;
     const long long gx = pairs * prm.row_groups;
     if (gx > 0x7fffffffLL || n_max > 65535)
@@ -1486,7 +1496,7 @@ int launch_d_bs(int rows, const CUtensorMap &mk, const CUtensorMap &mv, AttnPara
         if (prefill)
             return launch_t<D, BS, 2, PKV_WIDE_NMT, false, BITS>(mk, mv, prm, grid, st);
     }
-    return launch_t<D, BS, PKV_WIDE_NN, WIDE_NMT, false, BITS>(mk, mv, prm, grid, st);
+    return launch_t<D, BS, WIDE_NN, WIDE_NMT, false, BITS>(mk, mv, prm, grid, st);
 }
 
 struct WsLayout {
