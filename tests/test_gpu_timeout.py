@@ -67,11 +67,13 @@ def test_bf16_waits_that_give_up_report_timeout(pkv, name, num_seqs):
     _expect_timeout_then_clean(pkv, lambda: _attn(pkv, g, b), ref)
 
 
-@pytest.mark.parametrize("bits", [8, 4])
-def test_quantised_waits_that_give_up_report_timeout(pkv, bits):
+@pytest.mark.parametrize("bits,name,num_seqs", [(8, "tiny_decode", None), (4, "tiny_decode", None),
+                                                (8, "spec_verify", 3), (4, "spec_verify", 3)])
+def test_quantised_waits_that_give_up_report_timeout(pkv, bits, name, num_seqs):
     # Q8 records run two key-share consumer warps, Q4 three: their end-of-split merge
-    # barriers are on the timeout path too
-    b = wl.make_workload("tiny_decode", seed=32)
+    # barriers are on the timeout path too; verify windows add the wide-row CTAs (Q8: two
+    # row warps per key share, Q4: two n-tiles per row warp)
+    b = wl.make_workload(name, seed=32, num_seqs=num_seqs)
     rec = wl.random_records(1, b, bits)[0]
     r = rec.copy()
     oracle.paged_kv_append_quant(r, b.block_size, b.head_dim, bits, b.block_tables, b.context_lens_old,
