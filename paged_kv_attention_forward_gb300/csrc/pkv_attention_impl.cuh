@@ -1122,7 +1122,10 @@ paged_attention_combine_kernel(const AttnParams p)
 {
     constexpr int VEC = D / 32;   // output values per lane
     __shared__ float hand[2][VEC + 1][32];   // per pair: the second half's numerators and denominator
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Everything up to the partials reads only the call's inputs (q_starts, lengths, masks,
+    // lists, sinks), which the split kernel does not write and which every earlier kernel on
+    // the stream finished writing before the split grid started: that part runs while the
+    // split grid drains, and griddepcontrol.wait comes just before the first partial load.
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int pr = warp >> 1, half = warp & 1;
     const long long wid = (long long)blockIdx.x * 2 + pr;
@@ -1172,6 +1175,11 @@ paged_attention_combine_kernel(const AttnParams p)
     const size_t base = ((size_t)r * p.num_q_heads + h) * p.n_max;
     const float *src0 = p.part_o + base * D + lane * VEC;
     constexpr int BATCH = PKV_MERGE_BATCH;   // partial rows in flight per lane
+    float sink2 = 0.f;
+    const bool has_sink = p.sinks != nullptr;
+    if (has_sink)
+        sink2 = __ldg(p.sinks + h) * kLog2e;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // the first batch of this half's partial rows goes out with the (m, l) loads
     float x0[BATCH][VEC];
@@ -1206,12 +1214,8 @@ paged_attention_combine_kernel(const AttnParams p)
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
         Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, off));
-    float sink2 = 0.f;
-    const bool has_sink = p.sinks != nullptr;
-    if (has_sink) {
-        sink2 = __ldg(p.sinks + h) * kLog2e;
+    if (has_sink)
         Mx = fmaxf(Mx, sink2);
-    }
     float wc[MAXC], lc[MAXC];
 #pragma unroll
     for (int c = 0; c < MAXC; ++c) {
