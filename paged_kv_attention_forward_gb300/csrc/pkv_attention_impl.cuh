@@ -199,13 +199,6 @@ __device__ __forceinline__ void load_group(const uint8_t *g, int lane, uint32_t 
 template <int BITS>
 constexpr int kCodeOff = 1 << (BITS - 1);   // 128, 8, 2: the stored field is c + off
 
-// Ring stages of quantised records between two removals of the code offset from the
-// output accumulators (the weights' sum of the stages in between is carried, rescaled
-// with the running max like every other part of the state).
-#ifndef PKV_QUANT_OFFSET_STAGES
-#define PKV_QUANT_OFFSET_STAGES 1
-#endif
-
 // Floor of log2 of a V scale folded into a logit: keeps p = 2^(x - m) below 2^100 for a
 // key whose V row is zero (scale 0) or tiny, so the denominator stays finite.
 constexpr float kVlogFloor = -100.f;
@@ -312,6 +305,11 @@ __device__ __forceinline__ void split_kernel_body(const CUtensorMap &tm_k, const
     constexpr int C = kSplitTokens;
     constexpr int RPW = 8 * NN;   // rows per consumer warp
     constexpr int NBW = (C / BS + 31) / 32;   // block ids per producer lane
+    // Row sums of a stage's rounded weights (for the code offset): Q8 takes them from the tensor
+    // core, one more MMA per 16-key tile with an A operand of ones (Q8 verify call 299 -> 292 us,
+    // sinks_scale 217 -> 214 us); 4- and 2-bit records add the lanes' weights (the MMA made a Q4
+    // cb_mix call 218 -> 223 us)
+    constexpr bool kMmaRowSum = BITS == 8;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -623,7 +621,7 @@ __device__ __forceinline__ void split_kernel_body(const CUtensorMap &tm_k, const
         // every score (see q_frag), qscale =
         // scale * log2(e) * 2^-e.  Both are needed for the rows cr, cr + 1 of this lane's
         // S^T elements, so they are taken from the lanes that hold those rows' q.
-        float qbias[NN][2], qscale[NN][2], opend[NN][2];   // opend: weights whose offset is pending
+        float qbias[NN][2], qscale[NN][2];
         if constexpr (BITS != 16) {
 #pragma unroll
             for (int nn = 0; nn < NN; ++nn) {
@@ -671,7 +669,6 @@ __device__ __forceinline__ void split_kernel_body(const CUtensorMap &tm_k, const
                 for (int e = 0; e < 2; ++e) {
                     qbias[nn][e] = __shfl_sync(0xffffffffu, bias_r, 4 * (cr + e));
                     qscale[nn][e] = __shfl_sync(0xffffffffu, scale_r, 4 * (cr + e));
-                    opend[nn][e] = 0.f;
                 }
             }
         }
@@ -848,9 +845,10 @@ __device__ __forceinline__ void split_kernel_body(const CUtensorMap &tm_k, const
                         pk[mt][nn][1] = pack_f16x2(w2, w3);
                         sum[nn][0] = fmaf(w0, vunlog[mt].x, fmaf(w2, vunlog[mt].y, sum[nn][0]));
                         sum[nn][1] = fmaf(w1, vunlog[mt].x, fmaf(w3, vunlog[mt].y, sum[nn][1]));
-                        // the rounded weights, for the code offset's share of this stage's P V
-                        psum[nn][0] += f16_lo_to_f32(pk[mt][nn][0]) + f16_lo_to_f32(pk[mt][nn][1]);
-                        psum[nn][1] += f16_hi_to_f32(pk[mt][nn][0]) + f16_hi_to_f32(pk[mt][nn][1]);
+                        if constexpr (!kMmaRowSum) {   // the rounded weights, for the code offset
+                            psum[nn][0] += f16_lo_to_f32(pk[mt][nn][0]) + f16_lo_to_f32(pk[mt][nn][1]);
+                            psum[nn][1] += f16_hi_to_f32(pk[mt][nn][0]) + f16_hi_to_f32(pk[mt][nn][1]);
+                        }
                     }
                 }
             bool moved = false;   // did any row's running max change?
@@ -858,10 +856,6 @@ __device__ __forceinline__ void split_kernel_body(const CUtensorMap &tm_k, const
             for (int nn = 0; nn < NN; ++nn) {
                 lrow[nn][0] = lrow[nn][0] * alpha[nn][0] + sum[nn][0];
                 lrow[nn][1] = lrow[nn][1] * alpha[nn][1] + sum[nn][1];
-                if constexpr (BITS != 16) {
-                    opend[nn][0] = opend[nn][0] * alpha[nn][0] + psum[nn][0];
-                    opend[nn][1] = opend[nn][1] * alpha[nn][1] + psum[nn][1];
-                }
                 moved = moved || alpha[nn][0] != 1.f || alpha[nn][1] != 1.f;
             }
             // o *= alpha; skipped when every alpha is exactly 1 (then it changes no bit)
@@ -877,7 +871,14 @@ __device__ __forceinline__ void split_kernel_body(const CUtensorMap &tm_k, const
                     }
             }
 
-            // O^T += V^T P^T
+            // O^T += V^T P^T.  (Q8: the stage's rounded weights are also summed per row by the
+            // tensor core, through an A operand whose first row is all ones: pc row 0.)
+            float pc[NN][4];
+            if constexpr (kMmaRowSum) {
+#pragma unroll
+                for (int nn = 0; nn < NN; ++nn)
+                    pc[nn][0] = pc[nn][1] = pc[nn][2] = pc[nn][3] = 0.f;
+            }
 #pragma unroll
             for (int kk = 0; kk < MTE; ++kk) {
                 uint32_t b[NN][2];
@@ -897,6 +898,13 @@ __device__ __forceinline__ void split_kernel_body(const CUtensorMap &tm_k, const
 #pragma unroll
                         for (int nn = 0; nn < NN; ++nn)   // row half c >> 1 carries 2^fpos, taken out at the end
                             mma_f16_16x8x16(o[dm][nn], a, b[nn][0], b[nn][1]);
+                    }
+                    if constexpr (kMmaRowSum) {
+                        const uint32_t ones = lane < 4 ? 0x3C003C00u : 0u;   // f16 1.0 pairs in A row 0
+                        const uint32_t a1[4] = {ones, 0u, ones, 0u};
+#pragma unroll
+                        for (int nn = 0; nn < NN; ++nn)
+                            mma_f16_16x8x16(pc[nn], a1, b[nn][0], b[nn][1]);
                     }
                 } else {
                     // keys at or past L may hold anything (even NaN): a tail stage zeroes them
@@ -929,29 +937,32 @@ __device__ __forceinline__ void split_kernel_body(const CUtensorMap &tm_k, const
                         pv_tiles(std::false_type{});
                 }
             }
-            // Remove the code offset: each weight P met 1024 + 2^fpos (c + off), so the O^T
+            // Remove this stage's code offset: each weight P met 1024 + 2^fpos (c + off), so the O^T
             // elements of dims whose field sits at fpos also gained (1024 + 2^fpos off) * sum(P).
-            // Removed every PKV_QUANT_OFFSET_STAGES stages of this warp (and after its last), the
-            // offset never builds up in the accumulator against the far smaller sum of P c.
+            // Removed every stage, the offset never builds up in the accumulator against the far
+            // smaller sum of P c.  (Q8: the row sums sit in row 0 of pc, lanes 0-3, columns 2 l + e;
+            // otherwise the lanes' sums are added across the 8 lanes of a row.)
             if constexpr (BITS != 16) {
-                if ((k / KW) % PKV_QUANT_OFFSET_STAGES == PKV_QUANT_OFFSET_STAGES - 1 || k + KW >= nstage) {
 #pragma unroll
-                    for (int nn = 0; nn < NN; ++nn)
+                for (int nn = 0; nn < NN; ++nn)
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            float v = opend[nn][e];
-                            opend[nn][e] = 0.f;
+                    for (int e = 0; e < 2; ++e) {
+                        float v;
+                        if constexpr (kMmaRowSum) {
+                            v = __shfl_sync(0xffffffffu, pc[nn][e], lane & 3);
+                        } else {
+                            v = psum[nn][e];
                             v += __shfl_xor_sync(0xffffffffu, v, 4);
                             v += __shfl_xor_sync(0xffffffffu, v, 8);
                             v += __shfl_xor_sync(0xffffffffu, v, 16);
-#pragma unroll
-                            for (int dm = 0; dm < DM; ++dm) {
-                                o[dm][nn][e] = fmaf(-(1024.f + (float)((1 << fpos<BITS>(dm, 0)) * kCodeOff<BITS>)), v, o[dm][nn][e]);
-                                o[dm][nn][2 + e] =
-                                    fmaf(-(1024.f + (float)((1 << fpos<BITS>(dm, 1)) * kCodeOff<BITS>)), v, o[dm][nn][2 + e]);
-                            }
                         }
-                }
+#pragma unroll
+                        for (int dm = 0; dm < DM; ++dm) {
+                            o[dm][nn][e] = fmaf(-(1024.f + (float)((1 << fpos<BITS>(dm, 0)) * kCodeOff<BITS>)), v, o[dm][nn][e]);
+                            o[dm][nn][2 + e] =
+                                fmaf(-(1024.f + (float)((1 << fpos<BITS>(dm, 1)) * kCodeOff<BITS>)), v, o[dm][nn][2 + e]);
+                        }
+                    }
             }
             __syncwarp();
             if (lane == 0)
