@@ -85,8 +85,11 @@ static_assert(PKV_QUANT_RECS_PER_STAGE == 1 || PKV_QUANT_RECS_PER_STAGE == 2, "r
 // 16-key bf16 blocks per ring stage (1 or 2).  This sets the granularity of the online
 // softmax update, so it is one constant for every CTA shape (decode, verify, prefill,
 // gather): a verify row must take the same steps as the same row decoded alone.
+// Two: the bookkeeping is paid once per 32 keys (with 2-stage decode and wide rings:
+// cb_mix call 341.4 -> 338.7 us, spec_verify 275.0 -> 242.4 us, spec_tree 315.4 -> 279.3 us,
+// ministral 23.2 -> 17.5 us per layer, prefill_mix 1780 -> 1486 us with a 3-stage ring).
 #ifndef PKV_BF16_BLOCKS_PER_STAGE
-#define PKV_BF16_BLOCKS_PER_STAGE 1
+#define PKV_BF16_BLOCKS_PER_STAGE 2
 #endif
 static_assert(PKV_BF16_BLOCKS_PER_STAGE == 1 || PKV_BF16_BLOCKS_PER_STAGE == 2, "bf16 blocks per stage");
 // blocks per ring stage: 32-key blocks always go one at a time
@@ -1329,10 +1332,14 @@ paged_attention_combine_kernel(const AttnParams p)
 
 // ---------------------------------------------------------------- host side --
 #ifndef PKV_STAGES_DECODE
-#define PKV_STAGES_DECODE 3
+#define PKV_STAGES_DECODE 2
 #endif
 #ifndef PKV_STAGES_WIDE
-#define PKV_STAGES_WIDE 4
+#define PKV_STAGES_WIDE 2
+#endif
+// bf16 prefill CTAs (16-row warps; 2 stages: 1521 us, 3: 1486 us)
+#ifndef PKV_STAGES_PREFILL
+#define PKV_STAGES_PREFILL 3
 #endif
 #ifndef PKV_STAGES_QUANT
 #define PKV_STAGES_QUANT 6
@@ -1375,7 +1382,12 @@ constexpr int kKeyWarps();
 #ifndef PKV_QUANT_RING_BYTES
 #define PKV_QUANT_RING_BYTES 49152
 #endif
-template <int D, int BS, int NN, int NMT, int BITS, bool DEEP = false>
+// ring depth of the index-list gather (its producer fills stages with 16-byte copies; with
+// two blocks per stage: 2 stages 45.7 us, 3: 43.3 us, 4: 60.7 us per sparse_gather call)
+#ifndef PKV_STAGES_GATHER
+#define PKV_STAGES_GATHER 3
+#endif
+template <int D, int BS, int NN, int NMT, int BITS, bool DEEP = false, bool GATHER = false>
 constexpr int kStages()
 {
     constexpr int tb = kBlocksPerStage<BITS, BS>;
@@ -1384,7 +1396,8 @@ constexpr int kStages()
     constexpr int quant_base = NMT > 1 ? PKV_STAGES_QUANT_WIDE : PKV_STAGES_QUANT;
     constexpr int quant = quant_base > by_bytes ? quant_base : by_bytes;
     constexpr int deep = BITS != 16 && quant > PKV_STAGES_DEEP ? quant : PKV_STAGES_DEEP;
-    constexpr int base = DEEP ? deep : BITS != 16 ? quant : NMT == 1 ? PKV_STAGES_DECODE : PKV_STAGES_WIDE;
+    constexpr int base = DEEP ? deep : BITS != 16 ? quant : GATHER ? PKV_STAGES_GATHER : NMT == 1 ? PKV_STAGES_DECODE
+                                                         : NN > 1 ? PKV_STAGES_PREFILL : PKV_STAGES_WIDE;
     // the KW - 1 key shares' states pass through the ring at the end: make it big enough
     constexpr int merge = (kKeyWarps<BITS>() - 1) * NMT * (D / 16 * 4 + 4) * NN * 32 * 4;
     constexpr int need = (merge + stage - 1) / stage;
@@ -1403,7 +1416,7 @@ constexpr int kKeyWarps()
 template <int D, int BS, int NN, int NMT, int BITS, bool DEEP = false, bool GATHER = false>
 constexpr size_t smem_bytes()
 {
-    constexpr int NST = kStages<D, BS, NN, NMT, BITS, DEEP>();
+    constexpr int NST = kStages<D, BS, NN, NMT, BITS, DEEP, GATHER>();
     constexpr size_t tb = kBlocksPerStage<BITS, BS>;
     constexpr size_t stage = BITS == 16 ? 2 * tb * (size_t)Tile<D, BS>::kTileBytes
                                         : tb * (size_t)QRec<D, BS, (BITS == 16 ? 8 : BITS)>::kBytes;
@@ -1415,7 +1428,7 @@ template <int D, int BS, int NN, int NMT, bool TREE, int BITS, bool GATHER = fal
 int launch_t(const CUtensorMap &mk, const CUtensorMap &mv, const AttnParams &prm, dim3 grid,
              cudaStream_t st)
 {
-    constexpr int NST = kStages<D, BS, NN, NMT, BITS, DEEP>();
+    constexpr int NST = kStages<D, BS, NN, NMT, BITS, DEEP, GATHER>();
     constexpr int KW = GATHER ? 1 : kKeyWarps<BITS>();
     void (*kern)(const CUtensorMap, const CUtensorMap, const AttnParams);
     if constexpr (kMinCtas<BITS, NMT>() > 0)
