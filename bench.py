@@ -290,10 +290,12 @@ def run_ours(args, rank, world, local_rank):
                                drafts=drafts, acc_out=acc_out, tree_masks=tree_masks, parents=parents,
                                positions=positions, keys=None)
 
-    def step(ev_pairs=None, li=None, io=io, st=None):
+    def step(ev_pairs=None, li=None, io=io, st=None, attn_only=False):
         st = stream if st is None else st
         for i in range(layers):
-            if has_append and quant:
+            if attn_only:
+                pass
+            elif has_append and quant:
                 pkv.paged_kv_append_quant(records[i], b.block_size, b.head_dim, bits, io.tables, io.lens_old,
                                           io.new_starts, io.k_new[i], io.v_new[i], stream=st)
             elif has_append:
@@ -326,6 +328,8 @@ def run_ours(args, rank, world, local_rank):
             if ev_pairs is not None:
                 ev_pairs[li][1].record(st)
                 li += 1
+        if attn_only:
+            return li
         if io.logits is not None and accept_mode in ("sampled", "sampled-topkp"):
             filt = dict(top_k=50, top_p=0.9) if accept_mode == "sampled-topkp" else {}
             pkv.spec_accept_sampled(io.logits, io.q_starts, io.drafts, io.positions, seed=args.seed + 1,
@@ -358,23 +362,27 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- device-resident timed region ----
     # By default the step is captured as a CUDA graph and replayed, as a serving loop replays
-    # its decode step (its launches then cost one graph launch); the per-call kernel
-    # durations for the roofline come from an eager pass beforehand, since a graph changes
-    # the gaps between kernels, not the kernels.  The index-list gather, whose lists change
-    # every step, captures one graph per list set and replays them in turn.  --eager: plain
-    # launches throughout.
+    # its decode step (its launches then cost one graph launch).  The per-call durations for
+    # the roofline come from a graph of the step's attention calls alone (no appends, no
+    # accept), several passes over the layers back to back, timed by CUDA events around its
+    # replays: the calls' own GPU time, without the host's launch gaps that an eager call of a
+    # few microseconds also measures (an eager pass, one event pair per call, is reported
+    # beside it).  The index-list gather, whose lists change every step, captures one graph
+    # per list set and replays them in turn.  --eager: plain launches throughout, and the
+    # per-call times come from the timed region's own event pairs.
     graph = not getattr(args, "eager", False)
 
-    def capture(io_):
+    def capture(io_, fn=None):
+        fn = fn or (lambda st_: step(io=io_, st=st_))
         g_ = torch.cuda.CUDAGraph()
         side = torch.cuda.Stream()
         side.wait_stream(stream)
         with torch.cuda.stream(side):
-            step(io=io_, st=side)
+            fn(side)
         stream.wait_stream(side)
         torch.cuda.synchronize()
         with torch.cuda.graph(g_):
-            step(io=io_, st=torch.cuda.current_stream())
+            fn(torch.cuda.current_stream())
         torch.cuda.synchronize()
         return g_
 
@@ -393,6 +401,26 @@ def run_ours(args, rank, world, local_rank):
             g_steps = [capture(io)]
         for k in range(3):
             g_steps[k % len(g_steps)].replay()
+        # the attention calls alone, back to back (about 200 calls per replay)
+        io_attn = types.SimpleNamespace(**{**vars(io), "keys": key_sets[0]}) if gather else io
+        reps = max(1, 200 // layers)
+
+        def attn_passes(st_):
+            for _ in range(reps):
+                step(io=io_attn, st=st_, attn_only=True)
+
+        g_attn = capture(io_attn, attn_passes)
+        g_attn.replay()
+        n_attn_replays = 3
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(n_attn_replays):
+            g_attn.replay()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        attn_graph_calls = n_attn_replays * reps * layers
+        attn_graph_ms = a0.elapsed_time(a1) / attn_graph_calls
+        del g_attn
     clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     barrier()
     if clocks:
@@ -531,9 +559,10 @@ def run_ours(args, rank, world, local_rank):
     # ---- max over ranks ----
     ms_per_step = ms_total / args.steps
     e2e_ms_per_step = e2e_ms / e2e_steps
-    attn_avg_ms = statistics.fmean(attn_ms)
-    ms_per_step, e2e_ms_per_step, attn_avg_ms = max_over_ranks(
-        [ms_per_step, e2e_ms_per_step, attn_avg_ms], dist, dev)
+    attn_eager_ms = statistics.fmean(attn_ms)
+    attn_avg_ms = attn_graph_ms if graph else attn_eager_ms
+    ms_per_step, e2e_ms_per_step, attn_avg_ms, attn_eager_ms = max_over_ranks(
+        [ms_per_step, e2e_ms_per_step, attn_avg_ms, attn_eager_ms], dist, dev)
     if rank != 0:
         return None
 
@@ -577,8 +606,11 @@ def run_ours(args, rank, world, local_rank):
                      + ("" if not quant else f", q{bits} records"), "bound": "hbm", "achieved": round(achieved, 2),
                      "peak": peak, "peak_kind": f"{peak_kind} (hbm_gbs, copy kernel)", "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "bytes_per_launch": per_launch_bytes,
-                     "avg_launch_ms": round(attn_avg_ms, 5), "launches_timed": len(attn_ms),
-                     "launches_timed_mode": "eager pass before the graph replays" if graph else "timed region",
+                     "avg_launch_ms": round(attn_avg_ms, 5),
+                     "launches_timed": attn_graph_calls if graph else len(attn_ms),
+                     "launches_timed_mode": ("a graph of the step's attention calls alone, replayed back to back "
+                                             "before the timed steps" if graph else "timed region"),
+                     "avg_launch_ms_eager": round(attn_eager_ms, 5),
                      "traffic": traffic},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms_per_step, 5),
