@@ -260,7 +260,7 @@ __device__ __forceinline__ void q_frag(const uint32_t (&cw)[NW], int ks, uint32_
 // GATHER: the index-list gather.  The work unit is (query row, KV head); its keys are
 // the row's list entries, 16 per stage, each row fetched through the block table with
 // 16-byte cp.async copies into the same swizzled tile layout the TMA path fills.
-// Residency hints: by default the compiler picks the register count (93-96 for the
+// Residency hints: by default the compiler picks the register count (94-126 for the
 // bf16 kernels at d 128); PKV_MIN_CTAS_WIDE / PKV_MIN_CTAS_DECODE request that many
 // resident CTAs of the wide-row / decode shapes, capping the registers to fit.
 // Quantised records: PKV_MIN_CTAS_Q8 / PKV_MIN_CTAS_QNARROW (decode shapes of 8-bit /
