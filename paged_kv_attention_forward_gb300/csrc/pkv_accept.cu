@@ -2,7 +2,7 @@
 //
 // TensorFold article, section "接受规则：GPU 上的 accept 内核": the accept kernel
 // compares each draft token with the target's choice and follows the chain to
-// the first mismatch, writing its verdict to a small arena; TensorSharp
+// the first mismatch, writing its outcome to a small arena; TensorSharp
 // "高级功能", DFlash paragraph: the argmax runs on the device so the
 // vocabulary-wide block never crosses PCIe.
 //
