@@ -1,9 +1,10 @@
 """Register budgets of the attention kernels, read from ptxas (-Xptxas -v).
 
-The occupancy the design relies on (eight 64-thread decode CTAs and five 128-thread
-verify CTAs per SM for head_dim 128) holds only while these kernels stay within 96
-registers per thread without spills, and the merge kernel (seven 128-thread CTAs per SM)
-within 72; a change that raises them slows every call without failing any numeric test.
+The occupancy the design relies on for head_dim 128 holds only while these kernels stay
+within their budgets without spills: 64-thread decode CTAs within 128 registers per thread
+(eight CTAs per SM by registers; their 34 KB ring of two 32-key stages sets six), 128-thread
+verify CTAs within 96 (five per SM), and the merge kernel (seven 128-thread CTAs per SM)
+within 72.  A change that raises them slows every call without failing any numeric test.
 """
 import os
 import re
@@ -49,8 +50,9 @@ def test_bf16_attention_kernels_fit_their_register_budget(attention_usage):
     pat = re.compile(r"paged_attention_kernelILi128ELi16ELi1ELi([13])ELi\d+ELb0ELi16ELi1ELb0E")
     found = {m.group(1): u for name, u in usage.items() for m in [pat.search(name)] if m}
     assert set(found) == {"1", "3"}, sorted(usage)[:5]
+    budget = {"1": 128, "3": 96}
     for shape, u in found.items():
-        assert u["regs"] <= 96, f"{shape} row warps: {u['regs']} registers"
+        assert u["regs"] <= budget[shape], f"{shape} row warps: {u['regs']} registers"
         assert u.get("spill", 0) == 0, f"{shape} row warps spill {u['spill']} bytes"
 
 
